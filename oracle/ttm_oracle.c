@@ -1,0 +1,313 @@
+/*
+ * Float64 CPU oracle for the chunked test-time-training memory scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * GPU library is compared against.  Only the test suite, the smoke check and
+ * the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA path.
+ *
+ * What it computes is the token-by-token ("primal") recurrence, written out
+ * exactly as the pages define it:
+ *
+ *   inner loss      l(W; k, v) = || f(k; W) - v ||^2
+ *                   ("TTT layers 与 fast weights", eq (2); "论文速览 | Titans" §3.6)
+ *   gradient        linear f(k;W) = W k:  grad = 2 (W k - v) k^T
+ *                   ("TTT layers 与 fast weights", eq (4))
+ *   mini-batch      every gradient of a chunk of b tokens is taken at the
+ *                   state left by the previous chunk
+ *                   ("TTT layers 与 fast weights", eq (6), mini-batch GD;
+ *                    "论文速览 | Titans" §4.2)
+ *   momentum        S_t = eta_t S_{t-1} - theta_t grad
+ *   forgetting      M_t = (1 - alpha_t) M_{t-1} + S_t
+ *                   ("论文速览 | Titans" §3.4 and §3.7;
+ *                    "Continual Learning: From Attention to Neural Memory" §5.2)
+ *   read            z_t = f(q_t; M_t), after token t's own write
+ *                   ("TTT layers 与 fast weights", eq (3); "Continual Learning:
+ *                    From Attention to Neural Memory" §4.2 and §4.7)
+ *
+ * Plain TTT-Linear is the same loop with eta = alpha = 0 (then S_t is just
+ * -theta_t grad and W_t = W_{t-1} - theta_t grad).
+ *
+ * The deep memory is f(k) = W2 GELU(W1 k) with exact GELU
+ * x/2 (1 + erf(x / sqrt 2)); its gradients are the chain rule written out:
+ *   h = W1 k, a = GELU(h), y = W2 a, e = 2 (y - v)
+ *   dl/dW2 = e a^T,   dl/dW1 = ((W2^T e) * GELU'(h)) k^T
+ * ("论文速览 | Titans" §3.9; "Continual Learning: From Attention to Neural
+ *  Memory" §4.2).  The pages name no activation; exact GELU is the reading
+ * taken here.
+ *
+ * Layouts (all float64, row-major, contiguous):
+ *   q, k      [B][H][T][dk]          v, z  [B][H][T][dv]
+ *   eta, theta, alpha  [B][H][T]     (eta or alpha NULL means all zero)
+ *   W0, S0    [B or 1][H][dv][dk]    (1 when shared_over_batch != 0; S0 NULL = 0)
+ *   W_out, S_out [B][H][dv][dk]      (S_out may be NULL)
+ * Deep memory: W1 [.][H][hidden][d], W2 [.][H][d][hidden], same for S1, S2.
+ *
+ * The (b, h) sequences are independent, so they are spread over POSIX
+ * threads; each one runs the plain loop below.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------ */
+/* linear memory                                                      */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int B, H, T, dk, dv, chunk;
+    const double *q, *k, *v, *eta, *theta, *alpha, *W0, *S0;
+    int shared;
+    double *z, *W_out, *S_out;
+} lin_args;
+
+/* one (b, h) sequence of the linear / Titans recurrence */
+static void lin_one(const lin_args* a, int b, int h) {
+    const int T = a->T, dk = a->dk, dv = a->dv;
+    const size_t seq = (size_t)b * a->H + h;
+    const size_t init = (size_t)(a->shared ? 0 : b) * a->H + h;
+    const size_t nstate = (size_t)dv * dk;
+
+    double* W = (double*)malloc(nstate * sizeof(double));
+    double* S = (double*)malloc(nstate * sizeof(double));
+    double* Wc = (double*)malloc(nstate * sizeof(double)); /* chunk-start snapshot */
+    double* e = (double*)malloc((size_t)dv * sizeof(double));
+
+    memcpy(W, a->W0 + init * nstate, nstate * sizeof(double));
+    if (a->S0) memcpy(S, a->S0 + init * nstate, nstate * sizeof(double));
+    else memset(S, 0, nstate * sizeof(double));
+
+    for (int t = 0; t < T; ++t) {
+        const double* kt = a->k + (seq * T + t) * dk;
+        const double* qt = a->q + (seq * T + t) * dk;
+        const double* vt = a->v + (seq * T + t) * dv;
+        const double th = a->theta[seq * T + t];
+        const double et = a->eta ? a->eta[seq * T + t] : 0.0;
+        const double al = a->alpha ? a->alpha[seq * T + t] : 0.0;
+
+        if (t % a->chunk == 0) memcpy(Wc, W, nstate * sizeof(double));
+
+        /* prediction error at the chunk-start state: e = Wc k - v */
+        for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += Wc[(size_t)i * dk + j] * kt[j];
+            e[i] = acc - vt[i];
+        }
+        /* grad_ij = 2 e_i k_j; momentum, then forgetting */
+        for (int i = 0; i < dv; ++i) {
+            for (int j = 0; j < dk; ++j) {
+                const size_t ij = (size_t)i * dk + j;
+                const double g = 2.0 * e[i] * kt[j];
+                S[ij] = et * S[ij] - th * g;
+                W[ij] = (1.0 - al) * W[ij] + S[ij];
+            }
+        }
+        /* read after the write: z = W q */
+        double* zt = a->z + (seq * T + t) * dv;
+        for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += W[(size_t)i * dk + j] * qt[j];
+            zt[i] = acc;
+        }
+    }
+    memcpy(a->W_out + seq * nstate, W, nstate * sizeof(double));
+    if (a->S_out) memcpy(a->S_out + seq * nstate, S, nstate * sizeof(double));
+    free(W); free(S); free(Wc); free(e);
+}
+
+/* ------------------------------------------------------------------ */
+/* deep (2-layer MLP) memory                                          */
+/* ------------------------------------------------------------------ */
+
+static double gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/* d/dx GELU(x) = Phi(x) + x phi(x) */
+static double gelu_grad(double x) {
+    const double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+    const double phi = exp(-0.5 * x * x) / sqrt(2.0 * M_PI);
+    return Phi + x * phi;
+}
+
+/* f(x) = W2 GELU(W1 x); W1 [hid][d], W2 [d][hid]; scratch hbuf/abuf [hid] */
+static void mlp_apply(int d, int hid, const double* W1, const double* W2, const double* x,
+                      double* hbuf, double* abuf, double* y) {
+    for (int u = 0; u < hid; ++u) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += W1[(size_t)u * d + j] * x[j];
+        hbuf[u] = acc;
+        abuf[u] = gelu(acc);
+    }
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int u = 0; u < hid; ++u) acc += W2[(size_t)i * hid + u] * abuf[u];
+        y[i] = acc;
+    }
+}
+
+/* Gradient of ||W2 GELU(W1 k) - v||^2 with respect to W1 and W2. */
+void oracle_mlp_grad(int d, int hid, const double* W1, const double* W2, const double* k,
+                     const double* v, double* gW1, double* gW2) {
+    double* hb = (double*)malloc((size_t)hid * sizeof(double));
+    double* ab = (double*)malloc((size_t)hid * sizeof(double));
+    double* y = (double*)malloc((size_t)d * sizeof(double));
+    double* e = (double*)malloc((size_t)d * sizeof(double));
+    mlp_apply(d, hid, W1, W2, k, hb, ab, y);
+    for (int i = 0; i < d; ++i) e[i] = 2.0 * (y[i] - v[i]);
+    for (int i = 0; i < d; ++i)
+        for (int u = 0; u < hid; ++u) gW2[(size_t)i * hid + u] = e[i] * ab[u];
+    for (int u = 0; u < hid; ++u) {
+        double back = 0.0; /* (W2^T e)_u */
+        for (int i = 0; i < d; ++i) back += W2[(size_t)i * hid + u] * e[i];
+        const double delta = back * gelu_grad(hb[u]);
+        for (int j = 0; j < d; ++j) gW1[(size_t)u * d + j] = delta * k[j];
+    }
+    free(hb); free(ab); free(y); free(e);
+}
+
+/* The loss itself, so that the gradient above can be checked by differences. */
+double oracle_mlp_loss(int d, int hid, const double* W1, const double* W2, const double* k,
+                       const double* v) {
+    double* hb = (double*)malloc((size_t)hid * sizeof(double));
+    double* ab = (double*)malloc((size_t)hid * sizeof(double));
+    double* y = (double*)malloc((size_t)d * sizeof(double));
+    mlp_apply(d, hid, W1, W2, k, hb, ab, y);
+    double l = 0.0;
+    for (int i = 0; i < d; ++i) l += (y[i] - v[i]) * (y[i] - v[i]);
+    free(hb); free(ab); free(y);
+    return l;
+}
+
+double oracle_gelu(double x) { return gelu(x); }
+double oracle_gelu_grad(double x) { return gelu_grad(x); }
+
+typedef struct {
+    int B, H, T, d, hid, chunk;
+    const double *q, *k, *v, *eta, *theta, *alpha, *W1_0, *W2_0, *S1_0, *S2_0;
+    int shared;
+    double *z, *W1_out, *W2_out, *S1_out, *S2_out;
+} mlp_args;
+
+static void mlp_one(const mlp_args* a, int b, int h) {
+    const int T = a->T, d = a->d, hid = a->hid;
+    const size_t seq = (size_t)b * a->H + h;
+    const size_t init = (size_t)(a->shared ? 0 : b) * a->H + h;
+    const size_t n = (size_t)hid * d; /* both W1 and W2 hold hid*d numbers */
+
+    double* W1 = (double*)malloc(n * sizeof(double));
+    double* W2 = (double*)malloc(n * sizeof(double));
+    double* S1 = (double*)malloc(n * sizeof(double));
+    double* S2 = (double*)malloc(n * sizeof(double));
+    double* W1c = (double*)malloc(n * sizeof(double));
+    double* W2c = (double*)malloc(n * sizeof(double));
+    double* g1 = (double*)malloc(n * sizeof(double));
+    double* g2 = (double*)malloc(n * sizeof(double));
+    double* hb = (double*)malloc((size_t)hid * sizeof(double));
+    double* ab = (double*)malloc((size_t)hid * sizeof(double));
+
+    memcpy(W1, a->W1_0 + init * n, n * sizeof(double));
+    memcpy(W2, a->W2_0 + init * n, n * sizeof(double));
+    if (a->S1_0) memcpy(S1, a->S1_0 + init * n, n * sizeof(double));
+    else memset(S1, 0, n * sizeof(double));
+    if (a->S2_0) memcpy(S2, a->S2_0 + init * n, n * sizeof(double));
+    else memset(S2, 0, n * sizeof(double));
+
+    for (int t = 0; t < T; ++t) {
+        const double* kt = a->k + (seq * T + t) * d;
+        const double* qt = a->q + (seq * T + t) * d;
+        const double* vt = a->v + (seq * T + t) * d;
+        const double th = a->theta[seq * T + t];
+        const double et = a->eta ? a->eta[seq * T + t] : 0.0;
+        const double al = a->alpha ? a->alpha[seq * T + t] : 0.0;
+
+        if (t % a->chunk == 0) {
+            memcpy(W1c, W1, n * sizeof(double));
+            memcpy(W2c, W2, n * sizeof(double));
+        }
+        oracle_mlp_grad(d, hid, W1c, W2c, kt, vt, g1, g2);
+        for (size_t x = 0; x < n; ++x) {
+            S1[x] = et * S1[x] - th * g1[x];
+            W1[x] = (1.0 - al) * W1[x] + S1[x];
+            S2[x] = et * S2[x] - th * g2[x];
+            W2[x] = (1.0 - al) * W2[x] + S2[x];
+        }
+        mlp_apply(d, hid, W1, W2, qt, hb, ab, a->z + (seq * T + t) * d);
+    }
+    memcpy(a->W1_out + seq * n, W1, n * sizeof(double));
+    memcpy(a->W2_out + seq * n, W2, n * sizeof(double));
+    if (a->S1_out) memcpy(a->S1_out + seq * n, S1, n * sizeof(double));
+    if (a->S2_out) memcpy(a->S2_out + seq * n, S2, n * sizeof(double));
+    free(W1); free(W2); free(S1); free(S2); free(W1c); free(W2c);
+    free(g1); free(g2); free(hb); free(ab);
+}
+
+/* ------------------------------------------------------------------ */
+/* thread pool over the independent (b, h) sequences                  */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int kind; /* 0 linear, 1 mlp */
+    const void* args;
+    int units, next;
+    pthread_mutex_t lock;
+} pool_t;
+
+static void* worker(void* p) {
+    pool_t* pool = (pool_t*)p;
+    for (;;) {
+        pthread_mutex_lock(&pool->lock);
+        const int u = pool->next++;
+        pthread_mutex_unlock(&pool->lock);
+        if (u >= pool->units) break;
+        if (pool->kind == 0) {
+            const lin_args* a = (const lin_args*)pool->args;
+            lin_one(a, u / a->H, u % a->H);
+        } else {
+            const mlp_args* a = (const mlp_args*)pool->args;
+            mlp_one(a, u / a->H, u % a->H);
+        }
+    }
+    return NULL;
+}
+
+/* Runs the sequences on nthreads threads (0: every online core).
+   Returns the number of threads actually used. */
+static int run_pool(int kind, const void* args, int units, int nthreads) {
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > units) nthreads = units;
+    pool_t pool;
+    pool.kind = kind; pool.args = args; pool.units = units; pool.next = 0;
+    pthread_mutex_init(&pool.lock, NULL);
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, worker, &pool);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&pool.lock);
+    return nthreads;
+}
+
+int oracle_linear_primal(int B, int H, int T, int dk, int dv, int chunk,
+                         const double* q, const double* k, const double* v,
+                         const double* eta, const double* theta, const double* alpha,
+                         const double* W0, const double* S0, int shared_over_batch,
+                         double* z, double* W_out, double* S_out, int nthreads) {
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return -1;
+    lin_args a = {B, H, T, dk, dv, chunk, q, k, v, eta, theta, alpha, W0, S0,
+                  shared_over_batch, z, W_out, S_out};
+    return run_pool(0, &a, B * H, nthreads);
+}
+
+int oracle_mlp_primal(int B, int H, int T, int d, int hidden, int chunk,
+                      const double* q, const double* k, const double* v,
+                      const double* eta, const double* theta, const double* alpha,
+                      const double* W1_0, const double* W2_0, const double* S1_0,
+                      const double* S2_0, int shared_over_batch,
+                      double* z, double* W1_out, double* W2_out, double* S1_out,
+                      double* S2_out, int nthreads) {
+    if (B < 1 || H < 1 || T < 0 || d < 1 || hidden < 1 || chunk < 1) return -1;
+    mlp_args a = {B, H, T, d, hidden, chunk, q, k, v, eta, theta, alpha, W1_0, W2_0,
+                  S1_0, S2_0, shared_over_batch, z, W1_out, W2_out, S1_out, S2_out};
+    return run_pool(1, &a, B * H, nthreads);
+}
