@@ -1,0 +1,455 @@
+"""Throughput of the chunked test-time-training memory scan on GB300.
+
+One step = one ttm_*_fwd call over the whole workload (every step of the scan:
+loads, coefficients, scores, errors, reads, state carry, final state).
+Default workload: Titans long context, B=1 H=16 T=131072 d=128 chunk 64, bf16
+inputs (2.2 GB of inputs, larger than L2, so no flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs the same
+workload on its own GPU with no communication on the data path (the scan's
+sequences are independent), so scaling is weak; only the timing uses a
+barrier and a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import ttm_inputs as wl  # noqa: E402
+
+METRIC = "memory-scan tokens/s (B·H·T per sec) on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work (what the chunked method must move and compute)
+# ----------------------------------------------------------------------------
+
+def algorithmic(w: wl.Workload) -> dict:
+    """Bytes and FLOPs per token-head and per call.
+
+    Bytes: q, k, v read and z written in the input dtype, the gates read (4 B
+    each), the initial state read and the final state written once per (b, h).
+    FLOPs: linear memory W.K, W.Q and the state update (6 d^2), Titans adds S.Q
+    and the S update (10 d^2), plus 4 b d for the chunk's score and correction
+    contractions; the 2-layer memory 22 hidden d + 2 b (2 d + 2 hidden).
+    """
+    es = 2 if w.dtype == "bf16" else 4
+    d, b = w.d, w.chunk
+    gates = 4 * (1 + (w.eta[0] != "zero") + (w.alpha[0] != "zero"))
+    per_tok = 4 * d * es + gates
+    seqs, nb0 = w.B * w.H, (1 if w.w0_shared else w.B) * w.H
+    if w.kind == "mlp":
+        state = 2 * w.hidden * d * 4                     # W1 and W2 of one sequence
+        state_bytes = nb0 * state + seqs * 2 * state     # read W1_0, W2_0; write W1, W2, S1, S2
+        flop_tok = 22 * w.hidden * d + 2 * b * (2 * d + 2 * w.hidden)
+    else:
+        state = d * d * 4
+        state_bytes = nb0 * state + seqs * state * (2 if w.kind == "titans" else 1)
+        flop_tok = (10 if w.kind == "titans" else 6) * d * d + 4 * b * d
+    total_bytes = w.tokens * per_tok + state_bytes
+    return dict(bytes_per_token=per_tok, flop_per_token=flop_tok, bytes=total_bytes,
+                flops=w.tokens * flop_tok)
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"])}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
+    a = algorithmic(w)
+    peaks, src = load_peaks()
+    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = a["bytes"] / kernel_s / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = a["flops"] / kernel_s / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["peak_source"] = src
+    r["kernel"] = kernel_name
+    r["algorithmic_bytes"] = a["bytes"]
+    r["algorithmic_flops"] = a["flops"]
+    r["traffic"] = profiled_traffic(kernel_name, w)
+    return r
+
+
+def kernel_source_digest(kernel_name: str) -> str:
+    src = {"linear_simt": "scan_simt.cu", "mlp_simt": "scan_simt.cu",
+           "linear_tc": "scan_linear_tc.cu", "mlp_tc": "scan_mlp_tc.cu"}.get(kernel_name)
+    if not src:
+        return ""
+    path = os.path.join(ROOT, "test_neural_memory_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return ""
+
+
+def profiled_traffic(kernel_name: str, w: wl.Workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = j.get(f"{kernel_name}/workload{w.id}")
+    if not e or e.get("source_sha256_16") != kernel_source_digest(kernel_name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled while the GPU is under load
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows: list[list[str]] = []
+        self.proc = None
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid if self.uuid.startswith('GPU-') else 'GPU-' + self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def call_fn(w: wl.Workload, d: dict, outs: dict, stream):
+    import test_neural_memory_gb300 as ttm
+    if w.kind == "linear":
+        return lambda: ttm.linear_fwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], w.chunk,
+                                      w0_shared=w.w0_shared, z=outs["z"], W_out=outs["W"],
+                                      stream=stream)
+    if w.kind == "titans":
+        return lambda: ttm.titans_fwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], w.chunk,
+                                      eta=d["eta"], alpha=d["alpha"], w0_shared=w.w0_shared,
+                                      z=outs["z"], W_out=outs["W"], S_out=outs["S"],
+                                      stream=stream)
+    return lambda: ttm.mlp_fwd(d["q"], d["k"], d["v"], d["theta"], d["W1_0"], d["W2_0"],
+                               w.chunk, eta=d["eta"], alpha=d["alpha"], w0_shared=w.w0_shared,
+                               z=outs["z"], W1_out=outs["W1"], W2_out=outs["W2"],
+                               S1_out=outs["S1"], S2_out=outs["S2"], stream=stream)
+
+
+def alloc_outputs(w: wl.Workload, dev, pin=False) -> dict:
+    es = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    mk = lambda shape, dt=torch.float32: torch.empty(shape, dtype=dt, device=dev,
+                                                     pin_memory=pin)
+    o = {"z": mk((w.B, w.H, w.T, w.d), es)}
+    if w.kind == "mlp":
+        o.update(W1=mk((w.B, w.H, w.hidden, w.d)), W2=mk((w.B, w.H, w.d, w.hidden)),
+                 S1=mk((w.B, w.H, w.hidden, w.d)), S2=mk((w.B, w.H, w.d, w.hidden)))
+    else:
+        o["W"] = mk((w.B, w.H, w.d, w.d))
+        o["S"] = mk((w.B, w.H, w.d, w.d)) if w.kind == "titans" else None
+    return o
+
+
+def oracle_sample(w: wl.Workload, inp: dict, T_s: int) -> dict:
+    """Time the float64 oracle, as it stands, on every (b, h) of the workload
+    but only its first T_s tokens."""
+    import oracle
+    f = lambda t: None if t is None else t[:, :, :T_s].double().numpy()
+    t0 = time.perf_counter()
+    if w.kind == "mlp":
+        r = oracle.mlp_primal(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["theta"]),
+                              inp["W1_0"].double().numpy(), inp["W2_0"].double().numpy(),
+                              w.chunk, eta=f(inp["eta"]), alpha=f(inp["alpha"]),
+                              shared_over_batch=w.w0_shared)
+    else:
+        r = oracle.linear_primal(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["theta"]),
+                                 inp["W0"].double().numpy(), w.chunk, eta=f(inp["eta"]),
+                                 alpha=f(inp["alpha"]), shared_over_batch=w.w0_shared)
+    dt = time.perf_counter() - t0
+    tokens = w.B * w.H * min(T_s, w.T)
+    return {"value": tokens / dt, "unit": UNIT, "cores": int(r["threads"]), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"all {w.B * w.H} (b,h) sequences, first {min(T_s, w.T)} of {w.T} tokens "
+                      f"each ({tokens} token-heads), float64, {r['threads']} threads"}
+
+
+def oracle_tokens_for(w: wl.Workload, seconds: float) -> int:
+    """Tokens per sequence that keep the oracle near `seconds` on this host,
+    from a short calibration run."""
+    inp = wl.generate(w.shrink(T=min(w.T, 256)))
+    probe = oracle_sample(w.shrink(T=min(w.T, 256)), inp, 256)
+    per_tok = probe["seconds"] / min(w.T, 256)
+    T_s = int(max(w.chunk, min(w.T, seconds / max(per_tok, 1e-9))))
+    return max(w.chunk, (T_s // w.chunk) * w.chunk) if T_s >= w.chunk else T_s
+
+
+def run_ours(args, rank, world, dev):
+    import test_neural_memory_gb300 as ttm
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w)
+    stream = torch.cuda.current_stream(dev)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    outs = alloc_outputs(w, dev)
+    step = call_fn(w, d, outs, stream)
+
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    kernel_name = ttm.last_kernel()
+    # keep the GPU busy ~1 s before the timed region so the clock record has samples
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ttm.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ttm.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = g0.elapsed_time(g1)
+    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    total_ms = max_over_ranks(total_ms, world, dev)
+    kern_ms = max_over_ranks(kern_ms, world, dev)
+    status = ttm.device_status()
+    if status != ttm.OK:
+        raise RuntimeError(f"device status {ttm.status_str(status)}")
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, w, inp, dev, stream, world)
+
+    value = w.tokens * world * args.steps / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                   "chunk": w.chunk, "kind": w.kind, "hidden": w.hidden or None,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (no flush needed)"
+                   if algorithmic(w)["bytes"] > 129e6 else "L2 not flushed: inputs fit in L2",
+                   "kernel": kernel_name},
+        "roofline": roofline(w, kern_ms / 1e3, kernel_name),
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        T_s = oracle_tokens_for(w, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_sample(w, inp, T_s)
+    return line
+
+
+def run_e2e(args, w, inp, dev, stream, world):
+    """Same metric through the public API with pinned host inputs: every step
+    copies its inputs host->device and reads the outputs back."""
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
+    outs = alloc_outputs(w, dev)
+    hout = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, pin_memory=True))
+            for k, v in outs.items()}
+    step = call_fn(w, dbuf, outs, stream)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in hout.values() if v is not None)
+
+    def one():
+        for k, v in host.items():
+            if v is not None:
+                dbuf[k].copy_(v, non_blocking=True)
+        step()
+        for k, v in outs.items():
+            if v is not None:
+                hout[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = args.e2e_steps
+    a.record(stream)
+    for _ in range(n):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": w.tokens * world * n / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": ms / n}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    w = wl.WORKLOADS[args.workload]
+    per_step = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
+    T_s = oracle_tokens_for(w, per_step)
+    inp = wl.generate(w.shrink(T=T_s))
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, T_s)
+    times = []
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(w, inp, T_s)
+        times.append(last["seconds"])
+    tokens = w.B * w.H * T_s
+    value = tokens * len(times) / sum(times)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                   "chunk": w.chunk, "kind": w.kind, "hidden": w.hidden or None,
+                   "sample_tokens_per_sequence": T_s},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    import test_neural_memory_gb300 as ttm
+    ttm.build()
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

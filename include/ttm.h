@@ -1,0 +1,161 @@
+/*
+ * ttm.h — C ABI of libttm.so, the GB300 (sm_103a) chunked test-time-training
+ * memory scan.
+ *
+ * What one call computes (per batch row b and head h, independently):
+ *
+ *   a fast-weight memory M takes one gradient step per token on the inner
+ *   loss  l(M; k_t, v_t) = || f(k_t; M) - v_t ||^2
+ *     ("TTT layers 与 fast weights", eqs (1)-(2); "论文速览 | Titans" §3.6);
+ *   mini-batch rule: every gradient inside a chunk of `chunk` tokens is taken
+ *   at the state left by the previous chunk; chunk c covers tokens
+ *   [c*chunk, min((c+1)*chunk, T)) and the last chunk may be shorter
+ *     ("TTT layers 与 fast weights", eq (6); "论文速览 | Titans" §4.2);
+ *   Titans momentum and forgetting:
+ *     S_t = eta_t S_{t-1} - theta_t grad_t,   M_t = (1 - alpha_t) M_{t-1} + S_t
+ *     ("论文速览 | Titans" §3.4, §3.7);
+ *   read after the token's own write: z_t = f(q_t; M_t)
+ *     ("TTT layers 与 fast weights", eq (3)).
+ *
+ * Conventions shared by every entry point
+ *   - Column vectors: linear memory f(k; W) = W k with W stored [dv][dk]
+ *     row-major; the deep memory is f(k) = W2 GELU(W1 k), GELU exact (erf).
+ *   - q, k: [B][H][T][dk], v and z: [B][H][T][dv] (deep memory: dk = dv = d),
+ *     contiguous, element type `dtype` (TTM_F32 or TTM_BF16); z is written in
+ *     `dtype`, rounded to nearest even.  All arithmetic accumulates in fp32.
+ *   - Gates eta (momentum), theta (step), alpha (forgetting): fp32 [B][H][T],
+ *     contiguous, used as given (no clamping).
+ *   - Initial state: fp32 [B][H][...], or [1][H][...] shared by every batch
+ *     row when w0_shared_over_batch != 0 (the same flag applies to S0).
+ *     NULL S0 (and S1_0/S2_0) means a zero momentum state.
+ *   - Final state: fp32 [B][H][...]; S_out (S1_out/S2_out) may be NULL to skip.
+ *     Continuing a sequence by passing a call's final state as the next call's
+ *     initial state is exact when the first call's T is a multiple of chunk.
+ *   - Pointers are device pointers owned by the caller.  The library
+ *     allocates no memory and keeps no state between calls, except the
+ *     process-wide kernel policy and the device status word below.
+ *     Every pointer must be 16-byte aligned.  Outputs must not overlap inputs,
+ *     except that W_out may be W0 (and S_out S0; W1_out/W2_out likewise) when
+ *     w0_shared_over_batch == 0.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  The call is
+ *     asynchronous: it validates on the host, enqueues kernels and returns.
+ *
+ * Errors
+ *   Argument validation happens on the host before anything is enqueued; a
+ *   failure returns TTM_ERR_INVALID_ARG (malformed) or TTM_ERR_UNSUPPORTED (a
+ *   well-formed shape no kernel of the current policy handles) and launches
+ *   nothing.  A CUDA launch failure returns TTM_ERR_CUDA.  A device-side wait
+ *   that gave up (tensor-core kernels bound every wait) is reported later
+ *   through ttm_device_status().
+ */
+#ifndef TTM_H
+#define TTM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TTM_OK = 0,
+    TTM_ERR_INVALID_ARG = 1,
+    TTM_ERR_UNSUPPORTED = 2,
+    TTM_ERR_CUDA = 3,
+    TTM_ERR_TIMEOUT = 4
+} ttm_status;
+
+typedef enum { TTM_F32 = 0, TTM_BF16 = 1 } ttm_dtype;
+
+/* Kernel selection policy (process-wide; default TTM_KERNEL_AUTO).
+ *   AUTO: tensor-core kernel where the shape and dtype allow it, else the
+ *         fp32 CUDA-core kernel.
+ *   SIMT: always the fp32 CUDA-core kernel.
+ *   TC:   the tensor-core kernel or TTM_ERR_UNSUPPORTED, never a substitute. */
+typedef enum { TTM_KERNEL_AUTO = 0, TTM_KERNEL_SIMT = 1, TTM_KERNEL_TC = 2 } ttm_kernel_policy;
+
+/* Kernel ids reported by ttm_last_kernel(). */
+typedef enum {
+    TTM_KID_NONE = 0,
+    TTM_KID_LINEAR_SIMT = 1,   /* fp32 CUDA-core chunked scan, linear memory */
+    TTM_KID_MLP_SIMT = 2,      /* fp32 CUDA-core chunked scan, 2-layer memory */
+    TTM_KID_LINEAR_TC = 3,     /* tcgen05 + TMA chunked scan, linear memory */
+    TTM_KID_MLP_TC = 4         /* tcgen05 chunked scan, 2-layer memory */
+} ttm_kernel_id;
+
+/*
+ * TTT-Linear: linear memory, plain mini-batch gradient descent
+ * ("TTT layers 与 fast weights", eqs (4)-(9): W_t = W_{t'} - theta sum of
+ * 2 (W_{t'} k_s - v_s) k_s^T over the chunk so far).
+ *   eta and alpha must be NULL (this form has no momentum or forgetting).
+ *   theta: required.  W0: [B|1][H][dv][dk].  W_out: [B][H][dv][dk].
+ *   z: [B][H][T][dv] in dtype.
+ * Shapes: B, H >= 1; T >= 0; dk, dv >= 1 (multiples of 8 for TTM_BF16,
+ * of 4 for TTM_F32); chunk >= 1.
+ */
+int ttm_linear_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                   const void* q, const void* k, const void* v,
+                   const float* eta, const float* theta, const float* alpha,
+                   const float* W0, int w0_shared_over_batch,
+                   void* z, float* W_out, void* stream);
+
+/*
+ * Titans neural memory with linear memory: momentum ("past surprise") and
+ * forgetting ("论文速览 | Titans" §3.4-§3.7, chunked as in §4.2-§4.5).
+ *   eta, alpha: may be NULL (treated as all zero).  theta: required.
+ *   S0: momentum state [B|1][H][dv][dk] or NULL (zero).
+ *   S_out: [B][H][dv][dk] or NULL (not written).
+ * Other arguments and shape rules as ttm_linear_fwd.
+ */
+int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                   const void* q, const void* k, const void* v,
+                   const float* eta, const float* theta, const float* alpha,
+                   const float* W0, const float* S0, int w0_shared_over_batch,
+                   void* z, float* W_out, float* S_out, void* stream);
+
+/*
+ * Deep memory: f(x) = W2 GELU(W1 x), hidden units `hidden`, analytic inner
+ * gradients e = 2 (y - v), dW2 = e a^T, dW1 = ((W2^T e) * GELU'(h)) k^T
+ * ("论文速览 | Titans" §3.9 with L_M = 2; "Continual Learning: From Attention
+ * to Neural Memory" §4.2), with the same momentum/forgetting and chunk rule.
+ *   q, k, v, z: [B][H][T][d].  W1_0, S1_0: [B|1][H][hidden][d].
+ *   W2_0, S2_0: [B|1][H][d][hidden].  Outputs likewise with B rows.
+ *   eta, alpha, S1_0, S2_0: may be NULL.  S1_out and S2_out are both NULL or
+ *   both given, and must be given whenever eta is (they double as the running
+ *   momentum state).
+ * Shapes: d a multiple of 8, hidden a multiple of 8 (kernel limits reported
+ * as TTM_ERR_UNSUPPORTED).
+ */
+int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype,
+                const void* q, const void* k, const void* v,
+                const float* eta, const float* theta, const float* alpha,
+                const float* W1_0, const float* W2_0, const float* S1_0, const float* S2_0,
+                int w0_shared_over_batch,
+                void* z, float* W1_out, float* W2_out, float* S1_out, float* S2_out,
+                void* stream);
+
+/* Static English text for a ttm_status value (never NULL). */
+const char* ttm_status_str(int status);
+
+/* Sets the process-wide kernel policy (ttm_kernel_policy); returns the previous
+ * one, or -1 for an unknown value (policy unchanged).  Not thread-safe with
+ * concurrent ttm_*_fwd calls. */
+int ttm_set_kernel_policy(int policy);
+
+/* ttm_kernel_id of the main kernel enqueued by this thread's last successful
+ * ttm_*_fwd call (TTM_KID_NONE before any). */
+int ttm_last_kernel(void);
+
+/* Number of kernels this process has enqueued through ttm_*_fwd so far
+ * (monotonic; counts successful launches only). */
+unsigned long long ttm_launch_count(void);
+
+/* Synchronises the current device, then returns and clears its status word:
+ * TTM_OK, or TTM_ERR_TIMEOUT if a tensor-core kernel abandoned a bounded wait
+ * since the last query (its outputs are then invalid).  TTM_ERR_CUDA if the
+ * synchronisation itself failed. */
+int ttm_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTM_H */

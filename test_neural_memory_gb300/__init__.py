@@ -1,0 +1,177 @@
+"""Thin Python binding of libttm.so, the GB300 chunked test-time-training memory scan.
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch supplies device memory and
+streams); outputs are allocated here when not given.  There is no CPU
+fallback: if the library is missing the calls raise.
+
+    z, W = linear_fwd(q, k, v, theta, W0, chunk)
+    z, W, S = titans_fwd(q, k, v, theta, W0, chunk, eta=eta, alpha=alpha)
+    z, W1, W2, S1, S2 = mlp_fwd(q, k, v, theta, W1_0, W2_0, chunk, eta=eta, alpha=alpha)
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import re
+
+from ._build import LIB, ROOT, build  # noqa: F401  (build is part of the public surface)
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
+F32, BF16 = 0, 1
+POLICY = {"auto": 0, "simt": 1, "tc": 2}
+KERNEL_NAMES = {0: "none", 1: "linear_simt", 2: "mlp_simt", 3: "linear_tc", 4: "mlp_tc"}
+
+_lib = None
+
+
+class TTMError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_str(code)} (status {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libttm.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing; build it with "
+                               "`python -m test_neural_memory_gb300._build`")
+        L = ctypes.CDLL(LIB)
+        i, p = ctypes.c_int, ctypes.c_void_p
+        L.ttm_linear_fwd.argtypes = [i] * 7 + [p] * 6 + [p, i, p, p, p]
+        L.ttm_titans_fwd.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p]
+        L.ttm_mlp_fwd.argtypes = [i] * 7 + [p] * 6 + [p] * 4 + [i] + [p] * 5 + [p]
+        for f in (L.ttm_linear_fwd, L.ttm_titans_fwd, L.ttm_mlp_fwd):
+            f.restype = i
+        L.ttm_status_str.argtypes = [i]
+        L.ttm_status_str.restype = ctypes.c_char_p
+        L.ttm_set_kernel_policy.argtypes = [i]
+        L.ttm_set_kernel_policy.restype = i
+        L.ttm_last_kernel.restype = i
+        L.ttm_device_status.restype = i
+        L.ttm_launch_count.restype = ctypes.c_ulonglong
+        _lib = L
+    return _lib
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/ttm.h (the ABI this binding wraps)."""
+    with open(os.path.join(ROOT, "include", "ttm.h")) as f:
+        text = f.read()
+    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(ttm_\w+)\s*\(", text, flags=re.M)
+
+
+def status_str(code: int) -> str:
+    return lib().ttm_status_str(int(code)).decode()
+
+
+def set_kernel_policy(policy: str) -> str:
+    old = lib().ttm_set_kernel_policy(POLICY[policy])
+    return {v: k for k, v in POLICY.items()}[old]
+
+
+@contextlib.contextmanager
+def kernel_policy(policy: str):
+    old = set_kernel_policy(policy)
+    try:
+        yield
+    finally:
+        set_kernel_policy(old)
+
+
+def last_kernel() -> str:
+    return KERNEL_NAMES.get(lib().ttm_last_kernel(), "unknown")
+
+
+def launch_count() -> int:
+    """Kernels enqueued by this process through the library so far."""
+    return int(lib().ttm_launch_count())
+
+
+def device_status() -> int:
+    return lib().ttm_device_status()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(t, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise TTMError(code, what)
+
+
+def linear_fwd(q, k, v, theta, W0, chunk, *, w0_shared=False, z=None, W_out=None, stream=None):
+    """TTT-Linear scan.  q, k: [B,H,T,dk]; v: [B,H,T,dv]; theta: [B,H,T] fp32;
+    W0: [B|1,H,dv,dk] fp32.  Returns (z, W_out)."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    W_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if W_out is None else W_out
+    _check(lib().ttm_linear_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
+                                _ptr(v), None, _ptr(theta), None, _ptr(W0), int(bool(w0_shared)),
+                                _ptr(z), _ptr(W_out), _stream(q, stream)), "ttm_linear_fwd")
+    return z, W_out
+
+
+def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_shared=False,
+               z=None, W_out=None, S_out=None, want_S=True, stream=None):
+    """Titans linear-memory scan with momentum (eta) and forgetting (alpha).
+    Returns (z, W_out, S_out); S_out is None when want_S is False."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    shape = (B, H, dv, dk)
+    W_out = torch.empty(shape, dtype=torch.float32, device=q.device) if W_out is None else W_out
+    if S_out is None and want_S:
+        S_out = torch.empty(shape, dtype=torch.float32, device=q.device)
+    _check(lib().ttm_titans_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W0), _ptr(S0),
+                                int(bool(w0_shared)), _ptr(z), _ptr(W_out), _ptr(S_out),
+                                _stream(q, stream)), "ttm_titans_fwd")
+    return z, W_out, S_out
+
+
+def mlp_fwd(q, k, v, theta, W1_0, W2_0, chunk, *, eta=None, alpha=None, S1_0=None, S2_0=None,
+            w0_shared=False, z=None, W1_out=None, W2_out=None, S1_out=None, S2_out=None,
+            want_S=True, stream=None):
+    """Deep-memory scan, f(x) = W2 GELU(W1 x).  W1_0: [B|1,H,hidden,d], W2_0: [B|1,H,d,hidden].
+    Returns (z, W1, W2, S1, S2)."""
+    import torch
+    B, H, T, d = q.shape
+    hidden = W1_0.shape[-2]
+    dev = q.device
+    z = torch.empty_like(v) if z is None else z
+    mk = lambda s: torch.empty(s, dtype=torch.float32, device=dev)
+    W1_out = mk((B, H, hidden, d)) if W1_out is None else W1_out
+    W2_out = mk((B, H, d, hidden)) if W2_out is None else W2_out
+    if want_S or eta is not None:
+        S1_out = mk((B, H, hidden, d)) if S1_out is None else S1_out
+        S2_out = mk((B, H, d, hidden)) if S2_out is None else S2_out
+    _check(lib().ttm_mlp_fwd(B, H, T, d, hidden, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
+                             _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W1_0),
+                             _ptr(W2_0), _ptr(S1_0), _ptr(S2_0), int(bool(w0_shared)), _ptr(z),
+                             _ptr(W1_out), _ptr(W2_out), _ptr(S1_out), _ptr(S2_out),
+                             _stream(q, stream)), "ttm_mlp_fwd")
+    return z, W1_out, W2_out, S1_out, S2_out

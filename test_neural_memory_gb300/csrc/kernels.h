@@ -1,0 +1,47 @@
+// Internal interface between the C-ABI layer (ttm_api.cu) and the kernel
+// translation units.  Host-side only; no torch types anywhere.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace ttm {
+
+// One call of the linear / Titans scan.  Pointers are device pointers that the
+// API layer has already validated (non-NULL where required, 16-byte aligned).
+struct LinearArgs {
+    int B, H, T, dk, dv, chunk;
+    int bf16;                 // 1: q, k, v, z are bf16; 0: fp32
+    const void *q, *k, *v;
+    const float *eta, *theta, *alpha;   // eta / alpha may be NULL (= 0)
+    const float *W0, *S0;               // S0 may be NULL (= 0)
+    int shared;                         // W0/S0 have a leading dim of 1
+    void* z;
+    float *W_out, *S_out;               // S_out may be NULL
+    int* status;                        // device status word (bounded waits)
+};
+
+struct MlpArgs {
+    int B, H, T, d, hidden, chunk;
+    int bf16;
+    const void *q, *k, *v;
+    const float *eta, *theta, *alpha;
+    const float *W1_0, *W2_0, *S1_0, *S2_0;
+    int shared;
+    void* z;
+    float *W1_out, *W2_out, *S1_out, *S2_out;
+    int* status;
+};
+
+// fp32 CUDA-core kernels (scan_simt.cu).  The *_supported functions decide
+// on the host whether a shape fits the kernel's on-chip budget.
+bool linear_simt_supported(const LinearArgs& a);
+cudaError_t linear_simt_launch(const LinearArgs& a, cudaStream_t s);
+bool mlp_simt_supported(const MlpArgs& a);
+cudaError_t mlp_simt_launch(const MlpArgs& a, cudaStream_t s);
+
+// tcgen05 + TMA kernel for the linear / Titans scan (scan_linear_tc.cu).
+bool linear_tc_supported(const LinearArgs& a);
+cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s);
+
+}  // namespace ttm

@@ -1,0 +1,237 @@
+// C ABI of libttm.so: host-side argument validation, kernel selection and
+// launch.  Declarations and the full contract are in include/ttm.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/ttm.h"
+#include "kernels.h"
+
+namespace {
+
+// Device status word: tensor-core kernels set it when a bounded wait gives up.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];  // per-device address of g_status_word
+
+int g_policy = TTM_KERNEL_AUTO;
+unsigned long long g_launches = 0;
+thread_local int t_last_kernel = TTM_KID_NONE;
+
+int* status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+    const void* p;
+    size_t bytes;
+};
+
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Output `o` may coincide exactly with input `in` only when `exact_ok`.
+bool bad_alias(Span o, Span in, bool exact_ok) {
+    if (!overlap(o, in)) return false;
+    return !(exact_ok && o.p == in.p && o.bytes == in.bytes);
+}
+
+bool dims_ok(int x, int dtype) { return x >= 1 && x % (dtype == TTM_BF16 ? 8 : 4) == 0; }
+
+int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                  const void* k, const void* v, const float* eta, const float* theta,
+                  const float* alpha, const float* W0, const float* S0, int shared, void* z,
+                  float* W_out, float* S_out, void* stream) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
+    if ((long long)B * H > (1LL << 31) - 1 || (long long)dv > 65535LL * 16)
+        return TTM_ERR_UNSUPPORTED;
+    if (!W0 || !W_out) return TTM_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !theta || !z)) return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W0, S0, z, W_out, S_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * T;
+    const size_t nb0 = shared ? 1 : (size_t)B;
+    const size_t st = (size_t)H * dv * dk * sizeof(float);
+    const Span sq{q, tok * dk * es}, sk{k, tok * dk * es}, sv{v, tok * dv * es};
+    const Span sg[] = {{eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
+    const Span sW0{W0, nb0 * st}, sS0{S0, nb0 * st};
+    const Span sz{z, tok * dv * es}, sW{W_out, (size_t)B * st}, sS{S_out, (size_t)B * st};
+    const Span outs[] = {sz, sW, sS};
+    for (const Span& o : outs) {
+        if (bad_alias(o, sq, false) || bad_alias(o, sk, false) || bad_alias(o, sv, false))
+            return TTM_ERR_INVALID_ARG;
+        for (const Span& g : sg)
+            if (bad_alias(o, g, false)) return TTM_ERR_INVALID_ARG;
+    }
+    // W_out may be W0 (S_out may be S0) in place when W0 is not shared.
+    if (bad_alias(sW, sW0, !shared) || bad_alias(sW, sS0, false)) return TTM_ERR_INVALID_ARG;
+    if (bad_alias(sS, sS0, !shared) || bad_alias(sS, sW0, false)) return TTM_ERR_INVALID_ARG;
+    if (overlap(sz, sW) || overlap(sz, sS) || overlap(sW, sS)) return TTM_ERR_INVALID_ARG;
+    if (bad_alias(sz, sW0, false) || bad_alias(sz, sS0, false)) return TTM_ERR_INVALID_ARG;
+
+    ttm::LinearArgs a{};
+    a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v;
+    a.eta = eta; a.theta = theta; a.alpha = alpha;
+    a.W0 = W0; a.S0 = S0; a.shared = shared ? 1 : 0;
+    a.z = z; a.W_out = W_out; a.S_out = S_out;
+
+    const bool tc_ok = ttm::linear_tc_supported(a);
+    const bool simt_ok = ttm::linear_simt_supported(a);
+    int kid = TTM_KID_NONE;
+    if (g_policy == TTM_KERNEL_TC) kid = tc_ok ? TTM_KID_LINEAR_TC : TTM_KID_NONE;
+    else if (g_policy == TTM_KERNEL_SIMT) kid = simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE;
+    else kid = tc_ok ? TTM_KID_LINEAR_TC : (simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE);
+    if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+
+    a.status = status_ptr();
+    if (!a.status) return TTM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = kid == TTM_KID_LINEAR_TC ? ttm::linear_tc_launch(a, s)
+                                                   : ttm::linear_simt_launch(a, s);
+    if (e != cudaSuccess) return TTM_ERR_CUDA;
+    t_last_kernel = kid;
+    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ttm_linear_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                   const void* k, const void* v, const float* eta, const float* theta,
+                   const float* alpha, const float* W0, int w0_shared_over_batch, void* z,
+                   float* W_out, void* stream) {
+    if (eta || alpha) return TTM_ERR_INVALID_ARG;
+    return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, nullptr, theta, nullptr, W0,
+                         nullptr, w0_shared_over_batch, z, W_out, nullptr, stream);
+}
+
+int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                   const void* k, const void* v, const float* eta, const float* theta,
+                   const float* alpha, const float* W0, const float* S0,
+                   int w0_shared_over_batch, void* z, float* W_out, float* S_out, void* stream) {
+    return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, eta, theta, alpha, W0, S0,
+                         w0_shared_over_batch, z, W_out, S_out, stream);
+}
+
+int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype, const void* q,
+                const void* k, const void* v, const float* eta, const float* theta,
+                const float* alpha, const float* W1_0, const float* W2_0, const float* S1_0,
+                const float* S2_0, int w0_shared_over_batch, void* z, float* W1_out,
+                float* W2_out, float* S1_out, float* S2_out, void* stream) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (d < 1 || hidden < 1 || d % 8 || hidden % 8) return TTM_ERR_INVALID_ARG;
+    if ((long long)B * H > (1LL << 31) - 1) return TTM_ERR_UNSUPPORTED;
+    if (!W1_0 || !W2_0 || !W1_out || !W2_out) return TTM_ERR_INVALID_ARG;
+    if ((S1_out == nullptr) != (S2_out == nullptr)) return TTM_ERR_INVALID_ARG;
+    if (eta && !S1_out) return TTM_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !theta || !z)) return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W1_0, W2_0, S1_0, S2_0,
+                          z, W1_out, W2_out, S1_out, S2_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * T;
+    const size_t nb0 = w0_shared_over_batch ? 1 : (size_t)B;
+    const size_t st = (size_t)H * hidden * d * sizeof(float);
+    const Span ins[] = {{q, tok * d * es}, {k, tok * d * es}, {v, tok * d * es},
+                        {eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
+    const Span init[] = {{W1_0, nb0 * st}, {W2_0, nb0 * st}, {S1_0, nb0 * st}, {S2_0, nb0 * st}};
+    const Span outs[] = {{W1_out, (size_t)B * st}, {W2_out, (size_t)B * st},
+                         {S1_out, (size_t)B * st}, {S2_out, (size_t)B * st}};
+    const Span sz{z, tok * d * es};
+    for (const Span& i : ins) {
+        if (overlap(sz, i)) return TTM_ERR_INVALID_ARG;
+        for (const Span& o : outs)
+            if (overlap(o, i)) return TTM_ERR_INVALID_ARG;
+    }
+    for (int o = 0; o < 4; ++o) {
+        if (overlap(outs[o], sz)) return TTM_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlap(outs[o], outs[o2])) return TTM_ERR_INVALID_ARG;
+        for (int i = 0; i < 4; ++i)
+            if (bad_alias(outs[o], init[i], i == o && !w0_shared_over_batch))
+                return TTM_ERR_INVALID_ARG;
+    }
+    for (const Span& i : init)
+        if (overlap(sz, i)) return TTM_ERR_INVALID_ARG;
+
+    ttm::MlpArgs a{};
+    a.B = B; a.H = H; a.T = T; a.d = d; a.hidden = hidden; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v;
+    a.eta = eta; a.theta = theta; a.alpha = alpha;
+    a.W1_0 = W1_0; a.W2_0 = W2_0; a.S1_0 = S1_0; a.S2_0 = S2_0;
+    a.shared = w0_shared_over_batch ? 1 : 0;
+    a.z = z; a.W1_out = W1_out; a.W2_out = W2_out; a.S1_out = S1_out; a.S2_out = S2_out;
+
+    const bool simt_ok = ttm::mlp_simt_supported(a);
+    int kid = TTM_KID_NONE;
+    if (g_policy != TTM_KERNEL_TC && simt_ok) kid = TTM_KID_MLP_SIMT;
+    if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+    a.status = status_ptr();
+    if (!a.status) return TTM_ERR_CUDA;
+    const cudaError_t e = ttm::mlp_simt_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return TTM_ERR_CUDA;
+    t_last_kernel = kid;
+    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+const char* ttm_status_str(int status) {
+    switch (status) {
+        case TTM_OK: return "ok";
+        case TTM_ERR_INVALID_ARG: return "invalid argument";
+        case TTM_ERR_UNSUPPORTED: return "shape or dtype not supported by the selected kernels";
+        case TTM_ERR_CUDA: return "CUDA error";
+        case TTM_ERR_TIMEOUT: return "a device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int ttm_set_kernel_policy(int policy) {
+    if (policy != TTM_KERNEL_AUTO && policy != TTM_KERNEL_SIMT && policy != TTM_KERNEL_TC)
+        return -1;
+    const int old = g_policy;
+    g_policy = policy;
+    return old;
+}
+
+int ttm_last_kernel(void) { return t_last_kernel; }
+
+unsigned long long ttm_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+int ttm_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return TTM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return TTM_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return TTM_ERR_CUDA;
+    return v == 0 ? TTM_OK : v;
+}
+
+}  // extern "C"

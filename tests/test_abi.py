@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports what include/ttm.h
+declares, and rejects malformed calls on the host before touching CUDA."""
+import ctypes
+
+import pytest
+import torch
+
+import test_neural_memory_gb300 as ttm
+
+INVALID, UNSUPPORTED, CUDA = ttm.ERR_INVALID_ARG, ttm.ERR_UNSUPPORTED, ttm.ERR_CUDA
+
+
+@pytest.fixture(scope="module")
+def L():
+    ttm.build()
+    return ttm.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = ttm.declared_symbols()
+    assert {"ttm_linear_fwd", "ttm_titans_fwd", "ttm_mlp_fwd", "ttm_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(5):
+        assert ttm.status_str(code) and ttm.status_str(code) != "unknown status"
+    assert ttm.status_str(99) == "unknown status"
+
+
+def test_policy_round_trip(L):
+    assert ttm.set_kernel_policy("simt") == "auto"
+    assert ttm.set_kernel_policy("tc") == "simt"
+    assert ttm.set_kernel_policy("auto") == "tc"
+    assert L.ttm_set_kernel_policy(7) == -1
+    assert ttm.set_kernel_policy("auto") == "auto"
+
+
+# Fake, never-dereferenced device addresses: validation rejects before any use.
+A = 1 << 20
+
+
+def P(i, misalign=0):
+    return ctypes.c_void_p(A * (i + 1) + misalign)
+
+
+def lin_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=4, dt=1, q=P(0), k=P(1), v=P(2), eta=None,
+             theta=P(3), alpha=None, W0=P(4), shared=0, z=P(5), W=P(6)):
+    return L.ttm_linear_fwd(B, H, T, dk, dv, chunk, dt, q, k, v, eta, theta, alpha, W0, shared,
+                            z, W, None)
+
+
+def test_linear_rejects_malformed(L):
+    assert lin_call(L, B=0) == INVALID
+    assert lin_call(L, T=-1) == INVALID
+    assert lin_call(L, chunk=0) == INVALID
+    assert lin_call(L, dt=5) == INVALID
+    assert lin_call(L, dk=12) == INVALID          # bf16 rows must be multiples of 8
+    assert lin_call(L, dt=0, dk=6) == INVALID     # fp32 rows must be multiples of 4
+    assert lin_call(L, W0=None) == INVALID
+    assert lin_call(L, theta=None) == INVALID
+    assert lin_call(L, q=P(0, 8)) == INVALID      # not 16-byte aligned
+    assert lin_call(L, eta=P(7)) == INVALID       # TTT-Linear has no momentum
+    assert lin_call(L, alpha=P(7)) == INVALID
+    assert lin_call(L, z=P(0)) == INVALID         # output overlaps an input
+    assert lin_call(L, W=P(4), shared=1) == INVALID   # in place only when not shared
+
+
+def test_titans_and_mlp_reject_malformed(L):
+    r = L.ttm_titans_fwd(1, 1, 8, 64, 64, 4, 1, P(0), P(1), P(2), P(3), P(4), P(5), P(6),
+                         P(7), 0, P(8), P(9), P(9), None)
+    assert r == INVALID                            # S_out == W_out
+    r = L.ttm_mlp_fwd(1, 1, 8, 64, 256, 4, 1, P(0), P(1), P(2), P(3), P(4), None, P(5), P(6),
+                      None, None, 0, P(8), P(9), P(10), None, None, None)
+    assert r == INVALID                            # eta given without S outputs
+    r = L.ttm_mlp_fwd(1, 1, 8, 64, 256, 4, 1, P(0), P(1), P(2), None, P(4), None, P(5), P(6),
+                      None, None, 0, P(8), P(9), P(10), P(11), None, None)
+    assert r == INVALID                            # S1_out without S2_out
+    r = L.ttm_mlp_fwd(1, 1, 8, 60, 256, 4, 1, P(0), P(1), P(2), None, P(4), None, P(5), P(6),
+                      None, None, 0, P(8), P(9), P(10), None, None, None)
+    assert r == INVALID                            # d not a multiple of 8
+
+
+def test_tc_policy_reports_unsupported_on_host(L):
+    with ttm.kernel_policy("tc"):
+        # fp32 inputs never run on the tensor-core kernel
+        assert lin_call(L, dt=0) == UNSUPPORTED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a GPU")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    assert lin_call(L) == CUDA
+
+
+def test_python_layer_raises(L):
+    with pytest.raises(ttm.TTMError) as e:
+        ttm._check(INVALID, "ttm_linear_fwd")
+    assert e.value.code == INVALID
