@@ -1,8 +1,681 @@
-// tcgen05 + TMA kernel of the linear / Titans scan (not available yet: every
-// shape is reported as unsupported so the dispatcher uses the CUDA-core kernel).
+// Tensor-core (tcgen05 + TMA) kernel of the chunked linear / Titans memory scan.
+//
+// Method (per sequence, chunks of 64 tokens; "TTT layers 与 fast weights" §1.1
+// eqs (7)-(9) for the matrix form of one chunk, "论文速览 | Titans" §4.3-§4.5
+// for the decay / momentum unrolling): with the chunk-start state (W, S), the
+// chunk's keys K, queries Q, values V (rows = tokens) and the per-chunk
+// coefficients beta_t, c_t, P_t, C[t][s] (see scan_simt.cu for their
+// definition),
+//
+//   E^T  = K W^T - V                       errors at the chunk-start state
+//   z_t  = beta_t (Q W^T)_t + c_t (Q S^T)_t - 2 sum_{s<=t} C[t][s] (q_t.k_s) e_s
+//   W'   = beta_n W + c_n S - 2 (E diag(C[n][.]) K)
+//   S'   = P_n S        - 2 (E diag(Pm[n][.]) K)
+//
+// Every row of W (and S) evolves independently of the others (its error only
+// involves that row), so one CTA owns a slice of 16 rows of one sequence's
+// memory and runs the whole sequence; the grid covers (sequence, slice).
+//
+// Roles inside a CTA (256 threads):
+//   warps 0-3  chain epilogues.  Thread j holds W[r0..r0+15][j] and
+//              S[r0..r0+15][j] in fp32 registers for the whole sequence.
+//              Warps 0-1 (thread = token) turn K W^T into the errors and the
+//              scaled error operands; all four apply the state carry.
+//   warp 4     producer: TMA loads of K, Q (128-byte swizzle) and the V slice;
+//              gates by plain loads; the chunk coefficients by warp scans.
+//   warp 5     MMA issuer (one thread) and TMEM owner.
+//   warps 6-7  reads: masked, coefficient-weighted scores and the output z.
+//
+// Tensor-core contractions per chunk (A operands are M = 128 rows: the K tile
+// and the Q tile are stacked so one instruction covers both):
+//   MMA1  [K;Q] . [W;S]^T      -> K W^T (errors), Q W^T, Q S^T     (chain)
+//   MMA2  K^T . [C_n E^T | Pm_n E^T] -> the state updates           (chain)
+//   MMAqk [K;Q] . K^T          -> Q K^T (scores), one chunk ahead
+//   MMAz  A~ . E^T             -> the causal correction of the reads
+// Operands are bf16, accumulators fp32 in tensor memory; the fp32 state
+// masters never leave registers.
+//
+// Every wait is bounded: a wait that exceeds its limit sets the device status
+// word to TTM_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are
+// drained, TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "../../include/ttm.h"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace ttm {
-bool linear_tc_supported(const LinearArgs&) { return false; }
-cudaError_t linear_tc_launch(const LinearArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
+constexpr int kRows = 16;       // rows of W per CTA
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+
+// TMEM column map
+constexpr uint32_t kAcc1 = 0;     // 2 x 32 columns: [K W^T | K S^T] on lanes 0-63, [Q W^T | Q S^T] on 64-127
+constexpr uint32_t kAcc2 = 64;    // 32 columns: W / S updates (lane = d_k index)
+constexpr uint32_t kAccQK = 128;  // 2 x 64 columns: Q K^T on lanes 64-127
+constexpr uint32_t kAccZ = 256;   // 2 x 16 columns: A~ E^T on lanes 64-127
+
+// Per-stage coefficient block (fp32, 64 tokens each)
+struct Coef {
+    float theta[kChunk];
+    float eta[kChunk];    // 1 past the chunk's last token
+    float keep[kChunk];   // 1 - alpha; 1 past the last token
+    float beta[kChunk];   // prod_{j<=t} keep_j
+    float cvec[kChunk];   // c_t
+    float cend[kChunk];   // C[n-1][s]
+    float pend[kChunk];   // Pm[n-1][s]
+    float scal[4];        // beta_{n-1}, c_{n-1}, P_{n-1}, n
+};
+static_assert(sizeof(Coef) <= 2048, "coefficient block");
+
+struct Layout {
+    int D, NS;
+    uint32_t kq_bytes, stage_bytes;
+    uint32_t off_ws, off_b2, off_et, off_at, total;
+};
+
+__host__ __device__ constexpr Layout make_layout(int D) {
+    Layout L{};
+    L.D = D;
+    L.NS = D == 128 ? 3 : 4;
+    L.kq_bytes = (D / 64) * 16384u;           // per 64-column half: K (8 KB) then Q (8 KB)
+    L.stage_bytes = L.kq_bytes + 2048u + 2048u;  // + V slice + coefficients
+    uint32_t off = L.NS * L.stage_bytes;
+    L.off_ws = off;  off += D * 128u;         // [W;S] operand, row = d_k index
+    L.off_b2 = off;  off += kChunk * 128u;    // [C E^T | Pm E^T], row = token
+    L.off_et = off;  off += 2 * kChunk * 128u;    // E^T, row = token, x2
+    L.off_at = off;  off += 2 * 128 * 128u;   // A~ (rows 64-127 used), x2
+    L.total = off;
+    return L;
+}
+
+struct Bars {
+    uint64_t full[4], empty[4];
+    uint64_t ws_ready, b2_ready, mma2_done;
+    uint64_t mma1_done[2], acc1_free[2], qk_done[2], qk_free[2], at_ready[2], z_done[2],
+        accz_free[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct TcParams {
+    LinearArgs a;
+    int nslices;
+};
+
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    const long long t0 = clock64();
+    uint32_t polls = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if ((++polls & 63u) == 0) {
+            if (*(volatile int*)&B->abort) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                *(volatile int*)&B->abort = 1;
+                atomicExch(status, TTM_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Warp-uniform variant: every lane of the warp gets the same answer, so a
+// timeout seen by one lane never splits the warp before a .sync.aligned op.
+__device__ __forceinline__ bool wait_all(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    return __all_sync(0xffffffffu, wait_bar(B, bar, parity, status));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Stores 8 consecutive bf16 values (one 16-byte chunk) of row `row` starting
+// at column `col` (multiple of 8) into a 128-byte-swizzled tile.
+__device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int col, const float* x) {
+    uint4 v;
+    v.x = pack_bf16(x[0], x[1]);
+    v.y = pack_bf16(x[2], x[3]);
+    v.z = pack_bf16(x[4], x[5]);
+    v.w = pack_bf16(x[6], x[7]);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col)) = v;
+}
+
+// ---------------------------------------------------------------- warp scans
+
+// Inclusive scan of affine maps x -> A x + B along lanes (lane order = token
+// order); the composition puts later lanes outside.
+__device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float A2 = __shfl_up_sync(0xffffffffu, A, off);
+        const float B2 = __shfl_up_sync(0xffffffffu, B, off);
+        if (lane >= off) {
+            B = A * B2 + B;
+            A = A * A2;
+        }
+    }
+}
+
+// Inclusive scan along decreasing lane index (suffix), later (lower) lanes outside.
+__device__ __forceinline__ void scan_affine_down(float& A, float& B, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float A2 = __shfl_down_sync(0xffffffffu, A, off);
+        const float B2 = __shfl_down_sync(0xffffffffu, B, off);
+        if (lane + off < 32) {
+            B = A * B2 + B;
+            A = A * A2;
+        }
+    }
+}
+
+// Producer-side chunk coefficients.  Lane l owns tokens 2l and 2l+1.
+__device__ void chunk_coefficients(const LinearArgs& a, size_t tok0, int n, Coef* cf, int lane) {
+    float th[2], et[2], kp[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int t = 2 * lane + u;
+        const bool ok = t < n;
+        th[u] = ok ? a.theta[tok0 + t] : 0.f;
+        et[u] = ok ? (a.eta ? a.eta[tok0 + t] : 0.f) : 1.f;
+        kp[u] = ok ? 1.f - (a.alpha ? a.alpha[tok0 + t] : 0.f) : 1.f;
+    }
+    // forward: beta_t = prod keep, P_t = prod eta, c_t = keep_t c_{t-1} + P_t.
+    // beta and P are scans of maps x -> keep x (resp. eta x); c is the affine
+    // recurrence whose maps x -> keep_t x + P_t need P first.
+    float Ab = kp[0] * kp[1], Bb = 0.f;
+    scan_affine_up(Ab, Bb, lane);
+    float Ap = et[0] * et[1], Bp = 0.f;
+    scan_affine_up(Ap, Bp, lane);
+    float pre_b = __shfl_up_sync(0xffffffffu, Ab, 1);
+    float pre_p = __shfl_up_sync(0xffffffffu, Ap, 1);
+    if (lane == 0) pre_b = pre_p = 1.f;
+    const float beta0 = pre_b * kp[0], beta1 = beta0 * kp[1];
+    const float P0 = pre_p * et[0], P1 = P0 * et[1];
+    // c: lane-local composition of (kp0, P0) then (kp1, P1)
+    float Ac = kp[1] * kp[0], Bc = kp[1] * P0 + P1;
+    scan_affine_up(Ac, Bc, lane);
+    float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);   // c just before this lane's tokens
+    if (lane == 0) cpre = 0.f;
+    const float c0 = kp[0] * cpre + P0, c1 = kp[1] * c0 + P1;
+
+    // backward from the last token n-1:
+    //   m_s    = prod_{j=s+1}^{n-1} eta_j      (suffix products; neutral past n-1)
+    //   bsuf_s = prod_{j=s+1}^{n-1} keep_j
+    //   w_s    = bsuf_s + eta_{s+1} w_{s+1},  w_{n-1} = 1
+    // eta / keep past n-1 are 1 and theta 0, so suffix products start at n-1.
+    // The eta_{s+1} / keep_{s+1} of a lane's second token come from the next lane.
+    const float et_next = __shfl_down_sync(0xffffffffu, et[0], 1);   // eta_{2l+2}
+    const float kp_next = __shfl_down_sync(0xffffffffu, kp[0], 1);
+    const float e_n1 = lane == 31 ? 1.f : et_next;
+    const float k_n1 = lane == 31 ? 1.f : kp_next;
+    // exclusive suffix products over tokens > t (lane-level then within the pair)
+    float Am = et[0] * et[1], Bm = 0.f;
+    scan_affine_down(Am, Bm, lane);
+    float Ak = kp[0] * kp[1], Bk = 0.f;
+    scan_affine_down(Ak, Bk, lane);
+    float suf_m = __shfl_down_sync(0xffffffffu, Am, 1);
+    float suf_k = __shfl_down_sync(0xffffffffu, Ak, 1);
+    if (lane == 31) suf_m = suf_k = 1.f;
+    const float m1 = suf_m, m0 = et[1] * suf_m;          // tokens 2l+1, 2l
+    const float bs1 = suf_k, bs0 = kp[1] * suf_k;
+    // w recurrence as maps applied from the end: w_s = F_s(w_{s+1}),
+    // F_s(x) = eta_{s+1} x + bsuf_s, except F_{n-1}(x) = 1 (absorbing).
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    float A1 = e_n1, B1 = bs1;               // token t1, its successor is 2l+2
+    if (t1 == n - 1) { A1 = 0.f; B1 = 1.f; }
+    float A0 = et[1], B0 = bs0;              // token t0, its successor is t1
+    if (t0 == n - 1) { A0 = 0.f; B0 = 1.f; }
+    // lane composition: w_{t0} = F0(F1(x))
+    float Aw = A0 * A1, Bw = A0 * B1 + B0;
+    scan_affine_down(Aw, Bw, lane);
+    float wnext = __shfl_down_sync(0xffffffffu, Bw, 1);   // w at token 2l+2 (any input: absorbed)
+    if (lane == 31) wnext = 1.f;
+    const float w1 = A1 * wnext + B1, w0 = A0 * w1 + B0;
+    (void)k_n1;
+
+    cf->theta[t0] = th[0];  cf->theta[t1] = th[1];
+    cf->eta[t0] = et[0];    cf->eta[t1] = et[1];
+    cf->keep[t0] = kp[0];   cf->keep[t1] = kp[1];
+    cf->beta[t0] = beta0;   cf->beta[t1] = beta1;
+    cf->cvec[t0] = c0;      cf->cvec[t1] = c1;
+    cf->cend[t0] = th[0] * w0;  cf->cend[t1] = th[1] * w1;
+    cf->pend[t0] = th[0] * m0;  cf->pend[t1] = th[1] * m1;
+    // scalars at the chunk's last token
+    const int ln = (n - 1) >> 1, un = (n - 1) & 1;
+    const float bn = __shfl_sync(0xffffffffu, un ? beta1 : beta0, ln);
+    const float cn = __shfl_sync(0xffffffffu, un ? c1 : c0, ln);
+    const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
+    if (lane == 0) {
+        cf->scal[0] = bn;
+        cf->scal[1] = cn;
+        cf->scal[2] = Pn;
+        cf->scal[3] = (float)n;
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap vmap, const TcParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    __shared__ Bars bars;
+    Bars* B = &bars;
+    constexpr Layout L = make_layout(D);
+    const LinearArgs& a = P.a;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slice = blockIdx.x % P.nslices;
+    const int seq = blockIdx.x / P.nslices;
+    const int bb = seq / a.H, hh = seq % a.H;
+    const int r0 = slice * kRows;
+    const int T = a.T;
+    const int nch = (T + kChunk - 1) / kChunk;
+    int* status = a.status;
+
+    auto stage = [&](int s) { return sm + s * L.stage_bytes; };
+    auto vtile = [&](int s) { return stage(s) + L.kq_bytes; };
+    auto coef = [&](int s) { return reinterpret_cast<Coef*>(stage(s) + L.kq_bytes + 2048); };
+    uint8_t* ws = sm + L.off_ws;
+    uint8_t* b2 = sm + L.off_b2;
+    auto et = [&](int b) { return sm + L.off_et + b * (kChunk * 128); };
+    auto at = [&](int b) { return sm + L.off_at + b * (128 * 128); };
+
+    if (tid == 0) {
+        for (int s = 0; s < L.NS; ++s) {
+            mbar_init(&B->full[s], 2);
+            mbar_init(&B->empty[s], 128 + 64 + 1);
+        }
+        mbar_init(&B->ws_ready, 128);
+        mbar_init(&B->b2_ready, 64);
+        mbar_init(&B->mma2_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&B->mma1_done[b], 1);
+            mbar_init(&B->acc1_free[b], 64);
+            mbar_init(&B->qk_done[b], 1);
+            mbar_init(&B->qk_free[b], 64);
+            mbar_init(&B->at_ready[b], 64);
+            mbar_init(&B->z_done[b], 1);
+            mbar_init(&B->accz_free[b], 64);
+        }
+        mbar_init(&B->drain, 1);
+        B->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(&B->tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem_base;
+
+    if (warp < 4) {
+        // ---------------------------------------------------- chain epilogues
+        const int j = tid;                 // d_k index (state), token index in Epi1
+        const bool own = j < D;
+        const size_t init = (size_t)(a.shared ? 0 : bb) * a.H + hh;
+        float w[kRows], s[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const size_t idx = (init * D + r0 + i) * (size_t)D + j;
+            w[i] = own ? a.W0[idx] : 0.f;
+            s[i] = (own && a.S0) ? a.S0[idx] : 0.f;
+        }
+        auto write_ws = [&]() {
+            if (!own) return;
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) st_chunk(ws, j, 8 * c8, w + 8 * c8);
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) st_chunk(ws, j, 16 + 8 * c8, s + 8 * c8);
+        };
+        write_ws();
+        fence_proxy_async_smem();
+        mbar_arrive(&B->ws_ready);
+        bool ok = true;
+        for (int c = 0; c < nch && ok; ++c) {
+            const int st = c % L.NS, b = c & 1;
+            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
+            if (!ok) break;
+            const Coef* cf = coef(st);
+            const float bn = cf->scal[0], cn = cf->scal[1], Pn = cf->scal[2];
+            if (warp < 2) {
+                const int t = j;
+                const float ce = cf->cend[t], pe = cf->pend[t];
+                ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
+                if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                float kw[16];
+                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
+                const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
+                const uint4 v0 = vrow[0], v1 = vrow[1];
+                tmem_wait_ld();
+                const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
+                const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
+                float e[16], ec[16], ep[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f0 = __bfloat1622float2(vb0[i]);
+                    const float2 f1 = __bfloat1622float2(vb1[i]);
+                    e[2 * i] = kw[2 * i] - f0.x;
+                    e[2 * i + 1] = kw[2 * i + 1] - f0.y;
+                    e[8 + 2 * i] = kw[8 + 2 * i] - f1.x;
+                    e[8 + 2 * i + 1] = kw[8 + 2 * i + 1] - f1.y;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    ec[i] = ce * e[i];
+                    ep[i] = pe * e[i];
+                }
+                st_chunk(b2, t, 0, ec);
+                st_chunk(b2, t, 8, ec + 8);
+                st_chunk(b2, t, 16, ep);
+                st_chunk(b2, t, 24, ep + 8);
+                st_chunk(et(b), t, 0, e);
+                st_chunk(et(b), t, 8, e + 8);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&B->b2_ready);
+            }
+            mbar_arrive(&B->empty[st]);
+            ok = wait_all(B, &B->mma2_done, c & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            if (own) {
+                float uw[16], us[16];
+                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2), uw);
+                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2 + 16), us);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    const float wn = bn * w[i] + cn * s[i] - 2.f * uw[i];
+                    s[i] = Pn * s[i] - 2.f * us[i];
+                    w[i] = wn;
+                }
+            }
+            write_ws();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&B->ws_ready);
+        }
+        if (own) {
+            const size_t dst = (size_t)seq * D * D;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                a.W_out[dst + (size_t)(r0 + i) * D + j] = w[i];
+                if (a.S_out) a.S_out[dst + (size_t)(r0 + i) * D + j] = s[i];
+            }
+        }
+    } else if (warp == 4) {
+        // --------------------------------------------------------- producer
+        const uint32_t tx = L.kq_bytes + kChunk * kRows * 2;
+        int issued = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int st = c % L.NS;
+            bool ok = true;
+            if (c >= L.NS && lane == 0) ok = wait_bar(B, &B->empty[st], ((c / L.NS) - 1) & 1, status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane == 0) {
+                mbar_expect_tx(&B->full[st], tx);
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(stage(st) + h * 16384, &kmap, &B->full[st], 64 * h, c * kChunk, seq);
+                    tma_load_3d(stage(st) + h * 16384 + 8192, &qmap, &B->full[st], 64 * h,
+                                c * kChunk, seq);
+                }
+                tma_load_3d(vtile(st), &vmap, &B->full[st], r0, c * kChunk, seq);
+            }
+            issued = c + 1;
+            const int n = min(kChunk, T - c * kChunk);
+            chunk_coefficients(a, (size_t)seq * T + (size_t)c * kChunk, n, coef(st), lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->full[st]);
+        }
+        // drain: every issued stage's copies must have landed before exit
+        if (lane == 0) {
+            for (int c = (issued > L.NS ? issued - L.NS : 0); c < issued; ++c) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&B->full[c % L.NS], (c / L.NS) & 1))
+                    if (clock64() - t0 > kWaitCycles) break;
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0 && nch > 0) {
+            const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);
+            const uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);
+            const uint32_t idqk = idesc_bf16_f32(128, 64, 0, 0);
+            const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
+            const uint32_t ws_a = smem_u32(ws), b2_a = smem_u32(b2);
+            auto issue_qk = [&](int c) {
+                const int st = c % L.NS;
+                const uint32_t base = smem_u32(stage(st));
+                const uint32_t d = tmem + kAccQK + (c & 1) * 64;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(d, sdesc(half, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk, kk > 0);
+                }
+                mma_commit(&B->qk_done[c & 1]);
+            };
+            bool ok = wait_bar(B, &B->full[0], 0, status);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0);
+            }
+            for (int c = 0; c < nch && ok; ++c) {
+                const int st = c % L.NS, b = c & 1;
+                const uint32_t base = smem_u32(stage(st));
+                ok = wait_bar(B, &B->ws_ready, c & 1, status);
+                if (ok && c >= 2) ok = wait_bar(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                // MMA1: [K;Q] . [W;S]^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
+                             sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
+                }
+                mma_commit(&B->mma1_done[b]);
+                // MMA2: K^T . [C E^T | Pm E^T]
+                ok = wait_bar(B, &B->b2_ready, c & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk) {
+                    mma_bf16(tmem + kAcc2, sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
+                             sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
+                }
+                mma_commit(&B->mma2_done);
+                mma_commit(&B->empty[st]);
+                // scores of the next chunk
+                if (c + 1 < nch) {
+                    ok = wait_bar(B, &B->full[(c + 1) % L.NS], ((c + 1) / L.NS) & 1, status);
+                    if (ok && c + 1 >= 2)
+                        ok = wait_bar(B, &B->qk_free[(c + 1) & 1], ((c - 1) >> 1) & 1, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(c + 1);
+                }
+                // MMAz: A~ . E^T
+                ok = wait_bar(B, &B->at_ready[b], (c >> 1) & 1, status);
+                if (ok && c >= 2) ok = wait_bar(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t at_a = smem_u32(at(b)), et_a = smem_u32(et(b));
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk) {
+                    mma_bf16(tmem + kAccZ + b * 16, sdesc(at_a + kk * 32, 16, 1024, 2),
+                             sdesc(et_a + kk * 2048, 8192, 1024, 2), idz, kk > 0);
+                }
+                mma_commit(&B->z_done[b]);
+            }
+            // drain: all issued MMAs complete before TMEM is released
+            mma_commit(&B->drain);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&B->drain, 0))
+                if (clock64() - t0 > kWaitCycles) break;
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- z warps 6-7
+        const int t = tid - 192;             // token, TMEM lane 64 + t
+        const int wl = (warp & 3) * 32;      // 64 or 96
+        bool ok = true;
+        for (int c = 0; c < nch && ok; ++c) {
+            const int st = c % L.NS, b = c & 1;
+            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
+            if (ok) ok = wait_all(B, &B->qk_done[b], (c >> 1) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            const Coef* cf = coef(st);
+            // A~[t][s] = C[t][s] (q_t . k_s) for s <= t, by the backward recurrence
+            //   w(t,t) = 1, w(s,t) = bsuf + eta_{s+1} w(s+1,t), bsuf *= keep_{s+1}
+            float qk[64];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float r[16];
+                tmem_ld16(tmem_addr(tmem, wl, kAccQK + b * 64 + 16 * q4), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) qk[16 * q4 + i] = r[i];
+            }
+            tc_fence_before();
+            mbar_arrive(&B->qk_free[b]);
+            float bs = 1.f, wv = 1.f;
+#pragma unroll
+            for (int s = kChunk - 1; s >= 0; --s) {
+                if (s < t) {
+                    bs *= cf->keep[s + 1];
+                    wv = bs + cf->eta[s + 1] * wv;
+                }
+                qk[s] = (s <= t) ? cf->theta[s] * wv * qk[s] : 0.f;
+            }
+            uint8_t* arow = at(b);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) st_chunk(arow, 64 + t, 8 * c8, qk + 8 * c8);
+            fence_proxy_async_smem();
+            mbar_arrive(&B->at_ready[b]);
+            // reads: z_t = beta_t Q W^T + c_t Q S^T - 2 A~ E^T
+            ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            float qw[16], qs[16], ae[16];
+            tmem_ld16(tmem_addr(tmem, wl, kAcc1 + b * 32), qw);
+            tmem_ld16(tmem_addr(tmem, wl, kAcc1 + b * 32 + 16), qs);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&B->acc1_free[b]);
+            ok = wait_all(B, &B->z_done[b], (c >> 1) & 1, status);
+            if (!ok) break;
+            tc_fence_after();
+            tmem_ld16(tmem_addr(tmem, wl, kAccZ + b * 16), ae);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&B->accz_free[b]);
+            const float bt = cf->beta[t], ct = cf->cvec[t];
+            const int n = (int)cf->scal[3];
+            mbar_arrive(&B->empty[st]);
+            if (t < n) {
+                float zz[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) zz[i] = bt * qw[i] + ct * qs[i] - 2.f * ae[i];
+                uint4 o0, o1;
+                o0.x = pack_bf16(zz[0], zz[1]);   o0.y = pack_bf16(zz[2], zz[3]);
+                o0.z = pack_bf16(zz[4], zz[5]);   o0.w = pack_bf16(zz[6], zz[7]);
+                o1.x = pack_bf16(zz[8], zz[9]);   o1.y = pack_bf16(zz[10], zz[11]);
+                o1.z = pack_bf16(zz[12], zz[13]); o1.w = pack_bf16(zz[14], zz[15]);
+                __nv_bfloat16* zr = static_cast<__nv_bfloat16*>(a.z) +
+                                    ((size_t)seq * T + (size_t)c * kChunk + t) * D + r0;
+                reinterpret_cast<uint4*>(zr)[0] = o0;
+                reinterpret_cast<uint4*>(zr)[1] = o1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D view [sequences][T][D] of a bf16 tensor, tile box {bx, 64, 1}.
+bool make_map(CUtensorMap* m, const void* ptr, int BH, int T, int D, int bx, bool swz) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)bx, (cuuint32_t)kChunk, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool linear_tc_supported(const LinearArgs& a) {
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kChunk &&
+           a.T >= 1 && encode_fn() != nullptr;
+}
+
+cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s) {
+    const int D = a.dk, BH = a.B * a.H;
+    CUtensorMap km, qm, vm;
+    if (!make_map(&km, a.k, BH, a.T, D, 64, true) || !make_map(&qm, a.q, BH, a.T, D, 64, true) ||
+        !make_map(&vm, a.v, BH, a.T, D, kRows, false))
+        return cudaErrorInvalidValue;
+    TcParams p{a, D / kRows};
+    const Layout L = make_layout(D);
+    const size_t smem = L.total + 1024;
+    dim3 grid(BH * (D / kRows));
+    if (D == 128) {
+        cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        linear_tc_kernel<128><<<grid, kThreads, smem, s>>>(km, qm, vm, p);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        linear_tc_kernel<64><<<grid, kThreads, smem, s>>>(km, qm, vm, p);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace ttm
