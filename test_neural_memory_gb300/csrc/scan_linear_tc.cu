@@ -458,24 +458,51 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------- MMA
-        if (lane == 0 && nch > 0) {
+        // The whole warp runs the schedule (waits are warp-uniform); one
+        // elected lane issues each group of MMAs from converged code.
+        if (nch > 0) {
             const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);
             const uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);
             const uint32_t idqk = idesc_bf16_f32(128, 64, 0, 0);
             const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
             const uint32_t ws_a = smem_u32(ws), b2_a = smem_u32(b2);
             auto issue_qk = [&](int c) {
-                const int st = c % L.NS;
-                const uint32_t base = smem_u32(stage(st));
+                const uint32_t base = smem_u32(stage(c % L.NS));
                 const uint32_t d = tmem + kAccQK + (c & 1) * 64;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(d, sdesc(half, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16(d, sdesc(half, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk, kk > 0);
+                    }
+                    mma_commit(&B->qk_done[c & 1]);
                 }
-                mma_commit(&B->qk_done[c & 1]);
+                __syncwarp();
             };
-            bool ok = wait_bar(B, &B->full[0], 0, status);
+            auto issue_z = [&](int c) {
+                const int b = c & 1;
+                const uint32_t at_a = smem_u32(at(b)), et_a = smem_u32(et(b));
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 16; ++kk)
+                        mma_bf16(tmem + kAccZ + b * 16, sdesc(at_a + kk * 32, 16, 1024, 2),
+                                 sdesc(et_a + kk * 2048, 8192, 1024, 2), idz, kk > 0);
+                    mma_commit(&B->z_done[b]);
+                }
+                __syncwarp();
+            };
+            // MMAz(c) needs the read side's A~(c); it is issued behind the next
+            // chain step so the issuer never stalls the chain on the read side.
+            auto try_z = [&](int c) -> bool {
+                const int b = c & 1;
+                bool ok = wait_all(B, &B->at_ready[b], (c >> 1) & 1, status);
+                if (ok && c >= 2) ok = wait_all(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
+                if (!ok) return false;
+                tc_fence_after();
+                issue_z(c);
+                return true;
+            };
+            bool ok = wait_all(B, &B->full[0], 0, status);
             if (ok) {
                 tc_fence_after();
                 issue_qk(0);
@@ -483,53 +510,49 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             for (int c = 0; c < nch && ok; ++c) {
                 const int st = c % L.NS, b = c & 1;
                 const uint32_t base = smem_u32(stage(st));
-                ok = wait_bar(B, &B->ws_ready, c & 1, status);
-                if (ok && c >= 2) ok = wait_bar(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
+                ok = wait_all(B, &B->ws_ready, c & 1, status);
+                if (ok && c >= 2) ok = wait_all(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: [K;Q] . [W;S]^T
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
-                             sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
+                                 sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
+                    }
+                    mma_commit(&B->mma1_done[b]);
                 }
-                mma_commit(&B->mma1_done[b]);
+                __syncwarp();
+                if (c >= 1 && !(ok = try_z(c - 1))) break;
                 // MMA2: K^T . [C E^T | Pm E^T]
-                ok = wait_bar(B, &B->b2_ready, c & 1, status);
+                ok = wait_all(B, &B->b2_ready, c & 1, status);
                 if (!ok) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk) {
-                    mma_bf16(tmem + kAcc2, sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
-                             sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
+                    for (int kk = 0; kk < kChunk / 16; ++kk)
+                        mma_bf16(tmem + kAcc2, sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
+                                 sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
+                    mma_commit(&B->mma2_done);
+                    mma_commit(&B->empty[st]);
                 }
-                mma_commit(&B->mma2_done);
-                mma_commit(&B->empty[st]);
+                __syncwarp();
                 // scores of the next chunk
                 if (c + 1 < nch) {
-                    ok = wait_bar(B, &B->full[(c + 1) % L.NS], ((c + 1) / L.NS) & 1, status);
+                    ok = wait_all(B, &B->full[(c + 1) % L.NS], ((c + 1) / L.NS) & 1, status);
                     if (ok && c + 1 >= 2)
-                        ok = wait_bar(B, &B->qk_free[(c + 1) & 1], ((c - 1) >> 1) & 1, status);
+                        ok = wait_all(B, &B->qk_free[(c + 1) & 1], ((c - 1) >> 1) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(c + 1);
                 }
-                // MMAz: A~ . E^T
-                ok = wait_bar(B, &B->at_ready[b], (c >> 1) & 1, status);
-                if (ok && c >= 2) ok = wait_bar(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t at_a = smem_u32(at(b)), et_a = smem_u32(et(b));
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk) {
-                    mma_bf16(tmem + kAccZ + b * 16, sdesc(at_a + kk * 32, 16, 1024, 2),
-                             sdesc(et_a + kk * 2048, 8192, 1024, 2), idz, kk > 0);
-                }
-                mma_commit(&B->z_done[b]);
             }
+            if (ok) try_z(nch - 1);
             // drain: all issued MMAs complete before TMEM is released
-            mma_commit(&B->drain);
+            if (elect_one()) mma_commit(&B->drain);
+            __syncwarp();
             const long long t0 = clock64();
             while (!mbar_try_wait(&B->drain, 0))
                 if (clock64() - t0 > kWaitCycles) break;
