@@ -56,7 +56,7 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map
@@ -81,29 +81,34 @@ static_assert(sizeof(Coef) <= 2048, "coefficient block");
 struct Layout {
     int D, NS;
     uint32_t kq_bytes, stage_bytes;
-    uint32_t off_ws, off_b2, off_et, off_at, total;
+    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, off_c, total;
 };
 
+// Shared-memory map.  Each A~ tile (8 KB, the 64 rows of the scores) is
+// preceded by another 8 KB buffer: its MMA reads 128 rows starting 8 KB
+// earlier and only the upper 64 rows of that product are used.
 __host__ __device__ constexpr Layout make_layout(int D) {
     Layout L{};
     L.D = D;
     L.NS = D == 128 ? 3 : 4;
-    L.kq_bytes = (D / 64) * 16384u;           // per 64-column half: K (8 KB) then Q (8 KB)
+    L.kq_bytes = (D / 64) * 16384u;              // per 64-column half: K (8 KB) then Q (8 KB)
     L.stage_bytes = L.kq_bytes + 2048u + 2048u;  // + V slice + coefficients
     uint32_t off = L.NS * L.stage_bytes;
-    L.off_ws = off;  off += D * 128u;         // [W;S] operand, row = d_k index
-    L.off_b2 = off;  off += kChunk * 128u;    // [C E^T | Pm E^T], row = token
-    L.off_et = off;  off += 2 * kChunk * 128u;    // E^T, row = token, x2
-    L.off_at = off;  off += 2 * 128 * 128u;   // A~ (rows 64-127 used), x2
+    L.off_ws = off;  off += D * 128u;            // [W;S] operand, row = d_k index
+    L.off_b2 = off;  off += kChunk * 128u;       // [C E^T | Pm E^T], row = token
+    L.off_at0 = off; off += kChunk * 128u;       // A~ (chunk parity 0)
+    L.off_et0 = off; off += kChunk * 128u;       // E^T (chunk parity 0)
+    L.off_at1 = off; off += kChunk * 128u;
+    L.off_et1 = off; off += kChunk * 128u;
+    L.off_c = off;   off += 2u * kChunk * (kChunk + 1) * 4u;   // C[t][s], fp32, x2
     L.total = off;
     return L;
 }
 
 struct Bars {
     uint64_t full[4], empty[4];
-    uint64_t ws_ready, b2_ready, mma2_done;
-    uint64_t mma1_done[2], acc1_free[2], qk_done[2], qk_free[2], at_ready[2], z_done[2],
-        accz_free[2];
+    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], qk_done[2], qk_free[2], at_ready[2], z_done[2],
+        accz_free[2], c_ready[2], c_free[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -184,17 +189,29 @@ __device__ __forceinline__ void scan_affine_down(float& A, float& B, int lane) {
     }
 }
 
-// Producer-side chunk coefficients.  Lane l owns tokens 2l and 2l+1.
-__device__ void chunk_coefficients(const LinearArgs& a, size_t tok0, int n, Coef* cf, int lane) {
+// Gates of one chunk for the producer warp: lane l owns tokens 2l and 2l+1.
+// Past the chunk's last token theta is 0 and eta / keep are 1 (neutral).
+struct Gates {
     float th[2], et[2], kp[2];
+};
+
+__device__ __forceinline__ void load_gates(const LinearArgs& a, size_t tok0, int n, int lane,
+                                           Gates& g) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int t = 2 * lane + u;
         const bool ok = t < n;
-        th[u] = ok ? a.theta[tok0 + t] : 0.f;
-        et[u] = ok ? (a.eta ? a.eta[tok0 + t] : 0.f) : 1.f;
-        kp[u] = ok ? 1.f - (a.alpha ? a.alpha[tok0 + t] : 0.f) : 1.f;
+        g.th[u] = ok ? __ldg(a.theta + tok0 + t) : 0.f;
+        g.et[u] = ok ? (a.eta ? __ldg(a.eta + tok0 + t) : 0.f) : 1.f;
+        g.kp[u] = ok ? 1.f - (a.alpha ? __ldg(a.alpha + tok0 + t) : 0.f) : 1.f;
     }
+}
+
+// Producer-side chunk coefficients from the gates (warp scans).
+__device__ void chunk_coefficients(const Gates& g, int n, Coef* cf, int lane) {
+    const float* th = g.th;
+    const float* et = g.et;
+    const float* kp = g.kp;
     // forward: beta_t = prod keep, P_t = prod eta, c_t = keep_t c_{t-1} + P_t.
     // beta and P are scans of maps x -> keep x (resp. eta x); c is the affine
     // recurrence whose maps x -> keep_t x + P_t need P first.
@@ -271,6 +288,8 @@ __device__ void chunk_coefficients(const LinearArgs& a, size_t tok0, int n, Coef
 
 // ------------------------------------------------------------------- kernel
 
+constexpr int kLdc = kChunk + 1;   // padded row length of the fp32 C matrix
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -296,18 +315,18 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     auto coef = [&](int s) { return reinterpret_cast<Coef*>(stage(s) + L.kq_bytes + 2048); };
     uint8_t* ws = sm + L.off_ws;
     uint8_t* b2 = sm + L.off_b2;
-    auto et = [&](int b) { return sm + L.off_et + b * (kChunk * 128); };
-    auto at = [&](int b) { return sm + L.off_at + b * (128 * 128); };
+    auto et = [&](int b) { return sm + (b ? L.off_et1 : L.off_et0); };
+    auto at = [&](int b) { return sm + (b ? L.off_at1 : L.off_at0); };
+    auto cmat = [&](int b) { return reinterpret_cast<float*>(sm + L.off_c) + b * kChunk * kLdc; };
 
     if (tid == 0) {
         for (int s = 0; s < L.NS; ++s) {
             mbar_init(&B->full[s], 2);
-            mbar_init(&B->empty[s], 128 + 64 + 1);
+            // chain 128 + read side 64 + coefficient pair 64 + MMA commit 1
+            mbar_init(&B->empty[s], 128 + 64 + 64 + 1);
         }
-        mbar_init(&B->ws_ready, 128);
-        mbar_init(&B->b2_ready, 64);
-        mbar_init(&B->mma2_done, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->mma1_done[b], 1);
             mbar_init(&B->acc1_free[b], 64);
             mbar_init(&B->qk_done[b], 1);
@@ -315,6 +334,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             mbar_init(&B->at_ready[b], 64);
             mbar_init(&B->z_done[b], 1);
             mbar_init(&B->accz_free[b], 64);
+            mbar_init(&B->c_ready[b], 64);
+            mbar_init(&B->c_free[b], 64);
         }
         mbar_init(&B->drain, 1);
         B->abort = 0;
@@ -326,9 +347,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = B->tmem_base;
 
+    const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);
+    const uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);
+
     if (warp < 4) {
-        // ---------------------------------------------------- chain epilogues
-        const int j = tid;                 // d_k index (state), token index in Epi1
+        // ----------------------------------------------------- chain warps
+        // Thread j holds row slice W[r0..r0+15][j], S[...][j] (fp32).  Every
+        // thread runs every iteration and reaches every named barrier, also
+        // after an abort (then it only skips work), so the barriers stay
+        // balanced.  Warp 0 issues the two chain MMAs itself.
+        const int j = tid;
         const bool own = j < D;
         const size_t init = (size_t)(a.shared ? 0 : bb) * a.H + hh;
         float w[kRows], s[kRows];
@@ -345,75 +373,118 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll
             for (int c8 = 0; c8 < 2; ++c8) st_chunk(ws, j, 16 + 8 * c8, s + 8 * c8);
         };
+        const uint32_t ws_a = smem_u32(ws), b2_a = smem_u32(b2);
+        // MMA1(c): [K;Q] . [W;S]^T, issued by warp 0 once [W;S] is in place
+        auto issue_mma1 = [&](int c, bool ok) -> bool {
+            if (warp != 0 || nch == 0) return ok;
+            const int st = c % L.NS, b = c & 1;
+            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
+            if (ok && c >= 2) ok = wait_all(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
+            if (!ok) return false;
+            tc_fence_after();
+            const uint32_t base = smem_u32(stage(st));
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
+                             sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
+                }
+                mma_commit(&B->mma1_done[b]);
+            }
+            __syncwarp();
+            return true;
+        };
         write_ws();
         fence_proxy_async_smem();
-        mbar_arrive(&B->ws_ready);
-        bool ok = true;
-        for (int c = 0; c < nch && ok; ++c) {
+        named_bar_sync(1, 128);
+        bool ok = issue_mma1(0, true);
+        for (int c = 0; c < nch; ++c) {
             const int st = c % L.NS, b = c & 1;
-            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (!ok) break;
+            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
             const Coef* cf = coef(st);
             const float bn = cf->scal[0], cn = cf->scal[1], Pn = cf->scal[2];
             if (warp < 2) {
+                // Epi1: errors of token t at the chunk-start state
                 const int t = j;
                 const float ce = cf->cend[t], pe = cf->pend[t];
-                ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
+                if (ok) ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
                 if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                float kw[16];
-                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
-                const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
-                const uint4 v0 = vrow[0], v1 = vrow[1];
-                tmem_wait_ld();
-                const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
-                const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
-                float e[16], ec[16], ep[16];
+                if (ok) {
+                    tc_fence_after();
+                    float kw[16];
+                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
+                    const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
+                    const uint4 v0 = vrow[0], v1 = vrow[1];
+                    tmem_wait_ld();
+                    const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
+                    const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
+                    float e[16], ec[16], ep[16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f0 = __bfloat1622float2(vb0[i]);
-                    const float2 f1 = __bfloat1622float2(vb1[i]);
-                    e[2 * i] = kw[2 * i] - f0.x;
-                    e[2 * i + 1] = kw[2 * i + 1] - f0.y;
-                    e[8 + 2 * i] = kw[8 + 2 * i] - f1.x;
-                    e[8 + 2 * i + 1] = kw[8 + 2 * i + 1] - f1.y;
-                }
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f0 = __bfloat1622float2(vb0[i]);
+                        const float2 f1 = __bfloat1622float2(vb1[i]);
+                        e[2 * i] = kw[2 * i] - f0.x;
+                        e[2 * i + 1] = kw[2 * i + 1] - f0.y;
+                        e[8 + 2 * i] = kw[8 + 2 * i] - f1.x;
+                        e[8 + 2 * i + 1] = kw[8 + 2 * i + 1] - f1.y;
+                    }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    ec[i] = ce * e[i];
-                    ep[i] = pe * e[i];
+                    for (int i = 0; i < 16; ++i) {
+                        ec[i] = ce * e[i];
+                        ep[i] = pe * e[i];
+                    }
+                    st_chunk(b2, t, 0, ec);
+                    st_chunk(b2, t, 8, ec + 8);
+                    st_chunk(b2, t, 16, ep);
+                    st_chunk(b2, t, 24, ep + 8);
+                    st_chunk(et(b), t, 0, e);
+                    st_chunk(et(b), t, 8, e + 8);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
                 }
-                st_chunk(b2, t, 0, ec);
-                st_chunk(b2, t, 8, ec + 8);
-                st_chunk(b2, t, 16, ep);
-                st_chunk(b2, t, 24, ep + 8);
-                st_chunk(et(b), t, 0, e);
-                st_chunk(et(b), t, 8, e + 8);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(&B->b2_ready);
+                named_bar_sync(2, 64);
+                // MMA2(c): K^T . [C E^T | Pm E^T]
+                if (warp == 0 && ok) {
+                    tc_fence_after();
+                    const uint32_t base = smem_u32(stage(st));
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 16; ++kk)
+                            mma_bf16(tmem + kAcc2,
+                                     sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
+                                     sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
+                        mma_commit(&B->mma2_done[b]);
+                        mma_commit(&B->empty[st]);
+                    }
+                    __syncwarp();
+                }
             }
             mbar_arrive(&B->empty[st]);
-            ok = wait_all(B, &B->mma2_done, c & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            if (own) {
-                float uw[16], us[16];
-                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2), uw);
-                tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2 + 16), us);
-                tmem_wait_ld();
+            // Epi2: state carry
+            if (ok) ok = wait_all(B, &B->mma2_done[b], (c >> 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                if (own) {
+                    float uw[16], us[16];
+                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2), uw);
+                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2 + 16), us);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < kRows; ++i) {
-                    const float wn = bn * w[i] + cn * s[i] - 2.f * uw[i];
-                    s[i] = Pn * s[i] - 2.f * us[i];
-                    w[i] = wn;
+                    for (int i = 0; i < kRows; ++i) {
+                        const float wn = bn * w[i] + cn * s[i] - 2.f * uw[i];
+                        s[i] = Pn * s[i] - 2.f * us[i];
+                        w[i] = wn;
+                    }
                 }
+                if (c + 1 < nch) {
+                    write_ws();
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
             }
-            write_ws();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&B->ws_ready);
+            named_bar_sync(1, 128);
+            if (c + 1 < nch) ok = issue_mma1(c + 1, ok);
         }
         if (own) {
             const size_t dst = (size_t)seq * D * D;
@@ -427,6 +498,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // --------------------------------------------------------- producer
         const uint32_t tx = L.kq_bytes + kChunk * kRows * 2;
         int issued = 0;
+        Gates g;
+        if (nch > 0) load_gates(a, (size_t)seq * T, min(kChunk, T), lane, g);
         for (int c = 0; c < nch; ++c) {
             const int st = c % L.NS;
             bool ok = true;
@@ -444,7 +517,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             issued = c + 1;
             const int n = min(kChunk, T - c * kChunk);
-            chunk_coefficients(a, (size_t)seq * T + (size_t)c * kChunk, n, coef(st), lane);
+            Gates gn = g;
+            if (c + 1 < nch)   // prefetch the next chunk's gates while this one is scanned
+                load_gates(a, (size_t)seq * T + (size_t)(c + 1) * kChunk,
+                           min(kChunk, T - (c + 1) * kChunk), lane, gn);
+            chunk_coefficients(g, n, coef(st), lane);
+            g = gn;
             __syncwarp();
             if (lane == 0) mbar_arrive(&B->full[st]);
         }
@@ -457,16 +535,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
         }
     } else if (warp == 5) {
-        // ------------------------------------------------------------- MMA
-        // The whole warp runs the schedule (waits are warp-uniform); one
-        // elected lane issues each group of MMAs from converged code.
+        // ------------------------------------------ read-side MMA issuer
+        // Issues the score MMA (one chunk ahead) and the correction MMA into
+        // the gaps the chain leaves: MMAz(c-1) right after MMA1(c) completes
+        // (it runs while the errors of chunk c are formed) and the scores of
+        // chunk c+1 right after MMA2(c) completes (they run during the carry).
         if (nch > 0) {
-            const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);
-            const uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);
             const uint32_t idqk = idesc_bf16_f32(128, 64, 0, 0);
             const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
-            const uint32_t ws_a = smem_u32(ws), b2_a = smem_u32(b2);
-            auto issue_qk = [&](int c) {
+            auto issue_qk = [&](int c) -> bool {
+                bool ok = wait_all(B, &B->full[c % L.NS], (c / L.NS) & 1, status);
+                if (ok && c >= 2) ok = wait_all(B, &B->qk_free[c & 1], ((c - 2) >> 1) & 1, status);
+                if (!ok) return false;
+                tc_fence_after();
                 const uint32_t base = smem_u32(stage(c % L.NS));
                 const uint32_t d = tmem + kAccQK + (c & 1) * 64;
                 if (elect_one()) {
@@ -478,10 +559,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     mma_commit(&B->qk_done[c & 1]);
                 }
                 __syncwarp();
+                return true;
             };
-            auto issue_z = [&](int c) {
+            auto issue_z = [&](int c) -> bool {
                 const int b = c & 1;
-                const uint32_t at_a = smem_u32(at(b)), et_a = smem_u32(et(b));
+                bool ok = wait_all(B, &B->at_ready[b], (c >> 1) & 1, status);
+                if (ok && c >= 2) ok = wait_all(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
+                if (!ok) return false;
+                tc_fence_after();
+                // 128-row A operand starting 8 KB before the 64 rows of A~
+                const uint32_t at_a = smem_u32(at(b)) - 8192, et_a = smem_u32(et(b));
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk)
@@ -490,67 +577,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     mma_commit(&B->z_done[b]);
                 }
                 __syncwarp();
-            };
-            // MMAz(c) needs the read side's A~(c); it is issued behind the next
-            // chain step so the issuer never stalls the chain on the read side.
-            auto try_z = [&](int c) -> bool {
-                const int b = c & 1;
-                bool ok = wait_all(B, &B->at_ready[b], (c >> 1) & 1, status);
-                if (ok && c >= 2) ok = wait_all(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
-                if (!ok) return false;
-                tc_fence_after();
-                issue_z(c);
                 return true;
             };
-            bool ok = wait_all(B, &B->full[0], 0, status);
-            if (ok) {
-                tc_fence_after();
-                issue_qk(0);
-            }
+            bool ok = issue_qk(0);
             for (int c = 0; c < nch && ok; ++c) {
-                const int st = c % L.NS, b = c & 1;
-                const uint32_t base = smem_u32(stage(st));
-                ok = wait_all(B, &B->ws_ready, c & 1, status);
-                if (ok && c >= 2) ok = wait_all(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                // MMA1: [K;Q] . [W;S]^T
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
-                                 sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
-                    }
-                    mma_commit(&B->mma1_done[b]);
-                }
-                __syncwarp();
-                if (c >= 1 && !(ok = try_z(c - 1))) break;
-                // MMA2: K^T . [C E^T | Pm E^T]
-                ok = wait_all(B, &B->b2_ready, c & 1, status);
-                if (!ok) break;
-                tc_fence_after();
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < kChunk / 16; ++kk)
-                        mma_bf16(tmem + kAcc2, sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
-                                 sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
-                    mma_commit(&B->mma2_done);
-                    mma_commit(&B->empty[st]);
-                }
-                __syncwarp();
-                // scores of the next chunk
-                if (c + 1 < nch) {
-                    ok = wait_all(B, &B->full[(c + 1) % L.NS], ((c + 1) / L.NS) & 1, status);
-                    if (ok && c + 1 >= 2)
-                        ok = wait_all(B, &B->qk_free[(c + 1) & 1], ((c - 1) >> 1) & 1, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(c + 1);
-                }
+                ok = wait_all(B, &B->mma1_done[c & 1], (c >> 1) & 1, status);
+                if (ok && c >= 1) ok = issue_z(c - 1);
+                if (ok) ok = wait_all(B, &B->mma2_done[c & 1], (c >> 1) & 1, status);
+                if (ok && c + 1 < nch) ok = issue_qk(c + 1);
             }
-            if (ok) try_z(nch - 1);
-            // drain: all issued MMAs complete before TMEM is released
+            if (ok) issue_z(nch - 1);
+            // drain: all issued MMAs complete before TMEM is released (the
+            // commit tracks every MMA this thread issued; the chain's own MMAs
+            // were waited for by the chain warps)
             if (elect_one()) mma_commit(&B->drain);
             __syncwarp();
             const long long t0 = clock64();
@@ -558,8 +597,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 if (clock64() - t0 > kWaitCycles) break;
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------- z warps 6-7
+    } else if (warp < 8) {
+        // ------------------------------------------------ read side (6-7)
         const int t = tid - 192;             // token, TMEM lane 64 + t
         const int wl = (warp & 3) * 32;      // 64 or 96
         bool ok = true;
@@ -567,34 +606,29 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int st = c % L.NS, b = c & 1;
             ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
             if (ok) ok = wait_all(B, &B->qk_done[b], (c >> 1) & 1, status);
+            if (ok) ok = wait_all(B, &B->c_ready[b], (c >> 1) & 1, status);
             if (!ok) break;
             tc_fence_after();
             const Coef* cf = coef(st);
-            // A~[t][s] = C[t][s] (q_t . k_s) for s <= t, by the backward recurrence
-            //   w(t,t) = 1, w(s,t) = bsuf + eta_{s+1} w(s+1,t), bsuf *= keep_{s+1}
-            float qk[64];
+            // A~[t][s] = C[t][s] (q_t . k_s) for s <= t
+            const float* crow = cmat(b) + t * kLdc;
+            uint8_t* arow = at(b);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float r[16];
                 tmem_ld16(tmem_addr(tmem, wl, kAccQK + b * 64 + 16 * q4), r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) qk[16 * q4 + i] = r[i];
+                for (int i = 0; i < 16; ++i) {
+                    const int sidx = 16 * q4 + i;
+                    r[i] = sidx <= t ? crow[sidx] * r[i] : 0.f;
+                }
+                st_chunk(arow, t, 16 * q4, r);
+                st_chunk(arow, t, 16 * q4 + 8, r + 8);
             }
             tc_fence_before();
             mbar_arrive(&B->qk_free[b]);
-            float bs = 1.f, wv = 1.f;
-#pragma unroll
-            for (int s = kChunk - 1; s >= 0; --s) {
-                if (s < t) {
-                    bs *= cf->keep[s + 1];
-                    wv = bs + cf->eta[s + 1] * wv;
-                }
-                qk[s] = (s <= t) ? cf->theta[s] * wv * qk[s] : 0.f;
-            }
-            uint8_t* arow = at(b);
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) st_chunk(arow, 64 + t, 8 * c8, qk + 8 * c8);
+            mbar_arrive(&B->c_free[b]);
             fence_proxy_async_smem();
             mbar_arrive(&B->at_ready[b]);
             // reads: z_t = beta_t Q W^T + c_t Q S^T - 2 A~ E^T
@@ -631,6 +665,34 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 reinterpret_cast<uint4*>(zr)[0] = o0;
                 reinterpret_cast<uint4*>(zr)[1] = o1;
             }
+        }
+    } else {
+        // --------------------------------------- coefficient warps (8-11)
+        // Pair p = (warp - 8) / 2 builds C[t][s] = theta_s w(s,t) for the chunks
+        // of parity p; thread s runs the forward recurrence of column s:
+        //   m(s,s) = w(s,s) = 1, m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t)
+        const int p = (warp - 8) >> 1;
+        const int sc = tid - 256 - 64 * p;   // column s
+        bool ok = true;
+        for (int c = p; c < nch && ok; c += 2) {
+            const int st = c % L.NS;
+            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
+            if (ok && c >= 2) ok = wait_all(B, &B->c_free[p], ((c - 2) >> 1) & 1, status);
+            if (!ok) break;
+            const Coef* cf = coef(st);
+            float* C = cmat(p);
+            const float th = cf->theta[sc];
+            float m = 1.f, wv = 1.f;
+#pragma unroll 8
+            for (int t = 0; t < kChunk; ++t) {
+                if (t > sc) {
+                    m = cf->eta[t] * m;
+                    wv = cf->keep[t] * wv + m;
+                }
+                C[t * kLdc + sc] = t >= sc ? th * wv : 0.f;
+            }
+            mbar_arrive(&B->empty[st]);
+            mbar_arrive(&B->c_ready[p]);
         }
     }
 
