@@ -56,32 +56,41 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map
 constexpr uint32_t kAcc1 = 0;     // 2 x 32 columns: [K W^T | K S^T] on lanes 0-63, [Q W^T | Q S^T] on 64-127
 constexpr uint32_t kAcc2 = 64;    // 32 columns: W / S updates (lane = d_k index)
-constexpr uint32_t kAccQK = 128;  // 2 x 64 columns: Q K^T on lanes 64-127
-constexpr uint32_t kAccZ = 256;   // 2 x 16 columns: A~ E^T on lanes 64-127
+constexpr uint32_t kAccQK = 128;  // 3 x 64 columns: Q K^T on lanes 64-127
+constexpr uint32_t kAccZ = 320;   // 2 x 16 columns: A~ E^T on lanes 64-127
 
-// Per-stage coefficient block (fp32, 64 tokens each)
-struct Coef {
+// Raw gates of one chunk as copied into a pipeline stage (fp32, 64 tokens).
+struct StageGates {
     float theta[kChunk];
-    float eta[kChunk];    // 1 past the chunk's last token
-    float keep[kChunk];   // 1 - alpha; 1 past the last token
-    float beta[kChunk];   // prod_{j<=t} keep_j
+    float eta[kChunk];
+    float alpha[kChunk];
+    float pad[kChunk];
+};
+static_assert(sizeof(StageGates) == 1024, "gate block");
+
+// Per-chunk coefficients, produced by a coefficient warp (two slots, by chunk
+// parity).  C[t][s] = theta_s w(s,t) is stored for s <= t only (the rest of a
+// row is never read).
+constexpr int kLdc = kChunk + 1;
+struct CoefSlot {
+    float C[kChunk * kLdc];
+    float beta[kChunk];   // prod_{j<=t} (1 - alpha_j)
     float cvec[kChunk];   // c_t
     float cend[kChunk];   // C[n-1][s]
-    float pend[kChunk];   // Pm[n-1][s]
+    float pend[kChunk];   // theta_s m(s, n-1)
     float scal[4];        // beta_{n-1}, c_{n-1}, P_{n-1}, n
 };
-static_assert(sizeof(Coef) <= 2048, "coefficient block");
 
 struct Layout {
     int D, NS;
-    uint32_t kq_bytes, stage_bytes;
-    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, off_c, total;
+    uint32_t kq_bytes, stage_bytes, off_v, off_g;
+    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, off_coef, total;
 };
 
 // Shared-memory map.  Each A~ tile (8 KB, the 64 rows of the scores) is
@@ -92,23 +101,27 @@ __host__ __device__ constexpr Layout make_layout(int D) {
     L.D = D;
     L.NS = D == 128 ? 3 : 4;
     L.kq_bytes = (D / 64) * 16384u;              // per 64-column half: K (8 KB) then Q (8 KB)
-    L.stage_bytes = L.kq_bytes + 2048u + 2048u;  // + V slice + coefficients
+    L.off_v = L.kq_bytes;                        // V slice, 64 x 16 bf16
+    L.off_g = L.kq_bytes + 2048u;                // raw gates
+    L.stage_bytes = L.kq_bytes + 2048u + 1024u;
     uint32_t off = L.NS * L.stage_bytes;
+    off = (off + 1023u) & ~1023u;
     L.off_ws = off;  off += D * 128u;            // [W;S] operand, row = d_k index
     L.off_b2 = off;  off += kChunk * 128u;       // [C E^T | Pm E^T], row = token
     L.off_at0 = off; off += kChunk * 128u;       // A~ (chunk parity 0)
     L.off_et0 = off; off += kChunk * 128u;       // E^T (chunk parity 0)
     L.off_at1 = off; off += kChunk * 128u;
     L.off_et1 = off; off += kChunk * 128u;
-    L.off_c = off;   off += 2u * kChunk * (kChunk + 1) * 4u;   // C[t][s], fp32, x2
+    L.off_coef = off; off += 2u * (uint32_t)sizeof(CoefSlot);
     L.total = off;
     return L;
 }
 
 struct Bars {
     uint64_t full[4], empty[4];
-    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], qk_done[2], qk_free[2], at_ready[2], z_done[2],
-        accz_free[2], c_ready[2], c_free[2];
+    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], at_ready[2], z_done[2], accz_free[2],
+        coef_ready[2], coef_free[2];
+    uint64_t qk_done[3], qk_free[3];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -176,119 +189,91 @@ __device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
     }
 }
 
-// Inclusive scan along decreasing lane index (suffix), later (lower) lanes outside.
-__device__ __forceinline__ void scan_affine_down(float& A, float& B, int lane) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float A2 = __shfl_down_sync(0xffffffffu, A, off);
-        const float B2 = __shfl_down_sync(0xffffffffu, B, off);
-        if (lane + off < 32) {
-            B = A * B2 + B;
-            A = A * A2;
-        }
-    }
-}
+// ------------------------------------------------------- coefficient warp
 
-// Gates of one chunk for the producer warp: lane l owns tokens 2l and 2l+1.
-// Past the chunk's last token theta is 0 and eta / keep are 1 (neutral).
-struct Gates {
-    float th[2], et[2], kp[2];
-};
-
-__device__ __forceinline__ void load_gates(const LinearArgs& a, size_t tok0, int n, int lane,
-                                           Gates& g) {
+// One warp computes all coefficients of one chunk of n tokens from its raw
+// gates g; it first makes the padded tokens neutral in place (eta 1,
+// alpha 0; theta is masked where read):
+//  * forward scans (lane l owns tokens 2l, 2l+1): beta_t = prod keep,
+//    P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
+//  * the matrix C[t][s] = theta_s w(s,t) with, per column s, the forward
+//    recurrences m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
+//    m(s,s) = w(s,s) = 1.  Lane l owns columns l and l + 32; all lanes walk
+//    the rows together.  A column holds m = w = 0 before its start row and the
+//    start enters as an additive unit, so a step is two dependent FMAs and the
+//    rows above the diagonal come out as exact zeros.  With neutral gates
+//    past the last token, m stops changing there, so the final m is
+//    m(s, n-1) (pend); cend is read back from row n-1.
+__device__ void coefficient_warp(StageGates* __restrict__ g, int n, CoefSlot* __restrict__ cs,
+                                 int lane) {
+    const int s0 = lane, s1 = lane + 32;
+    if (s0 >= n) { g->eta[s0] = 1.f; g->alpha[s0] = 0.f; }
+    if (s1 >= n) { g->eta[s1] = 1.f; g->alpha[s1] = 0.f; }
+    __syncwarp();
+    float et[2], kp[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int t = 2 * lane + u;
-        const bool ok = t < n;
-        g.th[u] = ok ? __ldg(a.theta + tok0 + t) : 0.f;
-        g.et[u] = ok ? (a.eta ? __ldg(a.eta + tok0 + t) : 0.f) : 1.f;
-        g.kp[u] = ok ? 1.f - (a.alpha ? __ldg(a.alpha + tok0 + t) : 0.f) : 1.f;
+        et[u] = g->eta[t];
+        kp[u] = 1.f - g->alpha[t];
     }
-}
-
-// Producer-side chunk coefficients from the gates (warp scans).
-__device__ void chunk_coefficients(const Gates& g, int n, Coef* cf, int lane) {
-    const float* th = g.th;
-    const float* et = g.et;
-    const float* kp = g.kp;
-    // forward: beta_t = prod keep, P_t = prod eta, c_t = keep_t c_{t-1} + P_t.
-    // beta and P are scans of maps x -> keep x (resp. eta x); c is the affine
-    // recurrence whose maps x -> keep_t x + P_t need P first.
     float Ab = kp[0] * kp[1], Bb = 0.f;
-    scan_affine_up(Ab, Bb, lane);
     float Ap = et[0] * et[1], Bp = 0.f;
+    scan_affine_up(Ab, Bb, lane);
     scan_affine_up(Ap, Bp, lane);
     float pre_b = __shfl_up_sync(0xffffffffu, Ab, 1);
     float pre_p = __shfl_up_sync(0xffffffffu, Ap, 1);
     if (lane == 0) pre_b = pre_p = 1.f;
     const float beta0 = pre_b * kp[0], beta1 = beta0 * kp[1];
     const float P0 = pre_p * et[0], P1 = P0 * et[1];
-    // c: lane-local composition of (kp0, P0) then (kp1, P1)
     float Ac = kp[1] * kp[0], Bc = kp[1] * P0 + P1;
     scan_affine_up(Ac, Bc, lane);
-    float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);   // c just before this lane's tokens
+    float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);
     if (lane == 0) cpre = 0.f;
     const float c0 = kp[0] * cpre + P0, c1 = kp[1] * c0 + P1;
-
-    // backward from the last token n-1:
-    //   m_s    = prod_{j=s+1}^{n-1} eta_j      (suffix products; neutral past n-1)
-    //   bsuf_s = prod_{j=s+1}^{n-1} keep_j
-    //   w_s    = bsuf_s + eta_{s+1} w_{s+1},  w_{n-1} = 1
-    // eta / keep past n-1 are 1 and theta 0, so suffix products start at n-1.
-    // The eta_{s+1} / keep_{s+1} of a lane's second token come from the next lane.
-    const float et_next = __shfl_down_sync(0xffffffffu, et[0], 1);   // eta_{2l+2}
-    const float kp_next = __shfl_down_sync(0xffffffffu, kp[0], 1);
-    const float e_n1 = lane == 31 ? 1.f : et_next;
-    const float k_n1 = lane == 31 ? 1.f : kp_next;
-    // exclusive suffix products over tokens > t (lane-level then within the pair)
-    float Am = et[0] * et[1], Bm = 0.f;
-    scan_affine_down(Am, Bm, lane);
-    float Ak = kp[0] * kp[1], Bk = 0.f;
-    scan_affine_down(Ak, Bk, lane);
-    float suf_m = __shfl_down_sync(0xffffffffu, Am, 1);
-    float suf_k = __shfl_down_sync(0xffffffffu, Ak, 1);
-    if (lane == 31) suf_m = suf_k = 1.f;
-    const float m1 = suf_m, m0 = et[1] * suf_m;          // tokens 2l+1, 2l
-    const float bs1 = suf_k, bs0 = kp[1] * suf_k;
-    // w recurrence as maps applied from the end: w_s = F_s(w_{s+1}),
-    // F_s(x) = eta_{s+1} x + bsuf_s, except F_{n-1}(x) = 1 (absorbing).
     const int t0 = 2 * lane, t1 = t0 + 1;
-    float A1 = e_n1, B1 = bs1;               // token t1, its successor is 2l+2
-    if (t1 == n - 1) { A1 = 0.f; B1 = 1.f; }
-    float A0 = et[1], B0 = bs0;              // token t0, its successor is t1
-    if (t0 == n - 1) { A0 = 0.f; B0 = 1.f; }
-    // lane composition: w_{t0} = F0(F1(x))
-    float Aw = A0 * A1, Bw = A0 * B1 + B0;
-    scan_affine_down(Aw, Bw, lane);
-    float wnext = __shfl_down_sync(0xffffffffu, Bw, 1);   // w at token 2l+2 (any input: absorbed)
-    if (lane == 31) wnext = 1.f;
-    const float w1 = A1 * wnext + B1, w0 = A0 * w1 + B0;
-    (void)k_n1;
-
-    cf->theta[t0] = th[0];  cf->theta[t1] = th[1];
-    cf->eta[t0] = et[0];    cf->eta[t1] = et[1];
-    cf->keep[t0] = kp[0];   cf->keep[t1] = kp[1];
-    cf->beta[t0] = beta0;   cf->beta[t1] = beta1;
-    cf->cvec[t0] = c0;      cf->cvec[t1] = c1;
-    cf->cend[t0] = th[0] * w0;  cf->cend[t1] = th[1] * w1;
-    cf->pend[t0] = th[0] * m0;  cf->pend[t1] = th[1] * m1;
-    // scalars at the chunk's last token
+    cs->beta[t0] = beta0;  cs->beta[t1] = beta1;
+    cs->cvec[t0] = c0;     cs->cvec[t1] = c1;
     const int ln = (n - 1) >> 1, un = (n - 1) & 1;
     const float bn = __shfl_sync(0xffffffffu, un ? beta1 : beta0, ln);
     const float cn = __shfl_sync(0xffffffffu, un ? c1 : c0, ln);
     const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
     if (lane == 0) {
-        cf->scal[0] = bn;
-        cf->scal[1] = cn;
-        cf->scal[2] = Pn;
-        cf->scal[3] = (float)n;
+        cs->scal[0] = bn;
+        cs->scal[1] = cn;
+        cs->scal[2] = Pn;
+        cs->scal[3] = (float)n;
     }
+    const float th0 = s0 < n ? g->theta[s0] : 0.f, th1 = s1 < n ? g->theta[s1] : 0.f;
+    const float e_lo = g->eta[s0], e_hi = g->eta[s1];
+    const float k_lo = 1.f - g->alpha[s0], k_hi = 1.f - g->alpha[s1];
+    float m0 = 0.f, w0 = 0.f, m1 = 0.f, w1 = 0.f;
+    float* __restrict__ C = cs->C;
+#pragma unroll
+    for (int t = 0; t < kChunk; ++t) {
+        const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
+        const float k1 = __shfl_sync(0xffffffffu, t < 32 ? k_lo : k_hi, t & 31);
+        const float d = (lane == (t & 31)) ? 1.f : 0.f;   // start of column t
+        if (t < 32) {
+            m0 = fmaf(e, m0, d);
+            m1 = e * m1;
+        } else {
+            m0 = e * m0;
+            m1 = fmaf(e, m1, d);
+        }
+        w0 = fmaf(k1, w0, m0);
+        w1 = fmaf(k1, w1, m1);
+        C[t * kLdc + s0] = th0 * w0;
+        C[t * kLdc + s1] = th1 * w1;
+    }
+    __syncwarp();
+    cs->pend[s0] = th0 * m0;
+    cs->pend[s1] = th1 * m1;
+    cs->cend[s0] = C[(n - 1) * kLdc + s0];
+    cs->cend[s1] = C[(n - 1) * kLdc + s1];
 }
 
 // ------------------------------------------------------------------- kernel
-
-constexpr int kLdc = kChunk + 1;   // padded row length of the fp32 C matrix
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -311,31 +296,33 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     int* status = a.status;
 
     auto stage = [&](int s) { return sm + s * L.stage_bytes; };
-    auto vtile = [&](int s) { return stage(s) + L.kq_bytes; };
-    auto coef = [&](int s) { return reinterpret_cast<Coef*>(stage(s) + L.kq_bytes + 2048); };
+    auto vtile = [&](int s) { return stage(s) + L.off_v; };
+    auto gates = [&](int s) { return reinterpret_cast<StageGates*>(stage(s) + L.off_g); };
     uint8_t* ws = sm + L.off_ws;
     uint8_t* b2 = sm + L.off_b2;
     auto et = [&](int b) { return sm + (b ? L.off_et1 : L.off_et0); };
     auto at = [&](int b) { return sm + (b ? L.off_at1 : L.off_at0); };
-    auto cmat = [&](int b) { return reinterpret_cast<float*>(sm + L.off_c) + b * kChunk * kLdc; };
+    auto coef = [&](int p) { return reinterpret_cast<CoefSlot*>(sm + L.off_coef) + p; };
 
     if (tid == 0) {
         for (int s = 0; s < L.NS; ++s) {
-            mbar_init(&B->full[s], 2);
-            // chain 128 + read side 64 + coefficient pair 64 + MMA commit 1
-            mbar_init(&B->empty[s], 128 + 64 + 64 + 1);
+            mbar_init(&B->full[s], 1 + 32);   // expect_tx + every producer lane
+            // Epi1 threads 64 + coefficient warp 1 + chain MMA commit 1 + score MMA commit 1
+            mbar_init(&B->empty[s], 64 + 1 + 1 + 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->mma1_done[b], 1);
+            mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->acc1_free[b], 64);
-            mbar_init(&B->qk_done[b], 1);
-            mbar_init(&B->qk_free[b], 64);
             mbar_init(&B->at_ready[b], 64);
             mbar_init(&B->z_done[b], 1);
             mbar_init(&B->accz_free[b], 64);
-            mbar_init(&B->c_ready[b], 64);
-            mbar_init(&B->c_free[b], 64);
+            mbar_init(&B->coef_ready[b], 32);
+            mbar_init(&B->coef_free[b], 128 + 64);
+        }
+        for (int b = 0; b < 3; ++b) {
+            mbar_init(&B->qk_done[b], 1);
+            mbar_init(&B->qk_free[b], 64);
         }
         mbar_init(&B->drain, 1);
         B->abort = 0;
@@ -400,23 +387,24 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         named_bar_sync(1, 128);
         bool ok = issue_mma1(0, true);
         for (int c = 0; c < nch; ++c) {
-            const int st = c % L.NS, b = c & 1;
-            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            const Coef* cf = coef(st);
-            const float bn = cf->scal[0], cn = cf->scal[1], Pn = cf->scal[2];
+            const int st = c % L.NS, b = c & 1, p = c & 1;
+            const CoefSlot* cs = coef(p);
+            if (ok) ok = wait_all(B, &B->coef_ready[p], (c >> 1) & 1, status);
             if (warp < 2) {
                 // Epi1: errors of token t at the chunk-start state
                 const int t = j;
-                const float ce = cf->cend[t], pe = cf->pend[t];
+                if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
                 if (ok) ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
                 if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
                 if (ok) {
+                    const float ce = cs->cend[t], pe = cs->pend[t];
                     tc_fence_after();
                     float kw[16];
                     tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
                     const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
                     const uint4 v0 = vrow[0], v1 = vrow[1];
                     tmem_wait_ld();
+                    mbar_arrive(&B->empty[st]);
                     const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
                     const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
                     float e[16], ec[16], ep[16];
@@ -460,10 +448,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     __syncwarp();
                 }
             }
-            mbar_arrive(&B->empty[st]);
             // Epi2: state carry
             if (ok) ok = wait_all(B, &B->mma2_done[b], (c >> 1) & 1, status);
             if (ok) {
+                const float bn = cs->scal[0], cn = cs->scal[1], Pn = cs->scal[2];
+                mbar_arrive(&B->coef_free[p]);
                 tc_fence_after();
                 if (own) {
                     float uw[16], us[16];
@@ -496,16 +485,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     } else if (warp == 4) {
         // --------------------------------------------------------- producer
-        const uint32_t tx = L.kq_bytes + kChunk * kRows * 2;
+        // K, Q (two 64-column halves each) and the V slice by TMA; the raw
+        // gates by bulk copies when the sequence length keeps them 16-byte
+        // aligned, else by plain loads.
+        const bool bulk_gates = (T % 4) == 0;
         int issued = 0;
-        Gates g;
-        if (nch > 0) load_gates(a, (size_t)seq * T, min(kChunk, T), lane, g);
         for (int c = 0; c < nch; ++c) {
             const int st = c % L.NS;
+            const int n = min(kChunk, T - c * kChunk);
+            const size_t tok0 = (size_t)seq * T + (size_t)c * kChunk;
             bool ok = true;
             if (c >= L.NS && lane == 0) ok = wait_bar(B, &B->empty[st], ((c / L.NS) - 1) & 1, status);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            StageGates* g = gates(st);
             if (lane == 0) {
+                uint32_t tx = L.kq_bytes + kChunk * kRows * 2;
+                const uint32_t gb = (uint32_t)n * 4u;
+                if (bulk_gates) tx += gb * (1 + (a.eta != nullptr) + (a.alpha != nullptr));
                 mbar_expect_tx(&B->full[st], tx);
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
@@ -514,17 +510,25 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                                 c * kChunk, seq);
                 }
                 tma_load_3d(vtile(st), &vmap, &B->full[st], r0, c * kChunk, seq);
+                if (bulk_gates) {
+                    bulk_load(g->theta, a.theta + tok0, gb, &B->full[st]);
+                    if (a.eta) bulk_load(g->eta, a.eta + tok0, gb, &B->full[st]);
+                    if (a.alpha) bulk_load(g->alpha, a.alpha + tok0, gb, &B->full[st]);
+                }
             }
+            if (!bulk_gates) {
+                for (int t = lane; t < n; t += 32) {
+                    g->theta[t] = a.theta[tok0 + t];
+                    if (a.eta) g->eta[t] = a.eta[tok0 + t];
+                    if (a.alpha) g->alpha[t] = a.alpha[tok0 + t];
+                }
+            }
+            if (!a.eta)
+                for (int t = lane; t < kChunk; t += 32) g->eta[t] = 0.f;
+            if (!a.alpha)
+                for (int t = lane; t < kChunk; t += 32) g->alpha[t] = 0.f;
             issued = c + 1;
-            const int n = min(kChunk, T - c * kChunk);
-            Gates gn = g;
-            if (c + 1 < nch)   // prefetch the next chunk's gates while this one is scanned
-                load_gates(a, (size_t)seq * T + (size_t)(c + 1) * kChunk,
-                           min(kChunk, T - (c + 1) * kChunk), lane, gn);
-            chunk_coefficients(g, n, coef(st), lane);
-            g = gn;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B->full[st]);
+            mbar_arrive(&B->full[st]);
         }
         // drain: every issued stage's copies must have landed before exit
         if (lane == 0) {
@@ -536,27 +540,28 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     } else if (warp == 5) {
         // ------------------------------------------ read-side MMA issuer
-        // Issues the score MMA (one chunk ahead) and the correction MMA into
-        // the gaps the chain leaves: MMAz(c-1) right after MMA1(c) completes
-        // (it runs while the errors of chunk c are formed) and the scores of
-        // chunk c+1 right after MMA2(c) completes (they run during the carry).
+        // The correction MMA of chunk c-1 goes right after MMA1(c) completes
+        // (it runs while the errors of chunk c are formed); the scores run two
+        // chunks ahead, issued after MMA2(c) completes (during the carry).
         if (nch > 0) {
             const uint32_t idqk = idesc_bf16_f32(128, 64, 0, 0);
             const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
             auto issue_qk = [&](int c) -> bool {
-                bool ok = wait_all(B, &B->full[c % L.NS], (c / L.NS) & 1, status);
-                if (ok && c >= 2) ok = wait_all(B, &B->qk_free[c & 1], ((c - 2) >> 1) & 1, status);
+                const int q = c % 3, st = c % L.NS;
+                bool ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
+                if (ok && c >= 3) ok = wait_all(B, &B->qk_free[q], ((c - 3) / 3) & 1, status);
                 if (!ok) return false;
                 tc_fence_after();
-                const uint32_t base = smem_u32(stage(c % L.NS));
-                const uint32_t d = tmem + kAccQK + (c & 1) * 64;
+                const uint32_t base = smem_u32(stage(st));
+                const uint32_t d = tmem + kAccQK + q * 64;
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
                         mma_bf16(d, sdesc(half, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk, kk > 0);
                     }
-                    mma_commit(&B->qk_done[c & 1]);
+                    mma_commit(&B->qk_done[q]);
+                    mma_commit(&B->empty[st]);
                 }
                 __syncwarp();
                 return true;
@@ -580,16 +585,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 return true;
             };
             bool ok = issue_qk(0);
+            if (ok && nch > 1) ok = issue_qk(1);
             for (int c = 0; c < nch && ok; ++c) {
                 ok = wait_all(B, &B->mma1_done[c & 1], (c >> 1) & 1, status);
                 if (ok && c >= 1) ok = issue_z(c - 1);
                 if (ok) ok = wait_all(B, &B->mma2_done[c & 1], (c >> 1) & 1, status);
-                if (ok && c + 1 < nch) ok = issue_qk(c + 1);
+                if (ok && c + 2 < nch) ok = issue_qk(c + 2);
             }
             if (ok) issue_z(nch - 1);
-            // drain: all issued MMAs complete before TMEM is released (the
-            // commit tracks every MMA this thread issued; the chain's own MMAs
-            // were waited for by the chain warps)
+            // drain: all MMAs issued by this thread complete before TMEM is
+            // released (the chain's own MMAs were waited for by the chain)
             if (elect_one()) mma_commit(&B->drain);
             __syncwarp();
             const long long t0 = clock64();
@@ -603,20 +608,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int wl = (warp & 3) * 32;      // 64 or 96
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const int st = c % L.NS, b = c & 1;
-            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (ok) ok = wait_all(B, &B->qk_done[b], (c >> 1) & 1, status);
-            if (ok) ok = wait_all(B, &B->c_ready[b], (c >> 1) & 1, status);
+            const int b = c & 1, p = c & 1, q = c % 3;
+            ok = wait_all(B, &B->coef_ready[p], (c >> 1) & 1, status);
+            if (ok) ok = wait_all(B, &B->qk_done[q], (c / 3) & 1, status);
             if (!ok) break;
             tc_fence_after();
-            const Coef* cf = coef(st);
+            const CoefSlot* cs = coef(p);
             // A~[t][s] = C[t][s] (q_t . k_s) for s <= t
-            const float* crow = cmat(b) + t * kLdc;
+            const float* crow = cs->C + t * kLdc;
             uint8_t* arow = at(b);
+            if (c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
+            if (!ok) break;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float r[16];
-                tmem_ld16(tmem_addr(tmem, wl, kAccQK + b * 64 + 16 * q4), r);
+                tmem_ld16(tmem_addr(tmem, wl, kAccQK + q * 64 + 16 * q4), r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -627,8 +633,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 st_chunk(arow, t, 16 * q4 + 8, r + 8);
             }
             tc_fence_before();
-            mbar_arrive(&B->qk_free[b]);
-            mbar_arrive(&B->c_free[b]);
+            mbar_arrive(&B->qk_free[q]);
             fence_proxy_async_smem();
             mbar_arrive(&B->at_ready[b]);
             // reads: z_t = beta_t Q W^T + c_t Q S^T - 2 A~ E^T
@@ -648,9 +653,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&B->accz_free[b]);
-            const float bt = cf->beta[t], ct = cf->cvec[t];
-            const int n = (int)cf->scal[3];
-            mbar_arrive(&B->empty[st]);
+            const float bt = cs->beta[t], ct = cs->cvec[t];
+            const int n = (int)cs->scal[3];
+            mbar_arrive(&B->coef_free[p]);
             if (t < n) {
                 float zz[16];
 #pragma unroll
@@ -667,32 +672,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
         }
     } else {
-        // --------------------------------------- coefficient warps (8-11)
-        // Pair p = (warp - 8) / 2 builds C[t][s] = theta_s w(s,t) for the chunks
-        // of parity p; thread s runs the forward recurrence of column s:
-        //   m(s,s) = w(s,s) = 1, m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t)
-        const int p = (warp - 8) >> 1;
-        const int sc = tid - 256 - 64 * p;   // column s
+        // ------------------------------------------ coefficient warps (8-9)
+        // Warp 8 + p handles the chunks of parity p into slot p.
+        const int p = warp - 8;
         bool ok = true;
         for (int c = p; c < nch && ok; c += 2) {
             const int st = c % L.NS;
             ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (ok && c >= 2) ok = wait_all(B, &B->c_free[p], ((c - 2) >> 1) & 1, status);
+            if (ok && c >= 2) ok = wait_all(B, &B->coef_free[p], ((c - 2) >> 1) & 1, status);
             if (!ok) break;
-            const Coef* cf = coef(st);
-            float* C = cmat(p);
-            const float th = cf->theta[sc];
-            float m = 1.f, wv = 1.f;
-#pragma unroll 8
-            for (int t = 0; t < kChunk; ++t) {
-                if (t > sc) {
-                    m = cf->eta[t] * m;
-                    wv = cf->keep[t] * wv + m;
-                }
-                C[t * kLdc + sc] = t >= sc ? th * wv : 0.f;
-            }
-            mbar_arrive(&B->empty[st]);
-            mbar_arrive(&B->c_ready[p]);
+            coefficient_warp(gates(st), min(kChunk, T - c * kChunk), coef(p), lane);
+            mbar_arrive(&B->coef_ready[p]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->empty[st]);
         }
     }
 
