@@ -199,12 +199,12 @@ def call_fn(w: wl.Workload, d: dict, outs: dict, stream):
     if w.kind == "linear":
         return lambda: ttm.linear_fwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], w.chunk,
                                       w0_shared=w.w0_shared, z=outs["z"], W_out=outs["W"],
-                                      stream=stream)
+                                      workspace=outs["ws"], stream=stream)
     if w.kind == "titans":
         return lambda: ttm.titans_fwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], w.chunk,
                                       eta=d["eta"], alpha=d["alpha"], w0_shared=w.w0_shared,
                                       z=outs["z"], W_out=outs["W"], S_out=outs["S"],
-                                      stream=stream)
+                                      workspace=outs["ws"], stream=stream)
     return lambda: ttm.mlp_fwd(d["q"], d["k"], d["v"], d["theta"], d["W1_0"], d["W2_0"],
                                w.chunk, eta=d["eta"], alpha=d["alpha"], w0_shared=w.w0_shared,
                                z=outs["z"], W1_out=outs["W1"], W2_out=outs["W2"],
@@ -220,8 +220,14 @@ def alloc_outputs(w: wl.Workload, dev, pin=False) -> dict:
         o.update(W1=mk((w.B, w.H, w.hidden, w.d)), W2=mk((w.B, w.H, w.d, w.hidden)),
                  S1=mk((w.B, w.H, w.hidden, w.d)), S2=mk((w.B, w.H, w.d, w.hidden)))
     else:
+        import test_neural_memory_gb300 as ttm
         o["W"] = mk((w.B, w.H, w.d, w.d))
         o["S"] = mk((w.B, w.H, w.d, w.d)) if w.kind == "titans" else None
+        # scratch for the per-chunk coefficients (device only; not an output)
+        nbytes = ttm.linear_workspace_size(w.B, w.H, w.T, w.d, w.d, w.chunk,
+                                           ttm.BF16 if w.dtype == "bf16" else ttm.F32)
+        o["ws"] = (torch.empty(nbytes, dtype=torch.uint8, device=dev if not pin else "cuda")
+                   if nbytes else None)
     return o
 
 
@@ -332,8 +338,8 @@ def run_e2e(args, w, inp, dev, stream, world):
     host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
     dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
     outs = alloc_outputs(w, dev)
-    hout = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, pin_memory=True))
-            for k, v in outs.items()}
+    hout = {k: (None if v is None or k == "ws" else
+                torch.empty(v.shape, dtype=v.dtype, pin_memory=True)) for k, v in outs.items()}
     step = call_fn(w, dbuf, outs, stream)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(v.numel() * v.element_size() for v in hout.values() if v is not None)
@@ -344,7 +350,7 @@ def run_e2e(args, w, inp, dev, stream, world):
                 dbuf[k].copy_(v, non_blocking=True)
         step()
         for k, v in outs.items():
-            if v is not None:
+            if hout.get(k) is not None:
                 hout[k].copy_(v, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):

@@ -39,6 +39,13 @@
  *     w0_shared_over_batch == 0.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  The call is
  *     asynchronous: it validates on the host, enqueues kernels and returns.
+ *   - Workspace: the tensor-core path of the linear / Titans scan first
+ *     computes every chunk's coefficients (they depend only on the gates) into
+ *     device scratch that the caller provides: `workspace` (16-byte aligned,
+ *     not overlapping any other argument) of at least
+ *     ttm_linear_workspace_size(...) bytes.  Its contents on entry are
+ *     ignored and on return are unspecified.  Kernels that need none accept
+ *     NULL / 0.
  *
  * Errors
  *   Argument validation happens on the host before anything is enqueued; a
@@ -50,6 +57,8 @@
  */
 #ifndef TTM_H
 #define TTM_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -95,7 +104,8 @@ int ttm_linear_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                    const void* q, const void* k, const void* v,
                    const float* eta, const float* theta, const float* alpha,
                    const float* W0, int w0_shared_over_batch,
-                   void* z, float* W_out, void* stream);
+                   void* z, float* W_out, void* workspace, size_t workspace_bytes,
+                   void* stream);
 
 /*
  * Titans neural memory with linear memory: momentum ("past surprise") and
@@ -109,7 +119,18 @@ int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                    const void* q, const void* k, const void* v,
                    const float* eta, const float* theta, const float* alpha,
                    const float* W0, const float* S0, int w0_shared_over_batch,
-                   void* z, float* W_out, float* S_out, void* stream);
+                   void* z, float* W_out, float* S_out, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace ttm_linear_fwd / ttm_titans_fwd need for these sizes
+ * under the current kernel policy: 0 when the selected kernel needs none (or
+ * the shape is rejected), else B*H*ceil(T/64) * 17424 for the tensor-core
+ * path.  The chunk coefficients are the matrix C of the chunk's matrix form
+ * ("TTT layers 与 fast weights" §1.1 eq (9) with the decay and momentum
+ * unrolling of "论文速览 | Titans" §4.3-§4.5).
+ */
+size_t ttm_linear_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
 
 /*
  * Deep memory: f(x) = W2 GELU(W1 x), hidden units `hidden`, analytic inner

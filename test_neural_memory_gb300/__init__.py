@@ -41,8 +41,11 @@ def lib() -> ctypes.CDLL:
                                "`python -m test_neural_memory_gb300._build`")
         L = ctypes.CDLL(LIB)
         i, p = ctypes.c_int, ctypes.c_void_p
-        L.ttm_linear_fwd.argtypes = [i] * 7 + [p] * 6 + [p, i, p, p, p]
-        L.ttm_titans_fwd.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p]
+        sz = ctypes.c_size_t
+        L.ttm_linear_fwd.argtypes = [i] * 7 + [p] * 6 + [p, i, p, p, p, sz, p]
+        L.ttm_titans_fwd.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p, sz, p]
+        L.ttm_linear_workspace_size.argtypes = [i] * 7
+        L.ttm_linear_workspace_size.restype = sz
         L.ttm_mlp_fwd.argtypes = [i] * 7 + [p] * 6 + [p] * 4 + [i] + [p] * 5 + [p]
         for f in (L.ttm_linear_fwd, L.ttm_titans_fwd, L.ttm_mlp_fwd):
             f.restype = i
@@ -120,7 +123,27 @@ def _check(code: int, what: str):
         raise TTMError(code, what)
 
 
-def linear_fwd(q, k, v, theta, W0, chunk, *, w0_shared=False, z=None, W_out=None, stream=None):
+def linear_workspace_size(B, H, T, dk, dv, chunk, dtype_code) -> int:
+    """Workspace bytes the linear / Titans scan needs under the current policy."""
+    return int(lib().ttm_linear_workspace_size(B, H, T, dk, dv, int(chunk), dtype_code))
+
+
+def alloc_workspace(q, v, chunk):
+    """A device workspace (uint8 tensor) sized for this call, or None."""
+    import torch
+    B, H, T, dk = q.shape
+    n = linear_workspace_size(B, H, T, dk, v.shape[-1], chunk, _dtype_code(q))
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def linear_fwd(q, k, v, theta, W0, chunk, *, w0_shared=False, z=None, W_out=None,
+               workspace=None, stream=None):
     """TTT-Linear scan.  q, k: [B,H,T,dk]; v: [B,H,T,dv]; theta: [B,H,T] fp32;
     W0: [B|1,H,dv,dk] fp32.  Returns (z, W_out)."""
     import torch
@@ -128,14 +151,18 @@ def linear_fwd(q, k, v, theta, W0, chunk, *, w0_shared=False, z=None, W_out=None
     dv = v.shape[-1]
     z = torch.empty_like(v) if z is None else z
     W_out = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if W_out is None else W_out
+    if workspace is None:
+        workspace = alloc_workspace(q, v, chunk)
+    wp, wb = _ws(workspace)
     _check(lib().ttm_linear_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
                                 _ptr(v), None, _ptr(theta), None, _ptr(W0), int(bool(w0_shared)),
-                                _ptr(z), _ptr(W_out), _stream(q, stream)), "ttm_linear_fwd")
+                                _ptr(z), _ptr(W_out), wp, wb, _stream(q, stream)),
+           "ttm_linear_fwd")
     return z, W_out
 
 
 def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_shared=False,
-               z=None, W_out=None, S_out=None, want_S=True, stream=None):
+               z=None, W_out=None, S_out=None, want_S=True, workspace=None, stream=None):
     """Titans linear-memory scan with momentum (eta) and forgetting (alpha).
     Returns (z, W_out, S_out); S_out is None when want_S is False."""
     import torch
@@ -146,9 +173,12 @@ def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_s
     W_out = torch.empty(shape, dtype=torch.float32, device=q.device) if W_out is None else W_out
     if S_out is None and want_S:
         S_out = torch.empty(shape, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(q, v, chunk)
+    wp, wb = _ws(workspace)
     _check(lib().ttm_titans_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
                                 _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W0), _ptr(S0),
-                                int(bool(w0_shared)), _ptr(z), _ptr(W_out), _ptr(S_out),
+                                int(bool(w0_shared)), _ptr(z), _ptr(W_out), _ptr(S_out), wp, wb,
                                 _stream(q, stream)), "ttm_titans_fwd")
     return z, W_out, S_out
 

@@ -18,6 +18,8 @@ struct LinearArgs {
     int shared;                         // W0/S0 have a leading dim of 1
     void* z;
     float *W_out, *S_out;               // S_out may be NULL
+    void* workspace;                    // caller-provided device scratch (may be NULL)
+    size_t workspace_bytes;
     int* status;                        // device status word (bounded waits)
 };
 
@@ -40,8 +42,11 @@ cudaError_t linear_simt_launch(const LinearArgs& a, cudaStream_t s);
 bool mlp_simt_supported(const MlpArgs& a);
 cudaError_t mlp_simt_launch(const MlpArgs& a, cudaStream_t s);
 
-// tcgen05 + TMA kernel for the linear / Titans scan (scan_linear_tc.cu).
+// tcgen05 + TMA kernel for the linear / Titans scan (scan_linear_tc.cu).  It
+// needs linear_tc_workspace_bytes() of workspace for the per-chunk
+// coefficients computed by its pre-pass.
 bool linear_tc_supported(const LinearArgs& a);
+size_t linear_tc_workspace_bytes(const LinearArgs& a);
 cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s);
 
 }  // namespace ttm

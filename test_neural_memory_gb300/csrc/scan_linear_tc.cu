@@ -16,14 +16,22 @@
 // involves that row), so one CTA owns a slice of 16 rows of one sequence's
 // memory and runs the whole sequence; the grid covers (sequence, slice).
 //
-// Roles inside a CTA (256 threads):
-//   warps 0-3  chain epilogues.  Thread j holds W[r0..r0+15][j] and
-//              S[r0..r0+15][j] in fp32 registers for the whole sequence.
-//              Warps 0-1 (thread = token) turn K W^T into the errors and the
-//              scaled error operands; all four apply the state carry.
-//   warp 4     producer: TMA loads of K, Q (128-byte swizzle) and the V slice;
-//              gates by plain loads; the chunk coefficients by warp scans.
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+// The per-chunk coefficients depend only on the gates, so a pre-pass kernel
+// (one warp per sequence and chunk) writes them into the caller's workspace:
+// the 64 x 64 matrix C (fp32) and the vectors beta_t, c_t, C[n-1][s],
+// Pm[n-1][s] and the chunk-end scalars.  The scan kernel copies each chunk's
+// record into its pipeline stage next to the K, Q and V tiles.
+//
+// Roles inside a CTA of the scan kernel (256 threads):
+//   warps 0-3  chain.  Thread j holds W[r0..r0+15][j] and S[r0..r0+15][j] in
+//              fp32 registers for the whole sequence.  Warps 0-1 (thread =
+//              token) turn K W^T into the errors and the scaled error
+//              operands; all four apply the state carry; warp 0 issues the
+//              two chain MMAs itself after named barriers.
+//   warp 4     producer: TMA loads of K, Q (128-byte swizzle) and the V
+//              slice, bulk copy of the coefficient record.
+//   warp 5     read-side MMA issuer (scores two chunks ahead, corrections)
+//              and TMEM owner.
 //   warps 6-7  reads: masked, coefficient-weighted scores and the output z.
 //
 // Tensor-core contractions per chunk (A operands are M = 128 rows: the K tile
@@ -56,7 +64,7 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map
@@ -65,32 +73,26 @@ constexpr uint32_t kAcc2 = 64;    // 32 columns: W / S updates (lane = d_k index
 constexpr uint32_t kAccQK = 128;  // 3 x 64 columns: Q K^T on lanes 64-127
 constexpr uint32_t kAccZ = 320;   // 2 x 16 columns: A~ E^T on lanes 64-127
 
-// Raw gates of one chunk as copied into a pipeline stage (fp32, 64 tokens).
-struct StageGates {
-    float theta[kChunk];
-    float eta[kChunk];
-    float alpha[kChunk];
-    float pad[kChunk];
-};
-static_assert(sizeof(StageGates) == 1024, "gate block");
+// Per-chunk coefficient record (workspace and pipeline stage).  C[t][s] =
+// theta_s w(s,t) (zero above the diagonal) is stored row-major in fp32 with
+// the 16-byte chunks of row t XOR-permuted by t % 16, so that 32 threads
+// reading 32 different rows stay free of bank conflicts.
+constexpr uint32_t kRecC = 0;                    // 64 x 64 fp32
+constexpr uint32_t kRecBeta = 16384;             // beta_t
+constexpr uint32_t kRecCvec = kRecBeta + 256;    // c_t
+constexpr uint32_t kRecCend = kRecCvec + 256;    // C[n-1][s]
+constexpr uint32_t kRecPend = kRecCend + 256;    // theta_s m(s, n-1)
+constexpr uint32_t kRecScal = kRecPend + 256;    // beta_{n-1}, c_{n-1}, P_{n-1}, n
+constexpr uint32_t kRecBytes = kRecScal + 16;    // 17424 (a multiple of 16)
 
-// Per-chunk coefficients, produced by a coefficient warp (two slots, by chunk
-// parity).  C[t][s] = theta_s w(s,t) is stored for s <= t only (the rest of a
-// row is never read).
-constexpr int kLdc = kChunk + 1;
-struct CoefSlot {
-    float C[kChunk * kLdc];
-    float beta[kChunk];   // prod_{j<=t} (1 - alpha_j)
-    float cvec[kChunk];   // c_t
-    float cend[kChunk];   // C[n-1][s]
-    float pend[kChunk];   // theta_s m(s, n-1)
-    float scal[4];        // beta_{n-1}, c_{n-1}, P_{n-1}, n
-};
+__host__ __device__ constexpr uint32_t c_offset(int t, int s) {
+    return (uint32_t)t * 256u + (uint32_t)(((s >> 2) ^ (t & 15)) << 4) + (uint32_t)(s & 3) * 4u;
+}
 
 struct Layout {
     int D, NS;
-    uint32_t kq_bytes, stage_bytes, off_v, off_g;
-    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, off_coef, total;
+    uint32_t kq_bytes, off_v, off_rec, stage_bytes;
+    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, total;
 };
 
 // Shared-memory map.  Each A~ tile (8 KB, the 64 rows of the scores) is
@@ -100,27 +102,24 @@ __host__ __device__ constexpr Layout make_layout(int D) {
     Layout L{};
     L.D = D;
     L.NS = D == 128 ? 3 : 4;
-    L.kq_bytes = (D / 64) * 16384u;              // per 64-column half: K (8 KB) then Q (8 KB)
-    L.off_v = L.kq_bytes;                        // V slice, 64 x 16 bf16
-    L.off_g = L.kq_bytes + 2048u;                // raw gates
-    L.stage_bytes = L.kq_bytes + 2048u + 1024u;
+    L.kq_bytes = (D / 64) * 16384u;   // per 64-column half: K (8 KB) then Q (8 KB)
+    L.off_v = L.kq_bytes;             // V slice, 64 x 16 bf16
+    L.off_rec = L.kq_bytes + 2048u;   // coefficient record
+    L.stage_bytes = (L.off_rec + kRecBytes + 1023u) & ~1023u;
     uint32_t off = L.NS * L.stage_bytes;
-    off = (off + 1023u) & ~1023u;
-    L.off_ws = off;  off += D * 128u;            // [W;S] operand, row = d_k index
-    L.off_b2 = off;  off += kChunk * 128u;       // [C E^T | Pm E^T], row = token
-    L.off_at0 = off; off += kChunk * 128u;       // A~ (chunk parity 0)
-    L.off_et0 = off; off += kChunk * 128u;       // E^T (chunk parity 0)
+    L.off_ws = off;  off += D * 128u;        // [W;S] operand, row = d_k index
+    L.off_b2 = off;  off += kChunk * 128u;   // [C E^T | Pm E^T], row = token
+    L.off_at0 = off; off += kChunk * 128u;   // A~ (chunk parity 0)
+    L.off_et0 = off; off += kChunk * 128u;   // E^T (chunk parity 0)
     L.off_at1 = off; off += kChunk * 128u;
     L.off_et1 = off; off += kChunk * 128u;
-    L.off_coef = off; off += 2u * (uint32_t)sizeof(CoefSlot);
     L.total = off;
     return L;
 }
 
 struct Bars {
     uint64_t full[4], empty[4];
-    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], at_ready[2], z_done[2], accz_free[2],
-        coef_ready[2], coef_free[2];
+    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], at_ready[2], z_done[2], accz_free[2];
     uint64_t qk_done[3], qk_free[3];
     uint64_t drain;
     uint32_t tmem_base;
@@ -198,57 +197,68 @@ __device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
 //    P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
 //  * the matrix C[t][s] = theta_s w(s,t) with, per column s, the forward
 //    recurrences m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
+
+// ------------------------------------------------------- coefficient pre-pass
+
+// One warp per (sequence, chunk) of n tokens.  Padded tokens have theta 0
+// and eta = keep = 1 (neutral).
+//  * forward scans (lane l owns tokens 2l, 2l+1): beta_t = prod keep,
+//    P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
+//  * C[t][s] = theta_s w(s,t) with, per column s, the forward recurrences
+//    m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
 //    m(s,s) = w(s,s) = 1.  Lane l owns columns l and l + 32; all lanes walk
 //    the rows together.  A column holds m = w = 0 before its start row and the
 //    start enters as an additive unit, so a step is two dependent FMAs and the
 //    rows above the diagonal come out as exact zeros.  With neutral gates
-//    past the last token, m stops changing there, so the final m is
-//    m(s, n-1) (pend); cend is read back from row n-1.
-__device__ void coefficient_warp(StageGates* __restrict__ g, int n, CoefSlot* __restrict__ cs,
-                                 int lane) {
-    const int s0 = lane, s1 = lane + 32;
-    if (s0 >= n) { g->eta[s0] = 1.f; g->alpha[s0] = 0.f; }
-    if (s1 >= n) { g->eta[s1] = 1.f; g->alpha[s1] = 0.f; }
-    __syncwarp();
-    float et[2], kp[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int t = 2 * lane + u;
-        et[u] = g->eta[t];
-        kp[u] = 1.f - g->alpha[t];
-    }
-    float Ab = kp[0] * kp[1], Bb = 0.f;
-    float Ap = et[0] * et[1], Bp = 0.f;
+//    past the last token m stops changing, so the final m is m(s, n-1).
+__global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, int nch) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long BH = (long long)a.B * a.H;
+    if (wid >= BH * nch) return;
+    const int seq = (int)(wid / nch), c = (int)(wid % nch);
+    const int T = a.T;
+    const int n = min(kChunk, T - c * kChunk);
+    const size_t tok0 = (size_t)seq * T + (size_t)c * kChunk;
+    uint8_t* rec = static_cast<uint8_t*>(a.workspace) + (size_t)wid * kRecBytes;
+
+    auto eta_at = [&](int t) { return t < n ? (a.eta ? a.eta[tok0 + t] : 0.f) : 1.f; };
+    auto keep_at = [&](int t) { return t < n ? 1.f - (a.alpha ? a.alpha[tok0 + t] : 0.f) : 1.f; };
+    auto theta_at = [&](int t) { return t < n ? a.theta[tok0 + t] : 0.f; };
+
+    // forward scans
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    const float et0 = eta_at(t0), et1 = eta_at(t1), kp0 = keep_at(t0), kp1 = keep_at(t1);
+    float Ab = kp0 * kp1, Bb = 0.f;
+    float Ap = et0 * et1, Bp = 0.f;
     scan_affine_up(Ab, Bb, lane);
     scan_affine_up(Ap, Bp, lane);
     float pre_b = __shfl_up_sync(0xffffffffu, Ab, 1);
     float pre_p = __shfl_up_sync(0xffffffffu, Ap, 1);
     if (lane == 0) pre_b = pre_p = 1.f;
-    const float beta0 = pre_b * kp[0], beta1 = beta0 * kp[1];
-    const float P0 = pre_p * et[0], P1 = P0 * et[1];
-    float Ac = kp[1] * kp[0], Bc = kp[1] * P0 + P1;
+    const float beta0 = pre_b * kp0, beta1 = beta0 * kp1;
+    const float P0 = pre_p * et0, P1 = P0 * et1;
+    float Ac = kp1 * kp0, Bc = kp1 * P0 + P1;
     scan_affine_up(Ac, Bc, lane);
     float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);
     if (lane == 0) cpre = 0.f;
-    const float c0 = kp[0] * cpre + P0, c1 = kp[1] * c0 + P1;
-    const int t0 = 2 * lane, t1 = t0 + 1;
-    cs->beta[t0] = beta0;  cs->beta[t1] = beta1;
-    cs->cvec[t0] = c0;     cs->cvec[t1] = c1;
+    const float c0 = kp0 * cpre + P0, c1 = kp1 * c0 + P1;
+    float* beta = reinterpret_cast<float*>(rec + kRecBeta);
+    float* cvec = reinterpret_cast<float*>(rec + kRecCvec);
+    reinterpret_cast<float2*>(beta)[lane] = make_float2(beta0, beta1);
+    reinterpret_cast<float2*>(cvec)[lane] = make_float2(c0, c1);
     const int ln = (n - 1) >> 1, un = (n - 1) & 1;
     const float bn = __shfl_sync(0xffffffffu, un ? beta1 : beta0, ln);
     const float cn = __shfl_sync(0xffffffffu, un ? c1 : c0, ln);
     const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
-    if (lane == 0) {
-        cs->scal[0] = bn;
-        cs->scal[1] = cn;
-        cs->scal[2] = Pn;
-        cs->scal[3] = (float)n;
-    }
-    const float th0 = s0 < n ? g->theta[s0] : 0.f, th1 = s1 < n ? g->theta[s1] : 0.f;
-    const float e_lo = g->eta[s0], e_hi = g->eta[s1];
-    const float k_lo = 1.f - g->alpha[s0], k_hi = 1.f - g->alpha[s1];
-    float m0 = 0.f, w0 = 0.f, m1 = 0.f, w1 = 0.f;
-    float* __restrict__ C = cs->C;
+    if (lane == 0)
+        *reinterpret_cast<float4*>(rec + kRecScal) = make_float4(bn, cn, Pn, (float)n);
+
+    // C matrix
+    const int s0 = lane, s1 = lane + 32;
+    const float th0 = theta_at(s0), th1 = theta_at(s1);
+    const float e_lo = eta_at(s0), e_hi = eta_at(s1), k_lo = keep_at(s0), k_hi = keep_at(s1);
+    float m0 = 0.f, w0 = 0.f, m1 = 0.f, w1 = 0.f, ce0 = 0.f, ce1 = 0.f;
 #pragma unroll
     for (int t = 0; t < kChunk; ++t) {
         const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
@@ -263,17 +273,23 @@ __device__ void coefficient_warp(StageGates* __restrict__ g, int n, CoefSlot* __
         }
         w0 = fmaf(k1, w0, m0);
         w1 = fmaf(k1, w1, m1);
-        C[t * kLdc + s0] = th0 * w0;
-        C[t * kLdc + s1] = th1 * w1;
+        const float v0 = th0 * w0, v1 = th1 * w1;
+        *reinterpret_cast<float*>(rec + kRecC + c_offset(t, s0)) = v0;
+        *reinterpret_cast<float*>(rec + kRecC + c_offset(t, s1)) = v1;
+        if (t == n - 1) {
+            ce0 = v0;
+            ce1 = v1;
+        }
     }
-    __syncwarp();
-    cs->pend[s0] = th0 * m0;
-    cs->pend[s1] = th1 * m1;
-    cs->cend[s0] = C[(n - 1) * kLdc + s0];
-    cs->cend[s1] = C[(n - 1) * kLdc + s1];
+    float* cend = reinterpret_cast<float*>(rec + kRecCend);
+    float* pend = reinterpret_cast<float*>(rec + kRecPend);
+    cend[s0] = ce0;
+    cend[s1] = ce1;
+    pend[s0] = th0 * m0;
+    pend[s1] = th1 * m1;
 }
 
-// ------------------------------------------------------------------- kernel
+// ------------------------------------------------------------- scan kernel
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -297,18 +313,18 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
     auto stage = [&](int s) { return sm + s * L.stage_bytes; };
     auto vtile = [&](int s) { return stage(s) + L.off_v; };
-    auto gates = [&](int s) { return reinterpret_cast<StageGates*>(stage(s) + L.off_g); };
+    auto rec = [&](int s) { return stage(s) + L.off_rec; };
+    auto recf = [&](int s, uint32_t off) { return reinterpret_cast<const float*>(rec(s) + off); };
     uint8_t* ws = sm + L.off_ws;
     uint8_t* b2 = sm + L.off_b2;
     auto et = [&](int b) { return sm + (b ? L.off_et1 : L.off_et0); };
     auto at = [&](int b) { return sm + (b ? L.off_at1 : L.off_at0); };
-    auto coef = [&](int p) { return reinterpret_cast<CoefSlot*>(sm + L.off_coef) + p; };
 
     if (tid == 0) {
         for (int s = 0; s < L.NS; ++s) {
-            mbar_init(&B->full[s], 1 + 32);   // expect_tx + every producer lane
-            // Epi1 threads 64 + coefficient warp 1 + chain MMA commit 1 + score MMA commit 1
-            mbar_init(&B->empty[s], 64 + 1 + 1 + 1);
+            mbar_init(&B->full[s], 1);
+            // chain 128 + read side 64 + chain MMA commit 1 + score MMA commit 1
+            mbar_init(&B->empty[s], 128 + 64 + 1 + 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&B->mma1_done[b], 1);
@@ -317,8 +333,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             mbar_init(&B->at_ready[b], 64);
             mbar_init(&B->z_done[b], 1);
             mbar_init(&B->accz_free[b], 64);
-            mbar_init(&B->coef_ready[b], 32);
-            mbar_init(&B->coef_free[b], 128 + 64);
         }
         for (int b = 0; b < 3; ++b) {
             mbar_init(&B->qk_done[b], 1);
@@ -339,10 +353,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
     if (warp < 4) {
         // ----------------------------------------------------- chain warps
-        // Thread j holds row slice W[r0..r0+15][j], S[...][j] (fp32).  Every
-        // thread runs every iteration and reaches every named barrier, also
-        // after an abort (then it only skips work), so the barriers stay
-        // balanced.  Warp 0 issues the two chain MMAs itself.
+        // Every thread runs every iteration and reaches every named barrier,
+        // also after an abort (then it only skips work), so the barriers
+        // stay balanced.
         const int j = tid;
         const bool own = j < D;
         const size_t init = (size_t)(a.shared ? 0 : bb) * a.H + hh;
@@ -387,24 +400,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         named_bar_sync(1, 128);
         bool ok = issue_mma1(0, true);
         for (int c = 0; c < nch; ++c) {
-            const int st = c % L.NS, b = c & 1, p = c & 1;
-            const CoefSlot* cs = coef(p);
-            if (ok) ok = wait_all(B, &B->coef_ready[p], (c >> 1) & 1, status);
+            const int st = c % L.NS, b = c & 1;
+            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
             if (warp < 2) {
                 // Epi1: errors of token t at the chunk-start state
                 const int t = j;
-                if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
                 if (ok) ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
                 if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
                 if (ok) {
-                    const float ce = cs->cend[t], pe = cs->pend[t];
+                    const float ce = recf(st, kRecCend)[t], pe = recf(st, kRecPend)[t];
                     tc_fence_after();
                     float kw[16];
                     tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
                     const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
                     const uint4 v0 = vrow[0], v1 = vrow[1];
                     tmem_wait_ld();
-                    mbar_arrive(&B->empty[st]);
                     const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
                     const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
                     float e[16], ec[16], ep[16];
@@ -451,8 +461,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // Epi2: state carry
             if (ok) ok = wait_all(B, &B->mma2_done[b], (c >> 1) & 1, status);
             if (ok) {
-                const float bn = cs->scal[0], cn = cs->scal[1], Pn = cs->scal[2];
-                mbar_arrive(&B->coef_free[p]);
+                const float* sc = recf(st, kRecScal);
+                const float bn = sc[0], cn = sc[1], Pn = sc[2];
+                mbar_arrive(&B->empty[st]);
                 tc_fence_after();
                 if (own) {
                     float uw[16], us[16];
@@ -485,23 +496,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     } else if (warp == 4) {
         // --------------------------------------------------------- producer
-        // K, Q (two 64-column halves each) and the V slice by TMA; the raw
-        // gates by bulk copies when the sequence length keeps them 16-byte
-        // aligned, else by plain loads.
-        const bool bulk_gates = (T % 4) == 0;
-        int issued = 0;
-        for (int c = 0; c < nch; ++c) {
-            const int st = c % L.NS;
-            const int n = min(kChunk, T - c * kChunk);
-            const size_t tok0 = (size_t)seq * T + (size_t)c * kChunk;
-            bool ok = true;
-            if (c >= L.NS && lane == 0) ok = wait_bar(B, &B->empty[st], ((c / L.NS) - 1) & 1, status);
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            StageGates* g = gates(st);
-            if (lane == 0) {
-                uint32_t tx = L.kq_bytes + kChunk * kRows * 2;
-                const uint32_t gb = (uint32_t)n * 4u;
-                if (bulk_gates) tx += gb * (1 + (a.eta != nullptr) + (a.alpha != nullptr));
+        if (lane == 0) {
+            const uint32_t tx = L.kq_bytes + kChunk * kRows * 2 + kRecBytes;
+            const uint8_t* recs = static_cast<const uint8_t*>(a.workspace) +
+                                  (size_t)seq * nch * kRecBytes;
+            int issued = 0;
+            for (int c = 0; c < nch; ++c) {
+                const int st = c % L.NS;
+                if (c >= L.NS && !wait_bar(B, &B->empty[st], ((c / L.NS) - 1) & 1, status)) break;
                 mbar_expect_tx(&B->full[st], tx);
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
@@ -510,34 +512,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                                 c * kChunk, seq);
                 }
                 tma_load_3d(vtile(st), &vmap, &B->full[st], r0, c * kChunk, seq);
-                if (bulk_gates) {
-                    bulk_load(g->theta, a.theta + tok0, gb, &B->full[st]);
-                    if (a.eta) bulk_load(g->eta, a.eta + tok0, gb, &B->full[st]);
-                    if (a.alpha) bulk_load(g->alpha, a.alpha + tok0, gb, &B->full[st]);
-                }
+                bulk_load(rec(st), recs + (size_t)c * kRecBytes, kRecBytes, &B->full[st]);
+                issued = c + 1;
             }
-            if (!bulk_gates) {
-                for (int t = lane; t < n; t += 32) {
-                    g->theta[t] = a.theta[tok0 + t];
-                    if (a.eta) g->eta[t] = a.eta[tok0 + t];
-                    if (a.alpha) g->alpha[t] = a.alpha[tok0 + t];
-                }
-            }
-            if (!a.eta)
-                for (int t = lane; t < kChunk; t += 32) g->eta[t] = 0.f;
-            if (!a.alpha)
-                for (int t = lane; t < kChunk; t += 32) g->alpha[t] = 0.f;
-            issued = c + 1;
-            mbar_arrive(&B->full[st]);
-        }
-        // drain: every issued stage's copies must have landed before exit
-        if (lane == 0) {
+            // drain: every issued stage's copies must have landed before exit
             for (int c = (issued > L.NS ? issued - L.NS : 0); c < issued; ++c) {
                 const long long t0 = clock64();
                 while (!mbar_try_wait(&B->full[c % L.NS], (c / L.NS) & 1))
                     if (clock64() - t0 > kWaitCycles) break;
             }
         }
+        __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------ read-side MMA issuer
         // The correction MMA of chunk c-1 goes right after MMA1(c) completes
@@ -602,33 +587,38 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 if (clock64() - t0 > kWaitCycles) break;
         }
         __syncwarp();
-    } else if (warp < 8) {
+    } else {
         // ------------------------------------------------ read side (6-7)
         const int t = tid - 192;             // token, TMEM lane 64 + t
         const int wl = (warp & 3) * 32;      // 64 or 96
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const int b = c & 1, p = c & 1, q = c % 3;
-            ok = wait_all(B, &B->coef_ready[p], (c >> 1) & 1, status);
+            const int st = c % L.NS, b = c & 1, q = c % 3;
+            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
             if (ok) ok = wait_all(B, &B->qk_done[q], (c / 3) & 1, status);
+            if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
             if (!ok) break;
             tc_fence_after();
-            const CoefSlot* cs = coef(p);
-            // A~[t][s] = C[t][s] (q_t . k_s) for s <= t
-            const float* crow = cs->C + t * kLdc;
+            // A~[t][s] = C[t][s] (q_t . k_s); C is zero above the diagonal
+            const uint8_t* crow = rec(st) + kRecC + t * 256;
             uint8_t* arow = at(b);
-            if (c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
-            if (!ok) break;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float r[16];
                 tmem_ld16(tmem_addr(tmem, wl, kAccQK + q * 64 + 16 * q4), r);
+                float cv[16];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 f = *reinterpret_cast<const float4*>(
+                        crow + (((4 * q4 + jj) ^ (t & 15)) << 4));
+                    cv[4 * jj] = f.x;
+                    cv[4 * jj + 1] = f.y;
+                    cv[4 * jj + 2] = f.z;
+                    cv[4 * jj + 3] = f.w;
+                }
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int sidx = 16 * q4 + i;
-                    r[i] = sidx <= t ? crow[sidx] * r[i] : 0.f;
-                }
+                for (int i = 0; i < 16; ++i) r[i] *= cv[i];
                 st_chunk(arow, t, 16 * q4, r);
                 st_chunk(arow, t, 16 * q4 + 8, r + 8);
             }
@@ -636,6 +626,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             mbar_arrive(&B->qk_free[q]);
             fence_proxy_async_smem();
             mbar_arrive(&B->at_ready[b]);
+            const float bt = recf(st, kRecBeta)[t], ct = recf(st, kRecCvec)[t];
+            const int n = (int)recf(st, kRecScal)[3];
+            mbar_arrive(&B->empty[st]);
             // reads: z_t = beta_t Q W^T + c_t Q S^T - 2 A~ E^T
             ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
             if (!ok) break;
@@ -653,9 +646,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&B->accz_free[b]);
-            const float bt = cs->beta[t], ct = cs->cvec[t];
-            const int n = (int)cs->scal[3];
-            mbar_arrive(&B->coef_free[p]);
             if (t < n) {
                 float zz[16];
 #pragma unroll
@@ -670,21 +660,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 reinterpret_cast<uint4*>(zr)[0] = o0;
                 reinterpret_cast<uint4*>(zr)[1] = o1;
             }
-        }
-    } else {
-        // ------------------------------------------ coefficient warps (8-9)
-        // Warp 8 + p handles the chunks of parity p into slot p.
-        const int p = warp - 8;
-        bool ok = true;
-        for (int c = p; c < nch && ok; c += 2) {
-            const int st = c % L.NS;
-            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (ok && c >= 2) ok = wait_all(B, &B->coef_free[p], ((c - 2) >> 1) & 1, status);
-            if (!ok) break;
-            coefficient_warp(gates(st), min(kChunk, T - c * kChunk), coef(p), lane);
-            mbar_arrive(&B->coef_ready[p]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B->empty[st]);
         }
     }
 
@@ -728,11 +703,27 @@ bool make_map(CUtensorMap* m, const void* ptr, int BH, int T, int D, int bx, boo
 
 bool linear_tc_supported(const LinearArgs& a) {
     return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kChunk &&
-           a.T >= 1 && encode_fn() != nullptr;
+           a.T >= 1;
+}
+
+size_t linear_tc_workspace_bytes(const LinearArgs& a) {
+    const size_t nch = ((size_t)a.T + kChunk - 1) / kChunk;
+    return (size_t)a.B * a.H * nch * kRecBytes;
 }
 
 cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s) {
     const int D = a.dk, BH = a.B * a.H;
+    const int nch = (a.T + kChunk - 1) / kChunk;
+    if (!a.workspace || a.workspace_bytes < linear_tc_workspace_bytes(a) ||
+        (reinterpret_cast<uintptr_t>(a.workspace) & 15u))
+        return cudaErrorInvalidValue;
+    {
+        const long long warps = (long long)BH * nch;
+        const unsigned blocks = (unsigned)((warps + 3) / 4);
+        linear_coef_kernel<<<blocks, 128, 0, s>>>(a, nch);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     CUtensorMap km, qm, vm;
     if (!make_map(&km, a.k, BH, a.T, D, 64, true) || !make_map(&qm, a.q, BH, a.T, D, 64, true) ||
         !make_map(&vm, a.v, BH, a.T, D, kRows, false))

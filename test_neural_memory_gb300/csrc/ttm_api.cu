@@ -52,10 +52,20 @@ bool bad_alias(Span o, Span in, bool exact_ok) {
 
 bool dims_ok(int x, int dtype) { return x >= 1 && x % (dtype == TTM_BF16 ? 8 : 4) == 0; }
 
+// Kernel the current policy would pick for these arguments (host decision).
+int select_linear(const ttm::LinearArgs& a) {
+    const bool tc_ok = ttm::linear_tc_supported(a);
+    const bool simt_ok = ttm::linear_simt_supported(a);
+    if (g_policy == TTM_KERNEL_TC) return tc_ok ? TTM_KID_LINEAR_TC : TTM_KID_NONE;
+    if (g_policy == TTM_KERNEL_SIMT) return simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE;
+    return tc_ok ? TTM_KID_LINEAR_TC : (simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE);
+}
+
 int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
                   const void* k, const void* v, const float* eta, const float* theta,
                   const float* alpha, const float* W0, const float* S0, int shared, void* z,
-                  float* W_out, float* S_out, void* stream) {
+                  float* W_out, float* S_out, void* workspace, size_t workspace_bytes,
+                  void* stream) {
     if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
     if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
     if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
@@ -63,7 +73,7 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
         return TTM_ERR_UNSUPPORTED;
     if (!W0 || !W_out) return TTM_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !theta || !z)) return TTM_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, eta, theta, alpha, W0, S0, z, W_out, S_out};
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W0, S0, z, W_out, S_out, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
 
@@ -87,6 +97,12 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     if (bad_alias(sS, sS0, !shared) || bad_alias(sS, sW0, false)) return TTM_ERR_INVALID_ARG;
     if (overlap(sz, sW) || overlap(sz, sS) || overlap(sW, sS)) return TTM_ERR_INVALID_ARG;
     if (bad_alias(sz, sW0, false) || bad_alias(sz, sS0, false)) return TTM_ERR_INVALID_ARG;
+    const Span swk{workspace, workspace_bytes};
+    {
+        const Span all[] = {sq, sk, sv, sg[0], sg[1], sg[2], sW0, sS0, sz, sW, sS};
+        for (const Span& x : all)
+            if (overlap(swk, x)) return TTM_ERR_INVALID_ARG;
+    }
 
     ttm::LinearArgs a{};
     a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
@@ -95,14 +111,13 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     a.eta = eta; a.theta = theta; a.alpha = alpha;
     a.W0 = W0; a.S0 = S0; a.shared = shared ? 1 : 0;
     a.z = z; a.W_out = W_out; a.S_out = S_out;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
 
-    const bool tc_ok = ttm::linear_tc_supported(a);
-    const bool simt_ok = ttm::linear_simt_supported(a);
-    int kid = TTM_KID_NONE;
-    if (g_policy == TTM_KERNEL_TC) kid = tc_ok ? TTM_KID_LINEAR_TC : TTM_KID_NONE;
-    else if (g_policy == TTM_KERNEL_SIMT) kid = simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE;
-    else kid = tc_ok ? TTM_KID_LINEAR_TC : (simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE);
+    const int kid = select_linear(a);
     if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+    if (kid == TTM_KID_LINEAR_TC &&
+        (!workspace || workspace_bytes < ttm::linear_tc_workspace_bytes(a)))
+        return TTM_ERR_INVALID_ARG;
 
     a.status = status_ptr();
     if (!a.status) return TTM_ERR_CUDA;
@@ -122,18 +137,31 @@ extern "C" {
 int ttm_linear_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
                    const void* k, const void* v, const float* eta, const float* theta,
                    const float* alpha, const float* W0, int w0_shared_over_batch, void* z,
-                   float* W_out, void* stream) {
+                   float* W_out, void* workspace, size_t workspace_bytes, void* stream) {
     if (eta || alpha) return TTM_ERR_INVALID_ARG;
     return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, nullptr, theta, nullptr, W0,
-                         nullptr, w0_shared_over_batch, z, W_out, nullptr, stream);
+                         nullptr, w0_shared_over_batch, z, W_out, nullptr, workspace,
+                         workspace_bytes, stream);
 }
 
 int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
                    const void* k, const void* v, const float* eta, const float* theta,
                    const float* alpha, const float* W0, const float* S0,
-                   int w0_shared_over_batch, void* z, float* W_out, float* S_out, void* stream) {
+                   int w0_shared_over_batch, void* z, float* W_out, float* S_out,
+                   void* workspace, size_t workspace_bytes, void* stream) {
     return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, eta, theta, alpha, W0, S0,
-                         w0_shared_over_batch, z, W_out, S_out, stream);
+                         w0_shared_over_batch, z, W_out, S_out, workspace, workspace_bytes,
+                         stream);
+}
+
+size_t ttm_linear_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1 || (dtype != TTM_F32 && dtype != TTM_BF16) ||
+        !dims_ok(dk, dtype) || !dims_ok(dv, dtype))
+        return 0;
+    ttm::LinearArgs a{};
+    a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    return select_linear(a) == TTM_KID_LINEAR_TC ? ttm::linear_tc_workspace_bytes(a) : 0;
 }
 
 int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype, const void* q,

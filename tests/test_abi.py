@@ -46,9 +46,9 @@ def P(i, misalign=0):
 
 
 def lin_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=4, dt=1, q=P(0), k=P(1), v=P(2), eta=None,
-             theta=P(3), alpha=None, W0=P(4), shared=0, z=P(5), W=P(6)):
+             theta=P(3), alpha=None, W0=P(4), shared=0, z=P(5), W=P(6), ws=None, wsb=0):
     return L.ttm_linear_fwd(B, H, T, dk, dv, chunk, dt, q, k, v, eta, theta, alpha, W0, shared,
-                            z, W, None)
+                            z, W, ws, wsb, None)
 
 
 def test_linear_rejects_malformed(L):
@@ -69,7 +69,7 @@ def test_linear_rejects_malformed(L):
 
 def test_titans_and_mlp_reject_malformed(L):
     r = L.ttm_titans_fwd(1, 1, 8, 64, 64, 4, 1, P(0), P(1), P(2), P(3), P(4), P(5), P(6),
-                         P(7), 0, P(8), P(9), P(9), None)
+                         P(7), 0, P(8), P(9), P(9), None, 0, None)
     assert r == INVALID                            # S_out == W_out
     r = L.ttm_mlp_fwd(1, 1, 8, 64, 256, 4, 1, P(0), P(1), P(2), P(3), P(4), None, P(5), P(6),
                       None, None, 0, P(8), P(9), P(10), None, None, None)
@@ -86,6 +86,20 @@ def test_tc_policy_reports_unsupported_on_host(L):
     with ttm.kernel_policy("tc"):
         # fp32 inputs never run on the tensor-core kernel
         assert lin_call(L, dt=0) == UNSUPPORTED
+
+
+def test_workspace_size_and_checks(L):
+    # tensor-core shapes need one 17424-byte record per (sequence, 64-token chunk)
+    with ttm.kernel_policy("tc"):
+        assert L.ttm_linear_workspace_size(2, 3, 130, 128, 128, 64, 1) == 2 * 3 * 3 * 17424
+        assert L.ttm_linear_workspace_size(1, 1, 64, 64, 64, 64, 0) == 0   # fp32: rejected
+        # a tensor-core call without (enough) workspace is malformed
+        assert lin_call(L, T=64, chunk=64) == INVALID
+        assert lin_call(L, T=64, chunk=64, ws=P(9), wsb=100) == INVALID
+        # workspace overlapping an input
+        assert lin_call(L, T=64, chunk=64, ws=P(0), wsb=17424) == INVALID
+    with ttm.kernel_policy("simt"):
+        assert L.ttm_linear_workspace_size(2, 3, 130, 128, 128, 64, 1) == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a GPU")
