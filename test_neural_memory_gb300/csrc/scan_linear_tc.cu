@@ -32,7 +32,8 @@
 //              slice, bulk copy of the coefficient record.
 //   warp 5     read-side MMA issuer (scores two chunks ahead, corrections)
 //              and TMEM owner.
-//   warps 6-7  reads: masked, coefficient-weighted scores and the output z.
+//   warps 6-9  weight the scores by C (warp w takes the 16 tokens of TMEM
+//              sub-partition w % 4); warps 6-7 then form the outputs z.
 //
 // Tensor-core contractions per chunk (A operands are M = 128 rows: the K tile
 // and the Q tile are stacked so one instruction covers both):
@@ -64,13 +65,13 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM column map
 constexpr uint32_t kAcc1 = 0;     // 2 x 32 columns: [K W^T | K S^T] on lanes 0-63, [Q W^T | Q S^T] on 64-127
 constexpr uint32_t kAcc2 = 64;    // 32 columns: W / S updates (lane = d_k index)
-constexpr uint32_t kAccQK = 128;  // 3 x 64 columns: Q K^T on lanes 64-127
+constexpr uint32_t kAccQK = 128;  // 3 x 64 columns: Q K^T (M = 64 layout: 16 tokens per sub-partition)
 constexpr uint32_t kAccZ = 320;   // 2 x 16 columns: A~ E^T on lanes 64-127
 
 // Per-chunk coefficient record (workspace and pipeline stage).  C[t][s] =
@@ -323,20 +324,20 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     if (tid == 0) {
         for (int s = 0; s < L.NS; ++s) {
             mbar_init(&B->full[s], 1);
-            // chain 128 + read side 64 + chain MMA commit 1 + score MMA commit 1
-            mbar_init(&B->empty[s], 128 + 64 + 1 + 1);
+            // chain 128 + read side 128 + chain MMA commit 1 + score MMA commit 1
+            mbar_init(&B->empty[s], 128 + 128 + 1 + 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&B->mma1_done[b], 1);
             mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->acc1_free[b], 64);
-            mbar_init(&B->at_ready[b], 64);
+            mbar_init(&B->at_ready[b], 128);
             mbar_init(&B->z_done[b], 1);
             mbar_init(&B->accz_free[b], 64);
         }
         for (int b = 0; b < 3; ++b) {
             mbar_init(&B->qk_done[b], 1);
-            mbar_init(&B->qk_free[b], 64);
+            mbar_init(&B->qk_free[b], 128);
         }
         mbar_init(&B->drain, 1);
         B->abort = 0;
@@ -529,7 +530,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // (it runs while the errors of chunk c are formed); the scores run two
         // chunks ahead, issued after MMA2(c) completes (during the carry).
         if (nch > 0) {
-            const uint32_t idqk = idesc_bf16_f32(128, 64, 0, 0);
+            const uint32_t idqk = idesc_bf16_f32(64, 64, 0, 0);
             const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
             auto issue_qk = [&](int c) -> bool {
                 const int q = c % 3, st = c % L.NS;
@@ -543,7 +544,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(d, sdesc(half, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk, kk > 0);
+                        // A = the 64 Q rows (8 KB after the K rows), B = the 64 K rows
+                        mma_bf16(d, sdesc(half + 8192, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk,
+                                 kk > 0);
                     }
                     mma_commit(&B->qk_done[q]);
                     mma_commit(&B->empty[st]);
@@ -588,9 +591,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ read side (6-7)
-        const int t = tid - 192;             // token, TMEM lane 64 + t
-        const int wl = (warp & 3) * 32;      // 64 or 96
+        // ------------------------------------------------ read side (6-9)
+        // Score weighting: warp w owns TMEM sub-partition p = w % 4, i.e. the
+        // tokens 16p + lane (lane < 16) of the M = 64 score accumulator.
+        const int p = warp & 3;
+        const int ta = 16 * p + lane;        // token of this lane in A~ (lane < 16)
+        const bool zw = warp < 8;            // warps 6-7 also form the outputs
+        const int t = tid - 192;             // output token of warps 6-7 (TMEM lane 64 + t)
+        const int wl = (warp & 3) * 32;
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
             const int st = c % L.NS, b = c & 1, q = c % 3;
@@ -600,32 +608,40 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (!ok) break;
             tc_fence_after();
             // A~[t][s] = C[t][s] (q_t . k_s); C is zero above the diagonal
-            const uint8_t* crow = rec(st) + kRecC + t * 256;
+            const uint8_t* crow = rec(st) + kRecC + ta * 256;
             uint8_t* arow = at(b);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float r[16];
                 tmem_ld16(tmem_addr(tmem, wl, kAccQK + q * 64 + 16 * q4), r);
                 float cv[16];
+                if (lane < 16) {
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const float4 f = *reinterpret_cast<const float4*>(
-                        crow + (((4 * q4 + jj) ^ (t & 15)) << 4));
-                    cv[4 * jj] = f.x;
-                    cv[4 * jj + 1] = f.y;
-                    cv[4 * jj + 2] = f.z;
-                    cv[4 * jj + 3] = f.w;
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const float4 f = *reinterpret_cast<const float4*>(
+                            crow + (((4 * q4 + jj) ^ (ta & 15)) << 4));
+                        cv[4 * jj] = f.x;
+                        cv[4 * jj + 1] = f.y;
+                        cv[4 * jj + 2] = f.z;
+                        cv[4 * jj + 3] = f.w;
+                    }
                 }
                 tmem_wait_ld();
+                if (lane < 16) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] *= cv[i];
-                st_chunk(arow, t, 16 * q4, r);
-                st_chunk(arow, t, 16 * q4 + 8, r + 8);
+                    for (int i = 0; i < 16; ++i) r[i] *= cv[i];
+                    st_chunk(arow, ta, 16 * q4, r);
+                    st_chunk(arow, ta, 16 * q4 + 8, r + 8);
+                }
             }
             tc_fence_before();
             mbar_arrive(&B->qk_free[q]);
             fence_proxy_async_smem();
             mbar_arrive(&B->at_ready[b]);
+            if (!zw) {
+                mbar_arrive(&B->empty[st]);
+                continue;
+            }
             const float bt = recf(st, kRecBeta)[t], ct = recf(st, kRecCvec)[t];
             const int n = (int)recf(st, kRecScal)[3];
             mbar_arrive(&B->empty[st]);
