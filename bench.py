@@ -267,7 +267,7 @@ def oracle_tokens_for(w: wl.Workload, seconds: float) -> int:
 def run_ours(args, rank, world, dev):
     import test_neural_memory_gb300 as ttm
 
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = wl.generate(w)
     stream = torch.cuda.current_stream(dev)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
@@ -310,7 +310,7 @@ def run_ours(args, rank, world, dev):
         raise RuntimeError(f"device status {ttm.status_str(status)}")
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, w, inp, dev, stream, world)
+    e2e = run_e2e(args, w, inp, dev, stream, world) if args.e2e_steps > 0 else None
 
     value = w.tokens * world * args.steps / (total_ms / 1e3)
     line = {
@@ -374,8 +374,16 @@ def run_e2e(args, w, inp, dev, stream, world):
 # reference arm: the float64 oracle on the host cores
 # ----------------------------------------------------------------------------
 
-def run_reference(args):
+def workload_of(args) -> wl.Workload:
+    """The named workload, optionally with a shorter sequence (profiling runs)."""
     w = wl.WORKLOADS[args.workload]
+    if args.T:
+        w = w.shrink(T=args.T, name=f"{w.name} (T shortened to {args.T})")
+    return w
+
+
+def run_reference(args):
+    w = workload_of(args)
     per_step = max(0.5, args.reference_seconds / max(1, args.steps + args.warmup))
     T_s = oracle_tokens_for(w, per_step)
     inp = wl.generate(w.shrink(T=T_s))
@@ -425,7 +433,9 @@ def main():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=5, help="0 skips the end-to-end leg")
+    ap.add_argument("--T", type=int, default=0,
+                    help="shorten the sequence (profiling only; the metric line says so)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -166,7 +166,8 @@ int ttm_set_kernel_policy(int policy);
 int ttm_last_kernel(void);
 
 /* Number of kernels this process has enqueued through ttm_*_fwd so far
- * (monotonic; counts successful launches only). */
+ * (monotonic; successful calls only; the tensor-core linear path enqueues two:
+ * the coefficient pre-pass and the scan). */
 unsigned long long ttm_launch_count(void);
 
 /* Synchronises the current device, then returns and clears its status word:

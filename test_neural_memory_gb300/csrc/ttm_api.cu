@@ -126,7 +126,8 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
                                                    : ttm::linear_simt_launch(a, s);
     if (e != cudaSuccess) return TTM_ERR_CUDA;
     t_last_kernel = kid;
-    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    // the tensor-core path enqueues the coefficient pre-pass and the scan
+    __atomic_add_fetch(&g_launches, kid == TTM_KID_LINEAR_TC ? 2ULL : 1ULL, __ATOMIC_RELAXED);
     return TTM_OK;
 }
 
