@@ -153,6 +153,41 @@ int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype,
                 void* z, float* W1_out, float* W2_out, float* S1_out, float* S2_out,
                 void* stream);
 
+/*
+ * ttm_titans_fwd_noalloc — ttm_titans_fwd for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: this is a deployment variant
+ * of the same scan, not part of the method.)
+ *
+ * Who needs it: callers that are handed only their input and output buffers
+ * and may not call cudaMalloc or any allocating routine themselves, so they
+ * cannot provide the workspace ttm_titans_fwd needs for its tensor-core path
+ * (for example a plug-in inside a host framework that plans all device memory
+ * in advance, or code that must stay allocation-free).
+ *
+ * Arguments, results and errors are those of ttm_titans_fwd without the
+ * workspace arguments.  The scratch comes from one block of
+ * TTM_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library: every GPU that
+ * loads the library holds that block until the process exits.
+ *   - Limit: a call whose workspace requirement (ttm_linear_workspace_size)
+ *     exceeds TTM_NOALLOC_SCRATCH_BYTES returns TTM_ERR_UNSUPPORTED before
+ *     touching the GPU; with the tensor-core path that is
+ *     B*H*ceil(T/64) * 17424 bytes, i.e. at most 962 (sequence, 64-token
+ *     chunk) pairs.
+ *   - Set-up: the first call on each device looks up the block's device
+ *     address (with that device current); make that first call before any
+ *     stream capture.
+ *   - Sharing: all calls on a device use the same block and it keeps the
+ *     last call's contents (nothing in it needs to start at zero).  Calls
+ *     that overlap on the GPU (e.g. on two streams) race on it: serialise them.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define TTM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int ttm_titans_fwd_noalloc(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                           const void* q, const void* k, const void* v,
+                           const float* eta, const float* theta, const float* alpha,
+                           const float* W0, const float* S0, int w0_shared_over_batch,
+                           void* z, float* W_out, float* S_out, void* stream);
+
 /* Static English text for a ttm_status value (never NULL). */
 const char* ttm_status_str(int status);
 
