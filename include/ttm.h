@@ -188,6 +188,17 @@ int ttm_titans_fwd_noalloc(int B, int H, int T, int dk, int dv, int chunk, int d
                            const float* W0, const float* S0, int w0_shared_over_batch,
                            void* z, float* W_out, float* S_out, void* stream);
 
+/* The activation of the 2-layer memory and its derivative, evaluated on the
+ * device exactly as the tensor-core 2-layer kernel evaluates them: for the n
+ * values x[i], y[i] = GELU(x) = x Phi(x) and, if dy is not NULL,
+ * dy[i] = GELU'(x) = Phi(x) + x phi(x).  The pages name no activation for the
+ * memory MLP; the library reads it as the erf-based GELU (Phi the standard
+ * normal CDF, phi its density).  x, y, dy: device fp32 arrays of n elements,
+ * owned by the caller; y may be x (in place), dy must not overlap x or y.
+ * Asynchronous on `stream`.  Returns TTM_ERR_INVALID_ARG for n < 0 or bad
+ * pointers, TTM_ERR_CUDA if the launch fails. */
+int ttm_mlp_gelu(const float* x, float* y, float* dy, int n, void* stream);
+
 /* Static English text for a ttm_status value (never NULL). */
 const char* ttm_status_str(int status);
 

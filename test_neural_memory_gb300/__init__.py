@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
         L.ttm_linear_workspace_size.argtypes = [i] * 7
         L.ttm_linear_workspace_size.restype = sz
         L.ttm_mlp_fwd.argtypes = [i] * 7 + [p] * 6 + [p] * 4 + [i] + [p] * 5 + [p]
+        L.ttm_mlp_gelu.argtypes = [p, p, p, i, p]
+        L.ttm_mlp_gelu.restype = i
         for f in (L.ttm_linear_fwd, L.ttm_titans_fwd, L.ttm_mlp_fwd):
             f.restype = i
         L.ttm_status_str.argtypes = [i]
@@ -205,3 +207,17 @@ def mlp_fwd(q, k, v, theta, W1_0, W2_0, chunk, *, eta=None, alpha=None, S1_0=Non
                              _ptr(W1_out), _ptr(W2_out), _ptr(S1_out), _ptr(S2_out),
                              _stream(q, stream)), "ttm_mlp_fwd")
     return z, W1_out, W2_out, S1_out, S2_out
+
+
+def mlp_gelu(x, *, want_grad=True, stream=None):
+    """GELU(x) and GELU'(x) of a float32 CUDA tensor, as the 2-layer memory kernel
+    evaluates them on the device.  Returns (y, dy) (dy None unless want_grad)."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise TTMError(ERR_INVALID_ARG, "mlp_gelu (expects a float32 CUDA tensor)")
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x) if want_grad else None
+    _check(lib().ttm_mlp_gelu(_ptr(x), _ptr(y), _ptr(dy), x.numel(), _stream(x, stream)),
+           "ttm_mlp_gelu")
+    return y, dy

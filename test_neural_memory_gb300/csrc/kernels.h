@@ -49,4 +49,11 @@ bool linear_tc_supported(const LinearArgs& a);
 size_t linear_tc_workspace_bytes(const LinearArgs& a);
 cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s);
 
+// tcgen05 + TMA kernel for the 2-layer MLP memory (scan_mlp_tc.cu): bf16,
+// d = 64, hidden = 256, chunk 16; one cluster of two CTAs per sequence.
+bool mlp_tc_supported(const MlpArgs& a);
+cudaError_t mlp_tc_launch(const MlpArgs& a, cudaStream_t s);
+// The activation of that kernel on n values: y = GELU(x), dy = GELU'(x) (dy may be NULL).
+cudaError_t mlp_gelu_launch(const float* x, float* y, float* dy, int n, cudaStream_t s);
+
 }  // namespace ttm

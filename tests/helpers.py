@@ -62,22 +62,24 @@ def run_linear_oracle(w, inp, heads=None, S0=None):
     return r
 
 
-def run_mlp_gpu(w, inp, device="cuda"):
+def run_mlp_gpu(w, inp, device="cuda", S1_0=None, S2_0=None):
     import test_neural_memory_gb300 as ttm
     d = to_dev(inp, device)
+    dev = lambda t: None if t is None else t.to(device=device, dtype=torch.float32).contiguous()
     z, W1, W2, S1, S2 = ttm.mlp_fwd(d["q"], d["k"], d["v"], d["theta"], d["W1_0"], d["W2_0"],
                                     w.chunk, eta=d["eta"], alpha=d["alpha"],
-                                    w0_shared=w.w0_shared)
+                                    S1_0=dev(S1_0), S2_0=dev(S2_0), w0_shared=w.w0_shared)
     torch.cuda.synchronize()
     return dict(z=z, W1=W1, W2=W2, S1=S1, S2=S2, kernel=ttm.last_kernel())
 
 
-def run_mlp_oracle(w, inp, heads=None):
+def run_mlp_oracle(w, inp, heads=None, S1_0=None, S2_0=None):
     sel = slice(None) if heads is None else list(heads)
     pick = lambda t: None if t is None else f64(t)[:, sel]
     return oracle.mlp_primal(pick(inp["q"]), pick(inp["k"]), pick(inp["v"]), pick(inp["theta"]),
                              pick(inp["W1_0"]), pick(inp["W2_0"]), w.chunk, eta=pick(inp["eta"]),
-                             alpha=pick(inp["alpha"]), shared_over_batch=w.w0_shared)
+                             alpha=pick(inp["alpha"]), S1_0=pick(S1_0), S2_0=pick(S2_0),
+                             shared_over_batch=w.w0_shared)
 
 
 def compare(gpu: dict, ref: dict, names, tol, heads=None) -> dict:
