@@ -126,9 +126,10 @@ int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
  * Bytes of workspace ttm_linear_fwd / ttm_titans_fwd need for these sizes
  * under the current kernel policy: 0 when the selected kernel needs none (or
  * the shape is rejected), else B*H*ceil(T/64) * 17424 for the tensor-core
- * path.  The chunk coefficients are the matrix C of the chunk's matrix form
- * ("TTT layers 与 fast weights" §1.1 eq (9) with the decay and momentum
- * unrolling of "论文速览 | Titans" §4.3-§4.5).
+ * path: one record per (sequence, 64-token chunk) of the chunk coefficients
+ * of the matrix form ("TTT layers 与 fast weights" §1.1 eq (9) with the decay
+ * and momentum unrolling of "论文速览 | Titans" §4.3-§4.5): the matrix C,
+ * beta_t, c_t and the last rows of C and of the momentum weights.
  */
 size_t ttm_linear_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
 

@@ -2,51 +2,58 @@
 //
 // Method (per sequence, chunks of 64 tokens; "TTT layers 与 fast weights" §1.1
 // eqs (7)-(9) for the matrix form of one chunk, "论文速览 | Titans" §4.3-§4.5
-// for the decay / momentum unrolling): with the chunk-start state (W, S), the
-// chunk's keys K, queries Q, values V (rows = tokens) and the per-chunk
-// coefficients beta_t, c_t, P_t, C[t][s] (see scan_simt.cu for their
-// definition),
+// for the decay / momentum unrolling): with the chunk-start state (W_c, S_c),
+// the chunk's keys K_c, queries Q_c, values V_c (rows = tokens) and the
+// chunk coefficients beta_t, c_t, P_t, C[t][s], Pm[t][s] (see scan_simt.cu),
 //
-//   E^T  = K W^T - V                       errors at the chunk-start state
+//   E_c  = K_c W_c^T - V_c                           errors at the chunk start
 //   z_t  = beta_t (Q W^T)_t + c_t (Q S^T)_t - 2 sum_{s<=t} C[t][s] (q_t.k_s) e_s
-//   W'   = beta_n W + c_n S - 2 (E diag(C[n][.]) K)
-//   S'   = P_n S        - 2 (E diag(Pm[n][.]) K)
+//   W_{c+1} = beta_n W_c + c_n S_c - 2 E_c^T diag(C[n]) K_c
+//   S_{c+1} = P_n S_c            - 2 E_c^T diag(Pm[n]) K_c
 //
-// Every row of W (and S) evolves independently of the others (its error only
-// involves that row), so one CTA owns a slice of 16 rows of one sequence's
-// memory and runs the whole sequence; the grid covers (sequence, slice).
+// Serial chain.  Substituting the carry into the next chunk's errors gives
 //
-// The per-chunk coefficients depend only on the gates, so a pre-pass kernel
-// (one warp per sequence and chunk) writes them into the caller's workspace:
-// the 64 x 64 matrix C (fp32) and the vectors beta_t, c_t, C[n-1][s],
-// Pm[n-1][s] and the chunk-end scalars.  The scan kernel copies each chunk's
-// record into its pipeline stage next to the K, Q and V tiles.
+//   E_{c+1} = beta_n K_{c+1} W_c^T + c_n K_{c+1} S_c^T
+//             - 2 (K_{c+1} K_c^T diag(C[n])) E_c - V_{c+1},
 //
-// Roles inside a CTA of the scan kernel (256 threads):
-//   warps 0-3  chain.  Thread j holds W[r0..r0+15][j] and S[r0..r0+15][j] in
-//              fp32 registers for the whole sequence.  Warps 0-1 (thread =
-//              token) turn K W^T into the errors and the scaled error
-//              operands; all four apply the state carry; warp 0 issues the
-//              two chain MMAs itself after named barriers.
-//   warp 4     producer: TMA loads of K, Q (128-byte swizzle) and the V
-//              slice, bulk copy of the coefficient record.
-//   warp 5     read-side MMA issuer (scores two chunks ahead, corrections)
-//              and TMEM owner.
-//   warps 6-9  weight the scores by C (warp w takes the 16 tokens of TMEM
-//              sub-partition w % 4); warps 6-7 then form the outputs z.
+// whose first two terms only need the state at the start of chunk c and whose
+// matrix M_c = K_{c+1} K_c^T diag(C[n]) only needs the inputs.  So the chain
+// from one chunk's errors to the next is a single tensor-core product M_c E_c
+// plus an elementwise epilogue; the state carry itself (an MMA and a register
+// update) runs beside it, one chunk ahead of where its result is needed.
 //
-// Tensor-core contractions per chunk (A operands are M = 128 rows: the K tile
-// and the Q tile are stacked so one instruction covers both):
-//   MMA1  [K;Q] . [W;S]^T      -> K W^T (errors), Q W^T, Q S^T     (chain)
-//   MMA2  K^T . [C_n E^T | Pm_n E^T] -> the state updates           (chain)
-//   MMAqk [K;Q] . K^T          -> Q K^T (scores), one chunk ahead
-//   MMAz  A~ . E^T             -> the causal correction of the reads
-// Operands are bf16, accumulators fp32 in tensor memory; the fp32 state
-// masters never leave registers.
+// Stacked operands.  The queries of chunk c and the keys of chunk c+1 sit next
+// to each other in shared memory (a ring of [K_0][Q_0][K_1][Q_1]... tiles with
+// the first key tile duplicated at the end), so one 128-row A operand
+// [Q_c; K_{c+1}] serves
+//   scores  [Q_c; K_{c+1}] K_c^T       -> A~_c = mask(Q K^T) o C and M_c
+//   state   [Q_c; K_{c+1}] [W_c; S_c]^T -> Q W^T, Q S^T (reads) and the two
+//                                          state terms of E_{c+1}
+// and the chain product [A~_c; M_c] E_c gives the read correction of chunk c
+// and the recursion term of E_{c+1} in one go.
+//
+// Every row of W (and S) evolves independently of the others, so one CTA owns
+// a slice of 16 rows of one sequence's memory and runs the whole sequence; the
+// grid covers (sequence, slice).  The per-chunk coefficients depend only on
+// the gates and come from a pre-pass kernel (one warp per sequence and chunk)
+// through the caller's workspace.
+//
+// Roles inside a CTA (416 threads):
+//   warps 0-3   state: thread j holds column j of the 16 W rows and 16 S rows
+//               in fp32 registers, applies the carry and writes the bf16 copy
+//               [W; S] for the state MMA, which warp 0 issues.
+//   warps 4-5   outputs z (token = TMEM lane 0-63).
+//   warps 6-7   error chain (token of the next chunk = TMEM lane 64-127);
+//               warp 6 issues the chain MMA, warp 7 then the carry MMA.
+//   warps 8-11  score weighting (TMEM sub-partition = warp % 4); warp 8
+//               issues the score MMAs ahead of the chain.
+//   warp 12     producer: TMA loads of K, Q, the V slice and the coefficient
+//               vectors.
 //
 // Every wait is bounded: a wait that exceeds its limit sets the device status
-// word to TTM_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are
-// drained, TMEM is freed and the kernel returns.
+// word to TTM_ERR_TIMEOUT, every role runs out its loop doing no further work
+// (named barriers stay balanced), in-flight copies and MMAs are drained, TMEM
+// is freed and the kernel returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -65,64 +72,63 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 416;
+constexpr int kNS = 3;          // pipeline stages
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM column map
-constexpr uint32_t kAcc1 = 0;     // 2 x 32 columns: [K W^T | K S^T] on lanes 0-63, [Q W^T | Q S^T] on 64-127
-constexpr uint32_t kAcc2 = 64;    // 32 columns: W / S updates (lane = d_k index)
-constexpr uint32_t kAccQK = 128;  // 3 x 64 columns: Q K^T (M = 64 layout: 16 tokens per sub-partition)
-constexpr uint32_t kAccZ = 320;   // 2 x 16 columns: A~ E^T on lanes 64-127
+// TMEM column map (M = 128 accumulators: row = TMEM lane)
+constexpr uint32_t kAcc1 = 0;     // 2 x 32: [Q_c; K_{c+1}] [W_c; S_c]^T
+constexpr uint32_t kAccS = 64;    // 2 x 64: [Q_c; K_{c+1}] K_c^T (raw scores)
+constexpr uint32_t kAcc2 = 192;   // 2 x 32: K_c^T [C E | Pm E] (lane = d_k index)
+constexpr uint32_t kAcc3 = 256;   // 2 x 16: [A~_c; M_c] E_c
 
-// Per-chunk coefficient record (workspace and pipeline stage).  C[t][s] =
-// theta_s w(s,t) (zero above the diagonal) is stored row-major in fp32 with
-// the 16-byte chunks of row t XOR-permuted by t % 16, so that 32 threads
-// reading 32 different rows stay free of bank conflicts.
+// Per-chunk coefficient record (workspace, staged whole into shared memory).
+// C[t][s] = theta_s w(s,t) (zero above the diagonal) in fp32, row t at
+// t * 256 bytes with its sixteen 16-byte groups XOR-permuted by t % 16 (so the
+// weighting threads, one row each, read without bank conflicts), then vectors
+// over the chunk's tokens and four scalars.
 constexpr uint32_t kRecC = 0;                    // 64 x 64 fp32
-constexpr uint32_t kRecBeta = 16384;             // beta_t
-constexpr uint32_t kRecCvec = kRecBeta + 256;    // c_t
-constexpr uint32_t kRecCend = kRecCvec + 256;    // C[n-1][s]
-constexpr uint32_t kRecPend = kRecCend + 256;    // theta_s m(s, n-1)
-constexpr uint32_t kRecScal = kRecPend + 256;    // beta_{n-1}, c_{n-1}, P_{n-1}, n
-constexpr uint32_t kRecBytes = kRecScal + 16;    // 17424 (a multiple of 16)
+constexpr uint32_t kVBeta = 16384;               // beta_t
+constexpr uint32_t kVCvec = kVBeta + 256;        // c_t
+constexpr uint32_t kVCend = kVBeta + 512;        // C[n-1][s]
+constexpr uint32_t kVPend = kVBeta + 768;        // theta_s m(s, n-1)
+constexpr uint32_t kVScal = kVBeta + 1024;       // beta_{n-1}, c_{n-1}, P_{n-1}, n
+constexpr uint32_t kRecBytes = kVScal + 16;      // 17424 (a multiple of 16)
+constexpr uint32_t kVecSlot = 17472;             // staged copy, 64-byte aligned slots
 
 __host__ __device__ constexpr uint32_t c_offset(int t, int s) {
     return (uint32_t)t * 256u + (uint32_t)(((s >> 2) ^ (t & 15)) << 4) + (uint32_t)(s & 3) * 4u;
 }
 
+constexpr uint32_t kTile = 8192;                          // 64 rows x 128 bytes
+constexpr uint32_t kRingBytes = (2 * kNS + 1) * kTile;    // [K_0][Q_0]...[K_2][Q_2][K_0 copy]
+
 struct Layout {
-    int D, NS;
-    uint32_t kq_bytes, off_v, off_rec, stage_bytes;
-    uint32_t off_ws, off_b2, off_at0, off_et0, off_at1, off_et1, total;
+    uint32_t off_ete, off_ring, off_am, off_etcp, off_ws, off_v, off_rec, total;
 };
 
-// Shared-memory map.  Each A~ tile (8 KB, the 64 rows of the scores) is
-// preceded by another 8 KB buffer: its MMA reads 128 rows starting 8 KB
-// earlier and only the upper 64 rows of that product are used.
+// Shared-memory map.  The error tile E (8 KB) sits right before the key /
+// query ring, so the first state MMA, whose A operand starts one tile before
+// the first key tile, reads valid memory.
 __host__ __device__ constexpr Layout make_layout(int D) {
     Layout L{};
-    L.D = D;
-    L.NS = D == 128 ? 3 : 4;
-    L.kq_bytes = (D / 64) * 16384u;   // per 64-column half: K (8 KB) then Q (8 KB)
-    L.off_v = L.kq_bytes;             // V slice, 64 x 16 bf16
-    L.off_rec = L.kq_bytes + 2048u;   // coefficient record
-    L.stage_bytes = (L.off_rec + kRecBytes + 1023u) & ~1023u;
-    uint32_t off = L.NS * L.stage_bytes;
-    L.off_ws = off;  off += D * 128u;        // [W;S] operand, row = d_k index
-    L.off_b2 = off;  off += kChunk * 128u;   // [C E^T | Pm E^T], row = token
-    L.off_at0 = off; off += kChunk * 128u;   // A~ (chunk parity 0)
-    L.off_et0 = off; off += kChunk * 128u;   // E^T (chunk parity 0)
-    L.off_at1 = off; off += kChunk * 128u;
-    L.off_et1 = off; off += kChunk * 128u;
+    uint32_t off = 0;
+    L.off_ete = off;  off += kTile;                        // E_c [t][r] (16 of 64 columns)
+    L.off_ring = off; off += (D / 64) * kRingBytes;       // one ring per 64-column half
+    L.off_am = off;   off += 2 * kTile;                    // [A~; M] [128 rows][s]
+    L.off_etcp = off; off += 2 * kTile;                    // 2 x [C E | Pm E] [t][r'] (32 columns)
+    L.off_ws = off;   off += (D / 64) * 4096;              // [W; S] bf16, 32 rows per half
+    L.off_v = off;    off += kNS * 2048;                   // V slice [t][16]
+    L.off_rec = off;  off += kNS * kVecSlot;               // coefficient record
     L.total = off;
     return L;
 }
 
 struct Bars {
-    uint64_t full[4], empty[4];
-    uint64_t mma1_done[2], mma2_done[2], acc1_free[2], at_ready[2], z_done[2], accz_free[2];
-    uint64_t qk_done[3], qk_free[3];
-    uint64_t drain;
+    uint64_t full[kNS], empty[kNS];
+    uint64_t acc1_ready[2], acc1_free[2], sc_ready[2], am_ready;
+    uint64_t mma3_done[2], acc3_free[2], mma2_done[2], acc2_free[2], mma3_issued;
+    uint64_t drain[4];
     uint32_t tmem_base;
     int abort;
 };
@@ -134,12 +140,13 @@ struct TcParams {
 
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
-// Bounded wait that also gives up once another role has aborted.
-__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+// Bounded wait that also gives up once another role has aborted (the slow
+// path, out of line: ~25 call sites share one copy of it).
+__device__ __noinline__ bool wait_bar_slow(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
     const long long t0 = clock64();
     uint32_t polls = 0;
-    while (!mbar_try_wait(bar, parity)) {
-        if ((++polls & 63u) == 0) {
+    while (!mbar_try_wait_sleep(bar, parity, 20000)) {
+        if ((++polls & 3u) == 0) {
             if (*(volatile int*)&B->abort) return false;
             if (clock64() - t0 > kWaitCycles) {
                 *(volatile int*)&B->abort = 1;
@@ -151,10 +158,29 @@ __device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity
     return true;
 }
 
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;   // already complete: no clock, no loop
+    return wait_bar_slow(B, bar, parity, status);
+}
+
 // Warp-uniform variant: every lane of the warp gets the same answer, so a
 // timeout seen by one lane never splits the warp before a .sync.aligned op.
+// A converged warp reads the phase once for all lanes, so a completed phase
+// needs only the vote.
+__device__ __noinline__ bool wait_all_slow(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    return __all_sync(0xffffffffu, wait_bar_slow(B, bar, parity, status));
+}
+
 __device__ __forceinline__ bool wait_all(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
-    return __all_sync(0xffffffffu, wait_bar(B, bar, parity, status));
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return wait_all_slow(B, bar, parity, status);
+}
+
+// Wait used while draining: ignores the abort flag, gives up after the limit.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) break;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -173,6 +199,20 @@ __device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int col, const 
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, col)) = v;
 }
 
+__device__ __forceinline__ void unpack8(uint4 v, float* x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// Use index of a double-buffered slot by chunk x >= -1 (slot x & 1): chunks
+// -1, 1, 3, ... and 0, 2, 4, ... count up separately.
+__device__ __forceinline__ uint32_t use_parity(int x) { return (uint32_t)(((x + 1) >> 1) & 1); }
+
 // ---------------------------------------------------------------- warp scans
 
 // Inclusive scan of affine maps x -> A x + B along lanes (lane order = token
@@ -188,16 +228,6 @@ __device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
         }
     }
 }
-
-// ------------------------------------------------------- coefficient warp
-
-// One warp computes all coefficients of one chunk of n tokens from its raw
-// gates g; it first makes the padded tokens neutral in place (eta 1,
-// alpha 0; theta is masked where read):
-//  * forward scans (lane l owns tokens 2l, 2l+1): beta_t = prod keep,
-//    P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
-//  * the matrix C[t][s] = theta_s w(s,t) with, per column s, the forward
-//    recurrences m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
 
 // ------------------------------------------------------- coefficient pre-pass
 
@@ -222,6 +252,7 @@ __global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, in
     const int n = min(kChunk, T - c * kChunk);
     const size_t tok0 = (size_t)seq * T + (size_t)c * kChunk;
     uint8_t* rec = static_cast<uint8_t*>(a.workspace) + (size_t)wid * kRecBytes;
+    uint8_t* vec = rec;
 
     auto eta_at = [&](int t) { return t < n ? (a.eta ? a.eta[tok0 + t] : 0.f) : 1.f; };
     auto keep_at = [&](int t) { return t < n ? 1.f - (a.alpha ? a.alpha[tok0 + t] : 0.f) : 1.f; };
@@ -244,16 +275,14 @@ __global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, in
     float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);
     if (lane == 0) cpre = 0.f;
     const float c0 = kp0 * cpre + P0, c1 = kp1 * c0 + P1;
-    float* beta = reinterpret_cast<float*>(rec + kRecBeta);
-    float* cvec = reinterpret_cast<float*>(rec + kRecCvec);
-    reinterpret_cast<float2*>(beta)[lane] = make_float2(beta0, beta1);
-    reinterpret_cast<float2*>(cvec)[lane] = make_float2(c0, c1);
+    reinterpret_cast<float2*>(vec + kVBeta)[lane] = make_float2(beta0, beta1);
+    reinterpret_cast<float2*>(vec + kVCvec)[lane] = make_float2(c0, c1);
     const int ln = (n - 1) >> 1, un = (n - 1) & 1;
     const float bn = __shfl_sync(0xffffffffu, un ? beta1 : beta0, ln);
     const float cn = __shfl_sync(0xffffffffu, un ? c1 : c0, ln);
     const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
     if (lane == 0)
-        *reinterpret_cast<float4*>(rec + kRecScal) = make_float4(bn, cn, Pn, (float)n);
+        *reinterpret_cast<float4*>(vec + kVScal) = make_float4(bn, cn, Pn, (float)n);
 
     // C matrix
     const int s0 = lane, s1 = lane + 32;
@@ -282,8 +311,8 @@ __global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, in
             ce1 = v1;
         }
     }
-    float* cend = reinterpret_cast<float*>(rec + kRecCend);
-    float* pend = reinterpret_cast<float*>(rec + kRecPend);
+    float* cend = reinterpret_cast<float*>(vec + kVCend);
+    float* pend = reinterpret_cast<float*>(vec + kVPend);
     cend[s0] = ce0;
     cend[s1] = ce1;
     pend[s0] = th0 * m0;
@@ -302,6 +331,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     __shared__ Bars bars;
     Bars* B = &bars;
     constexpr Layout L = make_layout(D);
+    constexpr int NH = D / 64;         // 64-column halves
+    constexpr int KS = D / 16;         // K steps over d
     const LinearArgs& a = P.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slice = blockIdx.x % P.nslices;
@@ -311,52 +342,62 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const int T = a.T;
     const int nch = (T + kChunk - 1) / kChunk;
     int* status = a.status;
+    const uint8_t* recs = static_cast<const uint8_t*>(a.workspace) + (size_t)seq * nch * kRecBytes;
 
-    auto stage = [&](int s) { return sm + s * L.stage_bytes; };
-    auto vtile = [&](int s) { return stage(s) + L.off_v; };
-    auto rec = [&](int s) { return stage(s) + L.off_rec; };
-    auto recf = [&](int s, uint32_t off) { return reinterpret_cast<const float*>(rec(s) + off); };
+    auto ring = [&](int h) { return sm + L.off_ring + h * kRingBytes; };
+    auto ktile = [&](int h, int s) { return ring(h) + 2 * s * kTile; };
+    auto qtile = [&](int h, int s) { return ring(h) + (2 * s + 1) * kTile; };
+    auto vtile = [&](int s) { return sm + L.off_v + s * 2048; };
+    auto vec = [&](int s) { return sm + L.off_rec + s * kVecSlot; };
+    auto vecf = [&](int s, uint32_t off) { return reinterpret_cast<const float*>(vec(s) + off); };
+    uint8_t* amt = sm + L.off_am;
+    uint8_t* ete = sm + L.off_ete;
+    auto etcp = [&](int b) { return sm + L.off_etcp + b * kTile; };
     uint8_t* ws = sm + L.off_ws;
-    uint8_t* b2 = sm + L.off_b2;
-    auto et = [&](int b) { return sm + (b ? L.off_et1 : L.off_et0); };
-    auto at = [&](int b) { return sm + (b ? L.off_at1 : L.off_at0); };
 
     if (tid == 0) {
-        for (int s = 0; s < L.NS; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(&B->full[s], 1);
-            // chain 128 + read side 128 + chain MMA commit 1 + score MMA commit 1
-            mbar_init(&B->empty[s], 128 + 128 + 1 + 1);
+            mbar_init(&B->empty[s], 2);          // outputs + state
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&B->mma1_done[b], 1);
+            mbar_init(&B->acc1_ready[b], 1);
+            mbar_init(&B->acc1_free[b], 128);    // error chain 64 + outputs 64
+            mbar_init(&B->sc_ready[b], 1);
+            mbar_init(&B->mma3_done[b], 1);
+            mbar_init(&B->acc3_free[b], 128);    // error chain 64 + outputs 64
             mbar_init(&B->mma2_done[b], 1);
-            mbar_init(&B->acc1_free[b], 64);
-            mbar_init(&B->at_ready[b], 128);
-            mbar_init(&B->z_done[b], 1);
-            mbar_init(&B->accz_free[b], 64);
+            mbar_init(&B->acc2_free[b], 128);    // state warps
         }
-        for (int b = 0; b < 3; ++b) {
-            mbar_init(&B->qk_done[b], 1);
-            mbar_init(&B->qk_free[b], 128);
-        }
-        mbar_init(&B->drain, 1);
+        mbar_init(&B->am_ready, 128);            // weighting warps
+        mbar_init(&B->mma3_issued, 1);           // chain MMA queued (carry MMA goes after it)
+        for (int i = 0; i < 4; ++i) mbar_init(&B->drain[i], 1);
         B->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&B->tmem_base, kTmemCols);
+    if (warp == 4) tmem_alloc(&B->tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);   // this warp's TMEM lanes
 
-    const uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);
-    const uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);
+    // [Q_c; K_{c+1}] K-major operand address for K step kk (c = -1: the rows
+    // before the first key tile, whose products are never read)
+    auto qk_a = [&](int c, int kk) -> uint32_t {
+        const int h = kk >> 2;
+        const uint8_t* base = c < 0 ? ktile(h, 0) - kTile : qtile(h, c % kNS);
+        return smem_u32(base) + (kk & 3) * 32;
+    };
+    constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 0);   // state MMA
+    constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);   // scores
+    constexpr uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);   // carry: A = K^T, B = [C E | Pm E]
+    constexpr uint32_t id3 = idesc_bf16_f32(128, 16, 0, 1);   // chain: [A~; M] E
 
     if (warp < 4) {
-        // ----------------------------------------------------- chain warps
+        // ------------------------------------------------------------ state
         // Every thread runs every iteration and reaches every named barrier,
-        // also after an abort (then it only skips work), so the barriers
-        // stay balanced.
+        // also after an abort (then it only skips work).
         const int j = tid;
         const bool own = j < D;
         const size_t init = (size_t)(a.shared ? 0 : bb) * a.H + hh;
@@ -369,29 +410,29 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         auto write_ws = [&]() {
             if (!own) return;
+            uint8_t* t = ws + (j >> 6) * 4096;
+            const int col = j & 63;
 #pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) st_chunk(ws, j, 8 * c8, w + 8 * c8);
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) st_chunk(ws, j, 16 + 8 * c8, s + 8 * c8);
+            for (int i = 0; i < kRows; ++i) {
+                *reinterpret_cast<__nv_bfloat16*>(t + sw128_offset(i, col)) = __float2bfloat16_rn(w[i]);
+                *reinterpret_cast<__nv_bfloat16*>(t + sw128_offset(16 + i, col)) = __float2bfloat16_rn(s[i]);
+            }
         };
-        const uint32_t ws_a = smem_u32(ws), b2_a = smem_u32(b2);
-        // MMA1(c): [K;Q] . [W;S]^T, issued by warp 0 once [W;S] is in place
-        auto issue_mma1 = [&](int c, bool ok) -> bool {
-            if (warp != 0 || nch == 0) return ok;
-            const int st = c % L.NS, b = c & 1;
-            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (ok && c >= 2) ok = wait_all(B, &B->acc1_free[b], ((c - 2) >> 1) & 1, status);
+        // state MMA of chunk x (x = -1, 0 use the initial state)
+        auto issue_state = [&](int x, bool ok) -> bool {
+            if (warp != 0) return ok;
+            if (ok && x >= 0) ok = wait_all(B, &B->full[x % kNS], (x / kNS) & 1, status);
+            if (ok && x + 1 < nch) ok = wait_all(B, &B->full[(x + 1) % kNS], ((x + 1) / kNS) & 1, status);
+            if (ok && x >= 1) ok = wait_all(B, &B->acc1_free[x & 1], use_parity(x - 2), status);
             if (!ok) return false;
             tc_fence_after();
-            const uint32_t base = smem_u32(stage(st));
+            const uint32_t wsa = smem_u32(ws);
             if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ad = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + kAcc1 + b * 32, sdesc(ad, 16, 1024, 2),
-                             sdesc(ws_a + kk * 2048, 8192, 1024, 2), id1, kk > 0);
-                }
-                mma_commit(&B->mma1_done[b]);
+#pragma unroll 1
+                for (int kk = 0; kk < KS; ++kk)
+                    mma_bf16(tmem + kAcc1 + (x & 1) * 32, sdesc(qk_a(x, kk), 16, 1024, 2),
+                             sdesc(wsa + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2), id1, kk > 0);
+                mma_commit(&B->acc1_ready[x & 1]);
             }
             __syncwarp();
             return true;
@@ -399,95 +440,45 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         write_ws();
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        bool ok = issue_mma1(0, true);
+        bool ok = issue_state(-1, true);
+        ok = issue_state(0, ok);
         for (int c = 0; c < nch; ++c) {
-            const int st = c % L.NS, b = c & 1;
-            if (ok) ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (warp < 2) {
-                // Epi1: errors of token t at the chunk-start state
-                const int t = j;
-                if (ok) ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
-                if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
-                if (ok) {
-                    const float ce = recf(st, kRecCend)[t], pe = recf(st, kRecPend)[t];
-                    tc_fence_after();
-                    float kw[16];
-                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc1 + b * 32), kw);
-                    const uint4* vrow = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
-                    const uint4 v0 = vrow[0], v1 = vrow[1];
-                    tmem_wait_ld();
-                    const __nv_bfloat162* vb0 = reinterpret_cast<const __nv_bfloat162*>(&v0);
-                    const __nv_bfloat162* vb1 = reinterpret_cast<const __nv_bfloat162*>(&v1);
-                    float e[16], ec[16], ep[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f0 = __bfloat1622float2(vb0[i]);
-                        const float2 f1 = __bfloat1622float2(vb1[i]);
-                        e[2 * i] = kw[2 * i] - f0.x;
-                        e[2 * i + 1] = kw[2 * i + 1] - f0.y;
-                        e[8 + 2 * i] = kw[8 + 2 * i] - f1.x;
-                        e[8 + 2 * i + 1] = kw[8 + 2 * i + 1] - f1.y;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        ec[i] = ce * e[i];
-                        ep[i] = pe * e[i];
-                    }
-                    st_chunk(b2, t, 0, ec);
-                    st_chunk(b2, t, 8, ec + 8);
-                    st_chunk(b2, t, 16, ep);
-                    st_chunk(b2, t, 24, ep + 8);
-                    st_chunk(et(b), t, 0, e);
-                    st_chunk(et(b), t, 8, e + 8);
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                }
-                named_bar_sync(2, 64);
-                // MMA2(c): K^T . [C E^T | Pm E^T]
-                if (warp == 0 && ok) {
-                    tc_fence_after();
-                    const uint32_t base = smem_u32(stage(st));
-                    if (elect_one()) {
-#pragma unroll
-                        for (int kk = 0; kk < kChunk / 16; ++kk)
-                            mma_bf16(tmem + kAcc2,
-                                     sdesc(base + kk * 2048, D == 128 ? 16384 : 8192, 1024, 2),
-                                     sdesc(b2_a + kk * 2048, 8192, 1024, 2), id2, kk > 0);
-                        mma_commit(&B->mma2_done[b]);
-                        mma_commit(&B->empty[st]);
-                    }
-                    __syncwarp();
-                }
-            }
-            // Epi2: state carry
+            const int b = c & 1, st = c % kNS;
+            if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
             if (ok) ok = wait_all(B, &B->mma2_done[b], (c >> 1) & 1, status);
             if (ok) {
-                const float* sc = recf(st, kRecScal);
-                const float bn = sc[0], cn = sc[1], Pn = sc[2];
-                mbar_arrive(&B->empty[st]);
                 tc_fence_after();
+                float uw[16], us[16];
+                tmem_ld16(tl + kAcc2 + b * 32, uw);
+                tmem_ld16(tl + kAcc2 + b * 32 + 16, us);
+                const float4 sc = *reinterpret_cast<const float4*>(vec(st) + kVScal);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&B->acc2_free[b]);
+                // the carry MMA (the last reader of K_c) is complete and the
+                // scalars are in registers: this role is done with the stage
+                if (tid == 0) mbar_arrive(&B->empty[st]);
                 if (own) {
-                    float uw[16], us[16];
-                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2), uw);
-                    tmem_ld16(tmem_addr(tmem, warp * 32, kAcc2 + 16), us);
-                    tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < kRows; ++i) {
-                        const float wn = bn * w[i] + cn * s[i] - 2.f * uw[i];
-                        s[i] = Pn * s[i] - 2.f * us[i];
+                        const float wn = sc.x * w[i] + sc.y * s[i] - 2.f * uw[i];
+                        s[i] = sc.z * s[i] - 2.f * us[i];
                         w[i] = wn;
                     }
                 }
                 if (c + 1 < nch) {
-                    write_ws();
-                    fence_proxy_async_smem();
+                    // the state MMA of chunk c still reads the previous copy
+                    ok = wait_all(B, &B->acc1_ready[b], use_parity(c), status);
+                    if (ok) {
+                        write_ws();
+                        fence_proxy_async_smem();
+                    }
                 }
-                tc_fence_before();
             }
             named_bar_sync(1, 128);
-            if (c + 1 < nch) ok = issue_mma1(c + 1, ok);
+            if (c + 1 < nch) ok = issue_state(c + 1, ok);
         }
-        if (own) {
+        if (own && ok) {
             const size_t dst = (size_t)seq * D * D;
 #pragma unroll
             for (int i = 0; i < kRows; ++i) {
@@ -495,194 +486,259 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 if (a.S_out) a.S_out[dst + (size_t)(r0 + i) * D + j] = s[i];
             }
         }
-    } else if (warp == 4) {
+    } else if (warp < 6) {
+        // ---------------------------------------------------------- outputs
+        const int t = tid - 128;                 // token = TMEM lane 0..63
+        bool ok = true;
+        mbar_arrive(&B->acc1_free[1]);           // the chunk -1 state product has no reads
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1, st = c % kNS;
+            if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
+            if (ok) ok = wait_all(B, &B->acc1_ready[b], use_parity(c), status);
+            if (ok) ok = wait_all(B, &B->mma3_done[b], (c >> 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                float qw[16], qs[16], ae[16];
+                tmem_ld16(tl + kAcc1 + b * 32, qw);
+                tmem_ld16(tl + kAcc1 + b * 32 + 16, qs);
+                tmem_ld16(tl + kAcc3 + b * 16, ae);
+                const float bt = vecf(st, kVBeta)[t], ct = vecf(st, kVCvec)[t];
+                const int n = (int)vecf(st, kVScal)[3];
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&B->acc1_free[b]);
+                mbar_arrive(&B->acc3_free[b]);
+                if (t < n) {
+                    float zz[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) zz[i] = bt * qw[i] + ct * qs[i] - 2.f * ae[i];
+                    uint4 o0, o1;
+                    o0.x = pack_bf16(zz[0], zz[1]);   o0.y = pack_bf16(zz[2], zz[3]);
+                    o0.z = pack_bf16(zz[4], zz[5]);   o0.w = pack_bf16(zz[6], zz[7]);
+                    o1.x = pack_bf16(zz[8], zz[9]);   o1.y = pack_bf16(zz[10], zz[11]);
+                    o1.z = pack_bf16(zz[12], zz[13]); o1.w = pack_bf16(zz[14], zz[15]);
+                    __nv_bfloat16* zr = static_cast<__nv_bfloat16*>(a.z) +
+                                        ((size_t)seq * T + (size_t)c * kChunk + t) * D + r0;
+                    reinterpret_cast<uint4*>(zr)[0] = o0;
+                    reinterpret_cast<uint4*>(zr)[1] = o1;
+                }
+            }
+            named_bar_sync(3, 64);
+            if (tid == 128 && ok) mbar_arrive(&B->empty[st]);
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------ error chain
+        // Thread t' produces row t' of E_x for x = 0, 1, ...: from the state
+        // product of chunk x-1 (lanes 64-127: K_x W^T, K_x S^T) and, for
+        // x >= 1, the chain product M_{x-1} E_{x-1}.
+        const int t = tid - 192;                 // token = TMEM lane 64 + t
+        bool ok = true;
+        float bn = 1.f, cn = 0.f;                // carry coefficients of chunk x-1
+        for (int x = 0; x < nch; ++x) {
+            const int st = x % kNS, pb = (x - 1) & 1;
+            if (ok) ok = wait_all(B, &B->full[st], (x / kNS) & 1, status);
+            if (ok) ok = wait_all(B, &B->acc1_ready[pb], use_parity(x - 1), status);
+            if (ok && x >= 1) ok = wait_all(B, &B->mma3_done[pb], ((x - 1) >> 1) & 1, status);
+            float e[16];
+            if (ok) {
+                tc_fence_after();
+                float f[16], g[16], m[16];
+                tmem_ld16(tl + kAcc1 + pb * 32, f);
+                tmem_ld16(tl + kAcc1 + pb * 32 + 16, g);
+                if (x >= 1) tmem_ld16(tl + kAcc3 + pb * 16, m);
+                float v[16];
+                {
+                    const uint4* vr = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
+                    unpack8(vr[0], v);
+                    unpack8(vr[1], v + 8);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&B->acc1_free[pb]);
+                if (x >= 1) {
+                    mbar_arrive(&B->acc3_free[pb]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) e[i] = bn * f[i] + cn * g[i] - 2.f * m[i] - v[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) e[i] = f[i] - v[i];
+                }
+                const float4 sc = *reinterpret_cast<const float4*>(vec(st) + kVScal);
+                const float ce = vecf(st, kVCend)[t], pe = vecf(st, kVPend)[t];
+                bn = sc.x;
+                cn = sc.y;
+                // the carry MMA of chunk x-2 read this [C E | Pm E] buffer; the
+                // chain MMA of chunk x-1 (complete) read the E tile
+                if (x >= 2) ok = wait_all(B, &B->mma2_done[x & 1], ((x - 2) >> 1) & 1, status);
+                if (ok) {
+                    float ec[16], ep[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        ec[i] = ce * e[i];
+                        ep[i] = pe * e[i];
+                    }
+                    st_chunk(ete, t, 0, e);
+                    st_chunk(ete, t, 8, e + 8);
+                    uint8_t* cp = etcp(x & 1);
+                    st_chunk(cp, t, 0, ec);
+                    st_chunk(cp, t, 8, ec + 8);
+                    st_chunk(cp, t, 16, ep);
+                    st_chunk(cp, t, 24, ep + 8);
+                    fence_proxy_async_smem();
+                }
+            }
+            named_bar_sync(2, 64);
+            // chain MMA of chunk x (warp 6), then the carry MMA (warp 7), so the
+            // chain product is first in the tensor pipe and warp 6 is free to
+            // wait for it at once
+            const int b = x & 1;
+            if (warp == 6) {
+                if (ok) ok = wait_all(B, &B->am_ready, x & 1, status);
+                if (ok && x >= 2) ok = wait_all(B, &B->acc3_free[b], ((x - 2) >> 1) & 1, status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t am = smem_u32(amt), et = smem_u32(ete);
+                    if (elect_one()) {
+#pragma unroll 1
+                        for (int kk = 0; kk < kChunk / 16; ++kk)
+                            mma_bf16(tmem + kAcc3 + b * 16, sdesc(am + kk * 32, 16, 1024, 2),
+                                     sdesc(et + kk * 2048, 8192, 1024, 2), id3, kk > 0);
+                        mma_commit(&B->mma3_done[b]);
+                        mbar_arrive(&B->mma3_issued);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                if (ok) ok = wait_all(B, &B->mma3_issued, x & 1, status);
+                if (ok && x >= 2) ok = wait_all(B, &B->acc2_free[b], ((x - 2) >> 1) & 1, status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t ecp = smem_u32(etcp(b)), kb = smem_u32(ktile(0, st));
+                    if (elect_one()) {
+#pragma unroll 1
+                        for (int kk = 0; kk < kChunk / 16; ++kk)
+                            mma_bf16(tmem + kAcc2 + b * 32,
+                                     sdesc(kb + kk * 2048, D == 128 ? kRingBytes : kTile, 1024, 2),
+                                     sdesc(ecp + kk * 2048, 8192, 1024, 2), id2, kk > 0);
+                        mma_commit(&B->mma2_done[b]);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    } else if (warp < 12) {
+        // -------------------------------------------------------- weighting
+        // Row m of the scores: m < 64 -> A~[m][s] = C[m][s] (q_m . k_s) with
+        // row m of the chunk's coefficient table; m >= 64 ->
+        // M[m-64][s] = C[n-1][s] (k'_{m-64} . k_s).
+        const int m = (warp & 3) * 32 + lane;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int b = c & 1, st = c % kNS;
+            if (warp == 8) {
+                if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
+                if (ok && c + 1 < nch)
+                    ok = wait_all(B, &B->full[(c + 1) % kNS], ((c + 1) / kNS) & 1, status);
+                if (ok) {
+                    tc_fence_after();
+                    if (elect_one()) {
+#pragma unroll 1
+                        for (int kk = 0; kk < KS; ++kk)
+                            mma_bf16(tmem + kAccS + b * 64, sdesc(qk_a(c, kk), 16, 1024, 2),
+                                     sdesc(smem_u32(ktile(kk >> 2, st)) + (kk & 3) * 32, 16, 1024, 2),
+                                     idS, kk > 0);
+                        mma_commit(&B->sc_ready[b]);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (ok && warp != 8) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
+            if (ok) ok = wait_all(B, &B->sc_ready[b], (c >> 1) & 1, status);
+            // the chain MMA of chunk c-1 reads the previous contents of the tile
+            if (ok && c >= 1) ok = wait_all(B, &B->mma3_done[(c - 1) & 1], ((c - 1) >> 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                // weights of this row: row m of the table (m < 64) or C[n-1][.]
+                const float* wrow = m < 64 ? vecf(st, kRecC + m * 256) : vecf(st, kVCend);
+                const int sw = m < 64 ? (m & 15) : 0;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float r[16], wt[16];
+                    tmem_ld16(tl + kAccS + b * 64 + 16 * q4, r);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float4 f = *reinterpret_cast<const float4*>(wrow + (((4 * q4 + g) ^ sw) << 2));
+                        wt[4 * g] = f.x;
+                        wt[4 * g + 1] = f.y;
+                        wt[4 * g + 2] = f.z;
+                        wt[4 * g + 3] = f.w;
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] *= wt[i];
+                    st_chunk(amt, m, 16 * q4, r);
+                    st_chunk(amt, m, 16 * q4 + 8, r + 8);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&B->am_ready);
+            }
+            named_bar_sync(4, 128);
+        }
+    } else {
         // --------------------------------------------------------- producer
         if (lane == 0) {
-            const uint32_t tx = L.kq_bytes + kChunk * kRows * 2 + kRecBytes;
-            const uint8_t* recs = static_cast<const uint8_t*>(a.workspace) +
-                                  (size_t)seq * nch * kRecBytes;
+            // tiles of chunk c are requested into L2 kPrefetch chunks before
+            // their load, so the load itself is an L2 hit
+            constexpr int kPrefetch = 4;
+            auto prefetch = [&](int c) {
+                if (c >= nch) return;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    tma_prefetch_l2_3d(&kmap, 64 * h, c * kChunk, seq);
+                    tma_prefetch_l2_3d(&qmap, 64 * h, c * kChunk, seq);
+                }
+                tma_prefetch_l2_3d(&vmap, r0, c * kChunk, seq);
+                bulk_prefetch_l2(recs + (size_t)c * kRecBytes, kRecBytes);
+            };
+            for (int c = 0; c < kPrefetch; ++c) prefetch(c);
             int issued = 0;
             for (int c = 0; c < nch; ++c) {
-                const int st = c % L.NS;
-                if (c >= L.NS && !wait_bar(B, &B->empty[st], ((c / L.NS) - 1) & 1, status)) break;
+                const int st = c % kNS;
+                prefetch(c + kPrefetch);
+                if (c >= kNS && !wait_bar(B, &B->empty[st], ((c / kNS) - 1) & 1, status)) break;
+                const uint32_t tx = (st == 0 ? 3 : 2) * NH * kTile + kChunk * kRows * 2 + kRecBytes;
                 mbar_expect_tx(&B->full[st], tx);
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    tma_load_3d(stage(st) + h * 16384, &kmap, &B->full[st], 64 * h, c * kChunk, seq);
-                    tma_load_3d(stage(st) + h * 16384 + 8192, &qmap, &B->full[st], 64 * h,
-                                c * kChunk, seq);
+                for (int h = 0; h < NH; ++h) {
+                    tma_load_3d(ktile(h, st), &kmap, &B->full[st], 64 * h, c * kChunk, seq);
+                    tma_load_3d(qtile(h, st), &qmap, &B->full[st], 64 * h, c * kChunk, seq);
+                    if (st == 0)   // the copy after the last query tile of the ring
+                        tma_load_3d(ktile(h, kNS), &kmap, &B->full[st], 64 * h, c * kChunk, seq);
                 }
                 tma_load_3d(vtile(st), &vmap, &B->full[st], r0, c * kChunk, seq);
-                bulk_load(rec(st), recs + (size_t)c * kRecBytes, kRecBytes, &B->full[st]);
+                bulk_load(vec(st), recs + (size_t)c * kRecBytes, kRecBytes, &B->full[st]);
                 issued = c + 1;
             }
             // drain: every issued stage's copies must have landed before exit
-            for (int c = (issued > L.NS ? issued - L.NS : 0); c < issued; ++c) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(&B->full[c % L.NS], (c / L.NS) & 1))
-                    if (clock64() - t0 > kWaitCycles) break;
-            }
+            for (int c = (issued > kNS ? issued - kNS : 0); c < issued; ++c)
+                wait_drain(&B->full[c % kNS], (c / kNS) & 1);
         }
         __syncwarp();
-    } else if (warp == 5) {
-        // ------------------------------------------ read-side MMA issuer
-        // The correction MMA of chunk c-1 goes right after MMA1(c) completes
-        // (it runs while the errors of chunk c are formed); the scores run two
-        // chunks ahead, issued after MMA2(c) completes (during the carry).
-        if (nch > 0) {
-            const uint32_t idqk = idesc_bf16_f32(64, 64, 0, 0);
-            const uint32_t idz = idesc_bf16_f32(128, 16, 0, 1);
-            auto issue_qk = [&](int c) -> bool {
-                const int q = c % 3, st = c % L.NS;
-                bool ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-                if (ok && c >= 3) ok = wait_all(B, &B->qk_free[q], ((c - 3) / 3) & 1, status);
-                if (!ok) return false;
-                tc_fence_after();
-                const uint32_t base = smem_u32(stage(st));
-                const uint32_t d = tmem + kAccQK + q * 64;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t half = base + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        // A = the 64 Q rows (8 KB after the K rows), B = the 64 K rows
-                        mma_bf16(d, sdesc(half + 8192, 16, 1024, 2), sdesc(half, 16, 1024, 2), idqk,
-                                 kk > 0);
-                    }
-                    mma_commit(&B->qk_done[q]);
-                    mma_commit(&B->empty[st]);
-                }
-                __syncwarp();
-                return true;
-            };
-            auto issue_z = [&](int c) -> bool {
-                const int b = c & 1;
-                bool ok = wait_all(B, &B->at_ready[b], (c >> 1) & 1, status);
-                if (ok && c >= 2) ok = wait_all(B, &B->accz_free[b], ((c - 2) >> 1) & 1, status);
-                if (!ok) return false;
-                tc_fence_after();
-                // 128-row A operand starting 8 KB before the 64 rows of A~
-                const uint32_t at_a = smem_u32(at(b)) - 8192, et_a = smem_u32(et(b));
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < kChunk / 16; ++kk)
-                        mma_bf16(tmem + kAccZ + b * 16, sdesc(at_a + kk * 32, 16, 1024, 2),
-                                 sdesc(et_a + kk * 2048, 8192, 1024, 2), idz, kk > 0);
-                    mma_commit(&B->z_done[b]);
-                }
-                __syncwarp();
-                return true;
-            };
-            bool ok = issue_qk(0);
-            if (ok && nch > 1) ok = issue_qk(1);
-            for (int c = 0; c < nch && ok; ++c) {
-                ok = wait_all(B, &B->mma1_done[c & 1], (c >> 1) & 1, status);
-                if (ok && c >= 1) ok = issue_z(c - 1);
-                if (ok) ok = wait_all(B, &B->mma2_done[c & 1], (c >> 1) & 1, status);
-                if (ok && c + 2 < nch) ok = issue_qk(c + 2);
-            }
-            if (ok) issue_z(nch - 1);
-            // drain: all MMAs issued by this thread complete before TMEM is
-            // released (the chain's own MMAs were waited for by the chain)
-            if (elect_one()) mma_commit(&B->drain);
-            __syncwarp();
-            const long long t0 = clock64();
-            while (!mbar_try_wait(&B->drain, 0))
-                if (clock64() - t0 > kWaitCycles) break;
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------ read side (6-9)
-        // Score weighting: warp w owns TMEM sub-partition p = w % 4, i.e. the
-        // tokens 16p + lane (lane < 16) of the M = 64 score accumulator.
-        const int p = warp & 3;
-        const int ta = 16 * p + lane;        // token of this lane in A~ (lane < 16)
-        const bool zw = warp < 8;            // warps 6-7 also form the outputs
-        const int t = tid - 192;             // output token of warps 6-7 (TMEM lane 64 + t)
-        const int wl = (warp & 3) * 32;
-        bool ok = true;
-        for (int c = 0; c < nch && ok; ++c) {
-            const int st = c % L.NS, b = c & 1, q = c % 3;
-            ok = wait_all(B, &B->full[st], (c / L.NS) & 1, status);
-            if (ok) ok = wait_all(B, &B->qk_done[q], (c / 3) & 1, status);
-            if (ok && c >= 2) ok = wait_all(B, &B->z_done[b], ((c - 2) >> 1) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            // A~[t][s] = C[t][s] (q_t . k_s); C is zero above the diagonal
-            const uint8_t* crow = rec(st) + kRecC + ta * 256;
-            uint8_t* arow = at(b);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float r[16];
-                tmem_ld16(tmem_addr(tmem, wl, kAccQK + q * 64 + 16 * q4), r);
-                float cv[16];
-                if (lane < 16) {
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const float4 f = *reinterpret_cast<const float4*>(
-                            crow + (((4 * q4 + jj) ^ (ta & 15)) << 4));
-                        cv[4 * jj] = f.x;
-                        cv[4 * jj + 1] = f.y;
-                        cv[4 * jj + 2] = f.z;
-                        cv[4 * jj + 3] = f.w;
-                    }
-                }
-                tmem_wait_ld();
-                if (lane < 16) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] *= cv[i];
-                    st_chunk(arow, ta, 16 * q4, r);
-                    st_chunk(arow, ta, 16 * q4 + 8, r + 8);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&B->qk_free[q]);
-            fence_proxy_async_smem();
-            mbar_arrive(&B->at_ready[b]);
-            if (!zw) {
-                mbar_arrive(&B->empty[st]);
-                continue;
-            }
-            const float bt = recf(st, kRecBeta)[t], ct = recf(st, kRecCvec)[t];
-            const int n = (int)recf(st, kRecScal)[3];
-            mbar_arrive(&B->empty[st]);
-            // reads: z_t = beta_t Q W^T + c_t Q S^T - 2 A~ E^T
-            ok = wait_all(B, &B->mma1_done[b], (c >> 1) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            float qw[16], qs[16], ae[16];
-            tmem_ld16(tmem_addr(tmem, wl, kAcc1 + b * 32), qw);
-            tmem_ld16(tmem_addr(tmem, wl, kAcc1 + b * 32 + 16), qs);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&B->acc1_free[b]);
-            ok = wait_all(B, &B->z_done[b], (c >> 1) & 1, status);
-            if (!ok) break;
-            tc_fence_after();
-            tmem_ld16(tmem_addr(tmem, wl, kAccZ + b * 16), ae);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&B->accz_free[b]);
-            if (t < n) {
-                float zz[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) zz[i] = bt * qw[i] + ct * qs[i] - 2.f * ae[i];
-                uint4 o0, o1;
-                o0.x = pack_bf16(zz[0], zz[1]);   o0.y = pack_bf16(zz[2], zz[3]);
-                o0.z = pack_bf16(zz[4], zz[5]);   o0.w = pack_bf16(zz[6], zz[7]);
-                o1.x = pack_bf16(zz[8], zz[9]);   o1.y = pack_bf16(zz[10], zz[11]);
-                o1.z = pack_bf16(zz[12], zz[13]); o1.w = pack_bf16(zz[14], zz[15]);
-                __nv_bfloat16* zr = static_cast<__nv_bfloat16*>(a.z) +
-                                    ((size_t)seq * T + (size_t)c * kChunk + t) * D + r0;
-                reinterpret_cast<uint4*>(zr)[0] = o0;
-                reinterpret_cast<uint4*>(zr)[1] = o1;
-            }
-        }
     }
 
+    // drain the MMAs of the three issuing warps before TMEM is released
+    if (warp == 0 || warp == 6 || warp == 7 || warp == 8) {
+        uint64_t* d = &B->drain[warp == 0 ? 0 : (warp == 6 ? 1 : (warp == 7 ? 3 : 2))];
+        if (elect_one()) mma_commit(d);
+        __syncwarp();
+        if (lane == 0) wait_drain(d, 0);
+        __syncwarp();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 4) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------- host

@@ -220,6 +220,7 @@ __device__ __forceinline__ void raise_abort(Bars* B, int* status, uint32_t peer)
 template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, int* status,
                                          uint32_t peer) {
+    if (kCluster ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     uint32_t polls = 0;
     while (!(kCluster ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))) {
@@ -239,6 +240,8 @@ __device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_all(Bars* B, uint64_t* bar, uint32_t parity, int* status,
                                          uint32_t peer) {
+    if (__all_sync(0xffffffffu, kCluster ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)))
+        return true;
     return __all_sync(0xffffffffu, wait_bar<kCluster>(B, bar, parity, status, peer));
 }
 

@@ -51,6 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass, instead of returning at once, so
+// waiting warps do not keep the shared-memory pipe busy with polls.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok = 0;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: gives up after `limit` polls and returns false (the caller
 // records the timeout and unwinds).  try_wait itself blocks for a bounded,
 // hardware-defined time per poll.
@@ -100,6 +114,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Prefetch of a 3-D tensor tile into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Prefetch of `bytes` (a multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int x, int y,
