@@ -81,6 +81,7 @@ constexpr uint32_t kAcc1 = 0;     // 2 x 32: [Q_c; K_{c+1}] [W_c; S_c]^T
 constexpr uint32_t kAccS = 64;    // 2 x 64: [Q_c; K_{c+1}] K_c^T (raw scores)
 constexpr uint32_t kAcc2 = 192;   // 2 x 32: K_c^T [C E | Pm E] (lane = d_k index)
 constexpr uint32_t kAcc3 = 256;   // 2 x 16: [A~_c; M_c] E_c
+constexpr uint32_t kAM = 288;     // 2 x 32: [A~_c; M_c] as a bf16 A operand (two values per column)
 
 // Per-chunk coefficient record (workspace, staged whole into shared memory).
 // C[t][s] = theta_s w(s,t) (zero above the diagonal) in fp32, row t at
@@ -103,8 +104,17 @@ __host__ __device__ constexpr uint32_t c_offset(int t, int s) {
 constexpr uint32_t kTile = 8192;                          // 64 rows x 128 bytes
 constexpr uint32_t kRingBytes = (2 * kNS + 1) * kTile;    // [K_0][Q_0]...[K_2][Q_2][K_0 copy]
 
+struct Bars {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t acc1_ready[2], acc1_free[2], sc_ready[2], am_ready[2];
+    uint64_t mma3_done[2], acc3_free[2], mma2_done[2], acc2_free[2], mma3_issued;
+    uint64_t drain[4];
+    uint32_t tmem_base;
+    int abort;
+};
+
 struct Layout {
-    uint32_t off_ete, off_ring, off_am, off_etcp, off_ws, off_v, off_rec, total;
+    uint32_t off_ete, off_ring, off_etcp, off_ws, off_v, off_rec, off_bars, total;
 };
 
 // Shared-memory map.  The error tile E (8 KB) sits right before the key /
@@ -115,23 +125,15 @@ __host__ __device__ constexpr Layout make_layout(int D) {
     uint32_t off = 0;
     L.off_ete = off;  off += kTile;                        // E_c [t][r] (16 of 64 columns)
     L.off_ring = off; off += (D / 64) * kRingBytes;       // one ring per 64-column half
-    L.off_am = off;   off += 2 * kTile;                    // [A~; M] [128 rows][s]
     L.off_etcp = off; off += 2 * kTile;                    // 2 x [C E | Pm E] [t][r'] (32 columns)
-    L.off_ws = off;   off += (D / 64) * 4096;              // [W; S] bf16, 32 rows per half
+    L.off_ws = off;   off += D * 128;                      // [W; S]^T bf16 [j][r'] (32 of 64 columns)
     L.off_v = off;    off += kNS * 2048;                   // V slice [t][16]
     L.off_rec = off;  off += kNS * kVecSlot;               // coefficient record
+    L.off_bars = off; off += (sizeof(Bars) + 15) & ~size_t(15);   // mbarriers (no static smem)
     L.total = off;
     return L;
 }
 
-struct Bars {
-    uint64_t full[kNS], empty[kNS];
-    uint64_t acc1_ready[2], acc1_free[2], sc_ready[2], am_ready;
-    uint64_t mma3_done[2], acc3_free[2], mma2_done[2], acc2_free[2], mma3_issued;
-    uint64_t drain[4];
-    uint32_t tmem_base;
-    int abort;
-};
 
 struct TcParams {
     LinearArgs a;
@@ -328,9 +330,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-    __shared__ Bars bars;
-    Bars* B = &bars;
     constexpr Layout L = make_layout(D);
+    Bars* B = reinterpret_cast<Bars*>(sm + L.off_bars);
     constexpr int NH = D / 64;         // 64-column halves
     constexpr int KS = D / 16;         // K steps over d
     const LinearArgs& a = P.a;
@@ -350,7 +351,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     auto vtile = [&](int s) { return sm + L.off_v + s * 2048; };
     auto vec = [&](int s) { return sm + L.off_rec + s * kVecSlot; };
     auto vecf = [&](int s, uint32_t off) { return reinterpret_cast<const float*>(vec(s) + off); };
-    uint8_t* amt = sm + L.off_am;
     uint8_t* ete = sm + L.off_ete;
     auto etcp = [&](int b) { return sm + L.off_etcp + b * kTile; };
     uint8_t* ws = sm + L.off_ws;
@@ -369,7 +369,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->acc2_free[b], 128);    // state warps
         }
-        mbar_init(&B->am_ready, 128);            // weighting warps
+        mbar_init(&B->am_ready[0], 128);         // weighting warps
+        mbar_init(&B->am_ready[1], 128);
         mbar_init(&B->mma3_issued, 1);           // chain MMA queued (carry MMA goes after it)
         for (int i = 0; i < 4; ++i) mbar_init(&B->drain[i], 1);
         B->abort = 0;
@@ -389,7 +390,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const uint8_t* base = c < 0 ? ktile(h, 0) - kTile : qtile(h, c % kNS);
         return smem_u32(base) + (kk & 3) * 32;
     };
-    constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 0);   // state MMA
+    constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // state MMA, B MN-major
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);   // scores
     constexpr uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);   // carry: A = K^T, B = [C E | Pm E]
     constexpr uint32_t id3 = idesc_bf16_f32(128, 16, 0, 1);   // chain: [A~; M] E
@@ -408,15 +409,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             w[i] = own ? a.W0[idx] : 0.f;
             s[i] = (own && a.S0) ? a.S0[idx] : 0.f;
         }
+        // the state operand MN-major: row j holds W[.][j] then S[.][j], so
+        // thread j writes its column with four 16-byte stores
         auto write_ws = [&]() {
             if (!own) return;
-            uint8_t* t = ws + (j >> 6) * 4096;
-            const int col = j & 63;
-#pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-                *reinterpret_cast<__nv_bfloat16*>(t + sw128_offset(i, col)) = __float2bfloat16_rn(w[i]);
-                *reinterpret_cast<__nv_bfloat16*>(t + sw128_offset(16 + i, col)) = __float2bfloat16_rn(s[i]);
-            }
+            st_chunk(ws, j, 0, w);
+            st_chunk(ws, j, 8, w + 8);
+            st_chunk(ws, j, 16, s);
+            st_chunk(ws, j, 24, s + 8);
         };
         // state MMA of chunk x (x = -1, 0 use the initial state)
         auto issue_state = [&](int x, bool ok) -> bool {
@@ -431,7 +431,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 #pragma unroll 1
                 for (int kk = 0; kk < KS; ++kk)
                     mma_bf16(tmem + kAcc1 + (x & 1) * 32, sdesc(qk_a(x, kk), 16, 1024, 2),
-                             sdesc(wsa + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2), id1, kk > 0);
+                             sdesc(wsa + kk * 2048, 8192, 1024, 2), id1, kk > 0);
                 mma_commit(&B->acc1_ready[x & 1]);
             }
             __syncwarp();
@@ -593,16 +593,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // wait for it at once
             const int b = x & 1;
             if (warp == 6) {
-                if (ok) ok = wait_all(B, &B->am_ready, x & 1, status);
+                if (ok) ok = wait_all(B, &B->am_ready[b], (x >> 1) & 1, status);
                 if (ok && x >= 2) ok = wait_all(B, &B->acc3_free[b], ((x - 2) >> 1) & 1, status);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t am = smem_u32(amt), et = smem_u32(ete);
+                    const uint32_t et = smem_u32(ete);
                     if (elect_one()) {
 #pragma unroll 1
                         for (int kk = 0; kk < kChunk / 16; ++kk)
-                            mma_bf16(tmem + kAcc3 + b * 16, sdesc(am + kk * 32, 16, 1024, 2),
-                                     sdesc(et + kk * 2048, 8192, 1024, 2), id3, kk > 0);
+                            mma_tmem_a(tmem + kAcc3 + b * 16, tmem + kAM + b * 32 + kk * 8,
+                                       sdesc(et + kk * 2048, 8192, 1024, 2), id3, kk > 0);
                         mma_commit(&B->mma3_done[b]);
                         mbar_arrive(&B->mma3_issued);
                     }
@@ -654,8 +654,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             if (ok && warp != 8) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
             if (ok) ok = wait_all(B, &B->sc_ready[b], (c >> 1) & 1, status);
-            // the chain MMA of chunk c-1 reads the previous contents of the tile
-            if (ok && c >= 1) ok = wait_all(B, &B->mma3_done[(c - 1) & 1], ((c - 1) >> 1) & 1, status);
+            // the chain MMA of chunk c-2 read this buffer's previous contents
+            if (ok && c >= 2) ok = wait_all(B, &B->mma3_done[b], ((c - 2) >> 1) & 1, status);
             if (ok) {
                 tc_fence_after();
                 // weights of this row: row m of the table (m < 64) or C[n-1][.]
@@ -674,14 +674,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                         wt[4 * g + 3] = f.w;
                     }
                     tmem_wait_ld();
+                    uint32_t p[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] *= wt[i];
-                    st_chunk(amt, m, 16 * q4, r);
-                    st_chunk(amt, m, 16 * q4 + 8, r + 8);
+                    for (int i = 0; i < 8; ++i)
+                        p[i] = pack_bf16(r[2 * i] * wt[2 * i], r[2 * i + 1] * wt[2 * i + 1]);
+                    tmem_st8(tl + kAM + b * 32 + 8 * q4, p);
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&B->am_ready);
+                mbar_arrive(&B->am_ready[b]);
             }
             named_bar_sync(4, 128);
         }
