@@ -38,17 +38,19 @@
 // the gates and come from a pre-pass kernel (one warp per sequence and chunk)
 // through the caller's workspace.
 //
-// Roles inside a CTA (416 threads):
+// Roles inside a CTA (512 threads):
 //   warps 0-3   state: thread j holds column j of the 16 W rows and 16 S rows
 //               in fp32 registers, applies the carry and writes the bf16 copy
 //               [W; S] for the state MMA, which warp 0 issues.
 //   warps 4-5   outputs z (token = TMEM lane 0-63).
-//   warps 6-7   error chain (token of the next chunk = TMEM lane 64-127);
+//   warps 6-7,  error chain (token of the next chunk = TMEM lane 64-127; warps
+//   14-15       6-7 take columns 0-7 of a row, warps 14-15 columns 8-15);
 //               warp 6 issues the chain MMA, warp 7 then the carry MMA.
 //   warps 8-11  score weighting (TMEM sub-partition = warp % 4); warp 8
 //               issues the score MMAs ahead of the chain.
 //   warp 12     producer: TMA loads of K, Q, the V slice and the coefficient
-//               vectors.
+//               record, L2 prefetch four chunks ahead.
+//   warp 13     idle.
 //
 // Every wait is bounded: a wait that exceeds its limit sets the device status
 // word to TTM_ERR_TIMEOUT, every role runs out its loop doing no further work
@@ -72,7 +74,7 @@ using namespace tc;
 
 constexpr int kChunk = 64;      // tokens per chunk (== TMA tile height)
 constexpr int kRows = 16;       // rows of W per CTA
-constexpr int kThreads = 416;
+constexpr int kThreads = 512;
 constexpr int kNS = 3;          // pipeline stages
 constexpr uint32_t kTmemCols = 512;
 
@@ -362,10 +364,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&B->acc1_ready[b], 1);
-            mbar_init(&B->acc1_free[b], 128);    // error chain 64 + outputs 64
+            mbar_init(&B->acc1_free[b], 192);    // error chain 128 + outputs 64
             mbar_init(&B->sc_ready[b], 1);
             mbar_init(&B->mma3_done[b], 1);
-            mbar_init(&B->acc3_free[b], 128);    // error chain 64 + outputs 64
+            mbar_init(&B->acc3_free[b], 192);    // error chain 128 + outputs 64
             mbar_init(&B->mma2_done[b], 1);
             mbar_init(&B->acc2_free[b], 128);    // state warps
         }
@@ -526,12 +528,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             named_bar_sync(3, 64);
             if (tid == 128 && ok) mbar_arrive(&B->empty[st]);
         }
-    } else if (warp < 8) {
+    } else if (warp < 8 || warp >= 14) {
         // ------------------------------------------------------ error chain
-        // Thread t' produces row t' of E_x for x = 0, 1, ...: from the state
-        // product of chunk x-1 (lanes 64-127: K_x W^T, K_x S^T) and, for
-        // x >= 1, the chain product M_{x-1} E_{x-1}.
-        const int t = tid - 192;                 // token = TMEM lane 64 + t
+        // Thread t' produces half h of row t' of E_x (columns 8h .. 8h + 7) for
+        // x = 0, 1, ...: from the state product of chunk x-1 (lanes 64-127:
+        // K_x W^T, K_x S^T) and, for x >= 1, the chain product M_{x-1} E_{x-1}.
+        // Warps 6-7 take h = 0, warps 14-15 (same TMEM lanes) h = 1.
+        const int t = lane + 32 * ((warp & 3) - 2);   // token = TMEM lane 64 + t
+        const int h = warp >= 14 ? 1 : 0;
         bool ok = true;
         float bn = 1.f, cn = 0.f;                // carry coefficients of chunk x-1
         for (int x = 0; x < nch; ++x) {
@@ -539,29 +543,25 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (ok) ok = wait_all(B, &B->full[st], (x / kNS) & 1, status);
             if (ok) ok = wait_all(B, &B->acc1_ready[pb], use_parity(x - 1), status);
             if (ok && x >= 1) ok = wait_all(B, &B->mma3_done[pb], ((x - 1) >> 1) & 1, status);
-            float e[16];
+            float e[8];
             if (ok) {
                 tc_fence_after();
-                float f[16], g[16], m[16];
-                tmem_ld16(tl + kAcc1 + pb * 32, f);
-                tmem_ld16(tl + kAcc1 + pb * 32 + 16, g);
-                if (x >= 1) tmem_ld16(tl + kAcc3 + pb * 16, m);
-                float v[16];
-                {
-                    const uint4* vr = reinterpret_cast<const uint4*>(vtile(st) + t * 32);
-                    unpack8(vr[0], v);
-                    unpack8(vr[1], v + 8);
-                }
+                float f[8], g[8], m[8];
+                tmem_ld8(tl + kAcc1 + pb * 32 + 8 * h, f);
+                tmem_ld8(tl + kAcc1 + pb * 32 + 16 + 8 * h, g);
+                if (x >= 1) tmem_ld8(tl + kAcc3 + pb * 16 + 8 * h, m);
+                float v[8];
+                unpack8(reinterpret_cast<const uint4*>(vtile(st) + t * 32)[h], v);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&B->acc1_free[pb]);
                 if (x >= 1) {
                     mbar_arrive(&B->acc3_free[pb]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) e[i] = bn * f[i] + cn * g[i] - 2.f * m[i] - v[i];
+                    for (int i = 0; i < 8; ++i) e[i] = bn * f[i] + cn * g[i] - 2.f * m[i] - v[i];
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) e[i] = f[i] - v[i];
+                    for (int i = 0; i < 8; ++i) e[i] = f[i] - v[i];
                 }
                 const float4 sc = *reinterpret_cast<const float4*>(vec(st) + kVScal);
                 const float ce = vecf(st, kVCend)[t], pe = vecf(st, kVPend)[t];
@@ -571,23 +571,20 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 // chain MMA of chunk x-1 (complete) read the E tile
                 if (x >= 2) ok = wait_all(B, &B->mma2_done[x & 1], ((x - 2) >> 1) & 1, status);
                 if (ok) {
-                    float ec[16], ep[16];
+                    float ec[8], ep[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         ec[i] = ce * e[i];
                         ep[i] = pe * e[i];
                     }
-                    st_chunk(ete, t, 0, e);
-                    st_chunk(ete, t, 8, e + 8);
                     uint8_t* cp = etcp(x & 1);
-                    st_chunk(cp, t, 0, ec);
-                    st_chunk(cp, t, 8, ec + 8);
-                    st_chunk(cp, t, 16, ep);
-                    st_chunk(cp, t, 24, ep + 8);
+                    st_chunk(ete, t, 8 * h, e);
+                    st_chunk(cp, t, 8 * h, ec);
+                    st_chunk(cp, t, 16 + 8 * h, ep);
                     fence_proxy_async_smem();
                 }
             }
-            named_bar_sync(2, 64);
+            named_bar_sync(2, 128);
             // chain MMA of chunk x (warp 6), then the carry MMA (warp 7), so the
             // chain product is first in the tensor pipe and warp 6 is free to
             // wait for it at once
@@ -608,7 +605,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     }
                     __syncwarp();
                 }
-            } else {
+            } else if (warp == 7) {
                 if (ok) ok = wait_all(B, &B->mma3_issued, x & 1, status);
                 if (ok && x >= 2) ok = wait_all(B, &B->acc2_free[b], ((x - 2) >> 1) & 1, status);
                 if (ok) {
@@ -686,7 +683,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             named_bar_sync(4, 128);
         }
-    } else {
+    } else if (warp == 12) {
         // --------------------------------------------------------- producer
         if (lane == 0) {
             // tiles of chunk c are requested into L2 kPrefetch chunks before
