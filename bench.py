@@ -131,6 +131,143 @@ def profiled_traffic(kernel_name: str, w: wl.Workload):
 # clocks sampled while the GPU is under load
 # ----------------------------------------------------------------------------
 
+# ----------------------------------------------------------------------------
+# decode step (--mode decode): n tokens per sequence per call, state resident
+# ----------------------------------------------------------------------------
+
+DECODE = dict(B=64, H=16, d=128, chunk=64)
+
+
+def decode_algorithmic(B, H, d, chunk, n, es=2) -> dict:
+    """Bytes one call must move: the state W, S and the chunk snapshot read
+    once, W and S written once, the snapshot written once per chunk; q, k, v
+    read and z written in the input dtype; three 4-byte gates per token."""
+    state = d * d * 4
+    per_seq = 3 * state + 2 * state + state * n / chunk + n * (4 * d * es + 12)
+    return {"bytes": B * H * per_seq, "flops": B * H * n * 6 * d * d}
+
+
+def run_decode(args, rank, world, dev):
+    import test_neural_memory_gb300 as ttm
+
+    c = DECODE
+    n = args.decode_tokens
+    B, H, d, chunk = c["B"], c["H"], c["d"], c["chunk"]
+    name = f"titans decode step B{B} H{H} d{d} chunk {chunk}, {n} token(s) per call, bf16"
+    w, inp = wl.generate_custom(kind="titans", dtype="bf16", B=B, H=H, T=n, d=d, chunk=chunk,
+                                seed=1234)
+    stream = torch.cuda.current_stream(dev)
+    dd = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    W = dd["W0"].clone()
+    S = torch.zeros_like(W)
+    Wc = torch.empty_like(W)
+    z = torch.empty_like(dd["v"])
+    pos = [0]
+
+    def step():
+        _, _, pos[0] = ttm.titans_step(dd["q"], dd["k"], dd["v"], dd["theta"], W, chunk, pos[0],
+                                       eta=dd["eta"], alpha=dd["alpha"], S=S, Wc=Wc, z=z,
+                                       stream=stream)
+
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ttm.launch_count()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ttm.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
+    status = ttm.device_status()
+    if status != ttm.OK:
+        raise RuntimeError(f"device status {ttm.status_str(status)}")
+
+    a = decode_algorithmic(B, H, d, chunk, n)
+    peaks, src = load_peaks()
+    achieved = a["bytes"] / (ms / 1e3) / 1e9
+    tokens = B * H * n
+    # end to end: each call's token inputs go host -> device, its outputs z back
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items() if k != "W0"}
+    hz = torch.empty(z.shape, dtype=z.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                dd[k].copy_(v, non_blocking=True)
+        step()
+        hz.copy_(z, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ems = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+    line = {
+        "metric": "decode-step tokens/s (B·H sequences x tokens per call) on 1 GB300; % of roofline",
+        "value": tokens * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "d": d, "chunk": chunk,
+                   "tokens_per_call": n, "kind": "titans-step",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "state larger than L2 (no flush needed)"
+                   if a["bytes"] > 129e6 else "L2 not flushed: state fits in L2",
+                   "kernel": "linear_step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": src,
+                     "kernel": "linear_step", "algorithmic_bytes": a["bytes"],
+                     "algorithmic_flops": a["flops"], "traffic": None},
+        "e2e": {"value": tokens * world / (ems / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hz.numel() * hz.element_size(),
+                "steps": args.steps, "ms_per_step": ems},
+        "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_decode_sample(B, H, d, chunk, args.cpu_seconds)
+    return line
+
+
+def oracle_decode_sample(B, H, d, chunk, seconds) -> dict:
+    """The float64 oracle's token loop on a bounded sample of sequences: the
+    same per-token work as a decode step (one gradient step and one read)."""
+    import oracle
+    seqs, T = 16, 64
+    w, inp = wl.generate_custom(kind="titans", dtype="bf16", B=1, H=seqs, T=T, d=d, chunk=chunk,
+                                seed=1234)
+    f = lambda t: None if t is None else t.double().numpy()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        r = oracle.linear_primal(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["theta"]),
+                                 f(inp["W0"]), chunk, eta=f(inp["eta"]), alpha=f(inp["alpha"]))
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > min(seconds, 5.0):
+            break
+    return {"value": seqs * T * reps / el, "unit": "tokens/s", "cores": r["threads"],
+            "kind": "oracle", "seconds": el,
+            "sample": f"{seqs} sequences x {T} tokens (d={d}), token loop, float64, x{reps}"}
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -439,6 +576,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["scan", "decode"], default="scan",
+                    help="decode: time the streaming decode step instead of the scan")
+    ap.add_argument("--decode-tokens", type=int, default=1, help="tokens per decode call")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -460,7 +600,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     import test_neural_memory_gb300 as ttm
     ttm.build()
-    line = run_ours(args, rank, world, dev)
+    line = run_decode(args, rank, world, dev) if args.mode == "decode" else run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -189,6 +189,45 @@ int ttm_titans_fwd_noalloc(int B, int H, int T, int dk, int dv, int chunk, int d
                            const float* W0, const float* S0, int w0_shared_over_batch,
                            void* z, float* W_out, float* S_out, void* stream);
 
+/*
+ * Streaming decode step of the Titans / linear memory: continues every
+ * sequence by n tokens in the primal, token-by-token form, as the pages
+ * prescribe for decoding after a chunked (dual-form) prefill ("TTT layers 与
+ * fast weights" §1.1 and eq (6): the gradient of every token of a chunk is
+ * taken at the chunk-start state; momentum and forgetting as in
+ * "论文速览 | Titans" §3.4-§3.7).  Per token t, with Wc the memory at the start
+ * of the current chunk:
+ *     e = Wc k_t - v_t;  S = eta_t S - theta_t 2 e k_t^T;
+ *     W = (1 - alpha_t) W + S;  z_t = W q_t  (read after the token's own write);
+ * a token that opens a chunk first sets Wc = W.
+ *   pos: tokens of the current chunk processed before this call, 0 <= pos <
+ *     chunk, the same for every sequence of the call (sequences decoded in
+ *     lockstep).  After the call the position is (pos + n) % chunk; the caller
+ *     keeps it.  A prefill by ttm_titans_fwd over a multiple of `chunk` tokens
+ *     continues with W = W_out, S = S_out, pos = 0 (Wc is then set by the first
+ *     token).
+ *   q, k: [B][H][n][dk], v: [B][H][n][dv] in dtype; eta, theta, alpha: [B][H][n]
+ *     fp32 (eta, alpha may be NULL = 0; theta required); z: [B][H][n][dv] in
+ *     dtype, written.
+ *   W, S, Wc: [B][H][dv][dk] fp32, read and updated in place (S may be NULL
+ *     only when eta is NULL; Wc is written when a chunk opens during the call).
+ *   All pointers are device memory owned by the caller, 16-byte aligned; the
+ *   outputs must not overlap each other or the inputs.
+ * Shapes: B, H, n >= 1; chunk >= 1; dk, dv as for ttm_titans_fwd, dk <= 512
+ * (else TTM_ERR_UNSUPPORTED).  Asynchronous on `stream`; TTM_ERR_INVALID_ARG
+ * for malformed arguments, TTM_ERR_CUDA if the launch fails.
+ */
+int ttm_titans_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                    const void* q, const void* k, const void* v,
+                    const float* eta, const float* theta, const float* alpha,
+                    float* W, float* S, float* Wc, void* z, void* stream);
+
+/* The decode step of TTT-Linear (no momentum, no forgetting): ttm_titans_step
+ * with eta = alpha = S = NULL, i.e. W = W - theta_t 2 (Wc k_t - v_t) k_t^T. */
+int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                    const void* q, const void* k, const void* v, const float* theta,
+                    float* W, float* Wc, void* z, void* stream);
+
 /* The activation of the 2-layer memory and its derivative, evaluated on the
  * device exactly as the tensor-core 2-layer kernel evaluates them: for the n
  * values x[i], y[i] = GELU(x) = x Phi(x) and, if dy is not NULL,

@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.ttm_linear_workspace_size.restype = sz
         L.ttm_mlp_fwd.argtypes = [i] * 7 + [p] * 6 + [p] * 4 + [i] + [p] * 5 + [p]
         L.ttm_mlp_gelu.argtypes = [p, p, p, i, p]
+        L.ttm_titans_step.argtypes = [i] * 8 + [p] * 6 + [p] * 4 + [p]
+        L.ttm_linear_step.argtypes = [i] * 8 + [p] * 4 + [p] * 3 + [p]
         L.ttm_mlp_gelu.restype = i
         for f in (L.ttm_linear_fwd, L.ttm_titans_fwd, L.ttm_mlp_fwd):
             f.restype = i
@@ -183,6 +185,27 @@ def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_s
                                 int(bool(w0_shared)), _ptr(z), _ptr(W_out), _ptr(S_out), wp, wb,
                                 _stream(q, stream)), "ttm_titans_fwd")
     return z, W_out, S_out
+
+
+def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, Wc=None,
+                z=None, stream=None):
+    """Decode step: continues every sequence by n tokens (q, k: [B,H,n,dk]; v: [B,H,n,dv];
+    gates [B,H,n]) from the state W (and momentum S) at position `pos` of the current
+    chunk.  W, S, Wc ([B,H,dv,dk] fp32) are updated in place; Wc is allocated when None
+    (allowed only at pos == 0).  Returns (z, Wc, new_pos)."""
+    import torch
+    B, H, n, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    if Wc is None:
+        if pos != 0:
+            raise TTMError(ERR_INVALID_ARG, "titans_step (Wc is required in mid-chunk)")
+        Wc = torch.empty_like(W)
+    _check(lib().ttm_titans_step(B, H, n, dk, dv, int(chunk), int(pos), _dtype_code(q), _ptr(q),
+                                 _ptr(k), _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W),
+                                 _ptr(S), _ptr(Wc), _ptr(z), _stream(q, stream)),
+           "ttm_titans_step")
+    return z, Wc, (pos + n) % chunk
 
 
 def mlp_fwd(q, k, v, theta, W1_0, W2_0, chunk, *, eta=None, alpha=None, S1_0=None, S2_0=None,

@@ -35,6 +35,18 @@ struct MlpArgs {
     int* status;
 };
 
+// One call of the decode step (step.cu): n tokens per sequence in the primal
+// form.  W, S, Wc are updated in place; pos is the shared position within the
+// chunk at the call's start.
+struct StepArgs {
+    int B, H, n, dk, dv, chunk, pos;
+    int bf16;
+    const void *q, *k, *v;
+    const float *eta, *theta, *alpha;   // eta / alpha may be NULL (= 0)
+    float *W, *S, *Wc;                  // S may be NULL when eta is NULL
+    void* z;
+};
+
 // fp32 CUDA-core kernels (scan_simt.cu).  The *_supported functions decide
 // on the host whether a shape fits the kernel's on-chip budget.
 bool linear_simt_supported(const LinearArgs& a);
@@ -53,6 +65,10 @@ cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s);
 // d = 64, hidden = 256, chunk 16; one cluster of two CTAs per sequence.
 bool mlp_tc_supported(const MlpArgs& a);
 cudaError_t mlp_tc_launch(const MlpArgs& a, cudaStream_t s);
+// Decode step (step.cu): one warp per row of W; dk <= 512.
+bool linear_step_supported(const StepArgs& a);
+cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
+
 // The activation of that kernel on n values: y = GELU(x), dy = GELU'(x) (dy may be NULL).
 cudaError_t mlp_gelu_launch(const float* x, float* y, float* dy, int n, cudaStream_t s);
 

@@ -1,0 +1,295 @@
+// Streaming decode step of the linear / Titans memory: continues every
+// sequence by n tokens in the primal, token-by-token form ("TTT layers 与 fast
+// weights" §1.1: decoding runs the primal form after a chunked prefill; the
+// gradient of every token of a chunk is taken at the chunk-start state, eq (6);
+// momentum and forgetting as in "论文速览 | Titans" §3.4-§3.7).
+//
+// Per token t, with W_c the memory at the start of the current chunk:
+//   e   = W_c k_t - v_t
+//   S   = eta_t S - theta_t 2 e k_t^T
+//   W   = (1 - alpha_t) W + S
+//   z_t = W q_t
+// and W_c is re-taken (W_c = W) whenever a token opens a chunk.
+//
+// Every row of W, S and W_c evolves on its own (row r only needs e_r), so one
+// warp owns one row of one sequence for the whole call: lane l holds the
+// columns l, l + 32, ... of the three rows in registers, the two dot products
+// per token are warp reductions, and the state is read and written once per
+// call whatever n is.  A one-token call is bound by HBM (it moves the state
+// W, S, W_c once in each direction plus one token's q, k, v, z) and issues
+// all its loads up front; a longer call is bound by the per-token chain and
+// stages its tokens through shared memory in groups, one memory round trip
+// per group instead of one per token.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace ttm {
+namespace {
+
+constexpr int kStepThreads = 256;   // 8 rows per block
+
+template <typename TIn>
+__device__ __forceinline__ float ld_in(const TIn* p);
+template <>
+__device__ __forceinline__ float ld_in<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+}
+
+template <typename TIn>
+__device__ __forceinline__ void st_out(TIn* p, float x);
+template <>
+__device__ __forceinline__ void st_out<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void st_out<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+    *p = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// One token per call (the streaming case): the call is bound by reading and
+// writing the state, so every load is issued as early as possible and nothing
+// is staged.  NJ = columns per lane (dk <= 32 NJ).
+template <typename TIn, int NJ>
+__global__ void __launch_bounds__(kStepThreads) linear_step_direct(const StepArgs a) {
+    const long long gw = ((long long)blockIdx.x * kStepThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long nrows = (long long)a.B * a.H * a.dv;
+    if (gw >= nrows) return;
+    const int r = (int)(gw % a.dv);
+    const long long seq = gw / a.dv;
+    const int dk = a.dk;
+    const size_t row = ((size_t)seq * a.dv + r) * dk;
+    const size_t tok = (size_t)seq;   // n == 1: token index = sequence index
+    const TIn* q = static_cast<const TIn*>(a.q);
+    const TIn* k = static_cast<const TIn*>(a.k);
+
+    float w[NJ], s[NJ], wc[NJ], kv[NJ], qv[NJ];
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        const bool in = j < dk;
+        w[i] = in ? a.W[row + j] : 0.f;
+        s[i] = (in && a.S) ? a.S[row + j] : 0.f;
+        wc[i] = in ? a.Wc[row + j] : 0.f;
+        kv[i] = in ? ld_in<TIn>(k + tok * dk + j) : 0.f;
+        qv[i] = in ? ld_in<TIn>(q + tok * dk + j) : 0.f;
+    }
+    const float th = __ldg(a.theta + tok);
+    const float et = a.eta ? __ldg(a.eta + tok) : 0.f;
+    const float keep = 1.f - (a.alpha ? __ldg(a.alpha + tok) : 0.f);
+    const float vr = ld_in<TIn>(static_cast<const TIn*>(a.v) + tok * a.dv + r);
+    const bool opens = a.pos == 0;   // the token opens a chunk: its gradient point is now
+    if (opens) {
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) wc[i] = w[i];
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+    const float ge = 2.f * th * (warp_sum(acc) - vr);   // theta times the gradient's row factor
+    float zq = 0.f;
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        s[i] = fmaf(et, s[i], -ge * kv[i]);
+        w[i] = fmaf(keep, w[i], s[i]);
+        zq = fmaf(w[i], qv[i], zq);
+    }
+    zq = warp_sum(zq);
+    if (lane == 0) st_out<TIn>(static_cast<TIn*>(a.z) + tok * a.dv + r, zq);
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        if (j >= dk) continue;
+        a.W[row + j] = w[i];
+        if (a.S) a.S[row + j] = s[i];
+        if (opens) a.Wc[row + j] = wc[i];
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Copies the keys and queries of tokens [t0, t0 + len) of one sequence into
+// the warp's staging area (k rows then q rows, G rows each) as 16-byte pieces;
+// rows are contiguous in memory and dk * sizeof(TIn) is a multiple of 16.
+template <typename TIn>
+__device__ __forceinline__ void stage_tokens(TIn* ks, int G, const TIn* k, const TIn* q,
+                                             size_t first, int len, int dk, int lane) {
+    const int nvec = (int)((size_t)len * dk * sizeof(TIn) / 16);
+    const char* kg = reinterpret_cast<const char*>(k + first * dk);
+    const char* qg = reinterpret_cast<const char*>(q + first * dk);
+    char* kd = reinterpret_cast<char*>(ks);
+    char* qd = kd + (size_t)G * dk * sizeof(TIn);
+    for (int i = lane; i < nvec; i += 32) {
+        cp_async16(kd + 16 * i, kg + 16 * i);
+        cp_async16(qd + 16 * i, qg + 16 * i);
+    }
+}
+
+template <typename TIn>
+__device__ __forceinline__ float to_f(TIn x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Several tokens per call.  NJ = columns per lane (dk <= 32 NJ).  Tokens are
+// taken in groups of G: one
+// round trip brings a group's keys and queries into the warp's shared-memory
+// staging area (the first group's copy is issued before the state is read,
+// so the two overlap) and lanes 0..G-1 fetch the group's per-token scalars,
+// which are broadcast by shuffles as each token is processed.  Without the
+// grouping every token would wait for its own loads, a full memory latency
+// per token.
+template <typename TIn, int NJ>
+__global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
+    linear_step_staged(const StepArgs a, int G) {
+    extern __shared__ __align__(16) unsigned char step_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * (kStepThreads / 32) + warp;
+    const long long nrows = (long long)a.B * a.H * a.dv;
+    if (gw >= nrows) return;
+    const int r = (int)(gw % a.dv);
+    const long long seq = gw / a.dv;
+    const int dk = a.dk, n = a.n;
+    const size_t row = ((size_t)seq * a.dv + r) * dk;
+    const TIn* q = static_cast<const TIn*>(a.q);
+    const TIn* k = static_cast<const TIn*>(a.k);
+    const TIn* v = static_cast<const TIn*>(a.v);
+    TIn* z = static_cast<TIn*>(a.z);
+    TIn* ks = reinterpret_cast<TIn*>(step_smem) + (size_t)warp * 2 * G * dk;
+    const TIn* qs = ks + (size_t)G * dk;
+
+    stage_tokens<TIn>(ks, G, k, q, (size_t)seq * n, min(G, n), dk, lane);
+    float w[NJ], s[NJ], wc[NJ];
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        const bool in = j < dk;
+        w[i] = in ? a.W[row + j] : 0.f;
+        s[i] = (in && a.S) ? a.S[row + j] : 0.f;
+        wc[i] = in ? a.Wc[row + j] : 0.f;
+    }
+    int p = a.pos;
+    bool wc_changed = false;
+    for (int t0 = 0; t0 < n; t0 += G) {
+        const int len = min(G, n - t0);
+        if (t0 > 0) {
+            __syncwarp();   // every lane is done reading the previous group
+            stage_tokens<TIn>(ks, G, k, q, (size_t)seq * n + t0, len, dk, lane);
+        }
+        float vr = 0.f, th = 0.f, et = 0.f, keep = 1.f;
+        if (lane < len) {
+            const size_t tok = (size_t)seq * n + t0 + lane;
+            vr = ld_in<TIn>(v + tok * a.dv + r);
+            th = __ldg(a.theta + tok);
+            et = a.eta ? __ldg(a.eta + tok) : 0.f;
+            keep = 1.f - (a.alpha ? __ldg(a.alpha + tok) : 0.f);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+        for (int u = 0; u < len; ++u) {
+            if (p == 0) {   // this token opens a chunk: its gradient point is now
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) wc[i] = w[i];
+                wc_changed = true;
+            }
+            float kv[NJ], qv[NJ];
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) {
+                const int j = lane + 32 * i;
+                kv[i] = j < dk ? to_f<TIn>(ks[u * dk + j]) : 0.f;
+                qv[i] = j < dk ? to_f<TIn>(qs[u * dk + j]) : 0.f;
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+            const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
+            // theta_t times the gradient's row factor
+            const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
+            const float etu = __shfl_sync(0xffffffffu, et, u);
+            const float keepu = __shfl_sync(0xffffffffu, keep, u);
+            float zq = 0.f;
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) {
+                s[i] = fmaf(etu, s[i], -ge * kv[i]);
+                w[i] = fmaf(keepu, w[i], s[i]);
+                zq = fmaf(w[i], qv[i], zq);
+            }
+            zq = warp_sum(zq);
+            if (lane == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
+            p = p + 1 == a.chunk ? 0 : p + 1;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        if (j >= dk) continue;
+        a.W[row + j] = w[i];
+        if (a.S) a.S[row + j] = s[i];
+        if (wc_changed) a.Wc[row + j] = wc[i];
+    }
+}
+
+// Tokens per staged group: the keys and queries of a group take at most
+// 4 KB per warp (32 KB per block), and a group never exceeds 32 tokens (one
+// per lane for the per-token scalars).
+int group_of(const StepArgs& a) {
+    const int es = a.bf16 ? 2 : 4;
+    const int per_token = 2 * a.dk * es;
+    int G = 4096 / per_token;
+    if (G < 1) G = 1;
+    if (G > 32) G = 32;
+    if (G > a.n) G = a.n;
+    return G;
+}
+
+template <typename TIn, int NJ>
+void launch_nj(const StepArgs& a, unsigned blocks, cudaStream_t s) {
+    if (a.n == 1) {
+        linear_step_direct<TIn, NJ><<<blocks, kStepThreads, 0, s>>>(a);
+    } else {
+        const int G = group_of(a);
+        const size_t smem = (size_t)(kStepThreads / 32) * 2 * G * a.dk * sizeof(TIn);
+        linear_step_staged<TIn, NJ><<<blocks, kStepThreads, smem, s>>>(a, G);
+    }
+}
+
+template <typename TIn>
+cudaError_t launch_typed(const StepArgs& a, cudaStream_t s) {
+    const long long warps = (long long)a.B * a.H * a.dv;
+    const unsigned blocks = (unsigned)((warps * 32 + kStepThreads - 1) / kStepThreads);
+    const int nj = (a.dk + 31) / 32;
+    if (nj <= 1) launch_nj<TIn, 1>(a, blocks, s);
+    else if (nj <= 2) launch_nj<TIn, 2>(a, blocks, s);
+    else if (nj <= 4) launch_nj<TIn, 4>(a, blocks, s);
+    else if (nj <= 8) launch_nj<TIn, 8>(a, blocks, s);
+    else launch_nj<TIn, 16>(a, blocks, s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool linear_step_supported(const StepArgs& a) { return a.dk >= 1 && a.dk <= 512; }
+
+cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s) {
+    return a.bf16 ? launch_typed<__nv_bfloat16>(a, s) : launch_typed<float>(a, s);
+}
+
+}  // namespace ttm

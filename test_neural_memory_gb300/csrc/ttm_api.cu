@@ -243,6 +243,50 @@ int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype, co
     return TTM_OK;
 }
 
+int ttm_titans_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                    const void* q, const void* k, const void* v, const float* eta,
+                    const float* theta, const float* alpha, float* W, float* S, float* Wc,
+                    void* z, void* stream) {
+    if (B < 1 || H < 1 || n < 1 || chunk < 1 || pos < 0 || pos >= chunk) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
+    if (!q || !k || !v || !theta || !W || !Wc || !z) return TTM_ERR_INVALID_ARG;
+    if (eta && !S) return TTM_ERR_INVALID_ARG;   // momentum needs its state
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W, S, Wc, z};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * n;
+    const size_t st = (size_t)B * H * dv * dk * sizeof(float);
+    const Span ins[] = {{q, tok * dk * es}, {k, tok * dk * es}, {v, tok * dv * es},
+                        {eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
+    const Span outs[] = {{W, st}, {S, st}, {Wc, st}, {z, tok * dv * es}};
+    for (int o = 0; o < 4; ++o) {
+        for (const Span& i : ins)
+            if (overlap(outs[o], i)) return TTM_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlap(outs[o], outs[o2])) return TTM_ERR_INVALID_ARG;
+    }
+    ttm::StepArgs a{};
+    a.B = B; a.H = H; a.n = n; a.dk = dk; a.dv = dv; a.chunk = chunk; a.pos = pos;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v;
+    a.eta = eta; a.theta = theta; a.alpha = alpha;
+    a.W = W; a.S = S; a.Wc = Wc; a.z = z;
+    if (!ttm::linear_step_supported(a)) return TTM_ERR_UNSUPPORTED;
+    if (ttm::linear_step_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTM_ERR_CUDA;
+    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                    const void* q, const void* k, const void* v, const float* theta, float* W,
+                    float* Wc, void* z, void* stream) {
+    return ttm_titans_step(B, H, n, dk, dv, chunk, pos, dtype, q, k, v, nullptr, theta, nullptr,
+                           W, nullptr, Wc, z, stream);
+}
+
 int ttm_mlp_gelu(const float* x, float* y, float* dy, int n, void* stream) {
     if (n < 0 || (n > 0 && (!x || !y))) return TTM_ERR_INVALID_ARG;
     if (overlap({y, (size_t)n * 4}, {x, (size_t)n * 4}) && y != x) return TTM_ERR_INVALID_ARG;

@@ -37,8 +37,12 @@ def test_policy_round_trip(L):
     assert ttm.set_kernel_policy("auto") == "auto"
 
 
-# Fake, never-dereferenced device addresses: validation rejects before any use.
+# Fake device addresses: validation must reject every call that gets them
+# before any use.  Tests that pass them run only where no GPU is reachable, so
+# that a regression in validation can never launch a kernel on them.
 A = 1 << 20
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="passes fake device addresses; host-only")
 
 
 def P(i, misalign=0):
@@ -51,6 +55,7 @@ def lin_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=4, dt=1, q=P(0), k=P(1), v=P(
                             z, W, ws, wsb, None)
 
 
+@host_only
 def test_linear_rejects_malformed(L):
     assert lin_call(L, B=0) == INVALID
     assert lin_call(L, T=-1) == INVALID
@@ -67,6 +72,7 @@ def test_linear_rejects_malformed(L):
     assert lin_call(L, W=P(4), shared=1) == INVALID   # in place only when not shared
 
 
+@host_only
 def test_titans_and_mlp_reject_malformed(L):
     r = L.ttm_titans_fwd(1, 1, 8, 64, 64, 4, 1, P(0), P(1), P(2), P(3), P(4), P(5), P(6),
                          P(7), 0, P(8), P(9), P(9), None, 0, None)
@@ -82,12 +88,14 @@ def test_titans_and_mlp_reject_malformed(L):
     assert r == INVALID                            # d not a multiple of 8
 
 
+@host_only
 def test_tc_policy_reports_unsupported_on_host(L):
     with ttm.kernel_policy("tc"):
         # fp32 inputs never run on the tensor-core kernel
         assert lin_call(L, dt=0) == UNSUPPORTED
 
 
+@host_only
 def test_workspace_size_and_checks(L):
     # tensor-core shapes need one 17424-byte record per (sequence, 64-token chunk)
     with ttm.kernel_policy("tc"):
@@ -102,7 +110,7 @@ def test_workspace_size_and_checks(L):
         assert L.ttm_linear_workspace_size(2, 3, 130, 128, 128, 64, 1) == 0
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a GPU")
+@host_only
 def test_valid_call_without_gpu_reports_cuda_error(L):
     assert lin_call(L) == CUDA
 
@@ -111,3 +119,32 @@ def test_python_layer_raises(L):
     with pytest.raises(ttm.TTMError) as e:
         ttm._check(INVALID, "ttm_linear_fwd")
     assert e.value.code == INVALID
+
+
+def step_call(L, B=1, H=1, n=1, dk=64, dv=64, chunk=4, pos=0, dt=1, q=P(0), k=P(1), v=P(2),
+              eta=None, theta=P(3), alpha=None, W=P(4), S=None, Wc=P(5), z=P(6)):
+    return L.ttm_titans_step(B, H, n, dk, dv, chunk, pos, dt, q, k, v, eta, theta, alpha, W, S,
+                             Wc, z, None)
+
+
+@host_only
+def test_step_rejects_malformed(L):
+    assert step_call(L, n=0) == INVALID
+    assert step_call(L, pos=-1) == INVALID
+    assert step_call(L, pos=4) == INVALID              # position must be inside the chunk
+    assert step_call(L, chunk=0) == INVALID
+    assert step_call(L, theta=None) == INVALID
+    assert step_call(L, Wc=None) == INVALID
+    assert step_call(L, eta=P(7)) == INVALID            # momentum without its state
+    assert step_call(L, dk=12) == INVALID
+    assert step_call(L, W=P(1)) == INVALID              # state overlaps an input
+    assert step_call(L, Wc=P(4)) == INVALID             # outputs overlap each other
+    assert step_call(L, q=P(0, 8)) == INVALID           # misaligned
+    assert step_call(L, dk=520) == UNSUPPORTED          # one warp per row holds <= 512 columns
+    assert L.ttm_linear_step(1, 1, 1, 64, 64, 4, 5, 1, P(0), P(1), P(2), P(3), P(4), P(5),
+                             P(6), None) == INVALID
+
+
+@host_only
+def test_step_valid_call_without_gpu_reports_cuda_error(L):
+    assert step_call(L, eta=P(7), S=P(8), alpha=P(9)) == CUDA

@@ -69,9 +69,16 @@ def test_noalloc_matches_titans_fwd_twice(L):
 def test_noalloc_refuses_more_than_its_scratch(L):
     import test_neural_memory_gb300 as ttm
     # 16 sequences x 64 chunks x 17424 bytes = 17.8 MB > 16 MiB: refused on the
-    # host before any argument is read (the pointers are never dereferenced)
-    fake = ctypes.c_void_p(1 << 20)
+    # host.  The buffers are real and full-sized all the same, so that a call
+    # that got through by mistake would stay inside memory it owns.
+    tok = lambda: torch.zeros((1, 16, 4096, 128), dtype=torch.bfloat16, device="cuda")
+    st = lambda: torch.zeros((1, 16, 128, 128), dtype=torch.float32, device="cuda")
+    q, k, v, z = tok(), tok(), tok(), tok()
+    theta = torch.zeros((1, 16, 4096), dtype=torch.float32, device="cuda")
+    W0, W = st(), st()
     with ttm.kernel_policy("auto"):
-        rc = L.ttm_titans_fwd_noalloc(1, 16, 4096, 128, 128, 64, 1, fake, fake, fake, None,
-                                      fake, None, fake, None, 0, fake, fake, None, None)
+        rc = L.ttm_titans_fwd_noalloc(1, 16, 4096, 128, 128, 64, 1, _ptr(q), _ptr(k), _ptr(v),
+                                      None, _ptr(theta), None, _ptr(W0), None, 0, _ptr(z),
+                                      _ptr(W), None, None)
+    torch.cuda.synchronize()
     assert rc == ttm.ERR_UNSUPPORTED
