@@ -101,7 +101,8 @@ def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
 
 def kernel_source_digest(kernel_name: str) -> str:
     src = {"linear_simt": "scan_simt.cu", "mlp_simt": "scan_simt.cu",
-           "linear_tc": "scan_linear_tc.cu", "mlp_tc": "scan_mlp_tc.cu"}.get(kernel_name)
+           "linear_tc": "scan_linear_tc.cu", "mlp_tc": "scan_mlp_tc.cu",
+           "linear_step": "step.cu"}.get(kernel_name)
     if not src:
         return ""
     path = os.path.join(ROOT, "test_neural_memory_gb300", "csrc", src)
@@ -112,24 +113,21 @@ def kernel_source_digest(kernel_name: str) -> str:
         return ""
 
 
-def profiled_traffic(kernel_name: str, w: wl.Workload):
+def profiled_traffic(kernel_name: str, w):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel source changed since the counters were taken.  `w` is a workload,
+    or the key of a decode configuration ("decode_n1", ...)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             j = json.load(f)
     except (OSError, ValueError):
         return None
-    e = j.get(f"{kernel_name}/workload{w.id}")
+    e = j.get(f"{kernel_name}/{w}" if isinstance(w, str) else f"{kernel_name}/workload{w.id}")
     if not e or e.get("source_sha256_16") != kernel_source_digest(kernel_name):
         return None
     return e.get("dram_bytes_per_launch")
 
-
-# ----------------------------------------------------------------------------
-# clocks sampled while the GPU is under load
-# ----------------------------------------------------------------------------
 
 # ----------------------------------------------------------------------------
 # decode step (--mode decode): n tokens per sequence per call, state resident
@@ -235,7 +233,8 @@ def run_decode(args, rank, world, dev):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": src,
                      "kernel": "linear_step", "algorithmic_bytes": a["bytes"],
-                     "algorithmic_flops": a["flops"], "traffic": None},
+                     "algorithmic_flops": a["flops"],
+                     "traffic": profiled_traffic("linear_step", f"decode_n{n}")},
         "e2e": {"value": tokens * world / (ems / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hz.numel() * hz.element_size(),
                 "steps": args.steps, "ms_per_step": ems},
@@ -267,6 +266,10 @@ def oracle_decode_sample(B, H, d, chunk, seconds) -> dict:
             "kind": "oracle", "seconds": el,
             "sample": f"{seqs} sequences x {T} tokens (d={d}), token loop, float64, x{reps}"}
 
+
+# ----------------------------------------------------------------------------
+# clocks sampled while the GPU is under load
+# ----------------------------------------------------------------------------
 
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
