@@ -47,6 +47,9 @@ def _load():
         lib.oracle_linear_primal.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, d, d, i,
                                              d, d, d, i]
         lib.oracle_linear_primal.restype = i
+        lib.oracle_linear_primal_bwd.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, d, d, i,
+                                                 d, d, d, d, d, d, d, d, d, d, d, i]
+        lib.oracle_linear_primal_bwd.restype = i
         lib.oracle_mlp_primal.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, d, d, d, d, i,
                                           d, d, d, d, d, i]
         lib.oracle_mlp_primal.restype = i
@@ -106,6 +109,48 @@ def linear_primal(q, k, v, theta, W0, chunk, eta=None, alpha=None, S0=None,
     if used < 0:
         raise ValueError("oracle_linear_primal rejected its arguments")
     return Result(z=z, W=W, S=S, threads=used)
+
+
+def linear_primal_bwd(q, k, v, theta, W0, chunk, dz, eta=None, alpha=None, S0=None, dW=None,
+                      dS=None, shared_over_batch=False, threads=0) -> Result:
+    """Gradient of the linear / Titans memory scan in float64, by reverse mode
+    through the token loop of `linear_primal`.
+
+    For the outer loss L with dL/dz = dz [B,H,T,dv], dL/dW_T = dW and
+    dL/dS_T = dS ([B,H,dv,dk] or None = 0), returns dq, dk [B,H,T,dk],
+    dv [B,H,T,dv], dtheta [B,H,T], deta / dalpha [B,H,T] (None when the gate
+    is None), dW0 / dS0 shaped like W0 (summed over the batch when W0 is
+    shared) and the thread count.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    theta = _f64(theta, (B, H, T))
+    eta = _f64(eta, (B, H, T)) if eta is not None else None
+    alpha = _f64(alpha, (B, H, T)) if alpha is not None else None
+    nb = 1 if shared_over_batch else B
+    W0 = _f64(W0, (nb, H, dv, dk))
+    S0 = _f64(S0, (nb, H, dv, dk)) if S0 is not None else None
+    dz = _f64(dz, (B, H, T, dv))
+    dW = _f64(dW, (B, H, dv, dk)) if dW is not None else None
+    dS = _f64(dS, (B, H, dv, dk)) if dS is not None else None
+    out = dict(dq=np.zeros((B, H, T, dk)), dk=np.zeros((B, H, T, dk)),
+               dv=np.zeros((B, H, T, dv)), dtheta=np.zeros((B, H, T)),
+               deta=np.zeros((B, H, T)) if eta is not None else None,
+               dalpha=np.zeros((B, H, T)) if alpha is not None else None,
+               dW0=np.zeros((B, H, dv, dk)), dS0=np.zeros((B, H, dv, dk)))
+    o = out
+    used = _load().oracle_linear_primal_bwd(
+        B, H, T, dk, dv, int(chunk), _ptr(q), _ptr(k), _ptr(v), _ptr(eta), _ptr(theta),
+        _ptr(alpha), _ptr(W0), _ptr(S0), int(bool(shared_over_batch)), _ptr(dz), _ptr(dW),
+        _ptr(dS), _ptr(o["dq"]), _ptr(o["dk"]), _ptr(o["dv"]), _ptr(o["deta"]),
+        _ptr(o["dtheta"]), _ptr(o["dalpha"]), _ptr(o["dW0"]), _ptr(o["dS0"]), int(threads))
+    if used < 0:
+        raise ValueError("oracle_linear_primal_bwd rejected its arguments")
+    if shared_over_batch:
+        o["dW0"] = o["dW0"].sum(axis=0, keepdims=True)
+        o["dS0"] = o["dS0"].sum(axis=0, keepdims=True)
+    return Result(**o, threads=used)
 
 
 def mlp_primal(q, k, v, theta, W1_0, W2_0, chunk, eta=None, alpha=None, S1_0=None, S2_0=None,

@@ -43,6 +43,15 @@
  *   W_out, S_out [B][H][dv][dk]      (S_out may be NULL)
  * Deep memory: W1 [.][H][hidden][d], W2 [.][H][d][hidden], same for S1, S2.
  *
+ * The gradient of the linear / Titans scan (oracle_linear_primal_bwd) is the
+ * reverse-mode derivative of the same token loop, taken step by step in the
+ * opposite order ("Continual Learning: From Attention to Neural Memory" §4.5:
+ * the outer gradient follows the chain of state transitions backward; the
+ * update is ordinary arithmetic and every step of it is differentiated, the
+ * chunk-start snapshot included).  For a scalar outer loss L with adjoints
+ * dz_t = dL/dz_t, dW_T = dL/dW_T, dS_T = dL/dS_T it returns dL/d of every
+ * input: q, k, v, eta, theta, alpha, W0, S0.
+ *
  * The (b, h) sequences are independent, so they are spread over POSIX
  * threads; each one runs the plain loop below.
  */
@@ -243,11 +252,170 @@ static void mlp_one(const mlp_args* a, int b, int h) {
 }
 
 /* ------------------------------------------------------------------ */
+/* gradient of the linear / Titans memory (reverse mode)              */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int B, H, T, dk, dv, chunk;
+    const double *q, *k, *v, *eta, *theta, *alpha, *W0, *S0;
+    int shared;
+    const double *dz, *dWT, *dST;              /* adjoints of the outputs (dWT, dST may be NULL) */
+    double *dq, *dk_, *dv_, *deta, *dtheta, *dalpha; /* deta / dalpha NULL when the gate is */
+    double *dW0, *dS0;                          /* [B][H][dv][dk], per sequence */
+} lin_bwd_args;
+
+/* one token of the forward loop, from (W, S) = state before token t and the
+   chunk snapshot Wc; leaves the state after the token in (W, S) */
+static void lin_token(int dk, int dv, const double* Wc, double* W, double* S, const double* kt,
+                      const double* vt, double th, double et, double al, double* e) {
+    for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += Wc[(size_t)i * dk + j] * kt[j];
+        e[i] = acc - vt[i];
+    }
+    for (int i = 0; i < dv; ++i)
+        for (int j = 0; j < dk; ++j) {
+            const size_t ij = (size_t)i * dk + j;
+            S[ij] = et * S[ij] - th * 2.0 * e[i] * kt[j];
+            W[ij] = (1.0 - al) * W[ij] + S[ij];
+        }
+}
+
+static void lin_bwd_one(const lin_bwd_args* a, int b, int h) {
+    const int T = a->T, dk = a->dk, dv = a->dv, bc = a->chunk;
+    const size_t seq = (size_t)b * a->H + h;
+    const size_t init = (size_t)(a->shared ? 0 : b) * a->H + h;
+    const size_t ns = (size_t)dv * dk, nsb = ns * sizeof(double);
+    const int nchunks = (T + bc - 1) / bc;
+
+    /* forward once, keeping the state at every chunk start */
+    double* Wck = (double*)malloc((size_t)(nchunks + 1) * nsb);
+    double* Sck = (double*)malloc((size_t)(nchunks + 1) * nsb);
+    double* W = (double*)malloc(nsb);
+    double* S = (double*)malloc(nsb);
+    double* e = (double*)malloc((size_t)dv * sizeof(double));
+    memcpy(W, a->W0 + init * ns, nsb);
+    if (a->S0) memcpy(S, a->S0 + init * ns, nsb);
+    else memset(S, 0, nsb);
+    for (int c = 0; c < nchunks; ++c) {
+        memcpy(Wck + (size_t)c * ns, W, nsb);
+        memcpy(Sck + (size_t)c * ns, S, nsb);
+        for (int t = c * bc; t < T && t < (c + 1) * bc; ++t) {
+            const size_t ti = seq * T + t;
+            lin_token(dk, dv, Wck + (size_t)c * ns, W, S, a->k + ti * dk, a->v + ti * dv,
+                      a->theta[ti], a->eta ? a->eta[ti] : 0.0, a->alpha ? a->alpha[ti] : 0.0, e);
+        }
+    }
+
+    /* adjoints of the current state and of the current chunk's snapshot */
+    double* dW = (double*)calloc(ns, sizeof(double));
+    double* dS = (double*)calloc(ns, sizeof(double));
+    double* dWc = (double*)calloc(ns, sizeof(double));
+    double* dSt = (double*)malloc(nsb);
+    double* de = (double*)malloc((size_t)dv * sizeof(double));
+    if (a->dWT) memcpy(dW, a->dWT + seq * ns, nsb);
+    if (a->dST) memcpy(dS, a->dST + seq * ns, nsb);
+    /* per-token states of one chunk: Wh[u] / Sh[u] = state before its token u, Wh[n] after the last */
+    double* Wh = (double*)malloc((size_t)(bc + 1) * nsb);
+    double* Sh = (double*)malloc((size_t)(bc + 1) * nsb);
+
+    for (int c = nchunks - 1; c >= 0; --c) {
+        const int t0 = c * bc, n = (T - t0 < bc) ? T - t0 : bc;
+        const double* Wc = Wck + (size_t)c * ns;
+        memcpy(Wh, Wc, nsb);
+        memcpy(Sh, Sck + (size_t)c * ns, nsb);
+        for (int u = 0; u < n; ++u) {
+            const size_t ti = seq * T + t0 + u;
+            memcpy(Wh + (size_t)(u + 1) * ns, Wh + (size_t)u * ns, nsb);
+            memcpy(Sh + (size_t)(u + 1) * ns, Sh + (size_t)u * ns, nsb);
+            lin_token(dk, dv, Wc, Wh + (size_t)(u + 1) * ns, Sh + (size_t)(u + 1) * ns,
+                      a->k + ti * dk, a->v + ti * dv, a->theta[ti], a->eta ? a->eta[ti] : 0.0,
+                      a->alpha ? a->alpha[ti] : 0.0, e);
+        }
+        for (int u = n - 1; u >= 0; --u) {
+            const size_t ti = seq * T + t0 + u;
+            const double* kt = a->k + ti * dk;
+            const double* qt = a->q + ti * dk;
+            const double* vt = a->v + ti * dv;
+            const double* dzt = a->dz + ti * dv;
+            const double th = a->theta[ti];
+            const double et = a->eta ? a->eta[ti] : 0.0;
+            const double al = a->alpha ? a->alpha[ti] : 0.0;
+            const double* Wprev = Wh + (size_t)u * ns;   /* W_{t-1} */
+            const double* Sprev = Sh + (size_t)u * ns;   /* S_{t-1} */
+            const double* Wnow = Wh + (size_t)(u + 1) * ns; /* W_t */
+            double* dqt = a->dq + ti * dk;
+            double* dkt = a->dk_ + ti * dk;
+            double* dvt = a->dv_ + ti * dv;
+
+            /* read z_t = W_t q_t */
+            for (int j = 0; j < dk; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dv; ++i) acc += Wnow[(size_t)i * dk + j] * dzt[i];
+                dqt[j] = acc;
+            }
+            for (int i = 0; i < dv; ++i)
+                for (int j = 0; j < dk; ++j) dW[(size_t)i * dk + j] += dzt[i] * qt[j];
+
+            /* forgetting W_t = (1 - alpha_t) W_{t-1} + S_t */
+            double dal = 0.0;
+            for (size_t ij = 0; ij < ns; ++ij) {
+                dal -= dW[ij] * Wprev[ij];
+                dSt[ij] = dS[ij] + dW[ij];   /* S_t feeds W_t and S_{t+1} */
+                dW[ij] *= (1.0 - al);        /* now the adjoint of W_{t-1} */
+            }
+            if (a->dalpha) a->dalpha[ti] = dal;
+
+            /* error at the snapshot, e = Wc k_t - v_t (recomputed) */
+            for (int i = 0; i < dv; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dk; ++j) acc += Wc[(size_t)i * dk + j] * kt[j];
+                e[i] = acc - vt[i];
+            }
+            /* momentum S_t = eta_t S_{t-1} - theta_t g_t, g_t = 2 e k_t^T */
+            double det = 0.0, dth = 0.0;
+            for (int i = 0; i < dv; ++i) de[i] = 0.0;
+            for (int j = 0; j < dk; ++j) dkt[j] = 0.0;
+            for (int i = 0; i < dv; ++i)
+                for (int j = 0; j < dk; ++j) {
+                    const size_t ij = (size_t)i * dk + j;
+                    det += dSt[ij] * Sprev[ij];
+                    dth -= dSt[ij] * 2.0 * e[i] * kt[j];
+                    const double dg = -th * dSt[ij];  /* adjoint of g_t[i][j] */
+                    de[i] += 2.0 * dg * kt[j];
+                    dkt[j] += 2.0 * dg * e[i];
+                    dS[ij] = et * dSt[ij];            /* adjoint of S_{t-1} */
+                }
+            if (a->deta) a->deta[ti] = det;
+            a->dtheta[ti] = dth;
+
+            /* e = Wc k_t - v_t */
+            for (int i = 0; i < dv; ++i) {
+                dvt[i] = -de[i];
+                for (int j = 0; j < dk; ++j) {
+                    dWc[(size_t)i * dk + j] += de[i] * kt[j];
+                    dkt[j] += Wc[(size_t)i * dk + j] * de[i];
+                }
+            }
+        }
+        /* the chunk's first token took its snapshot: Wc = W before it */
+        for (size_t ij = 0; ij < ns; ++ij) {
+            dW[ij] += dWc[ij];
+            dWc[ij] = 0.0;
+        }
+    }
+    memcpy(a->dW0 + seq * ns, dW, nsb);
+    if (a->dS0) memcpy(a->dS0 + seq * ns, dS, nsb);
+    free(Wck); free(Sck); free(W); free(S); free(e); free(dW); free(dS); free(dWc); free(dSt);
+    free(de); free(Wh); free(Sh);
+}
+
+/* ------------------------------------------------------------------ */
 /* thread pool over the independent (b, h) sequences                  */
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int kind; /* 0 linear, 1 mlp */
+    int kind; /* 0 linear, 1 mlp, 2 linear gradient */
     const void* args;
     int units, next;
     pthread_mutex_t lock;
@@ -263,9 +431,12 @@ static void* worker(void* p) {
         if (pool->kind == 0) {
             const lin_args* a = (const lin_args*)pool->args;
             lin_one(a, u / a->H, u % a->H);
-        } else {
+        } else if (pool->kind == 1) {
             const mlp_args* a = (const mlp_args*)pool->args;
             mlp_one(a, u / a->H, u % a->H);
+        } else {
+            const lin_bwd_args* a = (const lin_bwd_args*)pool->args;
+            lin_bwd_one(a, u / a->H, u % a->H);
         }
     }
     return NULL;
@@ -310,4 +481,24 @@ int oracle_mlp_primal(int B, int H, int T, int d, int hidden, int chunk,
     mlp_args a = {B, H, T, d, hidden, chunk, q, k, v, eta, theta, alpha, W1_0, W2_0,
                   S1_0, S2_0, shared_over_batch, z, W1_out, W2_out, S1_out, S2_out};
     return run_pool(1, &a, B * H, nthreads);
+}
+
+/* Gradient of the linear / Titans scan.  dz [B][H][T][dv]; dWT, dST
+   [B][H][dv][dk] or NULL (= 0).  Outputs dq, dk [B][H][T][dk], dv [B][H][T][dv],
+   deta, dtheta, dalpha [B][H][T] (deta / dalpha may be NULL and must be when
+   eta / alpha are), dW0 and dS0 [B][H][dv][dk] per sequence (the caller sums
+   over the batch when W0 is shared; dS0 may be NULL). */
+int oracle_linear_primal_bwd(int B, int H, int T, int dk, int dv, int chunk,
+                             const double* q, const double* k, const double* v,
+                             const double* eta, const double* theta, const double* alpha,
+                             const double* W0, const double* S0, int shared_over_batch,
+                             const double* dz, const double* dWT, const double* dST,
+                             double* dq, double* dk_, double* dv_, double* deta, double* dtheta,
+                             double* dalpha, double* dW0, double* dS0, int nthreads) {
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1) return -1;
+    if ((deta && !eta) || (dalpha && !alpha)) return -1;
+    lin_bwd_args a = {B, H, T, dk, dv, chunk, q, k, v, eta, theta, alpha, W0, S0,
+                      shared_over_batch, dz, dWT, dST, dq, dk_, dv_, deta, dtheta, dalpha,
+                      dW0, dS0};
+    return run_pool(2, &a, B * H, nthreads);
 }
