@@ -228,6 +228,56 @@ int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int
                     const void* q, const void* k, const void* v, const float* theta,
                     float* W, float* Wc, void* z, void* stream);
 
+/* Gradient of the linear / Titans scan (the outer, "meta" gradient): the
+ * derivative of a scalar outer loss L with respect to every input of
+ * ttm_titans_fwd, given the adjoints of its outputs.  The outer loss trains
+ * the projections, the rates and W0 through the inner updates, so the
+ * gradient follows the chain of state transitions backward, through every
+ * write ("Continual Learning: From Attention to Neural Memory" §4.5 and its
+ * expanded note; "TTT layers 与 fast weights" §1.2, which also prescribes the
+ * finite-difference and primal / dual gradient checks).
+ *   Inputs: exactly those of the ttm_titans_fwd call whose outputs the
+ *     adjoints belong to (same shapes, dtype, layouts, shared flag).
+ *   dz: [B][H][T][dv] in dtype, dL/dz.  dW, dS: [B][H][dv][dk] fp32, dL/dW_out
+ *     and dL/dS_out (NULL = 0).
+ *   Outputs (written, fp32 unless stated): dq_out, dk_out [B][H][T][dk] and
+ *     dv_out [B][H][T][dv] in dtype (dL/dq, dL/dk, dL/dv); dtheta [B][H][T]; deta, dalpha [B][H][T] (NULL to
+ *     skip; must be NULL when eta / alpha are); dW0, dS0 shaped like W0 / S0
+ *     ([1][H][dv][dk] summed over the batch when W0 is shared; dS0 NULL to skip).
+ *   workspace: device scratch of ttm_titans_bwd_workspace_size() bytes (may be
+ *     NULL when T = 0): the state and its adjoint at every chunk boundary plus
+ *     per-chunk coefficient records.  Contents on return are unspecified.
+ *   All pointers are device memory owned by the caller, 16-byte aligned; no
+ *   output may overlap an input, another output or the workspace.
+ * Shapes: as for ttm_titans_fwd, with chunk <= 64 and dk <= 128
+ * (TTM_ERR_UNSUPPORTED otherwise).  Computation is fp32 (CUDA cores) on the
+ * chunk form: the forward scan writes the state at every chunk start, a
+ * reverse pass over the chunks carries the adjoint of the state, and a
+ * chunk-parallel pass forms the token gradients.  Asynchronous on `stream`;
+ * TTM_ERR_INVALID_ARG for malformed arguments or a short workspace,
+ * TTM_ERR_CUDA if a launch fails. */
+size_t ttm_titans_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                                     int w0_shared_over_batch);
+int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                   const void* q, const void* k, const void* v,
+                   const float* eta, const float* theta, const float* alpha,
+                   const float* W0, const float* S0, int w0_shared_over_batch,
+                   const void* dz, const float* dW, const float* dS,
+                   void* dq_out, void* dk_out, void* dv_out,
+                   float* deta, float* dtheta, float* dalpha,
+                   float* dW0, float* dS0,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Gradient of TTT-Linear (no momentum, no forgetting): ttm_titans_bwd with
+ * eta = alpha = S0 = dS = NULL and no deta / dalpha / dS0; the workspace size
+ * is ttm_titans_bwd_workspace_size() of the same shape. */
+int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                   const void* q, const void* k, const void* v, const float* theta,
+                   const float* W0, int w0_shared_over_batch,
+                   const void* dz, const float* dW,
+                   void* dq_out, void* dk_out, void* dv_out, float* dtheta, float* dW0,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* The activation of the 2-layer memory and its derivative, evaluated on the
  * device exactly as the tensor-core 2-layer kernel evaluates them: for the n
  * values x[i], y[i] = GELU(x) = x Phi(x) and, if dy is not NULL,

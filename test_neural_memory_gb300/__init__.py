@@ -50,6 +50,11 @@ def lib() -> ctypes.CDLL:
         L.ttm_mlp_gelu.argtypes = [p, p, p, i, p]
         L.ttm_titans_step.argtypes = [i] * 8 + [p] * 6 + [p] * 4 + [p]
         L.ttm_linear_step.argtypes = [i] * 8 + [p] * 4 + [p] * 3 + [p]
+        L.ttm_titans_bwd_workspace_size.argtypes = [i] * 8
+        L.ttm_titans_bwd_workspace_size.restype = sz
+        L.ttm_titans_bwd.argtypes = ([i] * 7 + [p] * 6 + [p, p, i] + [p] * 3 + [p] * 3 +
+                                     [p] * 5 + [p, sz, p])
+        L.ttm_linear_bwd.argtypes = [i] * 7 + [p] * 4 + [p, i] + [p] * 7 + [p, sz, p]
         L.ttm_mlp_gelu.restype = i
         for f in (L.ttm_linear_fwd, L.ttm_titans_fwd, L.ttm_mlp_fwd):
             f.restype = i
@@ -206,6 +211,40 @@ def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, 
                                  _ptr(S), _ptr(Wc), _ptr(z), _stream(q, stream)),
            "ttm_titans_step")
     return z, Wc, (pos + n) % chunk
+
+
+def titans_bwd(q, k, v, theta, W0, chunk, dz, *, eta=None, alpha=None, S0=None, dW=None,
+               dS=None, w0_shared=False, want_gates=True, want_dS0=True, workspace=None,
+               stream=None):
+    """Gradient of the Titans (or, with eta = alpha = None, TTT-Linear) scan for the
+    adjoints dz ([B,H,T,dv], dtype of v), dW / dS ([B,H,dv,dk] fp32 or None).
+    Returns a dict with dq, dk, dv (dtype of q), dtheta, deta, dalpha ([B,H,T] fp32;
+    deta / dalpha None when the gate is None or want_gates is False), dW0, dS0 (shaped
+    like W0; dS0 None when want_dS0 is False)."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    f32 = lambda shape: torch.empty(shape, dtype=torch.float32, device=dev)
+    g = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+             dtheta=f32((B, H, T)),
+             deta=f32((B, H, T)) if (eta is not None and want_gates) else None,
+             dalpha=f32((B, H, T)) if (alpha is not None and want_gates) else None,
+             dW0=f32(tuple(W0.shape)), dS0=f32(tuple(W0.shape)) if want_dS0 else None)
+    if workspace is None:
+        n = int(lib().ttm_titans_bwd_workspace_size(B, H, T, dk, dv, int(chunk), _dtype_code(q),
+                                                    int(bool(w0_shared))))
+        if n == 0 and T > 0:
+            raise TTMError(ERR_UNSUPPORTED, "ttm_titans_bwd_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+    wp, wb = _ws(workspace)
+    _check(lib().ttm_titans_bwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W0), _ptr(S0),
+                                int(bool(w0_shared)), _ptr(dz), _ptr(dW), _ptr(dS), _ptr(g["dq"]),
+                                _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["deta"]), _ptr(g["dtheta"]),
+                                _ptr(g["dalpha"]), _ptr(g["dW0"]), _ptr(g["dS0"]), wp, wb,
+                                _stream(q, stream)), "ttm_titans_bwd")
+    return g
 
 
 def mlp_fwd(q, k, v, theta, W1_0, W2_0, chunk, *, eta=None, alpha=None, S1_0=None, S2_0=None,

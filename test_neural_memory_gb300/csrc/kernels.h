@@ -21,6 +21,10 @@ struct LinearArgs {
     void* workspace;                    // caller-provided device scratch (may be NULL)
     size_t workspace_bytes;
     int* status;                        // device status word (bounded waits)
+    // CUDA-core kernel only: when set, the state at every chunk start is
+    // written to ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be
+    // NULL.  The gradient passes read these checkpoints.
+    float* ckpt;
 };
 
 struct MlpArgs {
@@ -47,6 +51,27 @@ struct StepArgs {
     void* z;
 };
 
+// One call of the gradient of the linear / Titans scan (scan_bwd.cu).  Inputs
+// as in LinearArgs plus the adjoints of the outputs; every output is a
+// gradient of the same shape as its input (dq / dk / dv in the input dtype,
+// the rest fp32).  dW / dS (adjoints of the final state), deta, dalpha and dS0
+// may be NULL.
+struct BwdArgs {
+    int B, H, T, dk, dv, chunk;
+    int bf16;
+    const void *q, *k, *v;
+    const float *eta, *theta, *alpha;
+    const float *W0, *S0;
+    int shared;
+    const void* dz;
+    const float *dW, *dS;
+    void *dq, *dk_, *dv_;
+    float *deta, *dtheta, *dalpha;
+    float *dW0, *dS0;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
 // fp32 CUDA-core kernels (scan_simt.cu).  The *_supported functions decide
 // on the host whether a shape fits the kernel's on-chip budget.
 bool linear_simt_supported(const LinearArgs& a);
@@ -68,6 +93,12 @@ cudaError_t mlp_tc_launch(const MlpArgs& a, cudaStream_t s);
 // Decode step (step.cu): one warp per row of W; dk <= 512.
 bool linear_step_supported(const StepArgs& a);
 cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
+
+// Gradient of the linear / Titans scan (scan_bwd.cu): chunk <= 64, dk <= 128.
+// The workspace holds the state and its adjoint at every chunk boundary.
+bool linear_bwd_supported(const BwdArgs& a);
+size_t linear_bwd_workspace_bytes(const BwdArgs& a);
+cudaError_t linear_bwd_launch(const BwdArgs& a, cudaStream_t s, int* launches);
 
 // The activation of that kernel on n values: y = GELU(x), dy = GELU'(x) (dy may be NULL).
 cudaError_t mlp_gelu_launch(const float* x, float* y, float* dy, int n, cudaStream_t s);

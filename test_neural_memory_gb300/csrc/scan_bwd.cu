@@ -1,0 +1,693 @@
+// Gradient of the chunked linear / Titans memory scan (fp32 CUDA-core kernels).
+//
+// The outer loss trains the projections, the rates and W0 through the inner
+// updates, so the gradient follows the chain of state transitions backward
+// ("Continual Learning: From Attention to Neural Memory" §4.5; the pages ask
+// for the primal / dual and finite-difference gradient checks in
+// "TTT layers 与 fast weights" §1.2).  It is taken here through the chunk
+// ("dual") form that the forward scan uses ("TTT layers 与 fast weights" §1.1
+// eqs (7)-(9); momentum and decay unrolled as in "论文速览 | Titans" §4.3 and
+// §4.5).  Inside a chunk of n tokens starting from (W, S), with e_s = W k_s - v_s,
+// A[t][s] = C[t][s] (k_s . q_t) for s <= t:
+//
+//   z_t   = beta_t W q_t + c_t S q_t - 2 sum_{s<=t} A[t][s] e_s
+//   W_end = beta_n W + c_n S - 2 sum_s C[n][s] e_s k_s^T
+//   S_end = P_n S - 2 sum_s pm[s] e_s k_s^T,     pm[s] = theta_s m(s, n)
+//
+// (index n = the chunk's last token).  Given the adjoints dz_t, dWe = dL/dW_end
+// and dSe = dL/dS_end, the chunk's backward is
+//
+//   de_s  = -2 sum_{t>=s} A[t][s] dz_t - 2 C[n][s] dWe k_s - 2 pm[s] dSe k_s,  dv_s = -de_s
+//   dW    = beta_n dWe + sum_t beta_t dz_t q_t^T + sum_s de_s k_s^T            (chunk start)
+//   dS    = c_n dWe + P_n dSe + sum_t c_t dz_t q_t^T
+//   dq_t  = beta_t W^T dz_t + c_t S^T dz_t - 2 sum_{s<=t} C[t][s] (dz_t . e_s) k_s
+//   dk_s  = W^T de_s - 2 sum_{t>=s} C[t][s] (dz_t . e_s) q_t - 2 C[n][s] dWe^T e_s
+//           - 2 pm[s] dSe^T e_s
+//
+// and the adjoints of the coefficients (dC, dpm, dbeta, dc, dP) are carried
+// back through their defining recurrences to theta, eta and alpha.
+//
+// Three passes (plus the forward scan, which writes the state at every chunk
+// start):
+//   records  one CTA per (sequence, chunk): coefficients and A, stored;
+//   chain    one CTA per (sequence, slice of rows), chunks in reverse: the
+//            adjoint (dW, dS) at every chunk end.  It needs no forward state
+//            (the chunk map is affine in the state), only A, the coefficients,
+//            q, k and dz; rows are independent, as in the forward;
+//   local    one CTA per (sequence, chunk), all chunks at once: dq, dk, dv and
+//            the gate gradients from the chunk's start state and end adjoint.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "simt_common.cuh"
+
+namespace ttm {
+namespace {
+
+using simt::block_coefficients;
+using simt::load_in;
+using simt::store_out;
+
+constexpr int kBT = 256;      // threads per CTA
+constexpr int kMaxBC = 64;    // largest chunk
+constexpr int kMaxDK = 128;   // widest key
+constexpr int kR2 = 8;        // rows of the adjoint per chain CTA
+constexpr int kR3 = 16;       // rows per tile in the local pass
+
+// Workspace carve-up (floats).  ckpt and adj hold [seq][chunk][W | S][dv][dk];
+// rec holds per (seq, chunk): A [bc][bc], beta [bc], cc [bc], clast [bc],
+// pm [bc], P_n.
+struct BwdLayout {
+    int nch, bc;
+    size_t sd, rec_f;
+    size_t ckpt, adj, rec, part, total;
+};
+
+BwdLayout bwd_layout(const BwdArgs& a) {
+    BwdLayout L;
+    L.bc = a.chunk;
+    L.nch = (a.T + a.chunk - 1) / a.chunk;
+    L.sd = (size_t)a.dv * a.dk;
+    L.rec_f = ((size_t)L.bc * L.bc + 4 * (size_t)L.bc + 1 + 3) / 4 * 4;
+    const size_t nseq = (size_t)a.B * a.H;
+    L.ckpt = 0;
+    L.adj = L.ckpt + nseq * L.nch * 2 * L.sd;
+    L.rec = L.adj + nseq * L.nch * 2 * L.sd;
+    L.part = L.rec + nseq * L.nch * L.rec_f;
+    L.total = L.part + (a.shared ? nseq * 2 * L.sd : 0);
+    return L;
+}
+
+// ------------------------------------------------------------------------
+// records: coefficients and the score-times-coefficient table A per chunk
+// ------------------------------------------------------------------------
+
+template <typename Tin>
+__global__ void __launch_bounds__(kBT) bwd_records_kernel(const BwdArgs a, const BwdLayout L,
+                                                          float* ws) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x;
+    const int seq = blockIdx.x, c = blockIdx.y;
+    const int dk = a.dk, bc = L.bc, ldk = dk + 1;
+    const int t0 = c * bc, n = min(bc, a.T - t0);
+    float* Qs = sm;                    // [bc][ldk]
+    float* Ks = Qs + bc * ldk;         // [bc][ldk]
+    float* C = Ks + bc * ldk;          // [bc][bc + 1]
+    float* th = C + bc * (bc + 1);
+    float* et = th + bc;
+    float* al = et + bc;
+    float* beta = al + bc;
+    float* P = beta + bc;
+    float* cc = P + bc;
+    float* pm = cc + bc;
+    const Tin* q = static_cast<const Tin*>(a.q);
+    const Tin* k = static_cast<const Tin*>(a.k);
+    const size_t tok0 = (size_t)seq * a.T + t0;
+    for (int x = tid; x < bc * dk; x += kBT) {
+        const int s = x / dk, j = x % dk;
+        Qs[s * ldk + j] = s < n ? load_in(q, (tok0 + s) * dk + j) : 0.f;
+        Ks[s * ldk + j] = s < n ? load_in(k, (tok0 + s) * dk + j) : 0.f;
+    }
+    for (int s = tid; s < bc; s += kBT) {
+        th[s] = s < n ? a.theta[tok0 + s] : 0.f;
+        et[s] = (s < n && a.eta) ? a.eta[tok0 + s] : 0.f;
+        al[s] = (s < n && a.alpha) ? a.alpha[tok0 + s] : 0.f;
+    }
+    __syncthreads();
+    block_coefficients(n, bc, th, et, al, beta, P, cc, C, bc + 1, pm);
+    float* rec = ws + L.rec + ((size_t)seq * L.nch + c) * L.rec_f;
+    for (int x = tid; x < bc * bc; x += kBT) {
+        const int t = x / bc, s = x % bc;
+        float acc = 0.f;
+        if (s <= t && t < n) {
+            for (int j = 0; j < dk; ++j) acc += Qs[t * ldk + j] * Ks[s * ldk + j];
+            acc *= C[t * (bc + 1) + s];
+        }
+        rec[x] = acc;
+    }
+    float* vec = rec + (size_t)bc * bc;
+    for (int s = tid; s < bc; s += kBT) {
+        vec[s] = s < n ? beta[s] : 0.f;
+        vec[bc + s] = s < n ? cc[s] : 0.f;
+        vec[2 * bc + s] = s < n ? C[(n - 1) * (bc + 1) + s] : 0.f;
+        vec[3 * bc + s] = s < n ? pm[s] : 0.f;
+    }
+    if (tid == 0) vec[4 * bc] = P[n - 1];
+}
+
+// ------------------------------------------------------------------------
+// chain: the adjoint of the state at every chunk end, chunks in reverse
+// ------------------------------------------------------------------------
+
+template <typename Tin>
+__global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const BwdLayout L,
+                                                        float* ws) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x;
+    const int seq = blockIdx.x;
+    const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = dk + 1;
+    const int r0 = blockIdx.y * kR2, nr = min(kR2, dv - r0);
+    constexpr int ldr = kR2 + 1;
+    float* Qs = sm;                    // [bc][ldk]
+    float* Ks = Qs + bc * ldk;         // [bc][ldk]
+    float* A = Ks + bc * ldk;          // [bc][bc + 1]
+    float* dZ = A + bc * (bc + 1);     // [bc][ldr]
+    float* dWK = dZ + bc * ldr;        // [bc][ldr]  (dWe k_s)_i
+    float* dSK = dWK + bc * ldr;       // [bc][ldr]  (dSe k_s)_i
+    float* de = dSK + bc * ldr;        // [bc][ldr]
+    float* dW = de + bc * ldr;         // [kR2][ldk] running adjoint of W
+    float* dS = dW + kR2 * ldk;        // [kR2][ldk] running adjoint of S
+    float* vec = dS + kR2 * ldk;       // beta, cc, clast, pm [bc] each, P_n
+    const Tin* q = static_cast<const Tin*>(a.q);
+    const Tin* k = static_cast<const Tin*>(a.k);
+    const Tin* dz = static_cast<const Tin*>(a.dz);
+
+    const size_t sd = L.sd;
+    for (int x = tid; x < kR2 * dk; x += kBT) {
+        const int i = x / dk, j = x % dk;
+        const size_t g = (size_t)seq * sd + (size_t)(r0 + i) * dk + j;
+        dW[i * ldk + j] = (i < nr && a.dW) ? a.dW[g] : 0.f;
+        dS[i * ldk + j] = (i < nr && a.dS) ? a.dS[g] : 0.f;
+    }
+    for (int c = L.nch - 1; c >= 0; --c) {
+        const int t0 = c * bc, n = min(bc, a.T - t0);
+        const size_t tok0 = (size_t)seq * a.T + t0;
+        const float* rec = ws + L.rec + ((size_t)seq * L.nch + c) * L.rec_f;
+        __syncthreads();   // the previous chunk is done with every buffer
+        // this chunk's end adjoint, for the local pass
+        float* adj = ws + L.adj + ((size_t)seq * L.nch + c) * 2 * sd;
+        for (int x = tid; x < nr * dk; x += kBT) {
+            const int i = x / dk, j = x % dk;
+            adj[(size_t)(r0 + i) * dk + j] = dW[i * ldk + j];
+            adj[sd + (size_t)(r0 + i) * dk + j] = dS[i * ldk + j];
+        }
+        for (int x = tid; x < bc * dk; x += kBT) {
+            const int s = x / dk, j = x % dk;
+            Qs[s * ldk + j] = s < n ? load_in(q, (tok0 + s) * dk + j) : 0.f;
+            Ks[s * ldk + j] = s < n ? load_in(k, (tok0 + s) * dk + j) : 0.f;
+        }
+        for (int x = tid; x < bc * bc; x += kBT) A[(x / bc) * (bc + 1) + x % bc] = rec[x];
+        for (int x = tid; x < 4 * bc + 1; x += kBT) vec[x] = rec[(size_t)bc * bc + x];
+        for (int x = tid; x < bc * kR2; x += kBT) {
+            const int s = x / kR2, i = x % kR2;
+            dZ[s * ldr + i] = (s < n && i < nr) ? load_in(dz, (tok0 + s) * dv + r0 + i) : 0.f;
+        }
+        __syncthreads();
+        const float* beta = vec;
+        const float* cc = vec + bc;
+        const float* clast = vec + 2 * bc;
+        const float* pm = vec + 3 * bc;
+        const float Pn = vec[4 * bc];
+        for (int x = tid; x < bc * kR2; x += kBT) {
+            const int s = x / kR2, i = x % kR2;
+            float uw = 0.f, us = 0.f;
+            for (int j = 0; j < dk; ++j) {
+                const float ks = Ks[s * ldk + j];
+                uw += dW[i * ldk + j] * ks;
+                us += dS[i * ldk + j] * ks;
+            }
+            dWK[s * ldr + i] = uw;
+            dSK[s * ldr + i] = us;
+        }
+        __syncthreads();
+        for (int x = tid; x < bc * kR2; x += kBT) {
+            const int s = x / kR2, i = x % kR2;
+            float acc = 0.f;
+            for (int t = s; t < n; ++t) acc += A[t * (bc + 1) + s] * dZ[t * ldr + i];
+            de[s * ldr + i] = s < n ? -2.f * (acc + clast[s] * dWK[s * ldr + i] +
+                                              pm[s] * dSK[s * ldr + i])
+                                    : 0.f;
+        }
+        __syncthreads();
+        const float bn = beta[n - 1], cn = cc[n - 1];
+        for (int x = tid; x < kR2 * dk; x += kBT) {
+            const int i = x / dk, j = x % dk;
+            float gw = 0.f, gs = 0.f;
+            for (int t = 0; t < n; ++t) {
+                const float zq = dZ[t * ldr + i] * Qs[t * ldk + j];
+                gw += beta[t] * zq + de[t * ldr + i] * Ks[t * ldk + j];
+                gs += cc[t] * zq;
+            }
+            const float w = dW[i * ldk + j], s = dS[i * ldk + j];
+            dW[i * ldk + j] = bn * w + gw;
+            dS[i * ldk + j] = cn * w + Pn * s + gs;
+        }
+    }
+    __syncthreads();
+    // adjoint of the initial state: per sequence, or a per-sequence partial
+    // that a reduction sums over the batch when W0 / S0 are shared
+    float* oW;
+    float* oS;
+    size_t base;
+    if (a.shared) {
+        oW = ws + L.part;
+        oS = oW + sd;
+        base = (size_t)seq * 2 * sd;
+    } else {
+        oW = a.dW0;
+        oS = a.dS0;
+        base = (size_t)seq * sd;
+    }
+    for (int x = tid; x < nr * dk; x += kBT) {
+        const int i = x / dk, j = x % dk;
+        const size_t g = base + (size_t)(r0 + i) * dk + j;
+        oW[g] = dW[i * ldk + j];
+        if (oS) oS[g] = dS[i * ldk + j];
+    }
+}
+
+// No tokens: the initial state is the final one, so its adjoint is the
+// final state's (summed over the batch when W0 / S0 are shared).
+__global__ void bwd_empty_kernel(const BwdArgs a, size_t sd) {
+    const size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t nout = (size_t)(a.shared ? 1 : a.B) * a.H * sd;
+    if (x >= nout) return;
+    float gw = 0.f, gs = 0.f;
+    const int nb = a.shared ? a.B : 1;
+    for (int b = 0; b < nb; ++b) {
+        const size_t src = x + (size_t)b * a.H * sd;
+        gw += a.dW ? a.dW[src] : 0.f;
+        gs += a.dS ? a.dS[src] : 0.f;
+    }
+    a.dW0[x] = gw;
+    if (a.dS0) a.dS0[x] = gs;
+}
+
+// Sums the per-sequence adjoints of a batch-shared W0 / S0 over the batch.
+__global__ void bwd_shared_reduce_kernel(const BwdArgs a, const BwdLayout L, const float* ws) {
+    const size_t sd = L.sd;
+    const size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= (size_t)a.H * sd) return;
+    const int h = (int)(x / sd);
+    const size_t e = x % sd;
+    float gw = 0.f, gs = 0.f;
+    for (int b = 0; b < a.B; ++b) {
+        const float* p = ws + L.part + ((size_t)b * a.H + h) * 2 * sd;
+        gw += p[e];
+        gs += p[sd + e];
+    }
+    a.dW0[x] = gw;
+    if (a.dS0) a.dS0[x] = gs;
+}
+
+// ------------------------------------------------------------------------
+// local: dq, dk, dv and the gate gradients of one chunk
+// ------------------------------------------------------------------------
+
+// The q / k buffers are reused at the end for the two [bc][bc + 1] tables of
+// the gate gradients, so that region holds the larger of the two uses.
+__host__ __device__ inline size_t local_qk_floats(int bc, int dk) {
+    const size_t qk = 2 * (size_t)bc * (dk + 1), tables = 2 * (size_t)bc * (bc + 1);
+    return qk > tables ? qk : tables;
+}
+
+size_t local_smem_floats(int bc, int dk) {
+    const size_t ldk = dk + 1, ldb = bc + 1, ldr = kR3 + 1;
+    return local_qk_floats(bc, dk) + 3 * bc * ldb + 4 * kR3 * ldk + 5 * bc * ldr +
+           14 * (size_t)bc + 4;
+}
+
+// A thread owns rows t = 4 tg + a (a < 4) and columns j = jg + 16 bb (bb < 8)
+// of dq / dk (tg = tid / 16, jg = tid % 16), and the 4 x 4 block of
+// DE[t][s] = dz_t . e_s with s = jg + 16 bb (bb < 4).
+template <typename Tin>
+__global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, const BwdLayout L,
+                                                           const float* ws) {
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x;
+    const int seq = blockIdx.x, c = blockIdx.y;
+    const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = dk + 1, ldb = bc + 1;
+    constexpr int ldr = kR3 + 1;
+    const int t0 = c * bc, n = min(bc, a.T - t0);
+    const size_t tok0 = (size_t)seq * a.T + t0;
+    const size_t sd = L.sd;
+
+    float* Qs = sm;                    // [bc][ldk]
+    float* Ks = Qs + bc * ldk;         // [bc][ldk]
+    float* QK = Qs + local_qk_floats(bc, dk);   // [bc][ldb]  q_t . k_s (s <= t), later dC
+    float* Cm = QK + bc * ldb;         // [bc][ldb]  C[t][s]
+    float* Xm = Cm + bc * ldb;         // [bc][ldb]  A = C QK, later C DE
+    float* Wr = Xm + bc * ldb;         // [kR3][ldk] tile of W (chunk start)
+    float* Sr = Wr + kR3 * ldk;        //            tile of S
+    float* dWr = Sr + kR3 * ldk;       //            tile of dWe (chunk end adjoint)
+    float* dSr = dWr + kR3 * ldk;      //            tile of dSe
+    float* dZt = dSr + kR3 * ldk;      // [bc][ldr]
+    float* Et = dZt + bc * ldr;        // [bc][ldr]  e_s, rows of the tile
+    float* dWK = Et + bc * ldr;        // [bc][ldr]  (dWe k_s)_i
+    float* dSK = dWK + bc * ldr;       // [bc][ldr]  (dSe k_s)_i
+    float* de = dSK + bc * ldr;        // [bc][ldr]
+    float* th = de + bc * ldr;
+    float* et = th + bc;
+    float* al = et + bc;
+    float* beta = al + bc;
+    float* P = beta + bc;
+    float* cc = P + bc;
+    float* pm = cc + bc;
+    float* dbeta = pm + bc;
+    float* dcc = dbeta + bc;
+    float* dclast = dcc + bc;          // sum_i e_s[i] (dWe k_s)[i]
+    float* dpm = dclast + bc;          // sum_i e_s[i] (dSe k_s)[i]
+    float* dkeep = dpm + bc;
+    float* deta = dkeep + bc;
+    float* dth = deta + bc;
+    float* scal = dth + bc;            // <dWe, W>, <dWe, S>, <dSe, S>
+
+    const Tin* q = static_cast<const Tin*>(a.q);
+    const Tin* k = static_cast<const Tin*>(a.k);
+    const Tin* v = static_cast<const Tin*>(a.v);
+    const Tin* dz = static_cast<const Tin*>(a.dz);
+
+    for (int x = tid; x < bc * dk; x += kBT) {
+        const int s = x / dk, j = x % dk;
+        Qs[s * ldk + j] = s < n ? load_in(q, (tok0 + s) * dk + j) : 0.f;
+        Ks[s * ldk + j] = s < n ? load_in(k, (tok0 + s) * dk + j) : 0.f;
+    }
+    for (int s = tid; s < bc; s += kBT) {
+        th[s] = s < n ? a.theta[tok0 + s] : 0.f;
+        et[s] = (s < n && a.eta) ? a.eta[tok0 + s] : 0.f;
+        al[s] = (s < n && a.alpha) ? a.alpha[tok0 + s] : 0.f;
+        dbeta[s] = dcc[s] = dclast[s] = dpm[s] = dkeep[s] = deta[s] = 0.f;
+    }
+    if (tid < 4) scal[tid] = 0.f;
+    __syncthreads();
+    block_coefficients(n, bc, th, et, al, beta, P, cc, Cm, ldb, pm);
+    for (int x = tid; x < bc * bc; x += kBT) {
+        const int t = x / bc, s = x % bc;
+        float acc = 0.f;
+        if (s <= t && t < n)
+            for (int j = 0; j < dk; ++j) acc += Qs[t * ldk + j] * Ks[s * ldk + j];
+        QK[t * ldb + s] = acc;
+        Xm[t * ldb + s] = acc * Cm[t * ldb + s];
+    }
+
+    const int tg = tid >> 4, jg = tid & 15;
+    float U[4][8], V[4][8], DK[4][8], DE[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int bb = 0; bb < 8; ++bb) U[r][bb] = V[r][bb] = DK[r][bb] = 0.f;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) DE[r][bb] = 0.f;
+    }
+
+    const float* ck = ws + L.ckpt + ((size_t)seq * L.nch + c) * 2 * sd;
+    const float* ad = ws + L.adj + ((size_t)seq * L.nch + c) * 2 * sd;
+    for (int r0 = 0; r0 < dv; r0 += kR3) {
+        const int nr = min(kR3, dv - r0);
+        __syncthreads();   // the previous tile is consumed (and the tables above are built)
+        for (int x = tid; x < kR3 * dk; x += kBT) {
+            const int i = x / dk, j = x % dk;
+            const size_t g = (size_t)(r0 + i) * dk + j;
+            const bool in = i < nr;
+            Wr[i * ldk + j] = in ? ck[g] : 0.f;
+            Sr[i * ldk + j] = in ? ck[sd + g] : 0.f;
+            dWr[i * ldk + j] = in ? ad[g] : 0.f;
+            dSr[i * ldk + j] = in ? ad[sd + g] : 0.f;
+        }
+        for (int x = tid; x < bc * kR3; x += kBT) {
+            const int s = x / kR3, i = x % kR3;
+            dZt[s * ldr + i] = (s < n && i < nr) ? load_in(dz, (tok0 + s) * dv + r0 + i) : 0.f;
+        }
+        __syncthreads();
+        {   // errors at the chunk start and the end adjoints applied to each key
+            const int i = tid & 15, sg = tid >> 4;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int s = sg * 4 + r;
+                if (s >= bc) continue;
+                float e = 0.f, uw = 0.f, us = 0.f;
+                for (int j = 0; j < dk; ++j) {
+                    const float ks = Ks[s * ldk + j];
+                    e += ks * Wr[i * ldk + j];
+                    uw += ks * dWr[i * ldk + j];
+                    us += ks * dSr[i * ldk + j];
+                }
+                const bool live = s < n && i < nr;
+                e = live ? e - load_in(v, (tok0 + s) * dv + r0 + i) : 0.f;
+                Et[s * ldr + i] = e;
+                dWK[s * ldr + i] = uw;
+                dSK[s * ldr + i] = us;
+                if (live) {
+                    atomicAdd(&dclast[s], e * uw);
+                    atomicAdd(&dpm[s], e * us);
+                }
+            }
+        }
+        {   // <dWe, W>, <dWe, S>, <dSe, S> over the tile
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f;
+            for (int x = tid; x < kR3 * dk; x += kBT) {
+                const int i = x / dk, j = x % dk;
+                const float w = Wr[i * ldk + j], sv = Sr[i * ldk + j], gw = dWr[i * ldk + j];
+                p0 += gw * w;
+                p1 += gw * sv;
+                p2 += dSr[i * ldk + j] * sv;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                p0 += __shfl_xor_sync(0xffffffffu, p0, off);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, off);
+                p2 += __shfl_xor_sync(0xffffffffu, p2, off);
+            }
+            if ((tid & 31) == 0) {
+                atomicAdd(&scal[0], p0);
+                atomicAdd(&scal[1], p1);
+                atomicAdd(&scal[2], p2);
+            }
+        }
+        __syncthreads();
+        {   // de_s and dv_s
+            const int i = tid & 15, sg = tid >> 4;
+            const float* clast = Cm + (n - 1) * ldb;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int s = sg * 4 + r;
+                if (s >= bc) continue;
+                float acc = 0.f;
+                for (int t = s; t < n; ++t) acc += Xm[t * ldb + s] * dZt[t * ldr + i];
+                const float g = s < n ? -2.f * (acc + clast[s] * dWK[s * ldr + i] +
+                                                pm[s] * dSK[s * ldr + i])
+                                      : 0.f;
+                de[s * ldr + i] = g;
+                if (s < n && i < nr) store_out(static_cast<Tin*>(a.dv_), (tok0 + s) * dv + r0 + i, -g);
+            }
+        }
+        __syncthreads();
+        {   // owned blocks: U += dZ^T W, V += dZ^T S, DK += de W - 2 C_n e dWe - 2 pm e dSe,
+            // DE += dZ E^T over the tile's rows
+            const float* clast = Cm + (n - 1) * ldb;
+            float cl[4], pmv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = tg * 4 + r;
+                cl[r] = t < n ? -2.f * clast[t] : 0.f;
+                pmv[r] = t < n ? -2.f * pm[t] : 0.f;
+            }
+            for (int i = 0; i < kR3; ++i) {
+                float zt[4], dea[4], ea[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = tg * 4 + r;
+                    zt[r] = t < bc ? dZt[t * ldr + i] : 0.f;
+                    dea[r] = t < bc ? de[t * ldr + i] : 0.f;
+                    ea[r] = t < bc ? Et[t * ldr + i] : 0.f;
+                }
+#pragma unroll
+                for (int bb = 0; bb < 8; ++bb) {
+                    const int j = jg + 16 * bb;
+                    if (j >= dk) break;
+                    const float w = Wr[i * ldk + j], sv = Sr[i * ldk + j];
+                    const float gw = dWr[i * ldk + j], gs = dSr[i * ldk + j];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        U[r][bb] += zt[r] * w;
+                        V[r][bb] += zt[r] * sv;
+                        DK[r][bb] += dea[r] * w + cl[r] * ea[r] * gw + pmv[r] * ea[r] * gs;
+                    }
+                }
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int s = jg + 16 * bb;
+                    if (s >= bc) break;
+                    const float es = Et[s * ldr + i];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) DE[r][bb] += zt[r] * es;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // DE complete: dC[t][s] = -2 QK DE (+ the end-state term on the last row),
+    // and C DE for the remaining dq / dk terms
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            const int t = tg * 4 + r, s = jg + 16 * bb;
+            if (t < bc && s < bc) {
+                const float d = (s <= t && t < n) ? DE[r][bb] : 0.f;
+                const float g = -2.f * QK[t * ldb + s] * d - (t == n - 1 && s < n ? 2.f * dclast[s] : 0.f);
+                Xm[t * ldb + s] = Cm[t * ldb + s] * d;
+                QK[t * ldb + s] = g;
+            }
+        }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = tg * 4 + r;
+        if (t >= n) continue;
+        float pb = 0.f, pc = 0.f;
+#pragma unroll
+        for (int bb = 0; bb < 8; ++bb) {
+            const int j = jg + 16 * bb;
+            if (j >= dk) break;
+            float sq = 0.f, sk = 0.f;
+            for (int s = 0; s <= t; ++s) sq += Xm[t * ldb + s] * Ks[s * ldk + j];
+            for (int u = t; u < n; ++u) sk += Xm[u * ldb + t] * Qs[u * ldk + j];
+            const float qv = Qs[t * ldk + j];
+            pb += qv * U[r][bb];
+            pc += qv * V[r][bb];
+            store_out(static_cast<Tin*>(a.dq), (tok0 + t) * dk + j,
+                      beta[t] * U[r][bb] + cc[t] * V[r][bb] - 2.f * sq);
+            store_out(static_cast<Tin*>(a.dk_), (tok0 + t) * dk + j, DK[r][bb] - 2.f * sk);
+        }
+        atomicAdd(&dbeta[t], pb);
+        atomicAdd(&dcc[t], pc);
+    }
+    __syncthreads();
+    // gate gradients: C[t][s] = theta_s w(s,t), pm[s] = theta_s m(s,n-1) with
+    // m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t)
+    // (w(s,s) = m(s,s) = 1); tables of w and m reuse the q / k buffers.
+    float* Wm = Qs;                    // [bc][ldb]  w(s,t) at [t][s]
+    float* Mm = Wm + bc * ldb;         // [bc][ldb]  m(s,t) at [t][s]
+    const float* dC = QK;
+    for (int s = tid; s < n; s += kBT) {
+        float m = 1.f, w = 1.f;
+        Wm[s * ldb + s] = 1.f;
+        Mm[s * ldb + s] = 1.f;
+        for (int t = s + 1; t < n; ++t) {
+            m = et[t] * m;
+            w = (1.f - al[t]) * w + m;
+            Wm[t * ldb + s] = w;
+            Mm[t * ldb + s] = m;
+        }
+    }
+    __syncthreads();
+    for (int s = tid; s < n; s += kBT) {
+        const float ths = th[s];
+        float g = -2.f * dpm[s] * Mm[(n - 1) * ldb + s];   // d pm[s] / d theta_s
+        for (int t = s; t < n; ++t) g += dC[t * ldb + s] * Wm[t * ldb + s];
+        dth[s] = g;
+        float dw = ths * dC[(n - 1) * ldb + s];            // adjoint of w(s, n-1)
+        float dm = ths * (-2.f * dpm[s]);                  // adjoint of m(s, n-1), direct part
+        for (int t = n - 1; t > s; --t) {
+            atomicAdd(&dkeep[t], dw * Wm[(t - 1) * ldb + s]);
+            dm += dw;                                      // w(s,t) = ... + m(s,t)
+            atomicAdd(&deta[t], dm * Mm[(t - 1) * ldb + s]);
+            dm = et[t] * dm;
+            dw = (1.f - al[t]) * dw + ths * dC[(t - 1) * ldb + s];
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // beta_t = keep_t beta_{t-1}, P_t = eta_t P_{t-1}, c_t = keep_t c_{t-1} + P_t;
+        // the end state adds beta_n <dWe,W>, c_n <dWe,S> and P_n <dSe,S>
+        float rb = 0.f, rc = 0.f, rp = 0.f;
+        for (int t = n - 1; t >= 0; --t) {
+            const bool last = t == n - 1;
+            const float db = dbeta[t] + rb + (last ? scal[0] : 0.f);
+            const float dc = dcc[t] + rc + (last ? scal[1] : 0.f);
+            const float dp = rp + dc + (last ? scal[2] : 0.f);
+            const float keep = 1.f - al[t];
+            const float cprev = t > 0 ? cc[t - 1] : 0.f;
+            const float bprev = t > 0 ? beta[t - 1] : 1.f;
+            const float pprev = t > 0 ? P[t - 1] : 1.f;
+            dkeep[t] += dc * cprev + db * bprev;
+            deta[t] += dp * pprev;
+            rc = keep * dc;
+            rb = keep * db;
+            rp = et[t] * dp;
+        }
+    }
+    __syncthreads();
+    for (int t = tid; t < n; t += kBT) {
+        a.dtheta[tok0 + t] = dth[t];
+        if (a.deta) a.deta[tok0 + t] = deta[t];
+        if (a.dalpha) a.dalpha[tok0 + t] = -dkeep[t];
+    }
+}
+
+size_t records_smem_floats(int bc, int dk) {
+    return 2 * (size_t)bc * (dk + 1) + (size_t)bc * (bc + 1) + 7 * (size_t)bc;
+}
+
+size_t chain_smem_floats(int bc, int dk) {
+    return 2 * (size_t)bc * (dk + 1) + (size_t)bc * (bc + 1) + 4 * (size_t)bc * (kR2 + 1) +
+           2 * (size_t)kR2 * (dk + 1) + 4 * (size_t)bc + 1;
+}
+
+template <typename Tin>
+cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, int* launches) {
+    float* ws = static_cast<float*>(a.workspace);
+    // forward scan writing the state at every chunk start
+    LinearArgs f{};
+    f.B = a.B; f.H = a.H; f.T = a.T; f.dk = a.dk; f.dv = a.dv; f.chunk = a.chunk;
+    f.bf16 = a.bf16;
+    f.q = a.q; f.k = a.k; f.v = a.v;
+    f.eta = a.eta; f.theta = a.theta; f.alpha = a.alpha;
+    f.W0 = a.W0; f.S0 = a.S0; f.shared = a.shared;
+    f.ckpt = ws + L.ckpt;
+    cudaError_t e = linear_simt_launch(f, s);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+
+    const int nseq = a.B * a.H;
+    const size_t sm0 = records_smem_floats(L.bc, a.dk) * sizeof(float);
+    const size_t sm2 = chain_smem_floats(L.bc, a.dk) * sizeof(float);
+    const size_t sm3 = local_smem_floats(L.bc, a.dk) * sizeof(float);
+    if ((e = cudaFuncSetAttribute(bwd_records_kernel<Tin>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0)) ||
+        (e = cudaFuncSetAttribute(bwd_chain_kernel<Tin>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2)) ||
+        (e = cudaFuncSetAttribute(bwd_local_kernel<Tin>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
+        return e;
+    bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
+    bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT, sm2, s>>>(a, L, ws);
+    bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm3, s>>>(a, L, ws);
+    *launches += 3;
+    if (a.shared) {
+        const size_t n = (size_t)a.H * L.sd;
+        bwd_shared_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, L, ws);
+        ++*launches;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool linear_bwd_supported(const BwdArgs& a) {
+    LinearArgs f{};
+    f.dk = a.dk; f.chunk = a.chunk;
+    return a.chunk >= 1 && a.chunk <= kMaxBC && a.dk >= 1 && a.dk <= kMaxDK &&
+           linear_simt_supported(f) &&
+           local_smem_floats(a.chunk, a.dk) * sizeof(float) <= 227 * 1024;
+}
+
+size_t linear_bwd_workspace_bytes(const BwdArgs& a) { return bwd_layout(a).total * sizeof(float); }
+
+cudaError_t linear_bwd_launch(const BwdArgs& a, cudaStream_t s, int* launches) {
+    const BwdLayout L = bwd_layout(a);
+    if (a.T == 0) {
+        const size_t n = (size_t)(a.shared ? 1 : a.B) * a.H * L.sd;
+        bwd_empty_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, L.sd);
+        ++*launches;
+        return cudaGetLastError();
+    }
+    return a.bf16 ? launch_passes<__nv_bfloat16>(a, L, s, launches)
+                  : launch_passes<float>(a, L, s, launches);
+}
+
+}  // namespace ttm

@@ -27,59 +27,16 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "simt_common.cuh"
 
 namespace ttm {
 namespace {
 
+using simt::block_coefficients;
+using simt::load_in;
+using simt::store_out;
+
 constexpr int kThreads = 256;
-
-__device__ __forceinline__ float load_in(const float* p, size_t i) { return p[i]; }
-__device__ __forceinline__ float load_in(const __nv_bfloat16* p, size_t i) {
-    return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ void store_out(float* p, size_t i, float x) { p[i] = x; }
-__device__ __forceinline__ void store_out(__nv_bfloat16* p, size_t i, float x) {
-    p[i] = __float2bfloat16_rn(x);
-}
-
-// Per-block coefficients.  th/et/al hold the n gates of the block; writes
-// beta, P, cc (prefix forms), C[t][s] (ld = ldc, s <= t, zero above) and
-// pm[s] = theta_s m(s, n-1).  Runs on the whole block; ends with a barrier.
-__device__ void block_coefficients(int n, int nb, const float* th, const float* et,
-                                   const float* al, float* beta, float* P, float* cc,
-                                   float* C, int ldc, float* pm) {
-    const int tid = threadIdx.x;
-    if (tid == 0) {
-        float b = 1.f, p = 1.f, c = 0.f;
-        for (int t = 0; t < n; ++t) {
-            const float keep = 1.f - al[t];
-            b *= keep;
-            p *= et[t];
-            c = keep * c + p;
-            beta[t] = b;
-            P[t] = p;
-            cc[t] = c;
-        }
-    }
-    for (int s = tid; s < nb; s += blockDim.x) {
-        if (s >= n) {
-            for (int t = 0; t < nb; ++t) C[t * ldc + s] = 0.f;
-            pm[s] = 0.f;
-            continue;
-        }
-        for (int t = 0; t < s; ++t) C[t * ldc + s] = 0.f;
-        float m = 1.f, w = 1.f;
-        C[s * ldc + s] = th[s];
-        for (int t = s + 1; t < n; ++t) {
-            m = et[t] * m;
-            w = (1.f - al[t]) * w + m;
-            C[t * ldc + s] = th[s] * w;
-        }
-        for (int t = n; t < nb; ++t) C[t * ldc + s] = 0.f;
-        pm[s] = th[s] * m;
-    }
-    __syncthreads();
-}
 
 // ------------------------------------------------------------------------
 // linear / Titans memory: one CTA per (sequence, slice of kRows rows of W)
@@ -138,8 +95,17 @@ __global__ void __launch_bounds__(kThreads) linear_simt_kernel(LinearArgs p) {
     }
     __syncthreads();
 
+    const int nch = (T + p.chunk - 1) / p.chunk;
     for (int c0 = 0; c0 < T; c0 += p.chunk) {
         const int cend = min(c0 + p.chunk, T);
+        if (p.ckpt) {   // state at this chunk's start, for the gradient passes
+            float* dst = p.ckpt + ((size_t)seq * nch + c0 / p.chunk) * 2 * (size_t)dv * dk;
+            for (int x = tid; x < nr * dk; x += kThreads) {
+                const int i = x / dk, j = x % dk;
+                dst[(size_t)(r0 + i) * dk + j] = W[x];
+                dst[(size_t)dv * dk + (size_t)(r0 + i) * dk + j] = S[x];
+            }
+        }
         if (snap) {
             for (int x = tid; x < kRows * dk; x += kThreads) Wc[x] = W[x];
             __syncthreads();
@@ -198,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) linear_simt_kernel(LinearArgs p) {
             __syncthreads();
             for (int x = tid; x < n * kRows; x += kThreads) {
                 const int t = x / kRows, i = x % kRows;
-                if (i < nr) store_out(z, (tok0 + t) * dv + r0 + i, zs[t * (kRows + 1) + i]);
+                if (i < nr && z) store_out(z, (tok0 + t) * dv + r0 + i, zs[t * (kRows + 1) + i]);
             }
             // block-end state
             const float bn = beta[n - 1], cn = cc[n - 1], Pn = P[n - 1];
@@ -219,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) linear_simt_kernel(LinearArgs p) {
         }
     }
     const size_t dst = (size_t)seq * dv * dk;
-    for (int x = tid; x < nr * dk; x += kThreads) {
+    for (int x = tid; x < nr * dk && p.W_out; x += kThreads) {
         const int i = x / dk, j = x % dk;
         p.W_out[dst + (size_t)(r0 + i) * dk + j] = W[x];
         if (p.S_out) p.S_out[dst + (size_t)(r0 + i) * dk + j] = S[x];

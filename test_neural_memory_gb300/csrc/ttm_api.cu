@@ -287,6 +287,93 @@ int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int
                            W, nullptr, Wc, z, stream);
 }
 
+size_t ttm_titans_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                                     int w0_shared_over_batch) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1 || (dtype != TTM_F32 && dtype != TTM_BF16) ||
+        !dims_ok(dk, dtype) || !dims_ok(dv, dtype))
+        return 0;
+    ttm::BwdArgs a{};
+    a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    a.shared = w0_shared_over_batch ? 1 : 0;
+    if (!ttm::linear_bwd_supported(a)) return 0;
+    return ttm::linear_bwd_workspace_bytes(a);
+}
+
+int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                   const void* k, const void* v, const float* eta, const float* theta,
+                   const float* alpha, const float* W0, const float* S0,
+                   int w0_shared_over_batch, const void* dz, const float* dW, const float* dS,
+                   void* dq, void* dk_, void* dv_, float* deta, float* dtheta, float* dalpha,
+                   float* dW0, float* dS0, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
+    if (!W0 || !dW0) return TTM_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !theta || !dz || !dq || !dk_ || !dv_ || !dtheta))
+        return TTM_ERR_INVALID_ARG;
+    if ((deta && !eta) || (dalpha && !alpha)) return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W0, S0, dz, dW, dS, dq, dk_, dv_,
+                          deta, dtheta, dalpha, dW0, dS0, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+    const int shared = w0_shared_over_batch ? 1 : 0;
+    ttm::BwdArgs a{};
+    a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v; a.eta = eta; a.theta = theta; a.alpha = alpha;
+    a.W0 = W0; a.S0 = S0; a.shared = shared;
+    a.dz = dz; a.dW = dW; a.dS = dS;
+    a.dq = dq; a.dk_ = dk_; a.dv_ = dv_;
+    a.deta = deta; a.dtheta = dtheta; a.dalpha = dalpha; a.dW0 = dW0; a.dS0 = dS0;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    if (!ttm::linear_bwd_supported(a)) return TTM_ERR_UNSUPPORTED;
+    if ((long long)B * H > (1LL << 31) - 1 || (T + chunk - 1) / chunk > 65535)
+        return TTM_ERR_UNSUPPORTED;
+
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * T;
+    const size_t st = (size_t)H * dv * dk * sizeof(float);
+    const size_t nb0 = shared ? 1 : (size_t)B;
+    const Span ins[] = {{q, tok * dk * es}, {k, tok * dk * es}, {v, tok * dv * es},
+                        {eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4},
+                        {W0, nb0 * st}, {S0, nb0 * st}, {dz, tok * dv * es},
+                        {dW, (size_t)B * st}, {dS, (size_t)B * st}};
+    const Span outs[] = {{dq, tok * dk * es}, {dk_, tok * dk * es}, {dv_, tok * dv * es},
+                         {deta, tok * 4}, {dtheta, tok * 4}, {dalpha, tok * 4},
+                         {dW0, nb0 * st}, {dS0, nb0 * st}};
+    const size_t need = ttm::linear_bwd_workspace_bytes(a);
+    if (T > 0 && (!workspace || workspace_bytes < need)) return TTM_ERR_INVALID_ARG;
+    const Span swk{workspace, T > 0 ? workspace_bytes : 0};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const Span& in : ins)
+            if (overlap(outs[i], in)) return TTM_ERR_INVALID_ARG;
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (overlap(outs[i], outs[j])) return TTM_ERR_INVALID_ARG;
+        if (overlap(outs[i], swk)) return TTM_ERR_INVALID_ARG;
+    }
+    for (const Span& in : ins)
+        if (overlap(in, swk)) return TTM_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    const cudaError_t e = ttm::linear_bwd_launch(a, s, &launches);
+    if (e != cudaSuccess) return TTM_ERR_CUDA;
+    __atomic_add_fetch(&g_launches, (unsigned long long)launches, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                   const void* k, const void* v, const float* theta, const float* W0,
+                   int w0_shared_over_batch, const void* dz, const float* dW, void* dq,
+                   void* dk_, void* dv_, float* dtheta, float* dW0, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    return ttm_titans_bwd(B, H, T, dk, dv, chunk, dtype, q, k, v, nullptr, theta, nullptr, W0,
+                          nullptr, w0_shared_over_batch, dz, dW, nullptr, dq, dk_, dv_, nullptr,
+                          dtheta, nullptr, dW0, nullptr, workspace, workspace_bytes, stream);
+}
+
 int ttm_mlp_gelu(const float* x, float* y, float* dy, int n, void* stream) {
     if (n < 0 || (n > 0 && (!x || !y))) return TTM_ERR_INVALID_ARG;
     if (overlap({y, (size_t)n * 4}, {x, (size_t)n * 4}) && y != x) return TTM_ERR_INVALID_ARG;

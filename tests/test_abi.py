@@ -148,3 +148,45 @@ def test_step_rejects_malformed(L):
 @host_only
 def test_step_valid_call_without_gpu_reports_cuda_error(L):
     assert step_call(L, eta=P(7), S=P(8), alpha=P(9)) == CUDA
+
+
+def bwd_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=4, dt=1, q=P(0), k=P(1), v=P(2), eta=None,
+             theta=P(3), alpha=None, W0=P(4), S0=None, shared=0, dz=P(5), dW=None, dS=None,
+             dq=P(10), dk_=P(11), dv_=P(12), deta=None, dtheta=P(13), dalpha=None, dW0=P(14),
+             dS0=None, ws=P(20), wsb=1 << 30):
+    return L.ttm_titans_bwd(B, H, T, dk, dv, chunk, dt, q, k, v, eta, theta, alpha, W0, S0,
+                            shared, dz, dW, dS, dq, dk_, dv_, deta, dtheta, dalpha, dW0, dS0, ws,
+                            wsb, None)
+
+
+@host_only
+def test_bwd_rejects_malformed(L):
+    assert bwd_call(L, chunk=0) == INVALID
+    assert bwd_call(L, dz=None) == INVALID
+    assert bwd_call(L, dtheta=None) == INVALID
+    assert bwd_call(L, deta=P(15)) == INVALID                   # no eta, no deta
+    assert bwd_call(L, dalpha=P(15)) == INVALID
+    assert bwd_call(L, dq=P(0)) == INVALID                      # output overlaps an input
+    assert bwd_call(L, dk_=P(10)) == INVALID                    # outputs overlap each other
+    assert bwd_call(L, dW0=P(20)) == INVALID                    # output inside the workspace
+    assert bwd_call(L, q=P(0, 8)) == INVALID                    # misaligned
+    assert bwd_call(L, wsb=1024) == INVALID                     # workspace too small
+    assert bwd_call(L, ws=None, wsb=0) == INVALID
+    assert bwd_call(L, chunk=128) == UNSUPPORTED                # chunk above 64
+    assert bwd_call(L, dk=256) == UNSUPPORTED                   # key wider than 128
+    assert L.ttm_titans_bwd_workspace_size(1, 1, 8, 64, 64, 128, 1, 0) == 0
+
+
+@host_only
+def test_bwd_workspace_size(L):
+    # state and adjoint per chunk boundary (4 x dv x dk fp32) plus a record of
+    # bc^2 + 4 bc + 1 floats rounded up to 4; shared W0 adds per-sequence partials
+    per_chunk = 4 * 64 * 64 * 4 + ((64 * 64 + 4 * 64 + 1 + 3) // 4 * 4) * 4
+    assert L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 0) == 2 * 3 * 3 * per_chunk
+    assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 1) ==
+            2 * 3 * 3 * per_chunk + 2 * 3 * 2 * 64 * 64 * 4)
+
+
+@host_only
+def test_bwd_valid_call_without_gpu_reports_cuda_error(L):
+    assert bwd_call(L) == CUDA

@@ -124,3 +124,14 @@ def generate_custom(kind="titans", B=1, H=2, T=100, d=64, chunk=16, dtype="f32",
     w = Workload(0, "custom", kind, B, H, T, d, chunk, dtype, theta, eta, alpha, w0, w0_shared,
                  hidden)
     return w, generate(w, seed=seed)
+
+
+def generate_adjoints(B, H, T, dk, dv, dtype="f32", seed=0, with_S=True) -> dict:
+    """Seeded adjoints of a scan's outputs for gradient checks: dz ~ N(0, 1) in
+    the workload dtype ([B,H,T,dv]), dW and dS ~ N(0, 1) fp32 ([B,H,dv,dk]; dS
+    None unless with_S).  Drawn in that order from a CPU generator."""
+    g = torch.Generator().manual_seed(seed)
+    dz = torch.randn((B, H, T, dv), generator=g).to(_torch_dtype(dtype))
+    dW = torch.randn((B, H, dv, dk), generator=g)
+    dS = torch.randn((B, H, dv, dk), generator=g) if with_S else None
+    return dict(dz=dz, dW=dW, dS=dS)
