@@ -268,6 +268,168 @@ def oracle_decode_sample(B, H, d, chunk, seconds) -> dict:
 
 
 # ----------------------------------------------------------------------------
+# gradient of the scan (--mode bwd): one ttm_titans_bwd call per step
+# ----------------------------------------------------------------------------
+
+def fp32_alu_peak_tflops(sm_mhz: float) -> float:
+    """Dense fp32 FMA rate of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 FLOP
+    per FMA x the SM clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def bwd_algorithmic(w: wl.Workload) -> dict:
+    """FLOPs and bytes of one gradient call, per token-head: the forward scan
+    that rebuilds the chunk-start states (10 d^2 + 4 b d) plus the chunk-form
+    backward products evaluated once (22 d^2 + 8 b d: the errors, the end-state
+    adjoints applied to the keys, the state-adjoint update, W^T dz, S^T dz and
+    the three key-gradient products, each 2 d^2; the masked b x b score and
+    error products, 8 b d).  Bytes: q, k, v, dz read and dq, dk, dv written in
+    the input dtype, three gates read and their gradients written."""
+    es = 2 if w.dtype == "bf16" else 4
+    d, b = w.d, w.chunk
+    flop_tok = 32 * d * d + 12 * b * d
+    byte_tok = 7 * d * es + 2 * 12
+    return {"flops": w.tokens * flop_tok, "bytes": w.tokens * byte_tok,
+            "flop_per_token": flop_tok, "bytes_per_token": byte_tok}
+
+
+def run_bwd(args, rank, world, dev):
+    import test_neural_memory_gb300 as ttm
+
+    w = workload_of(args)
+    if w.kind == "mlp":
+        raise SystemExit("--mode bwd covers the linear / Titans memory")
+    inp = wl.generate(w)
+    adj = wl.generate_adjoints(w.B, w.H, w.T, w.d, w.d, dtype=w.dtype, seed=4321,
+                               with_S=w.kind == "titans")
+    stream = torch.cuda.current_stream(dev)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    a = {k: (None if v is None else v.to(dev)) for k, v in adj.items()}
+    ws_bytes = ttm.lib().ttm_titans_bwd_workspace_size(w.B, w.H, w.T, w.d, w.d, w.chunk,
+                                                       1 if w.dtype == "bf16" else 0,
+                                                       int(w.w0_shared))
+    ws = torch.empty(int(ws_bytes), dtype=torch.uint8, device=dev)
+    out = ttm.titans_bwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], w.chunk, a["dz"],
+                         eta=d["eta"], alpha=d["alpha"], dW=a["dW"], dS=a["dS"],
+                         w0_shared=w.w0_shared, workspace=ws, stream=stream)
+
+    def step(dd=d, aa=a, oo=out):
+        ttm.titans_bwd(dd["q"], dd["k"], dd["v"], dd["theta"], dd["W0"], w.chunk, aa["dz"],
+                       eta=dd["eta"], alpha=dd["alpha"], dW=aa["dW"], dS=aa["dS"],
+                       w0_shared=w.w0_shared, workspace=ws, out=oo, stream=stream)
+
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ttm.launch_count()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ttm.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
+    status = ttm.device_status()
+    if status != ttm.OK:
+        raise RuntimeError(f"device status {ttm.status_str(status)}")
+
+    # end to end: inputs and adjoints host -> device, every gradient back
+    host_in = {k: v.pin_memory() for k, v in {**inp, **adj}.items() if v is not None}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for k, v in out.items() if v is not None}
+    din = {k: dev_in.get(k) for k in inp}
+    ain = {k: dev_in.get(k) for k in adj}
+    out2 = {k: (None if v is None else torch.empty_like(v)) for k, v in out.items()}
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        step(din, ain, out2)
+        for k, v in host_out.items():
+            v.copy_(out2[k], non_blocking=True)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.e2e_steps
+        e2e = {"value": w.tokens * world / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in host_out.values()),
+               "steps": args.e2e_steps, "ms_per_step": ems}
+
+    alg = bwd_algorithmic(w)
+    mhz = clocks.get("sm_mhz") or 2070.0
+    peak = fp32_alu_peak_tflops(mhz)
+    achieved = alg["flops"] / (ms / 1e3) / 1e12
+    line = {
+        "metric": "gradient tokens/s (ttm_titans_bwd: dq, dk, dv, gates, W0) on 1 GB300",
+        "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name + " (gradient)", "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                   "chunk": w.chunk, "kind": w.kind,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (no flush needed)", "kernel": "linear_bwd",
+                   "workspace_bytes": int(ws_bytes)},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"derived: 152 SMs x 128 fp32 lanes x 2 x {mhz:.0f} MHz",
+                     "kernel": "linear_bwd (all passes)", "algorithmic_flops": alg["flops"],
+                     "algorithmic_bytes": alg["bytes"], "traffic": None},
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_bwd_sample(w, inp, adj, args.cpu_seconds)
+    return line
+
+
+def oracle_bwd_sample(w, inp, adj, seconds) -> dict:
+    """The float64 oracle's gradient on every (b, h) but only the first T_s tokens."""
+    import oracle
+    f = lambda t, T_s: None if t is None else t[:, :, :T_s].double().numpy()
+    T_s = min(w.T, 2 * w.chunk)
+    t0 = time.perf_counter()
+    while True:
+        r = oracle.linear_primal_bwd(f(inp["q"], T_s), f(inp["k"], T_s), f(inp["v"], T_s),
+                                     f(inp["theta"], T_s), inp["W0"].double().numpy(), w.chunk,
+                                     f(adj["dz"], T_s), eta=f(inp["eta"], T_s),
+                                     alpha=f(inp["alpha"], T_s),
+                                     dW=None if adj["dW"] is None else adj["dW"].double().numpy(),
+                                     dS=None if adj["dS"] is None else adj["dS"].double().numpy(),
+                                     shared_over_batch=w.w0_shared)
+        dt = time.perf_counter() - t0
+        if dt > seconds / 4 or T_s >= w.T:
+            break
+        T_s = min(w.T, T_s * 2)
+        t0 = time.perf_counter()
+    tokens = w.B * w.H * T_s
+    return {"value": tokens / dt, "unit": UNIT, "cores": int(r["threads"]), "kind": "oracle",
+            "seconds": dt, "sample": f"all {w.B * w.H} (b,h) sequences, first {T_s} of {w.T} "
+                                     f"tokens each, float64 reverse mode, {r['threads']} threads"}
+
+
+# ----------------------------------------------------------------------------
 # clocks sampled while the GPU is under load
 # ----------------------------------------------------------------------------
 
@@ -579,8 +741,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["scan", "decode"], default="scan",
-                    help="decode: time the streaming decode step instead of the scan")
+    ap.add_argument("--mode", choices=["scan", "decode", "bwd"], default="scan",
+                    help="decode: the streaming decode step; bwd: the scan's gradient")
     ap.add_argument("--decode-tokens", type=int, default=1, help="tokens per decode call")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -603,7 +765,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     import test_neural_memory_gb300 as ttm
     ttm.build()
-    line = run_decode(args, rank, world, dev) if args.mode == "decode" else run_ours(args, rank, world, dev)
+    runner = {"scan": run_ours, "decode": run_decode, "bwd": run_bwd}[args.mode]
+    line = runner(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

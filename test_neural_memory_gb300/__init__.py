@@ -215,22 +215,29 @@ def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, 
 
 def titans_bwd(q, k, v, theta, W0, chunk, dz, *, eta=None, alpha=None, S0=None, dW=None,
                dS=None, w0_shared=False, want_gates=True, want_dS0=True, workspace=None,
-               stream=None):
+               out=None, stream=None):
     """Gradient of the Titans (or, with eta = alpha = None, TTT-Linear) scan for the
     adjoints dz ([B,H,T,dv], dtype of v), dW / dS ([B,H,dv,dk] fp32 or None).
     Returns a dict with dq, dk, dv (dtype of q), dtheta, deta, dalpha ([B,H,T] fp32;
     deta / dalpha None when the gate is None or want_gates is False), dW0, dS0 (shaped
-    like W0; dS0 None when want_dS0 is False)."""
+    like W0; dS0 None when want_dS0 is False).  `out` may hold preallocated tensors for
+    any of these keys."""
     import torch
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
     f32 = lambda shape: torch.empty(shape, dtype=torch.float32, device=dev)
-    g = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-             dtheta=f32((B, H, T)),
-             deta=f32((B, H, T)) if (eta is not None and want_gates) else None,
-             dalpha=f32((B, H, T)) if (alpha is not None and want_gates) else None,
-             dW0=f32(tuple(W0.shape)), dS0=f32(tuple(W0.shape)) if want_dS0 else None)
+    out = out or {}
+    pick = lambda key, make: out[key] if out.get(key) is not None else make()
+    has_eta, has_alpha = eta is not None and want_gates, alpha is not None and want_gates
+    g = dict(dq=pick("dq", lambda: torch.empty_like(q)),
+             dk=pick("dk", lambda: torch.empty_like(k)),
+             dv=pick("dv", lambda: torch.empty_like(v)),
+             dtheta=pick("dtheta", lambda: f32((B, H, T))),
+             deta=pick("deta", lambda: f32((B, H, T))) if has_eta else None,
+             dalpha=pick("dalpha", lambda: f32((B, H, T))) if has_alpha else None,
+             dW0=pick("dW0", lambda: f32(tuple(W0.shape))),
+             dS0=pick("dS0", lambda: f32(tuple(W0.shape))) if want_dS0 else None)
     if workspace is None:
         n = int(lib().ttm_titans_bwd_workspace_size(B, H, T, dk, dv, int(chunk), _dtype_code(q),
                                                     int(bool(w0_shared))))

@@ -21,9 +21,9 @@ struct LinearArgs {
     void* workspace;                    // caller-provided device scratch (may be NULL)
     size_t workspace_bytes;
     int* status;                        // device status word (bounded waits)
-    // CUDA-core kernel only: when set, the state at every chunk start is
-    // written to ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be
-    // NULL.  The gradient passes read these checkpoints.
+    // When set, the state at every chunk start is written to
+    // ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be NULL.  The
+    // gradient passes read these checkpoints.
     float* ckpt;
 };
 
@@ -70,6 +70,8 @@ struct BwdArgs {
     float *dW0, *dS0;
     void* workspace;
     size_t workspace_bytes;
+    int fwd_tc;     // 1: the tensor-core scan writes the checkpoints (bf16, d 64 / 128, chunk 64)
+    int* status;    // device status word of the tensor-core scan's bounded waits
 };
 
 // fp32 CUDA-core kernels (scan_simt.cu).  The *_supported functions decide

@@ -63,7 +63,7 @@ constexpr int kR3 = 16;       // rows per tile in the local pass
 struct BwdLayout {
     int nch, bc;
     size_t sd, rec_f;
-    size_t ckpt, adj, rec, part, total;
+    size_t ckpt, adj, rec, part, tcws, total;
 };
 
 BwdLayout bwd_layout(const BwdArgs& a) {
@@ -77,7 +77,15 @@ BwdLayout bwd_layout(const BwdArgs& a) {
     L.adj = L.ckpt + nseq * L.nch * 2 * L.sd;
     L.rec = L.adj + nseq * L.nch * 2 * L.sd;
     L.part = L.rec + nseq * L.nch * L.rec_f;
-    L.total = L.part + (a.shared ? nseq * 2 * L.sd : 0);
+    L.tcws = L.part + (a.shared ? nseq * 2 * L.sd : 0);
+    L.total = L.tcws;
+    if (a.fwd_tc) {   // the tensor-core scan's own coefficient records
+        LinearArgs f{};
+        f.B = a.B; f.H = a.H; f.T = a.T; f.dk = a.dk; f.dv = a.dv; f.chunk = a.chunk;
+        f.bf16 = a.bf16;
+        L.tcws = (L.tcws + 3) / 4 * 4;   // 16-byte aligned
+        L.total = L.tcws + (linear_tc_workspace_bytes(f) + 3) / 4;
+    }
     return L;
 }
 
@@ -639,9 +647,18 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
     f.eta = a.eta; f.theta = a.theta; f.alpha = a.alpha;
     f.W0 = a.W0; f.S0 = a.S0; f.shared = a.shared;
     f.ckpt = ws + L.ckpt;
-    cudaError_t e = linear_simt_launch(f, s);
+    cudaError_t e;
+    if (a.fwd_tc) {
+        f.workspace = ws + L.tcws;
+        f.workspace_bytes = linear_tc_workspace_bytes(f);
+        f.status = a.status;
+        e = linear_tc_launch(f, s);
+        *launches += 2;   // coefficient pre-pass and scan
+    } else {
+        e = linear_simt_launch(f, s);
+        ++*launches;
+    }
     if (e != cudaSuccess) return e;
-    ++*launches;
 
     const int nseq = a.B * a.H;
     const size_t sm0 = records_smem_floats(L.bc, a.dk) * sizeof(float);

@@ -446,6 +446,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         ok = issue_state(0, ok);
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1, st = c % kNS;
+            if (a.ckpt && own && ok) {
+                // the state at this chunk's start, for the gradient passes
+                float* ck = a.ckpt + ((size_t)seq * nch + c) * 2 * (size_t)D * D +
+                            (size_t)r0 * D + j;
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    ck[(size_t)i * D] = w[i];
+                    ck[(size_t)D * D + (size_t)i * D] = s[i];
+                }
+            }
             if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
             if (ok) ok = wait_all(B, &B->mma2_done[b], (c >> 1) & 1, status);
             if (ok) {
@@ -480,7 +490,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             named_bar_sync(1, 128);
             if (c + 1 < nch) ok = issue_state(c + 1, ok);
         }
-        if (own && ok) {
+        if (own && ok && a.W_out) {
             const size_t dst = (size_t)seq * D * D;
 #pragma unroll
             for (int i = 0; i < kRows; ++i) {
@@ -510,7 +520,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 tc_fence_before();
                 mbar_arrive(&B->acc1_free[b]);
                 mbar_arrive(&B->acc3_free[b]);
-                if (t < n) {
+                if (t < n && a.z) {
                     float zz[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) zz[i] = bt * qw[i] + ct * qs[i] - 2.f * ae[i];

@@ -73,6 +73,15 @@ int select_mlp(const ttm::MlpArgs& a) {
     return simt_ok ? TTM_KID_MLP_SIMT : TTM_KID_NONE;
 }
 
+// The gradient's checkpoint pass runs the forward scan the policy would pick
+// for the same shape (the tensor-core scan when it applies).
+int bwd_forward_tc(const ttm::BwdArgs& b) {
+    ttm::LinearArgs f{};
+    f.B = b.B; f.H = b.H; f.T = b.T; f.dk = b.dk; f.dv = b.dv; f.chunk = b.chunk;
+    f.bf16 = b.bf16;
+    return select_linear(f) == TTM_KID_LINEAR_TC ? 1 : 0;
+}
+
 int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
                   const void* k, const void* v, const float* eta, const float* theta,
                   const float* alpha, const float* W0, const float* S0, int shared, void* z,
@@ -296,6 +305,7 @@ size_t ttm_titans_bwd_workspace_size(int B, int H, int T, int dk, int dv, int ch
     a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
     a.bf16 = dtype == TTM_BF16;
     a.shared = w0_shared_over_batch ? 1 : 0;
+    a.fwd_tc = bwd_forward_tc(a);
     if (!ttm::linear_bwd_supported(a)) return 0;
     return ttm::linear_bwd_workspace_bytes(a);
 }
@@ -328,6 +338,7 @@ int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     a.dq = dq; a.dk_ = dk_; a.dv_ = dv_;
     a.deta = deta; a.dtheta = dtheta; a.dalpha = dalpha; a.dW0 = dW0; a.dS0 = dS0;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.fwd_tc = bwd_forward_tc(a);
     if (!ttm::linear_bwd_supported(a)) return TTM_ERR_UNSUPPORTED;
     if ((long long)B * H > (1LL << 31) - 1 || (T + chunk - 1) / chunk > 65535)
         return TTM_ERR_UNSUPPORTED;
@@ -356,6 +367,8 @@ int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     for (const Span& in : ins)
         if (overlap(in, swk)) return TTM_ERR_INVALID_ARG;
 
+    a.status = status_ptr();
+    if (!a.status) return TTM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     const cudaError_t e = ttm::linear_bwd_launch(a, s, &launches);

@@ -182,9 +182,16 @@ def test_bwd_workspace_size(L):
     # state and adjoint per chunk boundary (4 x dv x dk fp32) plus a record of
     # bc^2 + 4 bc + 1 floats rounded up to 4; shared W0 adds per-sequence partials
     per_chunk = 4 * 64 * 64 * 4 + ((64 * 64 + 4 * 64 + 1 + 3) // 4 * 4) * 4
-    assert L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 0) == 2 * 3 * 3 * per_chunk
-    assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 1) ==
-            2 * 3 * 3 * per_chunk + 2 * 3 * 2 * 64 * 64 * 4)
+    with ttm.kernel_policy("simt"):
+        assert L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 0) == 2 * 3 * 3 * per_chunk
+        assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 1) ==
+                2 * 3 * 3 * per_chunk + 2 * 3 * 2 * 64 * 64 * 4)
+    # where the tensor-core scan writes the checkpoints, its 17424-byte records come on top
+    with ttm.kernel_policy("auto"):
+        assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 1, 0) ==
+                2 * 3 * 3 * per_chunk + 2 * 3 * 3 * 17424)
+        assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 0, 0) ==
+                2 * 3 * 3 * per_chunk)                         # fp32: CUDA-core forward
 
 
 @host_only

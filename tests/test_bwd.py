@@ -146,3 +146,14 @@ def test_narrow_key_long_chunk():
     # dk = 16 < chunk = 64: the gate-gradient tables outgrow the q / k buffers
     g, r, names = run_bwd("titans", "bf16", B=1, Hh=2, T=100, d=16, chunk=64, seed=9)
     check(g, r, names, H.TOL["bf16"])
+
+
+@pytest.mark.parametrize("policy", ["auto", "simt"])
+def test_bf16_d128_both_checkpoint_scans(policy):
+    # bf16, d = 128, chunk 64: the tensor-core scan writes the chunk-start
+    # states under the automatic policy, the CUDA-core scan under "simt"
+    import test_neural_memory_gb300 as ttm
+    with ttm.kernel_policy(policy):
+        g, r, names = run_bwd("titans", "bf16", B=1, Hh=2, T=200, d=128, chunk=64, seed=10,
+                              S0=True)
+    check(g, r, names, H.TOL["bf16"])
