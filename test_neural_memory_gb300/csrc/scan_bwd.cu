@@ -56,6 +56,7 @@ constexpr int kMaxBC = 64;    // largest chunk
 constexpr int kMaxDK = 128;   // widest key
 constexpr int kR2 = 8;        // rows of the adjoint per chain CTA
 constexpr int kR3 = 16;       // rows per tile in the local pass
+constexpr int kBT3 = 512;     // threads per local-pass CTA
 
 // Workspace carve-up (floats).  ckpt and adj hold [seq][chunk][W | S][dv][dk];
 // rec holds per (seq, chunk): A [bc][bc], beta [bc], cc [bc], clast [bc],
@@ -150,15 +151,82 @@ __global__ void __launch_bounds__(kBT) bwd_records_kernel(const BwdArgs a, const
 // chain: the adjoint of the state at every chunk end, chunks in reverse
 // ------------------------------------------------------------------------
 
+constexpr int kBT2 = 512;     // threads per chain CTA (two per SM: every CTA of a call resident)
+
+// 16-byte pieces of q (and of k) per thread and chunk, at most
 template <typename Tin>
-__global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const BwdLayout L,
-                                                        float* ws) {
+constexpr int pieces_per_thread() {
+    return (kMaxBC * kMaxDK / (16 / (int)sizeof(Tin)) + kBT2 - 1) / kBT2;
+}
+
+// A chunk's inputs to the chain, held in registers while the previous chunk
+// computes: q and k rows as 16-byte pieces, the record's A table and vectors,
+// and the slice's dz.
+template <typename Tin>
+struct ChainPrefetch {
+    static constexpr int kPre = pieces_per_thread<Tin>();
+    uint4 q[kPre], k[kPre];
+    float4 A[2];
+    float vec, dz;
+};
+
+template <typename Tin>
+__device__ __forceinline__ void chain_fetch(ChainPrefetch<Tin>& f, const BwdArgs& a,
+                                            const BwdLayout& L, const float* ws, int seq, int c,
+                                            int r0, int nr) {
+    const int tid = threadIdx.x, dk = a.dk, bc = L.bc;
+    const int t0 = c * bc, n = min(bc, a.T - t0);
+    const size_t tok0 = (size_t)seq * a.T + t0;
+    constexpr int per = 16 / sizeof(Tin);                  // elements per piece
+    const int nvec = n * dk / per;
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.q) + tok0 * dk);
+    const uint4* k = reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.k) + tok0 * dk);
+#pragma unroll
+    for (int u = 0; u < ChainPrefetch<Tin>::kPre; ++u) {
+        const int v = tid + u * kBT2;
+        f.q[u] = v < nvec ? __ldg(q + v) : make_uint4(0, 0, 0, 0);
+        f.k[u] = v < nvec ? __ldg(k + v) : make_uint4(0, 0, 0, 0);
+    }
+    const float* rec = ws + L.rec + ((size_t)seq * L.nch + c) * L.rec_f;
+    const float4* rec4 = reinterpret_cast<const float4*>(rec);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {   // the record's A table: bc^2 floats, read as 4-float pieces
+        const int v = tid + u * kBT2;
+        f.A[u] = v < (bc * bc + 3) / 4 ? __ldg(rec4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    f.vec = tid < 4 * bc + 1 ? __ldg(rec + (size_t)bc * bc + tid) : 0.f;
+    const int s = tid / kR2, i = tid % kR2;
+    f.dz = (s < n && i < nr) ? load_in(static_cast<const Tin*>(a.dz), (tok0 + s) * a.dv + r0 + i)
+                             : 0.f;
+}
+
+__device__ __forceinline__ void unpack_piece(const uint4& p, float* dst, const float*) {
+    const float4 x = *reinterpret_cast<const float4*>(&p);
+    dst[0] = x.x; dst[1] = x.y; dst[2] = x.z; dst[3] = x.w;
+}
+__device__ __forceinline__ void unpack_piece(const uint4& p, float* dst, const __nv_bfloat16*) {
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        dst[2 * e] = __uint_as_float(w[e] << 16);
+        dst[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+    }
+}
+
+// ------------------------------------------------------------------------
+// chain: the adjoint of the state at every chunk end, chunks in reverse
+// ------------------------------------------------------------------------
+
+template <typename Tin>
+__global__ void __launch_bounds__(kBT2, 2) bwd_chain_kernel(const BwdArgs a, const BwdLayout L,
+                                                         float* ws) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x;
     const int seq = blockIdx.x;
     const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = dk + 1;
     const int r0 = blockIdx.y * kR2, nr = min(kR2, dv - r0);
     constexpr int ldr = kR2 + 1;
+    constexpr int per = 16 / sizeof(Tin);
     float* Qs = sm;                    // [bc][ldk]
     float* Ks = Qs + bc * ldk;         // [bc][ldk]
     float* A = Ks + bc * ldk;          // [bc][bc + 1]
@@ -169,47 +237,58 @@ __global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const B
     float* dW = de + bc * ldr;         // [kR2][ldk] running adjoint of W
     float* dS = dW + kR2 * ldk;        // [kR2][ldk] running adjoint of S
     float* vec = dS + kR2 * ldk;       // beta, cc, clast, pm [bc] each, P_n
-    const Tin* q = static_cast<const Tin*>(a.q);
-    const Tin* k = static_cast<const Tin*>(a.k);
-    const Tin* dz = static_cast<const Tin*>(a.dz);
 
     const size_t sd = L.sd;
-    for (int x = tid; x < kR2 * dk; x += kBT) {
+    for (int x = tid; x < kR2 * dk; x += kBT2) {
         const int i = x / dk, j = x % dk;
         const size_t g = (size_t)seq * sd + (size_t)(r0 + i) * dk + j;
         dW[i * ldk + j] = (i < nr && a.dW) ? a.dW[g] : 0.f;
         dS[i * ldk + j] = (i < nr && a.dS) ? a.dS[g] : 0.f;
     }
+    ChainPrefetch<Tin> f;
+    chain_fetch<Tin>(f, a, L, ws, seq, L.nch - 1, r0, nr);
     for (int c = L.nch - 1; c >= 0; --c) {
         const int t0 = c * bc, n = min(bc, a.T - t0);
-        const size_t tok0 = (size_t)seq * a.T + t0;
-        const float* rec = ws + L.rec + ((size_t)seq * L.nch + c) * L.rec_f;
         __syncthreads();   // the previous chunk is done with every buffer
+        {   // this chunk's inputs from the prefetch registers into shared memory
+            const int nvec = bc * dk / per;
+#pragma unroll
+            for (int u = 0; u < ChainPrefetch<Tin>::kPre; ++u) {
+                const int v = tid + u * kBT2;
+                if (v < nvec) {
+                    const int e0 = v * per, srow = e0 / dk, j = e0 % dk;
+                    unpack_piece(f.q[u], Qs + srow * ldk + j, static_cast<const Tin*>(nullptr));
+                    unpack_piece(f.k[u], Ks + srow * ldk + j, static_cast<const Tin*>(nullptr));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int v = tid + u * kBT2;
+                const float x4[4] = {f.A[u].x, f.A[u].y, f.A[u].z, f.A[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = 4 * v + e;   // element t * bc + s of the table
+                    if (idx < bc * bc) A[(idx / bc) * (bc + 1) + idx % bc] = x4[e];
+                }
+            }
+            if (tid < 4 * bc + 1) vec[tid] = f.vec;
+            if (tid < bc * kR2) dZ[(tid / kR2) * ldr + tid % kR2] = f.dz;
+        }
         // this chunk's end adjoint, for the local pass
         float* adj = ws + L.adj + ((size_t)seq * L.nch + c) * 2 * sd;
-        for (int x = tid; x < nr * dk; x += kBT) {
+        for (int x = tid; x < nr * dk; x += kBT2) {
             const int i = x / dk, j = x % dk;
             adj[(size_t)(r0 + i) * dk + j] = dW[i * ldk + j];
             adj[sd + (size_t)(r0 + i) * dk + j] = dS[i * ldk + j];
         }
-        for (int x = tid; x < bc * dk; x += kBT) {
-            const int s = x / dk, j = x % dk;
-            Qs[s * ldk + j] = s < n ? load_in(q, (tok0 + s) * dk + j) : 0.f;
-            Ks[s * ldk + j] = s < n ? load_in(k, (tok0 + s) * dk + j) : 0.f;
-        }
-        for (int x = tid; x < bc * bc; x += kBT) A[(x / bc) * (bc + 1) + x % bc] = rec[x];
-        for (int x = tid; x < 4 * bc + 1; x += kBT) vec[x] = rec[(size_t)bc * bc + x];
-        for (int x = tid; x < bc * kR2; x += kBT) {
-            const int s = x / kR2, i = x % kR2;
-            dZ[s * ldr + i] = (s < n && i < nr) ? load_in(dz, (tok0 + s) * dv + r0 + i) : 0.f;
-        }
         __syncthreads();
+        if (c > 0) chain_fetch<Tin>(f, a, L, ws, seq, c - 1, r0, nr);   // overlaps the compute
         const float* beta = vec;
         const float* cc = vec + bc;
         const float* clast = vec + 2 * bc;
         const float* pm = vec + 3 * bc;
         const float Pn = vec[4 * bc];
-        for (int x = tid; x < bc * kR2; x += kBT) {
+        for (int x = tid; x < bc * kR2; x += kBT2) {
             const int s = x / kR2, i = x % kR2;
             float uw = 0.f, us = 0.f;
             for (int j = 0; j < dk; ++j) {
@@ -221,7 +300,7 @@ __global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const B
             dSK[s * ldr + i] = us;
         }
         __syncthreads();
-        for (int x = tid; x < bc * kR2; x += kBT) {
+        for (int x = tid; x < bc * kR2; x += kBT2) {
             const int s = x / kR2, i = x % kR2;
             float acc = 0.f;
             for (int t = s; t < n; ++t) acc += A[t * (bc + 1) + s] * dZ[t * ldr + i];
@@ -231,7 +310,7 @@ __global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const B
         }
         __syncthreads();
         const float bn = beta[n - 1], cn = cc[n - 1];
-        for (int x = tid; x < kR2 * dk; x += kBT) {
+        for (int x = tid; x < kR2 * dk; x += kBT2) {
             const int i = x / dk, j = x % dk;
             float gw = 0.f, gs = 0.f;
             for (int t = 0; t < n; ++t) {
@@ -239,9 +318,9 @@ __global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const B
                 gw += beta[t] * zq + de[t * ldr + i] * Ks[t * ldk + j];
                 gs += cc[t] * zq;
             }
-            const float w = dW[i * ldk + j], s = dS[i * ldk + j];
+            const float w = dW[i * ldk + j], sv = dS[i * ldk + j];
             dW[i * ldk + j] = bn * w + gw;
-            dS[i * ldk + j] = cn * w + Pn * s + gs;
+            dS[i * ldk + j] = cn * w + Pn * sv + gs;
         }
     }
     __syncthreads();
@@ -259,7 +338,7 @@ __global__ void __launch_bounds__(kBT) bwd_chain_kernel(const BwdArgs a, const B
         oS = a.dS0;
         base = (size_t)seq * sd;
     }
-    for (int x = tid; x < nr * dk; x += kBT) {
+    for (int x = tid; x < nr * dk; x += kBT2) {
         const int i = x / dk, j = x % dk;
         const size_t g = base + (size_t)(r0 + i) * dk + j;
         oW[g] = dW[i * ldk + j];
@@ -318,11 +397,11 @@ size_t local_smem_floats(int bc, int dk) {
            14 * (size_t)bc + 4;
 }
 
-// A thread owns rows t = 4 tg + a (a < 4) and columns j = jg + 16 bb (bb < 8)
-// of dq / dk (tg = tid / 16, jg = tid % 16), and the 4 x 4 block of
-// DE[t][s] = dz_t . e_s with s = jg + 16 bb (bb < 4).
+// A thread owns rows t = 4 tg + a (a < 4) and columns j = jg + 32 bb (bb < 4)
+// of dq / dk (tg = tid / 32, jg = tid % 32), and the 4 x 2 block of
+// DE[t][s] = dz_t . e_s with s = jg + 32 bb (bb < 2).
 template <typename Tin>
-__global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, const BwdLayout L,
+__global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, const BwdLayout L,
                                                            const float* ws) {
     extern __shared__ float sm[];
     const int tid = threadIdx.x;
@@ -368,12 +447,12 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
     const Tin* v = static_cast<const Tin*>(a.v);
     const Tin* dz = static_cast<const Tin*>(a.dz);
 
-    for (int x = tid; x < bc * dk; x += kBT) {
+    for (int x = tid; x < bc * dk; x += kBT3) {
         const int s = x / dk, j = x % dk;
         Qs[s * ldk + j] = s < n ? load_in(q, (tok0 + s) * dk + j) : 0.f;
         Ks[s * ldk + j] = s < n ? load_in(k, (tok0 + s) * dk + j) : 0.f;
     }
-    for (int s = tid; s < bc; s += kBT) {
+    for (int s = tid; s < bc; s += kBT3) {
         th[s] = s < n ? a.theta[tok0 + s] : 0.f;
         et[s] = (s < n && a.eta) ? a.eta[tok0 + s] : 0.f;
         al[s] = (s < n && a.alpha) ? a.alpha[tok0 + s] : 0.f;
@@ -382,7 +461,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
     if (tid < 4) scal[tid] = 0.f;
     __syncthreads();
     block_coefficients(n, bc, th, et, al, beta, P, cc, Cm, ldb, pm);
-    for (int x = tid; x < bc * bc; x += kBT) {
+    for (int x = tid; x < bc * bc; x += kBT3) {
         const int t = x / bc, s = x % bc;
         float acc = 0.f;
         if (s <= t && t < n)
@@ -391,14 +470,14 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         Xm[t * ldb + s] = acc * Cm[t * ldb + s];
     }
 
-    const int tg = tid >> 4, jg = tid & 15;
-    float U[4][8], V[4][8], DK[4][8], DE[4][4];
+    const int tg = tid >> 5, jg = tid & 31;
+    float U[4][4], V[4][4], DK[4][4], DE[4][2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb) U[r][bb] = V[r][bb] = DK[r][bb] = 0.f;
+        for (int bb = 0; bb < 4; ++bb) U[r][bb] = V[r][bb] = DK[r][bb] = 0.f;
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) DE[r][bb] = 0.f;
+        for (int bb = 0; bb < 2; ++bb) DE[r][bb] = 0.f;
     }
 
     const float* ck = ws + L.ckpt + ((size_t)seq * L.nch + c) * 2 * sd;
@@ -406,7 +485,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
     for (int r0 = 0; r0 < dv; r0 += kR3) {
         const int nr = min(kR3, dv - r0);
         __syncthreads();   // the previous tile is consumed (and the tables above are built)
-        for (int x = tid; x < kR3 * dk; x += kBT) {
+        for (int x = tid; x < kR3 * dk; x += kBT3) {
             const int i = x / dk, j = x % dk;
             const size_t g = (size_t)(r0 + i) * dk + j;
             const bool in = i < nr;
@@ -415,7 +494,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
             dWr[i * ldk + j] = in ? ad[g] : 0.f;
             dSr[i * ldk + j] = in ? ad[sd + g] : 0.f;
         }
-        for (int x = tid; x < bc * kR3; x += kBT) {
+        for (int x = tid; x < bc * kR3; x += kBT3) {
             const int s = x / kR3, i = x % kR3;
             dZt[s * ldr + i] = (s < n && i < nr) ? load_in(dz, (tok0 + s) * dv + r0 + i) : 0.f;
         }
@@ -423,8 +502,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         {   // errors at the chunk start and the end adjoints applied to each key
             const int i = tid & 15, sg = tid >> 4;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int s = sg * 4 + r;
+            for (int r = 0; r < 2; ++r) {
+                const int s = sg * 2 + r;
                 if (s >= bc) continue;
                 float e = 0.f, uw = 0.f, us = 0.f;
                 for (int j = 0; j < dk; ++j) {
@@ -446,7 +525,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         }
         {   // <dWe, W>, <dWe, S>, <dSe, S> over the tile
             float p0 = 0.f, p1 = 0.f, p2 = 0.f;
-            for (int x = tid; x < kR3 * dk; x += kBT) {
+            for (int x = tid; x < kR3 * dk; x += kBT3) {
                 const int i = x / dk, j = x % dk;
                 const float w = Wr[i * ldk + j], sv = Sr[i * ldk + j], gw = dWr[i * ldk + j];
                 p0 += gw * w;
@@ -470,8 +549,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
             const int i = tid & 15, sg = tid >> 4;
             const float* clast = Cm + (n - 1) * ldb;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int s = sg * 4 + r;
+            for (int r = 0; r < 2; ++r) {
+                const int s = sg * 2 + r;
                 if (s >= bc) continue;
                 float acc = 0.f;
                 for (int t = s; t < n; ++t) acc += Xm[t * ldb + s] * dZt[t * ldr + i];
@@ -503,8 +582,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
                     ea[r] = t < bc ? Et[t * ldr + i] : 0.f;
                 }
 #pragma unroll
-                for (int bb = 0; bb < 8; ++bb) {
-                    const int j = jg + 16 * bb;
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int j = jg + 32 * bb;
                     if (j >= dk) break;
                     const float w = Wr[i * ldk + j], sv = Sr[i * ldk + j];
                     const float gw = dWr[i * ldk + j], gs = dSr[i * ldk + j];
@@ -516,8 +595,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
                     }
                 }
 #pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    const int s = jg + 16 * bb;
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int s = jg + 32 * bb;
                     if (s >= bc) break;
                     const float es = Et[s * ldr + i];
 #pragma unroll
@@ -532,8 +611,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-            const int t = tg * 4 + r, s = jg + 16 * bb;
+        for (int bb = 0; bb < 2; ++bb) {
+            const int t = tg * 4 + r, s = jg + 32 * bb;
             if (t < bc && s < bc) {
                 const float d = (s <= t && t < n) ? DE[r][bb] : 0.f;
                 const float g = -2.f * QK[t * ldb + s] * d - (t == n - 1 && s < n ? 2.f * dclast[s] : 0.f);
@@ -548,8 +627,8 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         if (t >= n) continue;
         float pb = 0.f, pc = 0.f;
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb) {
-            const int j = jg + 16 * bb;
+        for (int bb = 0; bb < 4; ++bb) {
+            const int j = jg + 32 * bb;
             if (j >= dk) break;
             float sq = 0.f, sk = 0.f;
             for (int s = 0; s <= t; ++s) sq += Xm[t * ldb + s] * Ks[s * ldk + j];
@@ -571,7 +650,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
     float* Wm = Qs;                    // [bc][ldb]  w(s,t) at [t][s]
     float* Mm = Wm + bc * ldb;         // [bc][ldb]  m(s,t) at [t][s]
     const float* dC = QK;
-    for (int s = tid; s < n; s += kBT) {
+    for (int s = tid; s < n; s += kBT3) {
         float m = 1.f, w = 1.f;
         Wm[s * ldb + s] = 1.f;
         Mm[s * ldb + s] = 1.f;
@@ -583,7 +662,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         }
     }
     __syncthreads();
-    for (int s = tid; s < n; s += kBT) {
+    for (int s = tid; s < n; s += kBT3) {
         const float ths = th[s];
         float g = -2.f * dpm[s] * Mm[(n - 1) * ldb + s];   // d pm[s] / d theta_s
         for (int t = s; t < n; ++t) g += dC[t * ldb + s] * Wm[t * ldb + s];
@@ -620,7 +699,7 @@ __global__ void __launch_bounds__(kBT, 1) bwd_local_kernel(const BwdArgs a, cons
         }
     }
     __syncthreads();
-    for (int t = tid; t < n; t += kBT) {
+    for (int t = tid; t < n; t += kBT3) {
         a.dtheta[tok0 + t] = dth[t];
         if (a.deta) a.deta[tok0 + t] = deta[t];
         if (a.dalpha) a.dalpha[tok0 + t] = -dkeep[t];
@@ -672,8 +751,8 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
         return e;
     bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
-    bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT, sm2, s>>>(a, L, ws);
-    bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm3, s>>>(a, L, ws);
+    bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT2, sm2, s>>>(a, L, ws);
+    bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT3, sm3, s>>>(a, L, ws);
     *launches += 3;
     if (a.shared) {
         const size_t n = (size_t)a.H * L.sd;
