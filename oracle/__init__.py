@@ -50,6 +50,8 @@ def _load():
         lib.oracle_linear_primal_bwd.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, d, d, i,
                                                  d, d, d, d, d, d, d, d, d, d, d, i]
         lib.oracle_linear_primal_bwd.restype = i
+        lib.oracle_dgd_primal.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, i, d, d, i]
+        lib.oracle_dgd_primal.restype = i
         lib.oracle_mlp_primal.argtypes = [i, i, i, i, i, i, d, d, d, d, d, d, d, d, d, d, i,
                                           d, d, d, d, d, i]
         lib.oracle_mlp_primal.restype = i
@@ -151,6 +153,27 @@ def linear_primal_bwd(q, k, v, theta, W0, chunk, dz, eta=None, alpha=None, S0=No
         o["dW0"] = o["dW0"].sum(axis=0, keepdims=True)
         o["dS0"] = o["dS0"].sum(axis=0, keepdims=True)
     return Result(**o, threads=used)
+
+
+def dgd_primal(q, k, v, eta, alpha, W0, chunk, shared_over_batch=False, threads=0) -> Result:
+    """DGD memory scan in float64: M_t = M_{t-1}(alpha_t I - eta_t k k^T)
+    - eta_t (Mc k - v) k^T, read z_t = M_t q_t (see ttm_oracle.c).
+    q, k: [B,H,T,dk]; v: [B,H,T,dv]; eta (step), alpha (retention): [B,H,T];
+    W0: [B|1,H,dv,dk].  Returns z, W and the thread count."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    eta = _f64(eta, (B, H, T))
+    alpha = _f64(alpha, (B, H, T))
+    W0 = _f64(W0, (1 if shared_over_batch else B, H, dv, dk))
+    z = np.zeros((B, H, T, dv))
+    W = np.zeros((B, H, dv, dk))
+    used = _load().oracle_dgd_primal(B, H, T, dk, dv, int(chunk), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(eta), _ptr(alpha), _ptr(W0),
+                                     int(bool(shared_over_batch)), _ptr(z), _ptr(W), int(threads))
+    if used < 0:
+        raise ValueError("oracle_dgd_primal rejected its arguments")
+    return Result(z=z, W=W, threads=used)
 
 
 def mlp_primal(q, k, v, theta, W1_0, W2_0, chunk, eta=None, alpha=None, S1_0=None, S2_0=None,

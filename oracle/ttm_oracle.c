@@ -52,6 +52,16 @@
  * dz_t = dL/dz_t, dW_T = dL/dW_T, dS_T = dL/dS_T it returns dL/d of every
  * input: q, k, v, eta, theta, alpha, W0, S0.
  *
+ * The DGD memory (oracle_dgd_primal) is the update of "Nested Learning" §8.1
+ * eq (88) with the matrix memory and the L2 objective of eq (93), taken
+ * chunk-wise as in §8.2 (the gradient at the state left by the previous
+ * chunk):
+ *   M_t = M_{t-1} (alpha_t I - eta_t k_t k_t^T) - eta_t (Mc k_t - v_t) k_t^T
+ * with alpha_t a retention factor (alpha = 1 keeps everything) and eta_t the
+ * step, both as printed (no factor 2 on the gradient, as eq (93) writes it).
+ * The read is z_t = M_t q_t, after the token's write, as for every memory of
+ * this library.
+ *
  * The (b, h) sequences are independent, so they are spread over POSIX
  * threads; each one runs the plain loop below.
  */
@@ -411,11 +421,66 @@ static void lin_bwd_one(const lin_bwd_args* a, int b, int h) {
 }
 
 /* ------------------------------------------------------------------ */
+/* DGD memory                                                         */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int B, H, T, dk, dv, chunk;
+    const double *q, *k, *v, *eta, *alpha, *W0;
+    int shared;
+    double *z, *W_out;
+} dgd_args;
+
+static void dgd_one(const dgd_args* a, int b, int h) {
+    const int T = a->T, dk = a->dk, dv = a->dv;
+    const size_t seq = (size_t)b * a->H + h;
+    const size_t init = (size_t)(a->shared ? 0 : b) * a->H + h;
+    const size_t ns = (size_t)dv * dk;
+    double* M = (double*)malloc(ns * sizeof(double));
+    double* Mc = (double*)malloc(ns * sizeof(double));
+    double* u = (double*)malloc((size_t)dv * sizeof(double));
+    double* e = (double*)malloc((size_t)dv * sizeof(double));
+    memcpy(M, a->W0 + init * ns, ns * sizeof(double));
+    for (int t = 0; t < T; ++t) {
+        const double* kt = a->k + (seq * T + t) * dk;
+        const double* qt = a->q + (seq * T + t) * dk;
+        const double* vt = a->v + (seq * T + t) * dv;
+        const double et = a->eta[seq * T + t];
+        const double al = a->alpha[seq * T + t];
+        if (t % a->chunk == 0) memcpy(Mc, M, ns * sizeof(double));
+        /* u = M_{t-1} k_t (the k k^T term) and e = Mc k_t - v_t (the gradient) */
+        for (int i = 0; i < dv; ++i) {
+            double mu = 0.0, mc = 0.0;
+            for (int j = 0; j < dk; ++j) {
+                mu += M[(size_t)i * dk + j] * kt[j];
+                mc += Mc[(size_t)i * dk + j] * kt[j];
+            }
+            u[i] = mu;
+            e[i] = mc - vt[i];
+        }
+        /* M (alpha I - eta k k^T) - eta e k^T */
+        for (int i = 0; i < dv; ++i)
+            for (int j = 0; j < dk; ++j) {
+                const size_t ij = (size_t)i * dk + j;
+                M[ij] = al * M[ij] - et * u[i] * kt[j] - et * e[i] * kt[j];
+            }
+        double* zt = a->z + (seq * T + t) * dv;
+        for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += M[(size_t)i * dk + j] * qt[j];
+            zt[i] = acc;
+        }
+    }
+    memcpy(a->W_out + seq * ns, M, ns * sizeof(double));
+    free(M); free(Mc); free(u); free(e);
+}
+
+/* ------------------------------------------------------------------ */
 /* thread pool over the independent (b, h) sequences                  */
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int kind; /* 0 linear, 1 mlp, 2 linear gradient */
+    int kind; /* 0 linear, 1 mlp, 2 linear gradient, 3 DGD */
     const void* args;
     int units, next;
     pthread_mutex_t lock;
@@ -434,9 +499,12 @@ static void* worker(void* p) {
         } else if (pool->kind == 1) {
             const mlp_args* a = (const mlp_args*)pool->args;
             mlp_one(a, u / a->H, u % a->H);
-        } else {
+        } else if (pool->kind == 2) {
             const lin_bwd_args* a = (const lin_bwd_args*)pool->args;
             lin_bwd_one(a, u / a->H, u % a->H);
+        } else {
+            const dgd_args* a = (const dgd_args*)pool->args;
+            dgd_one(a, u / a->H, u % a->H);
         }
     }
     return NULL;
@@ -501,4 +569,16 @@ int oracle_linear_primal_bwd(int B, int H, int T, int dk, int dv, int chunk,
                       shared_over_batch, dz, dWT, dST, dq, dk_, dv_, deta, dtheta, dalpha,
                       dW0, dS0};
     return run_pool(2, &a, B * H, nthreads);
+}
+
+/* DGD memory scan (see the header).  q, k [B][H][T][dk], v [B][H][T][dv],
+   eta (step) and alpha (retention) [B][H][T], W0 [B or 1][H][dv][dk];
+   z [B][H][T][dv] and W_out [B][H][dv][dk] written. */
+int oracle_dgd_primal(int B, int H, int T, int dk, int dv, int chunk, const double* q,
+                      const double* k, const double* v, const double* eta, const double* alpha,
+                      const double* W0, int shared_over_batch, double* z, double* W_out,
+                      int nthreads) {
+    if (B < 1 || H < 1 || T < 0 || dk < 1 || dv < 1 || chunk < 1 || !eta || !alpha) return -1;
+    dgd_args a = {B, H, T, dk, dv, chunk, q, k, v, eta, alpha, W0, shared_over_batch, z, W_out};
+    return run_pool(3, &a, B * H, nthreads);
 }

@@ -1,0 +1,104 @@
+"""Pins of the float64 DGD oracle ("Nested Learning" §8.1 eq (88) with the
+matrix memory and L2 objective of eq (93), chunk-wise as in §8.2) to facts
+outside itself.  CPU only.
+
+- Chunk 1 with retention 1 is the online delta rule toward v / 2 with step
+  2 eta, i.e. the already pinned linear oracle with theta = eta and targets v / 2.
+- Orthonormal keys decouple the k k^T term: every M_{t-1} k_t is the snapshot's
+  M_c k_t times the retention so far, so the chunk has a closed form.
+- The chunk form: with w_t = -eta_t (M_{t-1} k_t + M_c k_t - v_t), M_t is
+  gamma_t M_c + sum_{s<=t} (gamma_t / gamma_s) w_s k_s^T, and the w_t solve a unit
+  lower-triangular system in the key products k_s . k_t (solved here by a
+  library routine), which must give the token loop's outputs.
+"""
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+
+
+def _dgd(q, k, v, eta, alpha, W0, chunk):
+    r = oracle.dgd_primal(q[None, None], k[None, None], v[None, None], eta[None, None],
+                          alpha[None, None], W0[None, None], chunk)
+    return r["z"][0, 0], r["W"][0, 0]
+
+
+def test_chunk_one_unit_retention_is_the_linear_delta_rule():
+    rng = np.random.default_rng(1)
+    T, dk, dv = 17, 5, 3
+    q, k = rng.standard_normal((T, dk)), rng.standard_normal((T, dk)) / np.sqrt(dk)
+    v = rng.standard_normal((T, dv))
+    eta = rng.uniform(0.05, 0.3, T)
+    W0 = rng.standard_normal((dv, dk))
+    z, W = _dgd(q, k, v, eta, np.ones(T), W0, 1)
+    r = oracle.linear_primal(q[None, None], k[None, None], (v / 2)[None, None], eta[None, None],
+                             W0[None, None], 1)
+    assert np.allclose(z, r["z"][0, 0], atol=1e-12)
+    assert np.allclose(W, r["W"][0, 0], atol=1e-12)
+
+
+def test_orthonormal_keys_closed_form():
+    rng = np.random.default_rng(2)
+    dk, dv = 6, 4
+    n = dk                                        # one chunk of dk orthonormal keys
+    Qk, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    k = Qk.T                                      # rows orthonormal
+    q = rng.standard_normal((n, dk))
+    v = rng.standard_normal((n, dv))
+    eta = rng.uniform(0.1, 0.4, n)
+    alpha = rng.uniform(0.7, 1.0, n)
+    Mc = rng.standard_normal((dv, dk))
+    z, W = _dgd(q, k, v, eta, alpha, Mc, n)
+    g = np.cumprod(alpha)                         # gamma_t = prod_{r<=t} alpha_r
+    gprev = np.concatenate([[1.0], g[:-1]])
+    # w_t = -eta_t (gamma_{t-1} Mc k_t + Mc k_t - v_t): no coupling between orthogonal keys
+    w = -eta[:, None] * ((gprev[:, None] + 1.0) * (k @ Mc.T) - v)
+    M_end = g[-1] * Mc + sum((g[-1] / g[s]) * np.outer(w[s], k[s]) for s in range(n))
+    assert np.allclose(W, M_end, atol=1e-12)
+    for t in range(n):
+        Mt = g[t] * Mc + sum((g[t] / g[s]) * np.outer(w[s], k[s]) for s in range(t + 1))
+        assert np.allclose(z[t], Mt @ q[t], atol=1e-12)
+
+
+@pytest.mark.parametrize("T,chunk", [(23, 8), (16, 16), (9, 4)])
+def test_chunk_form_with_triangular_solve(T, chunk):
+    rng = np.random.default_rng(T * 100 + chunk)
+    dk, dv = 5, 3
+    q, k = rng.standard_normal((T, dk)), rng.standard_normal((T, dk)) / np.sqrt(dk)
+    v = rng.standard_normal((T, dv))
+    eta = rng.uniform(0.05, 0.3, T)
+    alpha = rng.uniform(0.6, 1.0, T)
+    W0 = rng.standard_normal((dv, dk))
+    z, W = _dgd(q, k, v, eta, alpha, W0, chunk)
+    M = W0.copy()
+    zs = []
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        K, Q, V, et, al = k[sl], q[sl], v[sl], eta[sl], alpha[sl]
+        n = K.shape[0]
+        g = np.cumprod(al)
+        gprev = np.concatenate([[1.0], g[:-1]])
+        KK = K @ K.T
+        Lm = np.zeros((n, n))
+        for t in range(n):
+            for s in range(t):
+                Lm[t, s] = et[t] * (gprev[t] / g[s]) * KK[s, t]
+        R = -et[:, None] * (gprev[:, None] * (K @ M.T) + (K @ M.T) - V)
+        Wv = scipy.linalg.solve_triangular(np.eye(n) + Lm, R, lower=True, unit_diagonal=True)
+        D = np.tril(g[:, None] / g[None, :])      # gamma_t / gamma_s for s <= t
+        zs.append(g[:, None] * (Q @ M.T) + (D * (Q @ K.T)) @ Wv)
+        M = g[-1] * M + ((g[-1] / g)[:, None] * Wv).T @ K
+    assert np.allclose(z, np.concatenate(zs), atol=1e-11)
+    assert np.allclose(W, M, atol=1e-11)
+
+
+def test_shared_initial_memory():
+    rng = np.random.default_rng(4)
+    B, H, T, d = 2, 2, 7, 3
+    q, k, v = (rng.standard_normal((B, H, T, d)) for _ in range(3))
+    eta, alpha = rng.uniform(0.1, 0.3, (B, H, T)), rng.uniform(0.8, 1.0, (B, H, T))
+    W0 = rng.standard_normal((1, H, d, d))
+    r = oracle.dgd_primal(q, k, v, eta, alpha, W0, 3, shared_over_batch=True)
+    r2 = oracle.dgd_primal(q, k, v, eta, alpha, np.repeat(W0, B, axis=0), 3)
+    assert np.array_equal(r["z"], r2["z"]) and np.array_equal(r["W"], r2["W"])
