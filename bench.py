@@ -430,6 +430,87 @@ def oracle_bwd_sample(w, inp, adj, seconds) -> dict:
 
 
 # ----------------------------------------------------------------------------
+# DGD memory scan (--mode dgd): one ttm_dgd_fwd call per step
+# ----------------------------------------------------------------------------
+
+def run_dgd(args, rank, world, dev):
+    import test_neural_memory_gb300 as ttm
+
+    w = workload_of(args)
+    inp = wl.generate(w)
+    gates = wl.generate_dgd_gates(w.B, w.H, w.T, seed=77)
+    stream = torch.cuda.current_stream(dev)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    g = {k: v.to(dev) for k, v in gates.items()}
+    z = torch.empty_like(d["v"])
+    W = torch.empty((w.B, w.H, w.d, w.d), dtype=torch.float32, device=dev)
+
+    def step():
+        ttm.dgd_fwd(d["q"], d["k"], d["v"], g["eta"], g["alpha"], d["W0"], w.chunk,
+                    w0_shared=w.w0_shared, z=z, W_out=W, stream=stream)
+
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ttm.launch_count()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ttm.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
+    if ttm.device_status() != ttm.OK:
+        raise RuntimeError("device status")
+    es = 2 if w.dtype == "bf16" else 4
+    byte_tok = 4 * w.d * es + 8                     # q, k, v, z and the two gates
+    state = w.d * w.d * 4
+    nbytes = w.tokens * byte_tok + w.B * w.H * 2 * state
+    peaks, src = load_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "DGD-memory scan tokens/s (ttm_dgd_fwd) on 1 GB300",
+        "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name + " (DGD update)", "B": w.B, "H": w.H, "T": w.T,
+                   "d": w.d, "chunk": w.chunk, "kind": "dgd",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (no flush needed)", "kernel": "linear_step (DGD)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": src,
+                     "kernel": "linear_step (DGD)", "algorithmic_bytes": nbytes,
+                     "traffic": None},
+        "e2e": None, "gpu_launches": launches, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        T_s = min(w.T, 2048)
+        f = lambda t: t[:, :, :T_s].double().numpy()
+        t0 = time.perf_counter()
+        r = oracle.dgd_primal(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(gates["eta"]),
+                              f(gates["alpha"]), inp["W0"].double().numpy(), w.chunk,
+                              shared_over_batch=w.w0_shared)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": w.B * w.H * T_s / dt, "unit": UNIT,
+                                "cores": int(r["threads"]), "kind": "oracle", "seconds": dt,
+                                "sample": f"all {w.B * w.H} sequences, first {T_s} tokens"}
+    return line
+
+
+# ----------------------------------------------------------------------------
 # clocks sampled while the GPU is under load
 # ----------------------------------------------------------------------------
 
@@ -741,8 +822,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["scan", "decode", "bwd"], default="scan",
-                    help="decode: the streaming decode step; bwd: the scan's gradient")
+    ap.add_argument("--mode", choices=["scan", "decode", "bwd", "dgd"], default="scan",
+                    help="decode: the streaming decode step; bwd: the scan's gradient; "
+                         "dgd: the DGD-memory scan")
     ap.add_argument("--decode-tokens", type=int, default=1, help="tokens per decode call")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -765,7 +847,7 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     import test_neural_memory_gb300 as ttm
     ttm.build()
-    runner = {"scan": run_ours, "decode": run_decode, "bwd": run_bwd}[args.mode]
+    runner = {"scan": run_ours, "decode": run_decode, "bwd": run_bwd, "dgd": run_dgd}[args.mode]
     line = runner(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -133,6 +133,20 @@ int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
  */
 size_t ttm_linear_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
 
+/* The Titans scan with chunk-level gates ("论文速览 | Titans" §4.6): theta, eta
+ * and alpha are shared by all tokens of a chunk rather than given per token,
+ * which makes the recurrence inside each chunk time-invariant.  Identical to
+ * ttm_titans_fwd except that eta, theta, alpha are [B][H][ceil(T / chunk)] fp32
+ * (one value per sequence and chunk; eta / alpha may be NULL = 0), and that
+ * the kernels read them directly.  Same shapes, workspace
+ * (ttm_linear_workspace_size), errors and aliasing rules as ttm_titans_fwd. */
+int ttm_titans_fwd_chunk_gates(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                               const void* q, const void* k, const void* v,
+                               const float* eta, const float* theta, const float* alpha,
+                               const float* W0, const float* S0, int w0_shared_over_batch,
+                               void* z, float* W_out, float* S_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Deep memory: f(x) = W2 GELU(W1 x), hidden units `hidden`, analytic inner
  * gradients e = 2 (y - v), dW2 = e a^T, dW1 = ((W2^T e) * GELU'(h)) k^T
@@ -277,6 +291,43 @@ int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                    const void* dz, const float* dW,
                    void* dq_out, void* dk_out, void* dv_out, float* dtheta, float* dW0,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* DGD memory scan: the update of "Nested Learning" §8.1 eq (88) with a matrix
+ * memory and the L2 objective of eq (93), taken chunk-wise as in §8.2 (every
+ * gradient of a chunk at the state left by the previous chunk, Mc):
+ *     M_t = M_{t-1} (alpha_t I - eta_t k_t k_t^T) - eta_t (Mc k_t - v_t) k_t^T
+ *     z_t = M_t q_t   (read after the token's write, as for every memory here)
+ * eta_t is the step and alpha_t a retention factor (alpha = 1 keeps the
+ * memory), both as the page prints them: note that alpha here multiplies the
+ * memory, unlike the forgetting rate of ttm_titans_fwd (which keeps 1 - alpha),
+ * and the gradient carries no factor 2.  Unlike the Titans memory, the
+ * k k^T term acts on the running state, so the tokens of a chunk are coupled
+ * through the key products k_s . k_t.
+ *   q, k: [B][H][T][dk], v: [B][H][T][dv] in dtype; eta, alpha: [B][H][T] fp32
+ *     (both required when T > 0); W0: [B or 1][H][dv][dk] fp32 (1 when
+ *     w0_shared_over_batch); z: [B][H][T][dv] in dtype and W_out: [B][H][dv][dk]
+ *     fp32, written.  W_out may be W0 (in place) when W0 is not shared.
+ *   All pointers are device memory owned by the caller, 16-byte aligned; no
+ *   other overlap is allowed.
+ * Shapes: B, H >= 1; T >= 0; chunk >= 1; dk, dv as for ttm_titans_fwd, dk <= 512
+ * (else TTM_ERR_UNSUPPORTED).  Computed in fp32, token by token per row of M
+ * (every row evolves on its own): one warp per (sequence, row).  Asynchronous on
+ * `stream`; TTM_ERR_INVALID_ARG for malformed arguments, TTM_ERR_CUDA if the
+ * launch fails. */
+int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                const void* q, const void* k, const void* v,
+                const float* eta, const float* alpha,
+                const float* W0, int w0_shared_over_batch,
+                void* z, float* W_out, void* stream);
+
+/* Decode step of the DGD memory: continues every sequence by n tokens from the
+ * state W at in-chunk position pos, exactly as ttm_titans_step does for the
+ * Titans memory (same meaning of pos, Wc, shapes and errors), with the DGD
+ * update of ttm_dgd_fwd.  eta, alpha: [B][H][n] fp32, both required. */
+int ttm_dgd_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                 const void* q, const void* k, const void* v,
+                 const float* eta, const float* alpha,
+                 float* W, float* Wc, void* z, void* stream);
 
 /* The activation of the 2-layer memory and its derivative, evaluated on the
  * device exactly as the tensor-core 2-layer kernel evaluates them: for the n

@@ -50,6 +50,9 @@ def lib() -> ctypes.CDLL:
         L.ttm_mlp_gelu.argtypes = [p, p, p, i, p]
         L.ttm_titans_step.argtypes = [i] * 8 + [p] * 6 + [p] * 4 + [p]
         L.ttm_linear_step.argtypes = [i] * 8 + [p] * 4 + [p] * 3 + [p]
+        L.ttm_dgd_fwd.argtypes = [i] * 7 + [p] * 5 + [p, i, p, p, p]
+        L.ttm_titans_fwd_chunk_gates.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p, sz, p]
+        L.ttm_dgd_step.argtypes = [i] * 8 + [p] * 5 + [p, p, p, p]
         L.ttm_titans_bwd_workspace_size.argtypes = [i] * 8
         L.ttm_titans_bwd_workspace_size.restype = sz
         L.ttm_titans_bwd.argtypes = ([i] * 7 + [p] * 6 + [p, p, i] + [p] * 3 + [p] * 3 +
@@ -192,6 +195,29 @@ def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_s
     return z, W_out, S_out
 
 
+def titans_fwd_chunk_gates(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None,
+                           w0_shared=False, z=None, W_out=None, S_out=None, workspace=None,
+                           stream=None):
+    """Titans scan with one gate value per (sequence, chunk): theta / eta / alpha are
+    [B,H,ceil(T/chunk)] fp32.  Returns (z, W_out, S_out)."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    shape = (B, H, dv, dk)
+    W_out = torch.empty(shape, dtype=torch.float32, device=q.device) if W_out is None else W_out
+    S_out = torch.empty(shape, dtype=torch.float32, device=q.device) if S_out is None else S_out
+    if workspace is None:
+        workspace = alloc_workspace(q, v, chunk)
+    wp, wb = _ws(workspace)
+    _check(lib().ttm_titans_fwd_chunk_gates(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q),
+                                            _ptr(k), _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha),
+                                            _ptr(W0), _ptr(S0), int(bool(w0_shared)), _ptr(z),
+                                            _ptr(W_out), _ptr(S_out), wp, wb, _stream(q, stream)),
+           "ttm_titans_fwd_chunk_gates")
+    return z, W_out, S_out
+
+
 def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, Wc=None,
                 z=None, stream=None):
     """Decode step: continues every sequence by n tokens (q, k: [B,H,n,dk]; v: [B,H,n,dv];
@@ -210,6 +236,38 @@ def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, 
                                  _ptr(k), _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W),
                                  _ptr(S), _ptr(Wc), _ptr(z), _stream(q, stream)),
            "ttm_titans_step")
+    return z, Wc, (pos + n) % chunk
+
+
+def dgd_fwd(q, k, v, eta, alpha, W0, chunk, *, w0_shared=False, z=None, W_out=None,
+            stream=None):
+    """DGD memory scan ("Nested Learning" eqs (88), (93)): eta is the step and alpha the
+    retention factor ([B,H,T] fp32).  W0: [B|1,H,dv,dk] fp32.  Returns (z, W_out)."""
+    import torch
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    W_out = (torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+             if W_out is None else W_out)
+    _check(lib().ttm_dgd_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
+                             _ptr(v), _ptr(eta), _ptr(alpha), _ptr(W0), int(bool(w0_shared)),
+                             _ptr(z), _ptr(W_out), _stream(q, stream)), "ttm_dgd_fwd")
+    return z, W_out
+
+
+def dgd_step(q, k, v, eta, alpha, W, chunk, pos, *, Wc=None, z=None, stream=None):
+    """DGD decode step: as titans_step, with the DGD update.  Returns (z, Wc, new_pos)."""
+    import torch
+    B, H, n, dk = q.shape
+    dv = v.shape[-1]
+    z = torch.empty_like(v) if z is None else z
+    if Wc is None:
+        if pos != 0:
+            raise TTMError(ERR_INVALID_ARG, "dgd_step (Wc is required in mid-chunk)")
+        Wc = torch.empty_like(W)
+    _check(lib().ttm_dgd_step(B, H, n, dk, dv, int(chunk), int(pos), _dtype_code(q), _ptr(q),
+                              _ptr(k), _ptr(v), _ptr(eta), _ptr(alpha), _ptr(W), _ptr(Wc),
+                              _ptr(z), _stream(q, stream)), "ttm_dgd_step")
     return z, Wc, (pos + n) % chunk
 
 

@@ -25,7 +25,17 @@ struct LinearArgs {
     // ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be NULL.  The
     // gradient passes read these checkpoints.
     float* ckpt;
+    // Chunk-shared gates: theta / eta / alpha hold one value per (sequence,
+    // chunk), [B][H][ceil(T / chunk)], instead of one per token.
+    int gates_per_chunk;
 };
+
+// Index of token t's gate of sequence seq (per token, or per chunk).
+__host__ __device__ inline size_t gate_index(const LinearArgs& a, size_t seq, int t) {
+    if (!a.gates_per_chunk) return seq * a.T + t;
+    const int nch = (a.T + a.chunk - 1) / a.chunk;
+    return seq * nch + t / a.chunk;
+}
 
 struct MlpArgs {
     int B, H, T, d, hidden, chunk;
@@ -47,8 +57,15 @@ struct StepArgs {
     int bf16;
     const void *q, *k, *v;
     const float *eta, *theta, *alpha;   // eta / alpha may be NULL (= 0)
-    float *W, *S, *Wc;                  // S may be NULL when eta is NULL
+    float *W, *S, *Wc;                  // S may be NULL when eta is NULL; Wc NULL: not kept
     void* z;
+    // mode 0: linear / Titans memory.  mode 1: DGD memory, with theta the step
+    // eta_t and alpha the retention factor alpha_t (required); eta, S unused.
+    int mode;
+    // When W_in is set the state starts from W_in ([B or 1][H][dv][dk], 1 when
+    // w_shared) instead of W, and W only receives the result (a whole scan).
+    const float* W_in;
+    int w_shared;
 };
 
 // One call of the gradient of the linear / Titans scan (scan_bwd.cu).  Inputs

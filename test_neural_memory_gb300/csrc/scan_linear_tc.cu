@@ -258,9 +258,10 @@ __global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, in
     uint8_t* rec = static_cast<uint8_t*>(a.workspace) + (size_t)wid * kRecBytes;
     uint8_t* vec = rec;
 
-    auto eta_at = [&](int t) { return t < n ? (a.eta ? a.eta[tok0 + t] : 0.f) : 1.f; };
-    auto keep_at = [&](int t) { return t < n ? 1.f - (a.alpha ? a.alpha[tok0 + t] : 0.f) : 1.f; };
-    auto theta_at = [&](int t) { return t < n ? a.theta[tok0 + t] : 0.f; };
+    auto gi = [&](int t) { return gate_index(a, (size_t)seq, c * kChunk + t); };
+    auto eta_at = [&](int t) { return t < n ? (a.eta ? a.eta[gi(t)] : 0.f) : 1.f; };
+    auto keep_at = [&](int t) { return t < n ? 1.f - (a.alpha ? a.alpha[gi(t)] : 0.f) : 1.f; };
+    auto theta_at = [&](int t) { return t < n ? a.theta[gi(t)] : 0.f; };
 
     // forward scans
     const int t0 = 2 * lane, t1 = t0 + 1;

@@ -123,9 +123,10 @@ __global__ void __launch_bounds__(kThreads) linear_simt_kernel(LinearArgs p) {
                 Vs[x] = (s < n && i < nr) ? load_in(v, (tok0 + s) * dv + r0 + i) : 0.f;
             }
             for (int s = tid; s < kNB; s += kThreads) {
-                th[s] = s < n ? p.theta[tok0 + s] : 0.f;
-                et[s] = (s < n && mom) ? p.eta[tok0 + s] : 0.f;
-                al[s] = (s < n && p.alpha) ? p.alpha[tok0 + s] : 0.f;
+                const size_t g = gate_index(p, (size_t)seq, s0 + s);
+                th[s] = s < n ? p.theta[g] : 0.f;
+                et[s] = (s < n && mom) ? p.eta[g] : 0.f;
+                al[s] = (s < n && p.alpha) ? p.alpha[g] : 0.f;
             }
             __syncthreads();
             block_coefficients(n, kNB, th, et, al, beta, P, cc, C, kNB + 1, pm);

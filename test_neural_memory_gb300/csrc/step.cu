@@ -11,6 +11,13 @@
 //   z_t = W q_t
 // and W_c is re-taken (W_c = W) whenever a token opens a chunk.
 //
+// The DGD memory ("Nested Learning" §8.1 eq (88) with the matrix memory and
+// L2 objective of eq (93), chunk-wise per §8.2) uses the same row structure:
+//   W = W (alpha_t I - eta_t k k^T) - eta_t (W_c k - v) k^T
+// so row r takes W_r = alpha_t W_r - eta_t ((W_c + W)_r . k - v_r) k^T: one dot
+// product per token and row, like the Titans step.  Run over a whole sequence
+// from W0 (W_in) it is the DGD scan.
+//
 // Every row of W, S and W_c evolves on its own (row r only needs e_r), so one
 // warp owns one row of one sequence for the whole call: lane l holds the
 // columns l, l + 32, ... of the three rows in registers, the two dot products
@@ -59,7 +66,15 @@ __device__ __forceinline__ float warp_sum(float x) {
 // One token per call (the streaming case): the call is bound by reading and
 // writing the state, so every load is issued as early as possible and nothing
 // is staged.  NJ = columns per lane (dk <= 32 NJ).
-template <typename TIn, int NJ>
+// Initial row of the state: W_in (a whole scan; possibly shared over the
+// batch) or the caller's running state W.
+__device__ __forceinline__ const float* initial_row(const StepArgs& a, long long seq, int r) {
+    if (!a.W_in) return a.W + ((size_t)seq * a.dv + r) * a.dk;
+    const long long src = a.w_shared ? seq % a.H : seq;
+    return a.W_in + ((size_t)src * a.dv + r) * a.dk;
+}
+
+template <typename TIn, int NJ, int kMode>
 __global__ void __launch_bounds__(kStepThreads) linear_step_direct(const StepArgs a) {
     const long long gw = ((long long)blockIdx.x * kStepThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -73,36 +88,49 @@ __global__ void __launch_bounds__(kStepThreads) linear_step_direct(const StepArg
     const TIn* q = static_cast<const TIn*>(a.q);
     const TIn* k = static_cast<const TIn*>(a.k);
 
+    const float* w0 = initial_row(a, seq, r);
+    const bool opens = a.pos == 0;   // the token opens a chunk: its gradient point is now
     float w[NJ], s[NJ], wc[NJ], kv[NJ], qv[NJ];
 #pragma unroll
     for (int i = 0; i < NJ; ++i) {
         const int j = lane + 32 * i;
         const bool in = j < dk;
-        w[i] = in ? a.W[row + j] : 0.f;
+        w[i] = in ? w0[j] : 0.f;
         s[i] = (in && a.S) ? a.S[row + j] : 0.f;
-        wc[i] = in ? a.Wc[row + j] : 0.f;
+        wc[i] = (in && !opens) ? a.Wc[row + j] : 0.f;
         kv[i] = in ? ld_in<TIn>(k + tok * dk + j) : 0.f;
         qv[i] = in ? ld_in<TIn>(q + tok * dk + j) : 0.f;
     }
     const float th = __ldg(a.theta + tok);
     const float et = a.eta ? __ldg(a.eta + tok) : 0.f;
-    const float keep = 1.f - (a.alpha ? __ldg(a.alpha + tok) : 0.f);
+    const float al = a.alpha ? __ldg(a.alpha + tok) : 0.f;
     const float vr = ld_in<TIn>(static_cast<const TIn*>(a.v) + tok * a.dv + r);
-    const bool opens = a.pos == 0;   // the token opens a chunk: its gradient point is now
     if (opens) {
 #pragma unroll
         for (int i = 0; i < NJ; ++i) wc[i] = w[i];
     }
     float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
-    const float ge = 2.f * th * (warp_sum(acc) - vr);   // theta times the gradient's row factor
     float zq = 0.f;
+    if constexpr (kMode == 0) {
 #pragma unroll
-    for (int i = 0; i < NJ; ++i) {
-        s[i] = fmaf(et, s[i], -ge * kv[i]);
-        w[i] = fmaf(keep, w[i], s[i]);
-        zq = fmaf(w[i], qv[i], zq);
+        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+        const float ge = 2.f * th * (warp_sum(acc) - vr);   // theta times the gradient's row factor
+        const float keep = 1.f - al;
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            s[i] = fmaf(et, s[i], -ge * kv[i]);
+            w[i] = fmaf(keep, w[i], s[i]);
+            zq = fmaf(w[i], qv[i], zq);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+        const float g = th * (warp_sum(acc) - vr);   // eta_t ((W_c + W) k - v)_r
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            w[i] = fmaf(al, w[i], -g * kv[i]);
+            zq = fmaf(w[i], qv[i], zq);
+        }
     }
     zq = warp_sum(zq);
     if (lane == 0) st_out<TIn>(static_cast<TIn*>(a.z) + tok * a.dv + r, zq);
@@ -112,7 +140,7 @@ __global__ void __launch_bounds__(kStepThreads) linear_step_direct(const StepArg
         if (j >= dk) continue;
         a.W[row + j] = w[i];
         if (a.S) a.S[row + j] = s[i];
-        if (opens) a.Wc[row + j] = wc[i];
+        if (opens && a.Wc) a.Wc[row + j] = wc[i];
     }
 }
 
@@ -157,7 +185,7 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return _
 // which are broadcast by shuffles as each token is processed.  Without the
 // grouping every token would wait for its own loads, a full memory latency
 // per token.
-template <typename TIn, int NJ>
+template <typename TIn, int NJ, int kMode>
 __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
     linear_step_staged(const StepArgs a, int G) {
     extern __shared__ __align__(16) unsigned char step_smem[];
@@ -177,14 +205,15 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
     const TIn* qs = ks + (size_t)G * dk;
 
     stage_tokens<TIn>(ks, G, k, q, (size_t)seq * n, min(G, n), dk, lane);
+    const float* w0 = initial_row(a, seq, r);
     float w[NJ], s[NJ], wc[NJ];
 #pragma unroll
     for (int i = 0; i < NJ; ++i) {
         const int j = lane + 32 * i;
         const bool in = j < dk;
-        w[i] = in ? a.W[row + j] : 0.f;
+        w[i] = in ? w0[j] : 0.f;
         s[i] = (in && a.S) ? a.S[row + j] : 0.f;
-        wc[i] = in ? a.Wc[row + j] : 0.f;
+        wc[i] = (in && a.pos != 0) ? a.Wc[row + j] : 0.f;
     }
     int p = a.pos;
     bool wc_changed = false;
@@ -200,7 +229,8 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
             vr = ld_in<TIn>(v + tok * a.dv + r);
             th = __ldg(a.theta + tok);
             et = a.eta ? __ldg(a.eta + tok) : 0.f;
-            keep = 1.f - (a.alpha ? __ldg(a.alpha + tok) : 0.f);
+            const float al = a.alpha ? __ldg(a.alpha + tok) : 0.f;
+            keep = kMode == 0 ? 1.f - al : al;
         }
         cp_async_wait_all();
         __syncwarp();
@@ -218,19 +248,33 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
                 qv[i] = j < dk ? to_f<TIn>(qs[u * dk + j]) : 0.f;
             }
             float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
-            const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
-            // theta_t times the gradient's row factor
-            const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
-            const float etu = __shfl_sync(0xffffffffu, et, u);
-            const float keepu = __shfl_sync(0xffffffffu, keep, u);
             float zq = 0.f;
+            if constexpr (kMode == 0) {
 #pragma unroll
-            for (int i = 0; i < NJ; ++i) {
-                s[i] = fmaf(etu, s[i], -ge * kv[i]);
-                w[i] = fmaf(keepu, w[i], s[i]);
-                zq = fmaf(w[i], qv[i], zq);
+                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+                const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
+                // theta_t times the gradient's row factor
+                const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
+                const float etu = __shfl_sync(0xffffffffu, et, u);
+                const float keepu = __shfl_sync(0xffffffffu, keep, u);
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) {
+                    s[i] = fmaf(etu, s[i], -ge * kv[i]);
+                    w[i] = fmaf(keepu, w[i], s[i]);
+                    zq = fmaf(w[i], qv[i], zq);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+                // eta_t ((W_c + W) k - v)_r; the retention factor rides in `keep`
+                const float g = __shfl_sync(0xffffffffu, th, u) *
+                                (warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u));
+                const float alu = __shfl_sync(0xffffffffu, keep, u);
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) {
+                    w[i] = fmaf(alu, w[i], -g * kv[i]);
+                    zq = fmaf(w[i], qv[i], zq);
+                }
             }
             zq = warp_sum(zq);
             if (lane == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
@@ -243,7 +287,7 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
         if (j >= dk) continue;
         a.W[row + j] = w[i];
         if (a.S) a.S[row + j] = s[i];
-        if (wc_changed) a.Wc[row + j] = wc[i];
+        if (wc_changed && a.Wc) a.Wc[row + j] = wc[i];
     }
 }
 
@@ -256,19 +300,25 @@ int group_of(const StepArgs& a) {
     int G = 4096 / per_token;
     if (G < 1) G = 1;
     if (G > 32) G = 32;
-    if (G > a.n) G = a.n;
+    if (G > a.n && a.n > 0) G = a.n;
     return G;
+}
+
+template <typename TIn, int NJ, int kMode>
+void launch_mode(const StepArgs& a, unsigned blocks, cudaStream_t s) {
+    if (a.n == 1) {
+        linear_step_direct<TIn, NJ, kMode><<<blocks, kStepThreads, 0, s>>>(a);
+    } else {
+        const int G = group_of(a);
+        const size_t smem = (size_t)(kStepThreads / 32) * 2 * G * a.dk * sizeof(TIn);
+        linear_step_staged<TIn, NJ, kMode><<<blocks, kStepThreads, smem, s>>>(a, G);
+    }
 }
 
 template <typename TIn, int NJ>
 void launch_nj(const StepArgs& a, unsigned blocks, cudaStream_t s) {
-    if (a.n == 1) {
-        linear_step_direct<TIn, NJ><<<blocks, kStepThreads, 0, s>>>(a);
-    } else {
-        const int G = group_of(a);
-        const size_t smem = (size_t)(kStepThreads / 32) * 2 * G * a.dk * sizeof(TIn);
-        linear_step_staged<TIn, NJ><<<blocks, kStepThreads, smem, s>>>(a, G);
-    }
+    if (a.mode == 1) launch_mode<TIn, NJ, 1>(a, blocks, s);
+    else launch_mode<TIn, NJ, 0>(a, blocks, s);
 }
 
 template <typename TIn>

@@ -86,7 +86,7 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
                   const void* k, const void* v, const float* eta, const float* theta,
                   const float* alpha, const float* W0, const float* S0, int shared, void* z,
                   float* W_out, float* S_out, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+                  void* stream, int gates_per_chunk = 0) {
     if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
     if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
     if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
@@ -103,7 +103,8 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     const size_t nb0 = shared ? 1 : (size_t)B;
     const size_t st = (size_t)H * dv * dk * sizeof(float);
     const Span sq{q, tok * dk * es}, sk{k, tok * dk * es}, sv{v, tok * dv * es};
-    const Span sg[] = {{eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
+    const size_t ngate = gates_per_chunk ? (size_t)B * H * ((T + chunk - 1) / chunk) : tok;
+    const Span sg[] = {{eta, ngate * 4}, {theta, ngate * 4}, {alpha, ngate * 4}};
     const Span sW0{W0, nb0 * st}, sS0{S0, nb0 * st};
     const Span sz{z, tok * dv * es}, sW{W_out, (size_t)B * st}, sS{S_out, (size_t)B * st};
     const Span outs[] = {sz, sW, sS};
@@ -133,6 +134,7 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     a.W0 = W0; a.S0 = S0; a.shared = shared ? 1 : 0;
     a.z = z; a.W_out = W_out; a.S_out = S_out;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.gates_per_chunk = gates_per_chunk ? 1 : 0;
 
     const int kid = select_linear(a);
     if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
@@ -149,6 +151,45 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     t_last_kernel = kid;
     // the tensor-core path enqueues the coefficient pre-pass and the scan
     __atomic_add_fetch(&g_launches, kid == TTM_KID_LINEAR_TC ? 2ULL : 1ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+// Decode step of the linear / Titans (mode 0) or DGD (mode 1) memory.
+int step_common(int mode, int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                const void* q, const void* k, const void* v, const float* eta,
+                const float* theta, const float* alpha, float* W, float* S, float* Wc, void* z,
+                void* stream) {
+    if (B < 1 || H < 1 || n < 1 || chunk < 1 || pos < 0 || pos >= chunk) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
+    if (!q || !k || !v || !theta || !W || !Wc || !z) return TTM_ERR_INVALID_ARG;
+    if (mode == 1 && !alpha) return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, eta, theta, alpha, W, S, Wc, z};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * n;
+    const size_t st = (size_t)B * H * dv * dk * sizeof(float);
+    const Span ins[] = {{q, tok * dk * es}, {k, tok * dk * es}, {v, tok * dv * es},
+                        {eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
+    const Span outs[] = {{W, st}, {S, st}, {Wc, st}, {z, tok * dv * es}};
+    for (int o = 0; o < 4; ++o) {
+        for (const Span& i : ins)
+            if (overlap(outs[o], i)) return TTM_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlap(outs[o], outs[o2])) return TTM_ERR_INVALID_ARG;
+    }
+    ttm::StepArgs a{};
+    a.B = B; a.H = H; a.n = n; a.dk = dk; a.dv = dv; a.chunk = chunk; a.pos = pos;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v;
+    a.eta = eta; a.theta = theta; a.alpha = alpha;
+    a.W = W; a.S = S; a.Wc = Wc; a.z = z;
+    a.mode = mode;
+    if (!ttm::linear_step_supported(a)) return TTM_ERR_UNSUPPORTED;
+    if (ttm::linear_step_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTM_ERR_CUDA;
+    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
     return TTM_OK;
 }
 
@@ -174,6 +215,17 @@ int ttm_titans_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, eta, theta, alpha, W0, S0,
                          w0_shared_over_batch, z, W_out, S_out, workspace, workspace_bytes,
                          stream);
+}
+
+int ttm_titans_fwd_chunk_gates(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                               const void* q, const void* k, const void* v, const float* eta,
+                               const float* theta, const float* alpha, const float* W0,
+                               const float* S0, int w0_shared_over_batch, void* z,
+                               float* W_out, float* S_out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return linear_common(B, H, T, dk, dv, chunk, dtype, q, k, v, eta, theta, alpha, W0, S0,
+                         w0_shared_over_batch, z, W_out, S_out, workspace, workspace_bytes,
+                         stream, 1);
 }
 
 size_t ttm_linear_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
@@ -256,37 +308,9 @@ int ttm_titans_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int
                     const void* q, const void* k, const void* v, const float* eta,
                     const float* theta, const float* alpha, float* W, float* S, float* Wc,
                     void* z, void* stream) {
-    if (B < 1 || H < 1 || n < 1 || chunk < 1 || pos < 0 || pos >= chunk) return TTM_ERR_INVALID_ARG;
-    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
-    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
-    if (!q || !k || !v || !theta || !W || !Wc || !z) return TTM_ERR_INVALID_ARG;
     if (eta && !S) return TTM_ERR_INVALID_ARG;   // momentum needs its state
-    const void* ptrs[] = {q, k, v, eta, theta, alpha, W, S, Wc, z};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
-    const size_t es = dtype == TTM_BF16 ? 2 : 4;
-    const size_t tok = (size_t)B * H * n;
-    const size_t st = (size_t)B * H * dv * dk * sizeof(float);
-    const Span ins[] = {{q, tok * dk * es}, {k, tok * dk * es}, {v, tok * dv * es},
-                        {eta, tok * 4}, {theta, tok * 4}, {alpha, tok * 4}};
-    const Span outs[] = {{W, st}, {S, st}, {Wc, st}, {z, tok * dv * es}};
-    for (int o = 0; o < 4; ++o) {
-        for (const Span& i : ins)
-            if (overlap(outs[o], i)) return TTM_ERR_INVALID_ARG;
-        for (int o2 = o + 1; o2 < 4; ++o2)
-            if (overlap(outs[o], outs[o2])) return TTM_ERR_INVALID_ARG;
-    }
-    ttm::StepArgs a{};
-    a.B = B; a.H = H; a.n = n; a.dk = dk; a.dv = dv; a.chunk = chunk; a.pos = pos;
-    a.bf16 = dtype == TTM_BF16;
-    a.q = q; a.k = k; a.v = v;
-    a.eta = eta; a.theta = theta; a.alpha = alpha;
-    a.W = W; a.S = S; a.Wc = Wc; a.z = z;
-    if (!ttm::linear_step_supported(a)) return TTM_ERR_UNSUPPORTED;
-    if (ttm::linear_step_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return TTM_ERR_CUDA;
-    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
-    return TTM_OK;
+    return step_common(0, B, H, n, dk, dv, chunk, pos, dtype, q, k, v, eta, theta, alpha, W, S,
+                       Wc, z, stream);
 }
 
 int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
@@ -385,6 +409,52 @@ int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     return ttm_titans_bwd(B, H, T, dk, dv, chunk, dtype, q, k, v, nullptr, theta, nullptr, W0,
                           nullptr, w0_shared_over_batch, dz, dW, nullptr, dq, dk_, dv_, nullptr,
                           dtheta, nullptr, dW0, nullptr, workspace, workspace_bytes, stream);
+}
+
+int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
+                const void* k, const void* v, const float* eta, const float* alpha,
+                const float* W0, int w0_shared_over_batch, void* z, float* W_out,
+                void* stream) {
+    if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
+    if (!W0 || !W_out) return TTM_ERR_INVALID_ARG;
+    if (T > 0 && (!q || !k || !v || !eta || !alpha || !z)) return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, eta, alpha, W0, z, W_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+    const int shared = w0_shared_over_batch ? 1 : 0;
+    const size_t es = dtype == TTM_BF16 ? 2 : 4;
+    const size_t tok = (size_t)B * H * T;
+    const size_t st = (size_t)H * dv * dk * sizeof(float);
+    const Span ins[] = {{q, tok * dk * es}, {k, tok * dk * es}, {v, tok * dv * es},
+                        {eta, tok * 4}, {alpha, tok * 4}};
+    const Span sW0{W0, (shared ? 1 : (size_t)B) * st};
+    const Span sz{z, tok * dv * es}, sW{W_out, (size_t)B * st};
+    for (const Span& i : ins)
+        if (overlap(sz, i) || overlap(sW, i)) return TTM_ERR_INVALID_ARG;
+    if (overlap(sz, sW) || overlap(sz, sW0)) return TTM_ERR_INVALID_ARG;
+    if (bad_alias(sW, sW0, !shared)) return TTM_ERR_INVALID_ARG;   // in place when not shared
+    ttm::StepArgs a{};
+    a.B = B; a.H = H; a.n = T; a.dk = dk; a.dv = dv; a.chunk = chunk; a.pos = 0;
+    a.bf16 = dtype == TTM_BF16;
+    a.q = q; a.k = k; a.v = v;
+    a.theta = eta; a.alpha = alpha;
+    a.W = W_out; a.z = z;
+    a.mode = 1;
+    a.W_in = W0; a.w_shared = shared;
+    if (!ttm::linear_step_supported(a)) return TTM_ERR_UNSUPPORTED;
+    if (ttm::linear_step_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTM_ERR_CUDA;
+    __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
+}
+
+int ttm_dgd_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dtype,
+                 const void* q, const void* k, const void* v, const float* eta,
+                 const float* alpha, float* W, float* Wc, void* z, void* stream) {
+    return step_common(1, B, H, n, dk, dv, chunk, pos, dtype, q, k, v, nullptr, eta, alpha, W,
+                       nullptr, Wc, z, stream);
 }
 
 int ttm_mlp_gelu(const float* x, float* y, float* dy, int n, void* stream) {

@@ -135,3 +135,25 @@ def generate_adjoints(B, H, T, dk, dv, dtype="f32", seed=0, with_S=True) -> dict
     dW = torch.randn((B, H, dv, dk), generator=g)
     dS = torch.randn((B, H, dv, dk), generator=g) if with_S else None
     return dict(dz=dz, dW=dW, dS=dS)
+
+
+def generate_dgd_gates(B, H, T, seed=0) -> dict:
+    """Seeded gates of the DGD memory: step eta_t = 0.1 sigmoid(N(0,1)) and
+    retention alpha_t = 0.9 + 0.1 sigmoid(N(0,1)), [B,H,T] fp32, drawn in that
+    order from a CPU generator.  With L2-normalised keys the factor
+    (alpha I - eta k k^T) then stays a contraction."""
+    g = torch.Generator().manual_seed(seed)
+    eta = 0.1 * torch.sigmoid(torch.randn((B, H, T), generator=g))
+    alpha = 0.9 + 0.1 * torch.sigmoid(torch.randn((B, H, T), generator=g))
+    return dict(eta=eta, alpha=alpha)
+
+
+def generate_chunk_gates(B, H, nch, theta_scale=0.1, seed=0) -> dict:
+    """Seeded chunk-level gates with the Titans recipe, one value per (sequence,
+    chunk): theta = s sigmoid(N(0,1)), eta = 0.8 + 0.2 sigmoid(N(0,1)),
+    alpha = 0.05 sigmoid(N(0,1)), [B,H,nch] fp32, drawn in that order."""
+    g = torch.Generator().manual_seed(seed)
+    theta = theta_scale * torch.sigmoid(torch.randn((B, H, nch), generator=g))
+    eta = 0.8 + 0.2 * torch.sigmoid(torch.randn((B, H, nch), generator=g))
+    alpha = 0.05 * torch.sigmoid(torch.randn((B, H, nch), generator=g))
+    return dict(theta=theta, eta=eta, alpha=alpha)
