@@ -511,6 +511,80 @@ def run_dgd(args, rank, world, dev):
 
 
 # ----------------------------------------------------------------------------
+# LMM layer (--mode layer): one ttm_lmm_layer_fwd call per step
+# ----------------------------------------------------------------------------
+
+def run_layer(args, rank, world, dev):
+    import test_neural_memory_gb300 as ttm
+
+    w = workload_of(args)
+    B, T, Hh, d = w.B, w.T, w.H, w.d
+    D = Hh * d
+    p = wl.generate_lmm(B, T, Hh, d, conv_k=4, seed=99)
+    dp = {k: v.to(dev) for k, v in p.items()}
+    stream = torch.cuda.current_stream(dev)
+    n_ws = int(ttm.lib().ttm_lmm_layer_workspace_size(B, T, Hh, d, w.chunk, 1))
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(dp["x"])
+    Wout = torch.empty((B, Hh, d, d), dtype=torch.float32, device=dev)
+    Sout = torch.empty_like(Wout)
+
+    def step():
+        ttm.lmm_layer_fwd(dp["x"], dp["W_in"], dp["conv_w"], dp["rms_w"], dp["W_o"], 0.1,
+                          dp["W0"], w.chunk, y=y, W_out=Wout, S_out=Sout, workspace=ws,
+                          stream=stream)
+
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ttm.launch_count()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = ttm.launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
+    if ttm.device_status() != ttm.OK:
+        raise RuntimeError("device status")
+    P = 4 * D + 3 * Hh
+    gemm_flops = 2 * B * T * D * (P + D)
+    scan_flops = algorithmic(w)["flops"]
+    flops = gemm_flops + scan_flops
+    peaks, src = load_peaks()
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "LMM-layer tokens/s (ttm_lmm_layer_fwd: projections, conv, scan, output) on 1 GB300",
+        "value": B * T * world / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic, random-init weights",
+        "config": {"workload": f"LMM layer B{B} T{T} H{Hh} d{d} (D={D}) chunk {w.chunk} conv 4",
+                   "B": B, "T": T, "H": Hh, "d": d, "chunk": w.chunk,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (no flush needed)", "kernel": "lmm layer"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": src, "kernel": "lmm layer (whole call)",
+                     "algorithmic_flops": flops, "gemm_flops": gemm_flops,
+                     "scan_flops": scan_flops, "traffic": None},
+        "e2e": None, "gpu_launches": launches, "clocks": clocks,
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------
 # clocks sampled while the GPU is under load
 # ----------------------------------------------------------------------------
 
@@ -822,9 +896,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["scan", "decode", "bwd", "dgd"], default="scan",
+    ap.add_argument("--mode", choices=["scan", "decode", "bwd", "dgd", "layer"], default="scan",
                     help="decode: the streaming decode step; bwd: the scan's gradient; "
-                         "dgd: the DGD-memory scan")
+                         "dgd: the DGD-memory scan; layer: the LMM layer")
     ap.add_argument("--decode-tokens", type=int, default=1, help="tokens per decode call")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -847,7 +921,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     import test_neural_memory_gb300 as ttm
     ttm.build()
-    runner = {"scan": run_ours, "decode": run_decode, "bwd": run_bwd, "dgd": run_dgd}[args.mode]
+    runner = {"scan": run_ours, "decode": run_decode, "bwd": run_bwd, "dgd": run_dgd,
+              "layer": run_layer}[args.mode]
     line = runner(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -329,6 +329,41 @@ int ttm_dgd_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dt
                  const float* eta, const float* alpha,
                  float* W, float* Wc, void* z, void* stream);
 
+/* LMM layer: the neural memory used on its own as a sequence layer
+ * ("论文速览 | Titans" §6.4) with the projection details of §7.1-§7.3, for
+ * x [B][T][D] (D = H d) in bf16:
+ *   p = x W_in                          W_in [D][4D + 3H] bf16: columns q | k | v | g (D
+ *                                       each), then the theta, eta, alpha logits (H each)
+ *   q, k, v = SiLU(causal depthwise conv of width conv_k of p's q, k, v columns);
+ *     conv_w [3][D][conv_k] fp32, tap j weighting token t - (conv_k - 1) + j
+ *     (tokens before the sequence start read zero); q and k l2-normalised per head
+ *   theta = theta_scale sigmoid, eta = sigmoid, alpha = sigmoid of the logits
+ *   z = the Titans memory scan of ttm_titans_fwd per head, from W0 ([B or 1][H][d][d]
+ *     fp32, 1 when w0_shared_over_batch; S0 = 0)
+ *   o = z / sqrt(mean_d(z^2) + 1e-6) * rms_w * g   (per head; rms_w [d] fp32; g the
+ *     linear gate from p)
+ *   y = x + o W_o                       W_o [D][D] bf16; y [B][T][D] bf16, written
+ * W_out and S_out ([B][H][d][d] fp32; S_out may be NULL) receive the final memory.
+ * The pages leave the wiring open; this is the plainest reading: the
+ * projection, conv, SiLU order of the modern recurrent layers the page cites,
+ * and a linear (un-squashed) output gate.
+ * The two projections are plain bf16 GEMMs through cuBLAS (fp32 accumulation);
+ * p, q, k, v, z and o are stored in bf16.  workspace: device scratch of
+ * ttm_lmm_layer_workspace_size() bytes, owned by the caller (it also serves as
+ * cuBLAS's workspace).  All pointers are device memory, 16-byte aligned; no
+ * output may overlap an input, another output or the workspace.
+ * Shapes: B, T, H >= 1; d in {32, 64, 128, 256}; 1 <= conv_k <= 8; chunk >= 1
+ * (TTM_ERR_UNSUPPORTED otherwise).  Asynchronous on `stream`;
+ * TTM_ERR_INVALID_ARG for malformed arguments or a short workspace,
+ * TTM_ERR_CUDA if a launch or a GEMM fails. */
+size_t ttm_lmm_layer_workspace_size(int B, int T, int H, int d, int chunk, int w0_shared);
+int ttm_lmm_layer_fwd(int B, int T, int H, int d, int chunk, int conv_k,
+                      const void* x, const void* W_in, const float* conv_w,
+                      const float* rms_w, const void* W_o, float theta_scale,
+                      const float* W0, int w0_shared_over_batch,
+                      void* y, float* W_out, float* S_out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* The activation of the 2-layer memory and its derivative, evaluated on the
  * device exactly as the tensor-core 2-layer kernel evaluates them: for the n
  * values x[i], y[i] = GELU(x) = x Phi(x) and, if dy is not NULL,

@@ -51,6 +51,10 @@ def lib() -> ctypes.CDLL:
         L.ttm_titans_step.argtypes = [i] * 8 + [p] * 6 + [p] * 4 + [p]
         L.ttm_linear_step.argtypes = [i] * 8 + [p] * 4 + [p] * 3 + [p]
         L.ttm_dgd_fwd.argtypes = [i] * 7 + [p] * 5 + [p, i, p, p, p]
+        L.ttm_lmm_layer_workspace_size.argtypes = [i] * 6
+        L.ttm_lmm_layer_workspace_size.restype = sz
+        L.ttm_lmm_layer_fwd.argtypes = ([i] * 6 + [p] * 5 + [ctypes.c_float, p, i, p, p, p, p, sz,
+                                                              p])
         L.ttm_titans_fwd_chunk_gates.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p, sz, p]
         L.ttm_dgd_step.argtypes = [i] * 8 + [p] * 5 + [p, p, p, p]
         L.ttm_titans_bwd_workspace_size.argtypes = [i] * 8
@@ -269,6 +273,32 @@ def dgd_step(q, k, v, eta, alpha, W, chunk, pos, *, Wc=None, z=None, stream=None
                               _ptr(k), _ptr(v), _ptr(eta), _ptr(alpha), _ptr(W), _ptr(Wc),
                               _ptr(z), _stream(q, stream)), "ttm_dgd_step")
     return z, Wc, (pos + n) % chunk
+
+
+def lmm_layer_fwd(x, W_in, conv_w, rms_w, W_o, theta_scale, W0, chunk, *, w0_shared=True,
+                  y=None, W_out=None, S_out=None, workspace=None, stream=None):
+    """LMM layer (memory as a standalone sequence layer): x [B,T,H*d] bf16 -> y; see
+    ttm_lmm_layer_fwd for the wiring.  H is read from W0 ([1|B,H,d,d]).  Returns
+    (y, W_out, S_out)."""
+    import torch
+    B, T, D = x.shape
+    H, d = W0.shape[1], W0.shape[-1]
+    conv_k = conv_w.shape[-1]
+    y = torch.empty_like(x) if y is None else y
+    shape = (B, H, d, d)
+    W_out = torch.empty(shape, dtype=torch.float32, device=x.device) if W_out is None else W_out
+    S_out = torch.empty(shape, dtype=torch.float32, device=x.device) if S_out is None else S_out
+    if workspace is None:
+        n = int(lib().ttm_lmm_layer_workspace_size(B, T, H, d, int(chunk), int(bool(w0_shared))))
+        if n == 0:
+            raise TTMError(ERR_UNSUPPORTED, "ttm_lmm_layer_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    wp, wb = _ws(workspace)
+    _check(lib().ttm_lmm_layer_fwd(B, T, H, d, int(chunk), conv_k, _ptr(x), _ptr(W_in),
+                                   _ptr(conv_w), _ptr(rms_w), _ptr(W_o), float(theta_scale),
+                                   _ptr(W0), int(bool(w0_shared)), _ptr(y), _ptr(W_out),
+                                   _ptr(S_out), wp, wb, _stream(x, stream)), "ttm_lmm_layer_fwd")
+    return y, W_out, S_out
 
 
 def titans_bwd(q, k, v, theta, W0, chunk, dz, *, eta=None, alpha=None, S0=None, dW=None,

@@ -64,7 +64,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-lcublas",
+           "-Xlinker", "-rpath=" + os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64"),
+           "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

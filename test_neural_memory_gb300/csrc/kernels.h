@@ -91,6 +91,19 @@ struct BwdArgs {
     int* status;    // device status word of the tensor-core scan's bounded waits
 };
 
+// One call of the LMM layer (lmm_layer.cu + the scan); bf16 activations.
+struct LmmArgs {
+    int B, T, H, d, chunk, conv_k;
+    const void* x;          // [B][T][D] bf16, D = H d
+    const void* W_in;       // [D][4D + 3H] bf16: q | k | v | g | theta, eta, alpha logits
+    const float* conv_w;    // [3][D][conv_k]: causal depthwise taps of q, k, v
+    const float* rms_w;     // [d]: per-channel scale of the per-head RMS norm
+    const void* W_o;        // [D][D] bf16
+    float theta_scale;      // theta = theta_scale * sigmoid(logit)
+    const float* W0;        // [B or 1][H][d][d] initial memory
+    int w0_shared;
+};
+
 // fp32 CUDA-core kernels (scan_simt.cu).  The *_supported functions decide
 // on the host whether a shape fits the kernel's on-chip budget.
 bool linear_simt_supported(const LinearArgs& a);
@@ -118,6 +131,15 @@ cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
 bool linear_bwd_supported(const BwdArgs& a);
 size_t linear_bwd_workspace_bytes(const BwdArgs& a);
 cudaError_t linear_bwd_launch(const BwdArgs& a, cudaStream_t s, int* launches);
+
+// LMM layer pieces (lmm_layer.cu): d a multiple of 32 up to 256, conv width 1..8.
+bool lmm_supported(const LmmArgs& a);
+cudaError_t lmm_prep_launch(const LmmArgs& a, const void* proj, void* qkv, float* gates,
+                            cudaStream_t s);
+cudaError_t lmm_post_launch(const LmmArgs& a, const void* proj, const void* z, void* o,
+                            cudaStream_t s);
+bool gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float beta,
+               void* scratch, size_t scratch_bytes, cudaStream_t s);
 
 // The activation of that kernel on n values: y = GELU(x), dy = GELU'(x) (dy may be NULL).
 cudaError_t mlp_gelu_launch(const float* x, float* y, float* dy, int n, cudaStream_t s);

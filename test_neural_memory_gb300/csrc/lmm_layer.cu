@@ -1,0 +1,274 @@
+// LMM layer around the scan: the neural memory used on its own as a sequence
+// layer ("论文速览 | Titans" §6.4), with the projection details of §7.1-§7.3
+// (SiLU after the q, k, v projections, l2-normalised q and k, a short causal
+// depthwise convolution after the projections, residual connection,
+// normalisation and linear gating before the output projection).
+//
+//   p = x W_in                      one bf16 GEMM (cuBLAS): q | k | v | g | 3H gate logits
+//   prep: q, k, v = SiLU(causal depthwise conv of width K of p's q / k / v columns),
+//         q, k l2-normalised per head, stored head-major [B][H][T][d] in bf16;
+//         theta = s sigmoid, eta = sigmoid, alpha = sigmoid of the logits, [B][H][T]
+//   z = Titans memory scan (the library's scan kernels)
+//   post: o = RMSNorm_head(z) * rms_w * g, [B][T][D] in bf16
+//   y = x + o W_o                   one bf16 GEMM (cuBLAS), residual as beta = 1
+//
+// The prep and post kernels are HBM-bound elementwise / per-head reductions:
+// one warp per (token, head, stream), lanes over the head's d channels.
+#include <cublas_v2.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace ttm {
+namespace {
+
+constexpr int kLayerThreads = 256;
+
+__device__ __forceinline__ float lwarp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+__device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
+
+// VW consecutive bf16 values at p (p aligned to VW elements when kVec).
+template <int VW, bool kVec>
+__device__ __forceinline__ void load_vw(const __nv_bfloat16* p, float* out) {
+    if constexpr (kVec && VW == 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            out[2 * e] = __uint_as_float(w[e] << 16);
+            out[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+        }
+    } else if constexpr (kVec && VW == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        out[0] = __uint_as_float(u.x << 16); out[1] = __uint_as_float(u.x & 0xffff0000u);
+        out[2] = __uint_as_float(u.y << 16); out[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else if constexpr (kVec && VW == 2) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        out[0] = __uint_as_float(u << 16); out[1] = __uint_as_float(u & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int e = 0; e < VW; ++e) out[e] = __bfloat162float(p[e]);
+    }
+}
+
+template <int VW>
+__device__ __forceinline__ void store_vw(__nv_bfloat16* p, const float* x) {
+#pragma unroll
+    for (int e = 0; e < VW; e += 2)
+        *reinterpret_cast<__nv_bfloat162*>(p + e) = __floats2bfloat162_rn(x[e], x[e + 1]);
+}
+
+constexpr int kTile = 4;    // tokens per prep warp
+
+// One warp per (b, h, s, tile of kTile tokens), s = 0, 1, 2 for q, k, v.  Lane
+// l holds channels l, l + 32, ... (NJ = d / 32) of the head, so that each load
+// of the conv taps (a channel's taps are contiguous) and each row load is
+// contiguous across the warp.  The taps stay in registers for the tile, and
+// every input row of the tile (kTile + NW - 1 of them, NW >= the conv width) is
+// loaded before any is used.
+template <int NJ, int NW>
+__global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2) lmm_prep_kernel(const LmmArgs a,
+                                                                 const __nv_bfloat16* proj,
+                                                                 __nv_bfloat16* qkv,
+                                                                 float* gates) {
+    const long long gw = ((long long)blockIdx.x * kLayerThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, d = a.d, T = a.T, K = a.conv_k;
+    const int ntile = (T + kTile - 1) / kTile;
+    if (gw >= (long long)a.B * H * 3 * ntile) return;
+    const int s = (int)(gw % 3);
+    long long rest = gw / 3;
+    const int h = (int)(rest % H);
+    rest /= H;
+    const int tile = (int)(rest % ntile);
+    const int b = (int)(rest / ntile);
+    const int D = H * d, P = 4 * D + 3 * H;
+    const int c0 = s * D + h * d;                     // first channel of the head
+    const int t0 = tile * kTile, t1 = min(T, t0 + kTile);
+    // window slot j of token t0 + i is row i + j; its weight is tap j - (NW - K)
+    float wwin[NW][NJ];
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const float* w = a.conv_w + ((size_t)c0 + lane + 32 * i) * K;
+        if (K == 4 && NW == 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(w);
+            wwin[0][i] = w4.x; wwin[1][i] = w4.y; wwin[2][i] = w4.z; wwin[3][i] = w4.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < NW; ++j) {
+                const int tap = j - (NW - K);
+                wwin[j][i] = tap >= 0 ? w[tap] : 0.f;
+            }
+        }
+    }
+    constexpr int kRowsT = kTile + NW - 1;
+    float xr[kRowsT][NJ];
+#pragma unroll
+    for (int r = 0; r < kRowsT; ++r) {
+        const int ts = t0 - (NW - 1) + r;
+        const bool live = ts >= 0 && ts < t1 && r >= NW - K;
+        const __nv_bfloat16* src = proj + ((size_t)b * T + (live ? ts : 0)) * P + c0 + lane;
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) xr[r][i] = live ? __bfloat162float(src[32 * i]) : 0.f;
+    }
+    const size_t plane = (size_t)a.B * H * T;
+    if (s == 0) {   // lanes 0..kTile-1: the three gates of token t0 + lane of head h
+        const int t = t0 + lane;
+        if (lane < kTile && t < t1) {
+            const __nv_bfloat16* lg = proj + ((size_t)b * T + t) * P + 4 * D + h;
+            const size_t gi = ((size_t)b * H + h) * T + t;
+            gates[gi] = a.theta_scale * sigm(__bfloat162float(lg[0]));
+            gates[plane + gi] = sigm(__bfloat162float(lg[H]));
+            gates[2 * plane + gi] = sigm(__bfloat162float(lg[2 * H]));
+        }
+    }
+    const size_t stream_stride = (size_t)a.B * H * T * d;
+#pragma unroll
+    for (int tt = 0; tt < kTile; ++tt) {
+        const int t = t0 + tt;
+        if (t >= t1) break;
+        float u[NJ];
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < NW; ++j) acc = fmaf(wwin[j][i], xr[tt + j][i], acc);
+            // SiLU; the fast intrinsics' error is far below the bf16 rounding of the output
+            u[i] = __fdividef(acc, 1.f + __expf(-acc));
+        }
+        if (s < 2) {   // l2-normalise q and k per head
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) ss += u[i] * u[i];
+            const float inv = 1.f / fmaxf(sqrtf(lwarp_sum(ss)), 1e-6f);
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) u[i] *= inv;
+        }
+        __nv_bfloat16* dst = qkv + s * stream_stride + (((size_t)b * H + h) * T + t) * d + lane;
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) dst[32 * i] = __float2bfloat16_rn(u[i]);
+    }
+}
+
+// One warp per (b, t, h): o = z / sqrt(mean(z^2) + eps) * rms_w * g; lane l
+// holds channels l VW ... of the head.
+template <int VW, bool kVec>
+__global__ void __launch_bounds__(kLayerThreads) lmm_post_kernel(const LmmArgs a,
+                                                                 const __nv_bfloat16* proj,
+                                                                 const __nv_bfloat16* z,
+                                                                 __nv_bfloat16* o) {
+    const long long gw = ((long long)blockIdx.x * kLayerThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, d = a.d, T = a.T;
+    if (gw >= (long long)a.B * T * H) return;
+    const int h = (int)(gw % H);
+    const long long bt = gw / H;
+    const int t = (int)(bt % T);
+    const int b = (int)(bt / T);
+    const int D = H * d, P = 4 * D + 3 * H;
+    float zz[VW], gg[VW];
+    load_vw<VW, true>(z + (((size_t)b * H + h) * T + t) * d + lane * VW, zz);
+    load_vw<VW, kVec>(proj + ((size_t)b * T + t) * P + 3 * D + h * d + lane * VW, gg);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) ss += zz[e] * zz[e];
+    const float r = 1.f / sqrtf(lwarp_sum(ss) / d + 1e-6f);
+    float out[VW];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) out[e] = zz[e] * r * a.rms_w[lane * VW + e] * gg[e];
+    __nv_bfloat16* orow = o + ((size_t)b * T + t) * D + h * d + lane * VW;
+    if constexpr (VW == 1) orow[0] = __float2bfloat16_rn(out[0]);
+    else store_vw<VW>(orow, out);
+}
+
+std::mutex g_blas_lock;
+cublasHandle_t g_blas[64];
+
+cublasHandle_t blas_handle() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_blas_lock);
+    if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) g_blas[dev] = nullptr;
+    return g_blas[dev];
+}
+
+}  // namespace
+
+bool lmm_supported(const LmmArgs& a) {
+    return (a.d == 32 || a.d == 64 || a.d == 128 || a.d == 256) && a.conv_k >= 1 &&
+           a.conv_k <= 8;
+}
+
+template <int NJ>
+void prep_nj(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloat16* p,
+             __nv_bfloat16* q, float* g) {
+    if (a.conv_k <= 4) lmm_prep_kernel<NJ, 4><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+    else lmm_prep_kernel<NJ, 8><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+}
+
+template <int VW>
+void post_vw(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloat16* p,
+             const __nv_bfloat16* z, __nv_bfloat16* o) {
+    const int P = 4 * a.H * a.d + 3 * a.H;
+    if (P % VW == 0) lmm_post_kernel<VW, true><<<blocks, kLayerThreads, 0, s>>>(a, p, z, o);
+    else lmm_post_kernel<VW, false><<<blocks, kLayerThreads, 0, s>>>(a, p, z, o);
+}
+
+cudaError_t lmm_prep_launch(const LmmArgs& a, const void* proj, void* qkv, float* gates,
+                            cudaStream_t s) {
+    const long long warps = (long long)a.B * a.H * 3 * ((a.T + kTile - 1) / kTile);
+    const unsigned blocks = (unsigned)((warps * 32 + kLayerThreads - 1) / kLayerThreads);
+    auto p = static_cast<const __nv_bfloat16*>(proj);
+    auto q = static_cast<__nv_bfloat16*>(qkv);
+    switch (a.d / 32) {
+        case 1: prep_nj<1>(a, blocks, s, p, q, gates); break;
+        case 2: prep_nj<2>(a, blocks, s, p, q, gates); break;
+        case 4: prep_nj<4>(a, blocks, s, p, q, gates); break;
+        case 8: prep_nj<8>(a, blocks, s, p, q, gates); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t lmm_post_launch(const LmmArgs& a, const void* proj, const void* z, void* o,
+                            cudaStream_t s) {
+    const long long warps = (long long)a.B * a.T * a.H;
+    const unsigned blocks = (unsigned)((warps * 32 + kLayerThreads - 1) / kLayerThreads);
+    auto p = static_cast<const __nv_bfloat16*>(proj);
+    auto zz = static_cast<const __nv_bfloat16*>(z);
+    auto oo = static_cast<__nv_bfloat16*>(o);
+    switch (a.d / 32) {
+        case 1: post_vw<1>(a, blocks, s, p, zz, oo); break;
+        case 2: post_vw<2>(a, blocks, s, p, zz, oo); break;
+        case 4: post_vw<4>(a, blocks, s, p, zz, oo); break;
+        case 8: post_vw<8>(a, blocks, s, p, zz, oo); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// Row-major C[M x N] = alpha A[M x K] B[K x N] + beta C, bf16 operands, fp32
+// accumulation (cuBLAS, column-major: C^T = B^T A^T).  `scratch` is handed to
+// cuBLAS as its workspace so that the library allocates nothing.
+bool gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, float beta,
+               void* scratch, size_t scratch_bytes, cudaStream_t s) {
+    cublasHandle_t h = blas_handle();
+    if (!h) return false;
+    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return false;
+    if (cublasSetWorkspace(h, scratch, scratch_bytes) != CUBLAS_STATUS_SUCCESS) return false;
+    const float one = 1.f;
+    return cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, N, M, K, &one, B, CUDA_R_16BF, N, A,
+                        CUDA_R_16BF, K, &beta, C, CUDA_R_16BF, N, CUBLAS_COMPUTE_32F,
+                        CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+}
+
+}  // namespace ttm

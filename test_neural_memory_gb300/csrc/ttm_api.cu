@@ -193,6 +193,39 @@ int step_common(int mode, int B, int H, int n, int dk, int dv, int chunk, int po
     return TTM_OK;
 }
 
+// Workspace of the LMM layer (bytes, each piece 256-byte aligned): projection
+// output, q / k / v, gates, z, o, the scan's own workspace and cuBLAS scratch.
+struct LmmLayout {
+    size_t proj, qkv, gates, z, o, scan, blas, total, scan_bytes;
+};
+
+constexpr size_t kBlasScratch = 32u << 20;
+
+LmmLayout lmm_layout(const ttm::LmmArgs& a, const ttm::LinearArgs& scan) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t BT = (size_t)a.B * a.T, D = (size_t)a.H * a.d, P = 4 * D + 3 * a.H;
+    const size_t tok = (size_t)a.B * a.H * a.T;
+    LmmLayout L;
+    L.proj = 0;
+    L.qkv = L.proj + up(BT * P * 2);
+    L.gates = L.qkv + up(3 * tok * a.d * 2);
+    L.z = L.gates + up(3 * tok * 4);
+    L.o = L.z + up(tok * a.d * 2);
+    L.scan = L.o + up(BT * D * 2);
+    L.scan_bytes = select_linear(scan) == TTM_KID_LINEAR_TC ? ttm::linear_tc_workspace_bytes(scan) : 0;
+    L.blas = L.scan + up(L.scan_bytes);
+    L.total = L.blas + kBlasScratch;
+    return L;
+}
+
+ttm::LinearArgs lmm_scan_args(const ttm::LmmArgs& a) {
+    ttm::LinearArgs s{};
+    s.B = a.B; s.H = a.H; s.T = a.T; s.dk = a.d; s.dv = a.d; s.chunk = a.chunk;
+    s.bf16 = 1;
+    s.shared = a.w0_shared;
+    return s;
+}
+
 }  // namespace
 
 extern "C" {
@@ -455,6 +488,84 @@ int ttm_dgd_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int dt
                  const float* alpha, float* W, float* Wc, void* z, void* stream) {
     return step_common(1, B, H, n, dk, dv, chunk, pos, dtype, q, k, v, nullptr, eta, alpha, W,
                        nullptr, Wc, z, stream);
+}
+
+size_t ttm_lmm_layer_workspace_size(int B, int T, int H, int d, int chunk, int w0_shared) {
+    if (B < 1 || T < 1 || H < 1 || chunk < 1) return 0;
+    ttm::LmmArgs a{};
+    a.B = B; a.T = T; a.H = H; a.d = d; a.chunk = chunk; a.conv_k = 1;
+    a.w0_shared = w0_shared ? 1 : 0;
+    if (!ttm::lmm_supported(a)) return 0;
+    return lmm_layout(a, lmm_scan_args(a)).total;
+}
+
+int ttm_lmm_layer_fwd(int B, int T, int H, int d, int chunk, int conv_k, const void* x,
+                      const void* W_in, const float* conv_w, const float* rms_w,
+                      const void* W_o, float theta_scale, const float* W0,
+                      int w0_shared_over_batch, void* y, float* W_out, float* S_out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 1 || T < 1 || H < 1 || chunk < 1) return TTM_ERR_INVALID_ARG;
+    if (!x || !W_in || !conv_w || !rms_w || !W_o || !W0 || !y || !W_out || !workspace)
+        return TTM_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, W_in, conv_w, rms_w, W_o, W0, y, W_out, S_out, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
+    ttm::LmmArgs a{};
+    a.B = B; a.T = T; a.H = H; a.d = d; a.chunk = chunk; a.conv_k = conv_k;
+    a.x = x; a.W_in = W_in; a.conv_w = conv_w; a.rms_w = rms_w; a.W_o = W_o;
+    a.theta_scale = theta_scale; a.W0 = W0; a.w0_shared = w0_shared_over_batch ? 1 : 0;
+    if (!ttm::lmm_supported(a) || (long long)B * T > (1LL << 31) - 1) return TTM_ERR_UNSUPPORTED;
+    ttm::LinearArgs sc = lmm_scan_args(a);
+    if (select_linear(sc) == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+    const LmmLayout L = lmm_layout(a, sc);
+    if (workspace_bytes < L.total) return TTM_ERR_INVALID_ARG;
+    const size_t BT = (size_t)B * T, D = (size_t)H * d, P = 4 * D + 3 * H;
+    const size_t st = (size_t)H * d * d * 4;
+    const Span ins[] = {{x, BT * D * 2}, {W_in, D * P * 2}, {conv_w, 3 * D * conv_k * 4},
+                        {rms_w, (size_t)d * 4}, {W_o, D * D * 2},
+                        {W0, (a.w0_shared ? 1 : (size_t)B) * st}};
+    const Span outs[] = {{y, BT * D * 2}, {W_out, (size_t)B * st}, {S_out, (size_t)B * st},
+                         {workspace, workspace_bytes}};
+    for (int o = 0; o < 4; ++o) {
+        for (const Span& i : ins)
+            if (overlap(outs[o], i)) return TTM_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlap(outs[o], outs[o2])) return TTM_ERR_INVALID_ARG;
+    }
+    int* status = status_ptr();
+    if (!status) return TTM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* proj = ws + L.proj;
+    uint8_t* qkv = ws + L.qkv;
+    float* gates = reinterpret_cast<float*>(ws + L.gates);
+    void* z = ws + L.z;
+    void* o = ws + L.o;
+    const size_t tok = (size_t)B * H * T;
+    // p = x W_in
+    if (!ttm::gemm_bf16(x, W_in, proj, (int)BT, (int)P, (int)D, 0.f, ws + L.blas, kBlasScratch, s))
+        return TTM_ERR_CUDA;
+    if (ttm::lmm_prep_launch(a, proj, qkv, gates, s) != cudaSuccess) return TTM_ERR_CUDA;
+    // the memory scan over the prepared q, k, v and gates
+    sc.q = qkv; sc.k = qkv + tok * d * 2; sc.v = qkv + 2 * tok * d * 2;
+    sc.theta = gates; sc.eta = gates + tok; sc.alpha = gates + 2 * tok;
+    sc.W0 = W0; sc.z = z; sc.W_out = W_out; sc.S_out = S_out;
+    sc.workspace = L.scan_bytes ? ws + L.scan : nullptr;
+    sc.workspace_bytes = L.scan_bytes;
+    sc.status = status;
+    const int kid = select_linear(sc);
+    const cudaError_t e = kid == TTM_KID_LINEAR_TC ? ttm::linear_tc_launch(sc, s)
+                                                   : ttm::linear_simt_launch(sc, s);
+    if (e != cudaSuccess) return TTM_ERR_CUDA;
+    if (ttm::lmm_post_launch(a, proj, z, o, s) != cudaSuccess) return TTM_ERR_CUDA;
+    // y = x + o W_o
+    if (cudaMemcpyAsync(y, x, BT * D * 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return TTM_ERR_CUDA;
+    if (!ttm::gemm_bf16(o, W_o, y, (int)BT, (int)D, (int)D, 1.f, ws + L.blas, kBlasScratch, s))
+        return TTM_ERR_CUDA;
+    t_last_kernel = kid;
+    __atomic_add_fetch(&g_launches, kid == TTM_KID_LINEAR_TC ? 4ULL : 3ULL, __ATOMIC_RELAXED);
+    return TTM_OK;
 }
 
 int ttm_mlp_gelu(const float* x, float* y, float* dy, int n, void* stream) {

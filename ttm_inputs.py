@@ -157,3 +157,19 @@ def generate_chunk_gates(B, H, nch, theta_scale=0.1, seed=0) -> dict:
     eta = 0.8 + 0.2 * torch.sigmoid(torch.randn((B, H, nch), generator=g))
     alpha = 0.05 * torch.sigmoid(torch.randn((B, H, nch), generator=g))
     return dict(theta=theta, eta=eta, alpha=alpha)
+
+
+def generate_lmm(B, T, H, d, conv_k=4, seed=0) -> dict:
+    """Seeded input and random-init parameters of the LMM layer, drawn in this
+    order from a CPU generator: x ~ N(0,1) [B,T,D] bf16; W_in ~ N(0, 0.05^2)
+    [D, 4D+3H] bf16; conv_w ~ N(0,1)/conv_k [3,D,conv_k]; rms_w = 1 + 0.1 N(0,1)
+    [d]; W_o ~ N(0, 0.05^2) [D,D] bf16; W0 ~ N(0, 0.02^2) [1,H,d,d] (shared)."""
+    g = torch.Generator().manual_seed(seed)
+    D = H * d
+    x = torch.randn((B, T, D), generator=g).to(torch.bfloat16)
+    W_in = (0.05 * torch.randn((D, 4 * D + 3 * H), generator=g)).to(torch.bfloat16)
+    conv_w = torch.randn((3, D, conv_k), generator=g) / conv_k
+    rms_w = 1.0 + 0.1 * torch.randn((d,), generator=g)
+    W_o = (0.05 * torch.randn((D, D), generator=g)).to(torch.bfloat16)
+    W0 = 0.02 * torch.randn((1, H, d, d), generator=g)
+    return dict(x=x, W_in=W_in, conv_w=conv_w, rms_w=rms_w, W_o=W_o, W0=W0)
