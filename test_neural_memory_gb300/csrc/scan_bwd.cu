@@ -51,10 +51,16 @@ using simt::block_coefficients;
 using simt::load_in;
 using simt::store_out;
 
+__device__ __forceinline__ float warp_sum_f(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
 constexpr int kBT = 256;      // threads per CTA
 constexpr int kMaxBC = 64;    // largest chunk
 constexpr int kMaxDK = 128;   // widest key
-constexpr int kR2 = 8;        // rows of the adjoint per chain CTA
+constexpr int kR2 = 16;       // rows of the adjoint per chain CTA
 constexpr int kR3 = 16;       // rows per tile in the local pass
 constexpr int kBT3 = 512;     // threads per local-pass CTA
 
@@ -97,10 +103,10 @@ BwdLayout bwd_layout(const BwdArgs& a) {
 template <typename Tin>
 __global__ void __launch_bounds__(kBT) bwd_records_kernel(const BwdArgs a, const BwdLayout L,
                                                           float* ws) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int tid = threadIdx.x;
     const int seq = blockIdx.x, c = blockIdx.y;
-    const int dk = a.dk, bc = L.bc, ldk = dk + 1;
+    const int dk = a.dk, bc = L.bc, ldk = dk + 4;   // 16-byte aligned rows
     const int t0 = c * bc, n = min(bc, a.T - t0);
     float* Qs = sm;                    // [bc][ldk]
     float* Ks = Qs + bc * ldk;         // [bc][ldk]
@@ -132,7 +138,11 @@ __global__ void __launch_bounds__(kBT) bwd_records_kernel(const BwdArgs a, const
         const int t = x / bc, s = x % bc;
         float acc = 0.f;
         if (s <= t && t < n) {
-            for (int j = 0; j < dk; ++j) acc += Qs[t * ldk + j] * Ks[s * ldk + j];
+            for (int j = 0; j < dk; j += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(Qs + t * ldk + j);
+                const float4 b4 = *reinterpret_cast<const float4*>(Ks + s * ldk + j);
+                acc += a4.x * b4.x + a4.y * b4.y + a4.z * b4.z + a4.w * b4.w;
+            }
             acc *= C[t * (bc + 1) + s];
         }
         rec[x] = acc;
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kBT) bwd_records_kernel(const BwdArgs a, const
 // chain: the adjoint of the state at every chunk end, chunks in reverse
 // ------------------------------------------------------------------------
 
-constexpr int kBT2 = 512;     // threads per chain CTA (two per SM: every CTA of a call resident)
+constexpr int kBT2 = 512;     // threads per chain CTA (one per SM)
 
 // 16-byte pieces of q (and of k) per thread and chunk, at most
 template <typename Tin>
@@ -167,7 +177,7 @@ struct ChainPrefetch {
     static constexpr int kPre = pieces_per_thread<Tin>();
     uint4 q[kPre], k[kPre];
     float4 A[2];
-    float vec, dz;
+    float vec, dz[2];
 };
 
 template <typename Tin>
@@ -195,48 +205,94 @@ __device__ __forceinline__ void chain_fetch(ChainPrefetch<Tin>& f, const BwdArgs
         f.A[u] = v < (bc * bc + 3) / 4 ? __ldg(rec4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     f.vec = tid < 4 * bc + 1 ? __ldg(rec + (size_t)bc * bc + tid) : 0.f;
-    const int s = tid / kR2, i = tid % kR2;
-    f.dz = (s < n && i < nr) ? load_in(static_cast<const Tin*>(a.dz), (tok0 + s) * a.dv + r0 + i)
-                             : 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int x = tid + u * kBT2, s = x / kR2, i = x % kR2;
+        f.dz[u] = (s < n && i < nr)
+                      ? load_in(static_cast<const Tin*>(a.dz), (tok0 + s) * a.dv + r0 + i)
+                      : 0.f;
+    }
 }
 
+// dst is 16-byte aligned (rows of dk + 4 floats, pieces of 4 or 8 values).
 __device__ __forceinline__ void unpack_piece(const uint4& p, float* dst, const float*) {
-    const float4 x = *reinterpret_cast<const float4*>(&p);
-    dst[0] = x.x; dst[1] = x.y; dst[2] = x.z; dst[3] = x.w;
+    *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(&p);
 }
 __device__ __forceinline__ void unpack_piece(const uint4& p, float* dst, const __nv_bfloat16*) {
-    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        dst[2 * e] = __uint_as_float(w[e] << 16);
-        dst[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
+    float4* d4 = reinterpret_cast<float4*>(dst);
+    d4[0] = make_float4(__uint_as_float(p.x << 16), __uint_as_float(p.x & 0xffff0000u),
+                        __uint_as_float(p.y << 16), __uint_as_float(p.y & 0xffff0000u));
+    d4[1] = make_float4(__uint_as_float(p.z << 16), __uint_as_float(p.z & 0xffff0000u),
+                        __uint_as_float(p.w << 16), __uint_as_float(p.w & 0xffff0000u));
 }
 
 // ------------------------------------------------------------------------
 // chain: the adjoint of the state at every chunk end, chunks in reverse
 // ------------------------------------------------------------------------
 
+// Shared-memory carve-up of the chain pass (floats; every region a multiple of
+// 4 floats so that 16-byte rows stay aligned).
+struct ChainSmem {
+    int ldk;                       // row stride of q, k and the adjoint rows: dk + 4
+    size_t Qs, Ks, A, dZ, bz, cz, de, dWK, dSK, dW, dS, vec, total;
+};
+
+__host__ __device__ inline ChainSmem chain_smem(int bc, int dk) {
+    auto up = [](size_t x) { return (x + 3) / 4 * 4; };
+    ChainSmem m;
+    m.ldk = dk + 4;
+    size_t o = 0;
+    // q and k, later reused for the update's four token-group partial sums of
+    // W and S ([4][2][kR2][dk]): the region holds the larger of the two
+    const size_t qk = 2 * up((size_t)bc * m.ldk), parts = 8 * (size_t)kR2 * dk;
+    m.Qs = o;
+    m.Ks = o + up((size_t)bc * m.ldk);
+    o += qk > parts ? qk : parts;
+    m.A = o; o += up((size_t)bc * (bc + 1));
+    m.dZ = o; o += up((size_t)bc * kR2);
+    m.bz = o; o += up((size_t)bc * kR2);
+    m.cz = o; o += up((size_t)bc * kR2);
+    m.de = o; o += up((size_t)bc * kR2);
+    m.dWK = o; o += up((size_t)bc * kR2);
+    m.dSK = o; o += up((size_t)bc * kR2);
+    m.dW = o; o += up((size_t)kR2 * m.ldk);
+    m.dS = o; o += up((size_t)kR2 * m.ldk);
+    m.vec = o; o += up(4 * (size_t)bc + 1);
+    m.total = o;
+    return m;
+}
+
+// One CTA per (sequence, slice of kR2 = 16 rows), chunks in reverse.  Per chunk:
+//   keys:   dWK[s][i] = (dWe k_s)_i, dSK likewise  (thread: one key s, rows 2p, 2p+1,
+//           16-byte steps along the key)
+//   errors: de[s][i] = -2 (sum_{t>=s} A[t][s] dz_t[i] + C_n[s] dWK + pm[s] dSK)
+//   update: dW = beta_n dW + sum_t (beta_t dz_t[i] q_t + de_t[i] k_t),
+//           dS = c_n dW + P_n dS + sum_t c_t dz_t[i] q_t
+//           (thread: row i = tid / 32, columns 4 (tid % 32) .. + 3; per token one
+//           16-byte load of q and of k and three broadcasts)
 template <typename Tin>
-__global__ void __launch_bounds__(kBT2, 2) bwd_chain_kernel(const BwdArgs a, const BwdLayout L,
-                                                         float* ws) {
-    extern __shared__ float sm[];
+__global__ void __launch_bounds__(kBT2, 1) bwd_chain_kernel(const BwdArgs a, const BwdLayout L,
+                                                            float* ws) {
+    extern __shared__ __align__(16) float sm[];
     const int tid = threadIdx.x;
     const int seq = blockIdx.x;
-    const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = dk + 1;
+    const int dk = a.dk, dv = a.dv, bc = L.bc;
     const int r0 = blockIdx.y * kR2, nr = min(kR2, dv - r0);
-    constexpr int ldr = kR2 + 1;
     constexpr int per = 16 / sizeof(Tin);
-    float* Qs = sm;                    // [bc][ldk]
-    float* Ks = Qs + bc * ldk;         // [bc][ldk]
-    float* A = Ks + bc * ldk;          // [bc][bc + 1]
-    float* dZ = A + bc * (bc + 1);     // [bc][ldr]
-    float* dWK = dZ + bc * ldr;        // [bc][ldr]  (dWe k_s)_i
-    float* dSK = dWK + bc * ldr;       // [bc][ldr]  (dSe k_s)_i
-    float* de = dSK + bc * ldr;        // [bc][ldr]
-    float* dW = de + bc * ldr;         // [kR2][ldk] running adjoint of W
-    float* dS = dW + kR2 * ldk;        // [kR2][ldk] running adjoint of S
-    float* vec = dS + kR2 * ldk;       // beta, cc, clast, pm [bc] each, P_n
+    const ChainSmem M = chain_smem(bc, dk);
+    const int ldk = M.ldk;
+    float* Qs = sm + M.Qs;
+    float* Ks = sm + M.Ks;
+    float* A = sm + M.A;
+    float* dZ = sm + M.dZ;      // [bc][kR2]
+    float* bz = sm + M.bz;      // beta_t dz_t[i]
+    float* cz = sm + M.cz;      // c_t dz_t[i]
+    float* de = sm + M.de;
+    float* dWK = sm + M.dWK;
+    float* dSK = sm + M.dSK;
+    float* dW = sm + M.dW;      // [kR2][ldk] running adjoint of W
+    float* dS = sm + M.dS;
+    float* vec = sm + M.vec;    // beta, cc, clast, pm [bc] each, P_n
 
     const size_t sd = L.sd;
     for (int x = tid; x < kR2 * dk; x += kBT2) {
@@ -247,6 +303,11 @@ __global__ void __launch_bounds__(kBT2, 2) bwd_chain_kernel(const BwdArgs a, con
     }
     ChainPrefetch<Tin> f;
     chain_fetch<Tin>(f, a, L, ws, seq, L.nch - 1, r0, nr);
+    const int ks = tid >> 3, kp = tid & 7;          // errors phase: key, row pair
+    // keys phase: key = tid % 64 across the lanes, row pair = tid / 64 uniform per
+    // warp, so the adjoint rows are broadcast reads and the key rows conflict-free
+    const int kk = tid & 63, kq = tid >> 6;
+    const int uj = (tid & 31) * 4;                  // update phase: first column of the lane
     for (int c = L.nch - 1; c >= 0; --c) {
         const int t0 = c * bc, n = min(bc, a.T - t0);
         __syncthreads();   // the previous chunk is done with every buffer
@@ -270,9 +331,10 @@ __global__ void __launch_bounds__(kBT2, 2) bwd_chain_kernel(const BwdArgs a, con
                     const int idx = 4 * v + e;   // element t * bc + s of the table
                     if (idx < bc * bc) A[(idx / bc) * (bc + 1) + idx % bc] = x4[e];
                 }
+                const int x = tid + u * kBT2;
+                if (x < bc * kR2) dZ[x] = f.dz[u];
             }
             if (tid < 4 * bc + 1) vec[tid] = f.vec;
-            if (tid < bc * kR2) dZ[(tid / kR2) * ldr + tid % kR2] = f.dz;
         }
         // this chunk's end adjoint, for the local pass
         float* adj = ws + L.adj + ((size_t)seq * L.nch + c) * 2 * sd;
@@ -288,39 +350,103 @@ __global__ void __launch_bounds__(kBT2, 2) bwd_chain_kernel(const BwdArgs a, con
         const float* clast = vec + 2 * bc;
         const float* pm = vec + 3 * bc;
         const float Pn = vec[4 * bc];
-        for (int x = tid; x < bc * kR2; x += kBT2) {
-            const int s = x / kR2, i = x % kR2;
-            float uw = 0.f, us = 0.f;
-            for (int j = 0; j < dk; ++j) {
-                const float ks = Ks[s * ldk + j];
-                uw += dW[i * ldk + j] * ks;
-                us += dS[i * ldk + j] * ks;
+        if (kk < bc) {   // keys against the end adjoints; scaled dz for the update
+            const int ks = kk, i0 = 2 * kq, i1 = i0 + 1;
+            float uw0 = 0.f, uw1 = 0.f, us0 = 0.f, us1 = 0.f;
+            for (int j = 0; j < dk; j += 4) {
+                const float4 k4 = *reinterpret_cast<const float4*>(Ks + ks * ldk + j);
+                const float4 w0 = *reinterpret_cast<const float4*>(dW + i0 * ldk + j);
+                const float4 w1 = *reinterpret_cast<const float4*>(dW + i1 * ldk + j);
+                const float4 s0 = *reinterpret_cast<const float4*>(dS + i0 * ldk + j);
+                const float4 s1 = *reinterpret_cast<const float4*>(dS + i1 * ldk + j);
+                uw0 += k4.x * w0.x + k4.y * w0.y + k4.z * w0.z + k4.w * w0.w;
+                uw1 += k4.x * w1.x + k4.y * w1.y + k4.z * w1.z + k4.w * w1.w;
+                us0 += k4.x * s0.x + k4.y * s0.y + k4.z * s0.z + k4.w * s0.w;
+                us1 += k4.x * s1.x + k4.y * s1.y + k4.z * s1.z + k4.w * s1.w;
             }
-            dWK[s * ldr + i] = uw;
-            dSK[s * ldr + i] = us;
+            dWK[ks * kR2 + i0] = uw0;
+            dWK[ks * kR2 + i1] = uw1;
+            dSK[ks * kR2 + i0] = us0;
+            dSK[ks * kR2 + i1] = us1;
+            const float z0 = dZ[ks * kR2 + i0], z1 = dZ[ks * kR2 + i1];
+            const bool live = ks < n;
+            bz[ks * kR2 + i0] = live ? beta[ks] * z0 : 0.f;
+            bz[ks * kR2 + i1] = live ? beta[ks] * z1 : 0.f;
+            cz[ks * kR2 + i0] = live ? cc[ks] * z0 : 0.f;
+            cz[ks * kR2 + i1] = live ? cc[ks] * z1 : 0.f;
         }
         __syncthreads();
-        for (int x = tid; x < bc * kR2; x += kBT2) {
-            const int s = x / kR2, i = x % kR2;
-            float acc = 0.f;
-            for (int t = s; t < n; ++t) acc += A[t * (bc + 1) + s] * dZ[t * ldr + i];
-            de[s * ldr + i] = s < n ? -2.f * (acc + clast[s] * dWK[s * ldr + i] +
-                                              pm[s] * dSK[s * ldr + i])
-                                    : 0.f;
+        if (ks < bc) {   // errors
+            const int i0 = 2 * kp;
+            float a0 = 0.f, a1 = 0.f;
+            for (int t = ks; t < n; ++t) {
+                const float at = A[t * (bc + 1) + ks];
+                const float2 z = *reinterpret_cast<const float2*>(dZ + t * kR2 + i0);
+                a0 += at * z.x;
+                a1 += at * z.y;
+            }
+            const bool live = ks < n;
+            de[ks * kR2 + i0] = live ? -2.f * (a0 + clast[ks] * dWK[ks * kR2 + i0] +
+                                               pm[ks] * dSK[ks * kR2 + i0]) : 0.f;
+            de[ks * kR2 + i0 + 1] = live ? -2.f * (a1 + clast[ks] * dWK[ks * kR2 + i0 + 1] +
+                                                   pm[ks] * dSK[ks * kR2 + i0 + 1]) : 0.f;
         }
         __syncthreads();
-        const float bn = beta[n - 1], cn = cc[n - 1];
-        for (int x = tid; x < kR2 * dk; x += kBT2) {
-            const int i = x / dk, j = x % dk;
-            float gw = 0.f, gs = 0.f;
-            for (int t = 0; t < n; ++t) {
-                const float zq = dZ[t * ldr + i] * Qs[t * ldk + j];
-                gw += beta[t] * zq + de[t * ldr + i] * Ks[t * ldk + j];
-                gs += cc[t] * zq;
+        // State-adjoint update: warp w owns rows 4 (w % 4) .. + 3 and tokens
+        // 16 (w / 4) .. + 15; lane l columns 4 l .. + 3.  The four token groups'
+        // partial sums meet in the q / k buffers once every warp is done reading them.
+        float gw[4][4], gs[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gw[r][e] = gs[r][e] = 0.f;
+        const int uw = tid >> 5, rg = (uw & 3) * 4, tg = uw >> 2;
+        const int tq0 = tg * 16, tq1 = min(n, tq0 + 16);
+        if (uj < dk) {
+            for (int t = tq0; t < tq1; ++t) {
+                const float4 q4 = *reinterpret_cast<const float4*>(Qs + t * ldk + uj);
+                const float4 k4 = *reinterpret_cast<const float4*>(Ks + t * ldk + uj);
+                const float4 b4 = *reinterpret_cast<const float4*>(bz + t * kR2 + rg);
+                const float4 e4 = *reinterpret_cast<const float4*>(de + t * kR2 + rg);
+                const float4 c4 = *reinterpret_cast<const float4*>(cz + t * kR2 + rg);
+                const float qv[4] = {q4.x, q4.y, q4.z, q4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+                const float bv[4] = {b4.x, b4.y, b4.z, b4.w}, ev[4] = {e4.x, e4.y, e4.z, e4.w};
+                const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        gw[r][e] = fmaf(bv[r], qv[e], fmaf(ev[r], kv[e], gw[r][e]));
+                        gs[r][e] = fmaf(cv[r], qv[e], gs[r][e]);
+                    }
             }
-            const float w = dW[i * ldk + j], sv = dS[i * ldk + j];
-            dW[i * ldk + j] = bn * w + gw;
-            dS[i * ldk + j] = cn * w + Pn * sv + gs;
+        }
+        __syncthreads();   // every warp is done with q and k
+        float* part = Qs;  // [4 token groups][W | S][kR2][dk]
+        if (uj < dk) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float* pw = part + ((tg * 2 + 0) * kR2 + rg + r) * dk + uj;
+                float* ps = part + ((tg * 2 + 1) * kR2 + rg + r) * dk + uj;
+                *reinterpret_cast<float4*>(pw) = make_float4(gw[r][0], gw[r][1], gw[r][2], gw[r][3]);
+                *reinterpret_cast<float4*>(ps) = make_float4(gs[r][0], gs[r][1], gs[r][2], gs[r][3]);
+            }
+        }
+        __syncthreads();
+        {
+            const float bn = beta[n - 1], cn = cc[n - 1];
+            for (int x = tid; x < kR2 * dk; x += kBT2) {
+                const int i = x / dk, j = x % dk;
+                float sw = 0.f, ss = 0.f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    sw += part[((g * 2 + 0) * kR2 + i) * dk + j];
+                    ss += part[((g * 2 + 1) * kR2 + i) * dk + j];
+                }
+                const float w = dW[i * ldk + j], sv = dS[i * ldk + j];
+                dW[i * ldk + j] = bn * w + sw;
+                dS[i * ldk + j] = cn * w + Pn * sv + ss;
+            }
         }
     }
     __syncthreads();
@@ -384,18 +510,45 @@ __global__ void bwd_shared_reduce_kernel(const BwdArgs a, const BwdLayout L, con
 // local: dq, dk, dv and the gate gradients of one chunk
 // ------------------------------------------------------------------------
 
-// The q / k buffers are reused at the end for the two [bc][bc + 1] tables of
-// the gate gradients, so that region holds the larger of the two uses.
-__host__ __device__ inline size_t local_qk_floats(int bc, int dk) {
-    const size_t qk = 2 * (size_t)bc * (dk + 1), tables = 2 * (size_t)bc * (bc + 1);
-    return qk > tables ? qk : tables;
+// Shared-memory carve-up of the local pass (floats).  Rows of q, k and the
+// state tiles are dk + 4 floats (16-byte aligned for vector loads); every
+// region starts on a 4-float boundary.  The q / k buffers are reused at the end
+// for the two [bc][bc + 1] tables of the gate gradients, so that region holds
+// the larger of the two uses.
+struct LocalSmem {
+    int ldk, ldb;
+    size_t Qs, Ks, QK, Cm, Xm, Wr, Sr, dWr, dSr, dZt, Et, dWK, dSK, de, vec, total;
+};
+
+__host__ __device__ inline LocalSmem local_smem(int bc, int dk) {
+    auto up = [](size_t x) { return (x + 3) / 4 * 4; };
+    LocalSmem m;
+    m.ldk = dk + 4;
+    m.ldb = bc + 1;
+    const size_t ldr = kR3 + 1;
+    const size_t qk = 2 * (size_t)bc * m.ldk, tables = 2 * (size_t)bc * m.ldb;
+    size_t o = 0;
+    m.Qs = o;
+    m.Ks = o + (size_t)bc * m.ldk;
+    o += up(qk > tables ? qk : tables);
+    m.QK = o; o += up((size_t)bc * m.ldb);
+    m.Cm = o; o += up((size_t)bc * m.ldb);
+    m.Xm = o; o += up((size_t)bc * m.ldb);
+    m.Wr = o; o += (size_t)kR3 * m.ldk;
+    m.Sr = o; o += (size_t)kR3 * m.ldk;
+    m.dWr = o; o += (size_t)kR3 * m.ldk;
+    m.dSr = o; o += (size_t)kR3 * m.ldk;
+    m.dZt = o; o += up(bc * ldr);
+    m.Et = o; o += up(bc * ldr);
+    m.dWK = o; o += up(bc * ldr);
+    m.dSK = o; o += up(bc * ldr);
+    m.de = o; o += up(bc * ldr);
+    m.vec = o; o += up(14 * (size_t)bc + 4);
+    m.total = o;
+    return m;
 }
 
-size_t local_smem_floats(int bc, int dk) {
-    const size_t ldk = dk + 1, ldb = bc + 1, ldr = kR3 + 1;
-    return local_qk_floats(bc, dk) + 3 * bc * ldb + 4 * kR3 * ldk + 5 * bc * ldr +
-           14 * (size_t)bc + 4;
-}
+size_t local_smem_floats(int bc, int dk) { return local_smem(bc, dk).total; }
 
 // A thread owns rows t = 4 tg + a (a < 4) and columns j = jg + 32 bb (bb < 4)
 // of dq / dk (tg = tid / 32, jg = tid % 32), and the 4 x 2 block of
@@ -403,30 +556,31 @@ size_t local_smem_floats(int bc, int dk) {
 template <typename Tin>
 __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, const BwdLayout L,
                                                            const float* ws) {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     const int tid = threadIdx.x;
     const int seq = blockIdx.x, c = blockIdx.y;
-    const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = dk + 1, ldb = bc + 1;
+    const LocalSmem M = local_smem(L.bc, a.dk);
+    const int dk = a.dk, dv = a.dv, bc = L.bc, ldk = M.ldk, ldb = M.ldb;
     constexpr int ldr = kR3 + 1;
     const int t0 = c * bc, n = min(bc, a.T - t0);
     const size_t tok0 = (size_t)seq * a.T + t0;
     const size_t sd = L.sd;
 
-    float* Qs = sm;                    // [bc][ldk]
-    float* Ks = Qs + bc * ldk;         // [bc][ldk]
-    float* QK = Qs + local_qk_floats(bc, dk);   // [bc][ldb]  q_t . k_s (s <= t), later dC
-    float* Cm = QK + bc * ldb;         // [bc][ldb]  C[t][s]
-    float* Xm = Cm + bc * ldb;         // [bc][ldb]  A = C QK, later C DE
-    float* Wr = Xm + bc * ldb;         // [kR3][ldk] tile of W (chunk start)
-    float* Sr = Wr + kR3 * ldk;        //            tile of S
-    float* dWr = Sr + kR3 * ldk;       //            tile of dWe (chunk end adjoint)
-    float* dSr = dWr + kR3 * ldk;      //            tile of dSe
-    float* dZt = dSr + kR3 * ldk;      // [bc][ldr]
-    float* Et = dZt + bc * ldr;        // [bc][ldr]  e_s, rows of the tile
-    float* dWK = Et + bc * ldr;        // [bc][ldr]  (dWe k_s)_i
-    float* dSK = dWK + bc * ldr;       // [bc][ldr]  (dSe k_s)_i
-    float* de = dSK + bc * ldr;        // [bc][ldr]
-    float* th = de + bc * ldr;
+    float* Qs = sm + M.Qs;             // [bc][ldk]
+    float* Ks = sm + M.Ks;             // [bc][ldk]
+    float* QK = sm + M.QK;             // [bc][ldb]  q_t . k_s (s <= t), later dC
+    float* Cm = sm + M.Cm;             // [bc][ldb]  C[t][s]
+    float* Xm = sm + M.Xm;             // [bc][ldb]  A = C QK, later C DE
+    float* Wr = sm + M.Wr;             // [kR3][ldk] tile of W (chunk start)
+    float* Sr = sm + M.Sr;             //            tile of S
+    float* dWr = sm + M.dWr;           //            tile of dWe (chunk end adjoint)
+    float* dSr = sm + M.dSr;           //            tile of dSe
+    float* dZt = sm + M.dZt;           // [bc][ldr]
+    float* Et = sm + M.Et;             // [bc][ldr]  e_s, rows of the tile
+    float* dWK = sm + M.dWK;           // [bc][ldr]  (dWe k_s)_i
+    float* dSK = sm + M.dSK;           // [bc][ldr]  (dSe k_s)_i
+    float* de = sm + M.de;             // [bc][ldr]
+    float* th = sm + M.vec;
     float* et = th + bc;
     float* al = et + bc;
     float* beta = al + bc;
@@ -465,7 +619,11 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
         const int t = x / bc, s = x % bc;
         float acc = 0.f;
         if (s <= t && t < n)
-            for (int j = 0; j < dk; ++j) acc += Qs[t * ldk + j] * Ks[s * ldk + j];
+            for (int j = 0; j < dk; j += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(Qs + t * ldk + j);
+                const float4 b4 = *reinterpret_cast<const float4*>(Ks + s * ldk + j);
+                acc += a4.x * b4.x + a4.y * b4.y + a4.z * b4.z + a4.w * b4.w;
+            }
         QK[t * ldb + s] = acc;
         Xm[t * ldb + s] = acc * Cm[t * ldb + s];
     }
@@ -499,27 +657,28 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
             dZt[s * ldr + i] = (s < n && i < nr) ? load_in(dz, (tok0 + s) * dv + r0 + i) : 0.f;
         }
         __syncthreads();
-        {   // errors at the chunk start and the end adjoints applied to each key
-            const int i = tid & 15, sg = tid >> 4;
+        {   // errors at the chunk start and the end adjoints applied to each key:
+            // row i = warp (its W, dWe, dSe rows are broadcast reads), keys lane and
+            // lane + 32 (conflict-free rows of k)
+            const int i = tid >> 5, lane = tid & 31;
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int s = sg * 2 + r;
-                if (s >= bc) continue;
+                const int s = lane + 32 * r;
                 float e = 0.f, uw = 0.f, us = 0.f;
-                for (int j = 0; j < dk; ++j) {
-                    const float ks = Ks[s * ldk + j];
-                    e += ks * Wr[i * ldk + j];
-                    uw += ks * dWr[i * ldk + j];
-                    us += ks * dSr[i * ldk + j];
+                for (int j = 0; j < (s < bc ? dk : 0); j += 4) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(Ks + s * ldk + j);
+                    const float4 w4 = *reinterpret_cast<const float4*>(Wr + i * ldk + j);
+                    const float4 g4 = *reinterpret_cast<const float4*>(dWr + i * ldk + j);
+                    const float4 h4 = *reinterpret_cast<const float4*>(dSr + i * ldk + j);
+                    e += k4.x * w4.x + k4.y * w4.y + k4.z * w4.z + k4.w * w4.w;
+                    uw += k4.x * g4.x + k4.y * g4.y + k4.z * g4.z + k4.w * g4.w;
+                    us += k4.x * h4.x + k4.y * h4.y + k4.z * h4.z + k4.w * h4.w;
                 }
-                const bool live = s < n && i < nr;
-                e = live ? e - load_in(v, (tok0 + s) * dv + r0 + i) : 0.f;
-                Et[s * ldr + i] = e;
-                dWK[s * ldr + i] = uw;
-                dSK[s * ldr + i] = us;
-                if (live) {
-                    atomicAdd(&dclast[s], e * uw);
-                    atomicAdd(&dpm[s], e * us);
+                if (s < bc) {
+                    const bool live = s < n && i < nr;
+                    Et[s * ldr + i] = live ? e - load_in(v, (tok0 + s) * dv + r0 + i) : 0.f;
+                    dWK[s * ldr + i] = uw;
+                    dSK[s * ldr + i] = us;
                 }
             }
         }
@@ -545,6 +704,17 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
             }
         }
         __syncthreads();
+        for (int sk = tid; sk < n; sk += kBT3) {   // sum over the tile's rows, per key
+            float pw = 0.f, ps = 0.f;
+#pragma unroll
+            for (int i = 0; i < kR3; ++i) {
+                const float e = Et[sk * ldr + i];
+                pw += e * dWK[sk * ldr + i];
+                ps += e * dSK[sk * ldr + i];
+            }
+            dclast[sk] += pw;
+            dpm[sk] += ps;
+        }
         {   // de_s and dv_s
             const int i = tid & 15, sg = tid >> 4;
             const float* clast = Cm + (n - 1) * ldb;
@@ -626,22 +796,39 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
         const int t = tg * 4 + r;
         if (t >= n) continue;
         float pb = 0.f, pc = 0.f;
+        // the score terms of the four columns, each score read once
+        float sq[4] = {0.f, 0.f, 0.f, 0.f}, sk[4] = {0.f, 0.f, 0.f, 0.f};
+        const int jmax = dk - jg;   // columns jg + 32 bb < dk
+        for (int s2 = 0; s2 <= t; ++s2) {
+            const float x = Xm[t * ldb + s2];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+                if (32 * bb < jmax) sq[bb] += x * Ks[s2 * ldk + jg + 32 * bb];
+        }
+        for (int u = t; u < n; ++u) {
+            const float x = Xm[u * ldb + t];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+                if (32 * bb < jmax) sk[bb] += x * Qs[u * ldk + jg + 32 * bb];
+        }
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
             const int j = jg + 32 * bb;
             if (j >= dk) break;
-            float sq = 0.f, sk = 0.f;
-            for (int s = 0; s <= t; ++s) sq += Xm[t * ldb + s] * Ks[s * ldk + j];
-            for (int u = t; u < n; ++u) sk += Xm[u * ldb + t] * Qs[u * ldk + j];
             const float qv = Qs[t * ldk + j];
             pb += qv * U[r][bb];
             pc += qv * V[r][bb];
             store_out(static_cast<Tin*>(a.dq), (tok0 + t) * dk + j,
-                      beta[t] * U[r][bb] + cc[t] * V[r][bb] - 2.f * sq);
-            store_out(static_cast<Tin*>(a.dk_), (tok0 + t) * dk + j, DK[r][bb] - 2.f * sk);
+                      beta[t] * U[r][bb] + cc[t] * V[r][bb] - 2.f * sq[bb]);
+            store_out(static_cast<Tin*>(a.dk_), (tok0 + t) * dk + j, DK[r][bb] - 2.f * sk[bb]);
         }
-        atomicAdd(&dbeta[t], pb);
-        atomicAdd(&dcc[t], pc);
+        // the warp owns rows 4 tg .. 4 tg + 3: its lanes' partial sums are the whole
+        pb = warp_sum_f(pb);
+        pc = warp_sum_f(pc);
+        if (jg == 0) {
+            dbeta[t] = pb;
+            dcc[t] = pc;
+        }
     }
     __syncthreads();
     // gate gradients: C[t][s] = theta_s w(s,t), pm[s] = theta_s m(s,n-1) with
@@ -650,6 +837,10 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
     float* Wm = Qs;                    // [bc][ldb]  w(s,t) at [t][s]
     float* Mm = Wm + bc * ldb;         // [bc][ldb]  m(s,t) at [t][s]
     const float* dC = QK;
+    float* Kc = Xm;                    // [bc][ldb]  contributions of column s to dkeep[t]
+    float* Ec = Cm;                    // [bc][ldb]  contributions of column s to deta[t]
+    for (int s = tid; s < bc; s += kBT3)
+        for (int t = 0; t < bc; ++t) Kc[t * ldb + s] = Ec[t * ldb + s] = 0.f;
     for (int s = tid; s < n; s += kBT3) {
         float m = 1.f, w = 1.f;
         Wm[s * ldb + s] = 1.f;
@@ -670,12 +861,22 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
         float dw = ths * dC[(n - 1) * ldb + s];            // adjoint of w(s, n-1)
         float dm = ths * (-2.f * dpm[s]);                  // adjoint of m(s, n-1), direct part
         for (int t = n - 1; t > s; --t) {
-            atomicAdd(&dkeep[t], dw * Wm[(t - 1) * ldb + s]);
+            Kc[t * ldb + s] = dw * Wm[(t - 1) * ldb + s];
             dm += dw;                                      // w(s,t) = ... + m(s,t)
-            atomicAdd(&deta[t], dm * Mm[(t - 1) * ldb + s]);
+            Ec[t * ldb + s] = dm * Mm[(t - 1) * ldb + s];
             dm = et[t] * dm;
             dw = (1.f - al[t]) * dw + ths * dC[(t - 1) * ldb + s];
         }
+    }
+    __syncthreads();
+    for (int t = tid; t < n; t += kBT3) {   // sum every column's contribution per token
+        float gk = 0.f, ge = 0.f;
+        for (int s = 0; s < t; ++s) {
+            gk += Kc[t * ldb + s];
+            ge += Ec[t * ldb + s];
+        }
+        dkeep[t] += gk;
+        deta[t] += ge;
     }
     __syncthreads();
     if (tid == 0) {
@@ -707,13 +908,10 @@ __global__ void __launch_bounds__(kBT3, 1) bwd_local_kernel(const BwdArgs a, con
 }
 
 size_t records_smem_floats(int bc, int dk) {
-    return 2 * (size_t)bc * (dk + 1) + (size_t)bc * (bc + 1) + 7 * (size_t)bc;
+    return 2 * (size_t)bc * (dk + 4) + (size_t)bc * (bc + 1) + 7 * (size_t)bc;
 }
 
-size_t chain_smem_floats(int bc, int dk) {
-    return 2 * (size_t)bc * (dk + 1) + (size_t)bc * (bc + 1) + 4 * (size_t)bc * (kR2 + 1) +
-           2 * (size_t)kR2 * (dk + 1) + 4 * (size_t)bc + 1;
-}
+size_t chain_smem_floats(int bc, int dk) { return chain_smem(bc, dk).total; }
 
 template <typename Tin>
 cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, int* launches) {
