@@ -82,16 +82,20 @@ def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
     a = algorithmic(w)
     peaks, src = load_peaks()
     t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = a["flops"] / (peaks["bf16_tflops"] * 1e12)
+    # the CUDA-core kernels compute in fp32: their compute roof is the FMA pipe
+    simt = kernel_name.endswith("_simt")
+    flop_peak = fp32_alu_peak_tflops(2070.0) if simt else peaks["bf16_tflops"]
+    t_tc = a["flops"] / (flop_peak * 1e12)
     if t_hbm >= t_tc:
         achieved = a["bytes"] / kernel_s / 1e9
         r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         achieved = a["flops"] / kernel_s / 1e12
-        r = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+        r = {"bound": "alu" if simt else "tensor", "achieved": achieved, "peak": flop_peak,
              "unit": "TFLOP/s"}
     r["frac"] = r["achieved"] / r["peak"]
-    r["peak_source"] = src
+    r["peak_source"] = ("derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz"
+                        if r["bound"] == "alu" else src)
     r["kernel"] = kernel_name
     r["algorithmic_bytes"] = a["bytes"]
     r["algorithmic_flops"] = a["flops"]
@@ -100,15 +104,17 @@ def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
 
 
 def kernel_source_digest(kernel_name: str) -> str:
-    src = {"linear_simt": "scan_simt.cu", "mlp_simt": "scan_simt.cu",
-           "linear_tc": "scan_linear_tc.cu", "mlp_tc": "scan_mlp_tc.cu",
-           "linear_step": "step.cu"}.get(kernel_name)
+    src = {"linear_simt": ["scan_simt.cu"], "mlp_simt": ["scan_simt.cu", "scan_mlp_simt.cu"],
+           "linear_tc": ["scan_linear_tc.cu"], "mlp_tc": ["scan_mlp_tc.cu"],
+           "linear_step": ["step.cu"]}.get(kernel_name)
     if not src:
         return ""
-    path = os.path.join(ROOT, "test_neural_memory_gb300", "csrc", src)
+    h = hashlib.sha256()
     try:
-        with open(path, "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        for name in src:
+            with open(os.path.join(ROOT, "test_neural_memory_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        return h.hexdigest()[:16]
     except OSError:
         return ""
 

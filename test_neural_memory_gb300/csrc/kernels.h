@@ -110,6 +110,11 @@ bool linear_simt_supported(const LinearArgs& a);
 cudaError_t linear_simt_launch(const LinearArgs& a, cudaStream_t s);
 bool mlp_simt_supported(const MlpArgs& a);
 cudaError_t mlp_simt_launch(const MlpArgs& a, cudaStream_t s);
+// Register-blocked CUDA-core MLP kernel (scan_mlp_simt.cu): d in {16, 32, 64,
+// 128}, hidden a multiple of 4, chunk <= 32, 16-byte aligned state buffers.
+// mlp_simt_launch uses it whenever it applies.
+bool mlp_simt2_supported(const MlpArgs& a);
+cudaError_t mlp_simt2_launch(const MlpArgs& a, cudaStream_t s);
 
 // tcgen05 + TMA kernel for the linear / Titans scan (scan_linear_tc.cu).  It
 // needs linear_tc_workspace_bytes() of workspace for the per-chunk

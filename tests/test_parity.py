@@ -151,6 +151,10 @@ MLP_SHRUNK = [
     dict(B=1, H=2, T=50, d=64, hidden=256, chunk=16),
     dict(B=1, H=1, T=21, d=64, hidden=256, chunk=1),
     dict(B=2, H=1, T=40, d=32, hidden=128, chunk=8),
+    dict(B=1, H=2, T=75, d=128, hidden=64, chunk=32),
+    dict(B=1, H=1, T=19, d=16, hidden=24, chunk=5),
+    # d = 8: the one-token-per-lane kernel
+    dict(B=1, H=1, T=23, d=8, hidden=32, chunk=4),
 ]
 
 
