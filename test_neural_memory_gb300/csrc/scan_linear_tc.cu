@@ -187,6 +187,13 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitCycles) break;
 }
 
+// One arrival for the whole warp, after every lane's prior work (the lanes
+// converge first, which orders their memory and tcgen05 operations).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -254,7 +261,6 @@ __global__ void __launch_bounds__(128) linear_coef_kernel(const LinearArgs a, in
     const int seq = (int)(wid / nch), c = (int)(wid % nch);
     const int T = a.T;
     const int n = min(kChunk, T - c * kChunk);
-    const size_t tok0 = (size_t)seq * T + (size_t)c * kChunk;
     uint8_t* rec = static_cast<uint8_t*>(a.workspace) + (size_t)wid * kRecBytes;
     uint8_t* vec = rec;
 
@@ -365,15 +371,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&B->acc1_ready[b], 1);
-            mbar_init(&B->acc1_free[b], 192);    // error chain 128 + outputs 64
+            mbar_init(&B->acc1_free[b], 6);      // error chain 4 warps + outputs 2
             mbar_init(&B->sc_ready[b], 1);
             mbar_init(&B->mma3_done[b], 1);
-            mbar_init(&B->acc3_free[b], 192);    // error chain 128 + outputs 64
+            mbar_init(&B->acc3_free[b], 6);      // error chain 4 warps + outputs 2
             mbar_init(&B->mma2_done[b], 1);
-            mbar_init(&B->acc2_free[b], 128);    // state warps
+            mbar_init(&B->acc2_free[b], 4);      // state warps
         }
-        mbar_init(&B->am_ready[0], 128);         // weighting warps
-        mbar_init(&B->am_ready[1], 128);
+        mbar_init(&B->am_ready[0], 4);           // weighting warps
+        mbar_init(&B->am_ready[1], 4);
         mbar_init(&B->mma3_issued, 1);           // chain MMA queued (carry MMA goes after it)
         for (int i = 0; i < 4; ++i) mbar_init(&B->drain[i], 1);
         B->abort = 0;
@@ -393,6 +399,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const uint8_t* base = c < 0 ? ktile(h, 0) - kTile : qtile(h, c % kNS);
         return smem_u32(base) + (kk & 3) * 32;
     };
+    // Every MMA sequence below is unrolled so its descriptors are fixed at
+    // compile time: issued from a rolled loop, one MMA left the issuing thread
+    // every ~90 cycles, against ~40-50 (the pipe's own rate) unrolled.
     constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // state MMA, B MN-major
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, 0, 0);   // scores
     constexpr uint32_t id2 = idesc_bf16_f32(128, 32, 1, 1);   // carry: A = K^T, B = [C E | Pm E]
@@ -431,7 +440,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             tc_fence_after();
             const uint32_t wsa = smem_u32(ws);
             if (elect_one()) {
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < KS; ++kk)
                     mma_bf16(tmem + kAcc1 + (x & 1) * 32, sdesc(qk_a(x, kk), 16, 1024, 2),
                              sdesc(wsa + kk * 2048, 8192, 1024, 2), id1, kk > 0);
@@ -467,7 +476,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const float4 sc = *reinterpret_cast<const float4*>(vec(st) + kVScal);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&B->acc2_free[b]);
+                warp_arrive(&B->acc2_free[b]);
                 // the carry MMA (the last reader of K_c) is complete and the
                 // scalars are in registers: this role is done with the stage
                 if (tid == 0) mbar_arrive(&B->empty[st]);
@@ -503,7 +512,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // ---------------------------------------------------------- outputs
         const int t = tid - 128;                 // token = TMEM lane 0..63
         bool ok = true;
-        mbar_arrive(&B->acc1_free[1]);           // the chunk -1 state product has no reads
+        warp_arrive(&B->acc1_free[1]);           // the chunk -1 state product has no reads
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1, st = c % kNS;
             if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
@@ -519,8 +528,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const int n = (int)vecf(st, kVScal)[3];
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&B->acc1_free[b]);
-                mbar_arrive(&B->acc3_free[b]);
+                warp_arrive(&B->acc1_free[b]);
+                warp_arrive(&B->acc3_free[b]);
                 if (t < n && a.z) {
                     float zz[16];
 #pragma unroll
@@ -565,9 +574,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 unpack8(reinterpret_cast<const uint4*>(vtile(st) + t * 32)[h], v);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&B->acc1_free[pb]);
+                warp_arrive(&B->acc1_free[pb]);
                 if (x >= 1) {
-                    mbar_arrive(&B->acc3_free[pb]);
+                    warp_arrive(&B->acc3_free[pb]);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) e[i] = bn * f[i] + cn * g[i] - 2.f * m[i] - v[i];
                 } else {
@@ -607,7 +616,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     tc_fence_after();
                     const uint32_t et = smem_u32(ete);
                     if (elect_one()) {
-#pragma unroll 1
+#pragma unroll
                         for (int kk = 0; kk < kChunk / 16; ++kk)
                             mma_tmem_a(tmem + kAcc3 + b * 16, tmem + kAM + b * 32 + kk * 8,
                                        sdesc(et + kk * 2048, 8192, 1024, 2), id3, kk > 0);
@@ -623,7 +632,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     tc_fence_after();
                     const uint32_t ecp = smem_u32(etcp(b)), kb = smem_u32(ktile(0, st));
                     if (elect_one()) {
-#pragma unroll 1
+#pragma unroll
                         for (int kk = 0; kk < kChunk / 16; ++kk)
                             mma_bf16(tmem + kAcc2 + b * 32,
                                      sdesc(kb + kk * 2048, D == 128 ? kRingBytes : kTile, 1024, 2),
@@ -650,7 +659,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 if (ok) {
                     tc_fence_after();
                     if (elect_one()) {
-#pragma unroll 1
+#pragma unroll
                         for (int kk = 0; kk < KS; ++kk)
                             mma_bf16(tmem + kAccS + b * 64, sdesc(qk_a(c, kk), 16, 1024, 2),
                                      sdesc(smem_u32(ktile(kk >> 2, st)) + (kk & 3) * 32, 16, 1024, 2),
@@ -690,7 +699,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&B->am_ready[b]);
+                warp_arrive(&B->am_ready[b]);
             }
             named_bar_sync(4, 128);
         }
