@@ -115,6 +115,11 @@ cudaError_t mlp_simt_launch(const MlpArgs& a, cudaStream_t s);
 // mlp_simt_launch uses it whenever it applies.
 bool mlp_simt2_supported(const MlpArgs& a);
 cudaError_t mlp_simt2_launch(const MlpArgs& a, cudaStream_t s);
+// Two-CTA cluster variant (scan_mlp_cluster.cu): each CTA keeps half of the
+// state in shared memory.  (d, hidden) in {(32, 128), (64, 256), (128, 128)},
+// chunk <= 16.  mlp_simt_launch prefers it whenever it applies.
+bool mlp_cluster_supported(const MlpArgs& a);
+cudaError_t mlp_cluster_launch(const MlpArgs& a, cudaStream_t s);
 
 // tcgen05 + TMA kernel for the linear / Titans scan (scan_linear_tc.cu).  It
 // needs linear_tc_workspace_bytes() of workspace for the per-chunk

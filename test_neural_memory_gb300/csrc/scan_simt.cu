@@ -432,12 +432,13 @@ cudaError_t linear_simt_launch(const LinearArgs& a, cudaStream_t s) {
 }
 
 bool mlp_simt_supported(const MlpArgs& a) {
-    if (mlp_simt2_supported(a)) return true;
+    if (mlp_cluster_supported(a) || mlp_simt2_supported(a)) return true;
     const int nb = mlp_block_tokens(a.d, a.hidden);
     return nb >= 1 && a.chunk <= nb;
 }
 
 cudaError_t mlp_simt_launch(const MlpArgs& a, cudaStream_t s) {
+    if (mlp_cluster_supported(a)) return mlp_cluster_launch(a, s);
     if (mlp_simt2_supported(a)) return mlp_simt2_launch(a, s);
     const int nb = mlp_block_tokens(a.d, a.hidden);
     const size_t smem = mlp_smem_floats(a.d, a.hidden, nb) * sizeof(float);

@@ -153,6 +153,8 @@ MLP_SHRUNK = [
     dict(B=2, H=1, T=40, d=32, hidden=128, chunk=8),
     dict(B=1, H=2, T=75, d=128, hidden=64, chunk=32),
     dict(B=1, H=1, T=19, d=16, hidden=24, chunk=5),
+    # two-CTA cluster kernel: d = 128, hidden = 128, ragged last chunk
+    dict(B=1, H=2, T=45, d=128, hidden=128, chunk=12),
     # d = 8: the one-token-per-lane kernel
     dict(B=1, H=1, T=23, d=8, hidden=32, chunk=4),
 ]
