@@ -795,9 +795,17 @@ def run_ours(args, rank, world, dev):
     return line
 
 
+E2E_SEGMENT = 8192   # tokens per segment of the host-buffer scan
+
+
 def run_e2e(args, w, inp, dev, stream, world):
     """Same metric through the public API with pinned host inputs: every step
-    copies its inputs host->device and reads the outputs back."""
+    copies its inputs host->device and reads the outputs back.  The linear /
+    Titans scan uses its host-buffer entry point (ttm_titans_fwd_host), which
+    overlaps the copies of one segment with the scan of the next; the 2-layer
+    memory copies everything in, scans, and copies everything out."""
+    if w.kind != "mlp":
+        return run_e2e_host(args, w, inp, dev, stream, world)
     host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
     dbuf = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in inp.items()}
     outs = alloc_outputs(w, dev)
@@ -831,6 +839,45 @@ def run_e2e(args, w, inp, dev, stream, world):
     return {"value": w.tokens * world * n / (ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": ms / n}
+
+
+def run_e2e_host(args, w, inp, dev, stream, world):
+    import test_neural_memory_gb300 as ttm
+    h = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
+    outs = alloc_outputs(w, "cpu", pin=True)
+    seg = min(E2E_SEGMENT, (w.T + w.chunk - 1) // w.chunk * w.chunk)
+    seg = max(w.chunk, seg // w.chunk * w.chunk)
+    need = ttm.titans_fwd_host_workspace_size(w.B, w.H, w.T, w.d, w.d, w.chunk,
+                                              ttm.BF16 if w.dtype == "bf16" else ttm.F32, seg)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    titans = w.kind == "titans"
+
+    def one():
+        ttm.titans_fwd_host(h["q"], h["k"], h["v"], h["theta"], h["W0"], w.chunk,
+                            eta=h["eta"] if titans else None, alpha=h["alpha"] if titans else None,
+                            w0_shared=w.w0_shared, z=outs["z"], W_out=outs["W"],
+                            S_out=outs["S"] if titans else None, want_S=titans,
+                            seg_tokens=seg, workspace=ws, device=dev, stream=stream)
+
+    h2d = sum(v.numel() * v.element_size() for k, v in h.items()
+              if v is not None and (titans or k not in ("eta", "alpha")))
+    d2h = sum(v.numel() * v.element_size() for k, v in outs.items()
+              if v is not None and k != "ws")
+    for _ in range(max(1, min(args.warmup, 3))):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = args.e2e_steps
+    a.record(stream)
+    for _ in range(n):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": w.tokens * world * n / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": ms / n, "api": f"ttm_titans_fwd_host, {seg}-token segments"}
 
 
 # ----------------------------------------------------------------------------

@@ -148,6 +148,40 @@ int ttm_titans_fwd_chunk_gates(int B, int H, int T, int dk, int dv, int chunk, i
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The Titans / linear scan with every tensor in HOST memory: the sequence is
+ * streamed through the device in segments of `seg_tokens` tokens (a positive
+ * multiple of `chunk`).  While segment i is scanned on `stream`, an internal
+ * stream copies segment i + 1's q, k, v and gates in and another copies
+ * segment i - 1's z out.  The state crosses segment boundaries in fp32 on the
+ * device; a boundary falls between two chunks, where the chunk form restarts
+ * from whatever state the previous chunk left ("TTT layers 与 fast weights" eq
+ * (6): every gradient of a chunk is taken at the chunk-start state), so the
+ * result is that of ttm_titans_fwd up to rounding order.
+ *   q, k, v, eta, theta, alpha, W0, S0: host, layouts as ttm_titans_fwd (page-
+ *     locked memory gives full copy bandwidth; pageable memory works, slower).
+ *   z, W_out, S_out: host, written asynchronously: synchronise `stream` before
+ *     reading them.  S_out may be NULL.
+ *   workspace: device memory, 256-byte aligned, at least
+ *     ttm_titans_fwd_host_workspace_size(...) bytes (two segments of inputs and
+ *     outputs, four state buffers and the scan's own workspace); the caller
+ *     owns it and must not touch it until `stream` has passed the call.
+ * `stream` (the caller's) runs the scans; on return it has been made to wait
+ * for every copy of the call.  The internal streams and events are created
+ * once per device on first use and reused; calls are serialised on the host.
+ * Errors: TTM_ERR_INVALID_ARG for malformed arguments or a short workspace
+ * (nothing enqueued), anything ttm_titans_fwd returns for a segment, and
+ * TTM_ERR_CUDA for a failed copy or event operation.
+ */
+size_t ttm_titans_fwd_host_workspace_size(int B, int H, int T, int dk, int dv, int chunk,
+                                          int dtype, int seg_tokens);
+int ttm_titans_fwd_host(int B, int H, int T, int dk, int dv, int chunk, int dtype,
+                        const void* q, const void* k, const void* v,
+                        const float* eta, const float* theta, const float* alpha,
+                        const float* W0, const float* S0, int w0_shared_over_batch,
+                        void* z, float* W_out, float* S_out, int seg_tokens,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Deep memory: f(x) = W2 GELU(W1 x), hidden units `hidden`, analytic inner
  * gradients e = 2 (y - v), dW2 = e a^T, dW1 = ((W2^T e) * GELU'(h)) k^T
  * ("论文速览 | Titans" §3.9 with L_M = 2; "Continual Learning: From Attention

@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
         L.ttm_lmm_layer_fwd.argtypes = ([i] * 6 + [p] * 5 + [ctypes.c_float, p, i, p, p, p, p, sz,
                                                               p])
         L.ttm_titans_fwd_chunk_gates.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, p, sz, p]
+        L.ttm_titans_fwd_host_workspace_size.argtypes = [i] * 8
+        L.ttm_titans_fwd_host_workspace_size.restype = sz
+        L.ttm_titans_fwd_host.argtypes = [i] * 7 + [p] * 6 + [p, p, i, p, p, p, i, p, sz, p]
         L.ttm_dgd_step.argtypes = [i] * 8 + [p] * 5 + [p, p, p, p]
         L.ttm_titans_bwd_workspace_size.argtypes = [i] * 8
         L.ttm_titans_bwd_workspace_size.restype = sz
@@ -196,6 +199,45 @@ def titans_fwd(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None, w0_s
                                 _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha), _ptr(W0), _ptr(S0),
                                 int(bool(w0_shared)), _ptr(z), _ptr(W_out), _ptr(S_out), wp, wb,
                                 _stream(q, stream)), "ttm_titans_fwd")
+    return z, W_out, S_out
+
+
+def titans_fwd_host_workspace_size(B, H, T, dk, dv, chunk, dtype, seg_tokens) -> int:
+    """Device bytes ttm_titans_fwd_host needs (0 for rejected arguments)."""
+    code = BF16 if dtype in ("bf16", BF16) else F32
+    return int(lib().ttm_titans_fwd_host_workspace_size(B, H, T, dk, dv, int(chunk), code,
+                                                        int(seg_tokens)))
+
+
+def titans_fwd_host(q, k, v, theta, W0, chunk, *, eta=None, alpha=None, S0=None,
+                    w0_shared=False, z=None, W_out=None, S_out=None, want_S=True,
+                    seg_tokens=8192, workspace=None, device=None, stream=None):
+    """ttm_titans_fwd_host: q, k, v, gates, W0, S0 and the outputs are CPU tensors
+    (page-locked for full copy bandwidth); the sequence is streamed through
+    `device` in segments of `seg_tokens` tokens.  The outputs are complete once
+    `stream` (default: the device's current stream) has been synchronised.
+    Returns (z, W_out, S_out)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    pin = lambda shape, dt: torch.empty(shape, dtype=dt, pin_memory=True)
+    z = pin(v.shape, v.dtype) if z is None else z
+    shape = (B, H, dv, dk)
+    W_out = pin(shape, torch.float32) if W_out is None else W_out
+    if S_out is None and want_S:
+        S_out = pin(shape, torch.float32)
+    need = titans_fwd_host_workspace_size(B, H, T, dk, dv, chunk, _dtype_code(q), seg_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    _check(lib().ttm_titans_fwd_host(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q),
+                                     _ptr(k), _ptr(v), _ptr(eta), _ptr(theta), _ptr(alpha),
+                                     _ptr(W0), _ptr(S0), int(bool(w0_shared)), _ptr(z),
+                                     _ptr(W_out), _ptr(S_out), int(seg_tokens),
+                                     ctypes.c_void_p(workspace.data_ptr()),
+                                     workspace.numel() * workspace.element_size(),
+                                     ctypes.c_void_p(s.cuda_stream)), "ttm_titans_fwd_host")
     return z, W_out, S_out
 
 
