@@ -291,6 +291,139 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
     }
 }
 
+// Several tokens per call when the 8 warps of a block share one sequence
+// (dv a multiple of 8): the block stages each group of G tokens' keys and
+// queries once for all its rows, into one of two buffers, while it processes
+// the previous group from the other; lanes 0..G-1 of every warp load the
+// group's per-token scalars for that warp's row into registers one group
+// ahead.  One block barrier per group both publishes the group's copies and
+// frees the other buffer.
+template <typename TIn>
+__device__ __forceinline__ void stage_block(TIn* ks, int G, const TIn* k, const TIn* q,
+                                            size_t first, int len, int dk) {
+    const int nvec = (int)((size_t)len * dk * sizeof(TIn) / 16);
+    const char* kg = reinterpret_cast<const char*>(k + first * dk);
+    const char* qg = reinterpret_cast<const char*>(q + first * dk);
+    char* kd = reinterpret_cast<char*>(ks);
+    char* qd = kd + (size_t)G * dk * sizeof(TIn);
+    for (int i = threadIdx.x; i < nvec; i += kStepThreads) {
+        cp_async16(kd + 16 * i, kg + 16 * i);
+        cp_async16(qd + 16 * i, qg + 16 * i);
+    }
+}
+
+template <typename TIn, int NJ, int kMode>
+__global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
+    linear_step_block(const StepArgs a, int G) {
+    extern __shared__ __align__(16) unsigned char step_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * (kStepThreads / 32) + warp;
+    const int r = (int)(gw % a.dv);         // every warp of the block is a row of `seq`
+    const long long seq = gw / a.dv;
+    const int dk = a.dk, n = a.n;
+    const size_t row = ((size_t)seq * a.dv + r) * dk;
+    const TIn* q = static_cast<const TIn*>(a.q);
+    const TIn* k = static_cast<const TIn*>(a.k);
+    const TIn* v = static_cast<const TIn*>(a.v);
+    TIn* z = static_cast<TIn*>(a.z);
+    TIn* const buf0 = reinterpret_cast<TIn*>(step_smem);
+    TIn* const buf1 = buf0 + (size_t)2 * G * dk;
+
+    stage_block<TIn>(buf0, G, k, q, (size_t)seq * n, min(G, n), dk);
+    auto scalars = [&](int t0, int len, float& vr, float& th, float& et, float& keep) {
+        vr = 0.f; th = 0.f; et = 0.f; keep = 1.f;
+        if (lane < len) {
+            const size_t tok = (size_t)seq * n + t0 + lane;
+            vr = ld_in<TIn>(v + tok * a.dv + r);
+            th = __ldg(a.theta + tok);
+            et = a.eta ? __ldg(a.eta + tok) : 0.f;
+            const float al = a.alpha ? __ldg(a.alpha + tok) : 0.f;
+            keep = kMode == 0 ? 1.f - al : al;
+        }
+    };
+    float vr, th, et, keep;
+    scalars(0, min(G, n), vr, th, et, keep);
+    const float* w0 = initial_row(a, seq, r);
+    float w[NJ], s[NJ], wc[NJ];
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        const bool in = j < dk;
+        w[i] = in ? w0[j] : 0.f;
+        s[i] = (in && a.S) ? a.S[row + j] : 0.f;
+        wc[i] = (in && a.pos != 0) ? a.Wc[row + j] : 0.f;
+    }
+    int p = a.pos;
+    bool wc_changed = false;
+    for (int t0 = 0; t0 < n; t0 += G) {
+        const int len = min(G, n - t0);
+        const bool odd = ((t0 / G) & 1) != 0;
+        const TIn* ks = odd ? buf1 : buf0;
+        const TIn* qs = ks + (size_t)G * dk;
+        cp_async_wait_all();   // this thread's copies of the group
+        __syncthreads();       // everyone's; and every warp is done with the other buffer
+        float vn = 0.f, thn = 0.f, etn = 0.f, keepn = 1.f;
+        if (t0 + G < n) {
+            const int ln = min(G, n - t0 - G);
+            stage_block<TIn>(odd ? buf0 : buf1, G, k, q, (size_t)seq * n + t0 + G, ln, dk);
+            scalars(t0 + G, ln, vn, thn, etn, keepn);
+        }
+        for (int u = 0; u < len; ++u) {
+            if (p == 0) {   // this token opens a chunk: its gradient point is now
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) wc[i] = w[i];
+                wc_changed = true;
+            }
+            float kv[NJ], qv[NJ];
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) {
+                const int j = lane + 32 * i;
+                kv[i] = j < dk ? to_f<TIn>(ks[u * dk + j]) : 0.f;
+                qv[i] = j < dk ? to_f<TIn>(qs[u * dk + j]) : 0.f;
+            }
+            float acc = 0.f;
+            float zq = 0.f;
+            if constexpr (kMode == 0) {
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+                const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
+                const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
+                const float etu = __shfl_sync(0xffffffffu, et, u);
+                const float keepu = __shfl_sync(0xffffffffu, keep, u);
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) {
+                    s[i] = fmaf(etu, s[i], -ge * kv[i]);
+                    w[i] = fmaf(keepu, w[i], s[i]);
+                    zq = fmaf(w[i], qv[i], zq);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+                const float g = __shfl_sync(0xffffffffu, th, u) *
+                                (warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u));
+                const float alu = __shfl_sync(0xffffffffu, keep, u);
+#pragma unroll
+                for (int i = 0; i < NJ; ++i) {
+                    w[i] = fmaf(alu, w[i], -g * kv[i]);
+                    zq = fmaf(w[i], qv[i], zq);
+                }
+            }
+            zq = warp_sum(zq);
+            if (lane == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
+            p = p + 1 == a.chunk ? 0 : p + 1;
+        }
+        vr = vn; th = thn; et = etn; keep = keepn;
+    }
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        if (j >= dk) continue;
+        a.W[row + j] = w[i];
+        if (a.S) a.S[row + j] = s[i];
+        if (wc_changed && a.Wc) a.Wc[row + j] = wc[i];
+    }
+}
+
 // Tokens per staged group: the keys and queries of a group take at most
 // 4 KB per warp (32 KB per block), and a group never exceeds 32 tokens (one
 // per lane for the per-token scalars).
@@ -308,6 +441,15 @@ template <typename TIn, int NJ, int kMode>
 void launch_mode(const StepArgs& a, unsigned blocks, cudaStream_t s) {
     if (a.n == 1) {
         linear_step_direct<TIn, NJ, kMode><<<blocks, kStepThreads, 0, s>>>(a);
+    } else if (a.dv % (kStepThreads / 32) == 0) {
+        // whole blocks of one sequence: block-shared staging, groups of up to
+        // 32 tokens within 8 KB per buffer
+        const int per_token = 2 * a.dk * (int)sizeof(TIn);
+        int G = 8192 / per_token;
+        G = G < 1 ? 1 : (G > 32 ? 32 : G);
+        if (G > a.n) G = a.n;
+        const size_t smem = (size_t)4 * G * a.dk * sizeof(TIn);
+        linear_step_block<TIn, NJ, kMode><<<blocks, kStepThreads, smem, s>>>(a, G);
     } else {
         const int G = group_of(a);
         const size_t smem = (size_t)(kStepThreads / 32) * 2 * G * a.dk * sizeof(TIn);
