@@ -159,6 +159,118 @@ __global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2) lmm_prep_kerne
     }
 }
 
+// NJ consecutive bf16 values at p (NJ-aligned), one store.
+template <int NJ>
+__device__ __forceinline__ void store_nj(__nv_bfloat16* p, const float* x) {
+    if constexpr (NJ == 1) {
+        p[0] = __float2bfloat16_rn(x[0]);
+    } else if constexpr (NJ == 2) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x[0], x[1]);
+    } else {
+        uint32_t w[NJ / 2];
+#pragma unroll
+        for (int e = 0; e < NJ / 2; ++e) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        if constexpr (NJ == 4) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        else *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+constexpr int kPrepWarps = kLayerThreads / 32;   // tiles per block
+
+// Same arithmetic as lmm_prep_kernel with a layout built for wide accesses:
+// a block owns one (b, stream, head) and kPrepWarps consecutive tiles of kTile
+// tokens; the head's conv taps are staged once per block in shared memory,
+// transposed to [window slot][channel]; lane l holds the NJ consecutive
+// channels l NJ ... of the head, so each input row and each output row is one
+// vector access per lane (kVec: the projection's row length keeps NJ-element
+// alignment, else element-wise loads).
+template <int NJ, int NW, bool kVec>
+__global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2)
+    lmm_prep2_kernel(const LmmArgs a, const __nv_bfloat16* proj, __nv_bfloat16* qkv,
+                     float* gates) {
+    __shared__ __align__(16) float taps[NW][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, d = a.d, T = a.T, K = a.conv_k;
+    const int ntile = (T + kTile - 1) / kTile;
+    const int ngroup = (ntile + kPrepWarps - 1) / kPrepWarps;
+    long long bid = blockIdx.x;
+    const int grp = (int)(bid % ngroup);
+    bid /= ngroup;
+    const int h = (int)(bid % H);
+    bid /= H;
+    const int s = (int)(bid % 3);
+    const int b = (int)(bid / 3);
+    const int D = H * d, P = 4 * D + 3 * H;
+    const int c0 = s * D + h * d;                     // first channel of the head
+    // window slot j of token t0 + i is row i + j; its weight is tap j - (NW - K)
+    for (int x = threadIdx.x; x < NW * d; x += kLayerThreads) {
+        const int j = x / d, c = x % d;
+        const int tap = j - (NW - K);
+        taps[j][c] = tap >= 0 ? a.conv_w[(size_t)(c0 + c) * K + tap] : 0.f;
+    }
+    __syncthreads();
+    const int tile = grp * kPrepWarps + warp;
+    if (tile >= ntile) return;
+    const int t0 = tile * kTile, t1 = min(T, t0 + kTile);
+    const int cl = lane * NJ;                         // this lane's first channel
+    float wwin[NW][NJ];
+#pragma unroll
+    for (int j = 0; j < NW; ++j)
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) wwin[j][i] = taps[j][cl + i];
+    constexpr int kRowsT = kTile + NW - 1;
+    float xr[kRowsT][NJ];
+#pragma unroll
+    for (int r = 0; r < kRowsT; ++r) {
+        const int ts = t0 - (NW - 1) + r;
+        const bool live = ts >= 0 && ts < t1 && r >= NW - K;
+        if (live) {
+            load_vw<NJ, kVec>(proj + ((size_t)b * T + ts) * P + c0 + cl, xr[r]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) xr[r][i] = 0.f;
+        }
+    }
+    const size_t plane = (size_t)a.B * H * T;
+    if (s == 0) {   // lanes 0..kTile-1: the three gates of token t0 + lane of head h
+        const int t = t0 + lane;
+        if (lane < kTile && t < t1) {
+            const __nv_bfloat16* lg = proj + ((size_t)b * T + t) * P + 4 * D + h;
+            const size_t gi = ((size_t)b * H + h) * T + t;
+            gates[gi] = a.theta_scale * sigm(__bfloat162float(lg[0]));
+            gates[plane + gi] = sigm(__bfloat162float(lg[H]));
+            gates[2 * plane + gi] = sigm(__bfloat162float(lg[2 * H]));
+        }
+    }
+    const size_t stream_stride = (size_t)a.B * H * T * d;
+#pragma unroll
+    for (int tt = 0; tt < kTile; ++tt) {
+        const int t = t0 + tt;
+        if (t >= t1) break;
+        float u[NJ];
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < NW; ++j) acc = fmaf(wwin[j][i], xr[tt + j][i], acc);
+            // SiLU; the fast intrinsics' error is far below the bf16 rounding of the output
+            u[i] = __fdividef(acc, 1.f + __expf(-acc));
+        }
+        if (s < 2) {   // l2-normalise q and k per head
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) ss += u[i] * u[i];
+            const float inv = 1.f / fmaxf(sqrtf(lwarp_sum(ss)), 1e-6f);
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) u[i] *= inv;
+        }
+        store_nj<NJ>(qkv + s * stream_stride + (((size_t)b * H + h) * T + t) * d + cl, u);
+    }
+}
+
 // One warp per (b, t, h): o = z / sqrt(mean(z^2) + eps) * rms_w * g; lane l
 // holds channels l VW ... of the head.
 template <int VW, bool kVec>
@@ -209,10 +321,19 @@ bool lmm_supported(const LmmArgs& a) {
 }
 
 template <int NJ>
-void prep_nj(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloat16* p,
-             __nv_bfloat16* q, float* g) {
-    if (a.conv_k <= 4) lmm_prep_kernel<NJ, 4><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
-    else lmm_prep_kernel<NJ, 8><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+void prep_nj(const LmmArgs& a, unsigned /*warp-grid blocks*/, cudaStream_t s,
+             const __nv_bfloat16* p, __nv_bfloat16* q, float* g) {
+    const long long ntile = (a.T + kTile - 1) / kTile;
+    const unsigned blocks =
+        (unsigned)((long long)a.B * 3 * a.H * ((ntile + kPrepWarps - 1) / kPrepWarps));
+    const bool vec = (4 * a.H * a.d + 3 * a.H) % NJ == 0;
+    if (a.conv_k <= 4) {
+        if (vec) lmm_prep2_kernel<NJ, 4, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        else lmm_prep2_kernel<NJ, 4, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+    } else {
+        if (vec) lmm_prep2_kernel<NJ, 8, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        else lmm_prep2_kernel<NJ, 8, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+    }
 }
 
 template <int VW>
