@@ -12,8 +12,9 @@
 //   post: o = RMSNorm_head(z) * rms_w * g, [B][T][D] in bf16
 //   y = x + o W_o                   one bf16 GEMM (cuBLAS), residual as beta = 1
 //
-// The prep and post kernels are HBM-bound elementwise / per-head reductions:
-// one warp per (token, head, stream), lanes over the head's d channels.
+// The prep and post kernels are HBM-bound elementwise / per-head reductions
+// with a warp per (tile of tokens, head, stream) or (token, head), lanes over
+// the head's d channels.
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -69,96 +70,6 @@ __device__ __forceinline__ void store_vw(__nv_bfloat16* p, const float* x) {
 
 constexpr int kTile = 4;    // tokens per prep warp
 
-// One warp per (b, h, s, tile of kTile tokens), s = 0, 1, 2 for q, k, v.  Lane
-// l holds channels l, l + 32, ... (NJ = d / 32) of the head, so that each load
-// of the conv taps (a channel's taps are contiguous) and each row load is
-// contiguous across the warp.  The taps stay in registers for the tile, and
-// every input row of the tile (kTile + NW - 1 of them, NW >= the conv width) is
-// loaded before any is used.
-template <int NJ, int NW>
-__global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2) lmm_prep_kernel(const LmmArgs a,
-                                                                 const __nv_bfloat16* proj,
-                                                                 __nv_bfloat16* qkv,
-                                                                 float* gates) {
-    const long long gw = ((long long)blockIdx.x * kLayerThreads + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int H = a.H, d = a.d, T = a.T, K = a.conv_k;
-    const int ntile = (T + kTile - 1) / kTile;
-    if (gw >= (long long)a.B * H * 3 * ntile) return;
-    const int s = (int)(gw % 3);
-    long long rest = gw / 3;
-    const int h = (int)(rest % H);
-    rest /= H;
-    const int tile = (int)(rest % ntile);
-    const int b = (int)(rest / ntile);
-    const int D = H * d, P = 4 * D + 3 * H;
-    const int c0 = s * D + h * d;                     // first channel of the head
-    const int t0 = tile * kTile, t1 = min(T, t0 + kTile);
-    // window slot j of token t0 + i is row i + j; its weight is tap j - (NW - K)
-    float wwin[NW][NJ];
-#pragma unroll
-    for (int i = 0; i < NJ; ++i) {
-        const float* w = a.conv_w + ((size_t)c0 + lane + 32 * i) * K;
-        if (K == 4 && NW == 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(w);
-            wwin[0][i] = w4.x; wwin[1][i] = w4.y; wwin[2][i] = w4.z; wwin[3][i] = w4.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < NW; ++j) {
-                const int tap = j - (NW - K);
-                wwin[j][i] = tap >= 0 ? w[tap] : 0.f;
-            }
-        }
-    }
-    constexpr int kRowsT = kTile + NW - 1;
-    float xr[kRowsT][NJ];
-#pragma unroll
-    for (int r = 0; r < kRowsT; ++r) {
-        const int ts = t0 - (NW - 1) + r;
-        const bool live = ts >= 0 && ts < t1 && r >= NW - K;
-        const __nv_bfloat16* src = proj + ((size_t)b * T + (live ? ts : 0)) * P + c0 + lane;
-#pragma unroll
-        for (int i = 0; i < NJ; ++i) xr[r][i] = live ? __bfloat162float(src[32 * i]) : 0.f;
-    }
-    const size_t plane = (size_t)a.B * H * T;
-    if (s == 0) {   // lanes 0..kTile-1: the three gates of token t0 + lane of head h
-        const int t = t0 + lane;
-        if (lane < kTile && t < t1) {
-            const __nv_bfloat16* lg = proj + ((size_t)b * T + t) * P + 4 * D + h;
-            const size_t gi = ((size_t)b * H + h) * T + t;
-            gates[gi] = a.theta_scale * sigm(__bfloat162float(lg[0]));
-            gates[plane + gi] = sigm(__bfloat162float(lg[H]));
-            gates[2 * plane + gi] = sigm(__bfloat162float(lg[2 * H]));
-        }
-    }
-    const size_t stream_stride = (size_t)a.B * H * T * d;
-#pragma unroll
-    for (int tt = 0; tt < kTile; ++tt) {
-        const int t = t0 + tt;
-        if (t >= t1) break;
-        float u[NJ];
-#pragma unroll
-        for (int i = 0; i < NJ; ++i) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < NW; ++j) acc = fmaf(wwin[j][i], xr[tt + j][i], acc);
-            // SiLU; the fast intrinsics' error is far below the bf16 rounding of the output
-            u[i] = __fdividef(acc, 1.f + __expf(-acc));
-        }
-        if (s < 2) {   // l2-normalise q and k per head
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) ss += u[i] * u[i];
-            const float inv = 1.f / fmaxf(sqrtf(lwarp_sum(ss)), 1e-6f);
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) u[i] *= inv;
-        }
-        __nv_bfloat16* dst = qkv + s * stream_stride + (((size_t)b * H + h) * T + t) * d + lane;
-#pragma unroll
-        for (int i = 0; i < NJ; ++i) dst[32 * i] = __float2bfloat16_rn(u[i]);
-    }
-}
-
 // NJ consecutive bf16 values at p (NJ-aligned), one store.
 template <int NJ>
 __device__ __forceinline__ void store_nj(__nv_bfloat16* p, const float* x) {
@@ -180,8 +91,7 @@ __device__ __forceinline__ void store_nj(__nv_bfloat16* p, const float* x) {
 
 constexpr int kPrepWarps = kLayerThreads / 32;   // tiles per block
 
-// Same arithmetic as lmm_prep_kernel with a layout built for wide accesses:
-// a block owns one (b, stream, head) and kPrepWarps consecutive tiles of kTile
+// A block owns one (b, stream, head) and kPrepWarps consecutive tiles of kTile
 // tokens; the head's conv taps are staged once per block in shared memory,
 // transposed to [window slot][channel]; lane l holds the NJ consecutive
 // channels l NJ ... of the head, so each input row and each output row is one
@@ -189,7 +99,7 @@ constexpr int kPrepWarps = kLayerThreads / 32;   // tiles per block
 // alignment, else element-wise loads).
 template <int NJ, int NW, bool kVec>
 __global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2)
-    lmm_prep2_kernel(const LmmArgs a, const __nv_bfloat16* proj, __nv_bfloat16* qkv,
+    lmm_prep_kernel(const LmmArgs a, const __nv_bfloat16* proj, __nv_bfloat16* qkv,
                      float* gates) {
     __shared__ __align__(16) float taps[NW][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -321,18 +231,15 @@ bool lmm_supported(const LmmArgs& a) {
 }
 
 template <int NJ>
-void prep_nj(const LmmArgs& a, unsigned /*warp-grid blocks*/, cudaStream_t s,
-             const __nv_bfloat16* p, __nv_bfloat16* q, float* g) {
-    const long long ntile = (a.T + kTile - 1) / kTile;
-    const unsigned blocks =
-        (unsigned)((long long)a.B * 3 * a.H * ((ntile + kPrepWarps - 1) / kPrepWarps));
+void prep_nj(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloat16* p,
+             __nv_bfloat16* q, float* g) {
     const bool vec = (4 * a.H * a.d + 3 * a.H) % NJ == 0;
     if (a.conv_k <= 4) {
-        if (vec) lmm_prep2_kernel<NJ, 4, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
-        else lmm_prep2_kernel<NJ, 4, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        if (vec) lmm_prep_kernel<NJ, 4, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        else lmm_prep_kernel<NJ, 4, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
     } else {
-        if (vec) lmm_prep2_kernel<NJ, 8, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
-        else lmm_prep2_kernel<NJ, 8, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        if (vec) lmm_prep_kernel<NJ, 8, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
+        else lmm_prep_kernel<NJ, 8, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, g);
     }
 }
 
@@ -346,8 +253,10 @@ void post_vw(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloa
 
 cudaError_t lmm_prep_launch(const LmmArgs& a, const void* proj, void* qkv, float* gates,
                             cudaStream_t s) {
-    const long long warps = (long long)a.B * a.H * 3 * ((a.T + kTile - 1) / kTile);
-    const unsigned blocks = (unsigned)((warps * 32 + kLayerThreads - 1) / kLayerThreads);
+    // one block per (b, stream, head, kPrepWarps tiles)
+    const long long ntile = (a.T + kTile - 1) / kTile;
+    const unsigned blocks =
+        (unsigned)((long long)a.B * 3 * a.H * ((ntile + kPrepWarps - 1) / kPrepWarps));
     auto p = static_cast<const __nv_bfloat16*>(proj);
     auto q = static_cast<__nv_bfloat16*>(qkv);
     switch (a.d / 32) {
