@@ -424,6 +424,183 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
     }
 }
 
+// Several tokens per call, four rows per warp: lanes 8g ... 8g + 7 hold row
+// 4 (warp) + g of the block's rows, lane 8g + c its DK/8 consecutive columns
+// c DK/8 ..., so a row's two dot products per token reduce over 8 lanes (three
+// shuffles each) and every staged key / query load feeds four rows.  The block
+// stages each group of G tokens' keys, queries and its rows' values once,
+// double-buffered, with one block barrier per group (as linear_step_block).
+template <typename TIn, int DK, int kMode>
+__global__ void __launch_bounds__(kStepThreads, 2) linear_step_quad(const StepArgs a, int G) {
+    constexpr int CPL = DK / 8;                  // columns per lane
+    constexpr int kEl = 16 / (int)sizeof(TIn);   // elements per 16-byte piece
+    static_assert(CPL % kEl == 0, "whole pieces per lane");
+    extern __shared__ __align__(16) unsigned char step_smem[];
+    const int wpb = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 3, c = lane & 7;
+    const int rows_pb = 4 * wpb;
+    const long long row0 = (long long)blockIdx.x * rows_pb;   // the block's first row overall
+    const long long seq = row0 / a.dv;
+    const int rb = (int)(row0 % a.dv);
+    const int lr = 4 * warp + grp;                            // row within the block
+    const int r = rb + lr;
+    const int n = a.n;
+    const size_t row = ((size_t)seq * a.dv + r) * DK;
+    const TIn* q = static_cast<const TIn*>(a.q);
+    const TIn* k = static_cast<const TIn*>(a.k);
+    const TIn* v = static_cast<const TIn*>(a.v);
+    TIn* z = static_cast<TIn*>(a.z);
+    // buffer b: [G][DK] keys, [G][DK] queries, [G][rows_pb] values
+    const size_t kq = (size_t)G * DK, bufsz = 2 * kq + (size_t)G * rows_pb;
+    TIn* const buf = reinterpret_cast<TIn*>(step_smem);
+    auto stage = [&](int b, int t0, int len) {
+        TIn* kd = buf + b * bufsz;
+        TIn* qd = kd + kq;
+        TIn* vd = qd + kq;
+        const size_t first = (size_t)seq * n + t0;
+        const int nkq = len * DK / kEl;
+        for (int i = threadIdx.x; i < nkq; i += blockDim.x) {
+            cp_async16(kd + i * kEl, k + first * DK + (size_t)i * kEl);
+            cp_async16(qd + i * kEl, q + first * DK + (size_t)i * kEl);
+        }
+        const int vpt = rows_pb / kEl;                       // pieces per token
+        for (int i = threadIdx.x; i < len * vpt; i += blockDim.x) {
+            const int t = i / vpt, pc = i % vpt;
+            cp_async16(vd + t * rows_pb + pc * kEl, v + (first + t) * a.dv + rb + pc * kEl);
+        }
+    };
+    stage(0, 0, min(G, n));
+    auto gates = [&](int t0, int len, float& th, float& et, float& keep) {
+        th = 0.f; et = 0.f; keep = 1.f;
+        if (lane < len) {
+            const size_t tok = (size_t)seq * n + t0 + lane;
+            th = __ldg(a.theta + tok);
+            et = a.eta ? __ldg(a.eta + tok) : 0.f;
+            const float al = a.alpha ? __ldg(a.alpha + tok) : 0.f;
+            keep = kMode == 0 ? 1.f - al : al;
+        }
+    };
+    float th, et, keep;
+    gates(0, min(G, n), th, et, keep);
+    const float* w0 = initial_row(a, seq, r);
+    float w[CPL], sm_[CPL], wc[CPL];
+#pragma unroll
+    for (int i4 = 0; i4 < CPL / 4; ++i4) {
+        const int j = c * CPL + 4 * i4;
+        const float4 x = *reinterpret_cast<const float4*>(w0 + j);
+        const float4 y = (kMode == 0 && a.S) ? *reinterpret_cast<const float4*>(a.S + row + j)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 u = a.pos != 0 ? *reinterpret_cast<const float4*>(a.Wc + row + j)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[4 * i4] = x.x; w[4 * i4 + 1] = x.y; w[4 * i4 + 2] = x.z; w[4 * i4 + 3] = x.w;
+        sm_[4 * i4] = y.x; sm_[4 * i4 + 1] = y.y; sm_[4 * i4 + 2] = y.z; sm_[4 * i4 + 3] = y.w;
+        wc[4 * i4] = u.x; wc[4 * i4 + 1] = u.y; wc[4 * i4 + 2] = u.z; wc[4 * i4 + 3] = u.w;
+    }
+    int p = a.pos;
+    bool wc_changed = false;
+    for (int t0 = 0; t0 < n; t0 += G) {
+        const int len = min(G, n - t0);
+        const int b = (t0 / G) & 1;
+        const TIn* ks = buf + b * bufsz;
+        const TIn* qs = ks + kq;
+        const TIn* vs = qs + kq;
+        cp_async_wait_all();
+        __syncthreads();
+        float thn = 0.f, etn = 0.f, keepn = 1.f;
+        if (t0 + G < n) {
+            const int ln = min(G, n - t0 - G);
+            stage(b ^ 1, t0 + G, ln);
+            gates(t0 + G, ln, thn, etn, keepn);
+        }
+        for (int u = 0; u < len; ++u) {
+            if (p == 0) {   // this token opens a chunk: its gradient point is now
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) wc[i] = w[i];
+                wc_changed = true;
+            }
+            float kv[CPL], qv[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; i += kEl) {
+                const uint4 kk = *reinterpret_cast<const uint4*>(ks + u * DK + c * CPL + i);
+                const uint4 qq = *reinterpret_cast<const uint4*>(qs + u * DK + c * CPL + i);
+                if constexpr (sizeof(TIn) == 2) {
+                    const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w}, qw[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kv[i + 2 * e] = __uint_as_float(kw[e] << 16);
+                        kv[i + 2 * e + 1] = __uint_as_float(kw[e] & 0xffff0000u);
+                        qv[i + 2 * e] = __uint_as_float(qw[e] << 16);
+                        qv[i + 2 * e + 1] = __uint_as_float(qw[e] & 0xffff0000u);
+                    }
+                } else {
+                    kv[i] = __uint_as_float(kk.x); kv[i + 1] = __uint_as_float(kk.y);
+                    kv[i + 2] = __uint_as_float(kk.z); kv[i + 3] = __uint_as_float(kk.w);
+                    qv[i] = __uint_as_float(qq.x); qv[i + 1] = __uint_as_float(qq.y);
+                    qv[i + 2] = __uint_as_float(qq.z); qv[i + 3] = __uint_as_float(qq.w);
+                }
+            }
+            const float vr = to_f<TIn>(vs[u * rows_pb + lr]);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; i += 2) {
+                if constexpr (kMode == 0) {
+                    a0 = fmaf(wc[i], kv[i], a0);
+                    a1 = fmaf(wc[i + 1], kv[i + 1], a1);
+                } else {
+                    a0 = fmaf(wc[i] + w[i], kv[i], a0);
+                    a1 = fmaf(wc[i + 1] + w[i + 1], kv[i + 1], a1);
+                }
+            }
+            float acc = a0 + a1;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            const float thu = __shfl_sync(0xffffffffu, th, u);
+            const float keepu = __shfl_sync(0xffffffffu, keep, u);
+            float z0 = 0.f, z1 = 0.f;
+            if constexpr (kMode == 0) {
+                const float ge = 2.f * thu * (acc - vr);   // theta times the gradient's row factor
+                const float etu = __shfl_sync(0xffffffffu, et, u);
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    sm_[i] = fmaf(etu, sm_[i], -ge * kv[i]);
+                    w[i] = fmaf(keepu, w[i], sm_[i]);
+                    if (i & 1) z1 = fmaf(w[i], qv[i], z1);
+                    else z0 = fmaf(w[i], qv[i], z0);
+                }
+            } else {
+                const float gg = thu * (acc - vr);         // eta_t ((W_c + W) k - v)_r
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    w[i] = fmaf(keepu, w[i], -gg * kv[i]);
+                    if (i & 1) z1 = fmaf(w[i], qv[i], z1);
+                    else z0 = fmaf(w[i], qv[i], z0);
+                }
+            }
+            float zq = z0 + z1;
+            zq += __shfl_xor_sync(0xffffffffu, zq, 4);
+            zq += __shfl_xor_sync(0xffffffffu, zq, 2);
+            zq += __shfl_xor_sync(0xffffffffu, zq, 1);
+            if (c == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
+            p = p + 1 == a.chunk ? 0 : p + 1;
+        }
+        th = thn; et = etn; keep = keepn;
+    }
+#pragma unroll
+    for (int i4 = 0; i4 < CPL / 4; ++i4) {
+        const int j = c * CPL + 4 * i4;
+        *reinterpret_cast<float4*>(a.W + row + j) =
+            make_float4(w[4 * i4], w[4 * i4 + 1], w[4 * i4 + 2], w[4 * i4 + 3]);
+        if (kMode == 0 && a.S)
+            *reinterpret_cast<float4*>(a.S + row + j) =
+                make_float4(sm_[4 * i4], sm_[4 * i4 + 1], sm_[4 * i4 + 2], sm_[4 * i4 + 3]);
+        if (wc_changed && a.Wc)
+            *reinterpret_cast<float4*>(a.Wc + row + j) =
+                make_float4(wc[4 * i4], wc[4 * i4 + 1], wc[4 * i4 + 2], wc[4 * i4 + 3]);
+    }
+}
+
 // Tokens per staged group: the keys and queries of a group take at most
 // 4 KB per warp (32 KB per block), and a group never exceeds 32 tokens (one
 // per lane for the per-token scalars).
@@ -441,6 +618,29 @@ template <typename TIn, int NJ, int kMode>
 void launch_mode(const StepArgs& a, unsigned blocks, cudaStream_t s) {
     if (a.n == 1) {
         linear_step_direct<TIn, NJ, kMode><<<blocks, kStepThreads, 0, s>>>(a);
+    } else if ((NJ == 2 || NJ == 4) && a.dk == 32 * NJ && a.dv % 8 == 0) {
+        // four rows per warp; blocks of 8, 4 or 2 warps (the largest that still
+        // gives two blocks per SM, since a long sequence has few rows)
+        static int sms = 0;
+        if (sms == 0) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                sms = 152;
+        }
+        const long long rows = (long long)a.B * a.H * a.dv;
+        int wpb = 2;
+        for (int cand = 8; cand >= 2; cand /= 2)
+            if (a.dv % (4 * cand) == 0 && rows / (4 * cand) >= 2LL * sms) { wpb = cand; break; }
+        const int rows_pb = 4 * wpb;
+        const int per_token = (2 * a.dk + rows_pb) * (int)sizeof(TIn);
+        int G = 8192 / per_token;
+        G = G < 1 ? 1 : (G > 32 ? 32 : G);
+        if (G > a.n) G = a.n;
+        const size_t smem = (size_t)2 * G * (2 * a.dk + rows_pb) * sizeof(TIn);
+        const unsigned qblocks = (unsigned)(rows / rows_pb);
+        linear_step_quad<TIn, 32 * (NJ == 2 ? 2 : 4), kMode>
+            <<<qblocks, 32 * wpb, smem, s>>>(a, G);
     } else if (a.dv % (kStepThreads / 32) == 0) {
         // whole blocks of one sequence: block-shared staging, groups of up to
         // 32 tokens within 8 KB per buffer

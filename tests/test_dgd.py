@@ -67,7 +67,7 @@ def test_scan_rectangular_and_chunk_one():
     H.compare(gpu_run(inp, 1), oracle_run(inp, 1), ["z", "W"], H.TOL["f32"])
 
 
-@pytest.mark.parametrize("d", [16, 512])
+@pytest.mark.parametrize("d", [16, 128, 512])
 def test_scan_widths(d):
     inp = make("f32", B=1, Hh=1, T=40, d=d, seed=4)
     H.compare(gpu_run(inp, 8), oracle_run(inp, 8), ["z", "W"], H.TOL["f32"])
