@@ -33,19 +33,12 @@ namespace {
 
 using simt::block_coefficients;
 using simt::store_out;
+using simt::dot4;
+using simt::gelu;
+using simt::gelu_grad;
 
 constexpr int kCT = 512;   // threads per CTA
 
-__device__ __forceinline__ float gelu_c(float x) {
-    return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-}
-__device__ __forceinline__ float gelu_dc(float x) {
-    return 0.5f * (1.f + erff(x * 0.70710678118654752f)) +
-           x * 0.39894228040143268f * expf(-0.5f * x * x);
-}
-__device__ __forceinline__ float dot4c(const float4 a, const float4 b) {
-    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-}
 
 __device__ __forceinline__ uint32_t cta_rank() {
     uint32_t r;
@@ -261,13 +254,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
                 const float4 w4 = w[j4];
 #pragma unroll
                 for (int s = 0; s < TPG; ++s)
-                    acc[s] += dot4c(w4, *reinterpret_cast<const float4*>(Ks + (t0 + s) * ld + 4 * j4));
+                    acc[s] += dot4(w4, *reinterpret_cast<const float4*>(Ks + (t0 + s) * ld + 4 * j4));
             }
 #pragma unroll
             for (int s = 0; s < TPG; ++s) {
                 const bool live = t0 + s < n;
-                Ak[(t0 + s) * lh + hu] = live ? gelu_c(acc[s]) : 0.f;
-                Gp[(t0 + s) * lh + hu] = live ? gelu_dc(acc[s]) : 0.f;
+                Ak[(t0 + s) * lh + hu] = live ? gelu(acc[s]) : 0.f;
+                Gp[(t0 + s) * lh + hu] = live ? gelu_grad(acc[s]) : 0.f;
             }
         }
         // scores C[t][s] (q_t . k_s), s <= t (both CTAs)
@@ -277,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
             if (s <= t && t < n) {
 #pragma unroll 4
                 for (int j = 0; j < D; j += 4)
-                    acc += dot4c(*reinterpret_cast<const float4*>(Qs + t * ld + j),
+                    acc += dot4(*reinterpret_cast<const float4*>(Qs + t * ld + j),
                                  *reinterpret_cast<const float4*>(Ks + s * ld + j));
                 acc *= C[t * lc + s];
             }
@@ -295,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
                 const float4 w4 = w[u4];
 #pragma unroll
                 for (int s = 0; s < NB; ++s)
-                    acc[s] += dot4c(w4, *reinterpret_cast<const float4*>(Ak + s * lh + 4 * u4));
+                    acc[s] += dot4(w4, *reinterpret_cast<const float4*>(Ak + s * lh + 4 * u4));
             }
 #pragma unroll
             for (int s = 0; s < NB; ++s) {
@@ -333,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
                                               W2[(4 * i4 + 2) * l2 + hu], W2[(4 * i4 + 3) * l2 + hu]);
 #pragma unroll
                 for (int s = 0; s < TPG; ++s)
-                    acc[s] += dot4c(w4, *reinterpret_cast<const float4*>(E + (t0 + s) * ld + 4 * i4));
+                    acc[s] += dot4(w4, *reinterpret_cast<const float4*>(E + (t0 + s) * ld + 4 * i4));
             }
 #pragma unroll
             for (int s = 0; s < TPG; ++s)
@@ -354,8 +347,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
 #pragma unroll
                 for (int t = 0; t < TPG; ++t) {
                     const float4 q4 = *reinterpret_cast<const float4*>(Qs + (t0 + t) * ld + 4 * j4);
-                    aw[t] += dot4c(w4, q4);
-                    as[t] += dot4c(s4, q4);
+                    aw[t] += dot4(w4, q4);
+                    as[t] += dot4(s4, q4);
                 }
             }
             float dcol[NB];
@@ -368,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
 #pragma unroll
                 for (int s = 0; s < NB; ++s)
                     if (s <= tt) corr += SK[tt * lc + s] * dcol[s];
-                Aq[tt * lh + hu] = tt < n ? gelu_c(beta[tt] * aw[t] + cc[tt] * as[t] - corr) : 0.f;
+                Aq[tt * lh + hu] = tt < n ? gelu(beta[tt] * aw[t] + cc[tt] * as[t] - corr) : 0.f;
             }
         }
         __syncthreads();
@@ -379,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
             if (s <= t && t < n) {
 #pragma unroll 4
                 for (int u = 0; u < HH; u += 4)
-                    acc += dot4c(*reinterpret_cast<const float4*>(Aq + t * lh + u),
+                    acc += dot4(*reinterpret_cast<const float4*>(Aq + t * lh + u),
                                  *reinterpret_cast<const float4*>(Ak + s * lh + u));
             }
             Xs[x] = acc;
@@ -403,8 +396,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCT, 1) mlp_cl_kerne
 #pragma unroll
                 for (int t = 0; t < NB; ++t) {
                     const float4 a4 = *reinterpret_cast<const float4*>(Aq + t * lh + 4 * u4);
-                    aw[t] += dot4c(w4, a4);
-                    as[t] += dot4c(s4, a4);
+                    aw[t] += dot4(w4, a4);
+                    as[t] += dot4(s4, a4);
                 }
             }
 #pragma unroll

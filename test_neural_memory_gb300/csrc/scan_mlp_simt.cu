@@ -34,20 +34,13 @@ namespace {
 using simt::block_coefficients;
 using simt::load_in;
 using simt::store_out;
+using simt::dot4;
+using simt::gelu;
+using simt::gelu_grad;
 
 constexpr int kMT = 256;   // threads per CTA
 
-__device__ __forceinline__ float gelu_x(float x) {
-    return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-}
-__device__ __forceinline__ float gelu_dx(float x) {
-    return 0.5f * (1.f + erff(x * 0.70710678118654752f)) +
-           x * 0.39894228040143268f * expf(-0.5f * x * x);
-}
 
-__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
-    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-}
 
 // Shared-memory carve-up (floats; rows of d + 4 / hidden + 4 keep 16-byte alignment).
 struct MlpSmem {
@@ -161,7 +154,7 @@ __global__ void __launch_bounds__(kMT, 1) mlp_simt2_kernel(MlpArgs p) {
 #pragma unroll
             for (int s = 0; s < NB; ++s) {
                 Hk[s * lh + u] = acc[s];
-                Ak[s * lh + u] = s < n ? gelu_x(acc[s]) : 0.f;
+                Ak[s * lh + u] = s < n ? gelu(acc[s]) : 0.f;
             }
         }
         // scores C[t][s] (q_t . k_s), s <= t
@@ -220,7 +213,7 @@ __global__ void __launch_bounds__(kMT, 1) mlp_simt2_kernel(MlpArgs p) {
             }
 #pragma unroll
             for (int s = 0; s < NB; ++s)
-                D1[s * lh + u] = s < n ? acc[s] * gelu_dx(Hk[s * lh + u]) : 0.f;
+                D1[s * lh + u] = s < n ? acc[s] * gelu_grad(Hk[s * lh + u]) : 0.f;
         }
         __syncthreads();
         // Hq_t = beta_t W1 q_t + c_t S1 q_t - sum_{s<=t} SK[t][s] D1_s, Aq = GELU(Hq)
@@ -248,7 +241,7 @@ __global__ void __launch_bounds__(kMT, 1) mlp_simt2_kernel(MlpArgs p) {
                 float corr = 0.f;
 #pragma unroll
                 for (int s = 0; s <= t; ++s) corr += SK[t * lc + s] * dcol[s];
-                Aq[t * lh + u] = t < n ? gelu_x(beta[t] * aw[t] + cc[t] * as[t] - corr) : 0.f;
+                Aq[t * lh + u] = t < n ? gelu(beta[t] * aw[t] + cc[t] * as[t] - corr) : 0.f;
             }
         }
         __syncthreads();

@@ -35,6 +35,8 @@ namespace {
 using simt::block_coefficients;
 using simt::load_in;
 using simt::store_out;
+using simt::gelu;
+using simt::gelu_grad;
 
 constexpr int kThreads = 256;
 
@@ -198,14 +200,6 @@ __global__ void __launch_bounds__(kThreads) linear_simt_kernel(LinearArgs p) {
 // caller's output buffers (read at each chunk start, rewritten at its end).
 // ------------------------------------------------------------------------
 
-__device__ __forceinline__ float gelu_f(float x) {
-    return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
-}
-__device__ __forceinline__ float gelu_grad_f(float x) {
-    return 0.5f * (1.f + erff(x * 0.70710678118654752f)) +
-           x * 0.39894228040143268f * expf(-0.5f * x * x);
-}
-
 int mlp_block_tokens(int d, int hidden) {
     // largest power-of-two token block (<= 32) whose buffers fit in 200 KB
     for (int nb = 32; nb >= 1; nb /= 2) {
@@ -302,8 +296,8 @@ __global__ void __launch_bounds__(kThreads) mlp_simt_kernel(MlpArgs p, int nb) {
             for (int s = lane; s < nb; s += 32) {
                 float acc = 0.f;
                 for (int j = 0; j < d; ++j) acc += W1[(size_t)u * d + j] * Ks[s * ld + j];
-                Ak[s * lh + u] = s < n ? gelu_f(acc) : 0.f;
-                Gp[s * lh + u] = s < n ? gelu_grad_f(acc) : 0.f;
+                Ak[s * lh + u] = s < n ? gelu(acc) : 0.f;
+                Gp[s * lh + u] = s < n ? gelu_grad(acc) : 0.f;
             }
         }
         __syncthreads();
@@ -346,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) mlp_simt_kernel(MlpArgs p, int nb) {
                 }
                 float corr = 0.f;
                 for (int s = 0; s <= t && s < n; ++s) corr += SK[t * lc + s] * D1[s * lh + u];
-                Aq[t * lh + u] = t < n ? gelu_f(beta[t] * wq + cc[t] * sq - corr) : 0.f;
+                Aq[t * lh + u] = t < n ? gelu(beta[t] * wq + cc[t] * sq - corr) : 0.f;
             }
         }
         __syncthreads();

@@ -1,6 +1,6 @@
 // Device helpers shared by the CUDA-core kernels (forward scan and gradient):
-// element loads / stores in the input dtype and the per-block coefficients of
-// the chunk recurrences.
+// element loads / stores in the input dtype, the GELU of the 2-layer memory and
+// the per-block coefficients of the chunk recurrences.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -18,6 +18,20 @@ __device__ __forceinline__ float load_in(const __nv_bfloat16* p, size_t i) {
 __device__ __forceinline__ void store_out(float* p, size_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
+}
+
+// Exact GELU x/2 (1 + erf(x / sqrt 2)) of the 2-layer memory and its
+// derivative, with CUDA's erff / expf.
+__device__ __forceinline__ float gelu(float x) {
+    return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_grad(float x) {
+    return 0.5f * (1.f + erff(x * 0.70710678118654752f)) +
+           x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
 }
 
 // Per-block coefficients.  th/et/al hold the n gates of the block; writes

@@ -177,6 +177,47 @@ __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// One token of one row (one row per warp, NJ columns per lane): the error at
+// the chunk-start point, the row's update and the read of the updated row,
+// summed over the warp.  ks / qs: the token's staged key and query; vr, th,
+// et, keep: its value on this row and its gates (mode 0: theta, eta and
+// 1 - alpha; mode 1: the DGD step eta and retention alpha).
+template <typename TIn, int NJ, int kMode>
+__device__ __forceinline__ float row_token(float (&w)[NJ], float (&s)[NJ], const float (&wc)[NJ],
+                                           const TIn* ks, const TIn* qs, int dk, int lane,
+                                           float vr, float th, float et, float keep) {
+    float kv[NJ], qv[NJ];
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+        const int j = lane + 32 * i;
+        kv[i] = j < dk ? to_f<TIn>(ks[j]) : 0.f;
+        qv[i] = j < dk ? to_f<TIn>(qs[j]) : 0.f;
+    }
+    float acc = 0.f, zq = 0.f;
+    if constexpr (kMode == 0) {
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
+        const float ge = 2.f * th * (warp_sum(acc) - vr);   // theta times the gradient's row factor
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            s[i] = fmaf(et, s[i], -ge * kv[i]);
+            w[i] = fmaf(keep, w[i], s[i]);
+            zq = fmaf(w[i], qv[i], zq);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+        // eta_t ((W_c + W) k - v)_r; the retention factor rides in `keep`
+        const float g = th * (warp_sum(acc) - vr);
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) {
+            w[i] = fmaf(keep, w[i], -g * kv[i]);
+            zq = fmaf(w[i], qv[i], zq);
+        }
+    }
+    return warp_sum(zq);
+}
+
 // Several tokens per call.  NJ = columns per lane (dk <= 32 NJ).  Tokens are
 // taken in groups of G: one
 // round trip brings a group's keys and queries into the warp's shared-memory
@@ -240,43 +281,11 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
                 for (int i = 0; i < NJ; ++i) wc[i] = w[i];
                 wc_changed = true;
             }
-            float kv[NJ], qv[NJ];
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) {
-                const int j = lane + 32 * i;
-                kv[i] = j < dk ? to_f<TIn>(ks[u * dk + j]) : 0.f;
-                qv[i] = j < dk ? to_f<TIn>(qs[u * dk + j]) : 0.f;
-            }
-            float acc = 0.f;
-            float zq = 0.f;
-            if constexpr (kMode == 0) {
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
-                const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
-                // theta_t times the gradient's row factor
-                const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
-                const float etu = __shfl_sync(0xffffffffu, et, u);
-                const float keepu = __shfl_sync(0xffffffffu, keep, u);
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) {
-                    s[i] = fmaf(etu, s[i], -ge * kv[i]);
-                    w[i] = fmaf(keepu, w[i], s[i]);
-                    zq = fmaf(w[i], qv[i], zq);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
-                // eta_t ((W_c + W) k - v)_r; the retention factor rides in `keep`
-                const float g = __shfl_sync(0xffffffffu, th, u) *
-                                (warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u));
-                const float alu = __shfl_sync(0xffffffffu, keep, u);
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) {
-                    w[i] = fmaf(alu, w[i], -g * kv[i]);
-                    zq = fmaf(w[i], qv[i], zq);
-                }
-            }
-            zq = warp_sum(zq);
+            const float zq = row_token<TIn, NJ, kMode>(w, s, wc, ks + u * dk, qs + u * dk, dk, lane,
+                                                       __shfl_sync(0xffffffffu, vr, u),
+                                                       __shfl_sync(0xffffffffu, th, u),
+                                                       kMode == 0 ? __shfl_sync(0xffffffffu, et, u) : 0.f,
+                                                       __shfl_sync(0xffffffffu, keep, u));
             if (lane == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
             p = p + 1 == a.chunk ? 0 : p + 1;
         }
@@ -374,41 +383,11 @@ __global__ void __launch_bounds__(kStepThreads, NJ <= 4 ? 5 : 1)
                 for (int i = 0; i < NJ; ++i) wc[i] = w[i];
                 wc_changed = true;
             }
-            float kv[NJ], qv[NJ];
-#pragma unroll
-            for (int i = 0; i < NJ; ++i) {
-                const int j = lane + 32 * i;
-                kv[i] = j < dk ? to_f<TIn>(ks[u * dk + j]) : 0.f;
-                qv[i] = j < dk ? to_f<TIn>(qs[u * dk + j]) : 0.f;
-            }
-            float acc = 0.f;
-            float zq = 0.f;
-            if constexpr (kMode == 0) {
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i], kv[i], acc);
-                const float e = warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u);
-                const float ge = 2.f * __shfl_sync(0xffffffffu, th, u) * e;
-                const float etu = __shfl_sync(0xffffffffu, et, u);
-                const float keepu = __shfl_sync(0xffffffffu, keep, u);
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) {
-                    s[i] = fmaf(etu, s[i], -ge * kv[i]);
-                    w[i] = fmaf(keepu, w[i], s[i]);
-                    zq = fmaf(w[i], qv[i], zq);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
-                const float g = __shfl_sync(0xffffffffu, th, u) *
-                                (warp_sum(acc) - __shfl_sync(0xffffffffu, vr, u));
-                const float alu = __shfl_sync(0xffffffffu, keep, u);
-#pragma unroll
-                for (int i = 0; i < NJ; ++i) {
-                    w[i] = fmaf(alu, w[i], -g * kv[i]);
-                    zq = fmaf(w[i], qv[i], zq);
-                }
-            }
-            zq = warp_sum(zq);
+            const float zq = row_token<TIn, NJ, kMode>(w, s, wc, ks + u * dk, qs + u * dk, dk, lane,
+                                                       __shfl_sync(0xffffffffu, vr, u),
+                                                       __shfl_sync(0xffffffffu, th, u),
+                                                       kMode == 0 ? __shfl_sync(0xffffffffu, et, u) : 0.f,
+                                                       __shfl_sync(0xffffffffu, keep, u));
             if (lane == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
             p = p + 1 == a.chunk ? 0 : p + 1;
         }

@@ -94,7 +94,7 @@ def test_delta_rule_chunk_one():
     H.compare(gpu, ref, ["z", "W"], H.TOL["f32"])
 
 
-@pytest.mark.parametrize("d,dv", [(16, 8), (512, 32), (96, 64), (128, 128), (128, 24)])
+@pytest.mark.parametrize("d,dv", [(16, 8), (16, 12), (512, 32), (96, 64), (128, 128), (128, 24)])
 def test_decode_widths(d, dv):
     # dk below one warp, the widest row, and a width that is not a power of two
     gpu, ref = run_decode("titans", "f32", T0=0, calls=[3, 20, 1], chunk=8, d=d, dv=dv, B=1,
