@@ -73,6 +73,12 @@ def test_scan_widths(d):
     H.compare(gpu_run(inp, 8), oracle_run(inp, 8), ["z", "W"], H.TOL["f32"])
 
 
+def test_scan_many_rows_block_sizes():
+    """10 240 rows of d = 128: the four-rows-per-warp kernel in blocks of 8 warps."""
+    inp = make("bf16", B=8, Hh=10, T=24, d=128, seed=7)
+    H.compare(gpu_run(inp, 8), oracle_run(inp, 8), ["z", "W"], H.TOL["bf16"])
+
+
 def test_scan_in_place_and_empty():
     import test_neural_memory_gb300 as ttm
     inp = make("f32", B=2, Hh=1, T=20, d=32, seed=6)

@@ -102,6 +102,15 @@ def test_decode_widths(d, dv):
     H.compare(gpu, ref, ["z", "W", "S"], H.TOL["f32"])
 
 
+@pytest.mark.parametrize("dtype,B,Hh", [("bf16", 8, 10), ("f32", 4, 10)])
+def test_decode_many_rows_block_sizes(dtype, B, Hh):
+    """Enough rows that the four-rows-per-warp kernel takes blocks of 8 warps
+    (10 240 rows) or 4 warps (5 120 rows) instead of 2."""
+    gpu, ref = run_decode("titans", dtype, T0=0, calls=[3, 9, 1], chunk=8, d=128, B=B, Hh=Hh,
+                          seed=46, theta=("sigmoid", 0.02))
+    H.compare(gpu, ref, ["z", "W", "S"], H.TOL[dtype])
+
+
 def test_decode_rejects_mid_chunk_without_snapshot():
     import test_neural_memory_gb300 as ttm
     w, inp = wl.generate_custom(kind="titans", dtype="f32", B=1, H=1, T=2, d=64, chunk=4, seed=1)
