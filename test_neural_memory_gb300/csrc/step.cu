@@ -492,6 +492,10 @@ __global__ void __launch_bounds__(kStepThreads, 2) linear_step_quad(const StepAr
             stage(b ^ 1, t0 + G, ln);
             gates(t0 + G, ln, thn, etn, keepn);
         }
+        // The read of token u - 1 is summed over its 8 lanes together with token
+        // u's error (two independent shuffle chains issued side by side), so
+        // only the error's chain is on the state's dependency path.
+        float zprev = 0.f;
         for (int u = 0; u < len; ++u) {
             if (p == 0) {   // this token opens a chunk: its gradient point is now
 #pragma unroll
@@ -531,10 +535,14 @@ __global__ void __launch_bounds__(kStepThreads, 2) linear_step_quad(const StepAr
                     a1 = fmaf(wc[i + 1] + w[i + 1], kv[i + 1], a1);
                 }
             }
-            float acc = a0 + a1;
+            float acc = a0 + a1, zp = zprev;
             acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            zp += __shfl_xor_sync(0xffffffffu, zp, 4);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            zp += __shfl_xor_sync(0xffffffffu, zp, 2);
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            zp += __shfl_xor_sync(0xffffffffu, zp, 1);
+            if (u > 0 && c == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u - 1) * a.dv + r, zp);
             const float thu = __shfl_sync(0xffffffffu, th, u);
             const float keepu = __shfl_sync(0xffffffffu, keep, u);
             float z0 = 0.f, z1 = 0.f;
@@ -557,13 +565,14 @@ __global__ void __launch_bounds__(kStepThreads, 2) linear_step_quad(const StepAr
                     else z0 = fmaf(w[i], qv[i], z0);
                 }
             }
-            float zq = z0 + z1;
-            zq += __shfl_xor_sync(0xffffffffu, zq, 4);
-            zq += __shfl_xor_sync(0xffffffffu, zq, 2);
-            zq += __shfl_xor_sync(0xffffffffu, zq, 1);
-            if (c == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + u) * a.dv + r, zq);
+            zprev = z0 + z1;
             p = p + 1 == a.chunk ? 0 : p + 1;
         }
+        // the group's last read
+        zprev += __shfl_xor_sync(0xffffffffu, zprev, 4);
+        zprev += __shfl_xor_sync(0xffffffffu, zprev, 2);
+        zprev += __shfl_xor_sync(0xffffffffu, zprev, 1);
+        if (len > 0 && c == 0) st_out<TIn>(z + ((size_t)seq * n + t0 + len - 1) * a.dv + r, zprev);
         th = thn; et = etn; keep = keepn;
     }
 #pragma unroll
