@@ -18,8 +18,9 @@
 //   W2 A (for E), aq_t . a_s (for the second score table), W2 aq_t (for z).
 // Each CTA writes its partial sums into its own buffer, the cluster barrier
 // publishes them, and both CTAs add the two partials (addition commutes, so
-// both hold bit-identical E and score tables).  CTA r writes outputs z[., i] for its
-// half of the rows i.
+// both hold bit-identical E and score tables).  CTA r writes the outputs
+// z[., i] of its half of the rows i.  The next chunk's inputs are loaded into
+// registers while the current chunk computes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +39,6 @@ using simt::gelu;
 using simt::gelu_grad;
 
 constexpr int kCT = 512;   // threads per CTA
-
 
 __device__ __forceinline__ uint32_t cta_rank() {
     uint32_t r;
