@@ -193,6 +193,11 @@ int ttm_titans_fwd_host(int B, int H, int T, int dk, int dv, int chunk, int dtyp
  *   momentum state).
  * Shapes: d a multiple of 8, hidden a multiple of 8 (kernel limits reported
  * as TTM_ERR_UNSUPPORTED).
+ * Kernels: fp32 arithmetic by default (a two-CTA cluster per sequence with the
+ * state in shared memory for (d, hidden) in {(32, 128), (64, 256), (128, 128)}
+ * and chunk <= 16; one CTA per sequence otherwise).  Under the tensor-core
+ * policy (ttm_set_kernel_policy) bf16 inputs with d = 64, hidden = 256,
+ * chunk 16 run a tcgen05 kernel whose recurrent operands are rounded to bf16.
  */
 int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype,
                 const void* q, const void* k, const void* v,
