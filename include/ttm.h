@@ -334,8 +334,9 @@ int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
 /* DGD memory scan: the update of "Nested Learning" §8.1 eq (88) with a matrix
  * memory and the L2 objective of eq (93), taken chunk-wise as in §8.2 (every
  * gradient of a chunk at the state left by the previous chunk, Mc):
+ *     z_t = M_{t-1} q_t   (read before the token's write, as eq (86) prints
+ *                          y_t = M_{memory,t-1}(q_t))
  *     M_t = M_{t-1} (alpha_t I - eta_t k_t k_t^T) - eta_t (Mc k_t - v_t) k_t^T
- *     z_t = M_t q_t   (read after the token's write, as for every memory here)
  * eta_t is the step and alpha_t a retention factor (alpha = 1 keeps the
  * memory), both as the page prints them: note that alpha here multiplies the
  * memory, unlike the forgetting rate of ttm_titans_fwd (which keeps 1 - alpha),
@@ -430,6 +431,32 @@ int ttm_last_kernel(void);
  * (monotonic; successful calls only; the tensor-core linear path enqueues two:
  * the coefficient pre-pass and the scan). */
 unsigned long long ttm_launch_count(void);
+
+/* Failure-detection hooks for tests (no counterpart on the pages: they exist
+ * so that the error paths can be exercised without faulting a GPU).
+ *   TTM_DBG_WAIT_CYCLES, n >= 0: every bounded device wait of the tensor-core
+ *     kernels gives up after n SM clock cycles (0 restores the default, about
+ *     2 s).  Applies to calls made from now on.
+ *   TTM_DBG_STALL_CHUNK, c >= 0: the next call that runs the tensor-core
+ *     linear / Titans scan announces 16 bytes more for chunk c's input tiles
+ *     than it copies, so that chunk's barrier never completes: every wait on it
+ *     runs out, the kernel sets the device status word to TTM_ERR_TIMEOUT,
+ *     drains its copies and MMAs, frees its tensor memory and returns (its
+ *     outputs are then invalid).  The setting is used up by that one call; -1
+ *     clears it.  Nothing faults, traps or hangs.
+ *   TTM_DBG_FAIL_CALLS, n >= 0: the next n calls of ttm_linear_fwd,
+ *     ttm_titans_fwd (and the variants built on them) and ttm_mlp_fwd return
+ *     TTM_ERR_CUDA after validating their arguments, without enqueueing
+ *     anything (host-side injection of a failed launch).
+ * Returns TTM_OK, or TTM_ERR_INVALID_ARG for an unknown option or a value out
+ * of range.  The settings are process-wide. */
+enum { TTM_DBG_WAIT_CYCLES = 1, TTM_DBG_STALL_CHUNK = 2, TTM_DBG_FAIL_CALLS = 3 };
+int ttm_debug_set(int option, long long value);
+
+/* Number of CUDA devices this library's own runtime can reach (0 when there
+ * is no GPU or no usable driver).  Touches no device memory; host-side test
+ * suites use it to decide whether a GPU is reachable. */
+int ttm_cuda_device_count(void);
 
 /* Synchronises the current device, then returns and clears its status word:
  * TTM_OK, or TTM_ERR_TIMEOUT if a tensor-core kernel abandoned a bounded wait

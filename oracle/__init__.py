@@ -157,7 +157,8 @@ def linear_primal_bwd(q, k, v, theta, W0, chunk, dz, eta=None, alpha=None, S0=No
 
 def dgd_primal(q, k, v, eta, alpha, W0, chunk, shared_over_batch=False, threads=0) -> Result:
     """DGD memory scan in float64: M_t = M_{t-1}(alpha_t I - eta_t k k^T)
-    - eta_t (Mc k - v) k^T, read z_t = M_t q_t (see ttm_oracle.c).
+    - eta_t (Mc k - v) k^T, read z_t = M_{t-1} q_t before the token's write
+    ("Nested Learning" eq (86); see ttm_oracle.c).
     q, k: [B,H,T,dk]; v: [B,H,T,dv]; eta (step), alpha (retention): [B,H,T];
     W0: [B|1,H,dv,dk].  Returns z, W and the thread count."""
     q, k, v = _f64(q), _f64(k), _f64(v)

@@ -59,8 +59,9 @@
  *   M_t = M_{t-1} (alpha_t I - eta_t k_t k_t^T) - eta_t (Mc k_t - v_t) k_t^T
  * with alpha_t a retention factor (alpha = 1 keeps everything) and eta_t the
  * step, both as printed (no factor 2 on the gradient, as eq (93) writes it).
- * The read is z_t = M_t q_t, after the token's write, as for every memory of
- * this library.
+ * The read is the one eq (86) prints, y_t = M_{t-1} q_t: the memory as it
+ * stands before token t's own write (unlike the other memories here, whose
+ * pages read after the write).
  *
  * The (b, h) sequences are independent, so they are spread over POSIX
  * threads; each one runs the plain loop below.
@@ -448,6 +449,13 @@ static void dgd_one(const dgd_args* a, int b, int h) {
         const double et = a->eta[seq * T + t];
         const double al = a->alpha[seq * T + t];
         if (t % a->chunk == 0) memcpy(Mc, M, ns * sizeof(double));
+        /* read before the write: y_t = M_{t-1} q_t (eq (86)) */
+        double* zt = a->z + (seq * T + t) * dv;
+        for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += M[(size_t)i * dk + j] * qt[j];
+            zt[i] = acc;
+        }
         /* u = M_{t-1} k_t (the k k^T term) and e = Mc k_t - v_t (the gradient) */
         for (int i = 0; i < dv; ++i) {
             double mu = 0.0, mc = 0.0;
@@ -464,12 +472,6 @@ static void dgd_one(const dgd_args* a, int b, int h) {
                 const size_t ij = (size_t)i * dk + j;
                 M[ij] = al * M[ij] - et * u[i] * kt[j] - et * e[i] * kt[j];
             }
-        double* zt = a->z + (seq * T + t) * dv;
-        for (int i = 0; i < dv; ++i) {
-            double acc = 0.0;
-            for (int j = 0; j < dk; ++j) acc += M[(size_t)i * dk + j] * qt[j];
-            zt[i] = acc;
-        }
     }
     memcpy(a->W_out + seq * ns, M, ns * sizeof(double));
     free(M); free(Mc); free(u); free(e);

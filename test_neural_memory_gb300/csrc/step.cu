@@ -13,6 +13,7 @@
 //
 // The DGD memory ("Nested Learning" §8.1 eq (88) with the matrix memory and
 // L2 objective of eq (93), chunk-wise per §8.2) uses the same row structure:
+//   z_t = W q_t                       (read before the write, eq (86))
 //   W = W (alpha_t I - eta_t k k^T) - eta_t (W_c k - v) k^T
 // so row r takes W_r = alpha_t W_r - eta_t ((W_c + W)_r . k - v_r) k^T: one dot
 // product per token and row, like the Titans step.  Run over a whole sequence
@@ -124,13 +125,13 @@ __global__ void __launch_bounds__(kStepThreads) linear_step_direct(const StepArg
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+        for (int i = 0; i < NJ; ++i) {
+            acc = fmaf(wc[i] + w[i], kv[i], acc);
+            zq = fmaf(w[i], qv[i], zq);              // the read sees the memory before the write
+        }
         const float g = th * (warp_sum(acc) - vr);   // eta_t ((W_c + W) k - v)_r
 #pragma unroll
-        for (int i = 0; i < NJ; ++i) {
-            w[i] = fmaf(al, w[i], -g * kv[i]);
-            zq = fmaf(w[i], qv[i], zq);
-        }
+        for (int i = 0; i < NJ; ++i) w[i] = fmaf(al, w[i], -g * kv[i]);
     }
     zq = warp_sum(zq);
     if (lane == 0) st_out<TIn>(static_cast<TIn*>(a.z) + tok * a.dv + r, zq);
@@ -206,14 +207,14 @@ __device__ __forceinline__ float row_token(float (&w)[NJ], float (&s)[NJ], const
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < NJ; ++i) acc = fmaf(wc[i] + w[i], kv[i], acc);
+        for (int i = 0; i < NJ; ++i) {
+            acc = fmaf(wc[i] + w[i], kv[i], acc);
+            zq = fmaf(w[i], qv[i], zq);              // the read sees the memory before the write
+        }
         // eta_t ((W_c + W) k - v)_r; the retention factor rides in `keep`
         const float g = th * (warp_sum(acc) - vr);
 #pragma unroll
-        for (int i = 0; i < NJ; ++i) {
-            w[i] = fmaf(keep, w[i], -g * kv[i]);
-            zq = fmaf(w[i], qv[i], zq);
-        }
+        for (int i = 0; i < NJ; ++i) w[i] = fmaf(keep, w[i], -g * kv[i]);
     }
     return warp_sum(zq);
 }
@@ -560,9 +561,10 @@ __global__ void __launch_bounds__(kStepThreads, 2) linear_step_quad(const StepAr
                 const float gg = thu * (acc - vr);         // eta_t ((W_c + W) k - v)_r
 #pragma unroll
                 for (int i = 0; i < CPL; ++i) {
-                    w[i] = fmaf(keepu, w[i], -gg * kv[i]);
+                    // the read sees the memory before the write
                     if (i & 1) z1 = fmaf(w[i], qv[i], z1);
                     else z0 = fmaf(w[i], qv[i], z0);
+                    w[i] = fmaf(keepu, w[i], -gg * kv[i]);
                 }
             }
             zprev = z0 + z1;

@@ -1,9 +1,14 @@
 """Pins of the float64 DGD oracle ("Nested Learning" §8.1 eq (88) with the
-matrix memory and L2 objective of eq (93), chunk-wise as in §8.2) to facts
+matrix memory and L2 objective of eq (93), chunk-wise as in §8.2, read as eq
+(86) prints it: y_t = M_{t-1} q_t, before the token's own write) to facts
 outside itself.  CPU only.
 
+- Two hand-worked examples of eq (93) (a scalar memory at chunk 1 and 2, and
+  a 2x2 memory) fix the update, the gradient point and the read position; a
+  read after the write gives different numbers for both.
 - Chunk 1 with retention 1 is the online delta rule toward v / 2 with step
-  2 eta, i.e. the already pinned linear oracle with theta = eta and targets v / 2.
+  2 eta, i.e. the already pinned linear oracle with theta = eta and targets
+  v / 2, whose read after token t-1 is the DGD read of token t.
 - Orthonormal keys decouple the k k^T term: every M_{t-1} k_t is the snapshot's
   M_c k_t times the retention so far, so the chunk has a closed form.
 - The chunk form: with w_t = -eta_t (M_{t-1} k_t + M_c k_t - v_t), M_t is
@@ -24,6 +29,28 @@ def _dgd(q, k, v, eta, alpha, W0, chunk):
     return r["z"][0, 0], r["W"][0, 0]
 
 
+def test_hand_worked_examples(golden):
+    g = golden("p3_dgd_read_before_write.json")
+    sc = g["scalar"]
+    a = lambda x: np.asarray(x, dtype=np.float64)
+    for chunk in (1, 2):
+        z, W = _dgd(a(sc["q"])[:, None], a(sc["k"])[:, None], a(sc["v"])[:, None], a(sc["eta"]),
+                    a(sc["alpha"]), a([[sc["M0"]]]), chunk)
+        want = sc[f"chunk_{chunk}"]
+        assert np.allclose(z[:, 0], want["z"], atol=1e-14)
+        assert np.allclose(W[0, 0], want["M_final"], atol=1e-14)
+        assert not np.allclose(z[:, 0], sc["read_after_write_would_give"])
+    m = g["matrix"]
+    z, W = _dgd(a(m["q"]), a(m["k"]), a(m["v"]), a(m["eta"]), a(m["alpha"]), a(m["M0"]),
+                m["chunk"])
+    assert np.allclose(z, m["z"], atol=1e-14)
+    assert np.allclose(W, m["M_final"], atol=1e-14)
+    assert not np.allclose(z, m["read_after_write_would_give"])
+    z1, W1 = _dgd(a(m["q"])[:1], a(m["k"])[:1], a(m["v"])[:1], a(m["eta"])[:1],
+                  a(m["alpha"])[:1], a(m["M0"]), m["chunk"])
+    assert np.allclose(W1, m["M1"], atol=1e-14)
+
+
 def test_chunk_one_unit_retention_is_the_linear_delta_rule():
     rng = np.random.default_rng(1)
     T, dk, dv = 17, 5, 3
@@ -32,9 +59,13 @@ def test_chunk_one_unit_retention_is_the_linear_delta_rule():
     eta = rng.uniform(0.05, 0.3, T)
     W0 = rng.standard_normal((dv, dk))
     z, W = _dgd(q, k, v, eta, np.ones(T), W0, 1)
-    r = oracle.linear_primal(q[None, None], k[None, None], (v / 2)[None, None], eta[None, None],
-                             W0[None, None], 1)
-    assert np.allclose(z, r["z"][0, 0], atol=1e-12)
+    # the linear oracle reads after each write: its read after token t-1 with
+    # the query of token t is the DGD read of token t
+    q_next = np.concatenate([q[1:], q[:1]])
+    r = oracle.linear_primal(q_next[None, None], k[None, None], (v / 2)[None, None],
+                             eta[None, None], W0[None, None], 1)
+    assert np.allclose(z[0], W0 @ q[0], atol=1e-12)
+    assert np.allclose(z[1:], r["z"][0, 0][:-1], atol=1e-12)
     assert np.allclose(W, r["W"][0, 0], atol=1e-12)
 
 
@@ -57,8 +88,9 @@ def test_orthonormal_keys_closed_form():
     M_end = g[-1] * Mc + sum((g[-1] / g[s]) * np.outer(w[s], k[s]) for s in range(n))
     assert np.allclose(W, M_end, atol=1e-12)
     for t in range(n):
-        Mt = g[t] * Mc + sum((g[t] / g[s]) * np.outer(w[s], k[s]) for s in range(t + 1))
-        assert np.allclose(z[t], Mt @ q[t], atol=1e-12)
+        # the read of token t sees the memory before its write (step t - 1)
+        Mprev = gprev[t] * Mc + sum((gprev[t] / g[s]) * np.outer(w[s], k[s]) for s in range(t))
+        assert np.allclose(z[t], Mprev @ q[t], atol=1e-12)
 
 
 @pytest.mark.parametrize("T,chunk", [(23, 8), (16, 16), (9, 4)])
@@ -86,8 +118,8 @@ def test_chunk_form_with_triangular_solve(T, chunk):
                 Lm[t, s] = et[t] * (gprev[t] / g[s]) * KK[s, t]
         R = -et[:, None] * (gprev[:, None] * (K @ M.T) + (K @ M.T) - V)
         Wv = scipy.linalg.solve_triangular(np.eye(n) + Lm, R, lower=True, unit_diagonal=True)
-        D = np.tril(g[:, None] / g[None, :])      # gamma_t / gamma_s for s <= t
-        zs.append(g[:, None] * (Q @ M.T) + (D * (Q @ K.T)) @ Wv)
+        D = np.tril(gprev[:, None] / g[None, :], -1)   # gamma_{t-1} / gamma_s for s < t
+        zs.append(gprev[:, None] * (Q @ M.T) + (D * (Q @ K.T)) @ Wv)
         M = g[-1] * M + ((g[-1] / g)[:, None] * Wv).T @ K
     assert np.allclose(z, np.concatenate(zs), atol=1e-11)
     assert np.allclose(W, M, atol=1e-11)
