@@ -78,27 +78,39 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def roof(flops: float, nbytes: float, kernel_s: float, fp32_kernel: bool) -> dict:
+    """The roofline of the scan's target: t_roof is the slower of the
+    algorithmic bytes at the measured HBM copy bandwidth and the algorithmic
+    FLOPs at the measured dense bf16 tensor peak, whatever unit the kernel
+    computes on; frac = t_roof / measured time.  A kernel that computes on the
+    fp32 CUDA cores also reports its fraction of the fp32 FMA peak, as a
+    secondary figure only."""
+    peaks, src = load_peaks()
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        r = {"bound": "hbm", "achieved": nbytes / kernel_s / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / kernel_s / 1e12,
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["t_roof_s"] = max(t_hbm, t_tc)
+    r["peak_source"] = src
+    if fp32_kernel:
+        alu = fp32_alu_peak_tflops(2070.0)
+        r["fp32_alu"] = {"achieved": flops / kernel_s / 1e12, "peak": alu, "unit": "TFLOP/s",
+                         "frac": flops / kernel_s / 1e12 / alu,
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz"}
+    r["algorithmic_bytes"] = nbytes
+    r["algorithmic_flops"] = flops
+    return r
+
+
 def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
     a = algorithmic(w)
-    peaks, src = load_peaks()
-    t_hbm = a["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    # the CUDA-core kernels compute in fp32: their compute roof is the FMA pipe
-    simt = kernel_name.endswith("_simt")
-    flop_peak = fp32_alu_peak_tflops(2070.0) if simt else peaks["bf16_tflops"]
-    t_tc = a["flops"] / (flop_peak * 1e12)
-    if t_hbm >= t_tc:
-        achieved = a["bytes"] / kernel_s / 1e9
-        r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        achieved = a["flops"] / kernel_s / 1e12
-        r = {"bound": "alu" if simt else "tensor", "achieved": achieved, "peak": flop_peak,
-             "unit": "TFLOP/s"}
-    r["frac"] = r["achieved"] / r["peak"]
-    r["peak_source"] = ("derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz"
-                        if r["bound"] == "alu" else src)
+    r = roof(a["flops"], a["bytes"], kernel_s, kernel_name.endswith("_simt"))
     r["kernel"] = kernel_name
-    r["algorithmic_bytes"] = a["bytes"]
-    r["algorithmic_flops"] = a["flops"]
     r["traffic"] = profiled_traffic(kernel_name, w)
     return r
 
@@ -384,9 +396,6 @@ def run_bwd(args, rank, world, dev):
                "steps": args.e2e_steps, "ms_per_step": ems}
 
     alg = bwd_algorithmic(w)
-    mhz = clocks.get("sm_mhz") or 2070.0
-    peak = fp32_alu_peak_tflops(mhz)
-    achieved = alg["flops"] / (ms / 1e3) / 1e12
     line = {
         "metric": "gradient tokens/s (ttm_titans_bwd: dq, dk, dv, gates, W0) on 1 GB300",
         "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
@@ -398,11 +407,8 @@ def run_bwd(args, rank, world, dev):
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (no flush needed)", "kernel": "linear_bwd",
                    "workspace_bytes": int(ws_bytes)},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "peak_source": f"derived: 152 SMs x 128 fp32 lanes x 2 x {mhz:.0f} MHz",
-                     "kernel": "linear_bwd (all passes)", "algorithmic_flops": alg["flops"],
-                     "algorithmic_bytes": alg["bytes"], "traffic": None},
+        "roofline": dict(roof(alg["flops"], alg["bytes"], ms / 1e3, True),
+                         kernel="linear_bwd (all passes)", traffic=None),
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -694,9 +700,10 @@ def alloc_outputs(w: wl.Workload, dev, pin=False) -> dict:
     return o
 
 
-def oracle_sample(w: wl.Workload, inp: dict, T_s: int) -> dict:
+def oracle_sample(w: wl.Workload, inp: dict, T_s: int, keep: dict | None = None) -> dict:
     """Time the float64 oracle, as it stands, on every (b, h) of the workload
-    but only its first T_s tokens."""
+    but only its first T_s tokens.  If `keep` is a dict, the oracle's reads z
+    of those tokens are stored in keep["z"] (for the parity figures)."""
     import oracle
     f = lambda t: None if t is None else t[:, :, :T_s].double().numpy()
     t0 = time.perf_counter()
@@ -710,6 +717,8 @@ def oracle_sample(w: wl.Workload, inp: dict, T_s: int) -> dict:
                                  inp["W0"].double().numpy(), w.chunk, eta=f(inp["eta"]),
                                  alpha=f(inp["alpha"]), shared_over_batch=w.w0_shared)
     dt = time.perf_counter() - t0
+    if keep is not None:
+        keep["z"] = r["z"]
     tokens = w.B * w.H * min(T_s, w.T)
     return {"value": tokens / dt, "unit": UNIT, "cores": int(r["threads"]), "kind": "oracle",
             "seconds": dt,
@@ -730,8 +739,13 @@ def oracle_tokens_for(w: wl.Workload, seconds: float) -> int:
 def run_ours(args, rank, world, dev):
     import test_neural_memory_gb300 as ttm
 
-    w = workload_of(args)
-    inp = wl.generate(w)
+    w_full = workload_of(args)
+    inp = wl.generate(w_full)
+    if args.shard == "bh":
+        lo, hi = shard_bh(w_full.B, w_full.H, rank, world)
+        w, inp = shard_inputs(w_full, inp, lo, hi)
+    else:
+        w = w_full
     stream = torch.cuda.current_stream(dev)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     outs = alloc_outputs(w, dev)
@@ -775,14 +789,18 @@ def run_ours(args, rank, world, dev):
     # end to end through the public API with host buffers
     e2e = run_e2e(args, w, inp, dev, stream, world) if args.e2e_steps > 0 else None
 
-    value = w.tokens * world * args.steps / (total_ms / 1e3)
+    sharded = args.shard == "bh"
+    job_tokens = w_full.tokens if sharded else w.tokens * world
+    value = job_tokens * args.steps / (total_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+        "scaling": "strong" if sharded else "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w_full.name, "B": w_full.B, "H": w_full.H, "T": w.T, "d": w.d,
                    "chunk": w.chunk, "kind": w.kind, "hidden": w.hidden or None,
-                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "parallelism": (f"bh-shard{world}" if sharded else
+                                   (f"replicas{world}" if world > 1 else "single-gpu")),
                    "l2": "inputs larger than L2 (no flush needed)"
                    if algorithmic(w)["bytes"] > 129e6 else "L2 not flushed: inputs fit in L2",
                    "kernel": kernel_name},
@@ -791,8 +809,29 @@ def run_ours(args, rank, world, dev):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         T_s = oracle_tokens_for(w, args.cpu_seconds)
-        line["cpu_baseline"] = oracle_sample(w, inp, T_s)
+        keep = {}
+        line["cpu_baseline"] = oracle_sample(w, inp, T_s, keep)
+        line["parity"] = parity_of(outs["z"][:, :, :T_s], keep["z"], w.dtype)
     return line
+
+
+def parity_of(z_gpu, z_ref, dtype: str) -> dict:
+    """The GPU reads of the timed call against the oracle's on the tokens the
+    CPU baseline ran (a prefix of every sequence: the scan is causal, so the
+    full-length call's first tokens are exactly the oracle's case).  Normwise
+    max|gpu - oracle| / max|oracle| is the pass criterion; the elementwise
+    error with a 1e-6 max floor is reported beside it."""
+    import numpy as np
+    g = z_gpu.detach().double().cpu().numpy()
+    r = np.asarray(z_ref, dtype=np.float64)
+    scale = float(np.abs(r).max()) if r.size else 0.0
+    diff = np.abs(g - r)
+    normwise = float(diff.max() / scale) if scale > 0 else float(diff.max(initial=0.0))
+    elem = float((diff / (np.abs(r) + 1e-6 * scale)).max()) if scale > 0 else normwise
+    tol = 2e-2 if dtype == "bf16" else 1e-4
+    return {"output": "z", "tokens_checked": int(r.shape[0] * r.shape[1] * r.shape[2]),
+            "normwise": normwise, "elementwise_floor_1e-6": elem, "tol_normwise": tol,
+            "pass": normwise <= tol}
 
 
 E2E_SEGMENT = 8192   # tokens per segment of the host-buffer scan
@@ -922,6 +961,33 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------
 
+def shard_bh(B: int, H: int, rank: int, world: int) -> tuple[int, int]:
+    """The (b, h) sequences of rank `rank` under --shard bh: a contiguous,
+    balanced range [lo, hi) of the flat unit index b * H + h.  The sequences
+    are independent, so each rank scans its own with no exchange."""
+    n = B * H
+    base, extra = divmod(n, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def shard_inputs(w: wl.Workload, inp: dict, lo: int, hi: int) -> tuple[wl.Workload, dict]:
+    """Inputs of units lo..hi-1 as one batch row of hi - lo heads: q, k, v and
+    gates [1, n, T, .], the initial memory of each unit gathered to [1, n, ...]
+    (a shared initial memory is expanded per unit)."""
+    n = hi - lo
+    flat = lambda t: None if t is None else t.reshape(w.B * w.H, *t.shape[2:])[lo:hi].unsqueeze(0)
+    out = {k: flat(inp[k]) for k in ("q", "k", "v", "theta", "eta", "alpha")}
+    heads = torch.arange(lo, hi) % w.H
+    batch = torch.arange(lo, hi) // w.H
+    for k in ("W0", "W1_0", "W2_0"):
+        if k in inp:
+            t = inp[k]
+            out[k] = (t[0, heads] if w.w0_shared else t[batch, heads]).unsqueeze(0).contiguous()
+    out = {k: (None if v is None else v.contiguous()) for k, v in out.items()}
+    return w.shrink(B=1, H=n, w0_shared=False), out
+
+
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
@@ -953,6 +1019,9 @@ def main():
                     help="decode: the streaming decode step; bwd: the scan's gradient; "
                          "dgd: the DGD-memory scan; layer: the LMM layer")
     ap.add_argument("--decode-tokens", type=int, default=1, help="tokens per decode call")
+    ap.add_argument("--shard", choices=["none", "bh"], default="none",
+                    help="bh: split the workload's (b, h) sequences over the ranks "
+                         "(strong scaling, no exchange); none: one replica per rank")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.ttm_set_kernel_policy.restype = i
         L.ttm_last_kernel.restype = i
         L.ttm_device_status.restype = i
+        L.ttm_cuda_device_count.restype = i
+        L.ttm_debug_set.argtypes = [i, ctypes.c_longlong]
+        L.ttm_debug_set.restype = i
         L.ttm_launch_count.restype = ctypes.c_ulonglong
         _lib = L
     return _lib
@@ -115,6 +118,19 @@ def launch_count() -> int:
 
 def device_status() -> int:
     return lib().ttm_device_status()
+
+
+DEBUG = {"wait_cycles": 1, "stall_chunk": 2, "fail_calls": 3}
+
+
+def debug_set(option: str, value: int) -> None:
+    """Failure-detection test hooks of the library (see ttm_debug_set)."""
+    _check(lib().ttm_debug_set(DEBUG[option], int(value)), "ttm_debug_set")
+
+
+def cuda_device_count() -> int:
+    """CUDA devices the library's own runtime can reach (0 without a GPU)."""
+    return int(lib().ttm_cuda_device_count())
 
 
 def _ptr(t):

@@ -28,6 +28,14 @@ struct LinearArgs {
     // Chunk-shared gates: theta / eta / alpha hold one value per (sequence,
     // chunk), [B][H][ceil(T / chunk)], instead of one per token.
     int gates_per_chunk;
+    // Limit of every bounded wait of the tensor-core kernels, in SM clock
+    // cycles (0: the default, about 2 s).
+    long long wait_cycles;
+    // Failure-detection test hook of the tensor-core scan (0: off).  With
+    // c + 1 the producer announces 16 bytes more for chunk c's tiles than it
+    // copies, so that chunk's barrier never completes and every wait on it
+    // runs out: the kernel then reports TTM_ERR_TIMEOUT and unwinds.
+    int debug_stall;
 };
 
 // Index of token t's gate of sequence seq (per token, or per chunk).

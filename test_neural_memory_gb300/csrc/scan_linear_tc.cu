@@ -111,6 +111,7 @@ struct Bars {
     uint64_t acc1_ready[2], acc1_free[2], sc_ready[2], am_ready[2];
     uint64_t mma3_done[2], acc3_free[2], mma2_done[2], acc2_free[2], mma3_issued;
     uint64_t drain[4];
+    long long wait_limit;   // SM clock cycles a wait may take before it gives up
     uint32_t tmem_base;
     int abort;
 };
@@ -142,17 +143,18 @@ struct TcParams {
     int nslices;
 };
 
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr long long kWaitCycles = 4000000000LL;  // default limit, ~2 s at 2 GHz
 
 // Bounded wait that also gives up once another role has aborted (the slow
 // path, out of line: ~25 call sites share one copy of it).
 __device__ __noinline__ bool wait_bar_slow(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
     const long long t0 = clock64();
+    const long long limit = B->wait_limit;
     uint32_t polls = 0;
     while (!mbar_try_wait_sleep(bar, parity, 20000)) {
         if ((++polls & 3u) == 0) {
             if (*(volatile int*)&B->abort) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *(volatile int*)&B->abort = 1;
                 atomicExch(status, TTM_ERR_TIMEOUT);
                 return false;
@@ -181,10 +183,10 @@ __device__ __forceinline__ bool wait_all(Bars* B, uint64_t* bar, uint32_t parity
 }
 
 // Wait used while draining: ignores the abort flag, gives up after the limit.
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kWaitCycles) break;
+        if (clock64() - t0 > limit) break;
 }
 
 // One arrival for the whole warp, after every lane's prior work (the lanes
@@ -382,6 +384,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         mbar_init(&B->am_ready[1], 4);
         mbar_init(&B->mma3_issued, 1);           // chain MMA queued (carry MMA goes after it)
         for (int i = 0; i < 4; ++i) mbar_init(&B->drain[i], 1);
+        B->wait_limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
         B->abort = 0;
         fence_mbar_init();
     }
@@ -725,7 +728,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 const int st = c % kNS;
                 prefetch(c + kPrefetch);
                 if (c >= kNS && !wait_bar(B, &B->empty[st], ((c / kNS) - 1) & 1, status)) break;
-                const uint32_t tx = (st == 0 ? 3 : 2) * NH * kTile + kChunk * kRows * 2 + kRecBytes;
+                const uint32_t tx = (st == 0 ? 3 : 2) * NH * kTile + kChunk * kRows * 2 + kRecBytes +
+                                    (c + 1 == a.debug_stall ? 16u : 0u);
                 mbar_expect_tx(&B->full[st], tx);
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
@@ -740,7 +744,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             // drain: every issued stage's copies must have landed before exit
             for (int c = (issued > kNS ? issued - kNS : 0); c < issued; ++c)
-                wait_drain(&B->full[c % kNS], (c / kNS) & 1);
+                wait_drain(&B->full[c % kNS], (c / kNS) & 1, B->wait_limit);
         }
         __syncwarp();
     }
@@ -750,7 +754,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         uint64_t* d = &B->drain[warp == 0 ? 0 : (warp == 6 ? 1 : (warp == 7 ? 3 : 2))];
         if (elect_one()) mma_commit(d);
         __syncwarp();
-        if (lane == 0) wait_drain(d, 0);
+        if (lane == 0) wait_drain(d, 0, B->wait_limit);
         __syncwarp();
     }
     tc_fence_before();

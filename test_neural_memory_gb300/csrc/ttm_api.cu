@@ -2,8 +2,10 @@
 // launch.  Declarations and the full contract are in include/ttm.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/ttm.h"
 #include "kernels.h"
@@ -15,14 +17,30 @@ __device__ int g_status_word;
 
 constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices];  // per-device address of g_status_word
+std::mutex g_status_mu;          // guards the first lookup on each device
 
 int g_policy = TTM_KERNEL_AUTO;
+
+// Failure-detection test hooks (ttm_debug_set).
+std::atomic<long long> g_wait_cycles{0};   // bounded-wait limit of the tensor-core kernels
+std::atomic<int> g_stall_chunk{-1};        // next tensor-core linear scan: chunk that stalls
+std::atomic<int> g_fail_calls{0};          // scan calls still to fail before their launch
+
+// Host-side fault injection: true when this call must report a failed launch
+// (the hook counts down one call each time).
+bool injected_failure() {
+    int n = g_fail_calls.load();
+    while (n > 0)
+        if (g_fail_calls.compare_exchange_weak(n, n - 1)) return true;
+    return false;
+}
 unsigned long long g_launches = 0;
 thread_local int t_last_kernel = TTM_KID_NONE;
 
 int* status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
     if (!g_status_ptr[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
@@ -142,8 +160,11 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
         (!workspace || workspace_bytes < ttm::linear_tc_workspace_bytes(a)))
         return TTM_ERR_INVALID_ARG;
 
+    if (injected_failure()) return TTM_ERR_CUDA;
     a.status = status_ptr();
     if (!a.status) return TTM_ERR_CUDA;
+    a.wait_cycles = g_wait_cycles.load();
+    if (kid == TTM_KID_LINEAR_TC) a.debug_stall = g_stall_chunk.exchange(-1) + 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = kid == TTM_KID_LINEAR_TC ? ttm::linear_tc_launch(a, s)
                                                    : ttm::linear_simt_launch(a, s);
@@ -326,6 +347,7 @@ int ttm_mlp_fwd(int B, int H, int T, int d, int hidden, int chunk, int dtype, co
 
     const int kid = select_mlp(a);
     if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+    if (injected_failure()) return TTM_ERR_CUDA;
     a.status = status_ptr();
     if (!a.status) return TTM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -600,6 +622,30 @@ int ttm_set_kernel_policy(int policy) {
 int ttm_last_kernel(void) { return t_last_kernel; }
 
 unsigned long long ttm_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+int ttm_debug_set(int option, long long value) {
+    switch (option) {
+        case TTM_DBG_WAIT_CYCLES:
+            if (value < 0) return TTM_ERR_INVALID_ARG;
+            g_wait_cycles = value;
+            return TTM_OK;
+        case TTM_DBG_STALL_CHUNK:
+            if (value < -1 || value > (1LL << 30)) return TTM_ERR_INVALID_ARG;
+            g_stall_chunk = (int)value;
+            return TTM_OK;
+        case TTM_DBG_FAIL_CALLS:
+            if (value < 0 || value > (1LL << 30)) return TTM_ERR_INVALID_ARG;
+            g_fail_calls = (int)value;
+            return TTM_OK;
+        default: return TTM_ERR_INVALID_ARG;
+    }
+}
+
+int ttm_cuda_device_count(void) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) return 0;
+    return n;
+}
 
 int ttm_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return TTM_ERR_CUDA;

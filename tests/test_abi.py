@@ -38,10 +38,18 @@ def test_policy_round_trip(L):
 
 
 # Fake device addresses: validation must reject every call that gets them
-# before any use.  Tests that pass them run only where no GPU is reachable, so
-# that a regression in validation can never launch a kernel on them.
+# before any use, and no test hands them to a call that would pass validation.
+# Tests that pass them run only where the library's own runtime reaches no
+# GPU (torch may not see a device that the statically linked runtime does).
 A = 1 << 20
-host_only = pytest.mark.skipif(torch.cuda.is_available(),
+
+
+def _no_gpu_reachable() -> bool:
+    ttm.build()
+    return ttm.cuda_device_count() == 0 and not torch.cuda.is_available()
+
+
+host_only = pytest.mark.skipif(not _no_gpu_reachable(),
                                reason="passes fake device addresses; host-only")
 
 
@@ -111,8 +119,11 @@ def test_workspace_size_and_checks(L):
 
 
 @host_only
-def test_valid_call_without_gpu_reports_cuda_error(L):
-    assert lin_call(L) == CUDA
+def test_no_device_is_reported_without_any_address(L):
+    # with no reachable device the library's own queries fail cleanly: the
+    # device count is 0 and the status query reports a CUDA error
+    assert L.ttm_cuda_device_count() == 0
+    assert ttm.device_status() == CUDA
 
 
 def test_python_layer_raises(L):
@@ -143,11 +154,6 @@ def test_step_rejects_malformed(L):
     assert step_call(L, dk=520) == UNSUPPORTED          # one warp per row holds <= 512 columns
     assert L.ttm_linear_step(1, 1, 1, 64, 64, 4, 5, 1, P(0), P(1), P(2), P(3), P(4), P(5),
                              P(6), None) == INVALID
-
-
-@host_only
-def test_step_valid_call_without_gpu_reports_cuda_error(L):
-    assert step_call(L, eta=P(7), S=P(8), alpha=P(9)) == CUDA
 
 
 def bwd_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=4, dt=1, q=P(0), k=P(1), v=P(2), eta=None,
@@ -193,7 +199,3 @@ def test_bwd_workspace_size(L):
         assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 0, 0) ==
                 2 * 3 * 3 * per_chunk)                         # fp32: CUDA-core forward
 
-
-@host_only
-def test_bwd_valid_call_without_gpu_reports_cuda_error(L):
-    assert bwd_call(L) == CUDA

@@ -27,18 +27,27 @@ def test_mlp_workload_flops():
     assert abs(a["flops"] / 1e9 - 399.43) < 0.01
 
 
-def test_roof_per_kernel_kind():
+def test_roof_is_the_slower_of_hbm_and_bf16_for_every_kernel():
+    peaks, _ = bench.load_peaks()
     w4, w5 = wl.WORKLOADS[4], wl.WORKLOADS[5]
+    a4, a5 = bench.algorithmic(w4), bench.algorithmic(w5)
     r = bench.roofline(w4, 2.445e-3, "linear_tc")
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
-    assert abs(r["achieved"] - bench.algorithmic(w4)["bytes"] / 2.445e-3 / 1e9) < 1e-6
-    # the fp32 CUDA-core kernels are measured against the FMA pipe, not the tensor cores
+    assert abs(r["achieved"] - a4["bytes"] / 2.445e-3 / 1e9) < 1e-6
+    t_roof = max(a4["bytes"] / (peaks["hbm_gbs"] * 1e9), a4["flops"] / (peaks["bf16_tflops"] * 1e12))
+    assert abs(r["frac"] - t_roof / 2.445e-3) < 1e-12
+    # a CUDA-core kernel is measured against the same roof: for the 2-layer
+    # memory that is the bf16 tensor peak (399.4 GFLOP / 1909.9 TFLOP/s = 209 us)
     r = bench.roofline(w5, 24.15e-3, "mlp_simt")
-    assert r["bound"] == "alu" and abs(r["peak"] - 152 * 128 * 2 * 2070e6 / 1e12) < 1e-9
-    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
-    # the tensor-core MLP kernel against the bf16 tensor peak
+    assert r["bound"] == "tensor" and r["peak"] == peaks["bf16_tflops"]
+    t_roof = a5["flops"] / (peaks["bf16_tflops"] * 1e12)
+    assert abs(r["t_roof_s"] - t_roof) < 1e-15 and abs(r["frac"] - t_roof / 24.15e-3) < 1e-12
+    # its fraction of the fp32 FMA pipe is only a secondary field
+    alu = r["fp32_alu"]
+    assert abs(alu["peak"] - 152 * 128 * 2 * 2070e6 / 1e12) < 1e-9
+    assert abs(alu["frac"] - a5["flops"] / 24.15e-3 / 1e12 / alu["peak"]) < 1e-12
     r = bench.roofline(w5, 5.53e-3, "mlp_tc")
-    assert r["bound"] == "tensor"
+    assert r["bound"] == "tensor" and "fp32_alu" not in r
 
 
 def test_fp32_alu_peak():

@@ -17,7 +17,14 @@ from tests import helpers as H
 
 INVALID = ttm.ERR_INVALID_ARG
 gpu = pytest.mark.gpu
-host_only = pytest.mark.skipif(torch.cuda.is_available(),
+
+
+def _no_gpu_reachable() -> bool:
+    ttm.build()
+    return ttm.cuda_device_count() == 0 and not torch.cuda.is_available()
+
+
+host_only = pytest.mark.skipif(not _no_gpu_reachable(),
                                reason="passes fake addresses; host-only")
 
 

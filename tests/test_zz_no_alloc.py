@@ -4,8 +4,11 @@ Such a caller only has its inputs and outputs and may not call cudaMalloc, so
 it cannot hand ttm_titans_fwd the workspace its tensor-core path needs; the
 no-alloc entry point takes that scratch from a fixed 16 MiB block inside the
 library instead.  These tests call it through the C ABI and check that two
-calls in a row give what ttm_titans_fwd gives on the same inputs, and that a
-call needing more scratch than the block holds is refused.
+calls in a row give what ttm_titans_fwd gives on the same inputs (bit for bit:
+both run the same kernels on the same inputs, so any difference would be a
+scratch mix-up), that the shape really goes through the scratch-using
+tensor-core kernel, and that a call needing more scratch than the block holds
+is refused.
 """
 import ctypes
 
@@ -55,14 +58,19 @@ def test_noalloc_matches_titans_fwd_twice(L):
                                     chunk=64, seed=seed)
         d = H.to_dev(inp)
         S0 = 0.01 * torch.randn((w.B, w.H, w.d, w.d), device="cuda")
+        # the shape needs scratch, so the block inside the library is in use
+        assert ttm.linear_workspace_size(w.B, w.H, w.T, w.d, w.d, w.chunk, ttm.BF16) > 0
         rc, z, W, S = _noalloc(L, w, d, S0)
         torch.cuda.synchronize()
         assert rc == ttm.OK, ttm.status_str(rc)
+        assert ttm.last_kernel() == "linear_tc"
         z_ref, W_ref, S_ref = ttm.titans_fwd(d["q"], d["k"], d["v"], d["theta"], d["W0"],
                                              w.chunk, eta=d["eta"], alpha=d["alpha"], S0=S0)
         torch.cuda.synchronize()
+        assert ttm.last_kernel() == "linear_tc"
         for a, b in ((z, z_ref), (W, W_ref), (S, S_ref)):
             assert H.max_rel(H.f64(a), H.f64(b)) <= H.TOL["bf16"]
+            assert torch.equal(a, b)
     assert ttm.device_status() == ttm.OK
 
 
