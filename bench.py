@@ -118,6 +118,7 @@ def roofline(w: wl.Workload, kernel_s: float, kernel_name: str) -> dict:
 def kernel_source_digest(kernel_name: str) -> str:
     src = {"linear_simt": ["scan_simt.cu"], "mlp_simt": ["scan_simt.cu", "scan_mlp_simt.cu", "scan_mlp_cluster.cu"],
            "linear_tc": ["scan_linear_tc.cu"], "mlp_tc": ["scan_mlp_tc.cu"],
+           "linear_seq": ["scan_linear_seq.cu"],
            "linear_step": ["step.cu"]}.get(kernel_name)
     if not src:
         return ""

@@ -87,7 +87,9 @@ typedef enum {
     TTM_KID_LINEAR_SIMT = 1,   /* fp32 CUDA-core chunked scan, linear memory */
     TTM_KID_MLP_SIMT = 2,      /* fp32 CUDA-core chunked scan, 2-layer memory */
     TTM_KID_LINEAR_TC = 3,     /* tcgen05 + TMA chunked scan, linear memory */
-    TTM_KID_MLP_TC = 4         /* tcgen05 chunked scan, 2-layer memory */
+    TTM_KID_MLP_TC = 4,        /* tcgen05 chunked scan, 2-layer memory */
+    TTM_KID_LINEAR_SEQ = 5     /* tcgen05 + TMA scan, one CTA per sequence, d = 64,
+                                  gradient points every 16 or 32 tokens */
 } ttm_kernel_id;
 
 /*
@@ -99,6 +101,11 @@ typedef enum {
  *   z: [B][H][T][dv] in dtype.
  * Shapes: B, H >= 1; T >= 0; dk, dv >= 1 (multiples of 8 for TTM_BF16,
  * of 4 for TTM_F32); chunk >= 1.
+ * Kernels (policy AUTO): bf16 with dk = dv in {64, 128} and chunk 64 run the
+ * tcgen05 row-slice scan (workspace below); bf16 with dk = dv = 64 and chunk
+ * 16 or 32 run the tcgen05 scan with one CTA per sequence, whose 64-token
+ * tiles solve the tile's unit block-lower-triangular error system in the key
+ * products (no workspace); everything else runs the fp32 CUDA-core scan.
  */
 int ttm_linear_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                    const void* q, const void* k, const void* v,

@@ -21,7 +21,8 @@ from ._build import LIB, ROOT, build  # noqa: F401  (build is part of the public
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
 F32, BF16 = 0, 1
 POLICY = {"auto": 0, "simt": 1, "tc": 2}
-KERNEL_NAMES = {0: "none", 1: "linear_simt", 2: "mlp_simt", 3: "linear_tc", 4: "mlp_tc"}
+KERNEL_NAMES = {0: "none", 1: "linear_simt", 2: "mlp_simt", 3: "linear_tc", 4: "mlp_tc",
+                5: "linear_seq"}
 
 _lib = None
 

@@ -136,6 +136,17 @@ bool linear_tc_supported(const LinearArgs& a);
 size_t linear_tc_workspace_bytes(const LinearArgs& a);
 cudaError_t linear_tc_launch(const LinearArgs& a, cudaStream_t s);
 
+// 3-D TMA map (a CUtensorMap, passed as void*) of a bf16 tensor viewed as
+// [BH sequences][T tokens][D], tile box {bx, 64 tokens, 1}, optionally with the
+// 128-byte swizzle (scan_linear_tc.cu).
+bool make_token_tile_map(void* map, const void* ptr, int BH, int T, int D, int bx, bool swz);
+
+// tcgen05 + TMA kernel with one CTA per sequence for d_k = d_v = 64
+// (scan_linear_seq.cu): 64-token tiles whose gradient points fall every
+// `chunk` in {16, 32} tokens; no workspace.
+bool linear_seq_supported(const LinearArgs& a);
+cudaError_t linear_seq_launch(const LinearArgs& a, cudaStream_t s);
+
 // tcgen05 + TMA kernel for the 2-layer MLP memory (scan_mlp_tc.cu): bf16,
 // d = 64, hidden = 256, chunk 16; one cluster of two CTAs per sequence.
 bool mlp_tc_supported(const MlpArgs& a);

@@ -1,0 +1,799 @@
+// Tensor-core (tcgen05 + TMA) scan of the linear / Titans memory for
+// d_k = d_v = 64 with one CTA per sequence, in 64-token tiles whose gradient
+// points fall every b in {16, 32} tokens (mini-batch TTT with b = 16 is the
+// TTT-Linear setting, "TTT layers 与 fast weights" §1.1 eqs (6)-(9)).
+//
+// Method.  Let tile g hold tokens t = 0..n-1 (n <= 64) with the state (W_g, S_g)
+// at its start, keys K, queries Q, values V (rows = tokens) and the tile's
+// decay / momentum coefficients beta_t, c_t, C[t][s] ("论文速览 | Titans"
+// §4.3-§4.5; C[t][s] = theta_s w(s, t) is the weight of token s's gradient in
+// the state after token t).  Token t takes its gradient at the state left
+// before its sub-chunk, which starts at sigma(t) = b floor(t / b), so
+//
+//   e_t = beta'_t W_g k_t + c'_t S_g k_t - v_t
+//         - 2 sum_{s < sigma(t)} C[sigma(t)-1][s] (k_s . k_t) e_s,
+//   beta'_t = beta_{sigma(t)-1} (1 for sigma = 0), c'_t = c_{sigma(t)-1} (0).
+//
+// In matrix form (I + L) E = R0 with R0 = diag(beta') K W^T + diag(c') K S^T - V
+// and L[t][s] = 2 C[sigma(t)-1][s] (k_s . k_t), strictly block-lower with
+// b x b blocks, so E = N R0 with N = (I + L)^-1 = (I - L)(I + L^2) (at most four
+// blocks: L^4 = 0).  The reads and the carry are the chunk form of the tile:
+//
+//   Z       = diag(beta) Q W^T + diag(c) Q S^T - 2 (A~ N) R0,
+//             A~ = mask_{s<=t}(Q K^T) o C
+//   W_{g+1}^T = beta_n W^T + c_n S^T - 2 (K^T diag(C[n-1]) N) R0
+//   S_{g+1}^T = P_n S^T            - 2 (K^T diag(Pm)     N) R0,
+//             Pm[s] = theta_s prod_{j=s+1..n-1} eta_j.
+//
+// E itself is never formed: A~ N, Y_C = K^T diag(C[n-1]) N and
+// Y_P = K^T diag(Pm) N depend only on the tile's inputs and gates, so the
+// state's own chain per tile is two tensor-core products,
+//   C1: [Q; K] [W; S]^T      (reads and the state part of R0),
+//   C3: [A~N; Y_C; 0; Y_P] R0 (the read correction and the carry),
+// with an epilogue after each; everything else is prepared beside it.
+//
+// Roles (448 threads, one CTA per (b, h) sequence, all 64 rows of the state):
+//   warps 0,1,4,5   reads: token t = TMEM lane 0..63, 32 columns each
+//   warps 2,3,6,7   state: E1 (R0 for token = TMEM lane 64..127) and E3 (the
+//                   update; thread j holds W[r][j], S[r][j] for 32 rows r in
+//                   fp32 registers and writes their bf16 copy)
+//   warps 8-11      preparation of the next tile: gates, coefficient scans,
+//                   scores [Q; K] K^T (MMA), the weighted rows of A~ and L,
+//                   N applied to [A~; K^T diag C; K^T diag Pm] by two MMA rounds
+//   warp 12         TMA producer (Q, K, V tiles of 64 tokens, three stages)
+//   warp 13         issues C1 and C3
+// Every wait is bounded; a wait that runs out sets the status word, all roles
+// run out their loops without further work, copies and MMAs drain, TMEM is
+// freed and the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "../../include/ttm.h"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace ttm {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 64;              // d_k = d_v
+constexpr int kTile = 64;           // tokens per tile
+constexpr int kThreads = 448;
+constexpr int kNS = 3;              // input stages
+constexpr uint32_t kTileBytes = 8192;                 // 64 rows x 128 bytes of bf16
+constexpr uint32_t kStageBytes = 3 * kTileBytes;      // Q, K, V
+constexpr uint32_t kOpBytes = 32768;                  // a 256-row A operand
+constexpr uint32_t kTmemCols = 512;
+
+// TMEM columns
+constexpr uint32_t kC1 = 0;      // [Q; K] [W; S]^T: 64 (W) + 64 (S) columns
+constexpr uint32_t kC3 = 128;    // [A~N; Y_C] R0 (64) and [0; Y_P] R0 (64)
+constexpr uint32_t kP1 = 256;    // 2 x 64: [Q; K] K^T of two tiles
+constexpr uint32_t kPR = 384;    // preparation rounds: 2 x 64
+
+// Per-tile vectors (floats) in a slot of shared memory.
+constexpr int vTh = 0, vEt = 64, vKp = 128, vBeta = 192, vCv = 256, vBp = 320, vCp = 384,
+              vCn = 448, vPm = 512, vScal = 576;     // scal: beta_n, c_n, P_n, n
+constexpr uint32_t kVecBytes = 4096;
+
+struct Bars {
+    uint64_t full[kNS], empty[kNS];
+    uint64_t c1_done, c1_free, r0_ready, c3_free, ws_ready, pr_done;
+    uint64_t ay_ready[2], c3_done[2], vec_ready[2], vec_free[2], p1_done[2];
+    uint64_t drain[2];
+    long long wait_limit;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct Layout {
+    uint32_t stages, ay, ap, r0, ws, il, b2, vec, bars, total;
+};
+
+__host__ __device__ constexpr Layout make_layout() {
+    Layout L{};
+    uint32_t o = 0;
+    L.stages = o; o += kNS * kStageBytes;
+    L.ay = o;     o += 2 * kOpBytes;       // A operand of C3 (two tiles in flight)
+    L.ap = o;     o += kOpBytes;           // between the two preparation rounds
+    L.r0 = o;     o += kTileBytes;         // R0 [s][r] (MN-major B)
+    L.ws = o;     o += 2 * kTileBytes;     // bf16 W^T [j][r] then S^T [j][r] (MN-major B)
+    L.il = o;     o += kTileBytes;         // (I - L) [s][u] (MN-major B)
+    L.b2 = o;     o += kTileBytes;         // (I + L^2) [s][u] (MN-major B)
+    L.vec = o;    o += 2 * kVecBytes;
+    L.bars = o;   o += (uint32_t)((sizeof(Bars) + 15) & ~size_t(15));
+    L.total = o;
+    return L;
+}
+
+constexpr long long kWaitCycles = 4000000000LL;   // default limit, ~2 s at 2 GHz
+
+__device__ __noinline__ bool wait_bar_slow(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    const long long t0 = clock64();
+    const long long limit = B->wait_limit;
+    uint32_t polls = 0;
+    while (!mbar_try_wait_sleep(bar, parity, 20000)) {
+        if ((++polls & 3u) == 0) {
+            if (*(volatile int*)&B->abort) return false;
+            if (clock64() - t0 > limit) {
+                *(volatile int*)&B->abort = 1;
+                atomicExch(status, TTM_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(B, bar, parity, status);
+}
+
+// Warp-uniform bounded wait (every lane gets the same answer).
+__device__ __noinline__ bool wait_all_slow(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    return __all_sync(0xffffffffu, wait_bar_slow(B, bar, parity, status));
+}
+
+__device__ __forceinline__ bool wait_all(Bars* B, uint64_t* bar, uint32_t parity, int* status) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return wait_all_slow(B, bar, parity, status);
+}
+
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) break;
+}
+
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 consecutive bf16 values of row `row` from column `col` (a multiple of 8)
+// of a 128-byte-swizzled tile.
+__device__ __forceinline__ void st_chunk(uint8_t* tile, int row, int col, const float* x) {
+    uint4 v;
+    v.x = pack_bf16(x[0], x[1]);
+    v.y = pack_bf16(x[2], x[3]);
+    v.z = pack_bf16(x[4], x[5]);
+    v.w = pack_bf16(x[6], x[7]);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col)) = v;
+}
+
+__device__ __forceinline__ void ld_chunk(const uint8_t* tile, int row, int col, float* x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128_offset(row, col));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
+    const uint16_t u = *reinterpret_cast<const uint16_t*>(tile + sw128_offset(row, col));
+    return __uint_as_float((uint32_t)u << 16);
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
+    uint32_t u[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]),
+          "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
+          "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]),
+          "=r"(u[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(u[i]);
+}
+
+// Inclusive scan of affine maps x -> A x + B along lanes (later lanes outside).
+__device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float A2 = __shfl_up_sync(0xffffffffu, A, off);
+        const float B2 = __shfl_up_sync(0xffffffffu, B, off);
+        if (lane >= off) {
+            B = A * B2 + B;
+            A = A * A2;
+        }
+    }
+}
+
+// Four K steps (K = 64) of one M = 128 MMA with both operands in shared memory.
+__device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, bool a_mn_major_b, uint32_t b,
+                                        uint32_t idesc) {
+    (void)a_mn_major_b;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(d, sdesc(a + kk * 32, 16, 1024, 2), sdesc(b + kk * 2048, 8192, 1024, 2), idesc,
+                 kk > 0);
+}
+
+template <bool kTitans>
+__global__ void __launch_bounds__(kThreads, 1)
+linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap, const LinearArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    constexpr Layout L = make_layout();
+    Bars* B = reinterpret_cast<Bars*>(sm + L.bars);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq = blockIdx.x;
+    const int bb = seq / a.H, hh = seq % a.H;
+    const int T = a.T;
+    const int nt = (T + kTile - 1) / kTile;
+    const int bsub = a.chunk;
+    int* status = a.status;
+
+    auto stage = [&](int s) { return sm + L.stages + s * kStageBytes; };   // Q | K | V
+    auto ay = [&](int s) { return sm + L.ay + s * kOpBytes; };
+    uint8_t* ap = sm + L.ap;
+    uint8_t* r0 = sm + L.r0;
+    uint8_t* wsW = sm + L.ws;
+    uint8_t* wsS = wsW + kTileBytes;
+    uint8_t* il = sm + L.il;
+    uint8_t* b2 = sm + L.b2;
+    auto vec = [&](int v) { return reinterpret_cast<float*>(sm + L.vec + v * kVecBytes); };
+
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&B->full[s], 1);
+            mbar_init(&B->empty[s], 2);        // state warps + preparation warps
+        }
+        mbar_init(&B->c1_done, 1);
+        mbar_init(&B->c1_free, 4);             // read warps
+        mbar_init(&B->r0_ready, 4);            // state warps
+        mbar_init(&B->c3_free, 4);             // read warps
+        mbar_init(&B->ws_ready, 4);            // state warps
+        mbar_init(&B->pr_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&B->ay_ready[i], 1);
+            mbar_init(&B->c3_done[i], 1);
+            mbar_init(&B->vec_ready[i], 1);
+            mbar_init(&B->vec_free[i], 8);     // read warps + state warps
+            mbar_init(&B->p1_done[i], 1);
+            mbar_init(&B->drain[i], 1);
+        }
+        B->wait_limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
+        B->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&B->tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem_base;
+    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);   // this warp's TMEM lanes
+
+    constexpr uint32_t idC1 = idesc_bf16_f32(128, kTitans ? 128 : 64, 0, 1);
+    constexpr uint32_t idK = idesc_bf16_f32(128, 64, 0, 0);   // B K-major
+    constexpr uint32_t idM = idesc_bf16_f32(128, 64, 0, 1);   // B MN-major
+
+    if (warp < 8 && (warp & 3) < 2) {
+        // ------------------------------------------------------------- reads
+        const int h = warp >> 2;
+        const int t = 32 * (warp & 3) + lane;
+        bool ok = true;
+        for (int g = 0; g < nt; ++g) {
+            const int v = g & 1;
+            const int n = min(kTile, T - g * kTile);
+            float qw[32], qs[32], dz[32];
+            if (ok) ok = wait_all(B, &B->c1_done, g & 1, status);
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(tl + kC1 + 32 * h, qw);
+                if (kTitans) tmem_ld32(tl + kC1 + 64 + 32 * h, qs);
+                tmem_wait_ld();
+                tc_fence_before();
+                warp_arrive(&B->c1_free);
+            }
+            if (ok) ok = wait_all(B, &B->vec_ready[v], (g >> 1) & 1, status);
+            float bt = 1.f, ct = 0.f;
+            if (ok) {
+                bt = vec(v)[vBeta + t];
+                if (kTitans) ct = vec(v)[vCv + t];
+            }
+            if (ok) ok = wait_all(B, &B->c3_done[v], (g >> 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(tl + kC3 + 32 * h, dz);
+                tmem_wait_ld();
+                tc_fence_before();
+                warp_arrive(&B->c3_free);
+                if (t < n) {
+                    uint4 o[4];
+                    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float z0 = bt * qw[2 * i] - 2.f * dz[2 * i];
+                        float z1 = bt * qw[2 * i + 1] - 2.f * dz[2 * i + 1];
+                        if (kTitans) {
+                            z0 += ct * qs[2 * i];
+                            z1 += ct * qs[2 * i + 1];
+                        }
+                        ow[i] = pack_bf16(z0, z1);
+                    }
+                    uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.z) +
+                                                         ((size_t)seq * T + (size_t)g * kTile + t) * kD +
+                                                         32 * h);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) zr[i] = o[i];
+                }
+                warp_arrive(&B->vec_free[v]);
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------- state
+        const int h = warp >> 2;
+        const int j = 32 * ((warp & 3) - 2) + lane;   // E1: token; E3: key index
+        const size_t init = (size_t)(a.shared ? 0 : bb) * a.H + hh;
+        float w[32], s[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const size_t idx = (init * kD + 32 * h + i) * (size_t)kD + j;
+            w[i] = a.W0[idx];
+            s[i] = (kTitans && a.S0) ? a.S0[idx] : 0.f;
+        }
+        auto write_ws = [&]() {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                st_chunk(wsW, j, 32 * h + 8 * q, w + 8 * q);
+                if (kTitans) st_chunk(wsS, j, 32 * h + 8 * q, s + 8 * q);
+            }
+        };
+        write_ws();
+        fence_proxy_async_smem();
+        warp_arrive(&B->ws_ready);
+        bool ok = true;
+        for (int g = 0; g < nt; ++g) {
+            const int st = g % kNS, v = g & 1;
+            if (ok) ok = wait_all(B, &B->full[st], (g / kNS) & 1, status);
+            if (ok) ok = wait_all(B, &B->c1_done, g & 1, status);
+            if (ok) ok = wait_all(B, &B->vec_ready[v], (g >> 1) & 1, status);
+            if (ok) {
+                // E1: R0 for token j, rows 32h .. 32h + 31, sixteen at a time
+                tc_fence_after();
+                const uint8_t* vt = stage(st) + 2 * kTileBytes;
+                const float bp = vec(v)[vBp + j];
+                const float cp = kTitans ? vec(v)[vCp + j] : 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c0 = 32 * h + 16 * half;
+                    float kw[16], ks[16], vv[16];
+                    tmem_ld16(tl + kC1 + c0, kw);
+                    if (kTitans) tmem_ld16(tl + kC1 + 64 + c0, ks);
+                    ld_chunk(vt, j, c0, vv);
+                    ld_chunk(vt, j, c0 + 8, vv + 8);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        kw[i] = bp * kw[i] - vv[i];
+                        if (kTitans) kw[i] = fmaf(cp, ks[i], kw[i]);
+                    }
+                    st_chunk(r0, j, c0, kw);
+                    st_chunk(r0, j, c0 + 8, kw + 8);
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                warp_arrive(&B->r0_ready);
+            }
+            named_bar_sync(1, 128);
+            if (tid == 64 && ok) mbar_arrive(&B->empty[st]);   // V and the C1 reads are done
+            if (ok) ok = wait_all(B, &B->c3_done[v], (g >> 1) & 1, status);
+            if (ok) {
+                // E3: the carry for key index j, sixteen rows at a time
+                tc_fence_after();
+                const float4 sc = *reinterpret_cast<const float4*>(vec(v) + vScal);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float dc[16], dp[16];
+                    tmem_ld16(tl + kC3 + 32 * h + 16 * half, dc);
+                    if (kTitans) tmem_ld16(tl + kC3 + 64 + 32 * h + 16 * half, dp);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int ii = 16 * half + i;
+                        if (kTitans) {
+                            const float wn = sc.x * w[ii] + sc.y * s[ii] - 2.f * dc[i];
+                            s[ii] = sc.z * s[ii] - 2.f * dp[i];
+                            w[ii] = wn;
+                        } else {
+                            w[ii] = sc.x * w[ii] - 2.f * dc[i];
+                        }
+                    }
+                }
+                tc_fence_before();
+                write_ws();
+                fence_proxy_async_smem();
+                warp_arrive(&B->ws_ready);
+                warp_arrive(&B->vec_free[v]);
+            }
+        }
+        if (ok && a.W_out) {
+            const size_t dst = (size_t)seq * kD * kD;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const size_t idx = dst + (size_t)(32 * h + i) * kD + j;
+                a.W_out[idx] = w[i];
+                if (a.S_out) a.S_out[idx] = s[i];
+            }
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------- preparation
+        const int p = tid - 256;                 // TMEM lane 0..127
+        const bool issuer = warp == 8;
+        const bool qside = p < 64;
+        const int tr = qside ? p : p - 64;
+        bool ok = true;
+        uint32_t pr_phase = 0;
+        auto issue_p1 = [&](int g2) -> bool {
+            const int st2 = g2 % kNS;
+            if (!wait_all(B, &B->full[st2], (g2 / kNS) & 1, status)) return false;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t sa = smem_u32(stage(st2));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kP1 + 64 * (g2 & 1), sdesc(sa + kk * 32, 16, 1024, 2),
+                             sdesc(sa + kTileBytes + kk * 32, 16, 1024, 2), idK, kk > 0);
+                mma_commit(&B->p1_done[g2 & 1]);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (issuer) ok = issue_p1(0);
+        for (int g = 0; g < nt; ++g) {
+            const int v = g & 1, st = g % kNS;
+            const int n = min(kTile, T - g * kTile);
+            float* V = vec(v);
+            uint8_t* X = ay(v);
+            if (issuer && ok && g + 1 < nt) ok = issue_p1(g + 1);
+            if (ok && g >= 2) ok = wait_all(B, &B->vec_free[v], ((g - 2) >> 1) & 1, status);
+            if (ok && g >= 2) ok = wait_all(B, &B->c3_done[v], ((g - 2) >> 1) & 1, status);
+            // gates of the tile (padded tokens: theta 0, eta = keep = 1)
+            if (ok && qside) {
+                float th = 0.f, et = 1.f, kp = 1.f;
+                if (tr < n) {
+                    const size_t gi = gate_index(a, (size_t)seq, g * kTile + tr);
+                    th = a.theta[gi];
+                    et = a.eta ? a.eta[gi] : 0.f;
+                    kp = 1.f - (a.alpha ? a.alpha[gi] : 0.f);
+                }
+                V[vTh + tr] = th;
+                V[vEt + tr] = et;
+                V[vKp + tr] = kp;
+            }
+            named_bar_sync(3, 128);
+            if (ok && warp == 8) {
+                // beta_t = prod keep, P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
+                // lane l owns tokens 2l, 2l + 1
+                const int t0 = 2 * lane, t1 = t0 + 1;
+                const float et0 = V[vEt + t0], et1 = V[vEt + t1];
+                const float kp0 = V[vKp + t0], kp1 = V[vKp + t1];
+                float Ab = kp0 * kp1, Bb = 0.f, Ap = et0 * et1, Bp = 0.f;
+                scan_affine_up(Ab, Bb, lane);
+                scan_affine_up(Ap, Bp, lane);
+                float pre_b = __shfl_up_sync(0xffffffffu, Ab, 1);
+                float pre_p = __shfl_up_sync(0xffffffffu, Ap, 1);
+                if (lane == 0) pre_b = pre_p = 1.f;
+                const float be0 = pre_b * kp0, be1 = be0 * kp1;
+                const float P0 = pre_p * et0, P1 = P0 * et1;
+                float Ac = kp1 * kp0, Bc = kp1 * P0 + P1;
+                scan_affine_up(Ac, Bc, lane);
+                float cpre = __shfl_up_sync(0xffffffffu, Bc, 1);
+                if (lane == 0) cpre = 0.f;
+                const float c0 = kp0 * cpre + P0, c1 = kp1 * c0 + P1;
+                V[vBeta + t0] = be0;
+                V[vBeta + t1] = be1;
+                V[vCv + t0] = c0;
+                V[vCv + t1] = c1;
+                // beta', c': the values at the token before the sub-chunk's start
+                // (t0 and t1 share a sub-chunk: b is even)
+                const int src = bsub * (t0 / bsub) - 1;
+                const int sl = src < 0 ? 0 : src >> 1;
+                const float sb0 = __shfl_sync(0xffffffffu, be0, sl), sb1 = __shfl_sync(0xffffffffu, be1, sl);
+                const float sc0 = __shfl_sync(0xffffffffu, c0, sl), sc1 = __shfl_sync(0xffffffffu, c1, sl);
+                const float bp = src < 0 ? 1.f : ((src & 1) ? sb1 : sb0);
+                const float cp = src < 0 ? 0.f : ((src & 1) ? sc1 : sc0);
+                V[vBp + t0] = bp;
+                V[vBp + t1] = bp;
+                V[vCp + t0] = cp;
+                V[vCp + t1] = cp;
+                const int ln = (n - 1) >> 1, un = (n - 1) & 1;
+                const float bn = __shfl_sync(0xffffffffu, un ? be1 : be0, ln);
+                const float cn = __shfl_sync(0xffffffffu, un ? c1 : c0, ln);
+                const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
+                if (lane == 0)
+                    *reinterpret_cast<float4*>(V + vScal) = make_float4(bn, cn, Pn, (float)n);
+            }
+            if (ok && warp == 9) {
+                // Pm[s] = theta_s prod_{j = s+1 .. 63} eta_j (padded eta = 1):
+                // suffix products along the lanes
+                const int t0 = 2 * lane, t1 = t0 + 1;
+                const float e1 = V[vEt + t1];
+                float A = V[vEt + t0] * e1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_down_sync(0xffffffffu, A, off);
+                    if (lane + off < 32) A *= o;
+                }
+                float above = __shfl_down_sync(0xffffffffu, A, 1);
+                if (lane == 31) above = 1.f;
+                V[vPm + t0] = V[vTh + t0] * e1 * above;
+                V[vPm + t1] = V[vTh + t1] * above;
+            }
+            named_bar_sync(3, 128);
+            if (ok && p == 0) mbar_arrive(&B->vec_ready[v]);
+            // scores of this tile, weighted: rows of A~ (Q side) and of L (K side)
+            if (ok) ok = wait_all(B, &B->p1_done[v], (g >> 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                const int r = qside ? tr : bsub * (tr / bsub) - 1;   // row of C used
+                const float scale = qside ? 1.f : 2.f;
+                float Kc = 1.f, wv = 1.f;                            // recurrence at s = r
+#pragma unroll
+                for (int q4 = 3; q4 >= 0; --q4) {
+                    float raw[16], val[16];
+                    tmem_ld16(tl + kP1 + 64 * v + 16 * q4, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 15; i >= 0; --i) {
+                        const int sidx = 16 * q4 + i;
+                        float coef = 0.f;
+                        if (sidx <= r) {
+                            if (sidx < r) {
+                                Kc = V[vKp + sidx + 1] * Kc;
+                                wv = fmaf(V[vEt + sidx + 1], wv, Kc);
+                            }
+                            coef = V[vTh + sidx] * wv;
+                        }
+                        val[i] = scale * coef * raw[i];
+                        if (qside && tr == n - 1) V[vCn + sidx] = coef;
+                    }
+                    if (qside) {
+                        st_chunk(X, tr, 16 * q4, val);
+                        st_chunk(X, tr, 16 * q4 + 8, val + 8);
+                    } else {
+                        float iv[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) iv[i] = (16 * q4 + i == tr ? 1.f : 0.f) - val[i];
+                        st_chunk(X, 128 + tr, 16 * q4, val);
+                        st_chunk(X, 128 + tr, 16 * q4 + 8, val + 8);
+                        st_chunk(il, tr, 16 * q4, iv);
+                        st_chunk(il, tr, 16 * q4 + 8, iv + 8);
+                    }
+                }
+            }
+            tc_fence_before();
+            named_bar_sync(3, 128);
+            // K^T diag(C[n-1]) (rows 64..127) and K^T diag(Pm) (rows 192..255)
+            if (ok) {
+                const uint8_t* kt = stage(st) + kTileBytes;
+                const int jj = tr;
+                const float* wsc = V + (qside ? vCn : vPm);
+                const bool zero = !qside && !kTitans;
+                const int row = qside ? 64 + jj : 192 + jj;
+#pragma unroll
+                for (int s8 = 0; s8 < 8; ++s8) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int sidx = 8 * s8 + i;
+                        x[i] = zero ? 0.f : wsc[sidx] * bf16_at(kt, sidx, jj);
+                    }
+                    st_chunk(X, row, 8 * s8, x);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(3, 128);
+            if (ok && p == 0) mbar_arrive(&B->empty[st]);   // the scores and K reads are done
+            if (bsub < kTile) {
+                // round 1: [A~; Y0_C] (I - L) and [L; Y0_P] (I - L)
+                if (issuer && ok) {
+                    tc_fence_after();
+                    if (elect_one()) {
+                        mma_k64(tmem + kPR, smem_u32(X), true, smem_u32(il), idM);
+                        mma_k64(tmem + kPR + 64, smem_u32(X) + 128 * 128, true, smem_u32(il), idM);
+                        mma_commit(&B->pr_done);
+                    }
+                    __syncwarp();
+                }
+                if (ok) ok = wait_all(B, &B->pr_done, pr_phase & 1, status);
+                ++pr_phase;
+                if (ok) {
+                    tc_fence_after();
+                    uint8_t* dst = bsub == 32 ? X : ap;   // N = I - L when b = 32
+#pragma unroll
+                    for (int hh2 = 0; hh2 < 2; ++hh2) {
+                        float d1[32], d2[32];
+                        tmem_ld32(tl + kPR + 32 * hh2, d1);
+                        tmem_ld32(tl + kPR + 64 + 32 * hh2, d2);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) st_chunk(dst, p, 32 * hh2 + 8 * q, d1 + 8 * q);
+                        if (!qside && kTitans) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                st_chunk(dst, 192 + tr, 32 * hh2 + 8 * q, d2 + 8 * q);
+                        }
+                        if (qside && bsub == 16) {
+                            // I + L^2 = I + L - (L - L^2), with the bf16 L the MMA used
+                            float x[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int u = 32 * hh2 + i;
+                                x[i] = (u == p ? 1.f : 0.f) + bf16_at(X, 128 + p, u) - d2[i];
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) st_chunk(b2, p, 32 * hh2 + 8 * q, x + 8 * q);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(3, 128);
+                if (bsub == 16) {
+                    // round 2: [A~(I-L); Y0_C(I-L)] (I + L^2) and [.; Y0_P(I-L)] (I + L^2)
+                    if (issuer && ok) {
+                        tc_fence_after();
+                        if (elect_one()) {
+                            mma_k64(tmem + kPR, smem_u32(ap), true, smem_u32(b2), idM);
+                            if (kTitans)
+                                mma_k64(tmem + kPR + 64, smem_u32(ap) + 128 * 128, true,
+                                        smem_u32(b2), idM);
+                            mma_commit(&B->pr_done);
+                        }
+                        __syncwarp();
+                    }
+                    if (ok) ok = wait_all(B, &B->pr_done, pr_phase & 1, status);
+                    ++pr_phase;
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int hh2 = 0; hh2 < 2; ++hh2) {
+                            float d1[32], d2[32];
+                            tmem_ld32(tl + kPR + 32 * hh2, d1);
+                            if (kTitans) tmem_ld32(tl + kPR + 64 + 32 * hh2, d2);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) st_chunk(X, p, 32 * hh2 + 8 * q, d1 + 8 * q);
+                            if (!qside && kTitans) {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    st_chunk(X, 192 + tr, 32 * hh2 + 8 * q, d2 + 8 * q);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_bar_sync(3, 128);
+                }
+            }
+            if (ok && p == 0) mbar_arrive(&B->ay_ready[v]);
+        }
+    } else if (warp == 12) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            constexpr int kPrefetch = 4;
+            auto prefetch = [&](int g) {
+                if (g >= nt) return;
+                tma_prefetch_l2_3d(&qmap, 0, g * kTile, seq);
+                tma_prefetch_l2_3d(&kmap, 0, g * kTile, seq);
+                tma_prefetch_l2_3d(&vmap, 0, g * kTile, seq);
+            };
+            for (int g = 0; g < kPrefetch; ++g) prefetch(g);
+            int issued = 0;
+            for (int g = 0; g < nt; ++g) {
+                const int st = g % kNS;
+                prefetch(g + kPrefetch);
+                if (g >= kNS && !wait_bar(B, &B->empty[st], ((g / kNS) - 1) & 1, status)) break;
+                mbar_expect_tx(&B->full[st], kStageBytes + (g + 1 == a.debug_stall ? 16u : 0u));
+                tma_load_3d(stage(st), &qmap, &B->full[st], 0, g * kTile, seq);
+                tma_load_3d(stage(st) + kTileBytes, &kmap, &B->full[st], 0, g * kTile, seq);
+                tma_load_3d(stage(st) + 2 * kTileBytes, &vmap, &B->full[st], 0, g * kTile, seq);
+                issued = g + 1;
+            }
+            for (int g = (issued > kNS ? issued - kNS : 0); g < issued; ++g)
+                wait_drain(&B->full[g % kNS], (g / kNS) & 1, B->wait_limit);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------- chain MMA issue
+        bool ok = true;
+        for (int g = 0; g < nt; ++g) {
+            const int st = g % kNS, v = g & 1;
+            if (ok) ok = wait_all(B, &B->full[st], (g / kNS) & 1, status);
+            if (ok) ok = wait_all(B, &B->ws_ready, g & 1, status);
+            if (ok && g >= 1) ok = wait_all(B, &B->c1_free, (g - 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    // C1 = [Q; K] [W; S]^T (B: W^T then S^T, 8 KB apart)
+                    mma_k64(tmem + kC1, smem_u32(stage(st)), true, smem_u32(wsW), idC1);
+                    mma_commit(&B->c1_done);
+                }
+                __syncwarp();
+            }
+            if (ok) ok = wait_all(B, &B->r0_ready, g & 1, status);
+            if (ok) ok = wait_all(B, &B->ay_ready[v], (g >> 1) & 1, status);
+            if (ok && g >= 1) ok = wait_all(B, &B->c3_free, (g - 1) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    // C3 = [A~N; Y_C] R0 (and [.; Y_P] R0)
+                    mma_k64(tmem + kC3, smem_u32(ay(v)), true, smem_u32(r0), idM);
+                    if (kTitans)
+                        mma_k64(tmem + kC3 + 64, smem_u32(ay(v)) + 128 * 128, true, smem_u32(r0), idM);
+                    mma_commit(&B->c3_done[v]);
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    // drain the MMAs of the two issuing warps before TMEM is released
+    if (warp == 8 || warp == 13) {
+        uint64_t* d = &B->drain[warp == 8 ? 0 : 1];
+        if (elect_one()) mma_commit(d);
+        __syncwarp();
+        if (lane == 0) wait_drain(d, 0, B->wait_limit);
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool linear_seq_supported(const LinearArgs& a) {
+    return a.bf16 && a.dk == kD && a.dv == kD && (a.chunk == 16 || a.chunk == 32) && a.T >= 1 &&
+           !a.ckpt && a.z;
+}
+
+cudaError_t linear_seq_launch(const LinearArgs& a, cudaStream_t s) {
+    const int BH = a.B * a.H;
+    CUtensorMap qm, km, vm;
+    if (!make_token_tile_map(&qm, a.q, BH, a.T, kD, 64, true) ||
+        !make_token_tile_map(&km, a.k, BH, a.T, kD, 64, true) ||
+        !make_token_tile_map(&vm, a.v, BH, a.T, kD, 64, true))
+        return cudaErrorInvalidValue;
+    constexpr Layout L = make_layout();
+    const size_t smem = L.total + 1024;
+    const bool titans = a.eta || a.alpha || a.S0 || a.S_out;
+    if (titans) {
+        cudaError_t e = cudaFuncSetAttribute(linear_seq_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        linear_seq_kernel<true><<<BH, kThreads, smem, s>>>(qm, km, vm, a);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(linear_seq_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        linear_seq_kernel<false><<<BH, kThreads, smem, s>>>(qm, km, vm, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ttm

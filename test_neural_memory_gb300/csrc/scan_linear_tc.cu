@@ -778,22 +778,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D view [sequences][T][D] of a bf16 tensor, tile box {bx, 64, 1}.
 bool make_map(CUtensorMap* m, const void* ptr, int BH, int T, int D, int bx, bool swz) {
+    return make_token_tile_map(m, ptr, BH, T, D, bx, swz);
+}
+
+}  // namespace
+
+// 3-D view [sequences][T][D] of a bf16 tensor, tile box {bx, 64, 1}.
+bool make_token_tile_map(void* map, const void* ptr, int BH, int T, int D, int bx, bool swz) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
     cuuint32_t box[3] = {(cuuint32_t)bx, (cuuint32_t)kChunk, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return enc(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool linear_tc_supported(const LinearArgs& a) {
     return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kChunk &&

@@ -71,12 +71,23 @@ bool bad_alias(Span o, Span in, bool exact_ok) {
 bool dims_ok(int x, int dtype) { return x >= 1 && x % (dtype == TTM_BF16 ? 8 : 4) == 0; }
 
 // Kernel the current policy would pick for these arguments (host decision).
+// The two tensor-core kernels never compete: the sequence-per-CTA kernel
+// takes d = 64 with gradient points every 16 or 32 tokens, the row-slice
+// kernel chunk 64.
 int select_linear(const ttm::LinearArgs& a) {
+    const bool seq_ok = ttm::linear_seq_supported(a);
     const bool tc_ok = ttm::linear_tc_supported(a);
     const bool simt_ok = ttm::linear_simt_supported(a);
-    if (g_policy == TTM_KERNEL_TC) return tc_ok ? TTM_KID_LINEAR_TC : TTM_KID_NONE;
+    const int tc_kid = seq_ok ? TTM_KID_LINEAR_SEQ : (tc_ok ? TTM_KID_LINEAR_TC : TTM_KID_NONE);
+    if (g_policy == TTM_KERNEL_TC) return tc_kid;
     if (g_policy == TTM_KERNEL_SIMT) return simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE;
-    return tc_ok ? TTM_KID_LINEAR_TC : (simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE);
+    return tc_kid != TTM_KID_NONE ? tc_kid : (simt_ok ? TTM_KID_LINEAR_SIMT : TTM_KID_NONE);
+}
+
+cudaError_t launch_linear(int kid, const ttm::LinearArgs& a, cudaStream_t s) {
+    if (kid == TTM_KID_LINEAR_TC) return ttm::linear_tc_launch(a, s);
+    if (kid == TTM_KID_LINEAR_SEQ) return ttm::linear_seq_launch(a, s);
+    return ttm::linear_simt_launch(a, s);
 }
 
 // The tensor-core 2-layer kernel rounds its recurrent operands to bf16.  Over
@@ -164,10 +175,10 @@ int linear_common(int B, int H, int T, int dk, int dv, int chunk, int dtype, con
     a.status = status_ptr();
     if (!a.status) return TTM_ERR_CUDA;
     a.wait_cycles = g_wait_cycles.load();
-    if (kid == TTM_KID_LINEAR_TC) a.debug_stall = g_stall_chunk.exchange(-1) + 1;
+    if (kid == TTM_KID_LINEAR_TC || kid == TTM_KID_LINEAR_SEQ)
+        a.debug_stall = g_stall_chunk.exchange(-1) + 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = kid == TTM_KID_LINEAR_TC ? ttm::linear_tc_launch(a, s)
-                                                   : ttm::linear_simt_launch(a, s);
+    const cudaError_t e = launch_linear(kid, a, s);
     if (e != cudaSuccess) return TTM_ERR_CUDA;
     t_last_kernel = kid;
     // the tensor-core path enqueues the coefficient pre-pass and the scan
@@ -576,8 +587,7 @@ int ttm_lmm_layer_fwd(int B, int T, int H, int d, int chunk, int conv_k, const v
     sc.workspace_bytes = L.scan_bytes;
     sc.status = status;
     const int kid = select_linear(sc);
-    const cudaError_t e = kid == TTM_KID_LINEAR_TC ? ttm::linear_tc_launch(sc, s)
-                                                   : ttm::linear_simt_launch(sc, s);
+    const cudaError_t e = launch_linear(kid, sc, s);
     if (e != cudaSuccess) return TTM_ERR_CUDA;
     if (ttm::lmm_post_launch(a, proj, z, o, s) != cudaSuccess) return TTM_ERR_CUDA;
     // y = x + o W_o
