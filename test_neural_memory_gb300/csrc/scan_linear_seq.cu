@@ -37,9 +37,13 @@
 //   warps 2,3,6,7   state: E1 (R0 for token = TMEM lane 64..127) and E3 (the
 //                   update; thread j holds W[r][j], S[r][j] for 32 rows r in
 //                   fp32 registers and writes their bf16 copy)
-//   warps 8-11      preparation of the next tile: gates, coefficient scans,
-//                   scores [Q; K] K^T (MMA), the weighted rows of A~ and L,
-//                   N applied to [A~; K^T diag C; K^T diag Pm] by two MMA rounds
+//   warps 8-11      preparation, one tile ahead of the chain: gates (loaded a
+//                   tile early), C[t][s] by columns (one lane per column) into
+//                   shared memory with the vector scans beside it, the scores
+//                   [Q; K] K^T (MMA), the weighted rows of A~ and L, row-scaled
+//                   copies of K (the MN-major operand K^T diag C, K^T diag Pm),
+//                   and N applied to both by two MMA rounds ((I - L), then
+//                   (I + L^2))
 //   warp 12         TMA producer (Q, K, V tiles of 64 tokens, three stages)
 //   warp 13         issues C1 and C3
 // Every wait is bounded; a wait that runs out sets the status word, all roles
@@ -182,11 +186,6 @@ __device__ __forceinline__ void ld_chunk(const uint8_t* tile, int row, int col, 
     }
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
-    const uint16_t u = *reinterpret_cast<const uint16_t*>(tile + sw128_offset(row, col));
-    return __uint_as_float((uint32_t)u << 16);
-}
-
 // 32 lanes x 32 consecutive 32-bit TMEM columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
     uint32_t u[32];
@@ -218,14 +217,29 @@ __device__ __forceinline__ void scan_affine_up(float& A, float& B, int lane) {
     }
 }
 
-// Four K steps (K = 64) of one M = 128 MMA with both operands in shared memory.
-__device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, bool a_mn_major_b, uint32_t b,
-                                        uint32_t idesc) {
-    (void)a_mn_major_b;
+// Four K steps (K = 64) of one M = 128 MMA with both operands in shared
+// memory, B MN-major ([k][n] rows of 128 bytes, N atoms 8 KB apart); A
+// K-major (rows of the M index) or MN-major ([k][m], M atoms 8 KB apart).
+__device__ __forceinline__ void mma_k64_ka(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
         mma_bf16(d, sdesc(a + kk * 32, 16, 1024, 2), sdesc(b + kk * 2048, 8192, 1024, 2), idesc,
                  kk > 0);
+}
+
+__device__ __forceinline__ void mma_k64_ma(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(d, sdesc(a + kk * 2048, 8192, 1024, 2), sdesc(b + kk * 2048, 8192, 1024, 2), idesc,
+                 kk > 0);
+}
+
+// Index of C[t][s] in the tile's fp32 coefficient table: row t at 64 t floats,
+// its sixteen groups of four XOR-permuted by t % 16, so that the column walk
+// (one column per lane) and the row reads (one row per thread) are both free
+// of bank conflicts.
+__device__ __forceinline__ int c_index(int t, int s) {
+    return t * 64 + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3);
 }
 
 template <bool kTitans>
@@ -269,7 +283,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B->ay_ready[i], 1);
             mbar_init(&B->c3_done[i], 1);
-            mbar_init(&B->vec_ready[i], 1);
+            mbar_init(&B->vec_ready[i], 1);    // the scan warp
             mbar_init(&B->vec_free[i], 8);     // read warps + state warps
             mbar_init(&B->p1_done[i], 1);
             mbar_init(&B->drain[i], 1);
@@ -288,6 +302,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     constexpr uint32_t idC1 = idesc_bf16_f32(128, kTitans ? 128 : 64, 0, 1);
     constexpr uint32_t idK = idesc_bf16_f32(128, 64, 0, 0);   // B K-major
     constexpr uint32_t idM = idesc_bf16_f32(128, 64, 0, 1);   // B MN-major
+    constexpr uint32_t idMM = idesc_bf16_f32(128, 64, 1, 1);  // A and B MN-major
 
     if (warp < 8 && (warp & 3) < 2) {
         // ------------------------------------------------------------- reads
@@ -444,6 +459,8 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         const bool issuer = warp == 8;
         const bool qside = p < 64;
         const int tr = qside ? p : p - 64;
+        float* Ctab = reinterpret_cast<float*>(ap);   // the tile's C (fp32), until round 1
+        const bool gated = a.eta || a.alpha;
         bool ok = true;
         uint32_t pr_phase = 0;
         auto issue_p1 = [&](int g2) -> bool {
@@ -461,30 +478,100 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             __syncwarp();
             return true;
         };
+        // gates of token tr of tile gg (padded tokens: theta 0, eta = keep = 1),
+        // loaded one tile ahead so that their latency overlaps a tile's work
+        float th_n = 0.f, et_n = 1.f, kp_n = 1.f;
+        auto load_gates = [&](int gg) {
+            th_n = 0.f;
+            et_n = 1.f;
+            kp_n = 1.f;
+            if (qside && gg < nt && gg * kTile + tr < T) {
+                const size_t gi = gate_index(a, (size_t)seq, gg * kTile + tr);
+                th_n = a.theta[gi];
+                et_n = a.eta ? a.eta[gi] : 0.f;
+                kp_n = 1.f - (a.alpha ? a.alpha[gi] : 0.f);
+            }
+        };
+        if (!kTitans) {
+            // the momentum operand rows stay zero without momentum
+            const float zero8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (!qside)
+                for (int c8 = 0; c8 < 8; ++c8)
+                    for (int sl = 0; sl < 2; ++sl)
+                        st_chunk(ay(sl) + 128 * 128 + kTileBytes, tr, 8 * c8, zero8);
+        }
+        load_gates(0);
         if (issuer) ok = issue_p1(0);
         for (int g = 0; g < nt; ++g) {
             const int v = g & 1, st = g % kNS;
             const int n = min(kTile, T - g * kTile);
             float* V = vec(v);
-            uint8_t* X = ay(v);
+            uint8_t* X = ay(v);                  // [A~; L] rows 0..127 (K-major), then the C3 operand
+            uint8_t* KCP = X + 128 * 128;        // [s][j]: K scaled by C[n-1][s], then by Pm[s]
             if (issuer && ok && g + 1 < nt) ok = issue_p1(g + 1);
             if (ok && g >= 2) ok = wait_all(B, &B->vec_free[v], ((g - 2) >> 1) & 1, status);
             if (ok && g >= 2) ok = wait_all(B, &B->c3_done[v], ((g - 2) >> 1) & 1, status);
-            // gates of the tile (padded tokens: theta 0, eta = keep = 1)
             if (ok && qside) {
-                float th = 0.f, et = 1.f, kp = 1.f;
-                if (tr < n) {
-                    const size_t gi = gate_index(a, (size_t)seq, g * kTile + tr);
-                    th = a.theta[gi];
-                    et = a.eta ? a.eta[gi] : 0.f;
-                    kp = 1.f - (a.alpha ? a.alpha[gi] : 0.f);
-                }
-                V[vTh + tr] = th;
-                V[vEt + tr] = et;
-                V[vKp + tr] = kp;
+                V[vTh + tr] = th_n;
+                V[vEt + tr] = et_n;
+                V[vKp + tr] = kp_n;
             }
+            load_gates(g + 1);
             named_bar_sync(3, 128);
-            if (ok && warp == 8) {
+            if (ok && gated && warp < 10) {
+                // C[t][s] = theta_s w(s, t) by columns (lane = column s, rows in
+                // order): m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
+                // both 0 before row s and 1 at it; above the diagonal C is 0.
+                // The rows' gates are loaded sixteen at a time into registers, so
+                // no load sits on the recurrence.
+                const int sc = lane + 32 * (warp - 8);
+                const float ths = V[vTh + sc];
+                float m = 0.f, wv = 0.f, ce = 0.f;
+                float* __restrict__ ct = Ctab;
+#pragma unroll 1
+                for (int tb = 0; tb < kTile; tb += 16) {
+                    float e[16], k1[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 ev = *reinterpret_cast<const float4*>(V + vEt + tb + 4 * i);
+                        const float4 kv = *reinterpret_cast<const float4*>(V + vKp + tb + 4 * i);
+                        e[4 * i] = ev.x; e[4 * i + 1] = ev.y; e[4 * i + 2] = ev.z; e[4 * i + 3] = ev.w;
+                        k1[4 * i] = kv.x; k1[4 * i + 1] = kv.y; k1[4 * i + 2] = kv.z; k1[4 * i + 3] = kv.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = tb + i;
+                        m = fmaf(e[i], m, t == sc ? 1.f : 0.f);
+                        wv = fmaf(k1[i], wv, m);
+                        const float c = ths * wv;
+                        ct[c_index(t, sc)] = c;
+                        ce = t == n - 1 ? c : ce;
+                    }
+                }
+                V[vCn + sc] = ce;              // C[n-1][s]
+                V[vPm + sc] = ths * m;         // theta_s prod_{j=s+1..n-1} eta_j (padded eta = 1)
+            }
+            if (ok && !gated && warp < 10) {
+                // no momentum and no forgetting: C[t][s] = theta_s for s <= t
+                const int sc = lane + 32 * (warp - 8);
+                const float ths = V[vTh + sc];
+                V[vCn + sc] = sc <= n - 1 ? ths : 0.f;
+                V[vPm + sc] = sc == n - 1 ? ths : 0.f;
+            }
+            if (ok && !gated && warp == 10) {
+                // beta = 1, c = 0, P = 0 throughout
+                V[vBeta + lane] = 1.f;
+                V[vBeta + lane + 32] = 1.f;
+                V[vCv + lane] = 0.f;
+                V[vCv + lane + 32] = 0.f;
+                V[vBp + lane] = 1.f;
+                V[vBp + lane + 32] = 1.f;
+                V[vCp + lane] = 0.f;
+                V[vCp + lane + 32] = 0.f;
+                if (lane == 0) *reinterpret_cast<float4*>(V + vScal) = make_float4(1.f, 0.f, 0.f, (float)n);
+                warp_arrive(&B->vec_ready[v]);
+            }
+            if (ok && gated && warp == 10) {
                 // beta_t = prod keep, P_t = prod eta, c_t = keep_t c_{t-1} + P_t;
                 // lane l owns tokens 2l, 2l + 1
                 const int t0 = 2 * lane, t1 = t0 + 1;
@@ -525,95 +612,78 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 const float Pn = __shfl_sync(0xffffffffu, un ? P1 : P0, ln);
                 if (lane == 0)
                     *reinterpret_cast<float4*>(V + vScal) = make_float4(bn, cn, Pn, (float)n);
-            }
-            if (ok && warp == 9) {
-                // Pm[s] = theta_s prod_{j = s+1 .. 63} eta_j (padded eta = 1):
-                // suffix products along the lanes
-                const int t0 = 2 * lane, t1 = t0 + 1;
-                const float e1 = V[vEt + t1];
-                float A = V[vEt + t0] * e1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_down_sync(0xffffffffu, A, off);
-                    if (lane + off < 32) A *= o;
-                }
-                float above = __shfl_down_sync(0xffffffffu, A, 1);
-                if (lane == 31) above = 1.f;
-                V[vPm + t0] = V[vTh + t0] * e1 * above;
-                V[vPm + t1] = V[vTh + t1] * above;
+                // the reads and the state only need these vectors: publish them now
+                warp_arrive(&B->vec_ready[v]);
             }
             named_bar_sync(3, 128);
-            if (ok && p == 0) mbar_arrive(&B->vec_ready[v]);
-            // scores of this tile, weighted: rows of A~ (Q side) and of L (K side)
+            // weighted scores: row p of [A~; L] and row tr of (I - L); K rows
+            // scaled by C[n-1][s] (Q side) and Pm[s] (K side)
             if (ok) ok = wait_all(B, &B->p1_done[v], (g >> 1) & 1, status);
             if (ok) {
                 tc_fence_after();
                 const int r = qside ? tr : bsub * (tr / bsub) - 1;   // row of C used
                 const float scale = qside ? 1.f : 2.f;
-                float Kc = 1.f, wv = 1.f;                            // recurrence at s = r
-#pragma unroll
-                for (int q4 = 3; q4 >= 0; --q4) {
-                    float raw[16], val[16];
+#pragma unroll 1
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float raw[16], cr[16], val[16];
                     tmem_ld16(tl + kP1 + 64 * v + 16 * q4, raw);
+#pragma unroll
+                    for (int gq = 0; gq < 4; ++gq) {
+                        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (gated) {
+                            if (r >= 0) f = *reinterpret_cast<const float4*>(Ctab + c_index(r, 16 * q4 + 4 * gq));
+                        } else {
+                            // theta_s below and on the diagonal of row r
+                            const int s0 = 16 * q4 + 4 * gq;
+                            f = *reinterpret_cast<const float4*>(V + vTh + s0);
+                            f.x = s0 <= r ? f.x : 0.f;
+                            f.y = s0 + 1 <= r ? f.y : 0.f;
+                            f.z = s0 + 2 <= r ? f.z : 0.f;
+                            f.w = s0 + 3 <= r ? f.w : 0.f;
+                        }
+                        cr[4 * gq] = f.x;
+                        cr[4 * gq + 1] = f.y;
+                        cr[4 * gq + 2] = f.z;
+                        cr[4 * gq + 3] = f.w;
+                    }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 15; i >= 0; --i) {
-                        const int sidx = 16 * q4 + i;
-                        float coef = 0.f;
-                        if (sidx <= r) {
-                            if (sidx < r) {
-                                Kc = V[vKp + sidx + 1] * Kc;
-                                wv = fmaf(V[vEt + sidx + 1], wv, Kc);
-                            }
-                            coef = V[vTh + sidx] * wv;
-                        }
-                        val[i] = scale * coef * raw[i];
-                        if (qside && tr == n - 1) V[vCn + sidx] = coef;
-                    }
-                    if (qside) {
-                        st_chunk(X, tr, 16 * q4, val);
-                        st_chunk(X, tr, 16 * q4 + 8, val + 8);
-                    } else {
+                    for (int i = 0; i < 16; ++i) val[i] = scale * cr[i] * raw[i];
+                    st_chunk(X, p, 16 * q4, val);
+                    st_chunk(X, p, 16 * q4 + 8, val + 8);
+                    if (!qside) {
                         float iv[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) iv[i] = (16 * q4 + i == tr ? 1.f : 0.f) - val[i];
-                        st_chunk(X, 128 + tr, 16 * q4, val);
-                        st_chunk(X, 128 + tr, 16 * q4 + 8, val + 8);
                         st_chunk(il, tr, 16 * q4, iv);
                         st_chunk(il, tr, 16 * q4 + 8, iv + 8);
                     }
                 }
-            }
-            tc_fence_before();
-            named_bar_sync(3, 128);
-            // K^T diag(C[n-1]) (rows 64..127) and K^T diag(Pm) (rows 192..255)
-            if (ok) {
-                const uint8_t* kt = stage(st) + kTileBytes;
-                const int jj = tr;
-                const float* wsc = V + (qside ? vCn : vPm);
-                const bool zero = !qside && !kTitans;
-                const int row = qside ? 64 + jj : 192 + jj;
+                if (qside || kTitans) {
+                    const uint8_t* kt = stage(st) + kTileBytes;
+                    const float f = V[(qside ? vCn : vPm) + tr];
+                    uint8_t* dst = KCP + (qside ? 0u : kTileBytes);
+#pragma unroll 2
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float x[8];
+                        ld_chunk(kt, tr, 8 * c8, x);
 #pragma unroll
-                for (int s8 = 0; s8 < 8; ++s8) {
-                    float x[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int sidx = 8 * s8 + i;
-                        x[i] = zero ? 0.f : wsc[sidx] * bf16_at(kt, sidx, jj);
+                        for (int i = 0; i < 8; ++i) x[i] *= f;
+                        st_chunk(dst, tr, 8 * c8, x);
                     }
-                    st_chunk(X, row, 8 * s8, x);
                 }
             }
             fence_proxy_async_smem();
+            tc_fence_before();
             named_bar_sync(3, 128);
             if (ok && p == 0) mbar_arrive(&B->empty[st]);   // the scores and K reads are done
             if (bsub < kTile) {
-                // round 1: [A~; Y0_C] (I - L) and [L; Y0_P] (I - L)
+                // round 1: [A~; L] (I - L) and [K^T diag C; K^T diag Pm] (I - L)
                 if (issuer && ok) {
                     tc_fence_after();
                     if (elect_one()) {
-                        mma_k64(tmem + kPR, smem_u32(X), true, smem_u32(il), idM);
-                        mma_k64(tmem + kPR + 64, smem_u32(X) + 128 * 128, true, smem_u32(il), idM);
+                        mma_k64_ka(tmem + kPR, smem_u32(X), smem_u32(il), idM);
+                        mma_k64_ma(tmem + kPR + 64, smem_u32(KCP), smem_u32(il), idMM);
                         mma_commit(&B->pr_done);
                     }
                     __syncwarp();
@@ -622,30 +692,39 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 ++pr_phase;
                 if (ok) {
                     tc_fence_after();
-                    uint8_t* dst = bsub == 32 ? X : ap;   // N = I - L when b = 32
-#pragma unroll
+                    // b = 32: N = I - L, so this round gives the C3 operand itself
+                    uint8_t* dst = bsub == 32 ? X : ap;
+#pragma unroll 1
                     for (int hh2 = 0; hh2 < 2; ++hh2) {
                         float d1[32], d2[32];
                         tmem_ld32(tl + kPR + 32 * hh2, d1);
                         tmem_ld32(tl + kPR + 64 + 32 * hh2, d2);
                         tmem_wait_ld();
+                        if (qside) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) st_chunk(dst, p, 32 * hh2 + 8 * q, d1 + 8 * q);
-                        if (!qside && kTitans) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                st_chunk(dst, 192 + tr, 32 * hh2 + 8 * q, d2 + 8 * q);
-                        }
-                        if (qside && bsub == 16) {
-                            // I + L^2 = I + L - (L - L^2), with the bf16 L the MMA used
-                            float x[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int u = 32 * hh2 + i;
-                                x[i] = (u == p ? 1.f : 0.f) + bf16_at(X, 128 + p, u) - d2[i];
+                            for (int q = 0; q < 4; ++q) {
+                                st_chunk(dst, p, 32 * hh2 + 8 * q, d1 + 8 * q);        // A~ (I - L)
+                                st_chunk(dst, 64 + p, 32 * hh2 + 8 * q, d2 + 8 * q);   // Y0_C (I - L)
                             }
+                        } else {
+                            if (kTitans) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) st_chunk(b2, p, 32 * hh2 + 8 * q, x + 8 * q);
+                                for (int q = 0; q < 4; ++q)                            // Y0_P (I - L)
+                                    st_chunk(dst, 192 + tr, 32 * hh2 + 8 * q, d2 + 8 * q);
+                            }
+                            if (bsub == 16) {
+                                // I + L^2 = I + L - (L - L^2), with the bf16 L the MMA used
+                                float x[32];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) ld_chunk(X, p, 32 * hh2 + 8 * q, x + 8 * q);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const int u = 32 * hh2 + i;
+                                    x[i] = (u == tr ? 1.f : 0.f) + x[i] - d1[i];
+                                }
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) st_chunk(b2, tr, 32 * hh2 + 8 * q, x + 8 * q);
+                            }
                         }
                     }
                 }
@@ -657,10 +736,9 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     if (issuer && ok) {
                         tc_fence_after();
                         if (elect_one()) {
-                            mma_k64(tmem + kPR, smem_u32(ap), true, smem_u32(b2), idM);
+                            mma_k64_ka(tmem + kPR, smem_u32(ap), smem_u32(b2), idM);
                             if (kTitans)
-                                mma_k64(tmem + kPR + 64, smem_u32(ap) + 128 * 128, true,
-                                        smem_u32(b2), idM);
+                                mma_k64_ka(tmem + kPR + 64, smem_u32(ap) + 128 * 128, smem_u32(b2), idM);
                             mma_commit(&B->pr_done);
                         }
                         __syncwarp();
@@ -669,7 +747,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     ++pr_phase;
                     if (ok) {
                         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                         for (int hh2 = 0; hh2 < 2; ++hh2) {
                             float d1[32], d2[32];
                             tmem_ld32(tl + kPR + 32 * hh2, d1);
@@ -729,7 +807,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 tc_fence_after();
                 if (elect_one()) {
                     // C1 = [Q; K] [W; S]^T (B: W^T then S^T, 8 KB apart)
-                    mma_k64(tmem + kC1, smem_u32(stage(st)), true, smem_u32(wsW), idC1);
+                    mma_k64_ka(tmem + kC1, smem_u32(stage(st)), smem_u32(wsW), idC1);
                     mma_commit(&B->c1_done);
                 }
                 __syncwarp();
@@ -741,9 +819,9 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 tc_fence_after();
                 if (elect_one()) {
                     // C3 = [A~N; Y_C] R0 (and [.; Y_P] R0)
-                    mma_k64(tmem + kC3, smem_u32(ay(v)), true, smem_u32(r0), idM);
+                    mma_k64_ka(tmem + kC3, smem_u32(ay(v)), smem_u32(r0), idM);
                     if (kTitans)
-                        mma_k64(tmem + kC3 + 64, smem_u32(ay(v)) + 128 * 128, true, smem_u32(r0), idM);
+                        mma_k64_ka(tmem + kC3 + 64, smem_u32(ay(v)) + 128 * 128, smem_u32(r0), idM);
                     mma_commit(&B->c3_done[v]);
                 }
                 __syncwarp();
