@@ -32,18 +32,20 @@
 //   C3: [A~N; Y_C; 0; Y_P] R0 (the read correction and the carry),
 // with an epilogue after each; everything else is prepared beside it.
 //
-// Roles (448 threads, one CTA per (b, h) sequence, all 64 rows of the state):
-//   warps 0,1,4,5   reads: token t = TMEM lane 0..63, 32 columns each
+// Roles (512 threads, one CTA per (b, h) sequence, all 64 rows of the state):
+//   warps 0,1       reads: token t = TMEM lane 0..63, all 64 columns
 //   warps 2,3,6,7   state: E1 (R0 for token = TMEM lane 64..127) and E3 (the
 //                   update; thread j holds W[r][j], S[r][j] for 32 rows r in
 //                   fp32 registers and writes their bf16 copy)
-//   warps 8-11      preparation, one tile ahead of the chain: gates (loaded a
-//                   tile early), C[t][s] by columns (one lane per column) into
-//                   shared memory with the vector scans beside it, the scores
-//                   [Q; K] K^T (MMA), the weighted rows of A~ and L, row-scaled
-//                   copies of K (the MN-major operand K^T diag C, K^T diag Pm),
-//                   and N applied to both by two MMA rounds ((I - L), then
-//                   (I + L^2))
+//   warps 4,5,10,11 preparation, first group, one tile ahead of the chain:
+//                   gates (loaded a tile early), C[t][s] by columns (one lane
+//                   per column) with the vector scans beside it, the scores
+//                   [Q; K] K^T (MMA), the weighted rows of A~ and L, (I - L),
+//                   and row-scaled copies of K (the MN-major operand
+//                   K^T diag C, K^T diag Pm)
+//   warps 8,9,14,15 preparation, second group: N applied to those operands by
+//                   two MMA rounds ((I - L), then I + L^2), one tile behind the
+//                   first group, so the two groups' latencies overlap
 //   warp 12         TMA producer (Q, K, V tiles of 64 tokens, three stages)
 //   warp 13         issues C1 and C3
 // Every wait is bounded; a wait that runs out sets the status word, all roles
@@ -67,7 +69,7 @@ using namespace tc;
 
 constexpr int kD = 64;              // d_k = d_v
 constexpr int kTile = 64;           // tokens per tile
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kNS = 3;              // input stages
 constexpr uint32_t kTileBytes = 8192;                 // 64 rows x 128 bytes of bf16
 constexpr uint32_t kStageBytes = 3 * kTileBytes;      // Q, K, V
@@ -88,8 +90,9 @@ constexpr uint32_t kVecBytes = 4096;
 struct Bars {
     uint64_t full[kNS], empty[kNS];
     uint64_t c1_done, c1_free, r0_ready, c3_free, ws_ready, pr_done;
-    uint64_t ay_ready[2], c3_done[2], vec_ready[2], vec_free[2], p1_done[2];
-    uint64_t drain[2];
+    uint64_t ay_ready[2], c3_done[2], vec_ready[2], vec_free[2], p1_done[2], ops_ready[2];
+    uint64_t ap_free;
+    uint64_t drain[3];
     long long wait_limit;
     uint32_t tmem_base;
     int abort;
@@ -107,7 +110,7 @@ __host__ __device__ constexpr Layout make_layout() {
     L.ap = o;     o += kOpBytes;           // between the two preparation rounds
     L.r0 = o;     o += kTileBytes;         // R0 [s][r] (MN-major B)
     L.ws = o;     o += 2 * kTileBytes;     // bf16 W^T [j][r] then S^T [j][r] (MN-major B)
-    L.il = o;     o += kTileBytes;         // (I - L) [s][u] (MN-major B)
+    L.il = o;     o += 2 * kTileBytes;     // (I - L) [s][u] (MN-major B), two tiles in flight
     L.b2 = o;     o += kTileBytes;         // (I + L^2) [s][u] (MN-major B)
     L.vec = o;    o += 2 * kVecBytes;
     L.bars = o;   o += (uint32_t)((sizeof(Bars) + 15) & ~size_t(15));
@@ -275,19 +278,21 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             mbar_init(&B->empty[s], 2);        // state warps + preparation warps
         }
         mbar_init(&B->c1_done, 1);
-        mbar_init(&B->c1_free, 4);             // read warps
+        mbar_init(&B->c1_free, 2);             // read warps
         mbar_init(&B->r0_ready, 4);            // state warps
-        mbar_init(&B->c3_free, 4);             // read warps
+        mbar_init(&B->c3_free, 2);             // read warps
         mbar_init(&B->ws_ready, 4);            // state warps
         mbar_init(&B->pr_done, 1);
+        mbar_init(&B->ap_free, 1);             // second preparation group
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B->ay_ready[i], 1);
             mbar_init(&B->c3_done[i], 1);
             mbar_init(&B->vec_ready[i], 1);    // the scan warp
-            mbar_init(&B->vec_free[i], 8);     // read warps + state warps
+            mbar_init(&B->vec_free[i], 6);     // read warps + state warps
             mbar_init(&B->p1_done[i], 1);
-            mbar_init(&B->drain[i], 1);
+            mbar_init(&B->ops_ready[i], 1);    // first preparation group
         }
+        for (int i = 0; i < 3; ++i) mbar_init(&B->drain[i], 1);
         B->wait_limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
         B->abort = 0;
         fence_mbar_init();
@@ -304,60 +309,56 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     constexpr uint32_t idM = idesc_bf16_f32(128, 64, 0, 1);   // B MN-major
     constexpr uint32_t idMM = idesc_bf16_f32(128, 64, 1, 1);  // A and B MN-major
 
-    if (warp < 8 && (warp & 3) < 2) {
+    const bool is_read = warp < 2;
+    const bool is_state = warp == 2 || warp == 3 || warp == 6 || warp == 7;
+    const bool is_p1 = warp == 4 || warp == 5 || warp == 10 || warp == 11;
+    const bool is_p2 = warp == 8 || warp == 9 || warp == 14 || warp == 15;
+
+    if (is_read) {
         // ------------------------------------------------------------- reads
-        const int h = warp >> 2;
-        const int t = 32 * (warp & 3) + lane;
+        // token t = TMEM lane 0..63, all 64 columns.  C3 of a tile is issued
+        // after the state's E1, which waited for C1, so once C3 is complete both
+        // products of the tile are in tensor memory.
+        const int t = 32 * warp + lane;
         bool ok = true;
         for (int g = 0; g < nt; ++g) {
             const int v = g & 1;
             const int n = min(kTile, T - g * kTile);
-            float qw[32], qs[32], dz[32];
-            if (ok) ok = wait_all(B, &B->c1_done, g & 1, status);
-            if (ok) {
-                tc_fence_after();
-                tmem_ld32(tl + kC1 + 32 * h, qw);
-                if (kTitans) tmem_ld32(tl + kC1 + 64 + 32 * h, qs);
-                tmem_wait_ld();
-                tc_fence_before();
-                warp_arrive(&B->c1_free);
-            }
             if (ok) ok = wait_all(B, &B->vec_ready[v], (g >> 1) & 1, status);
-            float bt = 1.f, ct = 0.f;
-            if (ok) {
-                bt = vec(v)[vBeta + t];
-                if (kTitans) ct = vec(v)[vCv + t];
-            }
             if (ok) ok = wait_all(B, &B->c3_done[v], (g >> 1) & 1, status);
             if (ok) {
+                const float bt = vec(v)[vBeta + t];
+                const float ct = kTitans ? vec(v)[vCv + t] : 0.f;
                 tc_fence_after();
-                tmem_ld32(tl + kC3 + 32 * h, dz);
-                tmem_wait_ld();
-                tc_fence_before();
-                warp_arrive(&B->c3_free);
-                if (t < n) {
-                    uint4 o[4];
-                    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+                uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.z) +
+                                                     ((size_t)seq * T + (size_t)g * kTile + t) * kD);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float qw[16], qs[16], dz[16];
+                    tmem_ld16(tl + kC1 + 16 * q, qw);
+                    if (kTitans) tmem_ld16(tl + kC1 + 64 + 16 * q, qs);
+                    tmem_ld16(tl + kC3 + 16 * q, dz);
+                    tmem_wait_ld();
+                    float zz[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        float z0 = bt * qw[2 * i] - 2.f * dz[2 * i];
-                        float z1 = bt * qw[2 * i + 1] - 2.f * dz[2 * i + 1];
-                        if (kTitans) {
-                            z0 += ct * qs[2 * i];
-                            z1 += ct * qs[2 * i + 1];
-                        }
-                        ow[i] = pack_bf16(z0, z1);
+                        zz[i] = fmaf(-2.f, dz[i], bt * qw[i]);
+                        if (kTitans) zz[i] = fmaf(ct, qs[i], zz[i]);
                     }
-                    uint4* zr = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.z) +
-                                                         ((size_t)seq * T + (size_t)g * kTile + t) * kD +
-                                                         32 * h);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) zr[i] = o[i];
+                    if (t < n) {
+                        zr[2 * q] = make_uint4(pack_bf16(zz[0], zz[1]), pack_bf16(zz[2], zz[3]),
+                                               pack_bf16(zz[4], zz[5]), pack_bf16(zz[6], zz[7]));
+                        zr[2 * q + 1] = make_uint4(pack_bf16(zz[8], zz[9]), pack_bf16(zz[10], zz[11]),
+                                                   pack_bf16(zz[12], zz[13]), pack_bf16(zz[14], zz[15]));
+                    }
                 }
+                tc_fence_before();
+                warp_arrive(&B->c1_free);
+                warp_arrive(&B->c3_free);
                 warp_arrive(&B->vec_free[v]);
             }
         }
-    } else if (warp < 8) {
+    } else if (is_state) {
         // ------------------------------------------------------------- state
         const int h = warp >> 2;
         const int j = 32 * ((warp & 3) - 2) + lane;   // E1: token; E3: key index
@@ -453,16 +454,17 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 if (a.S_out) a.S_out[idx] = s[i];
             }
         }
-    } else if (warp < 12) {
-        // ------------------------------------------------------- preparation
-        const int p = tid - 256;                 // TMEM lane 0..127
-        const bool issuer = warp == 8;
+    } else if (is_p1) {
+        // ----------------------------------------- preparation, first group
+        // Gates, coefficients, the scores and the weighted rows of tile g
+        // (one tile ahead of the chain); the second group applies N to them.
+        const int p = 32 * (warp & 3) + lane;    // TMEM lane 0..127 (warps 4, 5, 10, 11)
+        const bool issuer = warp == 4;
         const bool qside = p < 64;
         const int tr = qside ? p : p - 64;
         float* Ctab = reinterpret_cast<float*>(ap);   // the tile's C (fp32), until round 1
         const bool gated = a.eta || a.alpha;
         bool ok = true;
-        uint32_t pr_phase = 0;
         auto issue_p1 = [&](int g2) -> bool {
             const int st2 = g2 % kNS;
             if (!wait_all(B, &B->full[st2], (g2 / kNS) & 1, status)) return false;
@@ -508,6 +510,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             float* V = vec(v);
             uint8_t* X = ay(v);                  // [A~; L] rows 0..127 (K-major), then the C3 operand
             uint8_t* KCP = X + 128 * 128;        // [s][j]: K scaled by C[n-1][s], then by Pm[s]
+            uint8_t* ilv = il + v * kTileBytes;  // (I - L) of this tile
             if (issuer && ok && g + 1 < nt) ok = issue_p1(g + 1);
             if (ok && g >= 2) ok = wait_all(B, &B->vec_free[v], ((g - 2) >> 1) & 1, status);
             if (ok && g >= 2) ok = wait_all(B, &B->c3_done[v], ((g - 2) >> 1) & 1, status);
@@ -518,13 +521,18 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             }
             load_gates(g + 1);
             named_bar_sync(3, 128);
-            if (ok && gated && warp < 10) {
+            if (ok && gated && (warp == 4 || warp == 5)) {
+                // the coefficient table shares its buffer with the second group's
+                // operand between its rounds: wait until that group is done with it
+                if (g >= 1) ok = wait_all(B, &B->ap_free, (g - 1) & 1, status);
+            }
+            if (ok && gated && (warp == 4 || warp == 5)) {
                 // C[t][s] = theta_s w(s, t) by columns (lane = column s, rows in
                 // order): m(s,t) = eta_t m(s,t-1), w(s,t) = keep_t w(s,t-1) + m(s,t),
                 // both 0 before row s and 1 at it; above the diagonal C is 0.
                 // The rows' gates are loaded sixteen at a time into registers, so
                 // no load sits on the recurrence.
-                const int sc = lane + 32 * (warp - 8);
+                const int sc = lane + 32 * (warp & 3);
                 const float ths = V[vTh + sc];
                 float m = 0.f, wv = 0.f, ce = 0.f;
                 float* __restrict__ ct = Ctab;
@@ -551,9 +559,9 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 V[vCn + sc] = ce;              // C[n-1][s]
                 V[vPm + sc] = ths * m;         // theta_s prod_{j=s+1..n-1} eta_j (padded eta = 1)
             }
-            if (ok && !gated && warp < 10) {
+            if (ok && !gated && (warp == 4 || warp == 5)) {
                 // no momentum and no forgetting: C[t][s] = theta_s for s <= t
-                const int sc = lane + 32 * (warp - 8);
+                const int sc = lane + 32 * (warp & 3);
                 const float ths = V[vTh + sc];
                 V[vCn + sc] = sc <= n - 1 ? ths : 0.f;
                 V[vPm + sc] = sc == n - 1 ? ths : 0.f;
@@ -655,8 +663,8 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                         float iv[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) iv[i] = (16 * q4 + i == tr ? 1.f : 0.f) - val[i];
-                        st_chunk(il, tr, 16 * q4, iv);
-                        st_chunk(il, tr, 16 * q4 + 8, iv + 8);
+                        st_chunk(ilv, tr, 16 * q4, iv);
+                        st_chunk(ilv, tr, 16 * q4 + 8, iv + 8);
                     }
                 }
                 if (qside || kTitans) {
@@ -676,14 +684,35 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(3, 128);
-            if (ok && p == 0) mbar_arrive(&B->empty[st]);   // the scores and K reads are done
+            if (ok && p == 0) {
+                mbar_arrive(&B->empty[st]);      // the scores and K reads are done
+                mbar_arrive(&B->ops_ready[v]);   // the second group may start on this tile
+            }
+        }
+    } else if (is_p2) {
+        // ---------------------------------------- preparation, second group
+        // N = (I - L)(I + L^2) applied to [A~; K^T diag C; K^T diag Pm] of tile
+        // g by two MMA rounds, while the first group prepares tile g + 1.
+        const int p = 32 * (warp & 3) + lane;    // TMEM lane 0..127 (warps 8, 9, 14, 15)
+        const bool issuer = warp == 8;
+        const bool qside = p < 64;
+        const int tr = qside ? p : p - 64;
+        bool ok = true;
+        uint32_t pr_phase = 0;
+        for (int g = 0; g < nt; ++g) {
+            const int v = g & 1;
+            uint8_t* X = ay(v);
+            uint8_t* KCP = X + 128 * 128;
+            uint8_t* ilv = il + v * kTileBytes;
+            if (ok) ok = wait_all(B, &B->ops_ready[v], (g >> 1) & 1, status);
+            tc_fence_after();
             if (bsub < kTile) {
                 // round 1: [A~; L] (I - L) and [K^T diag C; K^T diag Pm] (I - L)
                 if (issuer && ok) {
                     tc_fence_after();
                     if (elect_one()) {
-                        mma_k64_ka(tmem + kPR, smem_u32(X), smem_u32(il), idM);
-                        mma_k64_ma(tmem + kPR + 64, smem_u32(KCP), smem_u32(il), idMM);
+                        mma_k64_ka(tmem + kPR, smem_u32(X), smem_u32(ilv), idM);
+                        mma_k64_ma(tmem + kPR + 64, smem_u32(KCP), smem_u32(ilv), idMM);
                         mma_commit(&B->pr_done);
                     }
                     __syncwarp();
@@ -730,7 +759,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(3, 128);
+                named_bar_sync(5, 128);
                 if (bsub == 16) {
                     // round 2: [A~(I-L); Y0_C(I-L)] (I + L^2) and [.; Y0_P(I-L)] (I + L^2)
                     if (issuer && ok) {
@@ -764,10 +793,13 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     }
                     fence_proxy_async_smem();
                     tc_fence_before();
-                    named_bar_sync(3, 128);
+                    named_bar_sync(5, 128);
                 }
             }
-            if (ok && p == 0) mbar_arrive(&B->ay_ready[v]);
+            if (ok && p == 0) {
+                mbar_arrive(&B->ap_free);
+                mbar_arrive(&B->ay_ready[v]);
+            }
         }
     } else if (warp == 12) {
         // ---------------------------------------------------------- producer
@@ -830,8 +862,8 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
     }
 
     // drain the MMAs of the two issuing warps before TMEM is released
-    if (warp == 8 || warp == 13) {
-        uint64_t* d = &B->drain[warp == 8 ? 0 : 1];
+    if (warp == 4 || warp == 8 || warp == 13) {
+        uint64_t* d = &B->drain[warp == 4 ? 0 : (warp == 8 ? 1 : 2)];
         if (elect_one()) mma_commit(d);
         __syncwarp();
         if (lane == 0) wait_drain(d, 0, B->wait_limit);
