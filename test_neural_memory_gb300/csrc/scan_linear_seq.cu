@@ -39,15 +39,15 @@
 //                   fp32 registers and writes their bf16 copy)
 //   warps 4,5,10,11 preparation, first group, one tile ahead of the chain:
 //                   gates (loaded a tile early), C[t][s] by columns (one lane
-//                   per column) with the vector scans beside it, the scores
-//                   [Q; K] K^T (MMA), the weighted rows of A~ and L, (I - L),
+//                   per column) with the vector scans beside it, then from
+//                   the scores [Q; K] K^T the weighted rows of A~ and L, (I - L),
 //                   and row-scaled copies of K (the MN-major operand
 //                   K^T diag C, K^T diag Pm)
 //   warps 8,9,14,15 preparation, second group: N applied to those operands by
 //                   two MMA rounds ((I - L), then I + L^2), one tile behind the
 //                   first group, so the two groups' latencies overlap
 //   warp 12         TMA producer (Q, K, V tiles of 64 tokens, three stages)
-//   warp 13         issues C1 and C3
+//   warp 13         issues C1 and C3, and the next tile's score MMA
 // Every wait is bounded; a wait that runs out sets the status word, all roles
 // run out their loops without further work, copies and MMAs drain, TMEM is
 // freed and the kernel returns.
@@ -90,9 +90,9 @@ constexpr uint32_t kVecBytes = 4096;
 struct Bars {
     uint64_t full[kNS], empty[kNS];
     uint64_t c1_done, c1_free, r0_ready, c3_free, ws_ready, pr_done;
-    uint64_t ay_ready[2], c3_done[2], vec_ready[2], vec_free[2], p1_done[2], ops_ready[2];
+    uint64_t ay_ready[2], c3_done[2], vec_ready[2], vec_free[2], p1_done[2], p1_free[2], ops_ready[2];
     uint64_t ap_free;
-    uint64_t drain[3];
+    uint64_t drain[2];
     long long wait_limit;
     uint32_t tmem_base;
     int abort;
@@ -291,8 +291,9 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             mbar_init(&B->vec_free[i], 6);     // read warps + state warps
             mbar_init(&B->p1_done[i], 1);
             mbar_init(&B->ops_ready[i], 1);    // first preparation group
+            mbar_init(&B->p1_free[i], 1);      // first preparation group (scores read)
         }
-        for (int i = 0; i < 3; ++i) mbar_init(&B->drain[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&B->drain[i], 1);
         B->wait_limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
         B->abort = 0;
         fence_mbar_init();
@@ -459,27 +460,11 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         // Gates, coefficients, the scores and the weighted rows of tile g
         // (one tile ahead of the chain); the second group applies N to them.
         const int p = 32 * (warp & 3) + lane;    // TMEM lane 0..127 (warps 4, 5, 10, 11)
-        const bool issuer = warp == 4;
         const bool qside = p < 64;
         const int tr = qside ? p : p - 64;
         float* Ctab = reinterpret_cast<float*>(ap);   // the tile's C (fp32), until round 1
         const bool gated = a.eta || a.alpha;
         bool ok = true;
-        auto issue_p1 = [&](int g2) -> bool {
-            const int st2 = g2 % kNS;
-            if (!wait_all(B, &B->full[st2], (g2 / kNS) & 1, status)) return false;
-            tc_fence_after();
-            if (elect_one()) {
-                const uint32_t sa = smem_u32(stage(st2));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kP1 + 64 * (g2 & 1), sdesc(sa + kk * 32, 16, 1024, 2),
-                             sdesc(sa + kTileBytes + kk * 32, 16, 1024, 2), idK, kk > 0);
-                mma_commit(&B->p1_done[g2 & 1]);
-            }
-            __syncwarp();
-            return true;
-        };
         // gates of token tr of tile gg (padded tokens: theta 0, eta = keep = 1),
         // loaded one tile ahead so that their latency overlaps a tile's work
         float th_n = 0.f, et_n = 1.f, kp_n = 1.f;
@@ -503,7 +488,6 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                         st_chunk(ay(sl) + 128 * 128 + kTileBytes, tr, 8 * c8, zero8);
         }
         load_gates(0);
-        if (issuer) ok = issue_p1(0);
         for (int g = 0; g < nt; ++g) {
             const int v = g & 1, st = g % kNS;
             const int n = min(kTile, T - g * kTile);
@@ -511,7 +495,6 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             uint8_t* X = ay(v);                  // [A~; L] rows 0..127 (K-major), then the C3 operand
             uint8_t* KCP = X + 128 * 128;        // [s][j]: K scaled by C[n-1][s], then by Pm[s]
             uint8_t* ilv = il + v * kTileBytes;  // (I - L) of this tile
-            if (issuer && ok && g + 1 < nt) ok = issue_p1(g + 1);
             if (ok && g >= 2) ok = wait_all(B, &B->vec_free[v], ((g - 2) >> 1) & 1, status);
             if (ok && g >= 2) ok = wait_all(B, &B->c3_done[v], ((g - 2) >> 1) & 1, status);
             if (ok && qside) {
@@ -686,6 +669,7 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
             named_bar_sync(3, 128);
             if (ok && p == 0) {
                 mbar_arrive(&B->empty[st]);      // the scores and K reads are done
+                mbar_arrive(&B->p1_free[v]);     // the score accumulator may be reused
                 mbar_arrive(&B->ops_ready[v]);   // the second group may start on this tile
             }
         }
@@ -829,7 +813,26 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
         __syncwarp();
     } else {
         // --------------------------------------------------- chain MMA issue
+        // Also issues the score MMA [Q; K] K^T of the next tile, so that the
+        // wait for a free tensor pipe stays off the preparation's path.
         bool ok = true;
+        auto issue_scores = [&](int g2) -> bool {
+            const int st2 = g2 % kNS;
+            if (!wait_all(B, &B->full[st2], (g2 / kNS) & 1, status)) return false;
+            if (g2 >= 2 && !wait_all(B, &B->p1_free[g2 & 1], ((g2 - 2) >> 1) & 1, status)) return false;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t sa = smem_u32(stage(st2));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kP1 + 64 * (g2 & 1), sdesc(sa + kk * 32, 16, 1024, 2),
+                             sdesc(sa + kTileBytes + kk * 32, 16, 1024, 2), idK, kk > 0);
+                mma_commit(&B->p1_done[g2 & 1]);
+            }
+            __syncwarp();
+            return true;
+        };
+        ok = issue_scores(0);
         for (int g = 0; g < nt; ++g) {
             const int st = g % kNS, v = g & 1;
             if (ok) ok = wait_all(B, &B->full[st], (g / kNS) & 1, status);
@@ -843,6 +846,13 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                     mma_commit(&B->c1_done);
                 }
                 __syncwarp();
+            }
+            // the next tile's scores now if its operands have landed, else after C3
+            bool scored = g + 1 >= nt;
+            if (ok && !scored &&
+                __all_sync(0xffffffffu, mbar_try_wait(&B->full[(g + 1) % kNS], ((g + 1) / kNS) & 1))) {
+                ok = issue_scores(g + 1);
+                scored = true;
             }
             if (ok) ok = wait_all(B, &B->r0_ready, g & 1, status);
             if (ok) ok = wait_all(B, &B->ay_ready[v], (g >> 1) & 1, status);
@@ -858,12 +868,13 @@ linear_seq_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constan
                 }
                 __syncwarp();
             }
+            if (ok && !scored) ok = issue_scores(g + 1);
         }
     }
 
     // drain the MMAs of the two issuing warps before TMEM is released
-    if (warp == 4 || warp == 8 || warp == 13) {
-        uint64_t* d = &B->drain[warp == 4 ? 0 : (warp == 8 ? 1 : 2)];
+    if (warp == 8 || warp == 13) {
+        uint64_t* d = &B->drain[warp == 8 ? 0 : 1];
         if (elect_one()) mma_commit(d);
         __syncwarp();
         if (lane == 0) wait_drain(d, 0, B->wait_limit);
