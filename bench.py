@@ -486,12 +486,19 @@ def run_dgd(args, rank, world, dev):
     ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / args.steps
     if ttm.device_status() != ttm.OK:
         raise RuntimeError("device status")
+    kernel = ttm.last_kernel()
     es = 2 if w.dtype == "bf16" else 4
     byte_tok = 4 * w.d * es + 8                     # q, k, v, z and the two gates
     state = w.d * w.d * 4
     nbytes = w.tokens * byte_tok + w.B * w.H * 2 * state
-    peaks, src = load_peaks()
-    achieved = nbytes / (ms / 1e3) / 1e9
+    # chunk form per token: [Q; K] W^T, A~N R0 and Y R0, plus the pre-pass's
+    # scores [Q; K] K^T, A~N and Y = K^T diag(r) N per 64-token chunk
+    dk = dv = w.d
+    c = 64
+    flops_tok = (4 * dk * dv + 2 * c * dv + 2 * dk * dv +
+                 (2 * 2 * c * c * dk + 2 * c * c * c + 2 * dk * c * c) / c)
+    rl = roof(flops_tok * w.tokens, nbytes, ms / 1e3, kernel == "dgd_step")
+    rl.update({"kernel": kernel, "traffic": None})
     line = {
         "metric": "DGD-memory scan tokens/s (ttm_dgd_fwd) on 1 GB300",
         "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
@@ -501,11 +508,8 @@ def run_dgd(args, rank, world, dev):
         "config": {"workload": w.name + " (DGD update)", "B": w.B, "H": w.H, "T": w.T,
                    "d": w.d, "chunk": w.chunk, "kind": "dgd",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": "inputs larger than L2 (no flush needed)", "kernel": "linear_step (DGD)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "peak_source": src,
-                     "kernel": "linear_step (DGD)", "algorithmic_bytes": nbytes,
-                     "traffic": None},
+                   "l2": "inputs larger than L2 (no flush needed)", "kernel": kernel},
+        "roofline": rl,
         "e2e": None, "gpu_launches": launches, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

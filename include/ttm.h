@@ -88,8 +88,10 @@ typedef enum {
     TTM_KID_MLP_SIMT = 2,      /* fp32 CUDA-core chunked scan, 2-layer memory */
     TTM_KID_LINEAR_TC = 3,     /* tcgen05 + TMA chunked scan, linear memory */
     TTM_KID_MLP_TC = 4,        /* tcgen05 chunked scan, 2-layer memory */
-    TTM_KID_LINEAR_SEQ = 5     /* tcgen05 + TMA scan, one CTA per sequence, d = 64,
+    TTM_KID_LINEAR_SEQ = 5,    /* tcgen05 + TMA scan, one CTA per sequence, d = 64,
                                   gradient points every 16 or 32 tokens */
+    TTM_KID_DGD_STEP = 6,      /* fp32 CUDA-core token loop, DGD memory */
+    TTM_KID_DGD_TC = 7         /* tcgen05 + TMA chunk form, DGD memory (pre-pass + scan) */
 } ttm_kernel_id;
 
 /*
@@ -354,18 +356,39 @@ int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
  *     (both required when T > 0); W0: [B or 1][H][dv][dk] fp32 (1 when
  *     w0_shared_over_batch); z: [B][H][T][dv] in dtype and W_out: [B][H][dv][dk]
  *     fp32, written.  W_out may be W0 (in place) when W0 is not shared.
+ *   workspace: device scratch of ttm_dgd_workspace_size() bytes for these sizes
+ *     (NULL when that is 0), owned by the caller, no overlap with any other
+ *     argument.
  *   All pointers are device memory owned by the caller, 16-byte aligned; no
  *   other overlap is allowed.
  * Shapes: B, H >= 1; T >= 0; chunk >= 1; dk, dv as for ttm_titans_fwd, dk <= 512
- * (else TTM_ERR_UNSUPPORTED).  Computed in fp32, token by token per row of M
- * (every row evolves on its own): one warp per (sequence, row).  Asynchronous on
- * `stream`; TTM_ERR_INVALID_ARG for malformed arguments, TTM_ERR_CUDA if the
- * launch fails. */
+ * (else TTM_ERR_UNSUPPORTED).  Kernels (under the ttm_set_kernel_policy policy):
+ *   - bf16, dk = dv in {64, 128}, chunk 64: the chunk form on the tensor cores.
+ *     With a_t the product of the chunk's alpha up to t and R[t][s] the product
+ *     of alpha over s < tau < t, the chunk's gradients g solve the unit
+ *     lower-triangular system (I + L) g = R0, L[t][s] = eta_t R[t][s] (k_s.k_t),
+ *     R0_t = eta_t ((a_{t-1} + 1) Mc k_t - v_t); a pre-pass computes, for every
+ *     chunk at once, N = (I + L)^-1 in fp32 and the chunk operators
+ *     A~N (A~[t][s] = R[t][s] (q_t.k_s), s < t) and K^T diag(R[n-1][.]) N in
+ *     bf16 into the workspace (8192 + 128 dk + 1024 bytes per (sequence,
+ *     64-token chunk)); the scan then applies them with two tensor-core
+ *     products per chunk.  Operands bf16, accumulation fp32.
+ *   - otherwise (or under TTM_KERNEL_SIMT): fp32, token by token per row of M
+ *     (every row evolves on its own), one warp per (sequence, row); no
+ *     workspace.
+ * Asynchronous on `stream`; TTM_ERR_INVALID_ARG for malformed arguments or a
+ * short workspace, TTM_ERR_CUDA if the launch fails. */
 int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                 const void* q, const void* k, const void* v,
                 const float* eta, const float* alpha,
                 const float* W0, int w0_shared_over_batch,
-                void* z, float* W_out, void* stream);
+                void* z, float* W_out, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* Bytes of workspace ttm_dgd_fwd needs for these sizes under the current
+ * kernel policy: B*H*ceil(T/64) * (8192 + 128 dk + 1024) on the tensor-core
+ * path, else 0 (also for shapes no kernel takes). */
+size_t ttm_dgd_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
 
 /* Decode step of the DGD memory: continues every sequence by n tokens from the
  * state W at in-chunk position pos, exactly as ttm_titans_step does for the

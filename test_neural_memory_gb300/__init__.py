@@ -22,7 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
 F32, BF16 = 0, 1
 POLICY = {"auto": 0, "simt": 1, "tc": 2}
 KERNEL_NAMES = {0: "none", 1: "linear_simt", 2: "mlp_simt", 3: "linear_tc", 4: "mlp_tc",
-                5: "linear_seq"}
+                5: "linear_seq", 6: "dgd_step", 7: "dgd_tc"}
 
 _lib = None
 
@@ -51,7 +51,9 @@ def lib() -> ctypes.CDLL:
         L.ttm_mlp_gelu.argtypes = [p, p, p, i, p]
         L.ttm_titans_step.argtypes = [i] * 8 + [p] * 6 + [p] * 4 + [p]
         L.ttm_linear_step.argtypes = [i] * 8 + [p] * 4 + [p] * 3 + [p]
-        L.ttm_dgd_fwd.argtypes = [i] * 7 + [p] * 5 + [p, i, p, p, p]
+        L.ttm_dgd_fwd.argtypes = [i] * 7 + [p] * 5 + [p, i, p, p, p, sz, p]
+        L.ttm_dgd_workspace_size.argtypes = [i] * 7
+        L.ttm_dgd_workspace_size.restype = sz
         L.ttm_lmm_layer_workspace_size.argtypes = [i] * 6
         L.ttm_lmm_layer_workspace_size.restype = sz
         L.ttm_lmm_layer_fwd.argtypes = ([i] * 6 + [p] * 5 + [ctypes.c_float, p, i, p, p, p, p, sz,
@@ -302,19 +304,30 @@ def titans_step(q, k, v, theta, W, chunk, pos, *, eta=None, alpha=None, S=None, 
     return z, Wc, (pos + n) % chunk
 
 
+def dgd_workspace_size(B, H, T, dk, dv, chunk, dtype_code) -> int:
+    """Workspace bytes the DGD scan needs under the current policy."""
+    return int(lib().ttm_dgd_workspace_size(B, H, T, dk, dv, int(chunk), dtype_code))
+
+
 def dgd_fwd(q, k, v, eta, alpha, W0, chunk, *, w0_shared=False, z=None, W_out=None,
-            stream=None):
+            workspace=None, stream=None):
     """DGD memory scan ("Nested Learning" eqs (88), (93)): eta is the step and alpha the
-    retention factor ([B,H,T] fp32).  W0: [B|1,H,dv,dk] fp32.  Returns (z, W_out)."""
+    retention factor ([B,H,T] fp32).  W0: [B|1,H,dv,dk] fp32.  The workspace the
+    tensor-core path needs is allocated here unless given.  Returns (z, W_out)."""
     import torch
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     z = torch.empty_like(v) if z is None else z
     W_out = (torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
              if W_out is None else W_out)
+    if workspace is None:
+        n = dgd_workspace_size(B, H, T, dk, dv, chunk, _dtype_code(q))
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().ttm_dgd_fwd(B, H, T, dk, dv, int(chunk), _dtype_code(q), _ptr(q), _ptr(k),
                              _ptr(v), _ptr(eta), _ptr(alpha), _ptr(W0), int(bool(w0_shared)),
-                             _ptr(z), _ptr(W_out), _stream(q, stream)), "ttm_dgd_fwd")
+                             _ptr(z), _ptr(W_out), _ptr(workspace), wsb, _stream(q, stream)),
+           "ttm_dgd_fwd")
     return z, W_out
 
 

@@ -76,6 +76,23 @@ struct StepArgs {
     int w_shared;
 };
 
+// One call of the DGD memory scan in chunk form (scan_dgd_tc.cu): eta is the
+// step and alpha the retention factor, [B][H][T] fp32, both required.
+struct DgdArgs {
+    int B, H, T, dk, dv, chunk;
+    int bf16;
+    const void *q, *k, *v;
+    const float *eta, *alpha;
+    const float* W0;          // [B or 1][H][dv][dk]
+    int shared;
+    void* z;
+    float* W_out;
+    void* workspace;          // caller-provided device scratch
+    size_t workspace_bytes;
+    int* status;              // device status word (bounded waits)
+    long long wait_cycles;    // bounded-wait limit in SM clock cycles (0: default)
+};
+
 // One call of the gradient of the linear / Titans scan (scan_bwd.cu).  Inputs
 // as in LinearArgs plus the adjoints of the outputs; every output is a
 // gradient of the same shape as its input (dq / dk / dv in the input dtype,
@@ -151,6 +168,14 @@ cudaError_t linear_seq_launch(const LinearArgs& a, cudaStream_t s);
 // d = 64, hidden = 256, chunk 16; one cluster of two CTAs per sequence.
 bool mlp_tc_supported(const MlpArgs& a);
 cudaError_t mlp_tc_launch(const MlpArgs& a, cudaStream_t s);
+// tcgen05 + TMA kernels of the DGD memory in chunk form (scan_dgd_tc.cu):
+// bf16, d_k = d_v in {64, 128}, chunk 64.  A pre-pass writes per chunk the
+// operators A~N and K^T diag(r) N (dgd_tc_workspace_bytes() of workspace), then
+// the scan runs one CTA per (sequence, 16 rows of the memory).
+bool dgd_tc_supported(const DgdArgs& a);
+size_t dgd_tc_workspace_bytes(const DgdArgs& a);
+cudaError_t dgd_tc_launch(const DgdArgs& a, cudaStream_t s);
+
 // Decode step (step.cu): one warp per row of W; dk <= 512.
 bool linear_step_supported(const StepArgs& a);
 cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);

@@ -477,16 +477,48 @@ int ttm_linear_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
                           dtheta, nullptr, dW0, nullptr, workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+ttm::DgdArgs dgd_args(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+    ttm::DgdArgs a{};
+    a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.chunk = chunk;
+    a.bf16 = dtype == TTM_BF16;
+    return a;
+}
+
+// The chunk form on the tensor cores where it applies, else the fp32 token
+// loop of the decode kernel (which takes every shape up to dk = 512).
+int select_dgd(const ttm::DgdArgs& a) {
+    ttm::StepArgs s{};
+    s.B = a.B; s.H = a.H; s.n = a.T; s.dk = a.dk; s.dv = a.dv; s.chunk = a.chunk;
+    s.bf16 = a.bf16; s.mode = 1;
+    const bool tc_ok = ttm::dgd_tc_supported(a);
+    const bool simt_ok = ttm::linear_step_supported(s);
+    if (g_policy == TTM_KERNEL_TC) return tc_ok ? TTM_KID_DGD_TC : TTM_KID_NONE;
+    if (g_policy == TTM_KERNEL_SIMT) return simt_ok ? TTM_KID_DGD_STEP : TTM_KID_NONE;
+    return tc_ok ? TTM_KID_DGD_TC : (simt_ok ? TTM_KID_DGD_STEP : TTM_KID_NONE);
+}
+
+}  // namespace
+
+size_t ttm_dgd_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+    if (B < 1 || H < 1 || T < 1 || chunk < 1) return 0;
+    if (dtype != TTM_F32 && dtype != TTM_BF16) return 0;
+    if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return 0;
+    const ttm::DgdArgs a = dgd_args(B, H, T, dk, dv, chunk, dtype);
+    return select_dgd(a) == TTM_KID_DGD_TC ? ttm::dgd_tc_workspace_bytes(a) : 0;
+}
+
 int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const void* q,
                 const void* k, const void* v, const float* eta, const float* alpha,
                 const float* W0, int w0_shared_over_batch, void* z, float* W_out,
-                void* stream) {
+                void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 1 || H < 1 || T < 0 || chunk < 1) return TTM_ERR_INVALID_ARG;
     if (dtype != TTM_F32 && dtype != TTM_BF16) return TTM_ERR_INVALID_ARG;
     if (!dims_ok(dk, dtype) || !dims_ok(dv, dtype)) return TTM_ERR_INVALID_ARG;
     if (!W0 || !W_out) return TTM_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !eta || !alpha || !z)) return TTM_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, eta, alpha, W0, z, W_out};
+    const void* ptrs[] = {q, k, v, eta, alpha, W0, z, W_out, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return TTM_ERR_INVALID_ARG;
     const int shared = w0_shared_over_batch ? 1 : 0;
@@ -501,6 +533,28 @@ int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const
         if (overlap(sz, i) || overlap(sW, i)) return TTM_ERR_INVALID_ARG;
     if (overlap(sz, sW) || overlap(sz, sW0)) return TTM_ERR_INVALID_ARG;
     if (bad_alias(sW, sW0, !shared)) return TTM_ERR_INVALID_ARG;   // in place when not shared
+    const Span swk{workspace, workspace_bytes};
+    for (const Span& i : ins)
+        if (overlap(swk, i)) return TTM_ERR_INVALID_ARG;
+    if (overlap(swk, sz) || overlap(swk, sW) || overlap(swk, sW0)) return TTM_ERR_INVALID_ARG;
+    ttm::DgdArgs g = dgd_args(B, H, T, dk, dv, chunk, dtype);
+    const int kid = select_dgd(g);
+    if (kid == TTM_KID_NONE) return TTM_ERR_UNSUPPORTED;
+    if (kid == TTM_KID_DGD_TC) {
+        if (!workspace || workspace_bytes < ttm::dgd_tc_workspace_bytes(g)) return TTM_ERR_INVALID_ARG;
+        int* status = status_ptr();
+        if (!status) return TTM_ERR_CUDA;
+        g.q = q; g.k = k; g.v = v; g.eta = eta; g.alpha = alpha;
+        g.W0 = W0; g.shared = shared; g.z = z; g.W_out = W_out;
+        g.workspace = workspace; g.workspace_bytes = workspace_bytes;
+        g.status = status; g.wait_cycles = g_wait_cycles.load();
+        if (injected_failure()) return TTM_ERR_CUDA;
+        if (ttm::dgd_tc_launch(g, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return TTM_ERR_CUDA;
+        __atomic_add_fetch(&g_launches, 2ULL, __ATOMIC_RELAXED);
+        t_last_kernel = kid;
+        return TTM_OK;
+    }
     ttm::StepArgs a{};
     a.B = B; a.H = H; a.n = T; a.dk = dk; a.dv = dv; a.chunk = chunk; a.pos = 0;
     a.bf16 = dtype == TTM_BF16;
@@ -510,9 +564,11 @@ int ttm_dgd_fwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, const
     a.mode = 1;
     a.W_in = W0; a.w_shared = shared;
     if (!ttm::linear_step_supported(a)) return TTM_ERR_UNSUPPORTED;
+    if (injected_failure()) return TTM_ERR_CUDA;
     if (ttm::linear_step_launch(a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TTM_ERR_CUDA;
     __atomic_add_fetch(&g_launches, 1ULL, __ATOMIC_RELAXED);
+    t_last_kernel = kid;
     return TTM_OK;
 }
 

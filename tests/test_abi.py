@@ -199,3 +199,32 @@ def test_bwd_workspace_size(L):
         assert (L.ttm_titans_bwd_workspace_size(2, 3, 130, 64, 64, 64, 0, 0) ==
                 2 * 3 * 3 * per_chunk)                         # fp32: CUDA-core forward
 
+
+
+def dgd_call(L, B=1, H=1, T=8, dk=64, dv=64, chunk=64, dt=1, q=P(0), k=P(1), v=P(2), eta=P(3),
+             alpha=P(4), W0=P(5), shared=0, z=P(6), W=P(7), ws=None, wsb=0):
+    return L.ttm_dgd_fwd(B, H, T, dk, dv, chunk, dt, q, k, v, eta, alpha, W0, shared, z, W, ws,
+                         wsb, None)
+
+
+@host_only
+def test_dgd_workspace_size_and_checks(L):
+    # chunk form: per (sequence, 64-token chunk) A~N (64 rows) and K^T diag(r) N (dk rows)
+    # of 128 bytes each, then 1024 bytes of vectors
+    with ttm.kernel_policy("auto"):
+        assert L.ttm_dgd_workspace_size(2, 3, 130, 128, 128, 64, 1) == 2 * 3 * 3 * (8192 + 16384 + 1024)
+        assert L.ttm_dgd_workspace_size(1, 2, 64, 64, 64, 64, 1) == 2 * (8192 + 8192 + 1024)
+        assert L.ttm_dgd_workspace_size(1, 1, 64, 64, 64, 64, 0) == 0     # fp32: token loop
+        assert L.ttm_dgd_workspace_size(1, 1, 64, 64, 64, 32, 1) == 0     # chunk 32: token loop
+        assert L.ttm_dgd_workspace_size(1, 1, 64, 96, 96, 64, 1) == 0     # d 96: token loop
+        assert L.ttm_dgd_workspace_size(1, 1, 0, 64, 64, 64, 1) == 0
+        # the chunk form without (enough) workspace is malformed; so is overlap
+        assert dgd_call(L) == INVALID
+        assert dgd_call(L, ws=P(9), wsb=100) == INVALID
+        assert dgd_call(L, ws=P(0), wsb=1 << 20) == INVALID
+        assert dgd_call(L, ws=P(9, 8), wsb=1 << 20) == INVALID           # misaligned
+    with ttm.kernel_policy("simt"):
+        assert L.ttm_dgd_workspace_size(2, 3, 130, 128, 128, 64, 1) == 0
+    with ttm.kernel_policy("tc"):
+        assert dgd_call(L, dt=0) == UNSUPPORTED                         # fp32 never on tensor cores
+        assert dgd_call(L, chunk=16) == UNSUPPORTED

@@ -1,8 +1,9 @@
 """GPU parity of the DGD memory ("Nested Learning" §8.1 eq (88) with the eq (93)
-objective, chunk-wise per §8.2): the scan ttm_dgd_fwd and the decode step
-ttm_dgd_step against the float64 oracle on the same seeded inputs.  Tolerance
-per output tensor: max|gpu - oracle| / max|oracle| below 1e-4 for fp32
-inputs and 2e-2 for bf16 inputs."""
+objective, chunk-wise per §8.2): the scan ttm_dgd_fwd (the fp32 token loop and
+the tensor-core chunk form) and the decode step ttm_dgd_step against the
+float64 oracle on the same seeded inputs.  Tolerance per output tensor:
+max|gpu - oracle| / max|oracle| below 1e-4 for fp32 inputs and 2e-2 for bf16
+inputs."""
 import pytest
 import torch
 
@@ -40,12 +41,15 @@ def oracle_run(inp, chunk, shared=False):
                              f(inp["alpha"]), f(inp["W0"]), chunk, shared_over_batch=shared)
 
 
-def gpu_run(inp, chunk, shared=False):
+def gpu_run(inp, chunk, shared=False, policy="auto", kernel=None):
     import test_neural_memory_gb300 as ttm
     d = H.to_dev(inp)
-    z, W = ttm.dgd_fwd(d["q"], d["k"], d["v"], d["eta"], d["alpha"], d["W0"], chunk,
-                       w0_shared=shared)
-    torch.cuda.synchronize()
+    with ttm.kernel_policy(policy):
+        z, W = ttm.dgd_fwd(d["q"], d["k"], d["v"], d["eta"], d["alpha"], d["W0"], chunk,
+                           w0_shared=shared)
+        torch.cuda.synchronize()
+        if kernel is not None:
+            assert ttm.last_kernel() == kernel
     return dict(z=z, W=W)
 
 
@@ -112,3 +116,69 @@ def test_prefill_then_decode(dtype):
     torch.cuda.synchronize()
     H.compare(dict(z=torch.cat(zs, dim=2), W=W), oracle_run(inp, chunk), ["z", "W"],
               H.TOL[dtype])
+
+
+# ---------------------------------------------------------------- chunk form
+# Tensor-core path (bf16, d_k = d_v in {64, 128}, chunk 64) under the "tc"
+# policy, so a shape it does not take fails instead of running elsewhere.
+
+TC_CASES = [
+    dict(B=1, Hh=1, T=1),            # one token
+    dict(B=1, Hh=2, T=64),           # exactly one chunk
+    dict(B=2, Hh=1, T=65),           # one token into the second chunk
+    dict(B=2, Hh=3, T=1000),         # many chunks, ragged last chunk (40 tokens)
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("case", range(len(TC_CASES)))
+def test_chunk_form_shapes(d, case):
+    c = TC_CASES[case]
+    inp = make("bf16", B=c["B"], Hh=c["Hh"], T=c["T"], d=d, seed=40 + case)
+    H.compare(gpu_run(inp, 64, policy="tc", kernel="dgd_tc"), oracle_run(inp, 64), ["z", "W"],
+              H.TOL["bf16"])
+
+
+def test_chunk_form_shared_initial_memory():
+    inp = make("bf16", B=3, Hh=2, T=300, d=128, seed=50, shared=True)
+    H.compare(gpu_run(inp, 64, shared=True, policy="tc", kernel="dgd_tc"),
+              oracle_run(inp, 64, shared=True), ["z", "W"], H.TOL["bf16"])
+
+
+def test_chunk_form_in_place_and_no_retention_decay():
+    """alpha = 1 (nothing forgotten) and W_out = W0 in place."""
+    import test_neural_memory_gb300 as ttm
+    inp = make("bf16", B=2, Hh=2, T=200, d=64, seed=51)
+    inp["alpha"] = torch.ones_like(inp["alpha"])
+    ref = oracle_run(inp, 64)
+    d = H.to_dev(inp)
+    W = d["W0"].clone()
+    with ttm.kernel_policy("tc"):
+        z, W2 = ttm.dgd_fwd(d["q"], d["k"], d["v"], d["eta"], d["alpha"], W, 64, W_out=W)
+        torch.cuda.synchronize()
+        assert ttm.last_kernel() == "dgd_tc"
+    assert W2.data_ptr() == W.data_ptr()
+    H.compare(dict(z=z, W=W), ref, ["z", "W"], H.TOL["bf16"])
+
+
+def test_chunk_form_matches_token_loop():
+    """The chunk form and the fp32 token loop agree to bf16-operand precision."""
+    inp = make("bf16", B=1, Hh=4, T=2000, d=128, seed=52)
+    a = gpu_run(inp, 64, policy="tc", kernel="dgd_tc")
+    b = gpu_run(inp, 64, policy="simt", kernel="dgd_step")
+    for n in ("z", "W"):
+        assert H.max_rel(H.f64(a[n]), H.f64(b[n])) < H.TOL["bf16"], n
+
+
+def test_chunk_form_long_context_workload():
+    """The long-context shape (B1 H16 T131072 d128, bf16, chunk 64) with the DGD
+    gates of the bench: the automatic choice is the chunk form; z and W of two
+    heads against the oracle."""
+    w = wl.WORKLOADS[4]
+    inp = wl.generate(w)
+    inp.update(wl.generate_dgd_gates(w.B, w.H, w.T, seed=77))
+    out = gpu_run(inp, w.chunk, kernel="dgd_tc")
+    heads = [0, 9]
+    sub = {n: inp[n][:, heads] for n in ("q", "k", "v", "eta", "alpha", "W0")}
+    ref = oracle_run(sub, w.chunk)
+    H.compare({n: out[n][:, heads] for n in ("z", "W")}, ref, ["z", "W"], H.TOL["bf16"])
