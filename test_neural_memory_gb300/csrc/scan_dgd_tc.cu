@@ -169,20 +169,21 @@ struct PrepBars {
 };
 
 struct PrepLayout {
-    uint32_t off_qk, off_aop, off_ks, off_L, off_g, off_bars, total;
+    uint32_t off_qk, off_aop, off_L, off_g, off_bars, total;
 };
 
-// [Q h][K h] per 64-column half (so [Q; K] is one 128-row operand), then
-// [A~][N^T] (K-major, 64 rows each), the row-scaled keys diag(r) K (same
-// layout as the key tiles: the MN-major operand K^T diag(r)), L (fp32), the
-// gate vectors.
+constexpr int kLStride = 68;    // floats per row of L (16-byte rows offsets apart: no bank conflicts)
+
+// [Q h][K h] per 64-column half (so [Q; K] is one 128-row operand; once the
+// scores are taken, the row-scaled keys diag(r) K, the MN-major operand
+// K^T diag(r), take the place of the query tiles), then [A~][N^T] (K-major,
+// 64 rows each), L (fp32), the gate vectors.
 __host__ __device__ constexpr PrepLayout prep_layout(int D) {
     PrepLayout L{};
     uint32_t off = 0;
     L.off_qk = off;   off += (D / 64) * 2 * kTile;
     L.off_aop = off;  off += 2 * kTile;
-    L.off_ks = off;   off += (D / 64) * kTile;
-    L.off_L = off;    off += 64 * 64 * 4;
+    L.off_L = off;    off += 64 * kLStride * 4;
     L.off_g = off;    off += 4 * 256;           // alpha, eta, r, a_{t-1}
     L.off_bars = off; off += (sizeof(PrepBars) + 15) & ~size_t(15);
     L.total = off;
@@ -209,7 +210,7 @@ dgd_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     int* status = a.status;
     uint8_t* qk = sm + L.off_qk;
     uint8_t* aop = sm + L.off_aop;      // A~ rows 0..63, then N^T rows 64..127
-    uint8_t* ks = sm + L.off_ks;
+    uint8_t* ks = qk;                   // diag(r) K over the query tiles (stride 2 tiles)
     float* Lf = reinterpret_cast<float*>(sm + L.off_L);
     float* g_al = reinterpret_cast<float*>(sm + L.off_g);
     float* g_et = g_al + 64;
@@ -307,18 +308,21 @@ dgd_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             } else {
 #pragma unroll
                 for (int s4 = 0; s4 < kChunk / 4; ++s4)
-                    reinterpret_cast<float4*>(Lf + t * 64)[s4] =
+                    reinterpret_cast<float4*>(Lf + t * kLStride)[s4] =
                         make_float4(S[4 * s4], S[4 * s4 + 1], S[4 * s4 + 2], S[4 * s4 + 3]);
             }
         }
-    } else if (ok) {
-        // row-scaled keys r_s k_s (same swizzled positions as the key tiles)
+    } else {
+        // row-scaled keys r_s k_s (same swizzled positions as the key tiles),
+        // over the query tiles once the score MMA has read them
         const int u = tid - 128;
+        if (ok) ok = wait_all(&B->A, &B->mma, 0, status);
 #pragma unroll
         for (int i = 0; i < 4 * NH; ++i) {
+            if (!ok) break;
             const int idx = u + 128 * i;            // 16-byte chunk: half, row, chunk
             const int h = idx >> 9, row = (idx >> 3) & 63, ch = idx & 7;
-            const uint32_t off = (uint32_t)h * kTile + row * 128 + ch * 16;
+            const uint32_t off = (uint32_t)h * 2 * kTile + row * 128 + ch * 16;
             const uint8_t* src = qk + h * 2 * kTile + kTile + row * 128 + ch * 16;
             float x[8];
             unpack8(*reinterpret_cast<const uint4*>(src), x);
@@ -340,7 +344,7 @@ dgd_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 #pragma unroll
         for (int t = 0; t < kChunk; ++t) {
             float acc0 = t == j ? 1.f : 0.f, acc1 = 0.f;
-            const float4* Lr = reinterpret_cast<const float4*>(Lf + t * 64);
+            const float4* Lr = reinterpret_cast<const float4*>(Lf + t * kLStride);
 #pragma unroll
             for (int s4 = 0; s4 < (t + 3) / 4; ++s4) {
                 const float4 l = Lr[s4];
@@ -369,7 +373,7 @@ dgd_prep_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                          idA, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < kChunk / 16; ++kk)
-                mma_bf16(tmem + 64, sdesc(kb + kk * 2048, kTile, 1024, 2),
+                mma_bf16(tmem + 64, sdesc(kb + kk * 2048, 2 * kTile, 1024, 2),
                          sdesc(nb + kk * 32, 16, 1024, 2), idY, kk > 0);
             mma_commit(&B->mma);
         }
