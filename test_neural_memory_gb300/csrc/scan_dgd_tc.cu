@@ -34,8 +34,8 @@
 // Scan (dgd_tc_kernel): one CTA per (sequence, slice of 16 rows of the
 // memory) runs the whole sequence.  Per chunk the state's chain is two
 // products: C1 = [Q; K] W_c^T (reads and gradient terms) -> R0 (epilogue) ->
-// C3 = [A~N; Y] R0 (read correction and update) -> W_{c+1} (registers) ->
-// its bf16 copy for the next C1.
+// C3 = Y R0 (the update) -> W_{c+1} (registers) -> its bf16 copy for the next
+// C1; the read correction (A~N) R0 is issued right after Y R0, off that chain.
 //
 // Roles of the scan CTA (288 threads):
 //   warps 0-3  state: thread j holds column j of the slice's 16 rows in fp32
@@ -641,6 +641,7 @@ dgd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
             const int st = c % NS, b = c & 1;
             if (ok) ok = wait_all(&B->A, &B->full[st], (c / NS) & 1, status);
             if (ok) ok = wait_all(&B->A, &B->acc1_ready[b], (c >> 1) & 1, status);
+            float r[16];
             if (ok) {
                 tc_fence_after();
                 float kw[16], v[16];
@@ -651,9 +652,14 @@ dgd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                 unpack8(vr[1], v + 8);
                 tmem_wait_ld();
                 tc_fence_before();
-                float r[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) r[i] = fmaf(ea1, kw[i], -et * v[i]);
+                // the previous chunk's read-correction product (committed after the
+                // state's) has read the R0 tile
+                if (c >= 1)
+                    ok = wait_all(&B->A, &B->c3z_done[(c - 1) & 1], ((c - 1) >> 1) & 1, status);
+            }
+            if (ok) {
                 st_chunk(r0t, t, 0, r);
                 st_chunk(r0t, t, 8, r + 8);
                 fence_proxy_async_smem();
@@ -671,11 +677,11 @@ dgd_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
                         for (int kk = 0; kk < kChunk / 16; ++kk)
                             mma_bf16(tmem + kAccY, sdesc(ra + kTile + kk * 32, 16, 1024, 2),
                                      sdesc(rb + kk * 2048, 8192, 1024, 2), id3, kk > 0);
+                        mma_commit(&B->c3_done);        // the state's product first
 #pragma unroll
                         for (int kk = 0; kk < kChunk / 16; ++kk)
                             mma_bf16(tmem + kAccZ + b * 16, sdesc(ra + kk * 32, 16, 1024, 2),
                                      sdesc(rb + kk * 2048, 8192, 1024, 2), id3, kk > 0);
-                        mma_commit(&B->c3_done);
                         mma_commit(&B->c3z_done[b]);
                     }
                     __syncwarp();
