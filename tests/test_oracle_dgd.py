@@ -134,3 +134,54 @@ def test_shared_initial_memory():
     r = oracle.dgd_primal(q, k, v, eta, alpha, W0, 3, shared_over_batch=True)
     r2 = oracle.dgd_primal(q, k, v, eta, alpha, np.repeat(W0, B, axis=0), 3)
     assert np.array_equal(r["z"], r2["z"]) and np.array_equal(r["W"], r2["W"])
+
+
+@pytest.mark.parametrize("T", [150, 64, 1])
+def test_operator_form_of_the_tensor_core_scan(T):
+    """The form the tensor-core kernels apply, restated here in float64: per chunk
+    of 64 (the last one padded with alpha = 1, eta = 0 and zero rows), with
+    R[t][s] = prod_{s<tau<t} alpha_tau built by products (no division), a_{t-1}
+    the retention up to t - 1 and r_s = prod_{tau>s} alpha_tau:
+      L = eta_t R (K K^T) (strictly lower), N = (I + L)^-1,
+      A~N = (R o Q K^T) N, Y = K^T diag(r) N,
+      R0 = diag(eta (a_- + 1)) K W_c^T - diag(eta) V,
+      Z = diag(a_-) Q W_c^T - A~N R0,  W_end^T = a_{n-1} W_c^T - Y R0.
+    It must give the token loop's reads and final memory."""
+    rng = np.random.default_rng(T + 7)
+    dk, dv, C = 6, 4, 64
+    q, k = rng.standard_normal((T, dk)), rng.standard_normal((T, dk)) / np.sqrt(dk)
+    v = rng.standard_normal((T, dv))
+    eta = rng.uniform(0.02, 0.2, T)
+    alpha = rng.uniform(0.85, 1.0, T)
+    W0 = rng.standard_normal((dv, dk))
+    z, W = _dgd(q, k, v, eta, alpha, W0, C)
+    Wt = W0.T.copy()
+    zs = []
+    for c0 in range(0, T, C):
+        n = min(C, T - c0)
+        Q, K, V = (np.zeros((C, x.shape[1])) for x in (q, k, v))
+        Q[:n], K[:n], V[:n] = q[c0:c0 + n], k[c0:c0 + n], v[c0:c0 + n]
+        et, al = np.zeros(C), np.ones(C)
+        et[:n], al[:n] = eta[c0:c0 + n], alpha[c0:c0 + n]
+        R = np.zeros((C, C))
+        for t in range(C):
+            p = 1.0
+            for s in range(t - 1, -1, -1):       # walk down from the diagonal
+                R[t, s] = p
+                p *= al[s]
+        a_prev = np.ones(C)
+        for t in range(1, C):
+            a_prev[t] = a_prev[t - 1] * al[t - 1]
+        r = np.ones(C)
+        for s in range(C - 2, -1, -1):
+            r[s] = r[s + 1] * al[s + 1]
+        a_end = a_prev[-1] * al[-1]
+        L = et[:, None] * R * (K @ K.T)
+        N = np.linalg.inv(np.eye(C) + L)
+        AN = (R * (Q @ K.T)) @ N
+        Y = (K.T * r[None, :]) @ N
+        R0 = (et * (a_prev + 1.0))[:, None] * (K @ Wt) - et[:, None] * V
+        zs.append((a_prev[:, None] * (Q @ Wt) - AN @ R0)[:n])
+        Wt = a_end * Wt - Y @ R0
+    assert np.allclose(z, np.concatenate(zs), atol=1e-11)
+    assert np.allclose(W, Wt.T, atol=1e-11)
