@@ -181,6 +181,127 @@ __global__ void __launch_bounds__(kLayerThreads, NJ <= 4 ? 4 : 2)
     }
 }
 
+constexpr int kStrip = 64;   // tokens per warp of the strip kernel
+constexpr int kGrp = 4;      // tokens per unrolled group
+
+// Strip variant of the prep kernel for d <= 128 and conv width <= 4: a warp walks
+// kStrip consecutive tokens of one (b, stream, head) with the conv window in
+// registers, so every projection row is loaded once (one vector load per lane),
+// the next group's rows are in flight while a group is computed, and the l2 norms
+// of a group's kGrp tokens share their shuffle rounds.
+template <int NJ, bool kVec>
+__global__ void __launch_bounds__(kLayerThreads, 3)
+    lmm_prep_strip_kernel(const LmmArgs a, const __nv_bfloat16* proj, __nv_bfloat16* qkv,
+                          float* gates) {
+    constexpr int NW = 4;                             // window: taps of a width-4 conv
+    __shared__ __align__(16) float taps[NW][32 * NJ];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, d = a.d, T = a.T, K = a.conv_k;
+    const int nstrip = (T + kStrip - 1) / kStrip;
+    const int ngroup = (nstrip + kPrepWarps - 1) / kPrepWarps;
+    long long bid = blockIdx.x;
+    const int grp = (int)(bid % ngroup);
+    bid /= ngroup;
+    const int h = (int)(bid % H);
+    bid /= H;
+    const int s = (int)(bid % 3);
+    const int b = (int)(bid / 3);
+    const int D = H * d, P = 4 * D + 3 * H;
+    const int c0 = s * D + h * d;                     // first channel of the head
+    // window slot j of token t is row t - (NW - 1) + j; its weight is tap j - (NW - K)
+    for (int x = threadIdx.x; x < NW * d; x += kLayerThreads) {
+        const int j = x / d, c = x % d;
+        const int tap = j - (NW - K);
+        taps[j][c] = tap >= 0 ? a.conv_w[(size_t)(c0 + c) * K + tap] : 0.f;
+    }
+    __syncthreads();
+    const int strip = grp * kPrepWarps + warp;
+    if (strip >= nstrip) return;
+    const int t0 = strip * kStrip, t1 = min(T, t0 + kStrip);
+    const int cl = lane * NJ;
+    float wt[NW][NJ];
+#pragma unroll
+    for (int j = 0; j < NW; ++j)
+#pragma unroll
+        for (int i = 0; i < NJ; ++i) wt[j][i] = taps[j][cl + i];
+    const __nv_bfloat16* src = proj + (size_t)b * T * P + c0 + cl;
+    auto load_row = [&](int t, bool live, float* out) {
+        if (live && t >= 0) {
+            load_vw<NJ, kVec>(src + (size_t)t * P, out);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NJ; ++i) out[i] = 0.f;
+        }
+    };
+    const size_t plane = (size_t)a.B * H * T;
+    if (s == 0) {   // the three gates of the strip's tokens of head h (lanes: t0 + lane, + 32)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int t = t0 + lane + 32 * r;
+            if (t < t1) {
+                const __nv_bfloat16* lg = proj + ((size_t)b * T + t) * P + 4 * D + h;
+                const size_t gi = ((size_t)b * H + h) * T + t;
+                gates[gi] = a.theta_scale * sigm(__bfloat162float(lg[0]));
+                gates[plane + gi] = sigm(__bfloat162float(lg[H]));
+                gates[2 * plane + gi] = sigm(__bfloat162float(lg[2 * H]));
+            }
+        }
+    }
+    float win[NW - 1][NJ], cur[kGrp][NJ], nxt[kGrp][NJ];
+#pragma unroll
+    for (int j = 0; j < NW - 1; ++j) load_row(t0 - (NW - 1) + j, true, win[j]);
+#pragma unroll
+    for (int i = 0; i < kGrp; ++i) load_row(t0 + i, t0 + i < t1, cur[i]);
+    const size_t stream_stride = (size_t)a.B * H * T * d;
+    __nv_bfloat16* dst = qkv + s * stream_stride + ((size_t)b * H + h) * T * d + cl;
+    for (int tg = t0; tg < t1; tg += kGrp) {
+#pragma unroll
+        for (int i = 0; i < kGrp; ++i) load_row(tg + kGrp + i, tg + kGrp + i < t1, nxt[i]);
+        float u[kGrp][NJ], ss[kGrp];
+#pragma unroll
+        for (int i = 0; i < kGrp; ++i) {
+            ss[i] = 0.f;
+#pragma unroll
+            for (int e = 0; e < NJ; ++e) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    const int r = i + j;              // row of [win; cur]
+                    const float xv = r < NW - 1 ? win[r][e] : cur[r - (NW - 1)][e];
+                    acc = fmaf(wt[j][e], xv, acc);
+                }
+                // SiLU; the fast intrinsics' error is far below the bf16 rounding of the output
+                u[i][e] = __fdividef(acc, 1.f + __expf(-acc));
+                ss[i] = fmaf(u[i][e], u[i][e], ss[i]);
+            }
+        }
+        if (s < 2) {   // l2-normalise q and k per head, the group's four sums together
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int i = 0; i < kGrp; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], off);
+#pragma unroll
+            for (int i = 0; i < kGrp; ++i) {
+                const float inv = 1.f / fmaxf(sqrtf(ss[i]), 1e-6f);
+#pragma unroll
+                for (int e = 0; e < NJ; ++e) u[i][e] *= inv;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGrp; ++i)
+            if (tg + i < t1) store_nj<NJ>(dst + (size_t)(tg + i) * d, u[i]);
+        // slide: the last NW - 1 rows of [win; cur] become the window
+#pragma unroll
+        for (int j = 0; j < NW - 1; ++j)
+#pragma unroll
+            for (int e = 0; e < NJ; ++e) win[j][e] = cur[kGrp - (NW - 1) + j][e];
+#pragma unroll
+        for (int i = 0; i < kGrp; ++i)
+#pragma unroll
+            for (int e = 0; e < NJ; ++e) cur[i][e] = nxt[i][e];
+    }
+}
+
 // One warp per (b, t, h): o = z / sqrt(mean(z^2) + eps) * rms_w * g; lane l
 // holds channels l VW ... of the head.
 template <int VW, bool kVec>
@@ -253,12 +374,32 @@ void post_vw(const LmmArgs& a, unsigned blocks, cudaStream_t s, const __nv_bfloa
 
 cudaError_t lmm_prep_launch(const LmmArgs& a, const void* proj, void* qkv, float* gates,
                             cudaStream_t s) {
+    auto p = static_cast<const __nv_bfloat16*>(proj);
+    auto q = static_cast<__nv_bfloat16*>(qkv);
+    if (a.d <= 128 && a.conv_k <= 4) {
+        // one block per (b, stream, head, kPrepWarps strips of kStrip tokens)
+        const long long nstrip = (a.T + kStrip - 1) / kStrip;
+        const unsigned blocks =
+            (unsigned)((long long)a.B * 3 * a.H * ((nstrip + kPrepWarps - 1) / kPrepWarps));
+        const bool vec = (4 * a.H * a.d + 3 * a.H) % (a.d / 32) == 0;
+        switch (a.d / 32) {
+            case 1: lmm_prep_strip_kernel<1, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, gates); break;
+            case 2:
+                if (vec) lmm_prep_strip_kernel<2, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, gates);
+                else lmm_prep_strip_kernel<2, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, gates);
+                break;
+            case 4:
+                if (vec) lmm_prep_strip_kernel<4, true><<<blocks, kLayerThreads, 0, s>>>(a, p, q, gates);
+                else lmm_prep_strip_kernel<4, false><<<blocks, kLayerThreads, 0, s>>>(a, p, q, gates);
+                break;
+            default: return cudaErrorInvalidValue;
+        }
+        return cudaGetLastError();
+    }
     // one block per (b, stream, head, kPrepWarps tiles)
     const long long ntile = (a.T + kTile - 1) / kTile;
     const unsigned blocks =
         (unsigned)((long long)a.B * 3 * a.H * ((ntile + kPrepWarps - 1) / kPrepWarps));
-    auto p = static_cast<const __nv_bfloat16*>(proj);
-    auto q = static_cast<__nv_bfloat16*>(qkv);
     switch (a.d / 32) {
         case 1: prep_nj<1>(a, blocks, s, p, q, gates); break;
         case 2: prep_nj<2>(a, blocks, s, p, q, gates); break;
