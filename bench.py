@@ -119,7 +119,7 @@ def kernel_source_digest(kernel_name: str) -> str:
     src = {"linear_simt": ["scan_simt.cu"], "mlp_simt": ["scan_simt.cu", "scan_mlp_simt.cu", "scan_mlp_cluster.cu"],
            "linear_tc": ["scan_linear_tc.cu"], "mlp_tc": ["scan_mlp_tc.cu"],
            "linear_seq": ["scan_linear_seq.cu"],
-           "linear_step": ["step.cu"]}.get(kernel_name)
+           "linear_step": ["step.cu"], "dgd_tc": ["scan_dgd_tc.cu"]}.get(kernel_name)
     if not src:
         return ""
     h = hashlib.sha256()
@@ -498,7 +498,8 @@ def run_dgd(args, rank, world, dev):
     flops_tok = (4 * dk * dv + 2 * c * dv + 2 * dk * dv +
                  (2 * 2 * c * c * dk + 2 * c * c * c + 2 * dk * c * c) / c)
     rl = roof(flops_tok * w.tokens, nbytes, ms / 1e3, kernel == "dgd_step")
-    rl.update({"kernel": kernel, "traffic": None})
+    rl.update({"kernel": kernel,
+               "traffic": profiled_traffic(kernel, f"dgd_workload{w.id}") if not args.T else None})
     line = {
         "metric": "DGD-memory scan tokens/s (ttm_dgd_fwd) on 1 GB300",
         "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,
