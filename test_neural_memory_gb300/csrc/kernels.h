@@ -113,7 +113,9 @@ struct BwdArgs {
     void* workspace;
     size_t workspace_bytes;
     int fwd_tc;     // 1: the tensor-core scan writes the checkpoints (bf16, d 64 / 128, chunk 64)
-    int* status;    // device status word of the tensor-core scan's bounded waits
+    int local_tc;   // 1: the local pass runs on the tensor cores (bf16, d 64 / 128, chunk 64)
+    int* status;    // device status word of the tensor-core kernels' bounded waits
+    long long wait_cycles;   // their wait limit in SM clock cycles (0: the default)
 };
 
 // One call of the LMM layer (lmm_layer.cu + the scan); bf16 activations.
@@ -179,6 +181,13 @@ cudaError_t dgd_tc_launch(const DgdArgs& a, cudaStream_t s);
 // Decode step (step.cu): one warp per row of W; dk <= 512.
 bool linear_step_supported(const StepArgs& a);
 cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
+
+// Tensor-core local pass of the gradient (scan_bwd_tc.cu): bf16, dk = dv in
+// {64, 128}, chunk 64; reads the chunk-start checkpoints and chunk-end adjoints
+// (fp32, [seq][chunk][W | S][dv][dk]) that the other passes leave in the workspace.
+bool bwd_local_tc_supported(const BwdArgs& a);
+cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
+                                cudaStream_t s);
 
 // Gradient of the linear / Titans scan (scan_bwd.cu): chunk <= 64, dk <= 128.
 // The workspace holds the state and its adjoint at every chunk boundary.

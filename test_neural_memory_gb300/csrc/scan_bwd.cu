@@ -950,7 +950,12 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
         return e;
     bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
     bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT2, sm2, s>>>(a, L, ws);
-    bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT3, sm3, s>>>(a, L, ws);
+    if (a.local_tc) {
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = bwd_local_tc_launch(a, ws + L.ckpt, ws + L.adj, s)) != cudaSuccess) return e;
+    } else {
+        bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT3, sm3, s>>>(a, L, ws);
+    }
     *launches += 3;
     if (a.shared) {
         const size_t n = (size_t)a.H * L.sd;

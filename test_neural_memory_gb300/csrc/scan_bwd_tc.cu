@@ -1,0 +1,722 @@
+// Tensor-core (tcgen05 + TMA) local pass of the scan's gradient (bf16 inputs,
+// d_k = d_v in {64, 128}, chunks of 64 tokens).
+//
+// The local pass gives, for one chunk of n tokens with the chunk-start state
+// (W, S) and the adjoint of the chunk-end state (dWe, dSe), the gradients of
+// the chunk's q, k, v and gates ("Continual Learning: From Attention to
+// Neural Memory" §4.5; the chunk form of "TTT layers 与 fast weights" §1.1
+// eqs (7)-(9) with the momentum / decay unrolling of "论文速览 | Titans"
+// §4.3, §4.5).  With E = K W^T - V (errors at the chunk start), the masked
+// scores A~[t][s] = C[t][s] (q_t . k_s) (s <= t), DE[t][s] = dz_t . e_s and
+// G = C o DE (s <= t):
+//   De = -2 (A~^T dZ + diag(C[n-1]) K dWe^T + diag(pm) K dSe^T),   dV = -De
+//   dQ = diag(beta) dZ W + diag(c) dZ S - 2 G K
+//   dK = De W - 2 G^T Q - 2 diag(C[n-1]) E dWe - 2 diag(pm) E dSe
+// and the gate gradients from dC = -2 (Q K^T) o DE (plus the end-state term
+// on the last row), dbeta_t = dz_t . (W q_t), dc_t = dz_t . (S q_t),
+// e_s . (dWe k_s), e_s . (dSe k_s) and <dWe, W>, <dWe, S>, <dSe, S>, carried
+// back through the coefficient recurrences exactly as the CUDA-core pass
+// does.
+//
+// Every contraction is a tcgen05 MMA with M = 128: the token-row products
+// stack [K; Q] (or pad with rows that are never read back), and the products
+// whose rows are tokens and whose result is d wide are taken transposed
+// (dQ^T, dK^T: rows = key index j).  The state and adjoint matrices come in
+// fp32 from the checkpoints and are rounded to bf16 in shared memory, one
+// half of their rows (the value index i) at a time; DE, De, dQ^T and dK^T
+// accumulate over the halves in tensor memory.  One CTA of 256 threads per
+// (sequence, chunk), every chunk at once.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/ttm.h"
+#include "kernels.h"
+#include "simt_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace ttm {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;              // tokens per chunk (== TMA tile height)
+constexpr uint32_t kTile = 8192;    // 64 rows x 128 bytes (bf16)
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kLdc = kC + 1;        // row stride of the fp32 tables
+constexpr long long kWaitCycles = 4000000000LL;
+
+// TMEM columns (each accumulator 64 columns; lanes = rows)
+constexpr uint32_t kA1 = 0;     // [K; Q] W_I^T   (lanes 0-63: K W^T, 64-127: Q W^T); QK first
+constexpr uint32_t kA2 = 64;    // [K; Q] S_I^T   (lanes 64-127: Q S^T)
+constexpr uint32_t kA3 = 128;   // [K; Q] dWe_I^T (lanes 0-63: K dWe^T)
+constexpr uint32_t kA4 = 192;   // [K; Q] dSe_I^T (lanes 0-63: K dSe^T)
+constexpr uint32_t kDE = 256;   // DE (lanes t, columns s)
+constexpr uint32_t kDeI = 320;  // De of the half (lanes s, columns i)
+constexpr uint32_t kDQ = 384;   // dQ^T (lanes j, columns t)
+constexpr uint32_t kDK = 448;   // dK^T (lanes j, columns s)
+
+struct Layout {
+    uint32_t kq, dz, vv, mat, ei, ec, ep, bz, cz, dei, at, gg, qkb, cm, vec, bars, total;
+};
+
+// [K_h][Q_h] per 64-column half of the keys (so [K; Q] is one 128-row
+// operand); dZ and V per half of the value index; the four state / adjoint
+// matrices of the current value half (rows i, bf16, one tile per key half);
+// the bf16 operand tiles of the chunk; the fp32 coefficient table; vectors.
+__host__ __device__ constexpr Layout make_layout(int D) {
+    Layout L{};
+    uint32_t o = 0;
+    const uint32_t NH = D / 64;
+    L.kq = o;   o += NH * 2 * kTile;
+    L.dz = o;   o += NH * kTile;
+    L.vv = o;   o += NH * kTile;
+    L.mat = o;  o += 4 * NH * kTile;     // W, S, dWe, dSe of the value half
+    L.ei = o;   o += kTile;              // E of the half [s][i]
+    L.ec = o;   o += kTile;              // -2 C[n-1][s] E
+    L.ep = o;   o += kTile;              // -2 pm[s] E
+    L.bz = o;   o += kTile;              // beta_t dZ [t][i]
+    L.cz = o;   o += kTile;              // c_t dZ
+    L.dei = o;  o += kTile;              // De of the half [s][i]
+    L.at = o;   o += kTile;              // -2 A~ [t][s]
+    L.gg = o;   o += kTile;              // -2 G [t][s]
+    L.qkb = o;  o += kC * kC * 2;        // Q K^T (bf16, plain [t][s])
+    L.cm = o;   o += kC * kLdc * 4;      // C (fp32)
+    L.vec = o;  o += 16 * kC * 4;        // gate vectors
+    L.bars = o; o += 64;
+    L.total = o;
+    return L;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+}
+
+__device__ __forceinline__ void unpack8(uint4 v, float* x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// byte offset of 16-byte chunk c of row r in a 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4); }
+
+struct Sync {
+    uint64_t full, mma;
+    long long limit;
+    int abort;
+    uint32_t tmem;
+};
+
+// Bounded wait by every thread of the block (uniform answer per warp).
+__device__ __noinline__ bool wait_bar(Sync* Y, uint64_t* bar, uint32_t parity, int* status) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const long long t0 = clock64();
+    bool ok = true;
+    while (!mbar_try_wait_sleep(bar, parity, 20000)) {
+        if (*(volatile int*)&Y->abort || clock64() - t0 > Y->limit) {
+            *(volatile int*)&Y->abort = 1;
+            atomicExch(status, TTM_ERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap vmap,
+                    const BwdArgs a, const float* ckpt, const float* adj, int nch) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    constexpr Layout L = make_layout(D);
+    constexpr int NH = D / 64, KS = D / 16;
+    Sync* Y = reinterpret_cast<Sync*>(sm + L.bars);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq = blockIdx.x / nch, c = blockIdx.x % nch;
+    const int T = a.T;
+    const int n = min(kC, T - c * kC);
+    const size_t tok0 = (size_t)seq * T + (size_t)c * kC;
+    const size_t sd = (size_t)D * D;
+    int* status = a.status;
+
+    uint8_t* kq = sm + L.kq;
+    auto ktile = [&](int h) { return kq + h * 2 * kTile; };
+    auto qtile = [&](int h) { return kq + h * 2 * kTile + kTile; };
+    auto dztile = [&](int h) { return sm + L.dz + h * kTile; };
+    auto vtile = [&](int h) { return sm + L.vv + h * kTile; };
+    auto mtile = [&](int m, int h) { return sm + L.mat + (m * NH + h) * kTile; };   // m: W S dWe dSe
+    uint8_t* ei = sm + L.ei;
+    uint8_t* ec = sm + L.ec;
+    uint8_t* ep = sm + L.ep;
+    uint8_t* bz = sm + L.bz;
+    uint8_t* cz = sm + L.cz;
+    uint8_t* dei = sm + L.dei;
+    uint8_t* at = sm + L.at;
+    uint8_t* gg = sm + L.gg;
+    __nv_bfloat16* qkb = reinterpret_cast<__nv_bfloat16*>(sm + L.qkb);
+    float* Cm = reinterpret_cast<float*>(sm + L.cm);
+    float* th = reinterpret_cast<float*>(sm + L.vec);
+    float* et = th + kC;
+    float* al = et + kC;
+    float* beta = al + kC;
+    float* P = beta + kC;
+    float* cc = P + kC;
+    float* pm = cc + kC;
+    float* dbeta = pm + kC;
+    float* dcc = dbeta + kC;
+    float* dclast = dcc + kC;
+    float* dpm = dclast + kC;
+    float* dkeep = dpm + kC;
+    float* deta = dkeep + kC;
+    float* dth = deta + kC;
+    float* scal = dth + kC;          // <dWe, W>, <dWe, S>, <dSe, S>
+
+    if (tid == 0) {
+        mbar_init(&Y->full, 1);
+        mbar_init(&Y->mma, 1);
+        Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
+        Y->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&Y->tmem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = Y->tmem;
+    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);   // this warp's TMEM lanes
+    const int row = (warp & 3) * 32 + lane;                          // TMEM lane of this thread
+    const int chalf = warp >> 2;                                     // column half of an epilogue
+
+    if (tid == 0) {
+        mbar_expect_tx(&Y->full, 4 * NH * kTile);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            tma_load_3d(ktile(h), &kmap, &Y->full, 64 * h, c * kC, seq);
+            tma_load_3d(qtile(h), &qmap, &Y->full, 64 * h, c * kC, seq);
+            tma_load_3d(dztile(h), &zmap, &Y->full, 64 * h, c * kC, seq);
+            tma_load_3d(vtile(h), &vmap, &Y->full, 64 * h, c * kC, seq);
+        }
+    }
+    if (tid < kC) {
+        th[tid] = tid < n ? a.theta[tok0 + tid] : 0.f;
+        et[tid] = (tid < n && a.eta) ? a.eta[tok0 + tid] : 0.f;
+        al[tid] = (tid < n && a.alpha) ? a.alpha[tok0 + tid] : 0.f;
+        dbeta[tid] = dcc[tid] = dclast[tid] = dpm[tid] = dkeep[tid] = deta[tid] = 0.f;
+        beta[tid] = P[tid] = cc[tid] = 0.f;
+    }
+    if (tid < 4) scal[tid] = 0.f;
+    __syncthreads();
+    simt::block_coefficients(n, kC, th, et, al, beta, P, cc, Cm, kLdc, pm);   // ends in a barrier
+
+    const float* ck = ckpt + ((size_t)seq * nch + c) * 2 * sd;
+    const float* ad = adj + ((size_t)seq * nch + c) * 2 * sd;
+    uint32_t mma_phase = 0;
+    bool ok = wait_bar(Y, &Y->full, 0, status);
+
+    constexpr uint32_t idKK = idesc_bf16_f32(128, 64, 0, 0);   // A K-major, B K-major
+    constexpr uint32_t idMM = idesc_bf16_f32(128, 64, 1, 1);   // both MN-major
+    constexpr uint32_t idMK = idesc_bf16_f32(128, 64, 1, 0);   // A MN-major, B K-major
+
+    // [K; Q] K^T -> lanes 64-127 of kA1: Q K^T
+    if (warp == 0 && ok) {
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const uint32_t base = smem_u32(ktile(kk >> 2)) + (kk & 3) * 32;
+                mma_bf16(tmem + kA1, sdesc(base, 16, 1024, 2), sdesc(base, 16, 1024, 2), idKK, kk > 0);
+            }
+            mma_commit(&Y->mma);
+        }
+        __syncwarp();
+    }
+
+    // fp32 state / adjoint rows of value half I -> bf16 tiles [i][j] (and the
+    // three inner products of the end-state term); beta dZ, c dZ of the half
+    auto convert_half = [&](int I) {
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f;
+        constexpr int kChunks = 64 * (D / 8);                  // (row, 8-column chunk) pairs
+        for (int x = tid; x < kChunks; x += kThreads) {
+            const int i = x / (D / 8), c8 = x % (D / 8);
+            const size_t g = (size_t)(64 * I + i) * D + 8 * c8;
+            float w[8], s[8], gw[8], gs[8];
+            const float4* pw = reinterpret_cast<const float4*>(ck + g);
+            const float4* ps = reinterpret_cast<const float4*>(ck + sd + g);
+            const float4* pgw = reinterpret_cast<const float4*>(ad + g);
+            const float4* pgs = reinterpret_cast<const float4*>(ad + sd + g);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 a0 = pw[h], a1 = ps[h], a2 = pgw[h], a3 = pgs[h];
+                w[4 * h] = a0.x; w[4 * h + 1] = a0.y; w[4 * h + 2] = a0.z; w[4 * h + 3] = a0.w;
+                s[4 * h] = a1.x; s[4 * h + 1] = a1.y; s[4 * h + 2] = a1.z; s[4 * h + 3] = a1.w;
+                gw[4 * h] = a2.x; gw[4 * h + 1] = a2.y; gw[4 * h + 2] = a2.z; gw[4 * h + 3] = a2.w;
+                gs[4 * h] = a3.x; gs[4 * h + 1] = a3.y; gs[4 * h + 2] = a3.z; gs[4 * h + 3] = a3.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                p0 = fmaf(gw[e], w[e], p0);
+                p1 = fmaf(gw[e], s[e], p1);
+                p2 = fmaf(gs[e], s[e], p2);
+            }
+            const int h = c8 >> 3, cc8 = c8 & 7;
+            const uint32_t off = swz(i, cc8);
+            *reinterpret_cast<uint4*>(mtile(0, h) + off) = pack8(w);
+            *reinterpret_cast<uint4*>(mtile(1, h) + off) = pack8(s);
+            *reinterpret_cast<uint4*>(mtile(2, h) + off) = pack8(gw);
+            *reinterpret_cast<uint4*>(mtile(3, h) + off) = pack8(gs);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            p0 += __shfl_xor_sync(0xffffffffu, p0, off);
+            p1 += __shfl_xor_sync(0xffffffffu, p1, off);
+            p2 += __shfl_xor_sync(0xffffffffu, p2, off);
+        }
+        if (lane == 0) {
+            atomicAdd(&scal[0], p0);
+            atomicAdd(&scal[1], p1);
+            atomicAdd(&scal[2], p2);
+        }
+        // beta_t dZ[t][i], c_t dZ[t][i] (same swizzled places as the dZ tile)
+        for (int x = tid; x < 64 * 8; x += kThreads) {
+            const int t = x >> 3, c8 = x & 7;
+            const uint32_t off = swz(t, c8);
+            float v[8], vb[8], vc[8];
+            unpack8(*reinterpret_cast<const uint4*>(dztile(I) + off), v);
+            const float bt = beta[t], ct = cc[t];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                vb[e] = bt * v[e];
+                vc[e] = ct * v[e];
+            }
+            *reinterpret_cast<uint4*>(bz + off) = pack8(vb);
+            *reinterpret_cast<uint4*>(cz + off) = pack8(vc);
+        }
+    };
+
+    if (ok) convert_half(0);
+    if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+    if (ok && row >= 64) {
+        // -2 A~[t][s] = -2 C[t][s] (q_t . k_s) for s <= t, and Q K^T in bf16
+        tc_fence_after();
+        const int t = row - 64;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int s0 = 32 * chalf + 16 * q;
+            float r[16], x[16];
+            tmem_ld16(tl + kA1 + s0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int s = s0 + e;
+                x[e] = (s <= t && t < n) ? -2.f * Cm[t * kLdc + s] * r[e] : 0.f;
+                qkb[t * kC + s] = __float2bfloat16_rn(r[e]);
+            }
+            *reinterpret_cast<uint4*>(at + swz(t, s0 / 8)) = pack8(x);
+            *reinterpret_cast<uint4*>(at + swz(t, s0 / 8 + 1)) = pack8(x + 8);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    for (int I = 0; I < NH; ++I) {
+        if (I > 0 && ok) {
+            convert_half(I);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+        }
+        // [K; Q] {W, S, dWe, dSe}_I^T
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint32_t abase = smem_u32(ktile(kk >> 2)) + (kk & 3) * 32;
+                        const uint32_t bbase = smem_u32(mtile(m, kk >> 2)) + (kk & 3) * 32;
+                        mma_bf16(tmem + kA1 + 64 * m, sdesc(abase, 16, 1024, 2),
+                                 sdesc(bbase, 16, 1024, 2), idKK, kk > 0);
+                    }
+                }
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+        if (ok) {
+            tc_fence_after();
+            if (row < 64) {
+                // token s: E = K W^T - V, e_s . (dWe k_s), e_s . (dSe k_s), the scaled
+                // copies of E, and -2 (C[n-1][s] dWK + pm[s] dSK) into the De accumulator
+                const int s = row;
+                const float cn = n > 0 ? Cm[(n - 1) * kLdc + s] : 0.f, pms = pm[s];
+                float pw = 0.f, ps = 0.f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int i0 = 32 * chalf + 16 * q;
+                    float e[16], gw[16], gs[16], v[16];
+                    tmem_ld16(tl + kA1 + i0, e);
+                    tmem_ld16(tl + kA3 + i0, gw);
+                    tmem_ld16(tl + kA4 + i0, gs);
+                    unpack8(*reinterpret_cast<const uint4*>(vtile(I) + swz(s, i0 / 8)), v);
+                    unpack8(*reinterpret_cast<const uint4*>(vtile(I) + swz(s, i0 / 8 + 1)), v + 8);
+                    tmem_wait_ld();
+                    float x1[16], x2[16];
+                    uint32_t pre[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        e[k] = s < n ? e[k] - v[k] : 0.f;
+                        pw = fmaf(e[k], gw[k], pw);
+                        ps = fmaf(e[k], gs[k], ps);
+                        x1[k] = -2.f * cn * e[k];
+                        x2[k] = -2.f * pms * e[k];
+                        pre[k] = __float_as_uint(s < n ? -2.f * (cn * gw[k] + pms * gs[k]) : 0.f);
+                    }
+                    *reinterpret_cast<uint4*>(ei + swz(s, i0 / 8)) = pack8(e);
+                    *reinterpret_cast<uint4*>(ei + swz(s, i0 / 8 + 1)) = pack8(e + 8);
+                    *reinterpret_cast<uint4*>(ec + swz(s, i0 / 8)) = pack8(x1);
+                    *reinterpret_cast<uint4*>(ec + swz(s, i0 / 8 + 1)) = pack8(x1 + 8);
+                    *reinterpret_cast<uint4*>(ep + swz(s, i0 / 8)) = pack8(x2);
+                    *reinterpret_cast<uint4*>(ep + swz(s, i0 / 8 + 1)) = pack8(x2 + 8);
+                    const uint32_t lo[8] = {pre[0], pre[1], pre[2], pre[3], pre[4], pre[5], pre[6], pre[7]};
+                    const uint32_t hi[8] = {pre[8], pre[9], pre[10], pre[11], pre[12], pre[13], pre[14], pre[15]};
+                    tmem_st8(tl + kDeI + i0, lo);
+                    tmem_st8(tl + kDeI + i0 + 8, hi);
+                }
+                atomicAdd(&dclast[s], pw);
+                atomicAdd(&dpm[s], ps);
+                tmem_wait_st();
+            } else {
+                // token t: dz_t . (W q_t) and dz_t . (S q_t)
+                const int t = row - 64;
+                float pb = 0.f, pc = 0.f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int i0 = 32 * chalf + 16 * q;
+                    float qw[16], qs[16], z[16];
+                    tmem_ld16(tl + kA1 + i0, qw);
+                    tmem_ld16(tl + kA2 + i0, qs);
+                    unpack8(*reinterpret_cast<const uint4*>(dztile(I) + swz(t, i0 / 8)), z);
+                    unpack8(*reinterpret_cast<const uint4*>(dztile(I) + swz(t, i0 / 8 + 1)), z + 8);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        pb = fmaf(z[k], qw[k], pb);
+                        pc = fmaf(z[k], qs[k], pc);
+                    }
+                }
+                atomicAdd(&dbeta[t], pb);
+                atomicAdd(&dcc[t], pc);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // DE += [dZ_I; .] E_I^T;  De_I += (-2 A~^T) dZ_I
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t zb = smem_u32(dztile(I)), eb = smem_u32(ei), ab = smem_u32(at);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kDE, sdesc(zb + kk * 32, 16, 1024, 2), sdesc(eb + kk * 32, 16, 1024, 2),
+                             idKK, (I > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kDeI, sdesc(ab + kk * 2048, kTile, 1024, 2),
+                             sdesc(zb + kk * 2048, kTile, 1024, 2), idMM, 1u);
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+        if (ok && row < 64) {
+            // De of the half: dv = -De, and its bf16 tile [s][i]
+            tc_fence_after();
+            const int s = row;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int i0 = 32 * chalf + 16 * q;
+                float r[16], nv[16];
+                tmem_ld16(tl + kDeI + i0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k) nv[k] = -r[k];
+                *reinterpret_cast<uint4*>(dei + swz(s, i0 / 8)) = pack8(r);
+                *reinterpret_cast<uint4*>(dei + swz(s, i0 / 8 + 1)) = pack8(r + 8);
+                if (s < n) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv_) +
+                                                          (tok0 + s) * D + 64 * I + i0);
+                    dst[0] = pack8(nv);
+                    dst[1] = pack8(nv + 8);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // dQ^T += W_I^T (beta dZ_I)^T + S_I^T (c dZ_I)^T;
+        // dK^T += W_I^T De_I^T + dWe_I^T (-2 Cn E_I)^T + dSe_I^T (-2 pm E_I)^T
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t mw = smem_u32(mtile(0, 0)), ms = smem_u32(mtile(1, 0));
+                const uint32_t mgw = smem_u32(mtile(2, 0)), mgs = smem_u32(mtile(3, 0));
+                const uint32_t bzb = smem_u32(bz), czb = smem_u32(cz), deb = smem_u32(dei);
+                const uint32_t ecb = smem_u32(ec), epb = smem_u32(ep);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16(tmem + kDQ, sdesc(mw + kk * 2048, kTile, 1024, 2),
+                             sdesc(bzb + kk * 32, 16, 1024, 2), idMK, (I > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16(tmem + kDQ, sdesc(ms + kk * 2048, kTile, 1024, 2),
+                             sdesc(czb + kk * 32, 16, 1024, 2), idMK, 1u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16(tmem + kDK, sdesc(mw + kk * 2048, kTile, 1024, 2),
+                             sdesc(deb + kk * 32, 16, 1024, 2), idMK, (I > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16(tmem + kDK, sdesc(mgw + kk * 2048, kTile, 1024, 2),
+                             sdesc(ecb + kk * 32, 16, 1024, 2), idMK, 1u);
+                    mma_bf16(tmem + kDK, sdesc(mgs + kk * 2048, kTile, 1024, 2),
+                             sdesc(epb + kk * 32, 16, 1024, 2), idMK, 1u);
+                }
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        // the next half overwrites the matrices and operand tiles
+        if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+    }
+
+    // DE complete: dC = -2 (Q K^T) o DE (+ the end-state term on the last row)
+    // and -2 G = -2 C o DE, for s <= t < n
+    float* dC = reinterpret_cast<float*>(sm + L.mat);    // [t][kLdc], the matrices are done
+    if (ok && row < 64) {
+        tc_fence_after();
+        const int t = row;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int s0 = 32 * chalf + 16 * q;
+            float r[16], x[16];
+            tmem_ld16(tl + kDE + s0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int s = s0 + e;
+                const bool in = s <= t && t < n;
+                const float de = in ? r[e] : 0.f;
+                x[e] = -2.f * Cm[t * kLdc + s] * de;
+                dC[t * kLdc + s] = -2.f * __bfloat162float(qkb[t * kC + s]) * de -
+                                   (t == n - 1 && s < n ? 2.f * dclast[s] : 0.f);
+            }
+            *reinterpret_cast<uint4*>(gg + swz(t, s0 / 8)) = pack8(x);
+            *reinterpret_cast<uint4*>(gg + swz(t, s0 / 8 + 1)) = pack8(x + 8);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // dQ^T += K^T (-2 G)^T;  dK^T += Q^T (-2 G)
+    if (warp == 0 && ok) {
+        tc_fence_after();
+        if (elect_one()) {
+            const uint32_t kb = smem_u32(ktile(0)), qb = smem_u32(qtile(0)), gb = smem_u32(gg);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16(tmem + kDQ, sdesc(kb + kk * 2048, 2 * kTile, 1024, 2),
+                         sdesc(gb + kk * 32, 16, 1024, 2), idMK, 1u);
+                mma_bf16(tmem + kDK, sdesc(qb + kk * 2048, 2 * kTile, 1024, 2),
+                         sdesc(gb + kk * 2048, kTile, 1024, 2), idMM, 1u);
+            }
+            mma_commit(&Y->mma);
+        }
+        __syncwarp();
+    }
+    if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+    // dQ^T, dK^T (lanes j): transposed through shared memory into dq, dk rows
+    __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(sm + L.mat + kC * kLdc * 4);
+    __nv_bfloat16* stk = stq + kC * D;
+    if (ok && row < D) {
+        tc_fence_after();
+        const int j = row;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int t0 = 32 * chalf + 16 * q;
+            float rq[16], rk[16];
+            tmem_ld16(tl + kDQ + t0, rq);
+            tmem_ld16(tl + kDK + t0, rk);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                stq[(t0 + e) * D + j] = __float2bfloat16_rn(rq[e]);
+                stk[(t0 + e) * D + j] = __float2bfloat16_rn(rk[e]);
+            }
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        constexpr int kRowV = D / 8;                      // 16-byte pieces per row
+        for (int x = tid; x < n * kRowV; x += kThreads) {
+            const int t = x / kRowV, p = x % kRowV;
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + (tok0 + t) * D)[p] =
+                reinterpret_cast<const uint4*>(stq + t * D)[p];
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk_) + (tok0 + t) * D)[p] =
+                reinterpret_cast<const uint4*>(stk + t * D)[p];
+        }
+    }
+    __syncthreads();
+
+    // gate gradients: C[t][s] = theta_s w(s,t), pm[s] = theta_s m(s,n-1) with
+    // m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t)
+    // (w(s,s) = m(s,s) = 1), as in the CUDA-core local pass
+    float* Wm = dC + kC * kLdc;                      // after dC (the staging is consumed)
+    float* Mm = Wm + kC * kLdc;
+    float* Kc = Mm + kC * kLdc;
+    float* Ec = Kc + kC * kLdc;
+    if (ok) {
+        for (int s = tid; s < kC; s += kThreads)
+            for (int t = 0; t < kC; ++t) Kc[t * kLdc + s] = Ec[t * kLdc + s] = 0.f;
+        for (int s = tid; s < n; s += kThreads) {
+            float m = 1.f, w = 1.f;
+            Wm[s * kLdc + s] = 1.f;
+            Mm[s * kLdc + s] = 1.f;
+            for (int t = s + 1; t < n; ++t) {
+                m = et[t] * m;
+                w = (1.f - al[t]) * w + m;
+                Wm[t * kLdc + s] = w;
+                Mm[t * kLdc + s] = m;
+            }
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        for (int s = tid; s < n; s += kThreads) {
+            const float ths = th[s];
+            float g = -2.f * dpm[s] * Mm[(n - 1) * kLdc + s];
+            for (int t = s; t < n; ++t) g += dC[t * kLdc + s] * Wm[t * kLdc + s];
+            dth[s] = g;
+            float dw = ths * dC[(n - 1) * kLdc + s];
+            float dm = ths * (-2.f * dpm[s]);
+            for (int t = n - 1; t > s; --t) {
+                Kc[t * kLdc + s] = dw * Wm[(t - 1) * kLdc + s];
+                dm += dw;
+                Ec[t * kLdc + s] = dm * Mm[(t - 1) * kLdc + s];
+                dm = et[t] * dm;
+                dw = (1.f - al[t]) * dw + ths * dC[(t - 1) * kLdc + s];
+            }
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        for (int t = tid; t < n; t += kThreads) {
+            float gk = 0.f, ge = 0.f;
+            for (int s = 0; s < t; ++s) {
+                gk += Kc[t * kLdc + s];
+                ge += Ec[t * kLdc + s];
+            }
+            dkeep[t] += gk;
+            deta[t] += ge;
+        }
+    }
+    __syncthreads();
+    if (ok && tid == 0) {
+        float rb = 0.f, rc = 0.f, rp = 0.f;
+        for (int t = n - 1; t >= 0; --t) {
+            const bool last = t == n - 1;
+            const float db = dbeta[t] + rb + (last ? scal[0] : 0.f);
+            const float dcv = dcc[t] + rc + (last ? scal[1] : 0.f);
+            const float dp = rp + dcv + (last ? scal[2] : 0.f);
+            const float keep = 1.f - al[t];
+            const float cprev = t > 0 ? cc[t - 1] : 0.f;
+            const float bprev = t > 0 ? beta[t - 1] : 1.f;
+            const float pprev = t > 0 ? P[t - 1] : 1.f;
+            dkeep[t] += dcv * cprev + db * bprev;
+            deta[t] += dp * pprev;
+            rc = keep * dcv;
+            rb = keep * db;
+            rp = et[t] * dp;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        for (int t = tid; t < n; t += kThreads) {
+            a.dtheta[tok0 + t] = dth[t];
+            if (a.deta) a.deta[tok0 + t] = deta[t];
+            if (a.dalpha) a.dalpha[tok0 + t] = -dkeep[t];
+        }
+    }
+    if (tid == 0 && !ok) {
+        // copies in flight before the kernel's shared memory goes
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&Y->full, 0) && clock64() - t0 < Y->limit) {
+        }
+    }
+    if (warp == 0) {
+        // every MMA (also after an abort) completes before TMEM is released
+        if (elect_one()) mma_commit(&Y->mma);
+        __syncwarp();
+        const long long t0 = clock64();
+        if (lane == 0)
+            while (!mbar_try_wait(&Y->mma, mma_phase & 1) && clock64() - t0 < Y->limit) {
+            }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool bwd_local_tc_supported(const BwdArgs& a) {
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kC && a.T >= 1;
+}
+
+cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
+                                cudaStream_t s) {
+    const int D = a.dk, BH = a.B * a.H;
+    const int nch = (a.T + kC - 1) / kC;
+    CUtensorMap qm, km, zm, vm;
+    if (!make_token_tile_map(&qm, a.q, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&km, a.k, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&zm, a.dz, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&vm, a.v, BH, a.T, D, 64, true))
+        return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)(BH * nch));
+    if (D == 128) {
+        const size_t smem = make_layout(128).total + 1024;
+        cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bwd_local_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, a, ckpt, adj, nch);
+    } else {
+        const size_t smem = make_layout(64).total + 1024;
+        cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bwd_local_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, a, ckpt, adj, nch);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ttm
