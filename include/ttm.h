@@ -91,7 +91,9 @@ typedef enum {
     TTM_KID_LINEAR_SEQ = 5,    /* tcgen05 + TMA scan, one CTA per sequence, d = 64,
                                   gradient points every 16 or 32 tokens */
     TTM_KID_DGD_STEP = 6,      /* fp32 CUDA-core token loop, DGD memory */
-    TTM_KID_DGD_TC = 7         /* tcgen05 + TMA chunk form, DGD memory (pre-pass + scan) */
+    TTM_KID_DGD_TC = 7,        /* tcgen05 + TMA chunk form, DGD memory (pre-pass + scan) */
+    TTM_KID_BWD_SIMT = 8,      /* gradient: every pass on the fp32 CUDA cores */
+    TTM_KID_BWD_TC = 9         /* gradient: the local pass on tcgen05 (records and chain fp32) */
 } ttm_kernel_id;
 
 /*

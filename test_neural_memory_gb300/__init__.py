@@ -22,7 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(5)
 F32, BF16 = 0, 1
 POLICY = {"auto": 0, "simt": 1, "tc": 2}
 KERNEL_NAMES = {0: "none", 1: "linear_simt", 2: "mlp_simt", 3: "linear_tc", 4: "mlp_tc",
-                5: "linear_seq", 6: "dgd_step", 7: "dgd_tc"}
+                5: "linear_seq", 6: "dgd_step", 7: "dgd_tc", 8: "bwd_simt", 9: "bwd_tc"}
 
 _lib = None
 

@@ -466,6 +466,7 @@ int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     const cudaError_t e = ttm::linear_bwd_launch(a, s, &launches);
     if (e != cudaSuccess) return TTM_ERR_CUDA;
     __atomic_add_fetch(&g_launches, (unsigned long long)launches, __ATOMIC_RELAXED);
+    t_last_kernel = a.local_tc ? TTM_KID_BWD_TC : TTM_KID_BWD_SIMT;
     return TTM_OK;
 }
 

@@ -157,3 +157,41 @@ def test_bf16_d128_both_checkpoint_scans(policy):
         g, r, names = run_bwd("titans", "bf16", B=1, Hh=2, T=200, d=128, chunk=64, seed=10,
                               S0=True)
     check(g, r, names, H.TOL["bf16"])
+
+
+# ------------------------------------------------------- tensor-core local pass
+# bf16, d_k = d_v in {64, 128}, chunk 64: under the automatic policy the local
+# pass (dq, dk, dv and the gate gradients) runs on the tensor cores.
+
+@pytest.mark.parametrize("kind,d,T,seed", [("titans", 64, 130, 20), ("titans", 128, 64, 21),
+                                            ("linear", 128, 200, 22), ("titans", 128, 1, 23)])
+def test_tensor_core_local_pass(kind, d, T, seed):
+    import test_neural_memory_gb300 as ttm
+    with ttm.kernel_policy("auto"):
+        g, r, names = run_bwd(kind, "bf16", B=2, Hh=2, T=T, d=d, chunk=64, seed=seed,
+                              S0=(kind == "titans"))
+        assert ttm.last_kernel() == "bwd_tc"
+    check(g, r, names, H.TOL["bf16"])
+
+
+def test_tensor_core_local_pass_shared_memory_and_no_final_adjoint():
+    import test_neural_memory_gb300 as ttm
+    with ttm.kernel_policy("auto"):
+        g, r, names = run_bwd("titans", "bf16", B=3, Hh=2, T=150, d=128, chunk=64, seed=24,
+                              shared=True, adj_final=False)
+        assert ttm.last_kernel() == "bwd_tc"
+    check(g, r, names, H.TOL["bf16"])
+
+
+def test_tensor_core_and_cuda_core_local_passes_agree():
+    import test_neural_memory_gb300 as ttm
+    out = {}
+    for policy, kern in (("auto", "bwd_tc"), ("simt", "bwd_simt")):
+        with ttm.kernel_policy(policy):
+            g, r, names = run_bwd("titans", "bf16", B=1, Hh=4, T=640, d=128, chunk=64, seed=25)
+            assert ttm.last_kernel() == kern
+        out[policy] = g
+    for n in names:
+        if out["auto"][n] is None:
+            continue
+        assert H.max_rel(H.f64(out["auto"][n]), H.f64(out["simt"][n])) < H.TOL["bf16"], n
