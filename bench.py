@@ -397,8 +397,8 @@ def run_bwd(args, rank, world, dev):
                "steps": args.e2e_steps, "ms_per_step": ems}
 
     alg = bwd_algorithmic(w)
-    kern = ttm.last_kernel()           # bwd_tc: the local pass on tcgen05; bwd_simt: all fp32
-    label = ("linear_bwd (records, chain: fp32; local pass: tcgen05)" if kern == "bwd_tc"
+    kern = ttm.last_kernel()  # bwd_tc: chain and local passes on tcgen05; bwd_simt: all fp32
+    label = ("linear_bwd (records: fp32; chain, local pass: tcgen05)" if kern == "bwd_tc"
              else "linear_bwd (all passes fp32)")
     line = {
         "metric": "gradient tokens/s (ttm_titans_bwd: dq, dk, dv, gates, W0) on 1 GB300",
@@ -411,7 +411,7 @@ def run_bwd(args, rank, world, dev):
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (no flush needed)", "kernel": kern,
                    "workspace_bytes": int(ws_bytes)},
-        "roofline": dict(roof(alg["flops"], alg["bytes"], ms / 1e3, True),
+        "roofline": dict(roof(alg["flops"], alg["bytes"], ms / 1e3, kern == "bwd_simt"),
                          kernel=label, traffic=None),
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }

@@ -186,6 +186,10 @@ cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
 // {64, 128}, chunk 64; reads the chunk-start checkpoints and chunk-end adjoints
 // (fp32, [seq][chunk][W | S][dv][dk]) that the other passes leave in the workspace.
 bool bwd_local_tc_supported(const BwdArgs& a);
+// Its chain pass on the tensor cores (same shapes): the adjoint at every chunk
+// end from the records pass's records; offsets in floats into the workspace.
+cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, size_t off_rec,
+                                size_t off_part, cudaStream_t s);
 cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
                                 cudaStream_t s);
 

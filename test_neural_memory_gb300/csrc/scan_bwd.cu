@@ -1,4 +1,4 @@
-// Gradient of the chunked linear / Titans memory scan (fp32 CUDA-core kernels).
+// Gradient of the chunked linear / Titans memory scan.
 //
 // The outer loss trains the projections, the rates and W0 through the inner
 // updates, so the gradient follows the chain of state transitions backward
@@ -36,6 +36,9 @@
 //            q, k and dz; rows are independent, as in the forward;
 //   local    one CTA per (sequence, chunk), all chunks at once: dq, dk, dv and
 //            the gate gradients from the chunk's start state and end adjoint.
+// The records pass and the fp32 CUDA-core chain and local passes below serve
+// every shape; for bf16 inputs with d_k = d_v in {64, 128} and chunks of 64 the
+// chain and local passes run on the tensor cores instead (scan_bwd_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -949,11 +952,13 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
         return e;
     bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
-    bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT2, sm2, s>>>(a, L, ws);
     if (a.local_tc) {
+        // chain and local passes on the tensor cores
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = bwd_chain_tc_launch(a, ws, L.adj, L.rec, L.part, s)) != cudaSuccess) return e;
         if ((e = bwd_local_tc_launch(a, ws + L.ckpt, ws + L.adj, s)) != cudaSuccess) return e;
     } else {
+        bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT2, sm2, s>>>(a, L, ws);
         bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT3, sm3, s>>>(a, L, ws);
     }
     *launches += 3;

@@ -1,5 +1,5 @@
-// Tensor-core (tcgen05 + TMA) local pass of the scan's gradient (bf16 inputs,
-// d_k = d_v in {64, 128}, chunks of 64 tokens).
+// Tensor-core (tcgen05 + TMA) chain and local passes of the scan's gradient
+// (bf16 inputs, d_k = d_v in {64, 128}, chunks of 64 tokens).
 //
 // The local pass gives, for one chunk of n tokens with the chunk-start state
 // (W, S) and the adjoint of the chunk-end state (dWe, dSe), the gradients of
@@ -129,6 +129,23 @@ __device__ __noinline__ bool wait_bar(Sync* Y, uint64_t* bar, uint32_t parity, i
     while (!mbar_try_wait_sleep(bar, parity, 20000)) {
         if (*(volatile int*)&Y->abort || clock64() - t0 > Y->limit) {
             *(volatile int*)&Y->abort = 1;
+            atomicExch(status, TTM_ERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// The same bounded wait on an abort flag and a limit of any owner.
+__device__ __noinline__ bool wait_flag(int* abort, long long limit, uint64_t* bar, uint32_t parity,
+                                       int* status) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const long long t0 = clock64();
+    bool ok = true;
+    while (!mbar_try_wait_sleep(bar, parity, 20000)) {
+        if (*(volatile int*)abort || clock64() - t0 > limit) {
+            *(volatile int*)abort = 1;
             atomicExch(status, TTM_ERR_TIMEOUT);
             ok = false;
             break;
@@ -686,10 +703,346 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ chain
+//
+// The adjoint of the state at every chunk end, chunks in reverse, for a slice
+// of 16 rows i of (dW, dS) (rows evolve independently).  Per chunk, with the
+// chunk's record (A, beta, c, C[n-1][.], pm, P_n):
+//   dWK = K dW^T, dSK = K dS^T                       [K; .] [dW; dS]^T  (MMA)
+//   de  = (-2 A^T) dZ - 2 (C_n o dWK + pm o dSK)      (-2A)^T dZ          (MMA)
+//   dW <- beta_n dW + (Q^T (beta o dZ) + K^T de)^T,    (Q^T, K^T MN-major; MMA)
+//   dS <- c_n dW + P_n dS + (Q^T (c o dZ))^T
+// with thread j holding column j of the slice's 16 rows of dW and dS in fp32
+// registers and writing their bf16 copy for the next chunk's first product.
+// The next chunk's tiles and record load into the second of two stages while a
+// chunk computes.
+
+constexpr uint32_t kRecF = (kC * kC + 4 * kC + 1 + 3) / 4 * 4;   // floats per record
+constexpr uint32_t kRecSlot = ((kRecF * 4) + 63) / 64 * 64;
+constexpr int kSl = 16;                                          // rows of the slice
+
+struct ChainLayout {
+    uint32_t kq, rec, dzs, at, dzt, bzt, czt, det, ws, total;
+};
+
+__host__ __device__ constexpr ChainLayout chain_layout(int D) {
+    ChainLayout L{};
+    uint32_t o = 0;
+    const uint32_t NH = D / 64;
+    L.kq = o;  o += 2 * NH * 2 * kTile;     // two stages of [K_h][Q_h]
+    L.rec = o; o += 2 * kRecSlot;           // two stages of the record
+    L.dzs = o; o += 2 * kC * kSl * 2;       // two stages of the dZ slice (64 x 16 bf16)
+    o = (o + 1023) / 1024 * 1024;
+    L.at = o;  o += kTile;                  // -2 A [t][s]
+    L.dzt = o; o += kTile;                  // dZ slice [t][i] (16 of 64 columns)
+    L.bzt = o; o += kTile;                  // beta_t dZ
+    L.czt = o; o += kTile;                  // c_t dZ
+    L.det = o; o += kTile;                  // de [s][i]
+    L.ws = o;  o += (uint32_t)D * 128;      // [dW; dS]^T bf16 [j][i'] (32 of 64 columns)
+    L.total = o + 64;                       // barriers
+    return L;
+}
+
+struct ChainSync {
+    uint64_t full[2], mma;
+    long long limit;
+    int abort;
+    uint32_t tmem;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap zmap, const BwdArgs a, float* ws,
+                    size_t off_adj, size_t off_rec, size_t off_part, int nch) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    constexpr ChainLayout L = chain_layout(D);
+    constexpr int NH = D / 64, KS = D / 16;
+    ChainSync* Y = reinterpret_cast<ChainSync*>(sm + L.total - 64);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nsl = D / kSl;
+    const int seq = blockIdx.x / nsl, r0 = (blockIdx.x % nsl) * kSl;
+    const int T = a.T;
+    const size_t sd = (size_t)D * D;
+    int* status = a.status;
+
+    auto kt = [&](int b, int h) { return sm + L.kq + (b * NH + h) * 2 * kTile; };
+    auto qt = [&](int b, int h) { return kt(b, h) + kTile; };
+    auto recb = [&](int b) { return reinterpret_cast<float*>(sm + L.rec + b * kRecSlot); };
+    auto dzs = [&](int b) { return sm + L.dzs + b * kC * kSl * 2; };
+    uint8_t* at = sm + L.at;
+    uint8_t* dzt = sm + L.dzt;
+    uint8_t* bzt = sm + L.bzt;
+    uint8_t* czt = sm + L.czt;
+    uint8_t* det = sm + L.det;
+    uint8_t* wsm = sm + L.ws;
+
+    if (tid == 0) {
+        mbar_init(&Y->full[0], 1);
+        mbar_init(&Y->full[1], 1);
+        mbar_init(&Y->mma, 1);
+        Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
+        Y->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&Y->tmem, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = Y->tmem;
+    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);
+    constexpr uint32_t kAc1 = 0, kAc2 = 32, kAc3 = 64;
+
+    auto issue_loads = [&](int c, int b) {
+        mbar_expect_tx(&Y->full[b], 2 * NH * kTile + kC * kSl * 2 + kRecF * 4);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            tma_load_3d(kt(b, h), &kmap, &Y->full[b], 64 * h, c * kC, seq);
+            tma_load_3d(qt(b, h), &qmap, &Y->full[b], 64 * h, c * kC, seq);
+        }
+        tma_load_3d(dzs(b), &zmap, &Y->full[b], r0, c * kC, seq);
+        bulk_load(recb(b), ws + off_rec + ((size_t)seq * nch + c) * kRecF, kRecF * 4, &Y->full[b]);
+    };
+    if (tid == 0 && nch > 0) issue_loads(nch - 1, 0);
+
+    // the slice's adjoint rows, column j per thread (the final state's adjoint)
+    const int j = tid;
+    const bool own = j < D;
+    float dw[kSl], dsv[kSl];
+#pragma unroll
+    for (int i = 0; i < kSl; ++i) {
+        const size_t g = (size_t)seq * sd + (size_t)(r0 + i) * D + j;
+        dw[i] = (own && a.dW) ? a.dW[g] : 0.f;
+        dsv[i] = (own && a.dS) ? a.dS[g] : 0.f;
+    }
+    auto write_ws = [&]() {
+        if (!own) return;
+        *reinterpret_cast<uint4*>(wsm + swz(j, 0)) = pack8(dw);
+        *reinterpret_cast<uint4*>(wsm + swz(j, 1)) = pack8(dw + 8);
+        *reinterpret_cast<uint4*>(wsm + swz(j, 2)) = pack8(dsv);
+        *reinterpret_cast<uint4*>(wsm + swz(j, 3)) = pack8(dsv + 8);
+    };
+    write_ws();
+
+    constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // [K; Q] [dW; dS]^T
+    constexpr uint32_t id16 = idesc_bf16_f32(128, 16, 1, 1);  // MN-major A and B, N = 16
+    uint32_t mma_phase = 0;
+    bool ok = true;
+    for (int k = 0; k < nch; ++k) {
+        const int c = nch - 1 - k, b = k & 1;
+        const int n = min(kC, T - c * kC);
+        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[b], (k >> 1) & 1, status);
+        // the next chunk's inputs into the other stage (its last use is complete)
+        if (tid == 0 && ok && c > 0) issue_loads(c - 1, b ^ 1);
+        const float* rv = recb(b);
+        const float* Arec = rv;                      // A[t][s], row stride 64
+        const float* vbeta = rv + kC * kC;
+        const float* vc = vbeta + kC;
+        const float* vclast = vc + kC;
+        const float* vpm = vclast + kC;
+        const float Pn = vpm[kC];
+        // this chunk's end adjoint, for the local pass
+        if (own && ok) {
+            float* adj = ws + off_adj + ((size_t)seq * nch + c) * 2 * sd;
+#pragma unroll
+            for (int i = 0; i < kSl; ++i) {
+                adj[(size_t)(r0 + i) * D + j] = dw[i];
+                adj[sd + (size_t)(r0 + i) * D + j] = dsv[i];
+            }
+        }
+        if (ok) {
+            // -2 A [t][s], and the dZ slice, beta dZ, c dZ as 16-column tiles [t][i]
+            for (int x = tid; x < kC * 8; x += kThreads) {
+                const int t = x >> 3, c8 = x & 7;
+                const float4* src = reinterpret_cast<const float4*>(Arec + t * kC + 8 * c8);
+                const float4 u0 = src[0], u1 = src[1];
+                const float v[8] = {-2.f * u0.x, -2.f * u0.y, -2.f * u0.z, -2.f * u0.w,
+                                    -2.f * u1.x, -2.f * u1.y, -2.f * u1.z, -2.f * u1.w};
+                *reinterpret_cast<uint4*>(at + swz(t, c8)) = pack8(v);
+            }
+            for (int x = tid; x < kC * 2; x += kThreads) {
+                const int t = x >> 1, c8 = x & 1;
+                float z[8], zb[8], zc[8];
+                unpack8(*reinterpret_cast<const uint4*>(dzs(b) + t * kSl * 2 + 16 * c8), z);
+                const float bt = t < n ? vbeta[t] : 0.f, ct = t < n ? vc[t] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    zb[e] = bt * z[e];
+                    zc[e] = ct * z[e];
+                }
+                *reinterpret_cast<uint4*>(dzt + swz(t, c8)) = pack8(z);
+                *reinterpret_cast<uint4*>(bzt + swz(t, c8)) = pack8(zb);
+                *reinterpret_cast<uint4*>(czt + swz(t, c8)) = pack8(zc);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK) and (-2 A)^T dZ (lanes 0-63)
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t wsa = smem_u32(wsm);
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint32_t abase = smem_u32(kt(b, kk >> 2)) + (kk & 3) * 32;
+                    mma_bf16(tmem + kAc1, sdesc(abase, 16, 1024, 2), sdesc(wsa + kk * 2048, 8192, 1024, 2),
+                             id1, kk > 0);
+                }
+                const uint32_t aa = smem_u32(at), za = smem_u32(dzt);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kAc2, sdesc(aa + kk * 2048, kTile, 1024, 2),
+                             sdesc(za + kk * 2048, kTile, 1024, 2), id16, kk > 0);
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma, mma_phase++ & 1, status);
+        if (ok && warp < 2) {
+            // de[s][i] = (-2 A^T dZ)[s][i] - 2 (C_n[s] dWK + pm[s] dSK), s < n
+            tc_fence_after();
+            const int sidx = warp * 32 + lane;
+            float gw[16], gs[16], ad[16], de[16];
+            tmem_ld16(tl + kAc1, gw);
+            tmem_ld16(tl + kAc1 + 16, gs);
+            tmem_ld16(tl + kAc2, ad);
+            tmem_wait_ld();
+            const float cl = vclast[sidx], pmv = vpm[sidx];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                de[e] = sidx < n ? ad[e] - 2.f * (cl * gw[e] + pmv * gs[e]) : 0.f;
+            *reinterpret_cast<uint4*>(det + swz(sidx, 0)) = pack8(de);
+            *reinterpret_cast<uint4*>(det + swz(sidx, 1)) = pack8(de + 8);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // (Q^T (beta dZ) + K^T de) and Q^T (c dZ), rows = key index j
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t qa = smem_u32(qt(b, 0)), ka = smem_u32(kt(b, 0));
+                const uint32_t bzb = smem_u32(bzt), czb = smem_u32(czt), deb = smem_u32(det);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kAc3, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
+                             sdesc(bzb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kAc3, sdesc(ka + kk * 2048, 2 * kTile, 1024, 2),
+                             sdesc(deb + kk * 2048, kTile, 1024, 2), id16, 1u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + kAc3 + 16, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
+                             sdesc(czb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma, mma_phase++ & 1, status);
+        if (ok && warp < 4) {
+            // dW <- beta_n dW + .,  dS <- c_n dW + P_n dS + .  (column j)
+            tc_fence_after();
+            float uw[16], us[16];
+            tmem_ld16(tl + kAc3, uw);
+            tmem_ld16(tl + kAc3 + 16, us);
+            tmem_wait_ld();
+            const float bn = vbeta[n - 1], cn = vc[n - 1];
+            if (own) {
+#pragma unroll
+                for (int i = 0; i < kSl; ++i) {
+                    const float w = dw[i];
+                    dw[i] = fmaf(bn, w, uw[i]);
+                    dsv[i] = fmaf(cn, w, fmaf(Pn, dsv[i], us[i]));
+                }
+            }
+            write_ws();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+    }
+    // adjoint of the initial state: per sequence, or a per-sequence partial that
+    // a reduction sums over the batch when W0 / S0 are shared
+    if (own && ok) {
+        float* oW;
+        float* oS;
+        size_t base;
+        if (a.shared) {
+            oW = ws + off_part;
+            oS = oW + sd;
+            base = (size_t)seq * 2 * sd;
+        } else {
+            oW = a.dW0;
+            oS = a.dS0;
+            base = (size_t)seq * sd;
+        }
+#pragma unroll
+        for (int i = 0; i < kSl; ++i) {
+            const size_t g = base + (size_t)(r0 + i) * D + j;
+            oW[g] = dw[i];
+            if (oS) oS[g] = dsv[i];
+        }
+    }
+    if (tid == 0 && !ok) {
+        // copies in flight before the kernel's shared memory goes
+        for (int bb = 0; bb < 2; ++bb) {
+            const long long t0 = clock64();
+            while (clock64() - t0 < Y->limit && !mbar_try_wait(&Y->full[bb], 0) &&
+                   !mbar_try_wait(&Y->full[bb], 1)) {
+            }
+        }
+    }
+    if (warp == 0) {
+        if (elect_one()) mma_commit(&Y->mma);
+        __syncwarp();
+        const long long t0 = clock64();
+        if (lane == 0)
+            while (!mbar_try_wait(&Y->mma, mma_phase & 1) && clock64() - t0 < Y->limit) {
+            }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
 }  // namespace
 
 bool bwd_local_tc_supported(const BwdArgs& a) {
     return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kC && a.T >= 1;
+}
+
+cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, size_t off_rec,
+                                size_t off_part, cudaStream_t s) {
+    const int D = a.dk, BH = a.B * a.H;
+    const int nch = (a.T + kC - 1) / kC;
+    CUtensorMap qm, km, zm;
+    if (!make_token_tile_map(&qm, a.q, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&km, a.k, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&zm, a.dz, BH, a.T, D, kSl, false))
+        return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)(BH * (D / kSl)));
+    if (D == 128) {
+        const size_t smem = chain_layout(128).total + 1024;
+        cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bwd_chain_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj, off_rec,
+                                                              off_part, nch);
+    } else {
+        const size_t smem = chain_layout(64).total + 1024;
+        cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bwd_chain_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj, off_rec,
+                                                             off_part, nch);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,

@@ -159,9 +159,10 @@ def test_bf16_d128_both_checkpoint_scans(policy):
     check(g, r, names, H.TOL["bf16"])
 
 
-# ------------------------------------------------------- tensor-core local pass
-# bf16, d_k = d_v in {64, 128}, chunk 64: under the automatic policy the local
-# pass (dq, dk, dv and the gate gradients) runs on the tensor cores.
+# ------------------------------------------ tensor-core chain and local passes
+# bf16, d_k = d_v in {64, 128}, chunk 64: under the automatic policy the chain
+# (the state adjoint at every chunk end) and the local pass (dq, dk, dv and the
+# gate gradients) run on the tensor cores.
 
 @pytest.mark.parametrize("kind,d,T,seed", [("titans", 64, 130, 20), ("titans", 128, 64, 21),
                                             ("linear", 128, 200, 22), ("titans", 128, 1, 23)])
@@ -170,6 +171,18 @@ def test_tensor_core_local_pass(kind, d, T, seed):
     with ttm.kernel_policy("auto"):
         g, r, names = run_bwd(kind, "bf16", B=2, Hh=2, T=T, d=d, chunk=64, seed=seed,
                               S0=(kind == "titans"))
+        assert ttm.last_kernel() == "bwd_tc"
+    check(g, r, names, H.TOL["bf16"])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_core_chain_many_chunks(d):
+    # thirteen chunks, the last one ragged: the chain's two-stage input ring
+    # wraps its phases several times and carries the adjoint through all of them
+    import test_neural_memory_gb300 as ttm
+    with ttm.kernel_policy("auto"):
+        g, r, names = run_bwd("titans", "bf16", B=1, Hh=2, T=12 * 64 + 5, d=d, chunk=64,
+                              seed=26 + d, S0=True)
         assert ttm.last_kernel() == "bwd_tc"
     check(g, r, names, H.TOL["bf16"])
 
@@ -183,7 +196,7 @@ def test_tensor_core_local_pass_shared_memory_and_no_final_adjoint():
     check(g, r, names, H.TOL["bf16"])
 
 
-def test_tensor_core_and_cuda_core_local_passes_agree():
+def test_tensor_core_and_cuda_core_gradients_agree():
     import test_neural_memory_gb300 as ttm
     out = {}
     for policy, kern in (("auto", "bwd_tc"), ("simt", "bwd_simt")):
