@@ -398,8 +398,8 @@ def run_bwd(args, rank, world, dev):
 
     alg = bwd_algorithmic(w)
     kern = ttm.last_kernel()  # bwd_tc: chain and local passes on tcgen05; bwd_simt: all fp32
-    label = ("linear_bwd (records: fp32; chain, local pass: tcgen05)" if kern == "bwd_tc"
-             else "linear_bwd (all passes fp32)")
+    label = ("linear_bwd (chain, local pass: tcgen05; scores from the forward scan)"
+             if kern == "bwd_tc" else "linear_bwd (all passes fp32)")
     line = {
         "metric": "gradient tokens/s (ttm_titans_bwd: dq, dk, dv, gates, W0) on 1 GB300",
         "value": w.tokens * world / (ms / 1e3), "unit": UNIT, "n_gpus": world,

@@ -25,6 +25,11 @@ struct LinearArgs {
     // ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be NULL.  The
     // gradient passes read these checkpoints.
     float* ckpt;
+    // Tensor-core scan with ckpt only (may be NULL): the masked score tile
+    // A~[t][s] = C[t][s] (q_t . k_s) (zero for s > t and outside the chunk) of
+    // every chunk in bf16, score_tiles[seq][chunk] = 64 rows t of 128 bytes,
+    // the 16-byte group g of row t stored at position g ^ (t % 8).
+    void* score_tiles;
     // Chunk-shared gates: theta / eta / alpha hold one value per (sequence,
     // chunk), [B][H][ceil(T / chunk)], instead of one per token.
     int gates_per_chunk;
@@ -37,6 +42,17 @@ struct LinearArgs {
     // runs out: the kernel then reports TTM_ERR_TIMEOUT and unwinds.
     int debug_stall;
 };
+
+// Per-chunk coefficient record that the tensor-core scan's pre-pass writes
+// into its workspace (record seq * nchunks + chunk, kCoefRecBytes each): the
+// table C[t][s] (64 x 64 fp32, row t at 256 t bytes, its 16-byte groups
+// XOR-permuted by t % 16), then at kCoefVec the vectors beta_t, c_t, C[n-1][s],
+// theta_s m(s, n-1) (64 floats each, offsets below) and the scalars
+// beta_{n-1}, c_{n-1}, P_{n-1}, n.
+constexpr uint32_t kCoefRecBytes = 17424;
+constexpr uint32_t kCoefVec = 16384;
+constexpr uint32_t kCoefBeta = 0, kCoefC = 256, kCoefCend = 512, kCoefPend = 768,
+                   kCoefScal = 1024, kCoefVecBytes = 1040;   // relative to kCoefVec
 
 // Index of token t's gate of sequence seq (per token, or per chunk).
 __host__ __device__ inline size_t gate_index(const LinearArgs& a, size_t seq, int t) {
@@ -188,8 +204,10 @@ cudaError_t linear_step_launch(const StepArgs& a, cudaStream_t s);
 bool bwd_local_tc_supported(const BwdArgs& a);
 // Its chain pass on the tensor cores (same shapes): the adjoint at every chunk
 // end from the records pass's records; offsets in floats into the workspace.
-cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, size_t off_rec,
-                                size_t off_part, cudaStream_t s);
+// The tensor-core scan that wrote the checkpoints also wrote its coefficient
+// records (coef, kCoefRecBytes per chunk) and the masked score tiles (tiles).
+cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, const void* coef,
+                                const void* tiles, size_t off_part, cudaStream_t s);
 cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
                                 cudaStream_t s);
 

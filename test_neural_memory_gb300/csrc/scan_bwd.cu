@@ -927,6 +927,9 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
     f.eta = a.eta; f.theta = a.theta; f.alpha = a.alpha;
     f.W0 = a.W0; f.S0 = a.S0; f.shared = a.shared;
     f.ckpt = ws + L.ckpt;
+    // the tensor-core passes take the scan's masked score tiles (in the space
+    // of the records, which they do not use) and its coefficient records
+    if (a.local_tc) f.score_tiles = ws + L.rec;
     cudaError_t e;
     if (a.fwd_tc) {
         f.workspace = ws + L.tcws;
@@ -951,17 +954,19 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
         (e = cudaFuncSetAttribute(bwd_local_kernel<Tin>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3)))
         return e;
-    bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
     if (a.local_tc) {
         // chain and local passes on the tensor cores
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = bwd_chain_tc_launch(a, ws, L.adj, L.rec, L.part, s)) != cudaSuccess) return e;
+        if ((e = bwd_chain_tc_launch(a, ws, L.adj, ws + L.tcws, ws + L.rec, L.part, s)) !=
+            cudaSuccess)
+            return e;
         if ((e = bwd_local_tc_launch(a, ws + L.ckpt, ws + L.adj, s)) != cudaSuccess) return e;
+        *launches += 2;
     } else {
+        bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);
         bwd_chain_kernel<Tin><<<dim3(nseq, (a.dv + kR2 - 1) / kR2), kBT2, sm2, s>>>(a, L, ws);
         bwd_local_kernel<Tin><<<dim3(nseq, L.nch), kBT3, sm3, s>>>(a, L, ws);
+        *launches += 3;
     }
-    *launches += 3;
     if (a.shared) {
         const size_t n = (size_t)a.H * L.sd;
         bwd_shared_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, L, ws);

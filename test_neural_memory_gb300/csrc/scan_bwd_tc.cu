@@ -707,9 +707,10 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 //
 // The adjoint of the state at every chunk end, chunks in reverse, for a slice
 // of 16 rows i of (dW, dS) (rows evolve independently).  Per chunk, with the
-// chunk's record (A, beta, c, C[n-1][.], pm, P_n):
+// masked score tile A~ and the coefficient vectors (beta, c, C[n-1][.], pm,
+// beta_n, c_n, P_n) that the forward scan left in the workspace:
 //   dWK = K dW^T, dSK = K dS^T                       [K; .] [dW; dS]^T  (MMA)
-//   de  = (-2 A^T) dZ - 2 (C_n o dWK + pm o dSK)      (-2A)^T dZ          (MMA)
+//   de  = -2 (A~^T dZ + C_n o dWK + pm o dSK)         A~^T dZ             (MMA)
 //   dW <- beta_n dW + (Q^T (beta o dZ) + K^T de)^T,    (Q^T, K^T MN-major; MMA)
 //   dS <- c_n dW + P_n dS + (Q^T (c o dZ))^T
 // with thread j holding column j of the slice's 16 rows of dW and dS in fp32
@@ -717,12 +718,11 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 // The next chunk's tiles and record load into the second of two stages while a
 // chunk computes.
 
-constexpr uint32_t kRecF = (kC * kC + 4 * kC + 1 + 3) / 4 * 4;   // floats per record
-constexpr uint32_t kRecSlot = ((kRecF * 4) + 63) / 64 * 64;
 constexpr int kSl = 16;                                          // rows of the slice
+constexpr uint32_t kVecSlot = (kCoefVecBytes + 63) / 64 * 64;
 
 struct ChainLayout {
-    uint32_t kq, rec, dzs, at, dzt, bzt, czt, det, ws, total;
+    uint32_t kq, at, dzs, vec, dzt, bzt, czt, det, ws, total;
 };
 
 __host__ __device__ constexpr ChainLayout chain_layout(int D) {
@@ -730,10 +730,10 @@ __host__ __device__ constexpr ChainLayout chain_layout(int D) {
     uint32_t o = 0;
     const uint32_t NH = D / 64;
     L.kq = o;  o += 2 * NH * 2 * kTile;     // two stages of [K_h][Q_h]
-    L.rec = o; o += 2 * kRecSlot;           // two stages of the record
+    L.at = o;  o += 2 * kTile;              // two stages of A~ [t][s] (swizzled, as stored)
     L.dzs = o; o += 2 * kC * kSl * 2;       // two stages of the dZ slice (64 x 16 bf16)
+    L.vec = o; o += 2 * kVecSlot;           // two stages of the coefficient vectors
     o = (o + 1023) / 1024 * 1024;
-    L.at = o;  o += kTile;                  // -2 A [t][s]
     L.dzt = o; o += kTile;                  // dZ slice [t][i] (16 of 64 columns)
     L.bzt = o; o += kTile;                  // beta_t dZ
     L.czt = o; o += kTile;                  // c_t dZ
@@ -754,7 +754,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap zmap, const BwdArgs a, float* ws,
-                    size_t off_adj, size_t off_rec, size_t off_part, int nch) {
+                    size_t off_adj, const uint8_t* coef, const uint8_t* tiles, size_t off_part,
+                    int nch) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -770,9 +771,9 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 
     auto kt = [&](int b, int h) { return sm + L.kq + (b * NH + h) * 2 * kTile; };
     auto qt = [&](int b, int h) { return kt(b, h) + kTile; };
-    auto recb = [&](int b) { return reinterpret_cast<float*>(sm + L.rec + b * kRecSlot); };
+    auto atb = [&](int b) { return sm + L.at + b * kTile; };
     auto dzs = [&](int b) { return sm + L.dzs + b * kC * kSl * 2; };
-    uint8_t* at = sm + L.at;
+    auto vecb = [&](int b) { return reinterpret_cast<float*>(sm + L.vec + b * kVecSlot); };
     uint8_t* dzt = sm + L.dzt;
     uint8_t* bzt = sm + L.bzt;
     uint8_t* czt = sm + L.czt;
@@ -796,14 +797,16 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     constexpr uint32_t kAc1 = 0, kAc2 = 32, kAc3 = 64;
 
     auto issue_loads = [&](int c, int b) {
-        mbar_expect_tx(&Y->full[b], 2 * NH * kTile + kC * kSl * 2 + kRecF * 4);
+        mbar_expect_tx(&Y->full[b], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
             tma_load_3d(kt(b, h), &kmap, &Y->full[b], 64 * h, c * kC, seq);
             tma_load_3d(qt(b, h), &qmap, &Y->full[b], 64 * h, c * kC, seq);
         }
         tma_load_3d(dzs(b), &zmap, &Y->full[b], r0, c * kC, seq);
-        bulk_load(recb(b), ws + off_rec + ((size_t)seq * nch + c) * kRecF, kRecF * 4, &Y->full[b]);
+        const size_t rec = (size_t)seq * nch + c;
+        bulk_load(atb(b), tiles + rec * kTile, kTile, &Y->full[b]);
+        bulk_load(vecb(b), coef + rec * kCoefRecBytes + kCoefVec, kCoefVecBytes, &Y->full[b]);
     };
     if (tid == 0 && nch > 0) issue_loads(nch - 1, 0);
 
@@ -836,13 +839,11 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[b], (k >> 1) & 1, status);
         // the next chunk's inputs into the other stage (its last use is complete)
         if (tid == 0 && ok && c > 0) issue_loads(c - 1, b ^ 1);
-        const float* rv = recb(b);
-        const float* Arec = rv;                      // A[t][s], row stride 64
-        const float* vbeta = rv + kC * kC;
-        const float* vc = vbeta + kC;
-        const float* vclast = vc + kC;
-        const float* vpm = vclast + kC;
-        const float Pn = vpm[kC];
+        const float* vbeta = vecb(b) + kCoefBeta / 4;
+        const float* vc = vecb(b) + kCoefC / 4;
+        const float* vclast = vecb(b) + kCoefCend / 4;
+        const float* vpm = vecb(b) + kCoefPend / 4;
+        const float* vscal = vecb(b) + kCoefScal / 4;   // beta_n, c_n, P_n, n
         // this chunk's end adjoint, for the local pass
         if (own && ok) {
             float* adj = ws + off_adj + ((size_t)seq * nch + c) * 2 * sd;
@@ -853,15 +854,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             }
         }
         if (ok) {
-            // -2 A [t][s], and the dZ slice, beta dZ, c dZ as 16-column tiles [t][i]
-            for (int x = tid; x < kC * 8; x += kThreads) {
-                const int t = x >> 3, c8 = x & 7;
-                const float4* src = reinterpret_cast<const float4*>(Arec + t * kC + 8 * c8);
-                const float4 u0 = src[0], u1 = src[1];
-                const float v[8] = {-2.f * u0.x, -2.f * u0.y, -2.f * u0.z, -2.f * u0.w,
-                                    -2.f * u1.x, -2.f * u1.y, -2.f * u1.z, -2.f * u1.w};
-                *reinterpret_cast<uint4*>(at + swz(t, c8)) = pack8(v);
-            }
+            // the dZ slice, beta dZ, c dZ as 16-column tiles [t][i]
             for (int x = tid; x < kC * 2; x += kThreads) {
                 const int t = x >> 1, c8 = x & 1;
                 float z[8], zb[8], zc[8];
@@ -880,7 +873,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK) and (-2 A)^T dZ (lanes 0-63)
+        // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK) and A~^T dZ (lanes 0-63)
         if (warp == 0 && ok) {
             tc_fence_after();
             if (elect_one()) {
@@ -891,7 +884,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                     mma_bf16(tmem + kAc1, sdesc(abase, 16, 1024, 2), sdesc(wsa + kk * 2048, 8192, 1024, 2),
                              id1, kk > 0);
                 }
-                const uint32_t aa = smem_u32(at), za = smem_u32(dzt);
+                const uint32_t aa = smem_u32(atb(b)), za = smem_u32(dzt);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + kAc2, sdesc(aa + kk * 2048, kTile, 1024, 2),
@@ -902,7 +895,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         }
         if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma, mma_phase++ & 1, status);
         if (ok && warp < 2) {
-            // de[s][i] = (-2 A^T dZ)[s][i] - 2 (C_n[s] dWK + pm[s] dSK), s < n
+            // de[s][i] = -2 ((A~^T dZ)[s][i] + C_n[s] dWK + pm[s] dSK), s < n
             tc_fence_after();
             const int sidx = warp * 32 + lane;
             float gw[16], gs[16], ad[16], de[16];
@@ -913,7 +906,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             const float cl = vclast[sidx], pmv = vpm[sidx];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                de[e] = sidx < n ? ad[e] - 2.f * (cl * gw[e] + pmv * gs[e]) : 0.f;
+                de[e] = sidx < n ? -2.f * (ad[e] + cl * gw[e] + pmv * gs[e]) : 0.f;
             *reinterpret_cast<uint4*>(det + swz(sidx, 0)) = pack8(de);
             *reinterpret_cast<uint4*>(det + swz(sidx, 1)) = pack8(de + 8);
         }
@@ -950,7 +943,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             tmem_ld16(tl + kAc3, uw);
             tmem_ld16(tl + kAc3 + 16, us);
             tmem_wait_ld();
-            const float bn = vbeta[n - 1], cn = vc[n - 1];
+            const float bn = vscal[0], cn = vscal[1], Pn = vscal[2];
             if (own) {
 #pragma unroll
                 for (int i = 0; i < kSl; ++i) {
@@ -1017,8 +1010,8 @@ bool bwd_local_tc_supported(const BwdArgs& a) {
     return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kC && a.T >= 1;
 }
 
-cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, size_t off_rec,
-                                size_t off_part, cudaStream_t s) {
+cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, const void* coef,
+                                const void* tiles, size_t off_part, cudaStream_t s) {
     const int D = a.dk, BH = a.B * a.H;
     const int nch = (a.T + kC - 1) / kC;
     CUtensorMap qm, km, zm;
@@ -1032,14 +1025,18 @@ cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, siz
         cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<128>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_chain_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj, off_rec,
+        bwd_chain_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
+                                                              static_cast<const uint8_t*>(coef),
+                                                              static_cast<const uint8_t*>(tiles),
                                                               off_part, nch);
     } else {
         const size_t smem = chain_layout(64).total + 1024;
         cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_chain_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj, off_rec,
+        bwd_chain_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
+                                                             static_cast<const uint8_t*>(coef),
+                                                             static_cast<const uint8_t*>(tiles),
                                                              off_part, nch);
     }
     return cudaGetLastError();

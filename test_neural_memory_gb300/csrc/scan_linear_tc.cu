@@ -99,6 +99,11 @@ constexpr uint32_t kVScal = kVBeta + 1024;       // beta_{n-1}, c_{n-1}, P_{n-1}
 constexpr uint32_t kRecBytes = kVScal + 16;      // 17424 (a multiple of 16)
 constexpr uint32_t kVecSlot = 17472;             // staged copy, 64-byte aligned slots
 
+static_assert(kRecBytes == kCoefRecBytes && kVBeta == kCoefVec && kVCvec == kCoefVec + kCoefC &&
+                  kVCend == kCoefVec + kCoefCend && kVPend == kCoefVec + kCoefPend &&
+                  kVScal == kCoefVec + kCoefScal,
+              "coefficient record layout");
+
 __host__ __device__ constexpr uint32_t c_offset(int t, int s) {
     return (uint32_t)t * 256u + (uint32_t)(((s >> 2) ^ (t & 15)) << 4) + (uint32_t)(s & 3) * 4u;
 }
@@ -652,6 +657,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // row m of the chunk's coefficient table; m >= 64 ->
         // M[m-64][s] = C[n-1][s] (k'_{m-64} . k_s).
         const int m = (warp & 3) * 32 + lane;
+        // the first slice of each sequence also stores the score tiles
+        uint8_t* tile_out = (a.score_tiles && slice == 0 && m < 64)
+                                ? static_cast<uint8_t*>(a.score_tiles) + (size_t)seq * nch * 8192 + m * 128
+                                : nullptr;
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int b = c & 1, st = c % kNS;
@@ -699,6 +708,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     for (int i = 0; i < 8; ++i)
                         p[i] = pack_bf16(r[2 * i] * wt[2 * i], r[2 * i + 1] * wt[2 * i + 1]);
                     tmem_st8(tl + kAM + b * 32 + 8 * q4, p);
+                    if (tile_out) {
+                        uint8_t* row = tile_out + (size_t)c * 8192;
+                        *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (m & 7)) << 4)) =
+                            make_uint4(p[0], p[1], p[2], p[3]);
+                        *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (m & 7)) << 4)) =
+                            make_uint4(p[4], p[5], p[6], p[7]);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();

@@ -460,7 +460,8 @@ int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     a.status = status_ptr();
     if (!a.status) return TTM_ERR_CUDA;
     a.wait_cycles = g_wait_cycles.load();
-    a.local_tc = g_policy != TTM_KERNEL_SIMT && ttm::bwd_local_tc_supported(a) ? 1 : 0;
+    // the tensor-core passes read what the tensor-core scan leaves in the workspace
+    a.local_tc = g_policy != TTM_KERNEL_SIMT && a.fwd_tc && ttm::bwd_local_tc_supported(a) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     const cudaError_t e = ttm::linear_bwd_launch(a, s, &launches);
