@@ -25,6 +25,7 @@ struct LinearArgs {
     // ckpt[seq][chunk][W | S][dv][dk] (fp32), and z / W_out may be NULL.  The
     // gradient passes read these checkpoints.
     float* ckpt;
+    int ckpt_bf16;            // tensor-core scan only: ckpt holds bf16 values
     // Tensor-core scan with ckpt only (may be NULL): the masked score tile
     // A~[t][s] = C[t][s] (q_t . k_s) (zero for s > t and outside the chunk) of
     // every chunk in bf16, score_tiles[seq][chunk] = 64 rows t of 128 bytes,
@@ -208,8 +209,11 @@ bool bwd_local_tc_supported(const BwdArgs& a);
 // records (coef, kCoefRecBytes per chunk) and the masked score tiles (tiles).
 cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, const void* coef,
                                 const void* tiles, size_t off_part, cudaStream_t s);
-cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
-                                cudaStream_t s);
+// Checkpoints (ckpt) and adjoints (adj) are bf16 [seq][chunk][W | S][d][d]:
+// the tensor-core scan writes them with ckpt_bf16, the tensor-core chain the
+// adjoints.
+cudaError_t bwd_local_tc_launch(const BwdArgs& a, const void* ckpt, const void* adj,
+                                const void* coef, cudaStream_t s);
 
 // Gradient of the linear / Titans scan (scan_bwd.cu): chunk <= 64, dk <= 128.
 // The workspace holds the state and its adjoint at every chunk boundary.

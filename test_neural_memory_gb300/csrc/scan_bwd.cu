@@ -929,7 +929,10 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
     f.ckpt = ws + L.ckpt;
     // the tensor-core passes take the scan's masked score tiles (in the space
     // of the records, which they do not use) and its coefficient records
-    if (a.local_tc) f.score_tiles = ws + L.rec;
+    if (a.local_tc) {
+        f.score_tiles = ws + L.rec;
+        f.ckpt_bf16 = 1;   // the tensor-core local pass loads bf16 checkpoints by TMA
+    }
     cudaError_t e;
     if (a.fwd_tc) {
         f.workspace = ws + L.tcws;
@@ -959,7 +962,8 @@ cudaError_t launch_passes(const BwdArgs& a, const BwdLayout& L, cudaStream_t s, 
         if ((e = bwd_chain_tc_launch(a, ws, L.adj, ws + L.tcws, ws + L.rec, L.part, s)) !=
             cudaSuccess)
             return e;
-        if ((e = bwd_local_tc_launch(a, ws + L.ckpt, ws + L.adj, s)) != cudaSuccess) return e;
+        if ((e = bwd_local_tc_launch(a, ws + L.ckpt, ws + L.adj, ws + L.tcws, s)) != cudaSuccess)
+            return e;
         *launches += 2;
     } else {
         bwd_records_kernel<Tin><<<dim3(nseq, L.nch), kBT, sm0, s>>>(a, L, ws);

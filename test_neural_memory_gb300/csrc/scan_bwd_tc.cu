@@ -21,11 +21,12 @@
 // Every contraction is a tcgen05 MMA with M = 128: the token-row products
 // stack [K; Q] (or pad with rows that are never read back), and the products
 // whose rows are tokens and whose result is d wide are taken transposed
-// (dQ^T, dK^T: rows = key index j).  The state and adjoint matrices come in
-// fp32 from the checkpoints and are rounded to bf16 in shared memory, one
-// half of their rows (the value index i) at a time; DE, De, dQ^T and dK^T
-// accumulate over the halves in tensor memory.  One CTA of 256 threads per
-// (sequence, chunk), every chunk at once.
+// (dQ^T, dK^T: rows = key index j).  The state and adjoint matrices arrive in
+// bf16 (the forward scan writes the checkpoints, the chain the adjoints) and
+// load by TMA straight into their operand tiles, one half of their rows (the
+// value index i) at a time; DE, De, dQ^T and dK^T accumulate over the halves
+// in tensor memory.  One CTA of 256 threads per (sequence, chunk), every
+// chunk at once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,6 +48,7 @@ constexpr uint32_t kTile = 8192;    // 64 rows x 128 bytes (bf16)
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kLdc = kC + 1;        // row stride of the fp32 tables
+constexpr int kQs = kC + 2;         // row stride of the bf16 score copy (33 words: no conflicts)
 constexpr long long kWaitCycles = 4000000000LL;
 
 // TMEM columns (each accumulator 64 columns; lanes = rows)
@@ -60,13 +62,14 @@ constexpr uint32_t kDQ = 384;   // dQ^T (lanes j, columns t)
 constexpr uint32_t kDK = 448;   // dK^T (lanes j, columns s)
 
 struct Layout {
-    uint32_t kq, dz, vv, mat, ei, ec, ep, bz, cz, dei, at, gg, qkb, cm, vec, bars, total;
+    uint32_t kq, dz, vv, mat, ei, ec, ep, bz, cz, dei, at, gg, qkb, crec, vec, bars, total;
 };
 
 // [K_h][Q_h] per 64-column half of the keys (so [K; Q] is one 128-row
 // operand); dZ and V per half of the value index; the four state / adjoint
 // matrices of the current value half (rows i, bf16, one tile per key half);
-// the bf16 operand tiles of the chunk; the fp32 coefficient table; vectors.
+// the bf16 operand tiles of the chunk; the chunk's coefficient record (as the
+// forward scan's pre-pass wrote it); vectors.
 __host__ __device__ constexpr Layout make_layout(int D) {
     Layout L{};
     uint32_t o = 0;
@@ -83,8 +86,8 @@ __host__ __device__ constexpr Layout make_layout(int D) {
     L.dei = o;  o += kTile;              // De of the half [s][i]
     L.at = o;   o += kTile;              // -2 A~ [t][s]
     L.gg = o;   o += kTile;              // -2 G [t][s]
-    L.qkb = o;  o += kC * kC * 2;        // Q K^T (bf16, plain [t][s])
-    L.cm = o;   o += kC * kLdc * 4;      // C (fp32)
+    L.qkb = o;  o += kC * kQs * 2;       // Q K^T (bf16, [t][s], padded rows)
+    L.crec = o; o += (kCoefRecBytes + 63) / 64 * 64;   // C table, beta, c, C[n-1], pm
     L.vec = o;  o += 16 * kC * 4;        // gate vectors
     L.bars = o; o += 64;
     L.total = o;
@@ -115,7 +118,7 @@ __device__ __forceinline__ void unpack8(uint4 v, float* x) {
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4); }
 
 struct Sync {
-    uint64_t full, mma;
+    uint64_t full, mma, mfull;
     long long limit;
     int abort;
     uint32_t tmem;
@@ -158,7 +161,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap zmap, const __grid_constant__ CUtensorMap vmap,
-                    const BwdArgs a, const float* ckpt, const float* adj, int nch) {
+                    const __grid_constant__ CUtensorMap ckmap, const __grid_constant__ CUtensorMap admap,
+                    const BwdArgs a, const uint8_t* coef, int nch) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -170,7 +174,6 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     const int T = a.T;
     const int n = min(kC, T - c * kC);
     const size_t tok0 = (size_t)seq * T + (size_t)c * kC;
-    const size_t sd = (size_t)D * D;
     int* status = a.status;
 
     uint8_t* kq = sm + L.kq;
@@ -188,15 +191,26 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     uint8_t* at = sm + L.at;
     uint8_t* gg = sm + L.gg;
     __nv_bfloat16* qkb = reinterpret_cast<__nv_bfloat16*>(sm + L.qkb);
-    float* Cm = reinterpret_cast<float*>(sm + L.cm);
+    const uint8_t* crec = sm + L.crec;
+    // C[t][4g .. 4g+3] from the record's table (row t: 16-byte groups permuted by t % 16)
+    auto cgroup = [&](int t, int g) {
+        return *reinterpret_cast<const float4*>(crec + t * 256 + ((g ^ (t & 15)) << 4));
+    };
+    auto crow16 = [&](int t, int s0, float* w) {   // C[t][s0 .. s0+15], s0 % 16 == 0
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 f = cgroup(t, s0 / 4 + g);
+            w[4 * g] = f.x; w[4 * g + 1] = f.y; w[4 * g + 2] = f.z; w[4 * g + 3] = f.w;
+        }
+    };
+    const float* beta = reinterpret_cast<const float*>(crec + kCoefVec + kCoefBeta);
+    const float* cc = reinterpret_cast<const float*>(crec + kCoefVec + kCoefC);
+    const float* cend = reinterpret_cast<const float*>(crec + kCoefVec + kCoefCend);
+    const float* pm = reinterpret_cast<const float*>(crec + kCoefVec + kCoefPend);
     float* th = reinterpret_cast<float*>(sm + L.vec);
     float* et = th + kC;
     float* al = et + kC;
-    float* beta = al + kC;
-    float* P = beta + kC;
-    float* cc = P + kC;
-    float* pm = cc + kC;
-    float* dbeta = pm + kC;
+    float* dbeta = al + kC;
     float* dcc = dbeta + kC;
     float* dclast = dcc + kC;
     float* dpm = dclast + kC;
@@ -208,6 +222,7 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     if (tid == 0) {
         mbar_init(&Y->full, 1);
         mbar_init(&Y->mma, 1);
+        mbar_init(&Y->mfull, 1);
         Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
         Y->abort = 0;
         fence_mbar_init();
@@ -221,8 +236,26 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     const int row = (warp & 3) * 32 + lane;                          // TMEM lane of this thread
     const int chalf = warp >> 2;                                     // column half of an epilogue
 
+    // W, S (checkpoint) and dWe, dSe (adjoint) rows 64 I .. 64 I + 63 of this
+    // chunk into the matrix tiles (one thread)
+    int halves_issued = 0;
+    auto load_half = [&](int I) {
+        mbar_expect_tx(&Y->mfull, 4 * NH * kTile);
+        const int z0 = (seq * nch + c) * 2;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            tma_load_3d(mtile(0, h), &ckmap, &Y->mfull, 64 * h, 64 * I, z0);
+            tma_load_3d(mtile(1, h), &ckmap, &Y->mfull, 64 * h, 64 * I, z0 + 1);
+            tma_load_3d(mtile(2, h), &admap, &Y->mfull, 64 * h, 64 * I, z0);
+            tma_load_3d(mtile(3, h), &admap, &Y->mfull, 64 * h, 64 * I, z0 + 1);
+        }
+        ++halves_issued;
+    };
     if (tid == 0) {
-        mbar_expect_tx(&Y->full, 4 * NH * kTile);
+        load_half(0);
+        mbar_expect_tx(&Y->full, 4 * NH * kTile + kCoefRecBytes);
+        bulk_load(sm + L.crec, coef + ((size_t)seq * nch + c) * kCoefRecBytes, kCoefRecBytes,
+                  &Y->full);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
             tma_load_3d(ktile(h), &kmap, &Y->full, 64 * h, c * kC, seq);
@@ -236,14 +269,10 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         et[tid] = (tid < n && a.eta) ? a.eta[tok0 + tid] : 0.f;
         al[tid] = (tid < n && a.alpha) ? a.alpha[tok0 + tid] : 0.f;
         dbeta[tid] = dcc[tid] = dclast[tid] = dpm[tid] = dkeep[tid] = deta[tid] = 0.f;
-        beta[tid] = P[tid] = cc[tid] = 0.f;
     }
     if (tid < 4) scal[tid] = 0.f;
     __syncthreads();
-    simt::block_coefficients(n, kC, th, et, al, beta, P, cc, Cm, kLdc, pm);   // ends in a barrier
 
-    const float* ck = ckpt + ((size_t)seq * nch + c) * 2 * sd;
-    const float* ad = adj + ((size_t)seq * nch + c) * 2 * sd;
     uint32_t mma_phase = 0;
     bool ok = wait_bar(Y, &Y->full, 0, status);
 
@@ -265,39 +294,26 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         __syncwarp();
     }
 
-    // fp32 state / adjoint rows of value half I -> bf16 tiles [i][j] (and the
-    // three inner products of the end-state term); beta dZ, c dZ of the half
-    auto convert_half = [&](int I) {
+    // the three inner products of the end-state term over value half I (from
+    // the bf16 matrix tiles), and beta dZ, c dZ of the half
+    auto prep_half = [&](int I) {
         float p0 = 0.f, p1 = 0.f, p2 = 0.f;
         constexpr int kChunks = 64 * (D / 8);                  // (row, 8-column chunk) pairs
         for (int x = tid; x < kChunks; x += kThreads) {
             const int i = x / (D / 8), c8 = x % (D / 8);
-            const size_t g = (size_t)(64 * I + i) * D + 8 * c8;
-            float w[8], s[8], gw[8], gs[8];
-            const float4* pw = reinterpret_cast<const float4*>(ck + g);
-            const float4* ps = reinterpret_cast<const float4*>(ck + sd + g);
-            const float4* pgw = reinterpret_cast<const float4*>(ad + g);
-            const float4* pgs = reinterpret_cast<const float4*>(ad + sd + g);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float4 a0 = pw[h], a1 = ps[h], a2 = pgw[h], a3 = pgs[h];
-                w[4 * h] = a0.x; w[4 * h + 1] = a0.y; w[4 * h + 2] = a0.z; w[4 * h + 3] = a0.w;
-                s[4 * h] = a1.x; s[4 * h + 1] = a1.y; s[4 * h + 2] = a1.z; s[4 * h + 3] = a1.w;
-                gw[4 * h] = a2.x; gw[4 * h + 1] = a2.y; gw[4 * h + 2] = a2.z; gw[4 * h + 3] = a2.w;
-                gs[4 * h] = a3.x; gs[4 * h + 1] = a3.y; gs[4 * h + 2] = a3.z; gs[4 * h + 3] = a3.w;
-            }
+            const int h = c8 >> 3;
+            const uint32_t off = swz(i, c8 & 7);
+            float w[8], sv[8], gw[8], gs[8];
+            unpack8(*reinterpret_cast<const uint4*>(mtile(0, h) + off), w);
+            unpack8(*reinterpret_cast<const uint4*>(mtile(1, h) + off), sv);
+            unpack8(*reinterpret_cast<const uint4*>(mtile(2, h) + off), gw);
+            unpack8(*reinterpret_cast<const uint4*>(mtile(3, h) + off), gs);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 p0 = fmaf(gw[e], w[e], p0);
-                p1 = fmaf(gw[e], s[e], p1);
-                p2 = fmaf(gs[e], s[e], p2);
+                p1 = fmaf(gw[e], sv[e], p1);
+                p2 = fmaf(gs[e], sv[e], p2);
             }
-            const int h = c8 >> 3, cc8 = c8 & 7;
-            const uint32_t off = swz(i, cc8);
-            *reinterpret_cast<uint4*>(mtile(0, h) + off) = pack8(w);
-            *reinterpret_cast<uint4*>(mtile(1, h) + off) = pack8(s);
-            *reinterpret_cast<uint4*>(mtile(2, h) + off) = pack8(gw);
-            *reinterpret_cast<uint4*>(mtile(3, h) + off) = pack8(gs);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -327,7 +343,8 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         }
     };
 
-    if (ok) convert_half(0);
+    if (ok) ok = wait_bar(Y, &Y->mfull, 0, status);
+    if (ok) prep_half(0);
     if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
     if (ok && row >= 64) {
         // -2 A~[t][s] = -2 C[t][s] (q_t . k_s) for s <= t, and Q K^T in bf16
@@ -336,15 +353,18 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int s0 = 32 * chalf + 16 * q;
-            float r[16], x[16];
+            float r[16], x[16], cw[16];
             tmem_ld16(tl + kA1 + s0, r);
+            crow16(t, s0, cw);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int s = s0 + e;
-                x[e] = (s <= t && t < n) ? -2.f * Cm[t * kLdc + s] * r[e] : 0.f;
-                qkb[t * kC + s] = __float2bfloat16_rn(r[e]);
+                x[e] = (s <= t && t < n) ? -2.f * cw[e] * r[e] : 0.f;
             }
+#pragma unroll
+            for (int e = 0; e < 16; e += 2)
+                *reinterpret_cast<uint32_t*>(qkb + t * kQs + s0 + e) = pack_bf16(r[e], r[e + 1]);
             *reinterpret_cast<uint4*>(at + swz(t, s0 / 8)) = pack8(x);
             *reinterpret_cast<uint4*>(at + swz(t, s0 / 8 + 1)) = pack8(x + 8);
         }
@@ -355,7 +375,8 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 
     for (int I = 0; I < NH; ++I) {
         if (I > 0 && ok) {
-            convert_half(I);
+            ok = wait_bar(Y, &Y->mfull, I & 1, status);
+            if (ok) prep_half(I);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -385,7 +406,7 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 // token s: E = K W^T - V, e_s . (dWe k_s), e_s . (dSe k_s), the scaled
                 // copies of E, and -2 (C[n-1][s] dWK + pm[s] dSK) into the De accumulator
                 const int s = row;
-                const float cn = n > 0 ? Cm[(n - 1) * kLdc + s] : 0.f, pms = pm[s];
+                const float cn = cend[s], pms = pm[s];
                 float pw = 0.f, ps = 0.f;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -522,6 +543,10 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         }
         // the next half overwrites the matrices and operand tiles
         if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+        if (ok && tid == 0 && I + 1 < NH) {
+            fence_proxy_async_smem();
+            load_half(I + 1);
+        }
     }
 
     // DE complete: dC = -2 (Q K^T) o DE (+ the end-state term on the last row)
@@ -533,16 +558,24 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int s0 = 32 * chalf + 16 * q;
-            float r[16], x[16];
+            float r[16], x[16], cw[16], qk[16];
             tmem_ld16(tl + kDE + s0, r);
+            crow16(t, s0, cw);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(qkb + t * kQs + s0 + e);
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+                qk[e] = f.x;
+                qk[e + 1] = f.y;
+            }
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int s = s0 + e;
                 const bool in = s <= t && t < n;
                 const float de = in ? r[e] : 0.f;
-                x[e] = -2.f * Cm[t * kLdc + s] * de;
-                dC[t * kLdc + s] = -2.f * __bfloat162float(qkb[t * kC + s]) * de -
+                x[e] = -2.f * cw[e] * de;
+                dC[t * kLdc + s] = -2.f * qk[e] * de -
                                    (t == n - 1 && s < n ? 2.f * dclast[s] : 0.f);
             }
             *reinterpret_cast<uint4*>(gg + swz(t, s0 / 8)) = pack8(x);
@@ -602,75 +635,164 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     }
     __syncthreads();
 
-    // gate gradients: C[t][s] = theta_s w(s,t), pm[s] = theta_s m(s,n-1) with
-    // m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t)
-    // (w(s,s) = m(s,s) = 1), as in the CUDA-core local pass
+    // gate gradients.  C[t][s] = theta_s w(s,t) and pm[s] = theta_s m(s,n-1)
+    // with m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t),
+    // w(s,s) = m(s,s) = 1.  Warps 0-1 walk the rows with one column s per lane
+    // (gates broadcast from registers): forward for w, m and d theta_s, then
+    // backward for the adjoints of w and m, whose products with w(s,t-1) and
+    // m(s,t-1), summed over s < t, give d(1 - alpha_t) and d eta_t.
     float* Wm = dC + kC * kLdc;                      // after dC (the staging is consumed)
     float* Mm = Wm + kC * kLdc;
     float* Kc = Mm + kC * kLdc;
     float* Ec = Kc + kC * kLdc;
-    if (ok) {
-        for (int s = tid; s < kC; s += kThreads)
-            for (int t = 0; t < kC; ++t) Kc[t * kLdc + s] = Ec[t * kLdc + s] = 0.f;
-        for (int s = tid; s < n; s += kThreads) {
-            float m = 1.f, w = 1.f;
-            Wm[s * kLdc + s] = 1.f;
-            Mm[s * kLdc + s] = 1.f;
-            for (int t = s + 1; t < n; ++t) {
-                m = et[t] * m;
-                w = (1.f - al[t]) * w + m;
-                Wm[t * kLdc + s] = w;
-                Mm[t * kLdc + s] = m;
+    if (ok && warp < 2) {
+        const int s = warp * 32 + lane;
+        const float e_lo = et[lane], e_hi = et[lane + 32];
+        const float a_lo = al[lane], a_hi = al[lane + 32];
+        const float ths = th[s];
+        // blocks of 8 rows: the block's loads, then its 8 dependent steps in
+        // registers, then its stores (so no load waits behind a store)
+        float m = 0.f, w = 0.f, g = 0.f;
+#pragma unroll
+        for (int t0 = 0; t0 < kC; t0 += 8) {
+            if (t0 < n) {
+                float dcb[8], wb[8], mb[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) dcb[u] = dC[(t0 + u) * kLdc + s];   // 0 past the chunk
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + u;
+                    const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
+                    const float k1 = 1.f - __shfl_sync(0xffffffffu, t < 32 ? a_lo : a_hi, t & 31);
+                    const float mn = t == s ? 1.f : e * m;     // stays 0 before the column starts
+                    const float wn = t == s ? 1.f : fmaf(k1, w, mn);
+                    const bool live = t < n;
+                    m = live ? mn : m;
+                    w = live ? wn : w;
+                    wb[u] = w;
+                    mb[u] = m;
+                    g = fmaf(dcb[u], w, g);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    Wm[(t0 + u) * kLdc + s] = wb[u];
+                    Mm[(t0 + u) * kLdc + s] = mb[u];
+                }
+            }
+        }
+        dth[s] = g - 2.f * dpm[s] * m;
+        float dw = s < n ? ths * dC[(n - 1) * kLdc + s] : 0.f;
+        float dm = s < n ? ths * (-2.f * dpm[s]) : 0.f;
+#pragma unroll
+        for (int tb = kC - 1; tb >= 1; tb -= 8) {      // rows tb, tb-1, .., tb-7 (row 0 skipped)
+            if (tb - 7 < n) {
+                float wm[8], mm[8], dc[8], kc[8], ec[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = tb - u;
+                    if (t >= 1) {
+                        wm[u] = Wm[(t - 1) * kLdc + s];
+                        mm[u] = Mm[(t - 1) * kLdc + s];
+                        dc[u] = dC[(t - 1) * kLdc + s];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = tb - u;
+                    if (t >= 1) {
+                        const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
+                        const float k1 = 1.f - __shfl_sync(0xffffffffu, t < 32 ? a_lo : a_hi, t & 31);
+                        const bool act = t < n && t > s;
+                        const float dm1 = dm + dw;
+                        kc[u] = act ? dw * wm[u] : 0.f;
+                        ec[u] = act ? dm1 * mm[u] : 0.f;
+                        dm = act ? e * dm1 : dm;
+                        dw = act ? fmaf(k1, dw, ths * dc[u]) : dw;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = tb - u;
+                    if (t >= 1) {
+                        Kc[t * kLdc + s] = kc[u];
+                        Ec[t * kLdc + s] = ec[u];
+                    }
+                }
             }
         }
     }
     __syncthreads();
     if (ok) {
-        for (int s = tid; s < n; s += kThreads) {
-            const float ths = th[s];
-            float g = -2.f * dpm[s] * Mm[(n - 1) * kLdc + s];
-            for (int t = s; t < n; ++t) g += dC[t * kLdc + s] * Wm[t * kLdc + s];
-            dth[s] = g;
-            float dw = ths * dC[(n - 1) * kLdc + s];
-            float dm = ths * (-2.f * dpm[s]);
-            for (int t = n - 1; t > s; --t) {
-                Kc[t * kLdc + s] = dw * Wm[(t - 1) * kLdc + s];
-                dm += dw;
-                Ec[t * kLdc + s] = dm * Mm[(t - 1) * kLdc + s];
-                dm = et[t] * dm;
-                dw = (1.f - al[t]) * dw + ths * dC[(t - 1) * kLdc + s];
-            }
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        for (int t = tid; t < n; t += kThreads) {
-            float gk = 0.f, ge = 0.f;
-            for (int s = 0; s < t; ++s) {
+        // sums over s < t, four threads per row
+        const int t = tid >> 2, part = tid & 3;
+        float gk = 0.f, ge = 0.f;
+        if (t < n) {
+            for (int s = part; s < t; s += 4) {
                 gk += Kc[t * kLdc + s];
                 ge += Ec[t * kLdc + s];
             }
+        }
+        gk += __shfl_xor_sync(0xffffffffu, gk, 1);
+        ge += __shfl_xor_sync(0xffffffffu, ge, 1);
+        gk += __shfl_xor_sync(0xffffffffu, gk, 2);
+        ge += __shfl_xor_sync(0xffffffffu, ge, 2);
+        if (part == 0 && t < n) {
             dkeep[t] += gk;
             deta[t] += ge;
         }
     }
     __syncthreads();
-    if (ok && tid == 0) {
-        float rb = 0.f, rc = 0.f, rp = 0.f;
-        for (int t = n - 1; t >= 0; --t) {
-            const bool last = t == n - 1;
-            const float db = dbeta[t] + rb + (last ? scal[0] : 0.f);
-            const float dcv = dcc[t] + rc + (last ? scal[1] : 0.f);
-            const float dp = rp + dcv + (last ? scal[2] : 0.f);
-            const float keep = 1.f - al[t];
-            const float cprev = t > 0 ? cc[t - 1] : 0.f;
-            const float bprev = t > 0 ? beta[t - 1] : 1.f;
-            const float pprev = t > 0 ? P[t - 1] : 1.f;
-            dkeep[t] += dcv * cprev + db * bprev;
-            deta[t] += dp * pprev;
-            rc = keep * dcv;
-            rb = keep * db;
-            rp = et[t] * dp;
+    if (ok && warp == 0) {
+        // the prefix recurrences beta_t = (1 - alpha_t) beta_{t-1},
+        // P_t = eta_t P_{t-1}, c_t = (1 - alpha_t) c_{t-1} + P_t taken back:
+        // their adjoints obey r_t = a_t + g_{t+1} r_{t+1}, solved by a warp scan
+        // with two tokens per lane
+        const int t0 = 2 * lane, t1 = t0 + 1;
+        const float kp0 = t0 < n ? 1.f - al[t0] : 0.f, kp1 = t1 < n ? 1.f - al[t1] : 0.f;
+        const float e0 = t0 < n ? et[t0] : 0.f, e1 = t1 < n ? et[t1] : 0.f;
+        const float kp_next = __shfl_down_sync(0xffffffffu, kp0, 1);
+        const float e_next = __shfl_down_sync(0xffffffffu, e0, 1);
+        const float kn1 = lane < 31 ? kp_next : 0.f, en1 = lane < 31 ? e_next : 0.f;
+        // P_{t-1} of both tokens (multiplicative prefix scan, 1 past the chunk)
+        float pp = (t0 < n ? e0 : 1.f) * (t1 < n ? e1 : 1.f);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, pp, off);
+            if (lane >= off) pp *= v;
+        }
+        float pex = __shfl_up_sync(0xffffffffu, pp, 1);
+        if (lane == 0) pex = 1.f;
+        const float pprev0 = pex, pprev1 = pex * (t0 < n ? e0 : 1.f);
+        auto rev = [&](float a0, float a1, float g0, float g1, float& r0, float& r1) {
+            float B = fmaf(g0, a1, a0), A = g0 * g1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float A2 = __shfl_down_sync(0xffffffffu, A, off);
+                const float B2 = __shfl_down_sync(0xffffffffu, B, off);
+                if (lane + off < 32) {
+                    B = fmaf(A, B2, B);
+                    A = A * A2;
+                }
+            }
+            r0 = B;
+            const float nx = __shfl_down_sync(0xffffffffu, B, 1);
+            r1 = fmaf(g1, lane < 31 ? nx : 0.f, a1);
+        };
+        auto av = [&](const float* v, int t, float last) {
+            return t < n ? v[t] + (t == n - 1 ? last : 0.f) : 0.f;
+        };
+        float db0, db1, dcv0, dcv1, dp0, dp1;
+        rev(av(dbeta, t0, scal[0]), av(dbeta, t1, scal[0]), kp1, kn1, db0, db1);
+        rev(av(dcc, t0, scal[1]), av(dcc, t1, scal[1]), kp1, kn1, dcv0, dcv1);
+        rev(t0 < n ? dcv0 + (t0 == n - 1 ? scal[2] : 0.f) : 0.f,
+            t1 < n ? dcv1 + (t1 == n - 1 ? scal[2] : 0.f) : 0.f, e1, en1, dp0, dp1);
+        if (t0 < n) {
+            dkeep[t0] += dcv0 * (t0 > 0 ? cc[t0 - 1] : 0.f) + db0 * (t0 > 0 ? beta[t0 - 1] : 1.f);
+            deta[t0] += dp0 * pprev0;
+        }
+        if (t1 < n) {
+            dkeep[t1] += dcv1 * cc[t0] + db1 * beta[t0];
+            deta[t1] += dp1 * pprev1;
         }
     }
     __syncthreads();
@@ -685,6 +807,11 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         // copies in flight before the kernel's shared memory goes
         const long long t0 = clock64();
         while (!mbar_try_wait(&Y->full, 0) && clock64() - t0 < Y->limit) {
+        }
+        if (halves_issued > 0) {
+            const long long t1 = clock64();
+            while (!mbar_try_wait(&Y->mfull, (halves_issued - 1) & 1) && clock64() - t1 < Y->limit) {
+            }
         }
     }
     if (warp == 0) {
@@ -846,11 +973,12 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         const float* vscal = vecb(b) + kCoefScal / 4;   // beta_n, c_n, P_n, n
         // this chunk's end adjoint, for the local pass
         if (own && ok) {
-            float* adj = ws + off_adj + ((size_t)seq * nch + c) * 2 * sd;
+            __nv_bfloat16* adj = reinterpret_cast<__nv_bfloat16*>(ws + off_adj) +
+                                 ((size_t)seq * nch + c) * 2 * sd;
 #pragma unroll
             for (int i = 0; i < kSl; ++i) {
-                adj[(size_t)(r0 + i) * D + j] = dw[i];
-                adj[sd + (size_t)(r0 + i) * D + j] = dsv[i];
+                adj[(size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dw[i]);
+                adj[sd + (size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dsv[i]);
             }
         }
         if (ok) {
@@ -1007,7 +1135,10 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 }  // namespace
 
 bool bwd_local_tc_supported(const BwdArgs& a) {
-    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kC && a.T >= 1;
+    // matrices of the checkpoints as the 32-bit third coordinate of a TMA tile
+    const long long nmat = (long long)a.B * a.H * ((a.T + kC - 1) / kC) * 2;
+    return a.bf16 && a.dk == a.dv && (a.dk == 64 || a.dk == 128) && a.chunk == kC && a.T >= 1 &&
+           nmat < (1LL << 31);
 }
 
 cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, const void* coef,
@@ -1042,29 +1173,35 @@ cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, con
     return cudaGetLastError();
 }
 
-cudaError_t bwd_local_tc_launch(const BwdArgs& a, const float* ckpt, const float* adj,
-                                cudaStream_t s) {
+cudaError_t bwd_local_tc_launch(const BwdArgs& a, const void* ckpt, const void* adj,
+                                const void* coef, cudaStream_t s) {
     const int D = a.dk, BH = a.B * a.H;
     const int nch = (a.T + kC - 1) / kC;
-    CUtensorMap qm, km, zm, vm;
+    CUtensorMap qm, km, zm, vm, cm, am;
+    // the checkpoints and adjoints as (64 columns j) x (64 rows i) tiles of the
+    // matrices [seq][chunk][W | S]
+    const int nmat = BH * nch * 2;
     if (!make_token_tile_map(&qm, a.q, BH, a.T, D, 64, true) ||
         !make_token_tile_map(&km, a.k, BH, a.T, D, 64, true) ||
         !make_token_tile_map(&zm, a.dz, BH, a.T, D, 64, true) ||
-        !make_token_tile_map(&vm, a.v, BH, a.T, D, 64, true))
+        !make_token_tile_map(&vm, a.v, BH, a.T, D, 64, true) ||
+        !make_token_tile_map(&cm, ckpt, nmat, D, D, 64, true) ||
+        !make_token_tile_map(&am, adj, nmat, D, D, 64, true))
         return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(BH * nch));
+    const uint8_t* cf = static_cast<const uint8_t*>(coef);
     if (D == 128) {
         const size_t smem = make_layout(128).total + 1024;
         cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel<128>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_local_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, a, ckpt, adj, nch);
+        bwd_local_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, cm, am, a, cf, nch);
     } else {
         const size_t smem = make_layout(64).total + 1024;
         cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel<64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_local_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, a, ckpt, adj, nch);
+        bwd_local_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, vm, cm, am, a, cf, nch);
     }
     return cudaGetLastError();
 }

@@ -466,12 +466,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int b = c & 1, st = c % kNS;
             if (a.ckpt && own && ok) {
                 // the state at this chunk's start, for the gradient passes
-                float* ck = a.ckpt + ((size_t)seq * nch + c) * 2 * (size_t)D * D +
-                            (size_t)r0 * D + j;
+                const size_t o = ((size_t)seq * nch + c) * 2 * (size_t)D * D + (size_t)r0 * D + j;
+                if (a.ckpt_bf16) {
+                    __nv_bfloat16* ck = reinterpret_cast<__nv_bfloat16*>(a.ckpt) + o;
 #pragma unroll
-                for (int i = 0; i < kRows; ++i) {
-                    ck[(size_t)i * D] = w[i];
-                    ck[(size_t)D * D + (size_t)i * D] = s[i];
+                    for (int i = 0; i < kRows; ++i) {
+                        ck[(size_t)i * D] = __float2bfloat16_rn(w[i]);
+                        ck[(size_t)D * D + (size_t)i * D] = __float2bfloat16_rn(s[i]);
+                    }
+                } else {
+                    float* ck = a.ckpt + o;
+#pragma unroll
+                    for (int i = 0; i < kRows; ++i) {
+                        ck[(size_t)i * D] = w[i];
+                        ck[(size_t)D * D + (size_t)i * D] = s[i];
+                    }
                 }
             }
             if (ok) ok = wait_all(B, &B->full[st], (c / kNS) & 1, status);
