@@ -219,23 +219,6 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     float* dth = deta + kC;
     float* scal = dth + kC;          // <dWe, W>, <dWe, S>, <dSe, S>
 
-    if (tid == 0) {
-        mbar_init(&Y->full, 1);
-        mbar_init(&Y->mma, 1);
-        mbar_init(&Y->mfull, 1);
-        Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
-        Y->abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0) tmem_alloc(&Y->tmem, kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = Y->tmem;
-    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);   // this warp's TMEM lanes
-    const int row = (warp & 3) * 32 + lane;                          // TMEM lane of this thread
-    const int chalf = warp >> 2;                                     // column half of an epilogue
-
     // W, S (checkpoint) and dWe, dSe (adjoint) rows 64 I .. 64 I + 63 of this
     // chunk into the matrix tiles (one thread)
     int halves_issued = 0;
@@ -251,9 +234,21 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         }
         ++halves_issued;
     };
+    // a full chunk whose gates start on a 16-byte boundary takes them with the
+    // tiles; otherwise threads load them
+    const bool gate_bulk = n == kC && (tok0 & 3) == 0;
     if (tid == 0) {
+        mbar_init(&Y->full, 1);
+        mbar_init(&Y->mma, 1);
+        mbar_init(&Y->mfull, 1);
+        Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
+        Y->abort = 0;
+        fence_mbar_init();
+        // every input copy starts before the tensor memory is allocated
         load_half(0);
-        mbar_expect_tx(&Y->full, 4 * NH * kTile + kCoefRecBytes);
+        const uint32_t gbytes =
+            gate_bulk ? kC * 4 * (1 + (a.eta ? 1 : 0) + (a.alpha ? 1 : 0)) : 0;
+        mbar_expect_tx(&Y->full, 4 * NH * kTile + kCoefRecBytes + gbytes);
         bulk_load(sm + L.crec, coef + ((size_t)seq * nch + c) * kCoefRecBytes, kCoefRecBytes,
                   &Y->full);
 #pragma unroll
@@ -263,15 +258,33 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             tma_load_3d(dztile(h), &zmap, &Y->full, 64 * h, c * kC, seq);
             tma_load_3d(vtile(h), &vmap, &Y->full, 64 * h, c * kC, seq);
         }
+        if (gate_bulk) {
+            bulk_load(th, a.theta + tok0, kC * 4, &Y->full);
+            if (a.eta) bulk_load(et, a.eta + tok0, kC * 4, &Y->full);
+            if (a.alpha) bulk_load(al, a.alpha + tok0, kC * 4, &Y->full);
+        }
     }
+    if (warp == 0) tmem_alloc(&Y->tmem, kTmemCols);
     if (tid < kC) {
-        th[tid] = tid < n ? a.theta[tok0 + tid] : 0.f;
-        et[tid] = (tid < n && a.eta) ? a.eta[tok0 + tid] : 0.f;
-        al[tid] = (tid < n && a.alpha) ? a.alpha[tok0 + tid] : 0.f;
+        if (!gate_bulk) {
+            th[tid] = tid < n ? a.theta[tok0 + tid] : 0.f;
+            et[tid] = (tid < n && a.eta) ? a.eta[tok0 + tid] : 0.f;
+            al[tid] = (tid < n && a.alpha) ? a.alpha[tok0 + tid] : 0.f;
+        } else {
+            if (!a.eta) et[tid] = 0.f;
+            if (!a.alpha) al[tid] = 0.f;
+        }
         dbeta[tid] = dcc[tid] = dclast[tid] = dpm[tid] = dkeep[tid] = deta[tid] = 0.f;
     }
     if (tid < 4) scal[tid] = 0.f;
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = Y->tmem;
+    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);   // this warp's TMEM lanes
+    const int row = (warp & 3) * 32 + lane;                          // TMEM lane of this thread
+    const int chalf = warp >> 2;                                     // column half of an epilogue
+
 
     uint32_t mma_phase = 0;
     bool ok = wait_bar(Y, &Y->full, 0, status);
@@ -647,8 +660,6 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     float* Ec = Kc + kC * kLdc;
     if (ok && warp < 2) {
         const int s = warp * 32 + lane;
-        const float e_lo = et[lane], e_hi = et[lane + 32];
-        const float a_lo = al[lane], a_hi = al[lane + 32];
         const float ths = th[s];
         // blocks of 8 rows: the block's loads, then its 8 dependent steps in
         // registers, then its stores (so no load waits behind a store)
@@ -656,14 +667,17 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 #pragma unroll
         for (int t0 = 0; t0 < kC; t0 += 8) {
             if (t0 < n) {
-                float dcb[8], wb[8], mb[8];
+                float dcb[8], wb[8], mb[8], eb[8], kb[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) dcb[u] = dC[(t0 + u) * kLdc + s];   // 0 past the chunk
+                for (int u = 0; u < 8; ++u) {
+                    dcb[u] = dC[(t0 + u) * kLdc + s];   // 0 past the chunk
+                    eb[u] = et[t0 + u];
+                    kb[u] = 1.f - al[t0 + u];
+                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int t = t0 + u;
-                    const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
-                    const float k1 = 1.f - __shfl_sync(0xffffffffu, t < 32 ? a_lo : a_hi, t & 31);
+                    const float e = eb[u], k1 = kb[u];
                     const float mn = t == s ? 1.f : e * m;     // stays 0 before the column starts
                     const float wn = t == s ? 1.f : fmaf(k1, w, mn);
                     const bool live = t < n;
@@ -686,7 +700,7 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 #pragma unroll
         for (int tb = kC - 1; tb >= 1; tb -= 8) {      // rows tb, tb-1, .., tb-7 (row 0 skipped)
             if (tb - 7 < n) {
-                float wm[8], mm[8], dc[8], kc[8], ec[8];
+                float wm[8], mm[8], dc[8], kc[8], ec[8], eb[8], kb[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int t = tb - u;
@@ -694,14 +708,15 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                         wm[u] = Wm[(t - 1) * kLdc + s];
                         mm[u] = Mm[(t - 1) * kLdc + s];
                         dc[u] = dC[(t - 1) * kLdc + s];
+                        eb[u] = et[t];
+                        kb[u] = 1.f - al[t];
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int t = tb - u;
                     if (t >= 1) {
-                        const float e = __shfl_sync(0xffffffffu, t < 32 ? e_lo : e_hi, t & 31);
-                        const float k1 = 1.f - __shfl_sync(0xffffffffu, t < 32 ? a_lo : a_hi, t & 31);
+                        const float e = eb[u], k1 = kb[u];
                         const bool act = t < n && t > s;
                         const float dm1 = dm + dw;
                         kc[u] = act ? dw * wm[u] : 0.f;
@@ -840,13 +855,29 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 //   de  = -2 (A~^T dZ + C_n o dWK + pm o dSK)         A~^T dZ             (MMA)
 //   dW <- beta_n dW + (Q^T (beta o dZ) + K^T de)^T,    (Q^T, K^T MN-major; MMA)
 //   dS <- c_n dW + P_n dS + (Q^T (c o dZ))^T
-// with thread j holding column j of the slice's 16 rows of dW and dS in fp32
-// registers and writing their bf16 copy for the next chunk's first product.
-// The next chunk's tiles and record load into the second of two stages while a
-// chunk computes.
+// A~^T dZ, Q^T (beta o dZ) and Q^T (c o dZ) depend on the inputs alone, so they
+// are computed one chunk ahead into alternating tensor-memory buffers; the
+// serial path per chunk is K [dW; dS]^T -> de -> K^T de -> the update.
+//
+// Roles (288 threads):
+//   warps 0-3  state: thread j holds column j of the slice's 16 rows of dW and
+//              dS in fp32 registers, applies the update and writes the bf16
+//              copy [dW; dS]^T for the next chunk's first product; warps 0-1
+//              (TMEM lanes 0-63 = tokens s) also form de.
+//   warps 4-7  the next chunk's dZ slice, beta dZ and c dZ tiles.
+//   warp 8     issues every MMA and the TMA loads (three input stages, two
+//              chunks ahead).
+// Hand-offs between roles are named barriers (state -> issuer: the adjoint
+// copy; de warps -> issuer: the de tile; tile warps -> issuer: the dZ tiles)
+// and MMA-completion mbarriers the other way.  Every wait on an mbarrier is
+// bounded; after a timeout every role runs out its loop doing no work, so the
+// named barriers stay balanced.
 
 constexpr int kSl = 16;                                          // rows of the slice
+constexpr int kNS = 3;                                           // input stages
+constexpr int kChainThreads = 288;
 constexpr uint32_t kVecSlot = (kCoefVecBytes + 63) / 64 * 64;
+constexpr uint32_t kBarWs = 1, kBarDe = 2, kBarTiles = 3;        // named barriers
 
 struct ChainLayout {
     uint32_t kq, at, dzs, vec, dzt, bzt, czt, det, ws, total;
@@ -856,14 +887,14 @@ __host__ __device__ constexpr ChainLayout chain_layout(int D) {
     ChainLayout L{};
     uint32_t o = 0;
     const uint32_t NH = D / 64;
-    L.kq = o;  o += 2 * NH * 2 * kTile;     // two stages of [K_h][Q_h]
-    L.at = o;  o += 2 * kTile;              // two stages of A~ [t][s] (swizzled, as stored)
-    L.dzs = o; o += 2 * kC * kSl * 2;       // two stages of the dZ slice (64 x 16 bf16)
-    L.vec = o; o += 2 * kVecSlot;           // two stages of the coefficient vectors
+    L.kq = o;  o += kNS * NH * 2 * kTile;   // stages of [K_h][Q_h]
+    L.at = o;  o += kNS * kTile;            // stages of A~ [t][s] (swizzled, as stored)
+    L.dzs = o; o += kNS * kC * kSl * 2;     // stages of the dZ slice (64 x 16 bf16)
+    L.vec = o; o += kNS * kVecSlot;         // stages of the coefficient vectors
     o = (o + 1023) / 1024 * 1024;
-    L.dzt = o; o += kTile;                  // dZ slice [t][i] (16 of 64 columns)
-    L.bzt = o; o += kTile;                  // beta_t dZ
-    L.czt = o; o += kTile;                  // c_t dZ
+    L.dzt = o; o += 2 * kTile;              // dZ slice [t][i] (16 of 64 columns), 2 buffers
+    L.bzt = o; o += 2 * kTile;              // beta_t dZ
+    L.czt = o; o += 2 * kTile;              // c_t dZ
     L.det = o; o += kTile;                  // de [s][i]
     L.ws = o;  o += (uint32_t)D * 128;      // [dW; dS]^T bf16 [j][i'] (32 of 64 columns)
     L.total = o + 64;                       // barriers
@@ -871,14 +902,14 @@ __host__ __device__ constexpr ChainLayout chain_layout(int D) {
 }
 
 struct ChainSync {
-    uint64_t full[2], mma;
+    uint64_t full[kNS], mma1, mma3;
     long long limit;
     int abort;
     uint32_t tmem;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kChainThreads, 1)
 bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap zmap, const BwdArgs a, float* ws,
                     size_t off_adj, const uint8_t* coef, const uint8_t* tiles, size_t off_part,
@@ -888,6 +919,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                                              ~uintptr_t(1023));
     constexpr ChainLayout L = chain_layout(D);
     constexpr int NH = D / 64, KS = D / 16;
+    static_assert(sizeof(ChainSync) <= 64, "chain barriers");
     ChainSync* Y = reinterpret_cast<ChainSync*>(sm + L.total - 64);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nsl = D / kSl;
@@ -896,21 +928,22 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     const size_t sd = (size_t)D * D;
     int* status = a.status;
 
-    auto kt = [&](int b, int h) { return sm + L.kq + (b * NH + h) * 2 * kTile; };
-    auto qt = [&](int b, int h) { return kt(b, h) + kTile; };
-    auto atb = [&](int b) { return sm + L.at + b * kTile; };
-    auto dzs = [&](int b) { return sm + L.dzs + b * kC * kSl * 2; };
-    auto vecb = [&](int b) { return reinterpret_cast<float*>(sm + L.vec + b * kVecSlot); };
-    uint8_t* dzt = sm + L.dzt;
-    uint8_t* bzt = sm + L.bzt;
-    uint8_t* czt = sm + L.czt;
+    auto kt = [&](int st, int h) { return sm + L.kq + (st * NH + h) * 2 * kTile; };
+    auto qt = [&](int st, int h) { return kt(st, h) + kTile; };
+    auto atb = [&](int st) { return sm + L.at + st * kTile; };
+    auto dzs = [&](int st) { return sm + L.dzs + st * kC * kSl * 2; };
+    auto vecb = [&](int st) { return reinterpret_cast<const float*>(sm + L.vec + st * kVecSlot); };
+    auto dzt = [&](int b) { return sm + L.dzt + b * kTile; };
+    auto bzt = [&](int b) { return sm + L.bzt + b * kTile; };
+    auto czt = [&](int b) { return sm + L.czt + b * kTile; };
     uint8_t* det = sm + L.det;
     uint8_t* wsm = sm + L.ws;
+    auto chunk_len = [&](int k) { return min(kC, T - (nch - 1 - k) * kC); };
 
     if (tid == 0) {
-        mbar_init(&Y->full[0], 1);
-        mbar_init(&Y->full[1], 1);
-        mbar_init(&Y->mma, 1);
+        for (int st = 0; st < kNS; ++st) mbar_init(&Y->full[st], 1);
+        mbar_init(&Y->mma1, 1);
+        mbar_init(&Y->mma3, 1);
         Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
         Y->abort = 0;
         fence_mbar_init();
@@ -920,210 +953,267 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = Y->tmem;
-    const uint32_t tl = tmem + ((uint32_t)(warp & 3) * 32 << 16);
-    constexpr uint32_t kAc1 = 0, kAc2 = 32, kAc3 = 64;
-
-    auto issue_loads = [&](int c, int b) {
-        mbar_expect_tx(&Y->full[b], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            tma_load_3d(kt(b, h), &kmap, &Y->full[b], 64 * h, c * kC, seq);
-            tma_load_3d(qt(b, h), &qmap, &Y->full[b], 64 * h, c * kC, seq);
-        }
-        tma_load_3d(dzs(b), &zmap, &Y->full[b], r0, c * kC, seq);
-        const size_t rec = (size_t)seq * nch + c;
-        bulk_load(atb(b), tiles + rec * kTile, kTile, &Y->full[b]);
-        bulk_load(vecb(b), coef + rec * kCoefRecBytes + kCoefVec, kCoefVecBytes, &Y->full[b]);
-    };
-    if (tid == 0 && nch > 0) issue_loads(nch - 1, 0);
-
-    // the slice's adjoint rows, column j per thread (the final state's adjoint)
-    const int j = tid;
-    const bool own = j < D;
-    float dw[kSl], dsv[kSl];
-#pragma unroll
-    for (int i = 0; i < kSl; ++i) {
-        const size_t g = (size_t)seq * sd + (size_t)(r0 + i) * D + j;
-        dw[i] = (own && a.dW) ? a.dW[g] : 0.f;
-        dsv[i] = (own && a.dS) ? a.dS[g] : 0.f;
-    }
-    auto write_ws = [&]() {
-        if (!own) return;
-        *reinterpret_cast<uint4*>(wsm + swz(j, 0)) = pack8(dw);
-        *reinterpret_cast<uint4*>(wsm + swz(j, 1)) = pack8(dw + 8);
-        *reinterpret_cast<uint4*>(wsm + swz(j, 2)) = pack8(dsv);
-        *reinterpret_cast<uint4*>(wsm + swz(j, 3)) = pack8(dsv + 8);
-    };
-    write_ws();
-
-    constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // [K; Q] [dW; dS]^T
-    constexpr uint32_t id16 = idesc_bf16_f32(128, 16, 1, 1);  // MN-major A and B, N = 16
-    uint32_t mma_phase = 0;
+    // TMEM columns: [K; Q][dW; dS]^T, then A~^T dZ and the Q^T . dZ pair per buffer
+    constexpr uint32_t kAc1 = 0;
+    auto kAc2 = [](int b) { return 32u + 16u * (uint32_t)b; };
+    auto kAc3 = [](int b) { return 64u + 32u * (uint32_t)b; };
     bool ok = true;
-    for (int k = 0; k < nch; ++k) {
-        const int c = nch - 1 - k, b = k & 1;
-        const int n = min(kC, T - c * kC);
-        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[b], (k >> 1) & 1, status);
-        // the next chunk's inputs into the other stage (its last use is complete)
-        if (tid == 0 && ok && c > 0) issue_loads(c - 1, b ^ 1);
-        const float* vbeta = vecb(b) + kCoefBeta / 4;
-        const float* vc = vecb(b) + kCoefC / 4;
-        const float* vclast = vecb(b) + kCoefCend / 4;
-        const float* vpm = vecb(b) + kCoefPend / 4;
-        const float* vscal = vecb(b) + kCoefScal / 4;   // beta_n, c_n, P_n, n
-        // this chunk's end adjoint, for the local pass
-        if (own && ok) {
-            __nv_bfloat16* adj = reinterpret_cast<__nv_bfloat16*>(ws + off_adj) +
-                                 ((size_t)seq * nch + c) * 2 * sd;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ state
+        const uint32_t tl = tmem + ((uint32_t)warp * 32 << 16);
+        const int j = tid;
+        const bool own = j < D;
+        float dw[kSl], dsv[kSl];
 #pragma unroll
-            for (int i = 0; i < kSl; ++i) {
-                adj[(size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dw[i]);
-                adj[sd + (size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dsv[i]);
+        for (int i = 0; i < kSl; ++i) {
+            const size_t g = (size_t)seq * sd + (size_t)(r0 + i) * D + j;
+            dw[i] = (own && a.dW) ? a.dW[g] : 0.f;
+            dsv[i] = (own && a.dS) ? a.dS[g] : 0.f;
+        }
+        auto write_ws = [&]() {
+            if (!own) return;
+            *reinterpret_cast<uint4*>(wsm + swz(j, 0)) = pack8(dw);
+            *reinterpret_cast<uint4*>(wsm + swz(j, 1)) = pack8(dw + 8);
+            *reinterpret_cast<uint4*>(wsm + swz(j, 2)) = pack8(dsv);
+            *reinterpret_cast<uint4*>(wsm + swz(j, 3)) = pack8(dsv + 8);
+        };
+        write_ws();
+        fence_proxy_async_smem();
+        named_bar_arrive(kBarWs, 160);
+        for (int k = 0; k < nch; ++k) {
+            const int c = nch - 1 - k, st = k % kNS, b = k & 1;
+            const int n = chunk_len(k);
+            const float* vclast = vecb(st) + kCoefCend / 4;
+            const float* vpm = vecb(st) + kCoefPend / 4;
+            const float* vscal = vecb(st) + kCoefScal / 4;   // beta_n, c_n, P_n, n
+            // the chunk's coefficient vectors have landed (long since, as a rule)
+            if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st], (k / kNS) & 1, status);
+            // this chunk's end adjoint, for the local pass
+            if (own && ok) {
+                __nv_bfloat16* adj = reinterpret_cast<__nv_bfloat16*>(ws + off_adj) +
+                                     ((size_t)seq * nch + c) * 2 * sd;
+#pragma unroll
+                for (int i = 0; i < kSl; ++i) {
+                    adj[(size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dw[i]);
+                    adj[sd + (size_t)(r0 + i) * D + j] = __float2bfloat16_rn(dsv[i]);
+                }
+            }
+            if (warp < 2) {
+                // de[s][i] = -2 ((A~^T dZ)[s][i] + C_n[s] dWK + pm[s] dSK), s < n
+                if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma1, k & 1, status);
+                if (ok) {
+                    tc_fence_after();
+                    const int sidx = j;
+                    float gw[16], gs[16], ad[16], de[16];
+                    tmem_ld16(tl + kAc1, gw);
+                    tmem_ld16(tl + kAc1 + 16, gs);
+                    tmem_ld16(tl + kAc2(b), ad);
+                    tmem_wait_ld();
+                    const float cl = vclast[sidx], pmv = vpm[sidx];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        de[e] = sidx < n ? -2.f * (ad[e] + cl * gw[e] + pmv * gs[e]) : 0.f;
+                    *reinterpret_cast<uint4*>(det + swz(sidx, 0)) = pack8(de);
+                    *reinterpret_cast<uint4*>(det + swz(sidx, 1)) = pack8(de + 8);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_arrive(kBarDe, 96);
+            }
+            // dW <- beta_n dW + .,  dS <- c_n dW + P_n dS + .  (column j)
+            if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma3, k & 1, status);
+            if (ok) {
+                tc_fence_after();
+                float uw[16], us[16];
+                tmem_ld16(tl + kAc3(b), uw);
+                tmem_ld16(tl + kAc3(b) + 16, us);
+                tmem_wait_ld();
+                const float bn = vscal[0], cn = vscal[1], Pn = vscal[2];
+                if (own) {
+#pragma unroll
+                    for (int i = 0; i < kSl; ++i) {
+                        const float w = dw[i];
+                        dw[i] = fmaf(bn, w, uw[i]);
+                        dsv[i] = fmaf(cn, w, fmaf(Pn, dsv[i], us[i]));
+                    }
+                }
+                write_ws();
+            }
+            if (k + 1 < nch) {
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_arrive(kBarWs, 160);
             }
         }
-        if (ok) {
-            // the dZ slice, beta dZ, c dZ as 16-column tiles [t][i]
-            for (int x = tid; x < kC * 2; x += kThreads) {
-                const int t = x >> 1, c8 = x & 1;
+        // adjoint of the initial state: per sequence, or a per-sequence partial
+        // that a reduction sums over the batch when W0 / S0 are shared
+        if (own && ok) {
+            float* oW;
+            float* oS;
+            size_t base;
+            if (a.shared) {
+                oW = ws + off_part;
+                oS = oW + sd;
+                base = (size_t)seq * 2 * sd;
+            } else {
+                oW = a.dW0;
+                oS = a.dS0;
+                base = (size_t)seq * sd;
+            }
+#pragma unroll
+            for (int i = 0; i < kSl; ++i) {
+                const size_t g = base + (size_t)(r0 + i) * D + j;
+                oW[g] = dw[i];
+                if (oS) oS[g] = dsv[i];
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ tiles
+        const int p = tid - 128;
+        for (int k = 0; k < nch; ++k) {
+            const int st = k % kNS, b = k & 1;
+            const int n = chunk_len(k);
+            // buffer b was last read by the chunk k-2 products, which complete
+            // before the first product of chunk k-1
+            if (k >= 1 && ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma1, (k - 1) & 1, status);
+            if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st], (k / kNS) & 1, status);
+            if (ok) {
+                const float* vbeta = vecb(st) + kCoefBeta / 4;
+                const float* vc = vecb(st) + kCoefC / 4;
+                const int t = p >> 1, c8 = p & 1;     // 64 tokens x 2 eight-column groups
                 float z[8], zb[8], zc[8];
-                unpack8(*reinterpret_cast<const uint4*>(dzs(b) + t * kSl * 2 + 16 * c8), z);
+                unpack8(*reinterpret_cast<const uint4*>(dzs(st) + t * kSl * 2 + 16 * c8), z);
                 const float bt = t < n ? vbeta[t] : 0.f, ct = t < n ? vc[t] : 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     zb[e] = bt * z[e];
                     zc[e] = ct * z[e];
                 }
-                *reinterpret_cast<uint4*>(dzt + swz(t, c8)) = pack8(z);
-                *reinterpret_cast<uint4*>(bzt + swz(t, c8)) = pack8(zb);
-                *reinterpret_cast<uint4*>(czt + swz(t, c8)) = pack8(zc);
+                *reinterpret_cast<uint4*>(dzt(b) + swz(t, c8)) = pack8(z);
+                *reinterpret_cast<uint4*>(bzt(b) + swz(t, c8)) = pack8(zb);
+                *reinterpret_cast<uint4*>(czt(b) + swz(t, c8)) = pack8(zc);
             }
+            fence_proxy_async_smem();
+            named_bar_arrive(kBarTiles, 160);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK) and A~^T dZ (lanes 0-63)
-        if (warp == 0 && ok) {
+    } else {
+        // ----------------------------------------------------------- issuer
+        auto issue_loads = [&](int k) {
+            const int c = nch - 1 - k, st = k % kNS;
+            mbar_expect_tx(&Y->full[st], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                tma_load_3d(kt(st, h), &kmap, &Y->full[st], 64 * h, c * kC, seq);
+                tma_load_3d(qt(st, h), &qmap, &Y->full[st], 64 * h, c * kC, seq);
+            }
+            tma_load_3d(dzs(st), &zmap, &Y->full[st], r0, c * kC, seq);
+            const size_t rec = (size_t)seq * nch + c;
+            bulk_load(atb(st), tiles + rec * kTile, kTile, &Y->full[st]);
+            bulk_load(sm + L.vec + st * kVecSlot, coef + rec * kCoefRecBytes + kCoefVec,
+                      kCoefVecBytes, &Y->full[st]);
+        };
+        constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // [K; Q] [dW; dS]^T
+        constexpr uint32_t id16 = idesc_bf16_f32(128, 16, 1, 1);  // MN-major A and B, N = 16
+        // the products of chunk k that need its inputs only
+        auto issue_pre = [&](int k) {
+            const int st = k % kNS, b = k & 1;
             tc_fence_after();
             if (elect_one()) {
-                const uint32_t wsa = smem_u32(wsm);
-#pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    const uint32_t abase = smem_u32(kt(b, kk >> 2)) + (kk & 3) * 32;
-                    mma_bf16(tmem + kAc1, sdesc(abase, 16, 1024, 2), sdesc(wsa + kk * 2048, 8192, 1024, 2),
-                             id1, kk > 0);
-                }
-                const uint32_t aa = smem_u32(atb(b)), za = smem_u32(dzt);
+                const uint32_t aa = smem_u32(atb(st)), za = smem_u32(dzt(b));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc2, sdesc(aa + kk * 2048, kTile, 1024, 2),
+                    mma_bf16(tmem + kAc2(b), sdesc(aa + kk * 2048, kTile, 1024, 2),
                              sdesc(za + kk * 2048, kTile, 1024, 2), id16, kk > 0);
-                mma_commit(&Y->mma);
-            }
-            __syncwarp();
-        }
-        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma, mma_phase++ & 1, status);
-        if (ok && warp < 2) {
-            // de[s][i] = -2 ((A~^T dZ)[s][i] + C_n[s] dWK + pm[s] dSK), s < n
-            tc_fence_after();
-            const int sidx = warp * 32 + lane;
-            float gw[16], gs[16], ad[16], de[16];
-            tmem_ld16(tl + kAc1, gw);
-            tmem_ld16(tl + kAc1 + 16, gs);
-            tmem_ld16(tl + kAc2, ad);
-            tmem_wait_ld();
-            const float cl = vclast[sidx], pmv = vpm[sidx];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                de[e] = sidx < n ? -2.f * (ad[e] + cl * gw[e] + pmv * gs[e]) : 0.f;
-            *reinterpret_cast<uint4*>(det + swz(sidx, 0)) = pack8(de);
-            *reinterpret_cast<uint4*>(det + swz(sidx, 1)) = pack8(de + 8);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // (Q^T (beta dZ) + K^T de) and Q^T (c dZ), rows = key index j
-        if (warp == 0 && ok) {
-            tc_fence_after();
-            if (elect_one()) {
-                const uint32_t qa = smem_u32(qt(b, 0)), ka = smem_u32(kt(b, 0));
-                const uint32_t bzb = smem_u32(bzt), czb = smem_u32(czt), deb = smem_u32(det);
+                const uint32_t qa = smem_u32(qt(st, 0));
+                const uint32_t bzb = smem_u32(bzt(b)), czb = smem_u32(czt(b));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc3, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
+                    mma_bf16(tmem + kAc3(b), sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
                              sdesc(bzb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc3, sdesc(ka + kk * 2048, 2 * kTile, 1024, 2),
-                             sdesc(deb + kk * 2048, kTile, 1024, 2), id16, 1u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc3 + 16, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
+                    mma_bf16(tmem + kAc3(b) + 16, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
                              sdesc(czb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
-                mma_commit(&Y->mma);
             }
             __syncwarp();
+        };
+        auto live = [&]() { return ok && !*(volatile int*)&Y->abort; };
+        int issued = 0, n3 = 0;   // chunks whose loads were issued; commits to mma3
+        if (lane == 0) {
+            for (int k = 0; k < min(2, nch); ++k) issue_loads(k);
         }
-        if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma, mma_phase++ & 1, status);
-        if (ok && warp < 4) {
-            // dW <- beta_n dW + .,  dS <- c_n dW + P_n dS + .  (column j)
-            tc_fence_after();
-            float uw[16], us[16];
-            tmem_ld16(tl + kAc3, uw);
-            tmem_ld16(tl + kAc3 + 16, us);
-            tmem_wait_ld();
-            const float bn = vscal[0], cn = vscal[1], Pn = vscal[2];
-            if (own) {
+        issued = min(2, nch);
+        named_bar_sync(kBarTiles, 160);
+        if (live()) ok = wait_flag(&Y->abort, Y->limit, &Y->full[0], 0, status);
+        if (live()) issue_pre(0);
+        for (int k = 0; k < nch; ++k) {
+            const int st = k % kNS, b = k & 1;
+            named_bar_sync(kBarWs, 160);
+            ok = live();
+            if (ok && k + 2 < nch) {
+                if (lane == 0) issue_loads(k + 2);
+                issued = k + 3;
+            }
+            // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK)
+            if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st], (k / kNS) & 1, status);
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t wsa = smem_u32(wsm);
 #pragma unroll
-                for (int i = 0; i < kSl; ++i) {
-                    const float w = dw[i];
-                    dw[i] = fmaf(bn, w, uw[i]);
-                    dsv[i] = fmaf(cn, w, fmaf(Pn, dsv[i], us[i]));
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint32_t abase = smem_u32(kt(st, kk >> 2)) + (kk & 3) * 32;
+                        mma_bf16(tmem + kAc1, sdesc(abase, 16, 1024, 2),
+                                 sdesc(wsa + kk * 2048, 8192, 1024, 2), id1, kk > 0);
+                    }
+                    mma_commit(&Y->mma1);
+                }
+                __syncwarp();
+            }
+            named_bar_sync(kBarDe, 96);
+            ok = live();
+            // + K^T de onto Q^T (beta dZ)
+            if (ok) {
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t ka = smem_u32(kt(st, 0)), deb = smem_u32(det);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + kAc3(b), sdesc(ka + kk * 2048, 2 * kTile, 1024, 2),
+                                 sdesc(deb + kk * 2048, kTile, 1024, 2), id16, 1u);
+                    mma_commit(&Y->mma3);
+                }
+                __syncwarp();
+                ++n3;
+            }
+            if (k + 1 < nch) {
+                named_bar_sync(kBarTiles, 160);
+                ok = live();
+                const int st1 = (k + 1) % kNS;
+                if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st1], ((k + 1) / kNS) & 1, status);
+                if (ok) issue_pre(k + 1);
+            }
+        }
+        // copies in flight and every MMA complete before shared and tensor
+        // memory go
+        if (lane == 0) {
+            for (int k = max(0, issued - kNS); k < issued; ++k) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&Y->full[k % kNS], (k / kNS) & 1) && clock64() - t0 < Y->limit) {
                 }
             }
-            write_ws();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-    }
-    // adjoint of the initial state: per sequence, or a per-sequence partial that
-    // a reduction sums over the batch when W0 / S0 are shared
-    if (own && ok) {
-        float* oW;
-        float* oS;
-        size_t base;
-        if (a.shared) {
-            oW = ws + off_part;
-            oS = oW + sd;
-            base = (size_t)seq * 2 * sd;
-        } else {
-            oW = a.dW0;
-            oS = a.dS0;
-            base = (size_t)seq * sd;
-        }
-#pragma unroll
-        for (int i = 0; i < kSl; ++i) {
-            const size_t g = base + (size_t)(r0 + i) * D + j;
-            oW[g] = dw[i];
-            if (oS) oS[g] = dsv[i];
-        }
-    }
-    if (tid == 0 && !ok) {
-        // copies in flight before the kernel's shared memory goes
-        for (int bb = 0; bb < 2; ++bb) {
-            const long long t0 = clock64();
-            while (clock64() - t0 < Y->limit && !mbar_try_wait(&Y->full[bb], 0) &&
-                   !mbar_try_wait(&Y->full[bb], 1)) {
-            }
-        }
-    }
-    if (warp == 0) {
-        if (elect_one()) mma_commit(&Y->mma);
         __syncwarp();
-        const long long t0 = clock64();
-        if (lane == 0)
-            while (!mbar_try_wait(&Y->mma, mma_phase & 1) && clock64() - t0 < Y->limit) {
+        // one more commit on mma3 completes its phase n3 once every MMA this
+        // thread issued has completed
+        if (elect_one()) mma_commit(&Y->mma3);
+        __syncwarp();
+        if (lane == 0) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&Y->mma3, n3 & 1) && clock64() - t0 < Y->limit) {
             }
+        }
         __syncwarp();
     }
     tc_fence_before();
@@ -1156,7 +1246,7 @@ cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, con
         cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<128>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_chain_tc_kernel<128><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
+        bwd_chain_tc_kernel<128><<<grid, kChainThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
                                                               static_cast<const uint8_t*>(coef),
                                                               static_cast<const uint8_t*>(tiles),
                                                               off_part, nch);
@@ -1165,7 +1255,7 @@ cudaError_t bwd_chain_tc_launch(const BwdArgs& a, float* ws, size_t off_adj, con
         cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc_kernel<64>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        bwd_chain_tc_kernel<64><<<grid, kThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
+        bwd_chain_tc_kernel<64><<<grid, kChainThreads, smem, s>>>(qm, km, zm, a, ws, off_adj,
                                                              static_cast<const uint8_t*>(coef),
                                                              static_cast<const uint8_t*>(tiles),
                                                              off_part, nch);
