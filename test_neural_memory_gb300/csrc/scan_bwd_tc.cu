@@ -855,32 +855,37 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 //   de  = -2 (A~^T dZ + C_n o dWK + pm o dSK)         A~^T dZ             (MMA)
 //   dW <- beta_n dW + (Q^T (beta o dZ) + K^T de)^T,    (Q^T, K^T MN-major; MMA)
 //   dS <- c_n dW + P_n dS + (Q^T (c o dZ))^T
-// A~^T dZ, Q^T (beta o dZ) and Q^T (c o dZ) depend on the inputs alone, so they
-// are computed one chunk ahead into alternating tensor-memory buffers; the
-// serial path per chunk is K [dW; dS]^T -> de -> K^T de -> the update.
+// A~^T dZ and Q^T [beta o dZ | c o dZ] depend on the inputs alone, so they are
+// computed one chunk ahead into alternating tensor-memory buffers; the serial
+// path per chunk is K [dW; dS]^T -> de -> K^T de -> the update.  These thin
+// products run at about a hundred cycles per 16-deep MMA step whatever their
+// width, so the chunk's step count (8 + 4 + 4 + 4) sets its time.
 //
-// Roles (288 threads):
+// Roles (320 threads):
 //   warps 0-3  state: thread j holds column j of the slice's 16 rows of dW and
 //              dS in fp32 registers, applies the update and writes the bf16
 //              copy [dW; dS]^T for the next chunk's first product; warps 0-1
 //              (TMEM lanes 0-63 = tokens s) also form de.
-//   warps 4-7  the next chunk's dZ slice, beta dZ and c dZ tiles.
-//   warp 8     issues every MMA and the TMA loads (three input stages, two
-//              chunks ahead).
+//   warps 4-7  the next chunk's dZ slice and [beta dZ | c dZ] tiles.
+//   warp 8     issues every MMA, ordered so that the input-only products of
+//              a chunk run while the state warps work on the previous one.
+//   warp 9     TMA loads into three input stages: a stage is refilled three
+//              chunks ahead once the state warps release it after its update.
 // Hand-offs between roles are named barriers (state -> issuer: the adjoint
 // copy; de warps -> issuer: the de tile; tile warps -> issuer: the dZ tiles)
-// and MMA-completion mbarriers the other way.  Every wait on an mbarrier is
+// and MMA-completion mbarriers the other way; stage release and refill are
+// mbarriers.  Every wait on an mbarrier is
 // bounded; after a timeout every role runs out its loop doing no work, so the
 // named barriers stay balanced.
 
 constexpr int kSl = 16;                                          // rows of the slice
 constexpr int kNS = 3;                                           // input stages
-constexpr int kChainThreads = 288;
+constexpr int kChainThreads = 320;
 constexpr uint32_t kVecSlot = (kCoefVecBytes + 63) / 64 * 64;
 constexpr uint32_t kBarWs = 1, kBarDe = 2, kBarTiles = 3;        // named barriers
 
 struct ChainLayout {
-    uint32_t kq, at, dzs, vec, dzt, bzt, czt, det, ws, total;
+    uint32_t kq, at, dzs, vec, dzt, bct, det, ws, total;
 };
 
 __host__ __device__ constexpr ChainLayout chain_layout(int D) {
@@ -893,16 +898,15 @@ __host__ __device__ constexpr ChainLayout chain_layout(int D) {
     L.vec = o; o += kNS * kVecSlot;         // stages of the coefficient vectors
     o = (o + 1023) / 1024 * 1024;
     L.dzt = o; o += 2 * kTile;              // dZ slice [t][i] (16 of 64 columns), 2 buffers
-    L.bzt = o; o += 2 * kTile;              // beta_t dZ
-    L.czt = o; o += 2 * kTile;              // c_t dZ
+    L.bct = o; o += 2 * kTile;              // [beta_t dZ | c_t dZ] [t][32 columns], 2 buffers
     L.det = o; o += kTile;                  // de [s][i]
     L.ws = o;  o += (uint32_t)D * 128;      // [dW; dS]^T bf16 [j][i'] (32 of 64 columns)
-    L.total = o + 64;                       // barriers
+    L.total = o + 128;                      // barriers
     return L;
 }
 
 struct ChainSync {
-    uint64_t full[kNS], mma1, mma3;
+    uint64_t full[kNS], sfree[kNS], mma1, mma3;
     long long limit;
     int abort;
     uint32_t tmem;
@@ -919,8 +923,8 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                                              ~uintptr_t(1023));
     constexpr ChainLayout L = chain_layout(D);
     constexpr int NH = D / 64, KS = D / 16;
-    static_assert(sizeof(ChainSync) <= 64, "chain barriers");
-    ChainSync* Y = reinterpret_cast<ChainSync*>(sm + L.total - 64);
+    static_assert(sizeof(ChainSync) <= 128, "chain barriers");
+    ChainSync* Y = reinterpret_cast<ChainSync*>(sm + L.total - 128);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nsl = D / kSl;
     const int seq = blockIdx.x / nsl, r0 = (blockIdx.x % nsl) * kSl;
@@ -934,14 +938,16 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     auto dzs = [&](int st) { return sm + L.dzs + st * kC * kSl * 2; };
     auto vecb = [&](int st) { return reinterpret_cast<const float*>(sm + L.vec + st * kVecSlot); };
     auto dzt = [&](int b) { return sm + L.dzt + b * kTile; };
-    auto bzt = [&](int b) { return sm + L.bzt + b * kTile; };
-    auto czt = [&](int b) { return sm + L.czt + b * kTile; };
+    auto bct = [&](int b) { return sm + L.bct + b * kTile; };
     uint8_t* det = sm + L.det;
     uint8_t* wsm = sm + L.ws;
     auto chunk_len = [&](int k) { return min(kC, T - (nch - 1 - k) * kC); };
 
     if (tid == 0) {
-        for (int st = 0; st < kNS; ++st) mbar_init(&Y->full[st], 1);
+        for (int st = 0; st < kNS; ++st) {
+            mbar_init(&Y->full[st], 1);
+            mbar_init(&Y->sfree[st], 4);   // one arrival per state warp
+        }
         mbar_init(&Y->mma1, 1);
         mbar_init(&Y->mma3, 1);
         Y->limit = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
@@ -1045,6 +1051,9 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 tc_fence_before();
                 named_bar_arrive(kBarWs, 160);
             }
+            // this warp is done with the chunk's stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&Y->sfree[st]);
         }
         // adjoint of the initial state: per sequence, or a per-sequence partial
         // that a reduction sums over the batch when W0 / S0 are shared
@@ -1091,32 +1100,20 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                     zc[e] = ct * z[e];
                 }
                 *reinterpret_cast<uint4*>(dzt(b) + swz(t, c8)) = pack8(z);
-                *reinterpret_cast<uint4*>(bzt(b) + swz(t, c8)) = pack8(zb);
-                *reinterpret_cast<uint4*>(czt(b) + swz(t, c8)) = pack8(zc);
+                *reinterpret_cast<uint4*>(bct(b) + swz(t, c8)) = pack8(zb);
+                *reinterpret_cast<uint4*>(bct(b) + swz(t, 2 + c8)) = pack8(zc);
             }
             fence_proxy_async_smem();
             named_bar_arrive(kBarTiles, 160);
         }
-    } else {
+    } else if (warp == 8) {
         // ----------------------------------------------------------- issuer
-        auto issue_loads = [&](int k) {
-            const int c = nch - 1 - k, st = k % kNS;
-            mbar_expect_tx(&Y->full[st], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                tma_load_3d(kt(st, h), &kmap, &Y->full[st], 64 * h, c * kC, seq);
-                tma_load_3d(qt(st, h), &qmap, &Y->full[st], 64 * h, c * kC, seq);
-            }
-            tma_load_3d(dzs(st), &zmap, &Y->full[st], r0, c * kC, seq);
-            const size_t rec = (size_t)seq * nch + c;
-            bulk_load(atb(st), tiles + rec * kTile, kTile, &Y->full[st]);
-            bulk_load(sm + L.vec + st * kVecSlot, coef + rec * kCoefRecBytes + kCoefVec,
-                      kCoefVecBytes, &Y->full[st]);
-        };
         constexpr uint32_t id1 = idesc_bf16_f32(128, 32, 0, 1);   // [K; Q] [dW; dS]^T
         constexpr uint32_t id16 = idesc_bf16_f32(128, 16, 1, 1);  // MN-major A and B, N = 16
-        // the products of chunk k that need its inputs only
-        auto issue_pre = [&](int k) {
+        constexpr uint32_t id32 = idesc_bf16_f32(128, 32, 1, 1);  // MN-major A and B, N = 32
+        auto live = [&]() { return ok && !*(volatile int*)&Y->abort; };
+        // A~^T dZ of chunk k (for its de)
+        auto issue_scores = [&](int k) {
             const int st = k % kNS, b = k & 1;
             tc_fence_after();
             if (elect_one()) {
@@ -1125,41 +1122,22 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + kAc2(b), sdesc(aa + kk * 2048, kTile, 1024, 2),
                              sdesc(za + kk * 2048, kTile, 1024, 2), id16, kk > 0);
-                const uint32_t qa = smem_u32(qt(st, 0));
-                const uint32_t bzb = smem_u32(bzt(b)), czb = smem_u32(czt(b));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc3(b), sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
-                             sdesc(bzb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + kAc3(b) + 16, sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
-                             sdesc(czb + kk * 2048, kTile, 1024, 2), id16, kk > 0);
             }
             __syncwarp();
         };
-        auto live = [&]() { return ok && !*(volatile int*)&Y->abort; };
-        int issued = 0, n3 = 0;   // chunks whose loads were issued; commits to mma3
-        if (lane == 0) {
-            for (int k = 0; k < min(2, nch); ++k) issue_loads(k);
-        }
-        issued = min(2, nch);
+        int n3 = 0;   // commits to mma3
         named_bar_sync(kBarTiles, 160);
         if (live()) ok = wait_flag(&Y->abort, Y->limit, &Y->full[0], 0, status);
-        if (live()) issue_pre(0);
+        if (live()) issue_scores(0);
         for (int k = 0; k < nch; ++k) {
             const int st = k % kNS, b = k & 1;
             named_bar_sync(kBarWs, 160);
             ok = live();
-            if (ok && k + 2 < nch) {
-                if (lane == 0) issue_loads(k + 2);
-                issued = k + 3;
-            }
-            // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK)
             if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st], (k / kNS) & 1, status);
             if (ok) {
                 tc_fence_after();
                 if (elect_one()) {
+                    // [K; Q] [dW; dS]^T (lanes 0-63: dWK, dSK)
                     const uint32_t wsa = smem_u32(wsm);
 #pragma unroll
                     for (int kk = 0; kk < KS; ++kk) {
@@ -1168,6 +1146,12 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                                  sdesc(wsa + kk * 2048, 8192, 1024, 2), id1, kk > 0);
                     }
                     mma_commit(&Y->mma1);
+                    // Q^T [beta dZ | c dZ], while the de warps work
+                    const uint32_t qa = smem_u32(qt(st, 0)), bcb = smem_u32(bct(b));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + kAc3(b), sdesc(qa + kk * 2048, 2 * kTile, 1024, 2),
+                                 sdesc(bcb + kk * 2048, kTile, 1024, 2), id32, kk > 0);
                 }
                 __syncwarp();
             }
@@ -1188,30 +1172,58 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 ++n3;
             }
             if (k + 1 < nch) {
+                // the next chunk's scores, while the state warps update
                 named_bar_sync(kBarTiles, 160);
                 ok = live();
                 const int st1 = (k + 1) % kNS;
                 if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->full[st1], ((k + 1) / kNS) & 1, status);
-                if (ok) issue_pre(k + 1);
+                if (ok) issue_scores(k + 1);
             }
         }
-        // copies in flight and every MMA complete before shared and tensor
-        // memory go
-        if (lane == 0) {
-            for (int k = max(0, issued - kNS); k < issued; ++k) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(&Y->full[k % kNS], (k / kNS) & 1) && clock64() - t0 < Y->limit) {
-                }
-            }
-        }
-        __syncwarp();
         // one more commit on mma3 completes its phase n3 once every MMA this
-        // thread issued has completed
+        // thread issued has completed (before tensor memory goes)
         if (elect_one()) mma_commit(&Y->mma3);
         __syncwarp();
         if (lane == 0) {
             const long long t0 = clock64();
             while (!mbar_try_wait(&Y->mma3, n3 & 1) && clock64() - t0 < Y->limit) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ----------------------------------------------------------- loader
+        auto issue_loads = [&](int k) {
+            const int c = nch - 1 - k, st = k % kNS;
+            mbar_expect_tx(&Y->full[st], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                tma_load_3d(kt(st, h), &kmap, &Y->full[st], 64 * h, c * kC, seq);
+                tma_load_3d(qt(st, h), &qmap, &Y->full[st], 64 * h, c * kC, seq);
+            }
+            tma_load_3d(dzs(st), &zmap, &Y->full[st], r0, c * kC, seq);
+            const size_t rec = (size_t)seq * nch + c;
+            bulk_load(atb(st), tiles + rec * kTile, kTile, &Y->full[st]);
+            bulk_load(sm + L.vec + st * kVecSlot, coef + rec * kCoefRecBytes + kCoefVec,
+                      kCoefVecBytes, &Y->full[st]);
+        };
+        int issued = min(kNS, nch);
+        if (lane == 0)
+            for (int k = 0; k < issued; ++k) issue_loads(k);
+        __syncwarp();
+        for (int k = 0; k + kNS < nch; ++k) {
+            // chunk k's stage, once the state warps have updated with it
+            if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->sfree[k % kNS], (k / kNS) & 1, status);
+            if (!ok) break;
+            if (lane == 0) issue_loads(k + kNS);
+            __syncwarp();
+            issued = k + kNS + 1;
+        }
+        // every copy lands before shared memory goes
+        if (lane == 0) {
+            for (int k = max(0, issued - kNS); k < issued; ++k) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&Y->full[k % kNS], (k / kNS) & 1) && clock64() - t0 < Y->limit) {
+                }
             }
         }
         __syncwarp();
