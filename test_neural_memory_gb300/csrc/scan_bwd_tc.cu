@@ -598,68 +598,86 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // dQ^T += K^T (-2 G)^T;  dK^T += Q^T (-2 G)
-    if (warp == 0 && ok) {
-        tc_fence_after();
-        if (elect_one()) {
-            const uint32_t kb = smem_u32(ktile(0)), qb = smem_u32(qtile(0)), gb = smem_u32(gg);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16(tmem + kDQ, sdesc(kb + kk * 2048, 2 * kTile, 1024, 2),
-                         sdesc(gb + kk * 32, 16, 1024, 2), idMK, 1u);
-                mma_bf16(tmem + kDK, sdesc(qb + kk * 2048, 2 * kTile, 1024, 2),
-                         sdesc(gb + kk * 2048, kTile, 1024, 2), idMM, 1u);
-            }
-            mma_commit(&Y->mma);
-        }
-        __syncwarp();
-    }
-    if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
-    // dQ^T, dK^T (lanes j): transposed through shared memory into dq, dk rows
     __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(sm + L.mat + kC * kLdc * 4);
     __nv_bfloat16* stk = stq + kC * D;
-    if (ok && row < D) {
-        tc_fence_after();
-        const int j = row;
+    // Two groups from here on, which meet again before the row sums: warps 2-3
+    // walk the gate recurrences (they need dC, the end-state adjoints and the
+    // gates only), the other six warps take the G products, the dQ / dK
+    // epilogue and the stores.  The walks' tables live in tiles that no one
+    // reads any more: Kc, Ec (rows read by other threads, padded) and Wm in
+    // the operand tiles ei .. at, Mm in the dZ / V tiles; Wm and Mm are read
+    // back only by the lane that wrote them.
+    // (512 bytes in: at d = 64 the dq / dk staging above runs 256 bytes past the
+    // matrix tiles)
+    constexpr uint32_t kWalkOff = 512;
+    static_assert(L.mat + kC * kLdc * 4 + 2 * kC * D * 2 <= L.ei + kWalkOff, "staging clear of the tables");
+    float* Kc = reinterpret_cast<float*>(sm + L.ei + kWalkOff);
+    float* Ec = Kc + kC * kLdc;
+    float* Wm = Ec + kC * kLdc;                      // [t][kC]
+    float* Mm = reinterpret_cast<float*>(sm + L.dz); // [t][kC]
+    static_assert(kWalkOff + 2 * kC * kLdc * 4 + kC * kC * 4 <= 7 * kTile, "walk tables in ei .. at");
+    static_assert(kC * kC * 4 <= 2 * (D / 64) * kTile, "Mm in the dZ / V tiles");
+    constexpr uint32_t kBarRest = 1;                 // named barrier of the six warps
+    if (warp != 2 && warp != 3) {
+        // dQ^T += K^T (-2 G)^T;  dK^T += Q^T (-2 G)
+        if (warp == 0 && ok) {
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t kb = smem_u32(ktile(0)), qb = smem_u32(qtile(0)), gb = smem_u32(gg);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int t0 = 32 * chalf + 16 * q;
-            float rq[16], rk[16];
-            tmem_ld16(tl + kDQ + t0, rq);
-            tmem_ld16(tl + kDK + t0, rk);
-            tmem_wait_ld();
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16(tmem + kDQ, sdesc(kb + kk * 2048, 2 * kTile, 1024, 2),
+                             sdesc(gb + kk * 32, 16, 1024, 2), idMK, 1u);
+                    mma_bf16(tmem + kDK, sdesc(qb + kk * 2048, 2 * kTile, 1024, 2),
+                             sdesc(gb + kk * 2048, kTile, 1024, 2), idMM, 1u);
+                }
+                mma_commit(&Y->mma);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = wait_bar(Y, &Y->mma, mma_phase++ & 1, status);
+        // dQ^T, dK^T (lanes j): transposed through shared memory into dq, dk rows;
+        // warps 6-7 take both column halves of lanes 64-127
+        if (ok && row < D) {
+            tc_fence_after();
+            const int j = row;
+            const int nq = warp >= 6 ? 4 : 2, tb = warp >= 6 ? 0 : 32 * chalf;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                stq[(t0 + e) * D + j] = __float2bfloat16_rn(rq[e]);
-                stk[(t0 + e) * D + j] = __float2bfloat16_rn(rk[e]);
+            for (int q = 0; q < 4; ++q) {
+                if (q < nq) {
+                    const int t0 = tb + 16 * q;
+                    float rq[16], rk[16];
+                    tmem_ld16(tl + kDQ + t0, rq);
+                    tmem_ld16(tl + kDK + t0, rk);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        stq[(t0 + e) * D + j] = __float2bfloat16_rn(rq[e]);
+                        stk[(t0 + e) * D + j] = __float2bfloat16_rn(rk[e]);
+                    }
+                }
             }
         }
-    }
-    __syncthreads();
-    if (ok) {
-        constexpr int kRowV = D / 8;                      // 16-byte pieces per row
-        for (int x = tid; x < n * kRowV; x += kThreads) {
-            const int t = x / kRowV, p = x % kRowV;
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + (tok0 + t) * D)[p] =
-                reinterpret_cast<const uint4*>(stq + t * D)[p];
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk_) + (tok0 + t) * D)[p] =
-                reinterpret_cast<const uint4*>(stk + t * D)[p];
+        named_bar_sync(kBarRest, 192);
+        if (ok) {
+            const int gt = tid < 64 ? tid : tid - 64;   // 0 .. 191 over the six warps
+            constexpr int kRowV = D / 8;                 // 16-byte pieces per row
+            for (int x = gt; x < n * kRowV; x += 192) {
+                const int t = x / kRowV, p = x % kRowV;
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + (tok0 + t) * D)[p] =
+                    reinterpret_cast<const uint4*>(stq + t * D)[p];
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk_) + (tok0 + t) * D)[p] =
+                    reinterpret_cast<const uint4*>(stk + t * D)[p];
+            }
         }
-    }
-    __syncthreads();
-
-    // gate gradients.  C[t][s] = theta_s w(s,t) and pm[s] = theta_s m(s,n-1)
-    // with m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t),
-    // w(s,s) = m(s,s) = 1.  Warps 0-1 walk the rows with one column s per lane
-    // (gates broadcast from registers): forward for w, m and d theta_s, then
-    // backward for the adjoints of w and m, whose products with w(s,t-1) and
-    // m(s,t-1), summed over s < t, give d(1 - alpha_t) and d eta_t.
-    float* Wm = dC + kC * kLdc;                      // after dC (the staging is consumed)
-    float* Mm = Wm + kC * kLdc;
-    float* Kc = Mm + kC * kLdc;
-    float* Ec = Kc + kC * kLdc;
-    if (ok && warp < 2) {
-        const int s = warp * 32 + lane;
+    } else if (ok) {
+        // gate gradients.  C[t][s] = theta_s w(s,t) and pm[s] = theta_s m(s,n-1)
+        // with m(s,t) = eta_t m(s,t-1), w(s,t) = (1 - alpha_t) w(s,t-1) + m(s,t),
+        // w(s,s) = m(s,s) = 1.  One column s per lane, walking the rows: forward
+        // for w, m and d theta_s, then backward for the adjoints of w and m, whose
+        // products with w(s,t-1) and m(s,t-1), summed over s < t, give
+        // d(1 - alpha_t) and d eta_t.
+        const int s = (warp - 2) * 32 + lane;
         const float ths = th[s];
         // blocks of 8 rows: the block's loads, then its 8 dependent steps in
         // registers, then its stores (so no load waits behind a store)
@@ -689,8 +707,8 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    Wm[(t0 + u) * kLdc + s] = wb[u];
-                    Mm[(t0 + u) * kLdc + s] = mb[u];
+                    Wm[(t0 + u) * kC + s] = wb[u];
+                    Mm[(t0 + u) * kC + s] = mb[u];
                 }
             }
         }
@@ -705,8 +723,8 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 for (int u = 0; u < 8; ++u) {
                     const int t = tb - u;
                     if (t >= 1) {
-                        wm[u] = Wm[(t - 1) * kLdc + s];
-                        mm[u] = Mm[(t - 1) * kLdc + s];
+                        wm[u] = Wm[(t - 1) * kC + s];
+                        mm[u] = Mm[(t - 1) * kC + s];
                         dc[u] = dC[(t - 1) * kLdc + s];
                         eb[u] = et[t];
                         kb[u] = 1.f - al[t];
@@ -735,7 +753,7 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 }
             }
         }
-    }
+        }
     __syncthreads();
     if (ok) {
         // sums over s < t, four threads per row
