@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/ttm.h"
 #include "kernels.h"
@@ -677,83 +678,92 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         // for w, m and d theta_s, then backward for the adjoints of w and m, whose
         // products with w(s,t-1) and m(s,t-1), summed over s < t, give
         // d(1 - alpha_t) and d eta_t.
-        const int s = (warp - 2) * 32 + lane;
-        const float ths = th[s];
-        // blocks of 8 rows: the block's loads, then its 8 dependent steps in
-        // registers, then its stores (so no load waits behind a store)
-        float m = 0.f, w = 0.f, g = 0.f;
-#pragma unroll
-        for (int t0 = 0; t0 < kC; t0 += 8) {
-            if (t0 < n) {
-                float dcb[8], wb[8], mb[8], eb[8], kb[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    dcb[u] = dC[(t0 + u) * kLdc + s];   // 0 past the chunk
-                    eb[u] = et[t0 + u];
-                    kb[u] = 1.f - al[t0 + u];
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = t0 + u;
-                    const float e = eb[u], k1 = kb[u];
-                    const float mn = t == s ? 1.f : e * m;     // stays 0 before the column starts
-                    const float wn = t == s ? 1.f : fmaf(k1, w, mn);
-                    const bool live = t < n;
-                    m = live ? mn : m;
-                    w = live ? wn : w;
-                    wb[u] = w;
-                    mb[u] = m;
-                    g = fmaf(dcb[u], w, g);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    Wm[(t0 + u) * kC + s] = wb[u];
-                    Mm[(t0 + u) * kC + s] = mb[u];
-                }
-            }
-        }
-        dth[s] = g - 2.f * dpm[s] * m;
-        float dw = s < n ? ths * dC[(n - 1) * kLdc + s] : 0.f;
-        float dm = s < n ? ths * (-2.f * dpm[s]) : 0.f;
-#pragma unroll
-        for (int tb = kC - 1; tb >= 1; tb -= 8) {      // rows tb, tb-1, .., tb-7 (row 0 skipped)
-            if (tb - 7 < n) {
-                float wm[8], mm[8], dc[8], kc[8], ec[8], eb[8], kb[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = tb - u;
-                    if (t >= 1) {
-                        wm[u] = Wm[(t - 1) * kC + s];
-                        mm[u] = Mm[(t - 1) * kC + s];
-                        dc[u] = dC[(t - 1) * kLdc + s];
-                        eb[u] = et[t];
-                        kb[u] = 1.f - al[t];
+        // (a full chunk takes a copy with its length known at compile time)
+        auto walk = [&](auto full) {
+            const int nn = decltype(full)::value ? kC : n;
+            const int s = (warp - 2) * 32 + lane;
+            const float ths = th[s];
+            // blocks of 8 rows: the block's loads, then its 8 dependent steps in
+            // registers, then its stores (so no load waits behind a store)
+            float m = 0.f, w = 0.f, g = 0.f;
+    #pragma unroll
+            for (int t0 = 0; t0 < kC; t0 += 8) {
+                if (t0 < nn) {
+                    float dcb[8], wb[8], mb[8], eb[8], kb[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        dcb[u] = dC[(t0 + u) * kLdc + s];   // 0 past the chunk
+                        eb[u] = et[t0 + u];
+                        kb[u] = 1.f - al[t0 + u];
                     }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = tb - u;
-                    if (t >= 1) {
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int t = t0 + u;
                         const float e = eb[u], k1 = kb[u];
-                        const bool act = t < n && t > s;
-                        const float dm1 = dm + dw;
-                        kc[u] = act ? dw * wm[u] : 0.f;
-                        ec[u] = act ? dm1 * mm[u] : 0.f;
-                        dm = act ? e * dm1 : dm;
-                        dw = act ? fmaf(k1, dw, ths * dc[u]) : dw;
+                        const float mn = t == s ? 1.f : e * m;     // stays 0 before the column starts
+                        const float wn = t == s ? 1.f : fmaf(k1, w, mn);
+                        const bool live = t < nn;
+                        m = live ? mn : m;
+                        w = live ? wn : w;
+                        wb[u] = w;
+                        mb[u] = m;
+                        g = fmaf(dcb[u], w, g);
                     }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int t = tb - u;
-                    if (t >= 1) {
-                        Kc[t * kLdc + s] = kc[u];
-                        Ec[t * kLdc + s] = ec[u];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        Wm[(t0 + u) * kC + s] = wb[u];
+                        Mm[(t0 + u) * kC + s] = mb[u];
                     }
                 }
             }
-        }
-        }
+            dth[s] = g - 2.f * dpm[s] * m;
+            float dw = s < nn ? ths * dC[(nn - 1) * kLdc + s] : 0.f;
+            float dm = s < nn ? ths * (-2.f * dpm[s]) : 0.f;
+    #pragma unroll
+            for (int tb = kC - 1; tb >= 1; tb -= 8) {      // rows tb, tb-1, .., tb-7 (row 0 skipped)
+                if (tb - 7 < nn) {
+                    float wm[8], mm[8], dc[8], kc[8], ec[8], eb[8], kb[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int t = tb - u;
+                        if (t >= 1) {
+                            wm[u] = Wm[(t - 1) * kC + s];
+                            mm[u] = Mm[(t - 1) * kC + s];
+                            dc[u] = dC[(t - 1) * kLdc + s];
+                            eb[u] = et[t];
+                            kb[u] = 1.f - al[t];
+                        }
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int t = tb - u;
+                        if (t >= 1) {
+                            const float e = eb[u], k1 = kb[u];
+                            const bool act = t < nn && t > s;
+                            const float dm1 = dm + dw;
+                            kc[u] = act ? dw * wm[u] : 0.f;
+                            ec[u] = act ? dm1 * mm[u] : 0.f;
+                            dm = act ? e * dm1 : dm;
+                            dw = act ? fmaf(k1, dw, ths * dc[u]) : dw;
+                        }
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int t = tb - u;
+                        if (t >= 1) {
+                            Kc[t * kLdc + s] = kc[u];
+                            Ec[t * kLdc + s] = ec[u];
+                        }
+                    }
+                }
+            }
+        
+        };
+        if (n == kC)
+            walk(std::true_type{});
+        else
+            walk(std::false_type{});
+    }
     __syncthreads();
     if (ok) {
         // sums over s < t, four threads per row
