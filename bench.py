@@ -119,7 +119,8 @@ def kernel_source_digest(kernel_name: str) -> str:
     src = {"linear_simt": ["scan_simt.cu"], "mlp_simt": ["scan_simt.cu", "scan_mlp_simt.cu", "scan_mlp_cluster.cu"],
            "linear_tc": ["scan_linear_tc.cu"], "mlp_tc": ["scan_mlp_tc.cu"],
            "linear_seq": ["scan_linear_seq.cu"],
-           "linear_step": ["step.cu"], "dgd_tc": ["scan_dgd_tc.cu"]}.get(kernel_name)
+           "linear_step": ["step.cu"], "dgd_tc": ["scan_dgd_tc.cu"],
+           "bwd_tc": ["scan_linear_tc.cu", "scan_bwd_tc.cu"]}.get(kernel_name)
     if not src:
         return ""
     h = hashlib.sha256()
@@ -412,7 +413,9 @@ def run_bwd(args, rank, world, dev):
                    "l2": "inputs larger than L2 (no flush needed)", "kernel": kern,
                    "workspace_bytes": int(ws_bytes)},
         "roofline": dict(roof(alg["flops"], alg["bytes"], ms / 1e3, kern == "bwd_simt"),
-                         kernel=label, traffic=None),
+                         kernel=label,
+                         traffic=(profiled_traffic(kern, f"bwd_workload{w.id}")
+                                  if kern == "bwd_tc" and not args.T else None)),
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
