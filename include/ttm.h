@@ -93,7 +93,7 @@ typedef enum {
     TTM_KID_DGD_STEP = 6,      /* fp32 CUDA-core token loop, DGD memory */
     TTM_KID_DGD_TC = 7,        /* tcgen05 + TMA chunk form, DGD memory (pre-pass + scan) */
     TTM_KID_BWD_SIMT = 8,      /* gradient: every pass on the fp32 CUDA cores */
-    TTM_KID_BWD_TC = 9         /* gradient: the local pass on tcgen05 (records and chain fp32) */
+    TTM_KID_BWD_TC = 9         /* gradient: chain and local pass on tcgen05 */
 } ttm_kernel_id;
 
 /*
@@ -310,16 +310,23 @@ int ttm_linear_step(int B, int H, int n, int dk, int dv, int chunk, int pos, int
  *     ([1][H][dv][dk] summed over the batch when W0 is shared; dS0 NULL to skip).
  *   workspace: device scratch of ttm_titans_bwd_workspace_size() bytes (may be
  *     NULL when T = 0): the state and its adjoint at every chunk boundary plus
- *     per-chunk coefficient records.  Contents on return are unspecified.
+ *     per-chunk coefficient records (and score tiles on the tensor-core path).
+ *     Contents on return are unspecified.
  *   All pointers are device memory owned by the caller, 16-byte aligned; no
  *   output may overlap an input, another output or the workspace.
  * Shapes: as for ttm_titans_fwd, with chunk <= 64 and dk <= 128
- * (TTM_ERR_UNSUPPORTED otherwise).  Computation is fp32 (CUDA cores) on the
- * chunk form: the forward scan writes the state at every chunk start, a
- * reverse pass over the chunks carries the adjoint of the state, and a
- * chunk-parallel pass forms the token gradients.  Asynchronous on `stream`;
- * TTM_ERR_INVALID_ARG for malformed arguments or a short workspace,
- * TTM_ERR_CUDA if a launch fails. */
+ * (TTM_ERR_UNSUPPORTED otherwise).  Computation follows the chunk form: the
+ * forward scan writes the state at every chunk start, a reverse pass over the
+ * chunks carries the adjoint of the state, and a chunk-parallel pass forms the
+ * token gradients.  For bf16 with dk = dv in {64, 128} and chunk 64 (unless the
+ * policy is TTM_KERNEL_SIMT) those passes run on the tensor cores: bf16
+ * operands with fp32 accumulation, the state and its adjoint kept in bf16 at the
+ * chunk boundaries, the adjoint carried in fp32 between them
+ * (ttm_last_kernel() reports TTM_KID_BWD_TC); otherwise in fp32 on the CUDA
+ * cores (TTM_KID_BWD_SIMT).  Asynchronous on `stream`; TTM_ERR_INVALID_ARG for
+ * malformed arguments or a short workspace, TTM_ERR_CUDA if a launch fails; a
+ * bounded wait of the tensor-core passes that gives up sets the device status
+ * word to TTM_ERR_TIMEOUT (ttm_device_status). */
 size_t ttm_titans_bwd_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype,
                                      int w0_shared_over_batch);
 int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype,
