@@ -481,8 +481,11 @@ unsigned long long ttm_launch_count(void);
  *     than it copies, so that chunk's barrier never completes: every wait on it
  *     runs out, the kernel sets the device status word to TTM_ERR_TIMEOUT,
  *     drains its copies and MMAs, frees its tensor memory and returns (its
- *     outputs are then invalid).  The setting is used up by that one call; -1
- *     clears it.  Nothing faults, traps or hangs.
+ *     outputs are then invalid).  A ttm_titans_bwd / ttm_linear_bwd call on
+ *     the tensor-core path takes the setting for its chain pass instead, with
+ *     c counted in the chain's order (c = 0 is the last chunk).  The setting
+ *     is used up by that one call; -1 clears it.  Nothing faults, traps or
+ *     hangs.
  *   TTM_DBG_FAIL_CALLS, n >= 0: the next n calls of ttm_linear_fwd,
  *     ttm_titans_fwd (and the variants built on them) and ttm_mlp_fwd return
  *     TTM_ERR_CUDA after validating their arguments, without enqueueing

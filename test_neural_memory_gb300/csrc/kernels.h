@@ -131,6 +131,10 @@ struct BwdArgs {
     size_t workspace_bytes;
     int fwd_tc;     // 1: the tensor-core scan writes the checkpoints (bf16, d 64 / 128, chunk 64)
     int local_tc;   // 1: the local pass runs on the tensor cores (bf16, d 64 / 128, chunk 64)
+    // Failure-detection test hook of the tensor-core chain (0: off): with k + 1
+    // the chain's loader announces 16 bytes more than it copies for its k-th
+    // chunk (in reverse order), so that stage's waits run out.
+    int debug_stall;
     int* status;    // device status word of the tensor-core kernels' bounded waits
     long long wait_cycles;   // their wait limit in SM clock cycles (0: the default)
 };

@@ -899,12 +899,13 @@ bwd_local_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
 //              a chunk run while the state warps work on the previous one.
 //   warp 9     TMA loads into three input stages: a stage is refilled three
 //              chunks ahead once the state warps release it after its update.
-// Hand-offs between roles are named barriers (state -> issuer: the adjoint
-// copy; de warps -> issuer: the de tile; tile warps -> issuer: the dZ tiles)
-// and MMA-completion mbarriers the other way; stage release and refill are
-// mbarriers.  Every wait on an mbarrier is
-// bounded; after a timeout every role runs out its loop doing no work, so the
-// named barriers stay balanced.
+// Hand-offs between roles are named barriers that both sides sync on (state ->
+// issuer: the adjoint copy; de warps -> issuer: the de tile; tile warps ->
+// issuer: the dZ tiles) and MMA-completion mbarriers the other way; stage
+// release and refill are mbarriers.  Every wait on an mbarrier is bounded;
+// after a timeout every role runs out its loop doing no work, and since every
+// role passes the same named barriers in the same order, they stay in
+// lockstep.
 
 constexpr int kSl = 16;                                          // rows of the slice
 constexpr int kNS = 3;                                           // input stages
@@ -1014,7 +1015,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         };
         write_ws();
         fence_proxy_async_smem();
-        named_bar_arrive(kBarWs, 160);
+        named_bar_sync(kBarWs, 160);
         for (int k = 0; k < nch; ++k) {
             const int c = nch - 1 - k, st = k % kNS, b = k & 1;
             const int n = chunk_len(k);
@@ -1053,7 +1054,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_arrive(kBarDe, 96);
+                named_bar_sync(kBarDe, 96);
             }
             // dW <- beta_n dW + .,  dS <- c_n dW + P_n dS + .  (column j)
             if (ok) ok = wait_flag(&Y->abort, Y->limit, &Y->mma3, k & 1, status);
@@ -1077,7 +1078,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
             if (k + 1 < nch) {
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_arrive(kBarWs, 160);
+                named_bar_sync(kBarWs, 160);
             }
             // this warp is done with the chunk's stage
             __syncwarp();
@@ -1132,7 +1133,7 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
                 *reinterpret_cast<uint4*>(bct(b) + swz(t, 2 + c8)) = pack8(zc);
             }
             fence_proxy_async_smem();
-            named_bar_arrive(kBarTiles, 160);
+            named_bar_sync(kBarTiles, 160);
         }
     } else if (warp == 8) {
         // ----------------------------------------------------------- issuer
@@ -1222,7 +1223,10 @@ bwd_chain_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_const
         // ----------------------------------------------------------- loader
         auto issue_loads = [&](int k) {
             const int c = nch - 1 - k, st = k % kNS;
-            mbar_expect_tx(&Y->full[st], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes);
+            // (a.debug_stall = k + 1: the test hook announces 16 bytes more than
+            // it copies, so this stage's barrier never completes)
+            mbar_expect_tx(&Y->full[st], 2 * NH * kTile + kTile + kC * kSl * 2 + kCoefVecBytes +
+                                             (k + 1 == a.debug_stall ? 16u : 0u));
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
                 tma_load_3d(kt(st, h), &kmap, &Y->full[st], 64 * h, c * kC, seq);

@@ -462,6 +462,7 @@ int ttm_titans_bwd(int B, int H, int T, int dk, int dv, int chunk, int dtype, co
     a.wait_cycles = g_wait_cycles.load();
     // the tensor-core passes read what the tensor-core scan leaves in the workspace
     a.local_tc = g_policy != TTM_KERNEL_SIMT && a.fwd_tc && ttm::bwd_local_tc_supported(a) ? 1 : 0;
+    if (a.local_tc) a.debug_stall = g_stall_chunk.exchange(-1) + 1;   // the chain takes the hook
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     const cudaError_t e = ttm::linear_bwd_launch(a, s, &launches);

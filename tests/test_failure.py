@@ -6,7 +6,8 @@
 - Device side: a bounded wait of the tensor-core scan is made to run out (a
   chunk whose barrier is announced 16 bytes more than is copied, so the wait
   can never complete) under a short wait limit; the call returns, the device
-  status word reports TTM_ERR_TIMEOUT once, and the next call is correct.
+  status word reports TTM_ERR_TIMEOUT once, and the next call is correct.  The
+  same for the chain pass of the tensor-core gradient.
 - Non-finite data: a step size far above the pages' stability bound
   ("TTT layers 与 fast weights" §1.2, eq (12): 0 < theta |k|^2 < 1 in this
   scale) makes the memory grow by ~300x per chunk; the scan must neither hang
@@ -94,6 +95,37 @@ def test_bounded_wait_runs_out_and_the_next_call_is_correct():
     assert ttm.device_status() == ttm.OK
     ref = H.run_linear_oracle(w, inp)
     H.compare({"z": z, "W": W, "S": S}, ref, ["z", "W", "S"], H.TOL["bf16"])
+
+
+@gpu
+def test_gradient_chain_bounded_wait_runs_out_and_the_next_call_is_correct():
+    # the tensor-core chain's loader announces 16 bytes more than it copies for
+    # its third chunk: that stage's waits run out, every role of the chain
+    # unwinds in lockstep, the status word reports TTM_ERR_TIMEOUT once, and the
+    # next gradient matches the oracle
+    from tests.test_bwd import check, run_bwd
+    T = 6 * 64 + 9
+    w, inp = wl.generate_custom(kind="titans", dtype="bf16", B=1, H=2, T=T, d=64, chunk=64,
+                                seed=31)
+    adj = wl.generate_adjoints(1, 2, T, 64, 64, dtype="bf16", seed=32, with_S=True)
+    d, a = H.to_dev(inp), H.to_dev(adj)
+    assert ttm.device_status() == ttm.OK
+    ttm.debug_set("wait_cycles", 20_000_000)     # ~10 ms at 2 GHz
+    ttm.debug_set("stall_chunk", 2)
+    t0 = time.perf_counter()
+    ttm.titans_bwd(d["q"], d["k"], d["v"], d["theta"], d["W0"], 64, a["dz"], eta=d.get("eta"),
+                   alpha=d.get("alpha"), dW=a["dW"], dS=a["dS"])
+    assert ttm.last_kernel() == "bwd_tc"
+    status = ttm.device_status()                 # synchronises
+    elapsed = time.perf_counter() - t0
+    assert status == ttm.ERR_TIMEOUT, ttm.status_str(status)
+    assert elapsed < 30.0
+    assert ttm.device_status() == ttm.OK         # the query cleared it
+    ttm.debug_set("wait_cycles", 0)
+    g, r, names = run_bwd("titans", "bf16", B=1, Hh=2, T=T, d=64, chunk=64, seed=31, S0=True)
+    assert ttm.last_kernel() == "bwd_tc"
+    check(g, r, names, H.TOL["bf16"])
+    assert ttm.device_status() == ttm.OK
 
 
 FP32_MAX = float(np.finfo(np.float32).max)
