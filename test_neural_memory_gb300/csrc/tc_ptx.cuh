@@ -92,12 +92,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Arrive on named barrier id without waiting (the consumer's bar.sync counts
-// these arrivals toward nthreads).
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // -------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
