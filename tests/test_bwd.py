@@ -165,7 +165,8 @@ def test_bf16_d128_both_checkpoint_scans(policy):
 # gate gradients) run on the tensor cores.
 
 @pytest.mark.parametrize("kind,d,T,seed", [("titans", 64, 130, 20), ("titans", 128, 64, 21),
-                                            ("linear", 128, 200, 22), ("titans", 128, 1, 23)])
+                                            ("linear", 128, 200, 22), ("titans", 128, 1, 23),
+                                            ("titans", 128, 100, 27)])
 def test_tensor_core_local_pass(kind, d, T, seed):
     import test_neural_memory_gb300 as ttm
     with ttm.kernel_policy("auto"):
